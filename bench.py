@@ -1,0 +1,476 @@
+"""Benchmark of the Gated DeltaNet state path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. chunked prefill of a 27B-shaped GDN layer (16 qk / 48 v heads, d = 128,
+     bf16 x and o, fp32 state), 4 sequences x 8192 tokens, block 896 with a
+     checkpoint written into the paged pool at every crossed boundary
+     (block table = seeded permutation of the pages);
+  2. batched decode of a 4B-shaped layer (16 qk / 32 v heads), 256 sequences
+     at seeded random pages, 24 layers back to back (separate pools);
+  3. replay verify on the same 4B-shaped layer: 16 requests x 16 rows
+     appended to a 32-slot bf16 log, rollback to an accepted length uniform on
+     [0, 16], then the flush of the kept rows into the checkpoint, 24 layers.
+
+`value` is prefill tokens/s per layer (device-timed, inputs resident in HBM);
+decode and flush are reported as microseconds per layer.  Every input is
+larger than L2 (x alone is 671 MB; decode touches 15 GiB of pages; the replay
+pools of 24 layers are 960 MiB), so no L2 flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       (N > 1: launch with torch.distributed.run; each rank runs a replica).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gated_deltanet_state_gb300 as gdn  # noqa: E402
+from gated_deltanet_state_gb300 import inputs  # noqa: E402
+
+METRIC = "GDN prefill tokens/s/layer; decode & replay-flush µs/layer; % of TC/HBM roofline"
+PREFILL = inputs.QWEN27B
+SMALL = inputs.QWEN4B
+N_SEQ, SEQ_LEN = 4, 8192
+DEC_SEQS, DEC_LAYERS = 256, 24
+REP_REQS, REP_ROWS, REP_LAYERS = 16, 16, 24
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class PrefillWork:
+    """4 x 8192 tokens of the 27B-shaped layer, checkpoints every 896 tokens."""
+
+    def __init__(self, seed: int):
+        sh = PREFILL
+        self.sh = sh
+        T = N_SEQ * SEQ_LEN
+        # a2: the scheduler's chunk for this call; the whole prompt fits the budget
+        self.chunk_end = gdn.gdn_chunk_end(0, SEQ_LEN, SEQ_LEN, sh.block_size)
+        assert self.chunk_end == SEQ_LEN
+        ti = inputs.token_inputs(sh, T, seed)
+        self.host = {k: v.pin_memory() for k, v in ti.items()}
+        self.x = ti["x"].cuda()
+        self.g = ti["g"].cuda()
+        self.beta = ti["beta"].cuda()
+        self.w = inputs.conv_weights(sh, seed).cuda()
+        nck = SEQ_LEN // sh.block_size            # 9 boundaries per sequence
+        self.num_pages = N_SEQ * (nck + 1)
+        perm = inputs.permutation(self.num_pages, seed).tolist()
+        self.block_table = torch.tensor([perm[s * nck:(s + 1) * nck] for s in range(N_SEQ)],
+                                        dtype=torch.int32).cuda()
+        self.out_slot = torch.tensor(perm[N_SEQ * nck:], dtype=torch.int32).cuda()
+        self.pool = gdn.StatePool(sh, self.num_pages, fill=0)
+        self.cu = torch.arange(0, T + 1, SEQ_LEN, dtype=torch.int32).cuda()
+        self.start = torch.zeros(N_SEQ, dtype=torch.int64).cuda()
+        self.init = torch.full((N_SEQ,), -1, dtype=torch.int32).cuda()
+        self.o = torch.empty(T, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
+        self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.tokens = T
+
+    def run(self, x=None, g=None, beta=None, o=None):
+        gdn.gdn_prefill_chunked(self.sh, self.pool, cu_seqlens=self.cu, start_pos=self.start,
+                                init_page=self.init, block_table=self.block_table, out_slot=self.out_slot,
+                                x=self.x if x is None else x, g=self.g if g is None else g,
+                                beta=self.beta if beta is None else beta, conv_w=self.w,
+                                o=self.o if o is None else o, dev_error=self.err,
+                                start_pos_host=[0] * N_SEQ, init_page_host=[-1] * N_SEQ)
+
+    def run_e2e(self):
+        """Host buffers in, host buffers out, through the same C-ABI call."""
+        x = self.host["x"].to("cuda", non_blocking=True)
+        g = self.host["g"].to("cuda", non_blocking=True)
+        beta = self.host["beta"].to("cuda", non_blocking=True)
+        self.run(x, g, beta)
+        self.o_host.copy_(self.o, non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(v.numel() * v.element_size() for v in self.host.values())
+
+    @property
+    def d2h_bytes(self):
+        return self.o_host.numel() * self.o_host.element_size()
+
+    # roofline inputs for the scan kernel
+    def algorithmic_flops(self):
+        sh = self.sh
+        return 6.0 * sh.head_dim_k * sh.head_dim_v * sh.num_v_heads * self.tokens
+
+    def algorithmic_bytes(self):
+        sh = self.sh
+        per_tok = sh.conv_dim * 2 + 2 * sh.num_v_heads * 4 + sh.num_v_heads * sh.head_dim_v * 2
+        ck = (SEQ_LEN // sh.block_size + 1) * N_SEQ * sh.payload_bytes
+        return per_tok * self.tokens + ck
+
+
+class DecodeWork:
+    """256 sequences x 24 layers of the 4B-shaped layer, one token each."""
+
+    def __init__(self, seed: int):
+        sh = SMALL
+        self.sh = sh
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        self.pools, self.slots, self.x, self.g, self.beta = [], [], [], [], []
+        for layer in range(DEC_LAYERS):
+            pool = gdn.StatePool(sh, DEC_SEQS, fill=0)
+            for p in range(0, DEC_SEQS, 64):
+                n = min(64, DEC_SEQS - p)
+                blk = pool.buf[p * sh.page:(p + n) * sh.page].view(n, sh.page)
+                st = blk[:, :sh.state_bytes].view(torch.float32)
+                st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
+            self.pools.append(pool)
+            self.slots.append(inputs.permutation(DEC_SEQS, seed + layer).cuda())
+            ti = inputs.token_inputs(sh, DEC_SEQS, seed + 1000 + layer)
+            self.x.append(ti["x"].cuda())
+            self.g.append(ti["g"].cuda())
+            self.beta.append(ti["beta"].cuda())
+        self.w = inputs.conv_weights(sh, seed).cuda()
+        self.o = torch.empty(DEC_SEQS, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run(self):
+        for L in range(DEC_LAYERS):
+            gdn.gdn_decode_step(self.sh, self.pools[L], x=self.x[L], g=self.g[L], beta=self.beta[L],
+                                conv_w=self.w, slot=self.slots[L], o=self.o, dev_error=self.err)
+
+    def bytes_per_layer(self):
+        sh = self.sh
+        per_seq = 2 * sh.state_bytes + 2 * sh.window_bytes + sh.conv_dim * 2 + 2 * sh.num_v_heads * 4 \
+            + sh.num_v_heads * sh.head_dim_v * 2
+        return per_seq * DEC_SEQS
+
+
+class ReplayWork:
+    """16 requests x 16 rows per layer, 24 layers: append, rollback, flush."""
+
+    def __init__(self, seed: int):
+        sh = SMALL
+        self.sh = sh
+        L = gdn.REPLAY_LOG_SLOTS
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        self.layers = []
+        for layer in range(REP_LAYERS):
+            pool = gdn.StatePool(sh, REP_REQS, fill=0)
+            st = pool.buf.view(REP_REQS, sh.page)[:, :sh.state_bytes].view(torch.float32)
+            st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
+            ti = inputs.token_inputs(sh, REP_REQS * REP_ROWS, seed + 2000 + layer)
+            self.layers.append({
+                "pool": pool,
+                "ckpt": inputs.permutation(REP_REQS, seed + layer).cuda(),
+                "log_x": torch.zeros(REP_REQS, L, sh.conv_dim, dtype=torch.bfloat16, device="cuda"),
+                "log_g": torch.zeros(REP_REQS, L, sh.num_v_heads, device="cuda"),
+                "log_b": torch.zeros(REP_REQS, L, sh.num_v_heads, device="cuda"),
+                "log_len": torch.zeros(REP_REQS, dtype=torch.int32, device="cuda"),
+                "x": ti["x"].cuda().view(REP_REQS, REP_ROWS, -1),
+                "g": ti["g"].cuda().view(REP_REQS, REP_ROWS, -1),
+                "beta": ti["beta"].cuda().view(REP_REQS, REP_ROWS, -1),
+                "acc": inputs.accept_lengths(REP_REQS, REP_ROWS, seed + layer).cuda(),
+            })
+        self.w = inputs.conv_weights(sh, seed).cuda()
+        self.o = torch.empty(REP_REQS, REP_ROWS, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16,
+                             device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.kept_rows = float(sum(int(l["acc"].sum()) for l in self.layers)) / REP_LAYERS
+
+    def _kw(self, l):
+        return dict(ckpt_slot=l["ckpt"], log_x=l["log_x"], log_g=l["log_g"], log_beta=l["log_b"],
+                    log_len=l["log_len"], conv_w=self.w, dev_error=self.err)
+
+    def verify(self):
+        for l in self.layers:
+            gdn.gdn_replay_append(self.sh, l["pool"], x_new=l["x"], g_new=l["g"], beta_new=l["beta"],
+                                  o=self.o, **self._kw(l))
+            gdn.gdn_replay_rollback(l["log_len"], l["acc"], REP_ROWS, self.err)
+
+    def flush(self):
+        for l in self.layers:
+            gdn.gdn_replay_flush(self.sh, l["pool"], **self._kw(l))
+
+    def flush_bytes_per_layer(self):
+        sh = self.sh
+        return REP_REQS * (2 * sh.payload_bytes) + self.kept_rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4)
+
+
+# ----------------------------------------------------------------------------- cpu baseline
+
+def _oracle_setup(seed: int):
+    import oracle
+    sh = PREFILL
+    d = oracle.Dims(sh.num_qk_heads, sh.num_v_heads, sh.head_dim_k, sh.head_dim_v, sh.q_scale, sh.norm_eps)
+    ti = inputs.token_inputs(sh, N_SEQ * SEQ_LEN, seed)
+    w = inputs.conv_weights(sh, seed)
+    oracle.build()
+
+    def run(n):
+        # n tokens of the workload: whole 8192-token sequences plus a prefix
+        cu = list(range(0, n, SEQ_LEN)) + [n]
+        t0 = time.perf_counter()
+        oracle.prefill(d, cu, [0] * (len(cu) - 1), sh.block_size, ti["x"][:n], ti["g"][:n],
+                       ti["beta"][:n], w)
+        return time.perf_counter() - t0
+
+    return run, oracle.num_threads()
+
+
+def _calibrate(run, seconds: float) -> int:
+    """Tokens of one 27B-shaped sequence the oracle prefills in about `seconds`."""
+    n, dt = 32, run(32)
+    while dt < min(2.0, seconds / 2) and n < N_SEQ * SEQ_LEN:
+        n = min(N_SEQ * SEQ_LEN, n * 4)
+        dt = run(n)
+    return max(16, min(N_SEQ * SEQ_LEN, int(n * seconds / max(dt, 1e-6))))
+
+
+def cpu_baseline(seconds: float = 12.0, seed: int = 0):
+    """The fp64 oracle on the host cores, on a bounded sample of the prefill
+    workload (one sequence of the 27B-shaped layer, all 48 heads, a prefix of
+    its tokens), scaled to tokens/s per layer."""
+    run, cores = _oracle_setup(seed)
+    n = _calibrate(run, seconds)
+    dt = run(n)
+    return {"value": n / dt, "unit": "tokens/s/layer", "cores": cores, "kind": "oracle",
+            "sample": f"27B-shaped layer, first {n} of the 4 x 8192 tokens, all 48 heads, fp64, "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: W warm-up and K timed steps, each a
+    bounded sample of the prefill workload on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    run, cores = _oracle_setup(args.seed)
+    per_step = max(2.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = _calibrate(run, per_step)
+    for _ in range(args.warmup):
+        run(n)
+    times = [run(n) for _ in range(args.steps)]
+    value = n / statistics.mean(times)
+    sample = (f"27B-shaped layer, first {n} of the 4 x 8192 tokens per step, all 48 heads, fp64, "
+              f"{statistics.mean(times):.1f} s per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s/layer",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * statistics.mean(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill 27B-shaped GDN layer (16 qk / 48 v heads, d 128), 4 x 8192 "
+                                   "tokens, block 896 (bounded sample per step)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s/layer", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    args.warmup = max(args.warmup, 3)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    gdn.load_library()
+
+    pre = PrefillWork(args.seed + rank)
+    dec = DecodeWork(args.seed + 10 + rank)
+    rep = ReplayWork(args.seed + 20 + rank)
+    stream = torch.cuda.current_stream()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(record=None):
+        e = [ev() for _ in range(6)] if record is not None else None
+        if e: e[0].record(stream)
+        pre.run()
+        if e: e[1].record(stream)
+        dec.run()
+        if e: e[2].record(stream)
+        rep.verify()
+        if e: e[3].record(stream)
+        rep.flush()
+        if e: e[4].record(stream)
+        if record is not None:
+            record.append(e)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    errs = [int(pre.err.item()), int(dec.err.item()), int(rep.err.item())]
+    if any(errs):
+        raise RuntimeError(f"device error words after warm-up: {errs}")
+
+    recs = []
+    with ClockSampler(local) as clk:
+        if dist: dist.barrier()
+        torch.cuda.synchronize()
+        t_start = ev(); t_end = ev()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(recs)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if dist: dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = sum(r[0].elapsed_time(r[1]) for r in recs) / args.steps
+    dec_ms = sum(r[1].elapsed_time(r[2]) for r in recs) / args.steps
+    ver_ms = sum(r[2].elapsed_time(r[3]) for r in recs) / args.steps
+    fl_ms = sum(r[3].elapsed_time(r[4]) for r in recs) / args.steps
+    if dist:
+        t = torch.tensor([total_ms, pre_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, pre_ms = float(t[0]), float(t[1])
+
+    # end to end through the same call with host buffers (prefill part)
+    for _ in range(2):
+        pre.run_e2e()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(args.steps):
+        pre.run_e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    peaks, peak_kind = _peaks()
+    clocks = clk.summary()
+    sm_max = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    alu_peak = 2.0 * 128 * 152 * sm_max * 1e6 / 1e12      # fp32 FMA TFLOP/s
+    achieved = pre.algorithmic_flops() / (pre_ms * 1e-3) / 1e12
+    dec_gbs = dec.bytes_per_layer() / (dec_ms / DEC_LAYERS * 1e-3) / 1e9
+    fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
+    value = world * pre.tokens / (pre_ms * 1e-3)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "prefill 27B-shaped GDN layer (16 qk / 48 v heads, d 128), 4 x 8192 tokens, "
+                               "block 896, checkpoints every block; + decode 4B-shaped 256 seqs x 24 layers; "
+                               "+ replay 16 req x 16 rows x 24 layers",
+                   "io_dtype": "bf16 x/o, fp32 state", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "prefill_ms": pre_ms, "decode_us_per_layer": 1000.0 * dec_ms / DEC_LAYERS,
+        "replay_verify_us_per_layer": 1000.0 * ver_ms / REP_LAYERS,
+        "flush_us_per_layer": 1000.0 * fl_ms / REP_LAYERS,
+        "decode_hbm_gbs": dec_gbs, "flush_hbm_gbs": fl_gbs,
+        "decode_hbm_frac": dec_gbs / peaks["hbm_gbs"], "flush_hbm_frac": fl_gbs / peaks["hbm_gbs"],
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": achieved / alu_peak, "traffic": None,
+                     "kernel": "scan_kernel<128,128,2,bf16,bf16,prefill>",
+                     "peak_kind": f"fp32 FMA 152 SMs x 128 lanes x 2 x {sm_max:.0f} MHz",
+                     "hbm_peak_kind": peak_kind},
+        "e2e": {"value": world * pre.tokens / (e2e_ms * 1e-3), "unit": "tokens/s/layer",
+                "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
+                "scope": "prefill part of the step"},
+        "gpu_launches": args.steps * (2 + DEC_LAYERS + 5 * REP_LAYERS),
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+// api.cu — the exported C ABI (include/gdn.h): host-side validation, then the
+// internal launchers.  Nothing here allocates memory or keeps state.
+#include <cstring>
+
+#include "launch.h"
+
+using namespace gdn;
+
+namespace {
+
+constexpr int32_t kMaxGrid = 65535;  // grid y/z limit used for sequences / pages
+
+bool shape_supported(const gdn_layer_desc* d) {
+  if (d->conv_kernel != kConvK || d->reserved != 0) return false;
+  const int dk = d->head_dim_k, dv = d->head_dim_v;
+  if (dk != dv || (dk != 32 && dk != 64 && dk != 128)) return false;
+  if (d->in_dtype != d->out_dtype) return false;
+  if (d->num_v_heads % d->num_qk_heads != 0 || d->num_v_heads > kMaxGrid) return false;
+  if (d->chunk_size != 16 && d->chunk_size != 32 && d->chunk_size != 64) return false;
+  if (d->block_size <= 0 || d->block_size % d->chunk_size != 0) return false;
+  return true;
+}
+
+gdn_status check_desc_pool(const gdn_layer_desc* d, const gdn_pool* pool) {
+  if (!d || !pool) return GDN_ERR_INVALID_ARG;
+  if (d->num_qk_heads <= 0 || d->num_v_heads <= 0 || d->head_dim_k <= 0 || d->head_dim_v <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (d->in_dtype != GDN_F32 && d->in_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (d->out_dtype != GDN_F32 && d->out_dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (!(d->norm_eps >= 0.0f)) return GDN_ERR_INVALID_ARG;
+  if (!shape_supported(d)) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (!pool->base || pool->num_pages <= 0) return GDN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(pool->base) % 256 != 0 || pool->page_bytes % 256 != 0)
+    return GDN_ERR_INVALID_ARG;
+  if (pool->page_bytes < gdn_mamba_page_bytes(d)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+Pool make_pool(const gdn_layer_desc* d, const gdn_pool* pool) {
+  Pool p;
+  p.base = static_cast<char*>(pool->base);
+  p.page_bytes = pool->page_bytes;
+  p.num_pages = pool->num_pages;
+  p.state_bytes = (int64_t)d->num_v_heads * d->head_dim_v * d->head_dim_k * 4;
+  return p;
+}
+
+ScanParams base_scan(const gdn_layer_desc* d, const gdn_pool* pool) {
+  ScanParams p;
+  memset(&p, 0, sizeof(p));
+  p.pool = make_pool(d, pool);
+  p.Hqk = d->num_qk_heads;
+  p.Hv = d->num_v_heads;
+  p.conv_dim = (int32_t)gdn_conv_dim(d);
+  p.block_size = d->block_size;
+  p.q_scale = d->q_scale;
+  p.eps = d->norm_eps;
+  return p;
+}
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
+                                  int64_t total_tokens) {
+  (void)desc; (void)num_seqs; (void)total_tokens;
+  return 0;  // the scan keeps every intermediate on chip
+}
+
+gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
+                               const gdn_prefill_args* a, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  (void)workspace; (void)workspace_bytes;
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (!a || a->num_seqs < 0 || a->num_seqs > kMaxGrid || a->total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (a->num_seqs == 0) return GDN_OK;
+  if (!a->cu_seqlens || !a->start_pos || !a->conv_w || !a->init_page || !a->out_slot ||
+      !a->dev_error || a->max_blocks < 0 || (a->max_blocks > 0 && !a->block_table))
+    return GDN_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 && (!a->x || !a->g || !a->beta || !a->o)) return GDN_ERR_INVALID_ARG;
+  // Fail closed before launching anything when the host can see an
+  // off-boundary resume or a cold start that does not begin at 0.
+  if (a->start_pos_host) {
+    for (int32_t s = 0; s < a->num_seqs; ++s) {
+      const int64_t sp = a->start_pos_host[s];
+      if (sp < 0) return GDN_ERR_INVALID_ARG;
+      const bool cold = a->init_page_host ? a->init_page_host[s] == -1 : sp == 0;
+      if (cold ? sp != 0 : (sp <= 0 || sp % desc->block_size != 0)) return GDN_ERR_NOT_BLOCK_ALIGNED;
+    }
+  }
+  if (a->init_page_host)
+    for (int32_t s = 0; s < a->num_seqs; ++s)
+      if (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages) return GDN_ERR_PAGE_RANGE;
+  ScanParams p = base_scan(desc, pool);
+  p.num_seqs = a->num_seqs;
+  p.conv_w = a->conv_w;
+  p.o = a->o;
+  p.err = a->dev_error;
+  p.cu_seqlens = a->cu_seqlens;
+  p.start_pos = a->start_pos;
+  p.init_page = a->init_page;
+  p.block_table = a->block_table;
+  p.max_blocks = a->max_blocks;
+  p.out_slot = a->out_slot;
+  p.x = a->x;
+  p.g = a->g;
+  p.beta = a->beta;
+  return cuda_status(launch_prefill(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                    desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
+                           const gdn_decode_args* a, void* stream) {
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (!a || a->num_seqs < 0 || a->num_seqs > kMaxGrid) return GDN_ERR_INVALID_ARG;
+  if (a->num_seqs == 0) return GDN_OK;
+  if (!a->x || !a->g || !a->beta || !a->conv_w || !a->slot || !a->o || !a->dev_error)
+    return GDN_ERR_INVALID_ARG;
+  DecodeParams p;
+  p.pool = make_pool(desc, pool);
+  p.Hqk = desc->num_qk_heads;
+  p.Hv = desc->num_v_heads;
+  p.conv_dim = (int32_t)gdn_conv_dim(desc);
+  p.num_seqs = a->num_seqs;
+  p.q_scale = desc->q_scale;
+  p.eps = desc->norm_eps;
+  p.x = a->x;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.conv_w = a->conv_w;
+  p.slot = a->slot;
+  p.o = a->o;
+  p.err = a->dev_error;
+  return cuda_status(launch_decode(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                   desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+static gdn_status checkpoint_copy(const gdn_layer_desc* desc, const gdn_pool* pool,
+                                  const int32_t* src, const int32_t* dst,
+                                  const int64_t* num_computed_host, int32_t n, int32_t* dev_error,
+                                  void* stream) {
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (n < 0 || n > kMaxGrid) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  if (!src || !dst || !num_computed_host || !dev_error) return GDN_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    if (num_computed_host[i] < 0) return GDN_ERR_INVALID_ARG;
+    if (num_computed_host[i] % desc->block_size != 0) return GDN_ERR_NOT_BLOCK_ALIGNED;
+  }
+  CopyParams p;
+  p.pool = make_pool(desc, pool);
+  p.payload_bytes = gdn_mamba_page_bytes(desc);
+  p.src = src;
+  p.dst = dst;
+  p.n = n;
+  p.err = dev_error;
+  return cuda_status(launch_copy(p, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_checkpoint_resume(const gdn_layer_desc* desc, const gdn_pool* pool,
+                                 const int32_t* src_page, const int32_t* dst_page,
+                                 const int64_t* num_computed_host, int32_t n, int32_t* dev_error,
+                                 void* stream) {
+  return checkpoint_copy(desc, pool, src_page, dst_page, num_computed_host, n, dev_error, stream);
+}
+
+gdn_status gdn_checkpoint_save(const gdn_layer_desc* desc, const gdn_pool* pool,
+                               const int32_t* src_page, const int32_t* dst_page,
+                               const int64_t* num_computed_host, int32_t n, int32_t* dev_error,
+                               void* stream) {
+  return checkpoint_copy(desc, pool, src_page, dst_page, num_computed_host, n, dev_error, stream);
+}
+
+static gdn_status replay_common(const gdn_layer_desc* desc, const gdn_pool* pool,
+                                const gdn_replay_args* a, bool append, ScanParams* out) {
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (!a || a->num_reqs < 0 || a->num_reqs > kMaxGrid) return GDN_ERR_INVALID_ARG;
+  if (!a->ckpt_slot || !a->log_x || !a->log_g || !a->log_beta || !a->log_len || !a->conv_w ||
+      !a->dev_error)
+    return a->num_reqs == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (append) {
+    if (a->num_new < 0) return GDN_ERR_INVALID_ARG;
+    if (a->num_new > GDN_REPLAY_LOG_SLOTS) return GDN_ERR_LOG_OVERFLOW;
+    if (a->num_new > 0 && (!a->x_new || !a->g_new || !a->beta_new || !a->o)) return GDN_ERR_INVALID_ARG;
+  }
+  ScanParams p = base_scan(desc, pool);
+  p.num_seqs = a->num_reqs;
+  p.conv_w = a->conv_w;
+  p.o = a->o;
+  p.err = a->dev_error;
+  p.ckpt_slot = a->ckpt_slot;
+  p.log_x = a->log_x;
+  p.log_g = a->log_g;
+  p.log_beta = a->log_beta;
+  p.log_len = a->log_len;
+  p.num_new = append ? a->num_new : 0;
+  p.x_new = a->x_new;
+  p.g_new = a->g_new;
+  p.beta_new = a->beta_new;
+  *out = p;
+  return GDN_OK;
+}
+
+gdn_status gdn_replay_append(const gdn_layer_desc* desc, const gdn_pool* pool,
+                             const gdn_replay_args* a, void* stream) {
+  ScanParams p;
+  gdn_status st = replay_common(desc, pool, a, true, &p);
+  if (st != GDN_OK || a->num_reqs == 0) return st;
+  return cuda_status(launch_replay_append(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                          desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_replay_flush(const gdn_layer_desc* desc, const gdn_pool* pool,
+                            const gdn_replay_args* a, void* stream) {
+  ScanParams p;
+  gdn_status st = replay_common(desc, pool, a, false, &p);
+  if (st != GDN_OK || a->num_reqs == 0) return st;
+  return cuda_status(launch_replay_flush(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                         desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_replay_rollback(int32_t* log_len, const int32_t* accepted, int32_t num_appended,
+                               int32_t n, int32_t* dev_error, void* stream) {
+  if (n < 0 || num_appended < 0 || num_appended > GDN_REPLAY_LOG_SLOTS) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  if (!log_len || !accepted || !dev_error) return GDN_ERR_INVALID_ARG;
+  return cuda_status(launch_replay_rollback(log_len, accepted, num_appended, n, dev_error,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// common.cuh — device helpers shared by the engine's kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kConvK = 4;        // depthwise conv taps
+constexpr int kWinRows = kConvK - 1;
+
+// ---- element access ------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// SiLU in fp32 with the accurate expf.
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// First error wins; later faults keep the first code.
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---- pool addressing -----------------------------------------------------
+struct Pool {
+  char* base;
+  int64_t page_bytes;
+  int32_t num_pages;
+  int64_t state_bytes;   // Hv*dv*dk*4, window starts here
+};
+
+__device__ __forceinline__ float* page_state(const Pool& p, int32_t page) {
+  return reinterpret_cast<float*>(p.base + (int64_t)page * p.page_bytes);
+}
+template <typename TIN>
+__device__ __forceinline__ TIN* page_window(const Pool& p, int32_t page) {
+  return reinterpret_cast<TIN*>(p.base + (int64_t)page * p.page_bytes + p.state_bytes);
+}
+__device__ __forceinline__ bool page_ok(const Pool& p, int32_t page) {
+  return page >= 0 && page < p.num_pages;
+}
+
+// ---- warp reductions (fixed xor order: deterministic) ----------------------
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace gdn

@@ -1,0 +1,43 @@
+// launch.h — internal launchers behind the C ABI (not exported).
+#pragma once
+
+#include "common.cuh"
+#include "scan.cuh"
+
+namespace gdn {
+
+struct DecodeParams {
+  Pool pool;
+  int32_t Hqk, Hv, conv_dim, num_seqs;
+  float q_scale, eps;
+  const void* x;
+  const float* g;
+  const float* beta;
+  const float* conv_w;
+  const int32_t* slot;
+  void* o;
+  int32_t* err;
+};
+
+struct CopyParams {
+  Pool pool;
+  int64_t payload_bytes;
+  const int32_t* src;
+  const int32_t* dst;
+  int32_t n;
+  int32_t* err;
+};
+
+cudaError_t launch_prefill(const ScanParams& p, int dk, int dv, int in_dtype, int out_dtype,
+                           cudaStream_t st);
+cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
+                                 int out_dtype, cudaStream_t st);
+cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtype,
+                                int out_dtype, cudaStream_t st);
+cudaError_t launch_replay_rollback(int32_t* log_len, const int32_t* accepted, int32_t num_appended,
+                                   int32_t n, int32_t* err, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, int dk, int dv, int in_dtype, int out_dtype,
+                          cudaStream_t st);
+cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,99 @@
+"""Shared helpers of the GPU tests: run the engine through its binding, run
+the oracle on the same inputs, compare with the stated tolerances.
+
+Tolerances: relative Frobenius error per (sequence, value head), outputs
+<= 2e-3 and states <= 1e-4 against the fp64 oracle; conv windows, page
+indexing and checkpoint placement must match exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import gated_deltanet_state_gb300 as gdn
+from gated_deltanet_state_gb300 import inputs
+
+OUT_TOL = 2e-3
+STATE_TOL = 1e-4
+
+
+def dims(shape) -> oracle.Dims:
+    return oracle.Dims(shape.num_qk_heads, shape.num_v_heads, shape.head_dim_k, shape.head_dim_v,
+                       shape.q_scale, shape.norm_eps)
+
+
+def rel_fro(x, ref, axis) -> np.ndarray:
+    """Relative Frobenius error reduced over `axis` (the rest is kept)."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    num = np.sqrt(((x - ref) ** 2).sum(axis=axis))
+    den = np.sqrt((ref ** 2).sum(axis=axis))
+    return num / np.maximum(den, 1e-30)
+
+
+def assert_out_close(o_gpu, o_ref, cu, tol=OUT_TOL):
+    """o [T, Hv, dv]: per (sequence, head) over (tokens, dv)."""
+    o_gpu = o_gpu.float().cpu().numpy() if hasattr(o_gpu, "cpu") else o_gpu
+    worst = 0.0
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        e = rel_fro(o_gpu[a:b], o_ref[a:b], axis=(0, 2))
+        worst = max(worst, float(e.max()))
+    assert worst <= tol, f"output rel. Frobenius error {worst:.3e} > {tol:.1e}"
+    return worst
+
+
+def assert_state_close(S_gpu, S_ref, tol=STATE_TOL):
+    """S [..., Hv, dv, dk]: per head over (dv, dk)."""
+    S_gpu = S_gpu.float().cpu().numpy() if hasattr(S_gpu, "cpu") else S_gpu
+    e = rel_fro(S_gpu, S_ref, axis=(-2, -1))
+    worst = float(np.max(e)) if e.size else 0.0
+    assert worst <= tol, f"state rel. Frobenius error {worst:.3e} > {tol:.1e}"
+    return worst
+
+
+def dev(t, dtype=None):
+    t = torch.as_tensor(t)
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.contiguous().cuda()
+
+
+def run_prefill(shape, pool, x, g, beta, conv_w, cu, start, init_page, block_table, out_slot,
+                raise_on_error=True):
+    """One gdn_prefill_chunked call; returns (o on the host, device error code)."""
+    T = int(cu[-1])
+    o = torch.full((T, shape.num_v_heads, shape.head_dim_v), float("nan"), dtype=shape.torch_out(), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt = torch.as_tensor(block_table, dtype=torch.int32)
+    if bt.dim() == 1:
+        bt = bt[None]
+    st = gdn.gdn_prefill_chunked(
+        shape, pool, cu_seqlens=dev(cu, torch.int32), start_pos=dev(start, torch.int64),
+        init_page=dev(init_page, torch.int32), block_table=dev(bt), out_slot=dev(out_slot, torch.int32),
+        x=dev(x), g=dev(g, torch.float32), beta=dev(beta, torch.float32), conv_w=dev(conv_w, torch.float32),
+        o=o, dev_error=err, start_pos_host=list(start), init_page_host=list(init_page),
+        raise_on_error=raise_on_error)
+    torch.cuda.synchronize()
+    return o.cpu(), int(err.item()), st
+
+
+def oracle_head(shape, x, g, beta, conv_w, h, cu, start, block_size, S0=None, win0=None):
+    """Oracle for one value head only: a 1-qk/1-v-head layer built from the
+    channels [q_j | k_j | v_h] that head h reads (j = h // (Hv/Hqk))."""
+    G = shape.num_v_heads // shape.num_qk_heads
+    j = h // G
+    dk, dv, Hqk = shape.head_dim_k, shape.head_dim_v, shape.num_qk_heads
+    ch = np.concatenate([np.arange(j * dk, (j + 1) * dk),
+                         np.arange(Hqk * dk + j * dk, Hqk * dk + (j + 1) * dk),
+                         np.arange(2 * Hqk * dk + h * dv, 2 * Hqk * dk + (h + 1) * dv)])
+    xs = x.float().numpy()[:, ch]
+    ws = conv_w.float().numpy()[ch]
+    d1 = oracle.Dims(1, 1, dk, dv, shape.q_scale, shape.norm_eps)
+    S0h = None if S0 is None else np.asarray(S0)[:, h:h + 1]
+    w0h = None if win0 is None else np.asarray(win0)[:, :, ch]
+    return oracle.prefill(d1, cu, start, block_size, xs, g.float().numpy()[:, h:h + 1],
+                          beta.float().numpy()[:, h:h + 1], ws, S0h, w0h)

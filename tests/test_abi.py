@@ -1,0 +1,115 @@
+"""The C ABI library: it loads, exports every function include/gdn.h declares,
+and rejects bad calls on the host before any launch (no GPU needed: the
+rejected calls never touch device memory)."""
+import ctypes
+import os
+import re
+
+import torch
+
+import gated_deltanet_state_gb300 as gdn
+from gated_deltanet_state_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = gdn.load_library()
+    names = _declared()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in gdn.__all__, f"binding lacks {n}"
+
+
+def test_status_strings_and_version():
+    for code in gdn.STATUS:
+        assert gdn.gdn_status_string(code)
+    assert gdn.gdn_version() >= 100
+
+
+def _fake(n=1):
+    # Never dereferenced: every call below fails validation first.
+    return ctypes.c_void_p(0x10000)
+
+
+def _prefill(shape, pool_pages=8, start_host=None, init_host=None, block_table=True):
+    lib = gdn.load_library()
+    desc = gdn.make_desc(shape)
+    pool = gdn._Pool(0x100000, shape.page, pool_pages, 0)
+    sph, k1 = gdn._host(start_host, torch.int64, "")
+    iph, k2 = gdn._host(init_host, torch.int32, "")
+    a = gdn._PrefillArgs(len(start_host or [0]), 4, 64, 0x10000, 0x10000, sph, iph, 0x10000, 0x10000,
+                         0x10000, 0x10000, 0x10000, 0x10000 if block_table else None, 0x10000, 0x10000, 0x10000)
+    return lib.gdn_prefill_chunked(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None, 0, None)
+
+
+def test_prefill_fails_closed_on_off_boundary_resume():
+    sh = inputs.TINY
+    assert _prefill(sh, start_host=[100], init_host=[3]) == gdn.STATUS_CODE["GDN_ERR_NOT_BLOCK_ALIGNED"]
+    # cold start must begin at 0; a resume at 0 is not a resume
+    assert _prefill(sh, start_host=[64], init_host=[-1]) == gdn.STATUS_CODE["GDN_ERR_NOT_BLOCK_ALIGNED"]
+    assert _prefill(sh, start_host=[0], init_host=[2]) == gdn.STATUS_CODE["GDN_ERR_NOT_BLOCK_ALIGNED"]
+    assert _prefill(sh, start_host=[64], init_host=[99]) == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
+
+
+def test_prefill_rejects_unsupported_shapes():
+    bad = [inputs.with_(inputs.TINY, head_dim_k=48, head_dim_v=48),
+           inputs.with_(inputs.TINY, head_dim_k=32, head_dim_v=64),
+           inputs.with_(inputs.TINY, chunk_size=24),
+           inputs.with_(inputs.TINY, block_size=72),
+           inputs.with_(inputs.TINY, in_dtype=inputs.BF16, out_dtype=inputs.F32),
+           inputs.with_(inputs.TINY, num_qk_heads=3, num_v_heads=4)]
+    for sh in bad:
+        assert _prefill(sh, start_host=[0], init_host=[-1]) == gdn.STATUS_CODE["GDN_ERR_UNSUPPORTED_SHAPE"], sh
+
+
+def test_pool_too_small_or_misaligned_is_rejected():
+    lib = gdn.load_library()
+    sh = inputs.TINY
+    desc = gdn.make_desc(sh)
+    a = gdn._DecodeArgs(1, 0, *([0x10000] * 7))
+    small = gdn._Pool(0x100000, 256, 4, 0)
+    assert lib.gdn_decode_step(ctypes.byref(desc), ctypes.byref(small), ctypes.byref(a), None) == 1
+    odd = gdn._Pool(0x100010, sh.page, 4, 0)
+    assert lib.gdn_decode_step(ctypes.byref(desc), ctypes.byref(odd), ctypes.byref(a), None) == 1
+
+
+def test_checkpoint_copy_fails_closed_off_boundary():
+    lib = gdn.load_library()
+    sh = inputs.TINY
+    desc = gdn.make_desc(sh)
+    pool = gdn._Pool(0x100000, sh.page, 8, 0)
+    nc = (ctypes.c_int64 * 2)(64, 100)
+    for fn in (lib.gdn_checkpoint_resume, lib.gdn_checkpoint_save):
+        st = fn(ctypes.byref(desc), ctypes.byref(pool), 0x10000, 0x10000, nc, 2, 0x10000, None)
+        assert st == gdn.STATUS_CODE["GDN_ERR_NOT_BLOCK_ALIGNED"]
+
+
+def test_replay_rejects_oversized_append_and_bad_rollback_args():
+    lib = gdn.load_library()
+    sh = inputs.TINY
+    desc = gdn.make_desc(sh)
+    pool = gdn._Pool(0x100000, sh.page, 8, 0)
+    a = gdn._ReplayArgs(2, 33, *([0x10000] * 11))
+    assert lib.gdn_replay_append(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None) == \
+        gdn.STATUS_CODE["GDN_ERR_LOG_OVERFLOW"]
+    assert lib.gdn_replay_rollback(0x10000, 0x10000, 40, 2, 0x10000, None) == gdn.STATUS_CODE["GDN_ERR_INVALID_ARG"]
+
+
+def test_empty_batches_are_no_ops():
+    lib = gdn.load_library()
+    sh = inputs.TINY
+    desc = gdn.make_desc(sh)
+    pool = gdn._Pool(0x100000, sh.page, 8, 0)
+    a = gdn._DecodeArgs(0, 0, *([None] * 7))
+    assert lib.gdn_decode_step(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None) == 0
+    r = gdn._ReplayArgs(0, 0, *([None] * 11))
+    assert lib.gdn_replay_flush(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(r), None) == 0
+    assert lib.gdn_replay_rollback(None, None, 4, 0, None, None) == 0
