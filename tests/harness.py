@@ -1,9 +1,16 @@
 """Shared helpers of the GPU tests: run the engine through its binding, run
 the oracle on the same inputs, compare with the stated tolerances.
 
-Tolerances: relative Frobenius error per (sequence, value head), outputs
-<= 2e-3 and states <= 1e-4 against the fp64 oracle; conv windows, page
-indexing and checkpoint placement must match exactly.
+Tolerances against the fp64 oracle:
+  * outputs: relative Frobenius error <= 2e-3 over each sequence's whole
+    output tensor [tokens, heads, dv].  Outputs are stored in the output dtype;
+    bf16 rounding alone costs ~1.7e-3 relative (rms), so a norm over a single
+    64-element row would fail even for an exact engine.  In addition the error
+    against the oracle *rounded to the output dtype* must stay <= 1e-3, which
+    bounds the kernel's own error apart from the format.
+  * states: relative Frobenius error <= 1e-4 per (sequence, value head) over
+    the dv x dk matrix (fp32 storage, no format loss).
+  * conv windows, page indexing and checkpoint placement: exact.
 """
 from __future__ import annotations
 
@@ -15,6 +22,7 @@ import gated_deltanet_state_gb300 as gdn
 from gated_deltanet_state_gb300 import inputs
 
 OUT_TOL = 2e-3
+OUT_FORMAT_TOL = 1e-3
 STATE_TOL = 1e-4
 
 
@@ -32,18 +40,34 @@ def rel_fro(x, ref, axis) -> np.ndarray:
     return num / np.maximum(den, 1e-30)
 
 
-def assert_out_close(o_gpu, o_ref, cu, tol=OUT_TOL):
-    """o [T, Hv, dv]: per (sequence, head) over (tokens, dv)."""
-    o_gpu = o_gpu.float().cpu().numpy() if hasattr(o_gpu, "cpu") else o_gpu
-    worst = 0.0
+def round_to(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """The oracle's values rounded to the engine's output dtype."""
+    return torch.from_numpy(np.ascontiguousarray(ref)).to(dtype).double().numpy()
+
+
+def out_errors(o_gpu, o_ref, cu):
+    """Worst per-sequence (plain, format-aware) relative Frobenius errors of
+    outputs laid out [T, ...] with sequences delimited by cu."""
+    dt = o_gpu.dtype if hasattr(o_gpu, "dtype") and isinstance(o_gpu.dtype, torch.dtype) else torch.float32
+    o = o_gpu.double().cpu().numpy() if hasattr(o_gpu, "cpu") else np.asarray(o_gpu, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    r_ref = round_to(o_ref, dt)
+    plain = fmt = 0.0
     for s in range(len(cu) - 1):
         a, b = int(cu[s]), int(cu[s + 1])
         if b == a:
             continue
-        e = rel_fro(o_gpu[a:b], o_ref[a:b], axis=(0, 2))
-        worst = max(worst, float(e.max()))
-    assert worst <= tol, f"output rel. Frobenius error {worst:.3e} > {tol:.1e}"
-    return worst
+        den = max(np.linalg.norm(o_ref[a:b]), 1e-30)
+        plain = max(plain, float(np.linalg.norm(o[a:b] - o_ref[a:b]) / den))
+        fmt = max(fmt, float(np.linalg.norm(o[a:b] - r_ref[a:b]) / den))
+    return plain, fmt
+
+
+def assert_out_close(o_gpu, o_ref, cu, tol=OUT_TOL, fmt_tol=OUT_FORMAT_TOL):
+    plain, fmt = out_errors(o_gpu, o_ref, cu)
+    assert plain <= tol, f"output rel. Frobenius error {plain:.3e} > {tol:.1e}"
+    assert fmt <= fmt_tol, f"output error beyond the output format {fmt:.3e} > {fmt_tol:.1e}"
+    return plain
 
 
 def assert_state_close(S_gpu, S_ref, tol=STATE_TOL):
