@@ -117,27 +117,28 @@ class ClockSampler:
 class PrefillWork:
     """4 x 8192 tokens of the 27B-shaped layer, checkpoints every 896 tokens."""
 
-    def __init__(self, seed: int):
+    def __init__(self, seed: int, seq_len: int = SEQ_LEN):
         sh = PREFILL
         self.sh = sh
-        T = N_SEQ * SEQ_LEN
+        T = N_SEQ * seq_len
         # a2: the scheduler's chunk for this call; the whole prompt fits the budget
-        self.chunk_end = gdn.gdn_chunk_end(0, SEQ_LEN, SEQ_LEN, sh.block_size)
-        assert self.chunk_end == SEQ_LEN
+        self.chunk_end = gdn.gdn_chunk_end(0, seq_len, seq_len, sh.block_size)
+        assert self.chunk_end == seq_len
         ti = inputs.token_inputs(sh, T, seed)
         self.host = {k: v.pin_memory() for k, v in ti.items()}
         self.x = ti["x"].cuda()
         self.g = ti["g"].cuda()
         self.beta = ti["beta"].cuda()
         self.w = inputs.conv_weights(sh, seed).cuda()
-        nck = SEQ_LEN // sh.block_size            # 9 boundaries per sequence
+        nck = max(1, seq_len // sh.block_size)    # 9 boundaries per sequence at 8192
         self.num_pages = N_SEQ * (nck + 1)
         perm = inputs.permutation(self.num_pages, seed).tolist()
         self.block_table = torch.tensor([perm[s * nck:(s + 1) * nck] for s in range(N_SEQ)],
                                         dtype=torch.int32).cuda()
         self.out_slot = torch.tensor(perm[N_SEQ * nck:], dtype=torch.int32).cuda()
         self.pool = gdn.StatePool(sh, self.num_pages, fill=0)
-        self.cu = torch.arange(0, T + 1, SEQ_LEN, dtype=torch.int32).cuda()
+        self.cu = torch.arange(0, T + 1, seq_len, dtype=torch.int32).cuda()
+        self.seq_len = seq_len
         self.start = torch.zeros(N_SEQ, dtype=torch.int64).cuda()
         self.init = torch.full((N_SEQ,), -1, dtype=torch.int32).cuda()
         self.o = torch.empty(T, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
@@ -177,7 +178,7 @@ class PrefillWork:
     def algorithmic_bytes(self):
         sh = self.sh
         per_tok = sh.conv_dim * 2 + 2 * sh.num_v_heads * 4 + sh.num_v_heads * sh.head_dim_v * 2
-        ck = (SEQ_LEN // sh.block_size + 1) * N_SEQ * sh.payload_bytes
+        ck = (self.seq_len // sh.block_size + 1) * N_SEQ * sh.payload_bytes
         return per_tok * self.tokens + ck
 
 
@@ -341,6 +342,35 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- main
 
+def run_part(args):
+    """One part of the step alone (for profiling): W warm-up and K timed runs,
+    one JSON line with the part's device time."""
+    if args.only == "prefill":
+        w = PrefillWork(args.seed, args.seq_len)
+        fn, unit_ms = w.run, None
+    elif args.only == "decode":
+        w = DecodeWork(args.seed)
+        fn = w.run
+    else:
+        w = ReplayWork(args.seed)
+        fn = lambda: (w.verify(), w.flush())
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    line = {"part": args.only, "ms_per_run": ms, "steps": args.steps, "warmup": args.warmup}
+    if args.only == "prefill":
+        line["tokens_per_s_per_layer"] = w.tokens / (ms * 1e-3)
+        line["seq_len"] = args.seq_len
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,6 +379,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "replay"],
+                    help="time one part only (profiling); the default times the whole step")
+    ap.add_argument("--seq-len", type=int, default=SEQ_LEN,
+                    help="prefill tokens per sequence (profiling of smaller cases)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -365,33 +399,52 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     gdn.load_library()
 
-    pre = PrefillWork(args.seed + rank)
+    if args.only != "all":
+        return run_part(args)
+    pre = PrefillWork(args.seed + rank, args.seq_len)
     dec = DecodeWork(args.seed + 10 + rank)
     rep = ReplayWork(args.seed + 20 + rank)
     stream = torch.cuda.current_stream()
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(record=None):
-        e = [ev() for _ in range(6)] if record is not None else None
-        if e: e[0].record(stream)
-        pre.run()
-        if e: e[1].record(stream)
-        dec.run()
-        if e: e[2].record(stream)
-        rep.verify()
-        if e: e[3].record(stream)
-        rep.flush()
-        if e: e[4].record(stream)
-        if record is not None:
-            record.append(e)
-
+    # Warm up eagerly, then capture the launch-bound 24-layer loops of decode
+    # and replay into CUDA graphs (the prefill is one call).
     for _ in range(args.warmup):
-        step()
+        pre.run(); dec.run(); rep.verify(); rep.flush()
     torch.cuda.synchronize()
     errs = [int(pre.err.item()), int(dec.err.item()), int(rep.err.item())]
     if any(errs):
         raise RuntimeError(f"device error words after warm-up: {errs}")
+    graphs = {}
+    for name, fn in (("dec", dec.run), ("ver", rep.verify), ("fl", rep.flush)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    for _ in range(2):
+        for g in graphs.values():
+            g.replay()
+    torch.cuda.synchronize()
+
+    def step(record=None):
+        e = [ev() for _ in range(5)] if record is not None else None
+        if e: e[0].record(stream)
+        pre.run()
+        if e: e[1].record(stream)
+        graphs["dec"].replay()
+        if e: e[2].record(stream)
+        graphs["ver"].replay()
+        if e: e[3].record(stream)
+        graphs["fl"].replay()
+        if e: e[4].record(stream)
+        if record is not None:
+            record.append(e)
+
+    step()
+    torch.cuda.synchronize()
+    if int(rep.err.item()) or int(dec.err.item()) or int(pre.err.item()):
+        raise RuntimeError("device error word set during graph replay")
 
     recs = []
     with ClockSampler(local) as clk:
@@ -461,7 +514,7 @@ def main():
         "e2e": {"value": world * pre.tokens / (e2e_ms * 1e-3), "unit": "tokens/s/layer",
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
                 "scope": "prefill part of the step"},
-        "gpu_launches": args.steps * (2 + DEC_LAYERS + 5 * REP_LAYERS),
+        "gpu_launches": args.steps * (2 + DEC_LAYERS + 7 * REP_LAYERS),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

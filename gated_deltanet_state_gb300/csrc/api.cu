@@ -60,6 +60,9 @@ ScanParams base_scan(const gdn_layer_desc* d, const gdn_pool* pool) {
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
+// Pre-conv rows and conv taps are read in 16-byte words.
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
 }  // namespace
 
 extern "C" {
@@ -82,6 +85,7 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
       !a->dev_error || a->max_blocks < 0 || (a->max_blocks > 0 && !a->block_table))
     return GDN_ERR_INVALID_ARG;
   if (a->total_tokens > 0 && (!a->x || !a->g || !a->beta || !a->o)) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(a->x) || !aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
   // Fail closed before launching anything when the host can see an
   // off-boundary resume or a cold start that does not begin at 0.
   if (a->start_pos_host) {
@@ -121,6 +125,7 @@ gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
   if (a->num_seqs == 0) return GDN_OK;
   if (!a->x || !a->g || !a->beta || !a->conv_w || !a->slot || !a->o || !a->dev_error)
     return GDN_ERR_INVALID_ARG;
+  if (!aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
   DecodeParams p;
   p.pool = make_pool(desc, pool);
   p.Hqk = desc->num_qk_heads;
@@ -185,6 +190,8 @@ static gdn_status replay_common(const gdn_layer_desc* desc, const gdn_pool* pool
   if (!a->ckpt_slot || !a->log_x || !a->log_g || !a->log_beta || !a->log_len || !a->conv_w ||
       !a->dev_error)
     return a->num_reqs == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!aligned16(a->log_x) || !aligned16(a->conv_w) || (append && !aligned16(a->x_new)))
+    return GDN_ERR_INVALID_ARG;
   if (append) {
     if (a->num_new < 0) return GDN_ERR_INVALID_ARG;
     if (a->num_new > GDN_REPLAY_LOG_SLOTS) return GDN_ERR_LOG_OVERFLOW;

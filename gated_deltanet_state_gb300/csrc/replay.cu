@@ -7,29 +7,30 @@
 
 namespace gdn {
 
-// Appends the m new rows (x, g, beta) after the n logged rows of request r and
-// then publishes log_len[r] = n + m.  One CTA per request, launched after the
-// append scan has read the old log_len.
+// Copies the m new rows (x, g, beta) of request r after its n logged rows.
+// Grid: (row chunks, requests).  log_len is published later by log_len_kernel.
 template <typename TIN>
 __global__ void __launch_bounds__(256) log_append_kernel(const ScanParams p) {
-  const int r = blockIdx.x;
+  const int r = blockIdx.y;
   const int32_t n = p.log_len[r];
   const int m = p.num_new;
   if (!page_ok(p.pool, p.ckpt_slot[r]) || n < 0 || n + m > GDN_REPLAY_LOG_SLOTS) return;
   const int64_t lrow = (int64_t)r * GDN_REPLAY_LOG_SLOTS + n;
   const int64_t nrow = (int64_t)r * m;
-  TIN* lx = reinterpret_cast<TIN*>(const_cast<void*>(p.log_x)) + lrow * p.conv_dim;
-  const TIN* xn = reinterpret_cast<const TIN*>(p.x_new) + nrow * p.conv_dim;
-  const int64_t nx = (int64_t)m * p.conv_dim;
-  for (int64_t i = threadIdx.x; i < nx; i += blockDim.x) lx[i] = xn[i];
-  float* lg = const_cast<float*>(p.log_g) + lrow * p.Hv;
-  float* lb = const_cast<float*>(p.log_beta) + lrow * p.Hv;
-  for (int i = threadIdx.x; i < m * p.Hv; i += blockDim.x) {
-    lg[i] = p.g_new[nrow * p.Hv + i];
-    lb[i] = p.beta_new[nrow * p.Hv + i];
+  // x rows as 16-byte words (conv_dim * sizeof(TIN) is a multiple of 16)
+  uint4* lx = reinterpret_cast<uint4*>(reinterpret_cast<TIN*>(const_cast<void*>(p.log_x)) + lrow * p.conv_dim);
+  const uint4* xn = reinterpret_cast<const uint4*>(reinterpret_cast<const TIN*>(p.x_new) + nrow * p.conv_dim);
+  const int64_t nw = (int64_t)m * p.conv_dim * sizeof(TIN) / 16;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nw; i += (int64_t)gridDim.x * blockDim.x)
+    lx[i] = xn[i];
+  if (blockIdx.x == 0) {
+    float* lg = const_cast<float*>(p.log_g) + lrow * p.Hv;
+    float* lb = const_cast<float*>(p.log_beta) + lrow * p.Hv;
+    for (int i = threadIdx.x; i < m * p.Hv; i += blockDim.x) {
+      lg[i] = p.g_new[nrow * p.Hv + i];
+      lb[i] = p.beta_new[nrow * p.Hv + i];
+    }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) const_cast<int32_t*>(p.log_len)[r] = n + m;
 }
 
 cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
@@ -38,8 +39,13 @@ cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dty
   cudaError_t e = [&]() -> cudaError_t { GDN_SCAN_DISPATCH(kAppend) }();
   if (e != cudaSuccess) return e;
   if (p.num_new == 0) return cudaSuccess;
-  if (in_dtype == GDN_BF16) log_append_kernel<__nv_bfloat16><<<p.num_seqs, 256, 0, st>>>(p);
-  else log_append_kernel<float><<<p.num_seqs, 256, 0, st>>>(p);
+  const int64_t words = (int64_t)p.num_new * p.conv_dim * (in_dtype == GDN_BF16 ? 2 : 4) / 16;
+  const dim3 grid((unsigned)((words + 256 * 4 - 1) / (256 * 4)), p.num_seqs);
+  if (in_dtype == GDN_BF16) log_append_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
+  else log_append_kernel<float><<<grid, 256, 0, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  log_len_kernel<kAppend><<<(p.num_seqs + 255) / 256, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -7,7 +7,7 @@ namespace gdn {
 
 template <int DK, int DV, int RPT, typename TIN, typename TOUT, int MODE>
 cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t st) {
-  constexpr size_t smem = scan_smem_bytes<DK, DV, RPT>();
+  constexpr size_t smem = scan_smem_bytes<DK, DV, RPT, TIN>();
   auto kern = scan_kernel<DK, DV, RPT, TIN, TOUT, MODE>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -17,11 +17,13 @@ cudaError_t launch_scan_t(const ScanParams& p, cudaStream_t st) {
   kern<<<grid, kScanThreads, smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // Windows: one CTA per sequence for the flush (it clears log_len after all
-  // channels are done), channel blocks otherwise.
-  const int wx = MODE == kFlush ? 1 : (p.conv_dim + 255) / 256;
+  // Windows: channel blocks x sequences (the append writes none).
   if (MODE != kAppend) {
-    window_kernel<TIN, MODE><<<dim3(wx, p.num_seqs), 256, 0, st>>>(p);
+    window_kernel<TIN, MODE><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+    e = cudaGetLastError();
+  }
+  if (MODE == kFlush && e == cudaSuccess) {
+    log_len_kernel<kFlush><<<(p.num_seqs + 255) / 256, 256, 0, st>>>(p);
     e = cudaGetLastError();
   }
   return e;

@@ -223,3 +223,30 @@ def test_replay_device_errors():
     torch.cuda.synchronize()
     assert R.err.item() == gdn.STATUS_CODE["GDN_ERR_ROLLBACK_RANGE"]
     assert R.log_len.cpu().tolist() == [5, 20]
+
+
+def test_decode_and_flush_replay_identically_inside_a_cuda_graph():
+    # The entry points are stream-ordered and allocate nothing, so a captured
+    # sequence of calls replays the eager arithmetic bit for bit.
+    sh = inputs.LayerShape(2, 4, 128, 128, 64, 16)
+    N = 3
+    st = inputs.random_state(sh, N, seed=31)
+    ti = inputs.token_inputs(sh, N, seed=32)
+    w = dev(inputs.conv_weights(sh, 32))
+    pools = []
+    for _ in range(2):
+        pool = gdn.StatePool(sh, N, fill=0)
+        _seed_pages(pool, list(range(N)), st)
+        pools.append(pool)
+    args = dict(x=dev(ti["x"]), g=dev(ti["g"]), beta=dev(ti["beta"]), conv_w=w, slot=dev(list(range(N)), torch.int32))
+    outs = [torch.empty(N, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_decode_step(sh, pools[0], o=outs[0], dev_error=err, **args)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdn.gdn_decode_step(sh, pools[1], o=outs[1], dev_error=err, **args)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(pools[0].buf, pools[1].buf)
