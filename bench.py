@@ -145,6 +145,7 @@ class PrefillWork:
         self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.tokens = T
+        self.ws = gdn.workspace_for(gdn.gdn_prefill_workspace_size(sh, N_SEQ, T))
 
     def run(self, x=None, g=None, beta=None, o=None):
         gdn.gdn_prefill_chunked(self.sh, self.pool, cu_seqlens=self.cu, start_pos=self.start,
@@ -152,7 +153,8 @@ class PrefillWork:
                                 x=self.x if x is None else x, g=self.g if g is None else g,
                                 beta=self.beta if beta is None else beta, conv_w=self.w,
                                 o=self.o if o is None else o, dev_error=self.err,
-                                start_pos_host=[0] * N_SEQ, init_page_host=[-1] * N_SEQ)
+                                start_pos_host=[0] * N_SEQ, init_page_host=[-1] * N_SEQ,
+                                workspace=self.ws, max_seq_len=self.seq_len)
 
     def run_e2e(self):
         """Host buffers in, host buffers out, through the same C-ABI call."""
@@ -252,10 +254,11 @@ class ReplayWork:
                              device="cuda")
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.kept_rows = float(sum(int(l["acc"].sum()) for l in self.layers)) / REP_LAYERS
+        self.ws = gdn.workspace_for(gdn.gdn_replay_workspace_size(sh, REP_REQS))
 
     def _kw(self, l):
         return dict(ckpt_slot=l["ckpt"], log_x=l["log_x"], log_g=l["log_g"], log_beta=l["log_b"],
-                    log_len=l["log_len"], conv_w=self.w, dev_error=self.err)
+                    log_len=l["log_len"], conv_w=self.w, dev_error=self.err, workspace=self.ws)
 
     def verify(self):
         for l in self.layers:
@@ -514,7 +517,7 @@ def main():
         "e2e": {"value": world * pre.tokens / (e2e_ms * 1e-3), "unit": "tokens/s/layer",
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
                 "scope": "prefill part of the step"},
-        "gpu_launches": args.steps * (2 + DEC_LAYERS + 7 * REP_LAYERS),
+        "gpu_launches": args.steps * (3 + DEC_LAYERS + 9 * REP_LAYERS),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -27,7 +27,8 @@ __all__ = [
     "gdn_status_string", "gdn_version", "gdn_conv_dim", "gdn_mamba_page_bytes",
     "gdn_block_size_for", "gdn_mamba_pages_per_request", "gdn_pool_blocks_for_pages",
     "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_spec_copy_bytes",
-    "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_prefill_chunked",
+    "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
+    "gdn_prefill_chunked", "workspace_for",
     "gdn_decode_step", "gdn_checkpoint_resume", "gdn_checkpoint_save", "gdn_replay_append",
     "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "STATUS",
 ]
@@ -75,7 +76,8 @@ _P = ctypes.c_void_p
 
 class _PrefillArgs(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
-                ("total_tokens", ctypes.c_int64), ("cu_seqlens", _P), ("start_pos", _P),
+                ("total_tokens", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
+                ("cu_seqlens", _P), ("start_pos", _P),
                 ("start_pos_host", _P), ("init_page_host", _P), ("x", _P), ("g", _P),
                 ("beta", _P), ("conv_w", _P), ("init_page", _P), ("block_table", _P),
                 ("out_slot", _P), ("o", _P), ("dev_error", _P)]
@@ -90,7 +92,8 @@ class _DecodeArgs(ctypes.Structure):
 class _ReplayArgs(ctypes.Structure):
     _fields_ = [("num_reqs", ctypes.c_int32), ("num_new", ctypes.c_int32), ("ckpt_slot", _P),
                 ("log_x", _P), ("log_g", _P), ("log_beta", _P), ("log_len", _P), ("x_new", _P),
-                ("g_new", _P), ("beta_new", _P), ("conv_w", _P), ("o", _P), ("dev_error", _P)]
+                ("g_new", _P), ("beta_new", _P), ("conv_w", _P), ("o", _P), ("dev_error", _P),
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
 
 
 # --------------------------------------------------------------------------- loading
@@ -127,6 +130,7 @@ def load_library(build_if_missing: bool = True):
         "gdn_spec_copy_bytes": ([i32, i32, i64], i64),
         "gdn_replay_bytes_per_request": ([i32, i64, i32, i64], i64),
         "gdn_prefill_workspace_size": ([D, i32, i64], sz),
+        "gdn_replay_workspace_size": ([D, i32], sz),
         "gdn_prefill_chunked": ([D, PL, ctypes.POINTER(_PrefillArgs), _P, sz, _P], i32),
         "gdn_decode_step": ([D, PL, ctypes.POINTER(_DecodeArgs), _P], i32),
         "gdn_checkpoint_resume": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
@@ -279,20 +283,33 @@ def gdn_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: i
     return int(load_library().gdn_prefill_workspace_size(ctypes.byref(make_desc(shape)), num_seqs, total_tokens))
 
 
+def gdn_replay_workspace_size(shape: LayerShape, num_reqs: int) -> int:
+    return int(load_library().gdn_replay_workspace_size(ctypes.byref(make_desc(shape)), num_reqs))
+
+
+def workspace_for(nbytes: int, device="cuda") -> torch.Tensor:
+    """A device scratch buffer of at least nbytes (PyTorch owns the memory)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
 # --------------------------------------------------------------------------- device entry points
 
 def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
                         block_table, out_slot, x, g, beta, conv_w, o, dev_error,
-                        start_pos_host=None, init_page_host=None, workspace=None, stream=None,
-                        raise_on_error: bool = True) -> int:
-    """Chunked prefill with block checkpoints (see gdn.h for the contract)."""
+                        start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
+                        stream=None, raise_on_error: bool = True) -> int:
+    """Chunked prefill with block checkpoints (see gdn.h for the contract).
+    Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
+    taken from PyTorch's allocator for the call."""
     lib = load_library()
     n = int(cu_seqlens.numel()) - 1
+    if workspace is None:
+        workspace = workspace_for(gdn_prefill_workspace_size(shape, n, int(x.shape[0])), x.device)
     sph, keep1 = _host(start_pos_host, torch.int64, "start_pos_host")
     iph, keep2 = _host(init_page_host, torch.int32, "init_page_host")
     bt = block_table
     a = _PrefillArgs(n, int(bt.shape[1]) if bt is not None and bt.dim() == 2 else 0,
-                     int(x.shape[0]), _dev(cu_seqlens, torch.int32, "cu_seqlens"),
+                     int(x.shape[0]), int(max_seq_len), _dev(cu_seqlens, torch.int32, "cu_seqlens"),
                      _dev(start_pos, torch.int64, "start_pos"), sph, iph,
                      _dev(x, shape.torch_in(), "x"), _dev(g, torch.float32, "g"),
                      _dev(beta, torch.float32, "beta"), _dev(conv_w, torch.float32, "conv_w"),
@@ -345,23 +362,27 @@ def gdn_checkpoint_save(shape: LayerShape, pool: StatePool, src_page, dst_page, 
 
 
 def _replay_args(shape, *, ckpt_slot, log_x, log_g, log_beta, log_len, conv_w, dev_error,
-                 x_new=None, g_new=None, beta_new=None, o=None, num_new=0):
-    return _ReplayArgs(int(ckpt_slot.numel()), int(num_new), _dev(ckpt_slot, torch.int32, "ckpt_slot"),
+                 x_new=None, g_new=None, beta_new=None, o=None, num_new=0, workspace=None):
+    if workspace is None:
+        workspace = workspace_for(gdn_replay_workspace_size(shape, int(ckpt_slot.numel())), log_x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    return workspace, _ReplayArgs(int(ckpt_slot.numel()), int(num_new), _dev(ckpt_slot, torch.int32, "ckpt_slot"),
                        _dev(log_x, shape.torch_in(), "log_x"), _dev(log_g, torch.float32, "log_g"),
                        _dev(log_beta, torch.float32, "log_beta"), _dev(log_len, torch.int32, "log_len"),
                        _dev(x_new, shape.torch_in(), "x_new"), _dev(g_new, torch.float32, "g_new"),
                        _dev(beta_new, torch.float32, "beta_new"), _dev(conv_w, torch.float32, "conv_w"),
-                       _dev(o, shape.torch_out(), "o"), _dev(dev_error, torch.int32, "dev_error"))
+                       _dev(o, shape.torch_out(), "o"), _dev(dev_error, torch.int32, "dev_error"),
+                       _dev(workspace, None, "workspace"), ws_bytes)
 
 
 def gdn_replay_append(shape: LayerShape, pool: StatePool, *, ckpt_slot, log_x, log_g, log_beta, log_len,
-                      x_new, g_new, beta_new, conv_w, o, dev_error, stream=None,
+                      x_new, g_new, beta_new, conv_w, o, dev_error, workspace=None, stream=None,
                       raise_on_error: bool = True) -> int:
     """Outputs of the new rows from checkpoint + log; the rows join the log."""
     lib = load_library()
-    a = _replay_args(shape, ckpt_slot=ckpt_slot, log_x=log_x, log_g=log_g, log_beta=log_beta,
-                     log_len=log_len, conv_w=conv_w, dev_error=dev_error, x_new=x_new, g_new=g_new,
-                     beta_new=beta_new, o=o, num_new=int(x_new.shape[1]))
+    keep, a = _replay_args(shape, ckpt_slot=ckpt_slot, log_x=log_x, log_g=log_g, log_beta=log_beta,
+                           log_len=log_len, conv_w=conv_w, dev_error=dev_error, x_new=x_new, g_new=g_new,
+                           beta_new=beta_new, o=o, num_new=int(x_new.shape[1]), workspace=workspace)
     st = lib.gdn_replay_append(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
                                _stream(stream))
     return _check(st, "gdn_replay_append") if raise_on_error else st
@@ -378,11 +399,11 @@ def gdn_replay_rollback(log_len, accepted, num_appended: int, dev_error, stream=
 
 
 def gdn_replay_flush(shape: LayerShape, pool: StatePool, *, ckpt_slot, log_x, log_g, log_beta, log_len,
-                     conv_w, dev_error, stream=None, raise_on_error: bool = True) -> int:
+                     conv_w, dev_error, workspace=None, stream=None, raise_on_error: bool = True) -> int:
     """Apply the logged rows to the checkpoint page in place; empties the log."""
     lib = load_library()
-    a = _replay_args(shape, ckpt_slot=ckpt_slot, log_x=log_x, log_g=log_g, log_beta=log_beta,
-                     log_len=log_len, conv_w=conv_w, dev_error=dev_error)
+    keep, a = _replay_args(shape, ckpt_slot=ckpt_slot, log_x=log_x, log_g=log_g, log_beta=log_beta,
+                           log_len=log_len, conv_w=conv_w, dev_error=dev_error, workspace=workspace)
     st = lib.gdn_replay_flush(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
                               _stream(stream))
     return _check(st, "gdn_replay_flush") if raise_on_error else st

@@ -69,14 +69,21 @@ extern "C" {
 
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens) {
-  (void)desc; (void)num_seqs; (void)total_tokens;
-  return 0;  // the scan keeps every intermediate on chip
+  (void)num_seqs;
+  if (gdn_conv_dim(desc) <= 0 || total_tokens < 0) return 0;
+  return scan_workspace_bytes(total_tokens, (int)gdn_conv_dim(desc), desc->num_qk_heads,
+                              desc->num_v_heads);
+}
+
+size_t gdn_replay_workspace_size(const gdn_layer_desc* desc, int32_t num_reqs) {
+  if (gdn_conv_dim(desc) <= 0 || num_reqs < 0) return 0;
+  return scan_workspace_bytes((int64_t)num_reqs * GDN_REPLAY_LOG_SLOTS, (int)gdn_conv_dim(desc),
+                              desc->num_qk_heads, desc->num_v_heads);
 }
 
 gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
                                const gdn_prefill_args* a, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  (void)workspace; (void)workspace_bytes;
   gdn_status st = check_desc_pool(desc, pool);
   if (st != GDN_OK) return st;
   if (!a || a->num_seqs < 0 || a->num_seqs > kMaxGrid || a->total_tokens < 0) return GDN_ERR_INVALID_ARG;
@@ -99,6 +106,10 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   if (a->init_page_host)
     for (int32_t s = 0; s < a->num_seqs; ++s)
       if (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages) return GDN_ERR_PAGE_RANGE;
+  if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
+  if (a->total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
   p.num_seqs = a->num_seqs;
   p.conv_w = a->conv_w;
@@ -113,7 +124,9 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.x = a->x;
   p.g = a->g;
   p.beta = a->beta;
-  return cuda_status(launch_prefill(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+  bind_workspace(p, workspace, a->total_tokens);
+  const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
+  return cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
                                     desc->out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
@@ -197,7 +210,10 @@ static gdn_status replay_common(const gdn_layer_desc* desc, const gdn_pool* pool
     if (a->num_new > GDN_REPLAY_LOG_SLOTS) return GDN_ERR_LOG_OVERFLOW;
     if (a->num_new > 0 && (!a->x_new || !a->g_new || !a->beta_new || !a->o)) return GDN_ERR_INVALID_ARG;
   }
+  const size_t need = gdn_replay_workspace_size(desc, a->num_reqs);
+  if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
+  bind_workspace(p, a->workspace, (int64_t)a->num_reqs * GDN_REPLAY_LOG_SLOTS);
   p.num_seqs = a->num_reqs;
   p.conv_w = a->conv_w;
   p.o = a->o;

@@ -28,8 +28,13 @@ struct CopyParams {
   int32_t* err;
 };
 
-cudaError_t launch_prefill(const ScanParams& p, int dk, int dv, int in_dtype, int out_dtype,
-                           cudaStream_t st);
+// Workspace bytes of the conv pre-pass for `rows` token rows.
+size_t scan_workspace_bytes(int64_t rows, int conv_dim, int Hqk, int Hv);
+// p.ws_* must be bound (bind_workspace) before the launchers run.
+void bind_workspace(ScanParams& p, void* ws, int64_t rows);
+
+cudaError_t launch_prefill(const ScanParams& p, int64_t max_len, int dk, int dv, int in_dtype,
+                           int out_dtype, cudaStream_t st);
 cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
                                  int out_dtype, cudaStream_t st);
 cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtype,

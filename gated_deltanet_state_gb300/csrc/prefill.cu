@@ -3,8 +3,14 @@
 
 namespace gdn {
 
-cudaError_t launch_prefill(const ScanParams& p, int dk, int dv, int in_dtype, int out_dtype,
-                           cudaStream_t st) {
+size_t scan_workspace_bytes(int64_t rows, int conv_dim, int Hqk, int Hv) {
+  return ws_layout(rows, conv_dim, Hqk, Hv).bytes;
+}
+
+void bind_workspace(ScanParams& p, void* ws, int64_t rows) { ws_bind(p, ws, rows); }
+
+cudaError_t launch_prefill(const ScanParams& p, int64_t max_len, int dk, int dv, int in_dtype,
+                           int out_dtype, cudaStream_t st) {
   GDN_SCAN_DISPATCH(kPrefill)
 }
 

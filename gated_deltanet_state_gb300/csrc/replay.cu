@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) log_append_kernel(const ScanParams p) {
 cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
                                  int out_dtype, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
+  const int64_t max_len = GDN_REPLAY_LOG_SLOTS;
   cudaError_t e = [&]() -> cudaError_t { GDN_SCAN_DISPATCH(kAppend) }();
   if (e != cudaSuccess) return e;
   if (p.num_new == 0) return cudaSuccess;
@@ -51,6 +52,7 @@ cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dty
 
 cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtype, int out_dtype,
                                 cudaStream_t st) {
+  const int64_t max_len = GDN_REPLAY_LOG_SLOTS;
   GDN_SCAN_DISPATCH(kFlush)
 }
 

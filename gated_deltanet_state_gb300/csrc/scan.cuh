@@ -9,7 +9,8 @@
 // communication and does not change any result bit.
 //
 // Deferred decay: inside a tile of 16 tokens the registers hold R = S / A with
-// A = prod a (a per-head scalar), so a token costs three FMAs per element:
+// A = prod a (a per-head scalar), so a token costs three FMAs per element
+// (issued as packed fp32 pairs, fma.rn.f32x2, two elements per instruction):
 // R += (c/A) k_t, o += R q_t, u += R k_{t+1}.  At each tile end R is scaled
 // back (R *= A, A = 1).  A token whose running product would fall below 2^-64
 // applies its decay directly instead (R = (A a) R + c k, A = 1), so R never
@@ -22,13 +23,17 @@
 // from it replays the cold run's arithmetic bit for bit.
 //
 // Thread layout: four lanes share a row, each owning DK/4 columns as float4
-// chunks 4*(4m+cq) (interleaved so a quad's shared-memory reads hit distinct
-// banks).  All sums run in a fixed order.
+// chunks 4*(4m+cq) (interleaved so a group's shared-memory reads hit distinct
+// banks); a 128-thread CTA covers 32 row groups x RPT rows.  All sums run in a
+// fixed order, with two partial sums per dot product for instruction-level
+// parallelism.
 //
-// Input staging: the CTA's q, k and v-slice channels of the pre-conv rows of
-// the next tile are copied into shared memory with cp.async while the current
-// tile is scanned (double buffer); conv + SiLU and the L2 norms of q and k are
-// then computed from shared memory.
+// Inputs: a pre-pass kernel computes SiLU(conv) of every channel once (plus
+// the q / k norm factors and the gates) into a workspace; the scan streams its
+// q, k and v-slice rows from there into two shared-memory stages with
+// cp.async, loading tile j+1 while it scans tile j.  q and k stay
+// unnormalised; their norm factors are applied as per-token scalars, which is
+// the same product reassociated.
 #pragma once
 
 #include "common.cuh"
@@ -65,6 +70,10 @@ struct ScanParams {
   const void* x_new;
   const float* g_new;
   const float* beta_new;
+  // workspace written by the conv pre-pass, read by the scan
+  float* ws_y;     // [rows][conv_dim]   SiLU(conv) of every channel
+  float* ws_nrm;   // [rows][2*Hqk]      q (times q_scale) and k norm factors
+  float* ws_ab;    // [rows][Hv][2]      a = exp(g), b
 };
 
 // Per-sequence view of the token stream: relative token t >= -3; negative t
@@ -77,6 +86,7 @@ struct TokenView {
   const float* g0; const float* g1;
   const float* b0; const float* b1;
   int64_t n0, n;
+  int64_t wrow0;         // workspace row of token 0
   int32_t conv_dim, Hv;
 
   __device__ __forceinline__ float x(int64_t t, int c) const {
@@ -140,6 +150,7 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
     v.g0 = v.g1 = p.g + t0 * p.Hv;
     v.b0 = v.b1 = p.beta + t0 * p.Hv;
     v.n0 = v.n = t1 - t0;
+    v.wrow0 = t0;
     return true;
   } else {
     init = p.ckpt_slot[s];
@@ -164,77 +175,142 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
     v.b1 = MODE == kAppend ? p.beta_new + nrow * p.Hv : v.b0;
     v.n0 = len;
     v.n = len + m;
+    v.wrow0 = lrow;
     return true;
   }
 }
 
-constexpr int kScanTile = 16;
-constexpr int kScanThreads = 128;
+// ---------------------------------------------------------------------------
+// Conv pre-pass: SiLU(depthwise causal conv) of every channel of every token,
+// once, into the workspace, with the L2-norm factors of each q and k head and
+// the gates of each value head.  One CTA covers one head's D channels for
+// kConvTokens tokens of one sequence; it is bound by HBM (reads x once, writes
+// fp32 rows), so it uses the accurate expf / division.
+constexpr int kConvTokens = 64;
 
-// Shared-memory plan of one scan CTA (byte offsets).
-template <int DK, int DV, int RPT, typename TIN>
-struct ScanSmem {
-  static constexpr int TT = kScanTile, ROWS = 32 * RPT, NC = 2 * DK + ROWS;
-  static constexpr int XROWS = TT + 3;  // pre-conv rows t0-3 .. t0+TT-1
-  static constexpr size_t q = 0;                                      // f32 [TT][DK]
-  static constexpr size_t k = q + sizeof(float) * TT * DK;            // f32 [TT][DK]
-  static constexpr size_t vo = k + sizeof(float) * TT * DK;           // f32 [TT][ROWS]: v in, o out
-  static constexpr size_t ab = vo + sizeof(float) * TT * ROWS;        // f32 [2][TT]: a, b
-  static constexpr size_t xs = (ab + sizeof(float) * 2 * TT + 15) / 16 * 16;  // TIN [2][XROWS][NC]
-  static constexpr size_t gb = xs + 2 * sizeof(TIN) * XROWS * NC;     // f32 [2][2][TT]: g, beta
-  static constexpr size_t bytes = gb + sizeof(float) * 2 * 2 * TT;
-};
-
-template <int DK, int DV, int RPT, typename TIN>
-constexpr size_t scan_smem_bytes() { return ScanSmem<DK, DV, RPT, TIN>::bytes; }
-
-// Issues the asynchronous copies of one tile: the CTA's q, k and v-slice
-// channels of pre-conv rows t0-3 .. t0+TT-1 (window rows before the sequence,
-// zeros on a cold start or past the end), and g, beta of tokens t0 .. t0+TT-1.
-template <int DK, int DV, int RPT, typename TIN>
-__device__ __forceinline__ void stage_tile(const ScanParams& p, const TokenView<TIN>& V, TIN* xs,
-                                           float* gb, int64_t t0, int cqk, int ckk, int cvv, int h,
-                                           int tid) {
-  using L = ScanSmem<DK, DV, RPT, TIN>;
-  constexpr int CH = 16 / sizeof(TIN);            // elements per 16-byte chunk
-  constexpr int QC = DK / CH, VC = L::ROWS / CH;  // chunks per channel segment
-  constexpr int RC = 2 * QC + VC;                 // chunks per row
-  const void* dummy = p.conv_w;                   // any valid address for zero-fill
-  for (int i = tid; i < L::XROWS * RC; i += kScanThreads) {
-    const int rr = i / RC, ch = i - rr * RC;
-    const int64_t t = t0 - 3 + rr;
-    int col, cidx;
-    if (ch < QC) { col = ch * CH; cidx = cqk + ch * CH; }
-    else if (ch < 2 * QC) { col = DK + (ch - QC) * CH; cidx = ckk + (ch - QC) * CH; }
-    else { col = 2 * DK + (ch - 2 * QC) * CH; cidx = cvv + (ch - 2 * QC) * CH; }
-    const TIN* row = V.row(t);
-    const bool ok = row != nullptr;
-    cp_async16(xs + rr * L::NC + col, ok ? static_cast<const void*>(row + cidx) : dummy, ok ? 16 : 0);
+template <typename TIN, int MODE, int D>
+__global__ void __launch_bounds__(D) conv_kernel(const ScanParams p) {
+  const int ch = blockIdx.x, s = blockIdx.z, tid = threadIdx.x;
+  TokenView<TIN> V;
+  int64_t start, n_log;
+  int32_t init, final_page;
+  if (!make_view<TIN, MODE>(p, s, V, start, init, final_page, n_log, false)) return;
+  const int64_t t0 = (int64_t)blockIdx.y * kConvTokens;
+  if (t0 >= V.n) return;
+  const int cnt = (int)(V.n - t0 < kConvTokens ? V.n - t0 : kConvTokens);
+  const int c = ch * D + tid;                      // heads are D channels wide
+  const bool qk = ch < 2 * p.Hqk;
+  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)c * kConvK);
+  __shared__ float part[D / 32][kConvTokens];
+  float h0 = V.x(t0 - 3, c), h1 = V.x(t0 - 2, c), h2 = V.x(t0 - 1, c);
+  for (int tt = 0; tt < cnt; ++tt) {
+    const float xv = V.x(t0 + tt, c);
+    float z = w.x * h0;
+    z = fmaf(w.y, h1, z);
+    z = fmaf(w.z, h2, z);
+    z = fmaf(w.w, xv, z);
+    const float y = silu(z);
+    p.ws_y[(V.wrow0 + t0 + tt) * p.conv_dim + c] = y;
+    if (qk) {
+      const float sq = warp_sum(y * y);
+      if ((tid & 31) == 0) part[tid >> 5][tt] = sq;
+    }
+    h0 = h1; h1 = h2; h2 = xv;
   }
-  for (int i = tid; i < 2 * L::TT; i += kScanThreads) {
-    const int which = i / L::TT, tt = i - which * L::TT;
-    const int64_t t = t0 + tt;
-    const bool ok = t < V.n;
-    const float* src = ok ? (which ? V.bptr(t, h) : V.gptr(t, h)) : static_cast<const float*>(dummy);
-    cp_async4(gb + i, src, ok ? 4 : 0);
+  if (qk) {
+    __syncthreads();
+    for (int tt = tid; tt < cnt; tt += D) {
+      float ss = 0.f;
+#pragma unroll
+      for (int wv = 0; wv < D / 32; ++wv) ss += part[wv][tt];
+      const float scale = ch < p.Hqk ? p.q_scale : 1.0f;
+      p.ws_nrm[(V.wrow0 + t0 + tt) * 2 * p.Hqk + ch] = scale / sqrtf(ss + p.eps);
+    }
+  } else {
+    const int h = ch - 2 * p.Hqk;
+    for (int tt = tid; tt < cnt; tt += D) {
+      const int64_t t = t0 + tt;
+      float* ab = p.ws_ab + ((V.wrow0 + t) * p.Hv + h) * 2;
+      ab[0] = expf(V.g(t, h));
+      ab[1] = V.b(t, h);
+    }
   }
 }
 
+// ---------------------------------------------------------------------------
+// The scan.
+constexpr int kScanTile = 16;
+// Lanes that share one state row (each owns DK / kLanesPerRow columns) and the
+// CTA size that gives 32 row groups.
+constexpr int kLanesPerRow = 4;
+constexpr int kScanThreads = 32 * kLanesPerRow;
+
+// Sum over the kLanesPerRow lanes of a row group (fixed xor order; every lane
+// of the group ends with the same bits).
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < kLanesPerRow; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Shared-memory plan of one scan CTA (byte offsets): two tile stages.
+template <int DK, int DV, int RPT>
+struct ScanSmem {
+  static constexpr int TT = kScanTile, ROWS = 32 * RPT;
+  static constexpr size_t q = 0;                                    // f32 [TT][DK] SiLU(conv) q
+  static constexpr size_t k = q + sizeof(float) * TT * DK;          // f32 [TT][DK] SiLU(conv) k
+  static constexpr size_t vo = k + sizeof(float) * TT * DK;         // f32 [TT][ROWS] v in, o out
+  static constexpr size_t sc = vo + sizeof(float) * TT * ROWS;      // float4 [TT]: a, b, fq, fk
+  static constexpr size_t stage = sc + sizeof(float4) * TT;
+  static constexpr size_t bytes = 2 * stage;
+  static_assert(stage % 16 == 0, "stages must stay 16-byte aligned");
+};
+
+template <int DK, int DV, int RPT>
+constexpr size_t scan_smem_bytes() { return ScanSmem<DK, DV, RPT>::bytes; }
+
+// Asynchronous copies of one tile from the workspace into a stage.
+template <int DK, int DV, int RPT, typename TIN>
+__device__ __forceinline__ void stage_tile(const ScanParams& p, const TokenView<TIN>& V, char* st,
+                                           int64_t t0, int cnt, int jq, int h, int row0, int tid) {
+  using L = ScanSmem<DK, DV, RPT>;
+  constexpr int QC = DK / 4, VC = L::ROWS / 4, RC = 2 * QC + VC;  // 16-byte chunks per token
+  float* q_s = reinterpret_cast<float*>(st + L::q);
+  float* k_s = reinterpret_cast<float*>(st + L::k);
+  float* v_s = reinterpret_cast<float*>(st + L::vo);
+  float* sc_s = reinterpret_cast<float*>(st + L::sc);
+  const int cq = jq * DK, ck = p.Hqk * DK + jq * DK, cv = 2 * p.Hqk * DK + h * DV + row0;
+  for (int i = tid; i < cnt * RC; i += kScanThreads) {
+    const int tt = i / RC, c = i - tt * RC;
+    const float* row = p.ws_y + (V.wrow0 + t0 + tt) * p.conv_dim;
+    if (c < QC) cp_async16(q_s + tt * DK + 4 * c, row + cq + 4 * c, 16);
+    else if (c < 2 * QC) cp_async16(k_s + tt * DK + 4 * (c - QC), row + ck + 4 * (c - QC), 16);
+    else cp_async16(v_s + tt * L::ROWS + 4 * (c - 2 * QC), row + cv + 4 * (c - 2 * QC), 16);
+  }
+  for (int i = tid; i < 3 * cnt; i += kScanThreads) {
+    const int tt = i / 3, c = i - tt * 3;
+    const int64_t wr = V.wrow0 + t0 + tt;
+    if (c == 0) cp_async8(sc_s + 4 * tt, p.ws_ab + (wr * p.Hv + h) * 2);
+    else cp_async4(sc_s + 4 * tt + 1 + c, p.ws_nrm + wr * 2 * p.Hqk + (c - 1) * p.Hqk + jq, 4);
+  }
+  cp_async_commit();
+}
+
 template <int DK, int DV, int RPT, typename TIN, typename TOUT, int MODE>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) {
-  using L = ScanSmem<DK, DV, RPT, TIN>;
+__global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanParams p) {
+  using L = ScanSmem<DK, DV, RPT>;
   constexpr int TT = L::TT;
   constexpr int ROWS = L::ROWS;
-  constexpr int NC = L::NC;
-  constexpr int NCH = DK / 16;   // float4 chunks per thread
-  constexpr int NW = (NC + kScanThreads - 1) / kScanThreads;
+  constexpr int LPR = kLanesPerRow;
+  constexpr int NCH = DK / (4 * LPR);   // float4 chunks per thread
+  static_assert(NCH >= 1, "dk too small for the lane layout");
   static_assert(DV % ROWS == 0, "row slices must tile dv");
   static_assert(DK % 32 == 0, "dk must be a multiple of 32");
 
   const int slice = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cq = lane & 3;
-  const int rg = warp * 8 + (lane >> 2);
+  const int cq = lane & (LPR - 1);                   // column group of this lane
+  const int rg = warp * (32 / LPR) + lane / LPR;     // row group 0..31
   const int row0 = slice * ROWS;
   const int grp = p.Hv / p.Hqk, jq = h / grp;
 
@@ -244,201 +320,133 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) 
   const bool report = (slice == 0 && h == 0 && tid == 0);
   if (!make_view<TIN, MODE>(p, s, V, start, init, final_page, n_log, report)) return;
   const int64_t n = V.n;
+  const int64_t ntiles = (n + TT - 1) / TT;
 
   extern __shared__ float4 smem4[];
   char* sm = reinterpret_cast<char*>(smem4);
-  float* q_s = reinterpret_cast<float*>(sm + L::q);
-  float* k_s = reinterpret_cast<float*>(sm + L::k);
-  float* vo_s = reinterpret_cast<float*>(sm + L::vo);
-  float* a_s = reinterpret_cast<float*>(sm + L::ab);
-  float* b_s = a_s + TT;
-  TIN* xs_s = reinterpret_cast<TIN*>(sm + L::xs);
-  float* gb_s = reinterpret_cast<float*>(sm + L::gb);
+  if (ntiles > 0) stage_tile<DK, DV, RPT, TIN>(p, V, sm, 0, (int)(n < TT ? n : TT), jq, h, row0, tid);
 
-  const int cqk = jq * DK;                         // q channels of this qk head
-  const int ckk = p.Hqk * DK + jq * DK;            // k channels
-  const int cvv = 2 * p.Hqk * DK + h * DV + row0;  // v channels of this slice
-
-  const int64_t ntiles = (n + TT - 1) / TT;
-  if (ntiles > 0) {
-    stage_tile<DK, DV, RPT, TIN>(p, V, xs_s, gb_s, 0, cqk, ckk, cvv, h, tid);
-    cp_async_commit();
-  }
-
-  // ---- initial state rows (zeros on a cold start: the pool is not read)
-  float S[RPT][NCH][4];
+  // initial state rows (zeros on a cold start: the pool is not read); each
+  // float4 chunk of a row is held as two packed pairs
+  f32x2 S[RPT][NCH][2];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     const int row = row0 + rg + 32 * i;
 #pragma unroll
     for (int m = 0; m < NCH; ++m) {
-      float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      ulonglong2 v2 = make_ulonglong2(0ull, 0ull);
       if (init >= 0)
-        v4 = *reinterpret_cast<const float4*>(page_state(p.pool, init) +
-                                              ((int64_t)h * DV + row) * DK + 4 * (4 * m + cq));
-      S[i][m][0] = v4.x; S[i][m][1] = v4.y; S[i][m][2] = v4.z; S[i][m][3] = v4.w;
+        v2 = *reinterpret_cast<const ulonglong2*>(page_state(p.pool, init) +
+                                                  ((int64_t)h * DV + row) * DK + 4 * (LPR * m + cq));
+      S[i][m][0] = v2.x;
+      S[i][m][1] = v2.y;
     }
   }
 
-  // conv taps of the channels this thread computes
-  float4 wreg[NW];
-#pragma unroll
-  for (int u = 0; u < NW; ++u) {
-    const int idx = tid + u * kScanThreads;
-    wreg[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (idx < NC) {
-      const int c = idx < DK ? cqk + idx : (idx < 2 * DK ? ckk + idx - DK : cvv + idx - 2 * DK);
-      wreg[u] = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)c * kConvK);
-    }
-  }
-
-  for (int64_t it = 0; it < ntiles; ++it) {
-    const int64_t t0 = it * TT;
+  for (int64_t j = 0; j < ntiles; ++j) {
+    const int64_t t0 = j * TT;
     const int cnt = (int)(n - t0 < TT ? n - t0 : TT);
-    if (it + 1 < ntiles) {
-      stage_tile<DK, DV, RPT, TIN>(p, V, xs_s + ((it + 1) & 1) * L::XROWS * NC,
-                                   gb_s + ((it + 1) & 1) * 2 * TT, t0 + TT, cqk, ckk, cvv, h, tid);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    cp_async_wait<0>();
+    __syncthreads();   // stage j is visible and every thread is done with tile j-1
+    if (j + 1 < ntiles) {
+      const int64_t t1 = t0 + TT;
+      stage_tile<DK, DV, RPT, TIN>(p, V, sm + ((j + 1) & 1) * L::stage, t1,
+                                   (int)(n - t1 < TT ? n - t1 : TT), jq, h, row0, tid);
     }
-    __syncthreads();  // this tile's rows are in shared memory; last tile's readers are done
+    const char* st = sm + (j & 1) * L::stage;
+    const float* q_s = reinterpret_cast<const float*>(st + L::q);
+    const float* k_s = reinterpret_cast<const float*>(st + L::k);
+    float* vo_s = reinterpret_cast<float*>(const_cast<char*>(st) + L::vo);
+    const float4* sc_s = reinterpret_cast<const float4*>(st + L::sc);
 
-    // ---- conv + SiLU for the tile's tokens on this CTA's channels
-    const TIN* xb = xs_s + (it & 1) * L::XROWS * NC;
-#pragma unroll
-    for (int uu = 0; uu < NW; ++uu) {
-      const int idx = tid + uu * kScanThreads;
-      if (idx < NC) {
-        const float4 w = wreg[uu];
-        float* dst;
-        int ld;
-        if (idx < DK) { dst = q_s + idx; ld = DK; }
-        else if (idx < 2 * DK) { dst = k_s + idx - DK; ld = DK; }
-        else { dst = vo_s + idx - 2 * DK; ld = ROWS; }
-        float h0 = to_f32(xb[idx]), h1 = to_f32(xb[NC + idx]), h2 = to_f32(xb[2 * NC + idx]);
-        for (int tt = 0; tt < cnt; ++tt) {
-          const float xv = to_f32(xb[(tt + 3) * NC + idx]);
-          float z = w.x * h0;
-          z = fmaf(w.y, h1, z);
-          z = fmaf(w.z, h2, z);
-          z = fmaf(w.w, xv, z);
-          dst[tt * ld] = silu_fast(z);
-          h0 = h1; h1 = h2; h2 = xv;
-        }
-      }
-    }
-    if (tid < cnt) {
-      const float* gbb = gb_s + (it & 1) * 2 * TT;
-      a_s[tid] = expf(gbb[tid]);
-      b_s[tid] = gbb[TT + tid];
-    }
-    __syncthreads();
-
-    // ---- L2 norms of q and k, one warp per token, fixed reduction order
-    for (int tt = warp; tt < cnt; tt += kScanThreads / 32) {
-      float sq = 0.f, sk = 0.f;
-#pragma unroll
-      for (int jj = 0; jj < DK / 32; ++jj) {
-        const float qv = q_s[tt * DK + lane + 32 * jj];
-        const float kv = k_s[tt * DK + lane + 32 * jj];
-        sq = fmaf(qv, qv, sq);
-        sk = fmaf(kv, kv, sk);
-      }
-      sq = warp_sum(sq);
-      sk = warp_sum(sk);
-      const float fq = p.q_scale / sqrtf(sq + p.eps);
-      const float fk = 1.0f / sqrtf(sk + p.eps);
-#pragma unroll
-      for (int jj = 0; jj < DK / 32; ++jj) {
-        q_s[tt * DK + lane + 32 * jj] *= fq;
-        k_s[tt * DK + lane + 32 * jj] *= fk;
-      }
-    }
-    __syncthreads();
-
-    // ---- tile prologue: u = R k_0 with R = S (A = 1)
-    float uh[RPT];
+    // tile prologue: h = R k_0 (k before its norm factor) with R = S, A = 1
+    float hk[RPT];
+    ulonglong2 kc[NCH];
     {
-      float acc0[RPT], acc1[RPT];
+      f32x2 acc[RPT];
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) { acc0[i] = 0.f; acc1[i] = 0.f; }
+      for (int i = 0; i < RPT; ++i) acc[i] = 0ull;
 #pragma unroll
       for (int m = 0; m < NCH; ++m) {
-        const float4 k4 = *reinterpret_cast<const float4*>(k_s + 4 * (4 * m + cq));
+        const ulonglong2 k2 = *reinterpret_cast<const ulonglong2*>(k_s + 4 * (LPR * m + cq));
+        kc[m] = k2;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
-          float& acc = (m & 1) ? acc1[i] : acc0[i];
-          acc = fmaf(S[i][m][0], k4.x, acc);
-          acc = fmaf(S[i][m][1], k4.y, acc);
-          acc = fmaf(S[i][m][2], k4.z, acc);
-          acc = fmaf(S[i][m][3], k4.w, acc);
+          acc[i] = fma2(S[i][m][0], k2.x, acc[i]);
+          acc[i] = fma2(S[i][m][1], k2.y, acc[i]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) uh[i] = quad_sum(acc0[i] + acc1[i]);
+      for (int i = 0; i < RPT; ++i) hk[i] = row_sum(sum2(acc[i]));
     }
     float A = 1.0f;
 
-    // ---- scan the tile
     for (int tt = 0; tt < cnt; ++tt) {
-      const float a = a_s[tt], b = b_s[tt];
+      const float4 scl = sc_s[tt];                      // a, b, fq, fk of token tt
+      const float a = scl.x, b = scl.y, fq = scl.z, fk = scl.w;
       const float An = A * a;
-      const bool direct = An < 0x1p-64f;  // uniform across the CTA
+      const bool direct = An < 0x1p-64f;                // uniform across the CTA
       const float inv = direct ? 1.0f : 1.0f / An;
       const bool nxt = tt + 1 < cnt;
-      float d[RPT], o0[RPT], o1[RPT], un0[RPT], un1[RPT];
+      f32x2 d2[RPT], o2[RPT][2], u2[RPT][2];
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
-        const float coef = b * fmaf(-a, A * uh[i], vo_s[tt * ROWS + rg + 32 * i]);
-        d[i] = coef * inv;
-        o0[i] = 0.f; o1[i] = 0.f; un0[i] = 0.f; un1[i] = 0.f;
+        const float u = (A * fk) * hk[i];               // u_t = S_{t-1} k_t (normalised k)
+        const float coef = b * fmaf(-a, u, vo_s[tt * ROWS + rg + 32 * i]);
+        const float d = (coef * fk) * inv;
+        d2[i] = pack2(d, d);
+        o2[i][0] = o2[i][1] = 0ull;
+        u2[i][0] = u2[i][1] = 0ull;
       }
       // The decay branch is uniform across the CTA; each variant is one loop.
-#define GDN_SCAN_TOKEN(UPDATE)                                                                 \
-  _Pragma("unroll") for (int m = 0; m < NCH; ++m) {                                           \
-    const float4 k4 = *reinterpret_cast<const float4*>(k_s + tt * DK + 4 * (4 * m + cq));     \
-    const float4 q4 = *reinterpret_cast<const float4*>(q_s + tt * DK + 4 * (4 * m + cq));     \
-    float4 n4 = make_float4(0.f, 0.f, 0.f, 0.f);                                              \
-    if (nxt) n4 = *reinterpret_cast<const float4*>(k_s + (tt + 1) * DK + 4 * (4 * m + cq));   \
-    const float kv[4] = {k4.x, k4.y, k4.z, k4.w};                                             \
-    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};                                             \
-    const float kn[4] = {n4.x, n4.y, n4.z, n4.w};                                             \
-    _Pragma("unroll") for (int i = 0; i < RPT; ++i) {                                         \
-      float& oa = (m & 1) ? o1[i] : o0[i];                                                    \
-      float& ua = (m & 1) ? un1[i] : un0[i];                                                  \
-      _Pragma("unroll") for (int e = 0; e < 4; ++e) {                                         \
-        const float sn = UPDATE;                                                              \
-        S[i][m][e] = sn;                                                                      \
-        oa = fmaf(sn, qv[e], oa);                                                             \
-        ua = fmaf(sn, kn[e], ua);                                                             \
-      }                                                                                       \
-    }                                                                                         \
+      // kc holds k_t (loaded as the previous token's k_{t+1}).
+#define GDN_SCAN_TOKEN(UPDATE)                                                                     \
+  _Pragma("unroll") for (int m = 0; m < NCH; ++m) {                                               \
+    const ulonglong2 q2 = *reinterpret_cast<const ulonglong2*>(q_s + tt * DK + 4 * (LPR * m + cq)); \
+    ulonglong2 n2 = make_ulonglong2(0ull, 0ull);                                                  \
+    if (nxt) n2 = *reinterpret_cast<const ulonglong2*>(k_s + (tt + 1) * DK + 4 * (LPR * m + cq)); \
+    _Pragma("unroll") for (int i = 0; i < RPT; ++i) {                                             \
+      S[i][m][0] = UPDATE(S[i][m][0], kc[m].x);                                                   \
+      S[i][m][1] = UPDATE(S[i][m][1], kc[m].y);                                                   \
+      o2[i][m & 1] = fma2(S[i][m][0], q2.x, o2[i][m & 1]);                                        \
+      u2[i][m & 1] = fma2(S[i][m][0], n2.x, u2[i][m & 1]);                                        \
+      o2[i][m & 1] = fma2(S[i][m][1], q2.y, o2[i][m & 1]);                                        \
+      u2[i][m & 1] = fma2(S[i][m][1], n2.y, u2[i][m & 1]);                                        \
+    }                                                                                             \
+    kc[m] = n2;                                                                                   \
   }
       if (!direct) {
-        GDN_SCAN_TOKEN(fmaf(d[i], kv[e], S[i][m][e]))
+#define GDN_UPD(SV, KV) fma2(d2[i], KV, SV)
+        GDN_SCAN_TOKEN(GDN_UPD)
+#undef GDN_UPD
       } else {
-        GDN_SCAN_TOKEN(fmaf(d[i], kv[e], An * S[i][m][e]))
+        const f32x2 an2 = pack2(An, An);
+#define GDN_UPD(SV, KV) fma2(d2[i], KV, mul2(an2, SV))
+        GDN_SCAN_TOKEN(GDN_UPD)
+#undef GDN_UPD
       }
 #undef GDN_SCAN_TOKEN
       A = direct ? 1.0f : An;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
-        const float o = A * quad_sum(o0[i] + o1[i]);
-        uh[i] = quad_sum(un0[i] + un1[i]);
+        const float o = (A * fq) * row_sum(sum2(o2[i][0]) + sum2(o2[i][1]));
+        hk[i] = row_sum(sum2(u2[i][0]) + sum2(u2[i][1]));
         // every lane of the quad has read v (the shuffles above synchronise it)
         if (cq == 0) vo_s[tt * ROWS + rg + 32 * i] = o;
       }
     }
 
-    // ---- tile end: back to the plain state (exact when A == 1)
+    // tile end: back to the plain state (exact when A == 1)
+    {
+      const f32x2 a2 = pack2(A, A);
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
+      for (int i = 0; i < RPT; ++i)
 #pragma unroll
-      for (int m = 0; m < NCH; ++m)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S[i][m][e] *= A;
+        for (int m = 0; m < NCH; ++m) {
+          S[i][m][0] = mul2(a2, S[i][m][0]);
+          S[i][m][1] = mul2(a2, S[i][m][1]);
+        }
+    }
 
     if (MODE == kPrefill) {
       const int64_t pos = start + t0 + cnt;   // a multiple of B only at a full tile's end
@@ -455,8 +463,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) 
               const int row = row0 + rg + 32 * i;
 #pragma unroll
               for (int m = 0; m < NCH; ++m)
-                *reinterpret_cast<float4*>(dstS + ((int64_t)h * DV + row) * DK + 4 * (4 * m + cq)) =
-                    make_float4(S[i][m][0], S[i][m][1], S[i][m][2], S[i][m][3]);
+                *reinterpret_cast<ulonglong2*>(dstS + ((int64_t)h * DV + row) * DK + 4 * (LPR * m + cq)) =
+                    make_ulonglong2(S[i][m][0], S[i][m][1]);
             }
           } else if (report) {
             set_error(p.err, GDN_ERR_PAGE_RANGE);
@@ -464,10 +472,10 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) 
         }
       }
     }
-    __syncthreads();
 
-    // ---- outputs of the tile, coalesced along dv
+    // outputs of the tile, coalesced along dv
     if (MODE != kFlush) {
+      __syncthreads();
       TOUT* out = reinterpret_cast<TOUT*>(p.o);
       for (int idx = tid; idx < cnt * ROWS; idx += kScanThreads) {
         const int tt = idx / ROWS, r = idx % ROWS;
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) 
     }
   }
 
-  // ---- final state
+  // final state
   if (final_page >= 0) {
     float* dstS = page_state(p.pool, final_page);
 #pragma unroll
@@ -491,8 +499,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanParams p) 
       const int row = row0 + rg + 32 * i;
 #pragma unroll
       for (int m = 0; m < NCH; ++m)
-        *reinterpret_cast<float4*>(dstS + ((int64_t)h * DV + row) * DK + 4 * (4 * m + cq)) =
-            make_float4(S[i][m][0], S[i][m][1], S[i][m][2], S[i][m][3]);
+        *reinterpret_cast<ulonglong2*>(dstS + ((int64_t)h * DV + row) * DK + 4 * (LPR * m + cq)) =
+            make_ulonglong2(S[i][m][0], S[i][m][1]);
     }
   }
 }

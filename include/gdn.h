@@ -213,6 +213,8 @@ typedef struct gdn_prefill_args {
   int32_t num_seqs;              /* N >= 0                                    */
   int32_t max_blocks;            /* row stride of block_table                 */
   int64_t total_tokens;          /* T = cu_seqlens[N]                         */
+  int64_t max_seq_len;           /* host bound on any cu_seqlens[s+1] -
+                                    cu_seqlens[s] (0: T); sizes the grid      */
   const int32_t* cu_seqlens;     /* [N+1], non-decreasing, cu_seqlens[0] = 0  */
   const int64_t* start_pos;      /* [N] absolute position of the first token  */
   const int64_t* start_pos_host; /* optional host copy of start_pos ([N]) for
@@ -229,7 +231,12 @@ typedef struct gdn_prefill_args {
   int32_t* dev_error;            /* one int32, set to a gdn_status on a fault */
 } gdn_prefill_args;
 
-/* Workspace bytes gdn_prefill_chunked needs for these sizes (0: none). */
+/* Device workspace bytes gdn_prefill_chunked needs for a call with
+ * total_tokens tokens: the SiLU(conv) rows of every token in fp32 (computed
+ * once and shared by every head that reads them), the q / k norm factors and
+ * the gates.  The caller allocates it (256-byte aligned); its contents are
+ * scratch, overwritten by every call, so calls that share a workspace must
+ * not overlap on the GPU.  0 for a malformed desc. */
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens);
 
@@ -301,7 +308,13 @@ typedef struct gdn_replay_args {
   const float* conv_w;           /* [conv_dim][4]                             */
   void* o;                       /* [N][m][Hv][dv] out_dtype (append)         */
   int32_t* dev_error;
+  void* workspace;               /* device scratch, >= gdn_replay_workspace_size */
+  size_t workspace_bytes;
 } gdn_replay_args;
+
+/* Device workspace bytes of gdn_replay_append / gdn_replay_flush for
+ * num_reqs requests (32 log rows each); same contract as the prefill's. */
+size_t gdn_replay_workspace_size(const gdn_layer_desc* desc, int32_t num_reqs);
 
 gdn_status gdn_replay_append(const gdn_layer_desc* desc, const gdn_pool* pool,
                              const gdn_replay_args* args, void* stream);

@@ -45,9 +45,9 @@ def _prefill(shape, pool_pages=8, start_host=None, init_host=None, block_table=T
     pool = gdn._Pool(0x100000, shape.page, pool_pages, 0)
     sph, k1 = gdn._host(start_host, torch.int64, "")
     iph, k2 = gdn._host(init_host, torch.int32, "")
-    a = gdn._PrefillArgs(len(start_host or [0]), 4, 64, 0x10000, 0x10000, sph, iph, 0x10000, 0x10000,
+    a = gdn._PrefillArgs(len(start_host or [0]), 4, 64, 0, 0x10000, 0x10000, sph, iph, 0x10000, 0x10000,
                          0x10000, 0x10000, 0x10000, 0x10000 if block_table else None, 0x10000, 0x10000, 0x10000)
-    return lib.gdn_prefill_chunked(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None, 0, None)
+    return lib.gdn_prefill_chunked(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), 0x10000, 1 << 40, None)
 
 
 def test_prefill_fails_closed_on_off_boundary_resume():
@@ -81,6 +81,22 @@ def test_pool_too_small_or_misaligned_is_rejected():
     assert lib.gdn_decode_step(ctypes.byref(desc), ctypes.byref(odd), ctypes.byref(a), None) == 1
 
 
+def test_workspace_is_required_and_sized():
+    sh = inputs.QWEN27B
+    need = gdn.gdn_prefill_workspace_size(sh, 4, 4 * 8192)
+    # SiLU(conv) rows in fp32 plus norm factors and gates
+    assert need >= 4 * 8192 * (sh.conv_dim + 2 * sh.num_qk_heads + 2 * sh.num_v_heads) * 4
+    assert need % 256 == 0
+    assert gdn.gdn_replay_workspace_size(inputs.QWEN4B, 16) >= 16 * 32 * inputs.QWEN4B.conv_dim * 4
+    lib = gdn.load_library()
+    desc = gdn.make_desc(inputs.TINY)
+    pool = gdn._Pool(0x100000, inputs.TINY.page, 8, 0)
+    # host-side arrays stay NULL: only device pointers are faked here
+    a = gdn._PrefillArgs(1, 4, 64, 0, 0x10000, 0x10000, None, None, *([0x10000] * 9))
+    st = lib.gdn_prefill_chunked(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), 0x10000, 16, None)
+    assert st == gdn.STATUS_CODE["GDN_ERR_WORKSPACE"]
+
+
 def test_checkpoint_copy_fails_closed_off_boundary():
     lib = gdn.load_library()
     sh = inputs.TINY
@@ -97,7 +113,7 @@ def test_replay_rejects_oversized_append_and_bad_rollback_args():
     sh = inputs.TINY
     desc = gdn.make_desc(sh)
     pool = gdn._Pool(0x100000, sh.page, 8, 0)
-    a = gdn._ReplayArgs(2, 33, *([0x10000] * 11))
+    a = gdn._ReplayArgs(2, 33, *([0x10000] * 11), 0x10000, 1 << 40)
     assert lib.gdn_replay_append(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None) == \
         gdn.STATUS_CODE["GDN_ERR_LOG_OVERFLOW"]
     assert lib.gdn_replay_rollback(0x10000, 0x10000, 40, 2, 0x10000, None) == gdn.STATUS_CODE["GDN_ERR_INVALID_ARG"]
@@ -110,6 +126,6 @@ def test_empty_batches_are_no_ops():
     pool = gdn._Pool(0x100000, sh.page, 8, 0)
     a = gdn._DecodeArgs(0, 0, *([None] * 7))
     assert lib.gdn_decode_step(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None) == 0
-    r = gdn._ReplayArgs(0, 0, *([None] * 11))
+    r = gdn._ReplayArgs(0, 0, *([None] * 11), None, 0)
     assert lib.gdn_replay_flush(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(r), None) == 0
     assert lib.gdn_replay_rollback(None, None, 4, 0, None, None) == 0
