@@ -43,6 +43,11 @@ METRIC = "GDN prefill tokens/s/layer; decode & replay-flush µs/layer; % of TC/H
 PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
+# DRAM bytes (read + write) of one prefill scan launch, from an ncu capture of
+# the current scan kernel at 4 x 2,048 tokens (profiles/
+# scan_kernel_prefill_27b_4x2048.md: 342.0 + 109.5 MB), scaled by 4 to the
+# 4 x 8,192 launch (the traffic is per token).  None once the kernel changes.
+SCAN_TRAFFIC_PER_LAUNCH = (342.006528e6 + 109.522176e6) * 4
 DEC_SEQS, DEC_LAYERS = 256, 24
 REP_REQS, REP_ROWS, REP_LAYERS = 16, 16, 24
 
@@ -187,13 +192,14 @@ class PrefillWork:
 class DecodeWork:
     """256 sequences x 24 layers of the 4B-shaped layer, one token each."""
 
-    def __init__(self, seed: int):
+    def __init__(self, seed: int, layers: int = DEC_LAYERS):
         sh = SMALL
         self.sh = sh
+        self.nlayers = layers
         gen = torch.Generator(device="cuda")
         gen.manual_seed(seed)
         self.pools, self.slots, self.x, self.g, self.beta = [], [], [], [], []
-        for layer in range(DEC_LAYERS):
+        for layer in range(layers):
             pool = gdn.StatePool(sh, DEC_SEQS, fill=0)
             for p in range(0, DEC_SEQS, 64):
                 n = min(64, DEC_SEQS - p)
@@ -211,7 +217,7 @@ class DecodeWork:
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def run(self):
-        for L in range(DEC_LAYERS):
+        for L in range(self.nlayers):
             gdn.gdn_decode_step(self.sh, self.pools[L], x=self.x[L], g=self.g[L], beta=self.beta[L],
                                 conv_w=self.w, slot=self.slots[L], o=self.o, dev_error=self.err)
 
@@ -225,14 +231,15 @@ class DecodeWork:
 class ReplayWork:
     """16 requests x 16 rows per layer, 24 layers: append, rollback, flush."""
 
-    def __init__(self, seed: int):
+    def __init__(self, seed: int, layers: int = REP_LAYERS):
         sh = SMALL
         self.sh = sh
+        self.nlayers = layers
         L = gdn.REPLAY_LOG_SLOTS
         gen = torch.Generator(device="cuda")
         gen.manual_seed(seed)
         self.layers = []
-        for layer in range(REP_LAYERS):
+        for layer in range(layers):
             pool = gdn.StatePool(sh, REP_REQS, fill=0)
             st = pool.buf.view(REP_REQS, sh.page)[:, :sh.state_bytes].view(torch.float32)
             st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
@@ -253,7 +260,7 @@ class ReplayWork:
         self.o = torch.empty(REP_REQS, REP_ROWS, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16,
                              device="cuda")
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        self.kept_rows = float(sum(int(l["acc"].sum()) for l in self.layers)) / REP_LAYERS
+        self.kept_rows = float(sum(int(l["acc"].sum()) for l in self.layers)) / layers
         self.ws = gdn.workspace_for(gdn.gdn_replay_workspace_size(sh, REP_REQS))
 
     def _kw(self, l):
@@ -352,10 +359,10 @@ def run_part(args):
         w = PrefillWork(args.seed, args.seq_len)
         fn, unit_ms = w.run, None
     elif args.only == "decode":
-        w = DecodeWork(args.seed)
+        w = DecodeWork(args.seed, args.layers)
         fn = w.run
     else:
-        w = ReplayWork(args.seed)
+        w = ReplayWork(args.seed, args.layers)
         fn = lambda: (w.verify(), w.flush())
     for _ in range(args.warmup):
         fn()
@@ -386,6 +393,8 @@ def main():
                     help="time one part only (profiling); the default times the whole step")
     ap.add_argument("--seq-len", type=int, default=SEQ_LEN,
                     help="prefill tokens per sequence (profiling of smaller cases)")
+    ap.add_argument("--layers", type=int, default=DEC_LAYERS,
+                    help="decode / replay layers with --only (profiling of smaller cases)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -510,7 +519,9 @@ def main():
         "decode_hbm_gbs": dec_gbs, "flush_hbm_gbs": fl_gbs,
         "decode_hbm_frac": dec_gbs / peaks["hbm_gbs"], "flush_hbm_frac": fl_gbs / peaks["hbm_gbs"],
         "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak, "traffic": None,
+                     "frac": achieved / alu_peak,
+                     "traffic": SCAN_TRAFFIC_PER_LAUNCH if args.seq_len == SEQ_LEN else None,
+                     "traffic_note": "bytes per launch, scaled from a 4 x 2048 capture",
                      "kernel": "scan_kernel<128,128,2,bf16,bf16,prefill>",
                      "peak_kind": f"fp32 FMA 152 SMs x 128 lanes x 2 x {sm_max:.0f} MHz",
                      "hbm_peak_kind": peak_kind},

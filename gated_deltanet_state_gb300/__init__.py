@@ -294,17 +294,9 @@ def workspace_for(nbytes: int, device="cuda") -> torch.Tensor:
 
 # --------------------------------------------------------------------------- device entry points
 
-def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
-                        block_table, out_slot, x, g, beta, conv_w, o, dev_error,
-                        start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
-                        stream=None, raise_on_error: bool = True) -> int:
-    """Chunked prefill with block checkpoints (see gdn.h for the contract).
-    Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
-    taken from PyTorch's allocator for the call."""
-    lib = load_library()
+def _prefill_args(shape, *, cu_seqlens, start_pos, init_page, block_table, out_slot, x, g, beta, conv_w,
+                  o, dev_error, start_pos_host, init_page_host, max_seq_len):
     n = int(cu_seqlens.numel()) - 1
-    if workspace is None:
-        workspace = workspace_for(gdn_prefill_workspace_size(shape, n, int(x.shape[0])), x.device)
     sph, keep1 = _host(start_pos_host, torch.int64, "start_pos_host")
     iph, keep2 = _host(init_page_host, torch.int32, "init_page_host")
     bt = block_table
@@ -317,8 +309,26 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
                      _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
                      _dev(out_slot, torch.int32, "out_slot"), _dev(o, shape.torch_out(), "o"),
                      _dev(dev_error, torch.int32, "dev_error"))
-    ws = _dev(workspace, None, "workspace") if workspace is not None else None
-    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return a, (keep1, keep2)
+
+
+def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
+                        block_table, out_slot, x, g, beta, conv_w, o, dev_error,
+                        start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
+                        stream=None, raise_on_error: bool = True) -> int:
+    """Chunked prefill with block checkpoints (see gdn.h for the contract).
+    Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
+    taken from PyTorch's allocator for the call."""
+    lib = load_library()
+    n = int(cu_seqlens.numel()) - 1
+    if workspace is None:
+        workspace = workspace_for(gdn_prefill_workspace_size(shape, n, int(x.shape[0])), x.device)
+    a, keep = _prefill_args(shape, cu_seqlens=cu_seqlens, start_pos=start_pos, init_page=init_page,
+                            block_table=block_table, out_slot=out_slot, x=x, g=g, beta=beta, conv_w=conv_w,
+                            o=o, dev_error=dev_error, start_pos_host=start_pos_host,
+                            init_page_host=init_page_host, max_seq_len=max_seq_len)
+    ws = _dev(workspace, None, "workspace")
+    wsb = workspace.numel() * workspace.element_size()
     st = lib.gdn_prefill_chunked(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
                                  ctypes.byref(a), ws, wsb, _stream(stream))
     return _check(st, "gdn_prefill_chunked") if raise_on_error else st

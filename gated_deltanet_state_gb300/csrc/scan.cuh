@@ -183,14 +183,30 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
 // ---------------------------------------------------------------------------
 // Conv pre-pass: SiLU(depthwise causal conv) of every channel of every token,
 // once, into the workspace, with the L2-norm factors of each q and k head and
-// the gates of each value head.  One CTA covers one head's D channels for
-// kConvTokens tokens of one sequence; it is bound by HBM (reads x once, writes
-// fp32 rows), so it uses the accurate expf / division.
-constexpr int kConvTokens = 64;
+// the gates of each value head.  It is bound by HBM (reads x once, writes fp32
+// rows), so each thread owns VEC consecutive channels and moves 16 bytes per
+// load; a head's D channels are D / VEC adjacent lanes, which reduce the
+// squared norm with shuffles.  SiLU uses the fast exponential and division
+// (a few ulp); the gates keep the accurate expf.
+constexpr int kConvTokens = 32;
+constexpr int kConvThreads = 128;
+
+template <typename TIN>
+struct Vec16 {                      // 16 bytes of TIN
+  static constexpr int N = 16 / sizeof(TIN);
+  TIN v[N];
+};
+template <typename TIN>
+__device__ __forceinline__ void load16(Vec16<TIN>& d, const TIN* src) {
+  *reinterpret_cast<uint4*>(d.v) = *reinterpret_cast<const uint4*>(src);
+}
 
 template <typename TIN, int MODE, int D>
-__global__ void __launch_bounds__(D) conv_kernel(const ScanParams p) {
-  const int ch = blockIdx.x, s = blockIdx.z, tid = threadIdx.x;
+__global__ void __launch_bounds__(kConvThreads) conv_kernel(const ScanParams p) {
+  constexpr int VEC = Vec16<TIN>::N;          // channels per thread
+  constexpr int TPH = D / VEC;                // lanes per head
+  static_assert(TPH >= 1 && TPH <= 32 && (TPH & (TPH - 1)) == 0, "head must map to a lane group");
+  const int s = blockIdx.z, tid = threadIdx.x;
   TokenView<TIN> V;
   int64_t start, n_log;
   int32_t init, final_page;
@@ -198,42 +214,80 @@ __global__ void __launch_bounds__(D) conv_kernel(const ScanParams p) {
   const int64_t t0 = (int64_t)blockIdx.y * kConvTokens;
   if (t0 >= V.n) return;
   const int cnt = (int)(V.n - t0 < kConvTokens ? V.n - t0 : kConvTokens);
-  const int c = ch * D + tid;                      // heads are D channels wide
-  const bool qk = ch < 2 * p.Hqk;
-  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)c * kConvK);
-  __shared__ float part[D / 32][kConvTokens];
-  float h0 = V.x(t0 - 3, c), h1 = V.x(t0 - 2, c), h2 = V.x(t0 - 1, c);
-  for (int tt = 0; tt < cnt; ++tt) {
-    const float xv = V.x(t0 + tt, c);
-    float z = w.x * h0;
-    z = fmaf(w.y, h1, z);
-    z = fmaf(w.z, h2, z);
-    z = fmaf(w.w, xv, z);
-    const float y = silu(z);
-    p.ws_y[(V.wrow0 + t0 + tt) * p.conv_dim + c] = y;
-    if (qk) {
-      const float sq = warp_sum(y * y);
-      if ((tid & 31) == 0) part[tid >> 5][tt] = sq;
-    }
-    h0 = h1; h1 = h2; h2 = xv;
-  }
-  if (qk) {
-    __syncthreads();
-    for (int tt = tid; tt < cnt; tt += D) {
-      float ss = 0.f;
+  const int c0 = (blockIdx.x * kConvThreads + tid) * VEC;   // first channel of this thread
+  const bool valid = c0 < p.conv_dim;
+  const int head = valid ? c0 / D : 0;        // channel head: q heads, k heads, v heads
+  const bool qk = head < 2 * p.Hqk;
+  const bool leader = (tid & (TPH - 1)) == 0;
+
+  float w[VEC][4];
 #pragma unroll
-      for (int wv = 0; wv < D / 32; ++wv) ss += part[wv][tt];
-      const float scale = ch < p.Hqk ? p.q_scale : 1.0f;
-      p.ws_nrm[(V.wrow0 + t0 + tt) * 2 * p.Hqk + ch] = scale / sqrtf(ss + p.eps);
+  for (int e = 0; e < VEC; ++e) {
+    const float4 w4 = valid ? *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(c0 + e) * kConvK)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    w[e][0] = w4.x; w[e][1] = w4.y; w[e][2] = w4.z; w[e][3] = w4.w;
+  }
+  // history rows t0-3 .. t0-1
+  float hist[3][VEC];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const TIN* row = V.row(t0 - 3 + r);
+    Vec16<TIN> x;
+    if (valid && row) load16(x, row + c0);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) hist[r][e] = (valid && row) ? to_f32(x.v[e]) : 0.f;
+  }
+  // rows are loaded GRP at a time, the next group in flight while this one computes
+  constexpr int GRP = 4;
+  Vec16<TIN> xr[GRP], xn[GRP];
+#pragma unroll
+  for (int u = 0; u < GRP; ++u)
+    if (valid && u < cnt) load16(xr[u], V.row(t0 + u) + c0);
+  for (int g0 = 0; g0 < cnt; g0 += GRP) {
+#pragma unroll
+    for (int u = 0; u < GRP; ++u)
+      if (valid && g0 + GRP + u < cnt) load16(xn[u], V.row(t0 + g0 + GRP + u) + c0);
+#pragma unroll
+    for (int u = 0; u < GRP; ++u) {
+      const int tt = g0 + u;
+      if (tt < cnt) {                         // uniform across the CTA
+        float y[VEC];
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float xv = to_f32(xr[u].v[e]);
+          float z = w[e][0] * hist[0][e];
+          z = fmaf(w[e][1], hist[1][e], z);
+          z = fmaf(w[e][2], hist[2][e], z);
+          z = fmaf(w[e][3], xv, z);
+          y[e] = silu_fast(z);
+          ss = fmaf(y[e], y[e], ss);
+          hist[0][e] = hist[1][e]; hist[1][e] = hist[2][e]; hist[2][e] = xv;
+        }
+        const int64_t wr = V.wrow0 + t0 + tt;
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_y + wr * p.conv_dim + c0);
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4) dst[e / 4] = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+        }
+        // squared norm of the head: sum over its TPH lanes (fixed xor order)
+#pragma unroll
+        for (int o = 1; o < TPH; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (valid && leader) {
+          if (qk) {
+            const float scale = head < p.Hqk ? p.q_scale : 1.0f;
+            p.ws_nrm[wr * 2 * p.Hqk + head] = scale / sqrtf(ss + p.eps);
+          } else {
+            const int h = head - 2 * p.Hqk;
+            float* ab = p.ws_ab + (wr * p.Hv + h) * 2;
+            ab[0] = expf(V.g(t0 + tt, h));
+            ab[1] = V.b(t0 + tt, h);
+          }
+        }
+      }
     }
-  } else {
-    const int h = ch - 2 * p.Hqk;
-    for (int tt = tid; tt < cnt; tt += D) {
-      const int64_t t = t0 + tt;
-      float* ab = p.ws_ab + ((V.wrow0 + t) * p.Hv + h) * 2;
-      ab[0] = expf(V.g(t, h));
-      ab[1] = V.b(t, h);
-    }
+#pragma unroll
+    for (int u = 0; u < GRP; ++u) xr[u] = xn[u];
   }
 }
 

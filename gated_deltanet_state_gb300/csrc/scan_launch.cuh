@@ -30,10 +30,12 @@ inline void ws_bind(ScanParams& p, void* ws, int64_t rows) {
 
 template <int DK, int DV, int RPT, typename TIN, typename TOUT, int MODE>
 cudaError_t launch_scan_t(const ScanParams& p, int64_t max_len, cudaStream_t st) {
-  // 1. conv pre-pass: one CTA per (head of channels, 64-token tile, sequence)
+  // 1. conv pre-pass: one CTA per (block of channels, 64-token tile, sequence)
   if (max_len > 0) {
-    const dim3 cgrid(2 * p.Hqk + p.Hv, (unsigned)((max_len + kConvTokens - 1) / kConvTokens), p.num_seqs);
-    conv_kernel<TIN, MODE, DK><<<cgrid, DK, 0, st>>>(p);
+    constexpr int per_cta = kConvThreads * Vec16<TIN>::N;
+    const dim3 cgrid((p.conv_dim + per_cta - 1) / per_cta,
+                     (unsigned)((max_len + kConvTokens - 1) / kConvTokens), p.num_seqs);
+    conv_kernel<TIN, MODE, DK><<<cgrid, kConvThreads, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
