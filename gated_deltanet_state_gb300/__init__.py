@@ -28,12 +28,13 @@ __all__ = [
     "gdn_block_size_for", "gdn_mamba_pages_per_request", "gdn_pool_blocks_for_pages",
     "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_spec_copy_bytes",
     "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
-    "gdn_prefill_chunked", "workspace_for",
+    "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "workspace_for", "NOALLOC_SCRATCH_BYTES",
     "gdn_decode_step", "gdn_checkpoint_resume", "gdn_checkpoint_save", "gdn_replay_append",
     "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "STATUS",
 ]
 
 REPLAY_LOG_SLOTS = 32
+NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
     3: "GDN_ERR_NOT_BLOCK_ALIGNED", 4: "GDN_ERR_PARTIAL_BLOCK", 5: "GDN_ERR_LOG_OVERFLOW",
@@ -132,6 +133,7 @@ def load_library(build_if_missing: bool = True):
         "gdn_prefill_workspace_size": ([D, i32, i64], sz),
         "gdn_replay_workspace_size": ([D, i32], sz),
         "gdn_prefill_chunked": ([D, PL, ctypes.POINTER(_PrefillArgs), _P, sz, _P], i32),
+        "gdn_prefill_chunked_noalloc": ([D, PL, ctypes.POINTER(_PrefillArgs), _P], i32),
         "gdn_decode_step": ([D, PL, ctypes.POINTER(_DecodeArgs), _P], i32),
         "gdn_checkpoint_resume": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
         "gdn_checkpoint_save": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
@@ -332,6 +334,22 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
     st = lib.gdn_prefill_chunked(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
                                  ctypes.byref(a), ws, wsb, _stream(stream))
     return _check(st, "gdn_prefill_chunked") if raise_on_error else st
+
+
+def gdn_prefill_chunked_noalloc(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
+                                block_table, out_slot, x, g, beta, conv_w, o, dev_error,
+                                start_pos_host=None, init_page_host=None, max_seq_len: int = 0,
+                                stream=None, raise_on_error: bool = True) -> int:
+    """The prefill with the library's fixed device scratch instead of a
+    workspace (gdn.h: gdn_prefill_chunked_noalloc); nothing is allocated."""
+    lib = load_library()
+    a, keep = _prefill_args(shape, cu_seqlens=cu_seqlens, start_pos=start_pos, init_page=init_page,
+                            block_table=block_table, out_slot=out_slot, x=x, g=g, beta=beta, conv_w=conv_w,
+                            o=o, dev_error=dev_error, start_pos_host=start_pos_host,
+                            init_page_host=init_page_host, max_seq_len=max_seq_len)
+    st = lib.gdn_prefill_chunked_noalloc(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
+                                         ctypes.byref(a), _stream(stream))
+    return _check(st, "gdn_prefill_chunked_noalloc") if raise_on_error else st
 
 
 def gdn_decode_step(shape: LayerShape, pool: StatePool, *, x, g, beta, conv_w, slot, o, dev_error,

@@ -244,6 +244,29 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
                                const gdn_prefill_args* args, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of gdn_prefill_chunked.  It has no counterpart on
+ * the pages; it exists for callers that cannot provide device memory for the
+ * workspace when they call the prefill: a serving runtime that reserved the
+ * GPU's free memory for its state and KV pools at start-up (a later
+ * cudaMalloc would fail or fragment those pools), or a C caller embedded in
+ * another framework without an allocator of its own.
+ *
+ * Same arguments and results as gdn_prefill_chunked, minus the workspace: the
+ * scratch is a fixed array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) in this
+ * library's device memory, held by every GPU that loads the library until the
+ * process exits.  Calls whose gdn_prefill_workspace_size exceeds it return
+ * GDN_ERR_WORKSPACE and launch nothing (at the 27B shape, about 1,600 tokens
+ * per call; split longer prefills at block boundaries, gdn_chunk_end).
+ * The entry point calls no cudaMalloc, cudaFree or other allocating routine.
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress (that device current); make that first call before
+ * any stream capture.  Every call shares the one array and it keeps the last
+ * call's contents (the kernels write every element they read, so nothing is
+ * cleared): calls that overlap on the GPU, on any streams, race. */
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+gdn_status gdn_prefill_chunked_noalloc(const gdn_layer_desc* desc, const gdn_pool* pool,
+                                       const gdn_prefill_args* args, void* stream);
+
 /* Batched single-token decode: for each sequence s the state and conv window
  * in page slot[s] advance by one token in place and o[s] = S_t q_t
  * ("Hybrid linear attention (gated DeltaNet)", "The part that is easy to get
