@@ -117,6 +117,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- replicas
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each timing's maximum over the ranks: the slowest replica sets the
+    job's time.  Without an initialised process group: the local values."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job units per second: every replica processes units_per_rank
+    units (weak scaling) in the max-over-ranks time ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- workloads
 
 class PrefillWork:
@@ -474,10 +492,8 @@ def main():
     dec_ms = sum(r[1].elapsed_time(r[2]) for r in recs) / args.steps
     ver_ms = sum(r[2].elapsed_time(r[3]) for r in recs) / args.steps
     fl_ms = sum(r[3].elapsed_time(r[4]) for r in recs) / args.steps
-    if dist:
-        t = torch.tensor([total_ms, pre_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, pre_ms = float(t[0]), float(t[1])
+    total_ms, pre_ms, dec_ms, ver_ms, fl_ms = max_over_ranks([total_ms, pre_ms, dec_ms, ver_ms, fl_ms],
+                                                            dist, "cuda")
 
     # end to end through the same call with host buffers (prefill part)
     for _ in range(2):
@@ -490,10 +506,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], dist, "cuda")
 
     peaks, peak_kind = _peaks()
     clocks = clk.summary()
@@ -502,7 +515,7 @@ def main():
     achieved = pre.algorithmic_flops() / (pre_ms * 1e-3) / 1e12
     dec_gbs = dec.bytes_per_layer() / (dec_ms / DEC_LAYERS * 1e-3) / 1e9
     fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
-    value = world * pre.tokens / (pre_ms * 1e-3)
+    value = job_throughput(pre.tokens, world, pre_ms)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
@@ -525,7 +538,7 @@ def main():
                      "kernel": "scan_kernel<128,128,2,bf16,bf16,prefill>",
                      "peak_kind": f"fp32 FMA 152 SMs x 128 lanes x 2 x {sm_max:.0f} MHz",
                      "hbm_peak_kind": peak_kind},
-        "e2e": {"value": world * pre.tokens / (e2e_ms * 1e-3), "unit": "tokens/s/layer",
+        "e2e": {"value": job_throughput(pre.tokens, world, e2e_ms), "unit": "tokens/s/layer",
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
                 "scope": "prefill part of the step"},
         "gpu_launches": args.steps * (3 + DEC_LAYERS + 9 * REP_LAYERS),

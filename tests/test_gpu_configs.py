@@ -1,0 +1,186 @@
+"""Parity at the full sizes of the benchmarked workloads and the cache
+scenarios the pages describe, through the C ABI.
+
+Full-size outputs are checked against the oracle on sampled heads (the
+oracle runs one head of a layer built from that head's channels) and against
+properties that hold at any size (bitwise cold = resume, checkpoint k = the
+state a cold run reaches at k blocks)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_deltanet_state_gb300 as gdn
+from gated_deltanet_state_gb300 import inputs
+
+from harness import (OUT_TOL, STATE_TOL, assert_out_close, assert_state_close, dev, dims, oracle_head,
+                     rel_fro, run_prefill)
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+def test_prefill_27b_4x8192_bench_configuration_matches_oracle_on_sampled_heads():
+    sh = inputs.QWEN27B
+    N, L = 4, 8192
+    cu = np.arange(0, N * L + 1, L)
+    ti = inputs.token_inputs(sh, N * L, seed=0)
+    w = inputs.conv_weights(sh, 0)
+    nck = L // sh.block_size
+    perm = inputs.permutation(N * (nck + 1), seed=0).tolist()
+    bt = [perm[s * nck:(s + 1) * nck] for s in range(N)]
+    slots = perm[N * nck:]
+    pool = gdn.StatePool(sh, N * (nck + 1), fill=0xFF)
+    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, [0] * N, [-1] * N, bt, slots)
+    assert err == 0
+    for h in (0, 29, 47):   # first, middle (qk head 9), last value head
+        ref = oracle_head(sh, ti["x"], ti["g"], ti["beta"], w, h, cu, [0] * N, sh.block_size)
+        assert_out_close(o[:, h:h + 1], ref["o"], cu)
+        assert_state_close(torch.stack([pool.state(p)[h:h + 1] for p in slots]), ref["S"])
+        cks = torch.stack([pool.state(bt[s][j])[h:h + 1] for s in range(N) for j in range(nck)])
+        assert_state_close(cks, ref["ck_S"])
+
+
+def test_decode_4b_256_sequences_matches_oracle():
+    sh = inputs.QWEN4B
+    N = 256
+    slots = inputs.permutation(2 * N, seed=3).tolist()[:N]
+    st = inputs.random_state(sh, N, seed=3)
+    pool = gdn.StatePool(sh, 2 * N, fill=0xFF)
+    for i, p in enumerate(slots):
+        pool.state(p).copy_(st["S"][i].cuda())
+        pool.window(p).copy_(st["win"][i].cuda())
+    ti = inputs.token_inputs(sh, N, seed=4)
+    w = inputs.conv_weights(sh, 4)
+    o = torch.empty(N, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_decode_step(sh, pool, x=dev(ti["x"]), g=dev(ti["g"]), beta=dev(ti["beta"]), conv_w=dev(w),
+                        slot=dev(slots, torch.int32), o=o, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    o_ref, S_ref, win_ref = oracle.decode(dims(sh), ti["x"], ti["g"], ti["beta"], w,
+                                          st["S"].double().numpy(), st["win"].float().numpy())
+    assert_out_close(o.cpu(), o_ref, list(range(N + 1)))
+    assert_state_close(torch.stack([pool.state(p) for p in slots]).cpu(), S_ref)
+    assert torch.equal(torch.stack([pool.window(p) for p in slots]).cpu().float(),
+                       torch.as_tensor(win_ref, dtype=torch.float32))
+
+
+@pytest.mark.parametrize("N,rows", [(16, 1), (16, 16), (16, 17), (64, 16), (256, 16)])
+def test_replay_flush_4b_requests_and_rows(N, rows):
+    sh = inputs.QWEN4B
+    pool = gdn.StatePool(sh, N, fill=0xFF)
+    slots = inputs.permutation(N, seed=N + rows).tolist()
+    st = inputs.random_state(sh, N, seed=N + rows)
+    for i, p in enumerate(slots):
+        pool.state(p).copy_(st["S"][i].cuda())
+        pool.window(p).copy_(st["win"][i].cuda())
+    Ls = gdn.REPLAY_LOG_SLOTS
+    log_x = torch.zeros(N, Ls, sh.conv_dim, dtype=torch.bfloat16, device="cuda")
+    log_g = torch.zeros(N, Ls, sh.num_v_heads, device="cuda")
+    log_b = torch.zeros(N, Ls, sh.num_v_heads, device="cuda")
+    log_len = torch.zeros(N, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w = dev(inputs.conv_weights(sh, rows))
+    ti = inputs.token_inputs(sh, N * rows, seed=rows)
+    kw = dict(ckpt_slot=dev(slots, torch.int32), log_x=log_x, log_g=log_g, log_beta=log_b, log_len=log_len,
+              conv_w=w, dev_error=err)
+    o = torch.empty(N, rows, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_replay_append(sh, pool, x_new=dev(ti["x"]).view(N, rows, -1), g_new=dev(ti["g"]).view(N, rows, -1),
+                          beta_new=dev(ti["beta"]).view(N, rows, -1), o=o, **kw)
+    acc = inputs.accept_lengths(N, rows, seed=rows)
+    gdn.gdn_replay_rollback(log_len, dev(acc), rows, err)
+    gdn.gdn_replay_flush(sh, pool, **kw)
+    torch.cuda.synchronize()
+    assert err.item() == 0 and log_len.cpu().tolist() == [0] * N
+    S_ref, win_ref = oracle.replay_flush(dims(sh), w.cpu(), st["S"].double().numpy(), st["win"].float().numpy(),
+                                         ti["x"].view(N, rows, -1), ti["g"].view(N, rows, -1),
+                                         ti["beta"].view(N, rows, -1), acc.numpy())
+    assert_state_close(torch.stack([pool.state(p) for p in slots]).cpu(), S_ref)
+    assert torch.equal(torch.stack([pool.window(p) for p in slots]).cpu().float(),
+                       torch.as_tensor(win_ref, dtype=torch.float32))
+
+
+def test_long_context_prefix_hit_resumes_bitwise_from_another_request():
+    """A 229,824-token first request writes 256 checkpoints (896-token blocks);
+    a second request of 229,376 tokens shares its first 200,000 tokens and
+    resumes from block floor(200000/896) - 1 = 222 (and from block 221, the
+    cached-token rule's point); both resumes equal its cold prefill bit for
+    bit, including every later checkpoint."""
+    sh = inputs.QWEN27B
+    B = sh.block_size
+    L1, L2, shared = 229_376 + 448, 229_376, 200_000
+    t1 = inputs.token_inputs(sh, L1, seed=5)
+    t2 = inputs.token_inputs(sh, L2, seed=6)
+    for k in ("x", "g", "beta"):
+        t2[k][:shared] = t1[k][:shared]
+    w = inputs.conv_weights(sh, 5)
+    nb1, nb2 = L1 // B, L2 // B          # 256 blocks each
+    pool = gdn.StatePool(sh, nb1 + nb2 + 4, fill=0xFF)
+    bt1 = list(range(nb1))
+    bt2 = list(range(nb1, nb1 + nb2))
+    _, err, _ = run_prefill(sh, pool, t1["x"], t1["g"], t1["beta"], w, [0, L1], [0], [-1], [bt1], [nb1 + nb2])
+    assert err == 0
+    o_cold, err, _ = run_prefill(sh, pool, t2["x"], t2["g"], t2["beta"], w, [0, L2], [0], [-1], [bt2],
+                                 [nb1 + nb2 + 1])
+    assert err == 0
+    cold_S = pool.state(nb1 + nb2 + 1).cpu().clone()
+    cold_ck = {j: pool.state(bt2[j]).cpu().clone() for j in range(200, nb2)}
+    for resume_block in (gdn.gdn_resume_block(shared // B * B, B),
+                         gdn.gdn_resume_block(gdn.gdn_cached_tokens(shared, B), B)):
+        assert resume_block in (222, 221)
+        P = (resume_block + 1) * B
+        # later checkpoints are rewritten into request 2's own pages (cleared
+        # first) and compared with the copies the cold run left there
+        later = {j: bt2[j] for j in range(resume_block + 1, nb2)}
+        for j, p in later.items():
+            pool.state(p).zero_()
+        bt_res = [-1] * (resume_block + 1) + [later[j] for j in range(resume_block + 1, nb2)]
+        o_res, err, _ = run_prefill(sh, pool, t2["x"][P:], t2["g"][P:], t2["beta"][P:], w, [0, L2 - P], [P],
+                                    [bt1[resume_block]], [bt_res], [nb1 + nb2 + 2])
+        assert err == 0
+        assert torch.equal(_bits(o_res), _bits(o_cold[P:]))
+        assert torch.equal(pool.state(nb1 + nb2 + 2).cpu().view(torch.int32), cold_S.view(torch.int32))
+        for j in range(resume_block + 1, nb2):
+            assert torch.equal(pool.state(later[j]).cpu().view(torch.int32), cold_ck[j].view(torch.int32)), j
+    # the shared prefix's checkpoints of both requests are the same bits
+    for j in (0, 100, 222):
+        assert torch.equal(pool.state(bt1[j]).cpu().view(torch.int32), pool.state(bt2[j]).cpu().view(torch.int32))
+    # one sampled head against the oracle over the full second request
+    h = 17
+    ref = oracle_head(sh, t2["x"], t2["g"], t2["beta"], w, h, [0, L2], [0], B)
+    assert_out_close(o_cold[:, h:h + 1], ref["o"], [0, L2])
+    assert_state_close(cold_S[h:h + 1][None], ref["S"])
+
+
+def test_nine_tokens_do_not_flip_the_checkpoint():
+    """The cold-vs-hit divergence scenario ("The prefix cache changed the
+    answer", block 1600): requests of 3,196 and 3,205 tokens both checkpoint
+    block 0 (every crossed boundary is written), to the same bits, and a
+    4,689-token request sharing their first 3,196 tokens resumed from that
+    block equals its cold run bit for bit."""
+    sh = inputs.LayerShape(2, 4, 64, 64, block_size=1600, chunk_size=64)
+    B = sh.block_size
+    base = inputs.token_inputs(sh, 4689, seed=9)
+    other = inputs.token_inputs(sh, 3205, seed=10)
+    w = inputs.conv_weights(sh, 9)
+    A1 = {k: v[:3196] for k, v in base.items()}
+    A2 = {k: torch.cat([base[k][:3196], other[k][3196:3205]]) for k in base}
+    pool = gdn.StatePool(sh, 10, fill=0xFF)
+    run_prefill(sh, pool, A1["x"], A1["g"], A1["beta"], w, [0, 3196], [0], [-1], [[1, -1, -1]], [0])
+    run_prefill(sh, pool, A2["x"], A2["g"], A2["beta"], w, [0, 3205], [0], [-1], [[2, 3, -1]], [0])
+    assert torch.equal(pool.payload(1).cpu(), pool.payload(2).cpu())
+    assert gdn.gdn_cached_tokens(3196, B) == 0 and gdn.gdn_cached_tokens(4689, B) == B
+    blk = gdn.gdn_resume_block(3196 // B * B, B)
+    assert blk == 0
+    o_cold, err, _ = run_prefill(sh, pool, base["x"], base["g"], base["beta"], w, [0, 4689], [0], [-1],
+                                 [[4, 5, -1]], [6])
+    o_res, err2, _ = run_prefill(sh, pool, base["x"][B:], base["g"][B:], base["beta"][B:], w, [0, 4689 - B], [B],
+                                 [1], [[-1, 7, -1]], [8])
+    assert err == 0 and err2 == 0
+    assert torch.equal(_bits(o_res), _bits(o_cold[B:]))
+    assert torch.equal(pool.payload(8).cpu(), pool.payload(6).cpu())
+    assert torch.equal(pool.payload(7).cpu(), pool.payload(5).cpu())
