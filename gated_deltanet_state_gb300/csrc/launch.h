@@ -44,5 +44,9 @@ cudaError_t launch_replay_rollback(int32_t* log_len, const int32_t* accepted, in
 cudaError_t launch_decode(const DecodeParams& p, int dk, int dv, int in_dtype, int out_dtype,
                           cudaStream_t st);
 cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
+// Tensor-core replay flush (dk = dv = 128): the state update only; the window
+// and log_len passes follow it.
+bool tc_flush_supported(int dk, int dv, int in_dtype);
+cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st);
 
 }  // namespace gdn
