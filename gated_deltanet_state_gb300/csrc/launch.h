@@ -48,5 +48,9 @@ cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
 // and log_len passes follow it.
 bool tc_flush_supported(int dk, int dv, int in_dtype);
 cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st);
+// Tensor-core chunked prefill (dk = dv = 128, bf16 in and out, block size a
+// multiple of 64), followed by the window pass; needs no workspace.
+bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size);
+cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st);
 
 }  // namespace gdn

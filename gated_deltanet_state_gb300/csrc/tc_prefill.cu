@@ -1,0 +1,700 @@
+// tc_prefill.cu — the chunked prefill on the tensor cores (dk = dv = 128, bf16
+// inputs and outputs).
+//
+// The gated delta rule ("Gated DeltaNet", the recurrence
+// S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = S_t q_t) taken a
+// chunk of C = 64 tokens at a time in its chunk (UT) form.  With k^, q^ the
+// L2-normalised rows of a chunk, G_i the running sum of the log decays inside
+// the chunk, gam_i = exp(G_i), S0 the state entering the chunk and row r of S
+// one value channel:
+//   u_i   = b_i (v_i - gam_i S0 k^_i) - sum_{j<i} A_ij u_j,
+//   A_ij  = b_i exp(G_i - G_j) k^_i.k^_j                        (j < i)
+//   o_i   = gam_i S0 q^_i + sum_{j<=i} exp(G_i - G_j) (q^_i.k^_j) u_j
+//   S_C   = gam_C S0 + sum_j exp(G_C - G_j) u_j k^_j^T
+// which is the token recurrence regrouped (u_i is the rank-one update of token
+// i, the triangular system collects the (I - b k k^T) factors of the tokens
+// before it).
+//
+// One CTA owns one (sequence, value head) and walks its tokens in chunks that
+// start at absolute multiples of 64, so a block boundary (a multiple of the
+// block size, itself a multiple of 64) is always a chunk end: a checkpoint is
+// the state between two chunks and a resume replays the cold run's arithmetic
+// bit for bit.  The fp32 state lives in tensor memory from the first chunk to
+// the last.  Per chunk:
+//   (A) conv + SiLU of the chunk's q, k, v channels from pre-conv rows staged
+//       in shared memory (prefetched during the previous chunk), L2 norms,
+//       cumulative gates; operands [K^; Q^] and K^T diag(exp(G_C - G)).
+//   (B) S0 from tensor memory into a bf16 operand (and gam_C S0 back);
+//       tensor cores: [K^K^T; Q^K^T] and S0 [K^; Q^]^T.
+//   (C) A and P = exp(G_i - G_j) q^_i.k^_j (j <= i) (computed while the
+//       tensor core forms S0 [K^; Q^]^T); T = (I + A)^{-1} by one warpgroup
+//       (16 x 16 blocks) while the other forms R_i = b_i (v_i - gam_i S0 k^_i);
+//       tensor cores: U^T = R T^T.
+//   (D) tensor cores: S += U^T (K^T diag(exp(G_C - G)))^T in tensor memory and
+//       U^T P^T; outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i.
+// Every product reads bf16 operands split into hi + lo parts and runs three
+// passes (hi*hi + hi*lo + lo*hi) into fp32 accumulators: each operand keeps
+// ~16 significant bits, so the chunk stays within ~1e-5 of an fp32 evaluation.
+// Every mbarrier wait is bounded; a wait that runs out sets GDN_ERR_TIMEOUT,
+// lets the tensor core drain (bounded again) and releases tensor memory.
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kPfThreads = 256;
+constexpr int kPfC = 64;                 // chunk rows
+constexpr int kPfD = 128;                // dk = dv
+constexpr int kPfXRows = kPfC + kWinRows;
+constexpr int kPfXCh = 3 * kPfD;         // staged channels per row: q | k | v
+constexpr uint32_t kPfCols = 512;        // tensor-memory columns (the whole SM's)
+// tensor-memory column map (lane = state row r, or chunk row i for D_KK / D_QK)
+constexpr uint32_t kColS = 0;            // S, fp32 128 x 128
+constexpr uint32_t kColSK = 128;         // S0 K^T, 128 x 64
+constexpr uint32_t kColSQ = 192;         // S0 Q^T, 128 x 64
+constexpr uint32_t kColKK = 256;         // [K^ K^T; Q^ K^T], 128 x 64
+constexpr uint32_t kColV = 320;          // v of the chunk, row r = channel r, 128 x 64
+constexpr uint32_t kColU = 384;          // U^T = R T^T, then U^T P^T, 128 x 64
+constexpr long long kPfWait = 4000000000LL;
+
+// Shared-memory plan (byte offsets from a 1024-byte aligned base).  The
+// 128-byte swizzled operands are K-major bf16 tiles (sw128_offset), hi part
+// then lo part.  Regions are reused phase by phase:
+//   R1: (A) y | (B) S0 operand | (C) T fp32, block scratch, T operand
+//   R2: (A-B) [K^; Q^] operand | (C-D) R^T then U^T operand, P operand, A^T fp32
+struct PfSmem {
+  static constexpr uint32_t R1 = 0;
+  static constexpr uint32_t YF = R1;                  // fp32 [64][256] (q | k)
+  static constexpr uint32_t S0 = R1;                  // S0 hi [2 kb][128][64], lo at +32 KB
+  static constexpr uint32_t S0_LO = R1 + 32768;
+  static constexpr uint32_t TF = R1;                  // T fp32 [64 i][64 j]
+  static constexpr uint32_t XSCR = R1 + 16384;        // fp32 [3][16][16] block products
+  static constexpr uint32_t TB = R1 + 32768;          // T hi [64][64], lo at +8 KB
+  static constexpr uint32_t TB_LO = R1 + 40960;
+  static constexpr uint32_t R2 = 65536;
+  static constexpr uint32_t KQ = R2;                  // [K^; Q^] hi [2 kb][128][64], lo at +32 KB
+  static constexpr uint32_t KQ_LO = R2 + 32768;
+  static constexpr uint32_t UT = R2;                  // R^T, then U^T: hi [128][64], lo at +16 KB
+  static constexpr uint32_t UT_LO = R2 + 16384;
+  static constexpr uint32_t PB = R2 + 32768;          // P hi [64][64], lo at +8 KB
+  static constexpr uint32_t PB_LO = R2 + 40960;
+  static constexpr uint32_t AT = R2 + 49152;          // A^T fp32 [64 j][64 i]
+  static constexpr uint32_t KT = 131072;              // K^T diag(dec) hi [128][64], lo at +16 KB
+  static constexpr uint32_t KT_LO = KT + 16384;
+  static constexpr uint32_t XS = 163840;              // bf16 [67][384] pre-conv rows t0-3 .. t0+63
+  static constexpr uint32_t GT = XS + kPfXRows * kPfXCh * 2;
+  // fp32 [64] each at GT: staged g, staged b, G, gam, dec = exp(G_C - G), b, q factor, k factor
+  static constexpr uint32_t MBAR = GT + 8 * 256;      // four mbarriers: K^K^T, S0[K^;Q^]^T, U, S/O
+  static constexpr uint32_t TSLOT = MBAR + 32;
+  static constexpr uint32_t BYTES = TSLOT + 8;
+  static constexpr uint32_t ALLOC = BYTES + 1024;     // + alignment slack
+};
+static_assert(PfSmem::GT % 16 == 0, "gate staging must be 16-byte aligned");
+static_assert(PfSmem::ALLOC <= 232448, "shared memory plan exceeds the per-CTA limit");
+
+// Eight fp32 values as bf16 hi and lo parts (x ~= hi + lo), converted in
+// pairs, each part stored as one 16-byte vector.
+__device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, const float* e) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(e[2 * u] - hf.x, e[2 * u + 1] - hf.y);
+    h[u] = *reinterpret_cast<const uint32_t*>(&hb);
+    l[u] = *reinterpret_cast<const uint32_t*>(&lb);
+  }
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Three-pass product D (+)= A B^T over `ksteps` K-steps of 16: A (M = 128
+// rows) and B (N rows) are K-major 128-byte swizzled tiles whose 64-wide
+// K-blocks lie `a_kb` / `b_kb` bytes apart.
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t a, uint32_t a_lo, uint32_t a_kb, uint32_t b,
+                                     uint32_t b_lo, uint32_t b_kb, int ksteps, uint32_t idesc,
+                                     bool accumulate) {
+  for (int pass = 0; pass < 3; ++pass) {
+    const uint32_t A = pass == 2 ? a_lo : a;
+    const uint32_t B = pass == 1 ? b_lo : b;
+    for (int ks = 0; ks < ksteps; ++ks) {
+      const uint32_t kb = ks >> 2, koff = (ks & 3) * 32;
+      tc::mma_bf16(d, tc::desc_sw128(A + kb * a_kb + koff), tc::desc_sw128(B + kb * b_kb + koff), idesc,
+                   (accumulate || pass != 0 || ks != 0) ? 1u : 0u);
+    }
+  }
+}
+
+// Barrier of the second warpgroup alone (threads 128..255).
+__device__ __forceinline__ void wg1_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+
+// T = (I + A)^{-1} for the 64 x 64 strictly lower triangular A given as A^T
+// (at[j * 64 + i] = A_ij, zero for i <= j), by the 128 threads t of the
+// second warpgroup.  The 16 x 16 diagonal blocks D_b = (I + A_bb)^{-1} by
+// forward substitution (a column per thread), then the blocks below them in
+// order of distance from the diagonal: T_pq = -D_p X, X = sum_{k=q}^{p-1}
+// A_pk T_kq (four adjacent columns per thread).  tf[i * 64 + j] receives T on
+// and below the diagonal (the blocks above it are left unwritten).
+__device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
+  if (t < 64) {
+    // column sweep: once x_k is final, x_i -= A_ik x_k for every i > k (A^T
+    // row o+k holds A_{o+i, o+k} contiguously in i; zero for i <= k)
+    const int o = 16 * (t >> 4), l = t & 15;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = i == l ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 15; ++k) {
+      const float xk = x[k];
+#pragma unroll
+      for (int i4 = (k + 1) / 4; i4 < 4; ++i4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(at + (o + k) * 64 + o + 4 * i4);
+        x[4 * i4] = fmaf(-a4.x, xk, x[4 * i4]);
+        x[4 * i4 + 1] = fmaf(-a4.y, xk, x[4 * i4 + 1]);
+        x[4 * i4 + 2] = fmaf(-a4.z, xk, x[4 * i4 + 2]);
+        x[4 * i4 + 3] = fmaf(-a4.w, xk, x[4 * i4 + 3]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) tf[(o + i) * 64 + o + l] = x[i];
+  }
+  wg1_sync();
+#pragma unroll
+  for (int d = 1; d < 4; ++d) {
+    const int tasks = (4 - d) * 64;
+#pragma unroll
+    for (int e0 = 0; e0 < tasks; e0 += 128) {
+      const int e = e0 + t;
+      if (e < tasks) {
+        const int q = e >> 6, p = q + d, i = (e >> 2) & 15, j4 = 4 * (e & 3);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int kk = 0; kk < 16 * d; ++kk) {
+          const int k = 16 * q + kk;
+          const float a = at[k * 64 + 16 * p + i];
+          const float4 b = *reinterpret_cast<const float4*>(tf + k * 64 + 16 * q + j4);
+          acc.x = fmaf(a, b.x, acc.x);
+          acc.y = fmaf(a, b.y, acc.y);
+          acc.z = fmaf(a, b.z, acc.z);
+          acc.w = fmaf(a, b.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(xscr + q * 256 + i * 16 + j4) = acc;
+      }
+    }
+    wg1_sync();
+#pragma unroll
+    for (int e0 = 0; e0 < tasks; e0 += 128) {
+      const int e = e0 + t;
+      if (e < tasks) {
+        const int q = e >> 6, p = q + d, i = (e >> 2) & 15, j4 = 4 * (e & 3);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // row i of D_p, read once (zero above its diagonal, so all 16 terms
+        // can be taken)
+        float dr[16];
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const float4 f = *reinterpret_cast<const float4*>(tf + (16 * p + i) * 64 + 16 * p + 4 * m4);
+          dr[4 * m4] = f.x; dr[4 * m4 + 1] = f.y; dr[4 * m4 + 2] = f.z; dr[4 * m4 + 3] = f.w;
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float a = dr[m];
+          const float4 b = *reinterpret_cast<const float4*>(xscr + q * 256 + m * 16 + j4);
+          acc.x = fmaf(-a, b.x, acc.x);
+          acc.y = fmaf(-a, b.y, acc.y);
+          acc.z = fmaf(-a, b.z, acc.z);
+          acc.w = fmaf(-a, b.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(tf + (16 * p + i) * 64 + 16 * q + j4) = acc;
+      }
+    }
+    wg1_sync();
+  }
+}
+
+__device__ __forceinline__ bool mma_wait(uint64_t* m, uint32_t parity) {
+  bool ok = tc::mbar_wait_bounded(m, parity, kPfWait);
+  ok = __syncthreads_and(ok);
+  tc::fence_after_sync();
+  return ok;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanParams p) {
+  using TIN = __nv_bfloat16;
+  using TOUT = __nv_bfloat16;
+  constexpr int D = kPfD, C = kPfC;
+  const int h = blockIdx.x, s = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;                  // state row = tensor-memory lane of this thread
+  const int half = tid >> 7;                  // column half handled in tensor-memory phases
+  const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
+
+  TokenView<TIN> V;
+  int64_t start, n_log;
+  int32_t init, final_page;
+  const bool report = (h == 0 && tid == 0);
+  if (!make_view<TIN, kPrefill>(p, s, V, start, init, final_page, n_log, report)) return;
+  const int64_t n = V.n;
+  const int64_t nch = (n + C - 1) / C;
+  const int grp = p.Hv / p.Hqk, jq = h / grp;
+  const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  float* yf = reinterpret_cast<float*>(sm + PfSmem::YF);
+  TIN* xs = reinterpret_cast<TIN*>(sm + PfSmem::XS);
+  float* gst = reinterpret_cast<float*>(sm + PfSmem::GT);
+  float* bst = gst + 64;
+  float* Gs = gst + 128;
+  float* gam = gst + 192;
+  float* dec = gst + 256;
+  float* bv = gst + 320;
+  float* rq = gst + 384;
+  float* rk = gst + 448;
+  float* at = reinterpret_cast<float*>(sm + PfSmem::AT);
+  float* tf = reinterpret_cast<float*>(sm + PfSmem::TF);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + PfSmem::MBAR);   // [0] K^K^T [1] S0 [K^;Q^]^T [2] U [3] S/O
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PfSmem::TSLOT);
+
+  // asynchronous copies of chunk c: pre-conv rows t0-3 .. t0+63 of the CTA's
+  // q, k, v channels (zeros before a cold start and past the end) and its gates
+  auto stage = [&](int64_t c) {
+    const int64_t t0 = c * C;
+    constexpr int RC = kPfXCh / 8;                   // 16-byte chunks per staged row
+    const bool inner = t0 >= kWinRows && t0 + C <= n;   // plain token rows only
+    const TIN* base = inner ? V.seg0 + (t0 - kWinRows) * p.conv_dim : nullptr;
+    for (int i = tid; i < kPfXRows * RC; i += kPfThreads) {
+      const int rr = i / RC, ch = i - rr * RC;
+      const TIN* src = inner ? base + (int64_t)rr * p.conv_dim : V.row(t0 - kWinRows + rr);
+      const int chan = ch < 16 ? cq0 + 8 * ch : (ch < 32 ? ck0 + 8 * (ch - 16) : cv0 + 8 * (ch - 32));
+      cp_async16(xs + rr * kPfXCh + 8 * ch, src ? src + chan : reinterpret_cast<const TIN*>(p.x), src ? 16 : 0);
+    }
+    if (tid < 2 * C) {
+      const int tt = tid & (C - 1);
+      const bool isb = tid >= C;
+      const int64_t t = t0 + tt;
+      const bool in = t < n;
+      const float* src = in ? (isb ? V.bptr(t, h) : V.gptr(t, h)) : p.g;
+      cp_async4((isb ? bst : gst) + tt, src, in ? 4 : 0);
+    }
+    cp_async_commit();
+  };
+  if (nch > 0) stage(0);
+
+  // conv taps of this thread's q | k channel (tid) and v channel (row)
+  const int qkch = tid < D ? cq0 + tid : ck0 + tid - D;
+  const float4 wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
+  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + row) * kConvK);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kPfCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tc::mbar_init(mbar + b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase + tlane + kColS + 64 * half;   // this thread's 64 state columns
+
+  // initial state (zeros on a cold start: the pool is not read)
+  {
+    const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float v[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 f = src ? reinterpret_cast<const float4*>(src + 32 * q)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
+      }
+      tc::tmem_st32(tS + 32 * q, v);
+    }
+    tc::tmem_st_wait();
+  }
+
+  int32_t pend = -1;    // checkpoint page due at the next read of S
+  bool ok = true;
+  uint32_t issued = 0;  // mbarriers committed in the current chunk (bit b: mbar[b])
+  int64_t c = 0;
+  for (; c < nch; ++c) {
+    const uint32_t par = (uint32_t)(c & 1);   // each mbarrier completes once per chunk
+    issued = 0;
+    const int64_t t0 = c * C;
+    const int cnt = (int)(n - t0 < C ? n - t0 : C);
+    cp_async_wait<0>();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // ---- (A) conv + SiLU.  q | k channel tid for all 64 rows -> y, in blocks
+    // of 16 rows whose loads all precede their stores.  Rows past the end are
+    // computed too (from zero inputs) and masked later: their norm factors
+    // and b are zero, so they contribute nothing (no data-dependent branch
+    // around the SiLU)
+    {
+      float xa = to_f32(xs[tid]), xb = to_f32(xs[kPfXCh + tid]), xc = to_f32(xs[2 * kPfXCh + tid]);
+#pragma unroll 1
+      for (int tb = 0; tb < C; tb += 16) {
+        float xv[16], yv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) xv[u] = to_f32(xs[(tb + u + 3) * kPfXCh + tid]);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          float z = wqk.x * xa;
+          z = fmaf(wqk.y, xb, z);
+          z = fmaf(wqk.z, xc, z);
+          z = fmaf(wqk.w, xv[u], z);
+          yv[u] = silu_fast(z);
+          xa = xb; xb = xc; xc = xv[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + tid] = yv[u];
+      }
+    }
+    // v channel `row` for rows [32 half, +32) -> tensor memory (lane = channel)
+    {
+      const int tb = 32 * half, cv = 2 * D + row;
+      float xv[35], vr[32];
+#pragma unroll
+      for (int u = 0; u < 35; ++u) xv[u] = to_f32(xs[(tb + u) * kPfXCh + cv]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float z = wv.x * xv[i];
+        z = fmaf(wv.y, xv[i + 1], z);
+        z = fmaf(wv.z, xv[i + 2], z);
+        z = fmaf(wv.w, xv[i + 3], z);
+        vr[i] = silu_fast(z);
+      }
+      tc::tmem_st32(tbase + tlane + kColV + 32 * half, vr);
+    }
+    // cumulative log decay, decay factors and b (rows past the end have g = b = 0)
+    if (warp == 0) {
+      float g0 = gst[lane], g1 = gst[lane + 32];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+        const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+        if (lane >= o) { g0 += a0; g1 += a1; }
+      }
+      g1 += __shfl_sync(0xffffffffu, g0, 31);
+      const float gC = __shfl_sync(0xffffffffu, g1, 31);
+      Gs[lane] = g0; Gs[lane + 32] = g1;
+      gam[lane] = expf(g0); gam[lane + 32] = expf(g1);
+      dec[lane] = expf(gC - g0); dec[lane + 32] = expf(gC - g1);
+      bv[lane] = bst[lane]; bv[lane + 32] = bst[lane + 32];
+    }
+    tc::tmem_st_wait();
+    __syncthreads();
+    // the staged rows and gates are consumed: prefetch the next chunk
+    if (c + 1 < nch) stage(c + 1);
+    // L2 norm factors: warp w reduces (row, q | k) pairs w, w+8, ... in a fixed
+    // order; rows past the end get factor 0
+    {
+      float ss[16];
+#pragma unroll
+      for (int it = 0; it < 16; ++it) {
+        const int k = warp + 8 * it, t = k >> 1, isk = k & 1;
+        const float* yr = yf + t * 256 + isk * D;
+        float a = 0.f;
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) {
+          const float y = yr[lane + 32 * m];
+          a = fmaf(y, y, a);
+        }
+        ss[it] = a;
+      }
+#pragma unroll
+      for (int it = 0; it < 16; ++it) ss[it] = warp_sum(ss[it]);
+      if (lane < 16) {
+        float a = ss[0];
+#pragma unroll
+        for (int it = 1; it < 16; ++it) a = lane == it ? ss[it] : a;
+        const int k = warp + 8 * lane, t = k >> 1, isk = k & 1;
+        (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
+      }
+    }
+    __syncthreads();
+    // operands: [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T diag(dec) (row =
+    // k channel); each thread loads all of its inputs before it stores
+    {
+      float4 ya[8], yb[8];
+      float fv[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int i = tid + kPfThreads * it, r = i >> 4, c8 = i & 15;
+        const int t = r & (C - 1);
+        const bool isq = r >= C;
+        fv[it] = isq ? rq[t] : rk[t];
+        const float4* src = reinterpret_cast<const float4*>(yf + t * 256 + (isq ? 0 : D) + 8 * c8);
+        ya[it] = src[0];
+        yb[it] = src[1];
+      }
+      float kt[4][8];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int i = tid + kPfThreads * it, k = i & 127, j8 = i >> 7;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = 8 * j8 + u;
+          kt[it][u] = (yf[j * 256 + D + k] * rk[j]) * dec[j];
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int i = tid + kPfThreads * it, r = i >> 4, c8 = i & 15;
+        const float f = fv[it];
+        const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
+                            yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
+        const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
+        store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int i = tid + kPfThreads * it, k = i & 127, j8 = i >> 7;
+        const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
+        store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();   // y is consumed before S0 overwrites it
+    tc::fence_after_sync();
+    // [K^ K^T; Q^ K^T] (M 128, N 64, K 128) needs no state: it runs during the split
+    if (tid == 0) {
+      mma3(tbase + kColKK, sbase + PfSmem::KQ, sbase + PfSmem::KQ_LO, 16384, sbase + PfSmem::KQ,
+           sbase + PfSmem::KQ_LO, 16384, D / 16, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 0);
+    }
+    issued |= 1u;
+
+    // ---- (B) S0 -> bf16 operand; checkpoint due at this boundary; gam_C S0 back
+    {
+      const float gC = gam[C - 1];
+      float v0[32], v1[32];
+      tc::tmem_ld32x2(tS, tS + 32, v0, v1);
+      if (pend >= 0) {
+        float* ck = page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          reinterpret_cast<float4*>(ck)[c4] = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+          reinterpret_cast<float4*>(ck + 32)[c4] =
+              make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
+        }
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t off = tc::sw128_offset(row, 64 * half + 8 * c8, 128);
+        store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
+        off = tc::sw128_offset(row, 64 * half + 32 + 8 * c8, 128);
+        store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v1 + 8 * c8);
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) { v0[e] *= gC; v1[e] *= gC; }
+      tc::tmem_st32(tS, v0);
+      tc::tmem_st32(tS + 32, v1);
+      tc::tmem_st_wait();
+      pend = -1;
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) {
+      // S0 [K^; Q^]^T (M 128, N 128, K 128)
+      mma3(tbase + kColSK, sbase + PfSmem::S0, sbase + PfSmem::S0_LO, 16384, sbase + PfSmem::KQ,
+           sbase + PfSmem::KQ_LO, 16384, D / 16, tc::idesc_bf16_f32(128, 128), false);
+      tc::mma_commit(mbar + 1);
+    }
+    issued |= 2u;
+
+    // ---- (C) A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j) for
+    // columns j in [32 half, +32), computed while S0 [K^; Q^]^T runs
+    ok = mma_wait(mbar + 0, par);
+    if (!ok) break;
+    const int q4 = warp & 3;
+    const int ir = (q4 & 1) * 32 + lane;   // chunk row i of this thread's lane
+    float ap[32];
+    {
+      tc::tmem_ld32(tbase + tlane + kColKK + 32 * half, ap);
+      const float Gi = Gs[ir];
+      const float bi = q4 < 2 ? bv[ir] : 1.0f;
+      const int lim = q4 < 2 ? ir : ir + 1;        // A: j < i; P: j <= i
+      // exp(G_i - G_j) <= 1 where it is kept; the clamp keeps the masked
+      // entries finite, the 0/1 mask avoids a branch around the exponential
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = 32 * half + e;
+        const float m = j < lim ? bi : 0.f;
+        ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
+      }
+    }
+    ok = mma_wait(mbar + 1, par);
+    if (!ok) break;
+    if (q4 < 2) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) at[(32 * half + e) * C + ir] = ap[e];
+    } else {
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint32_t off = tc::sw128_offset(ir, 32 * half + 8 * c8, 64);
+        store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
+      }
+    }
+    __syncthreads();
+    if (half == 1) {
+      // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
+      tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 128);
+      for (int e = tid - 128; e < 512; e += 128) {
+        const int i = e >> 3, c8 = e & 7;
+        const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
+        const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
+        float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (8 * c8 + u > i) v8[u] = 0.f;
+        const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
+        store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
+      }
+    } else {
+      // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` -> the A operand of U^T = R T^T
+      float a[32], b[32];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        tc::tmem_ld32x2(tbase + tlane + kColSK + 32 * q, tbase + tlane + kColV + 32 * q, a, b);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = 32 * q + e;
+          a[e] = bv[i] * fmaf(-gam[i], a[e], b[e]);
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint32_t off = tc::sw128_offset(row, 32 * q + 8 * c8, 128);
+          store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
+        }
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) {
+      // U^T = R T^T (M 128, N 64, K 64)
+      mma3(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::TB,
+           sbase + PfSmem::TB_LO, 0, C / 16, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 2);
+    }
+    issued |= 4u;
+    ok = mma_wait(mbar + 2, par);
+    if (!ok) break;
+    // U^T (rows r, K = i) as the A operand of the state update and the outputs
+    {
+      float u[32];
+      tc::tmem_ld32(tbase + tlane + kColU + 32 * half, u);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, 32 * half + 8 * c8, 128);
+        store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, u + 8 * c8);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // ---- (D) S += U^T (K^T diag(dec))^T (onto gam_C S0); U^T P^T
+    if (tid == 0) {
+      mma3(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::KT,
+           sbase + PfSmem::KT_LO, 0, C / 16, tc::idesc_bf16_f32(128, 128), true);
+      mma3(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::PB,
+           sbase + PfSmem::PB_LO, 0, C / 16, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 3);
+    }
+    issued |= 8u;
+    ok = mma_wait(mbar + 3, par);
+    if (!ok) break;
+    // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [32 half, +32)
+    {
+      float sq[32], up[32];
+      tc::tmem_ld32x2(tbase + tlane + kColSQ + 32 * half, tbase + tlane + kColU + 32 * half, sq, up);
+      TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((int64_t)(p.cu_seqlens[s] + t0) * p.Hv + h) * D + row;
+      const int64_t tstride = (int64_t)p.Hv * D;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = 32 * half + e;
+        if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
+      }
+    }
+    // a block boundary at this chunk's end: the state is checkpointed when it
+    // is next read
+    const int64_t pos = start + t0 + cnt;
+    if (pos % p.block_size == 0) {
+      const int64_t jb = pos / p.block_size - 1;
+      int32_t page = -1;
+      if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
+      else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+      if (page >= 0) {
+        if (page_ok(p.pool, page)) pend = page;
+        else if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
+      }
+    }
+    tc::fence_before_sync();
+  }
+
+  if (ok) {
+    // final state (and a checkpoint due at the last chunk's end)
+    float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 64 * half;
+    float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
+    float v0[32], v1[32];
+    tc::tmem_ld32x2(tS, tS + 32, v0, v1);
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+      const float4 f1 = make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
+      reinterpret_cast<float4*>(dst)[c4] = f0;
+      reinterpret_cast<float4*>(dst + 32)[c4] = f1;
+      if (ck) {
+        reinterpret_cast<float4*>(ck)[c4] = f0;
+        reinterpret_cast<float4*>(ck + 32)[c4] = f1;
+      }
+    }
+  } else {
+    // a wait ran out: report it, give the tensor core one more bounded wait
+    // for each product it may still hold, then release the tensor memory
+    if (tid == 0) set_error(p.err, GDN_ERR_TIMEOUT);
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b)
+      if (issued & (1u << b)) tc::mbar_wait_bounded(mbar + b, (uint32_t)(c & 1), kPfWait);
+    cp_async_wait<0>();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, kPfCols);
+}
+
+bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size) {
+  return dk == kPfD && dv == kPfD && in_dtype == GDN_BF16 && out_dtype == GDN_BF16 && block_size % kPfC == 0;
+}
+
+cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  const size_t smem = PfSmem::ALLOC;
+  cudaError_t e = cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  tc_prefill_kernel<<<dim3(p.Hv, p.num_seqs), kPfThreads, smem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // conv windows of every crossed boundary and of the final slot
+  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

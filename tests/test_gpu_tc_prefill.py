@@ -1,0 +1,121 @@
+"""The tensor-core chunk prefill (d = 128, bf16, block size a multiple of 64)
+against the fp64 oracle: lengths around the 64-row chunk edges, GQA groups of
+three, resumes from arbitrary states, strong decays, and the special cases
+that reduce to exact identities."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_deltanet_state_gb300 as gdn
+from gated_deltanet_state_gb300 import inputs
+
+from harness import assert_out_close, assert_state_close, dims, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _tables(lens, B, first_page):
+    nb = max(1, max(lens) // B)
+    bt = np.full((len(lens), nb), -1)
+    page = first_page
+    for s, L in enumerate(lens):
+        for jb in range(L // B):
+            bt[s, jb] = page
+            page += 1
+    return bt, page
+
+
+def _last_rows(x, a, b):
+    """The window a cold sequence x[a:b] leaves: its last three pre-conv rows,
+    zeros in front when it is shorter."""
+    rows = x[max(a, b - 3):b]
+    return torch.cat([rows.new_zeros(3 - rows.shape[0], x.shape[1]), rows])
+
+
+def test_chunk_edges_gqa3_match_oracle():
+    sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+    lens = [1, 63, 64, 65, 127, 128, 129, 300, 700]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    N = len(lens)
+    ti = inputs.token_inputs(sh, int(cu[-1]), seed=21)
+    w = inputs.conv_weights(sh, 21)
+    bt, npages = _tables(lens, 128, N)
+    pool = gdn.StatePool(sh, npages, fill=0xFF)
+    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, [0] * N, [-1] * N, bt, list(range(N)))
+    assert err == 0
+    ref = oracle.prefill(dims(sh), cu, [0] * N, 128, ti["x"], ti["g"], ti["beta"], w)
+    assert_out_close(o, ref["o"], cu)
+    assert_state_close(torch.stack([pool.state(s) for s in range(N)]).cpu(), ref["S"])
+    k = 0
+    for s, L in enumerate(lens):
+        for jb in range(L // 128):
+            p = int(bt[s, jb])
+            assert_state_close(pool.state(p).cpu()[None], ref["ck_S"][k][None])
+            assert torch.equal(pool.window(p).cpu().float(), torch.as_tensor(ref["ck_win"][k], dtype=torch.float32))
+            k += 1
+    for s in range(N):
+        assert torch.equal(pool.window(s).cpu(), _last_rows(ti["x"], int(cu[s]), int(cu[s + 1])))
+
+
+def test_resume_in_place_strong_decay_and_q_scale_match_oracle():
+    sh = inputs.LayerShape(1, 2, 128, 128, block_size=192, chunk_size=64, q_scale=0.5)
+    st = inputs.random_state(sh, 1, seed=31)
+    T = 450
+    ti = inputs.token_inputs(sh, T, seed=32)
+    # a stretch of very strong decays (a = e^-30): the chunk's running decay
+    # underflows toward zero inside one chunk
+    ti["g"][100:140] = -30.0
+    w = inputs.conv_weights(sh, 32)
+    pool = gdn.StatePool(sh, 4, fill=0)
+    pool.state(1).copy_(st["S"][0].cuda())
+    pool.window(1).copy_(st["win"][0].cuda())
+    # resume at 384 (two blocks); boundaries at 576 and 768 fall at rows 192, 384
+    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [384], [1], [[-1, -1, 2, 3]], [1])
+    assert err == 0
+    ref = oracle.prefill(dims(sh), [0, T], [384], 192, ti["x"], ti["g"], ti["beta"], w,
+                         st["S"].double().numpy(), st["win"].float().numpy())
+    assert_out_close(o, ref["o"], [0, T])
+    assert_state_close(pool.state(1).cpu()[None], ref["S"])
+    assert_state_close(pool.state(2).cpu()[None], ref["ck_S"][0][None])
+    assert_state_close(pool.state(3).cpu()[None], ref["ck_S"][1][None])
+
+
+def test_no_write_no_decay_keeps_the_state_bitwise():
+    """b = 0 and g = 0 (a = 1): every chunk adds exact zeros to gam_C S0 = S0,
+    so the state comes back with the same bits, and the outputs are S0 q^."""
+    sh = inputs.LayerShape(1, 2, 128, 128, block_size=128, chunk_size=64)
+    st = inputs.random_state(sh, 1, seed=41)
+    T = 200
+    ti = inputs.token_inputs(sh, T, seed=42)
+    ti["g"].zero_()
+    ti["beta"].zero_()
+    w = inputs.conv_weights(sh, 42)
+    pool = gdn.StatePool(sh, 3, fill=0)
+    pool.state(1).copy_(st["S"][0].cuda())
+    pool.window(1).copy_(st["win"][0].cuda())
+    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [128], [1], [[-1, 2, -1]], [0])
+    assert err == 0
+    assert torch.equal(pool.state(0).cpu().view(torch.int32), st["S"][0].view(torch.int32))
+    assert torch.equal(pool.state(2).cpu().view(torch.int32), st["S"][0].view(torch.int32))
+    ref = oracle.prefill(dims(sh), [0, T], [128], 128, ti["x"], ti["g"], ti["beta"], w,
+                         st["S"].double().numpy(), st["win"].float().numpy())
+    assert_out_close(o, ref["o"], [0, T])
+
+
+def test_cold_equals_resume_bitwise_at_64_multiple_blocks():
+    sh = inputs.LayerShape(2, 4, 128, 128, block_size=320, chunk_size=64)
+    T = 1000
+    ti = inputs.token_inputs(sh, T, seed=51)
+    w = inputs.conv_weights(sh, 51)
+    pool = gdn.StatePool(sh, 10, fill=0)
+    o_cold, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [0], [-1], [[1, 2, 3]], [0])
+    assert err == 0
+    P = 320
+    o_res, err, _ = run_prefill(sh, pool, ti["x"][P:], ti["g"][P:], ti["beta"][P:], w, [0, T - P], [P], [1],
+                                [[-1, 5, 6]], [4])
+    assert err == 0
+    assert torch.equal(o_res.view(torch.int16), o_cold[P:].view(torch.int16))
+    assert torch.equal(pool.payload(4).cpu(), pool.payload(0).cpu())
+    assert torch.equal(pool.payload(5).cpu(), pool.payload(2).cpu())
+    assert torch.equal(pool.payload(6).cpu(), pool.payload(3).cpu())
