@@ -124,6 +124,7 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.x = a->x;
   p.g = a->g;
   p.beta = a->beta;
+  p.total_rows = a->total_tokens;
   bind_workspace(p, workspace, a->total_tokens);
   const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
   return cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,

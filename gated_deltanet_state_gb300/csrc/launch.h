@@ -1,6 +1,8 @@
 // launch.h — internal launchers behind the C ABI (not exported).
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "scan.cuh"
 
@@ -47,6 +49,9 @@ cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
 // Tensor-core replay flush (dk = dv = 128): the state update only; the window
 // and log_len passes follow it.
 bool tc_flush_supported(int dk, int dv, int in_dtype);
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda); nullptr if the driver lacks it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st);
 // Tensor-core chunked prefill (dk = dv = 128, bf16 in and out, block size a
 // multiple of 64), followed by the window pass; needs no workspace.

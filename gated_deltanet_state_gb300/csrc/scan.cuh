@@ -60,6 +60,7 @@ struct ScanParams {
   const void* x;
   const float* g;
   const float* beta;
+  int64_t total_rows;   // rows of x, g, beta and o (all sequences)
   // replay
   const int32_t* ckpt_slot;
   const void* log_x;

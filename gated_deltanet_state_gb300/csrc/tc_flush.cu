@@ -20,8 +20,6 @@
 // computed in the kernel from the checkpoint's window and the log; the
 // window itself is rewritten afterwards by window_kernel (other heads of the
 // qk group still read it here).
-#include <cudaTypedefs.h>
-
 #include "launch.h"
 #include "tc.cuh"
 
@@ -399,9 +397,7 @@ bool tc_flush_supported(int dk, int dv, int in_dtype) {
   return dk == kTcD && dv == kTcD && in_dtype == GDN_BF16;   // staging sized for bf16 rows
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
-// (no link-time dependency on libcuda).
-static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -416,7 +412,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st) {
   (void)in_dtype;
   if (p.num_seqs == 0) return cudaSuccess;
-  auto encode = encode_tiled();
+  auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   // pool states as [page][Hv * 128 rows][128 columns] fp32
   CUtensorMap tmap;

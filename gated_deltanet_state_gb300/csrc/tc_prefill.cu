@@ -44,11 +44,12 @@ namespace gdn {
 
 namespace {
 
-constexpr int kPfThreads = 256;
+constexpr int kPfWorkers = 256;         // eight warps of CUDA-core work
+constexpr int kPfThreads = kPfWorkers + 32;   // + one warp that issues the tensor-core products
+constexpr int kMmaTid = kPfWorkers;      // the issuing thread (lane 0 of the ninth warp)
 constexpr int kPfC = 64;                 // chunk rows
 constexpr int kPfD = 128;                // dk = dv
 constexpr int kPfXRows = kPfC + kWinRows;
-constexpr int kPfXCh = 3 * kPfD;         // staged channels per row: q | k | v
 constexpr uint32_t kPfCols = 512;        // tensor-memory columns (the whole SM's)
 // tensor-memory column map (lane = state row r, or chunk row i for D_KK / D_QK)
 constexpr uint32_t kColS = 0;            // S, fp32 128 x 128
@@ -83,11 +84,14 @@ struct PfSmem {
   static constexpr uint32_t AT = R2 + 49152;          // A^T fp32 [64 j][64 i]
   static constexpr uint32_t KT = 131072;              // K^T diag(dec) hi [128][64], lo at +16 KB
   static constexpr uint32_t KT_LO = KT + 16384;
-  static constexpr uint32_t XS = 163840;              // bf16 [67][384] pre-conv rows t0-3 .. t0+63
-  static constexpr uint32_t GT = XS + kPfXRows * kPfXCh * 2;
+  static constexpr uint32_t OT = R1;                  // (D) outputs bf16 [64 rows][128 dv]
+  // pre-conv rows t0-3 .. t0+63 of the chunk, bf16 [67][128] per tile: q, k, v
+  static constexpr uint32_t XS = 163840;
+  static constexpr uint32_t XTILE = 17408;            // tile stride (1024-aligned)
+  static constexpr uint32_t GT = XS + 2 * XTILE + kPfXRows * kPfD * 2;
   // fp32 [64] each at GT: staged g, staged b, G, gam, dec = exp(G_C - G), b, q factor, k factor
-  static constexpr uint32_t MBAR = GT + 8 * 256;      // four mbarriers: K^K^T, S0[K^;Q^]^T, U, S/O
-  static constexpr uint32_t TSLOT = MBAR + 32;
+  static constexpr uint32_t MBAR = GT + 8 * 256;      // mbarriers: K^K^T, S0[K^;Q^]^T, U, S/O, staged rows
+  static constexpr uint32_t TSLOT = MBAR + 40;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;     // + alignment slack
 };
@@ -126,6 +130,9 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a, uint32_t a_lo, uint
     }
   }
 }
+
+// Barrier of the eight worker warps alone (threads 0..255).
+__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
 
 // Barrier of the second warpgroup alone (threads 128..255).
 __device__ __forceinline__ void wg1_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
@@ -214,8 +221,16 @@ __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
   }
 }
 
-__device__ __forceinline__ bool mma_wait(uint64_t* m, uint32_t parity) {
-  bool ok = tc::mbar_wait_bounded(m, parity, kPfWait);
+// A worker's bounded wait for a tensor-core product; a wait that runs out
+// clears `ok`, which the next whole-CTA barrier turns into a common exit.
+__device__ __forceinline__ void mma_wait(uint64_t* m, uint32_t parity, bool& ok) {
+  ok = tc::mbar_wait_bounded(m, parity, kPfWait) && ok;
+  tc::fence_after_sync();
+}
+
+// Whole-CTA barrier (workers and the issuing warp) that also agrees on `ok`.
+__device__ __forceinline__ bool cta_sync_ok(bool ok) {
+  tc::fence_before_sync();
   ok = __syncthreads_and(ok);
   tc::fence_after_sync();
   return ok;
@@ -223,14 +238,17 @@ __device__ __forceinline__ bool mma_wait(uint64_t* m, uint32_t parity) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1)
+    tc_prefill_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap,
+                      const __grid_constant__ CUtensorMap omap, int tma_out) {
   using TIN = __nv_bfloat16;
   using TOUT = __nv_bfloat16;
   constexpr int D = kPfD, C = kPfC;
   const int h = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool worker = tid < kPfWorkers;
   const int row = tid & 127;                  // state row = tensor-memory lane of this thread
-  const int half = tid >> 7;                  // column half handled in tensor-memory phases
+  const int half = (tid >> 7) & 1;            // column half handled in tensor-memory phases
   const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
 
   TokenView<TIN> V;
@@ -242,12 +260,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
   const int64_t nch = (n + C - 1) / C;
   const int grp = p.Hv / p.Hqk, jq = h / grp;
   const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
+  const int64_t row0 = p.cu_seqlens[s];      // first row of this sequence in x, g, beta, o
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   float* yf = reinterpret_cast<float*>(sm + PfSmem::YF);
-  TIN* xs = reinterpret_cast<TIN*>(sm + PfSmem::XS);
+  TIN* xq = reinterpret_cast<TIN*>(sm + PfSmem::XS);
+  TIN* xk = reinterpret_cast<TIN*>(sm + PfSmem::XS + PfSmem::XTILE);
+  TIN* xv = reinterpret_cast<TIN*>(sm + PfSmem::XS + 2 * PfSmem::XTILE);
   float* gst = reinterpret_cast<float*>(sm + PfSmem::GT);
   float* bst = gst + 64;
   float* Gs = gst + 128;
@@ -258,21 +279,37 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
   float* rk = gst + 448;
   float* at = reinterpret_cast<float*>(sm + PfSmem::AT);
   float* tf = reinterpret_cast<float*>(sm + PfSmem::TF);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + PfSmem::MBAR);   // [0] K^K^T [1] S0 [K^;Q^]^T [2] U [3] S/O
+  TOUT* ot = reinterpret_cast<TOUT*>(sm + PfSmem::OT);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + PfSmem::MBAR);   // [0] K^K^T [1] S0 [K^;Q^]^T [2] U [3] S/O [4] rows
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PfSmem::TSLOT);
 
-  // asynchronous copies of chunk c: pre-conv rows t0-3 .. t0+63 of the CTA's
-  // q, k, v channels (zeros before a cold start and past the end) and its gates
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kPfCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int b = 0; b < 5; ++b) tc::mbar_init(mbar + b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase + tlane + kColS + 64 * half;   // this thread's 64 state columns
+
+  // chunk c's pre-conv rows t0-3 .. t0+63 (three TMA tiles: q, k, v channels;
+  // rows outside x read as zeros) and its gates (zeros past the end).  Run by
+  // the workers; the rows before a sequence's first token are fixed up after
+  // they land (they belong to the previous sequence).
   auto stage = [&](int64_t c) {
     const int64_t t0 = c * C;
-    constexpr int RC = kPfXCh / 8;                   // 16-byte chunks per staged row
-    const bool inner = t0 >= kWinRows && t0 + C <= n;   // plain token rows only
-    const TIN* base = inner ? V.seg0 + (t0 - kWinRows) * p.conv_dim : nullptr;
-    for (int i = tid; i < kPfXRows * RC; i += kPfThreads) {
-      const int rr = i / RC, ch = i - rr * RC;
-      const TIN* src = inner ? base + (int64_t)rr * p.conv_dim : V.row(t0 - kWinRows + rr);
-      const int chan = ch < 16 ? cq0 + 8 * ch : (ch < 32 ? ck0 + 8 * (ch - 16) : cv0 + 8 * (ch - 32));
-      cp_async16(xs + rr * kPfXCh + 8 * ch, src ? src + chan : reinterpret_cast<const TIN*>(p.x), src ? 16 : 0);
+    if (tid == 0) {
+      tc::mbar_expect_tx(mbar + 4, 3 * kPfXRows * D * 2);
+      const int y = (int)(row0 + t0 - kWinRows);
+      tc::tma_load_2d(xq, &xmap, cq0, y, mbar + 4);
+      tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 4);
+      tc::tma_load_2d(xv, &xmap, cv0, y, mbar + 4);
     }
     if (tid < 2 * C) {
       const int tt = tid & (C - 1);
@@ -284,30 +321,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
     }
     cp_async_commit();
   };
-  if (nch > 0) stage(0);
+  int64_t x_issued = -1;   // chunk whose rows are in flight (every worker tracks it)
+  if (worker && nch > 0) {
+    stage(0);
+    x_issued = 0;
+  }
 
   // conv taps of this thread's q | k channel (tid) and v channel (row)
-  const int qkch = tid < D ? cq0 + tid : ck0 + tid - D;
-  const float4 wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
-  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + row) * kConvK);
-
-  if (warp == 0) {
-    tc::tmem_alloc(tslot, kPfCols);
-    tc::tmem_relinquish();
-  }
-  if (tid == 0) {
-#pragma unroll
-    for (int b = 0; b < 4; ++b) tc::mbar_init(mbar + b, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase + tlane + kColS + 64 * half;   // this thread's 64 state columns
-
-  // initial state (zeros on a cold start: the pool is not read)
-  {
+  float4 wqk = make_float4(0.f, 0.f, 0.f, 0.f), wv = wqk;
+  if (worker) {
+    const int qkch = tid < D ? cq0 + tid : ck0 + tid - D;
+    wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
+    wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + row) * kConvK);
+    // initial state (zeros on a cold start: the pool is not read)
     const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -324,152 +350,175 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
 
   int32_t pend = -1;    // checkpoint page due at the next read of S
   bool ok = true;
-  uint32_t issued = 0;  // mbarriers committed in the current chunk (bit b: mbar[b])
+  uint32_t issued = 0;  // tensor-core products committed in the current chunk (bit b: mbar[b])
   int64_t c = 0;
   for (; c < nch; ++c) {
     const uint32_t par = (uint32_t)(c & 1);   // each mbarrier completes once per chunk
-    issued = 0;
     const int64_t t0 = c * C;
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
-    cp_async_wait<0>();
-    __syncthreads();
-    tc::fence_after_sync();
+    issued = 0;
 
-    // ---- (A) conv + SiLU.  q | k channel tid for all 64 rows -> y, in blocks
-    // of 16 rows whose loads all precede their stores.  Rows past the end are
-    // computed too (from zero inputs) and masked later: their norm factors
-    // and b are zero, so they contribute nothing (no data-dependent branch
-    // around the SiLU)
-    {
-      float xa = to_f32(xs[tid]), xb = to_f32(xs[kPfXCh + tid]), xc = to_f32(xs[2 * kPfXCh + tid]);
+    if (worker) {
+      // ---- the chunk's rows and gates have landed; the previous output tile
+      // has been read out
+      if (tid == 0) tc::bulk_wait_read();
+      ok = tc::mbar_wait_bounded(mbar + 4, par, kPfWait) && ok;
+      cp_async_wait<0>();
+      workers_sync();
+      if (ok) x_issued = -1;
+      if (c == 0) {
+        // history rows of the first chunk: the resumed window, or zeros
+        const TIN* win = V.win;
+        for (int e = tid; e < 3 * kWinRows * (D / 2); e += kPfWorkers) {
+          const int tile = e / (kWinRows * (D / 2)), r = (e / (D / 2)) % kWinRows, c2 = e % (D / 2);
+          const int ch = (tile == 0 ? cq0 : tile == 1 ? ck0 : cv0) + 2 * c2;
+          uint32_t v = 0;
+          if (win) v = *reinterpret_cast<const uint32_t*>(win + (int64_t)r * p.conv_dim + ch);
+          TIN* dst = tile == 0 ? xq : tile == 1 ? xk : xv;
+          *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
+        }
+        workers_sync();
+      }
+
+      // ---- (A) conv + SiLU.  q | k channel tid for all 64 rows -> y, in
+      // blocks of 16 rows whose loads all precede their stores.  Rows past
+      // the end are computed too and masked later: their norm factors and b
+      // are zero, so they contribute nothing (no data-dependent branch around
+      // the SiLU)
+      {
+        const TIN* xc_ = tid < D ? xq + tid : xk + tid - D;
+        float xa = to_f32(xc_[0]), xb = to_f32(xc_[D]), xc = to_f32(xc_[2 * D]);
 #pragma unroll 1
-      for (int tb = 0; tb < C; tb += 16) {
-        float xv[16], yv[16];
+        for (int tb = 0; tb < C; tb += 16) {
+          float xr[16], yv[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) xv[u] = to_f32(xs[(tb + u + 3) * kPfXCh + tid]);
+          for (int u = 0; u < 16; ++u) xr[u] = to_f32(xc_[(tb + u + 3) * D]);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float z = wqk.x * xa;
-          z = fmaf(wqk.y, xb, z);
-          z = fmaf(wqk.z, xc, z);
-          z = fmaf(wqk.w, xv[u], z);
-          yv[u] = silu_fast(z);
-          xa = xb; xb = xc; xc = xv[u];
-        }
+          for (int u = 0; u < 16; ++u) {
+            float z = wqk.x * xa;
+            z = fmaf(wqk.y, xb, z);
+            z = fmaf(wqk.z, xc, z);
+            z = fmaf(wqk.w, xr[u], z);
+            yv[u] = silu_fast(z);
+            xa = xb; xb = xc; xc = xr[u];
+          }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + tid] = yv[u];
-      }
-    }
-    // v channel `row` for rows [32 half, +32) -> tensor memory (lane = channel)
-    {
-      const int tb = 32 * half, cv = 2 * D + row;
-      float xv[35], vr[32];
-#pragma unroll
-      for (int u = 0; u < 35; ++u) xv[u] = to_f32(xs[(tb + u) * kPfXCh + cv]);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float z = wv.x * xv[i];
-        z = fmaf(wv.y, xv[i + 1], z);
-        z = fmaf(wv.z, xv[i + 2], z);
-        z = fmaf(wv.w, xv[i + 3], z);
-        vr[i] = silu_fast(z);
-      }
-      tc::tmem_st32(tbase + tlane + kColV + 32 * half, vr);
-    }
-    // cumulative log decay, decay factors and b (rows past the end have g = b = 0)
-    if (warp == 0) {
-      float g0 = gst[lane], g1 = gst[lane + 32];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
-        const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
-        if (lane >= o) { g0 += a0; g1 += a1; }
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      const float gC = __shfl_sync(0xffffffffu, g1, 31);
-      Gs[lane] = g0; Gs[lane + 32] = g1;
-      gam[lane] = expf(g0); gam[lane + 32] = expf(g1);
-      dec[lane] = expf(gC - g0); dec[lane + 32] = expf(gC - g1);
-      bv[lane] = bst[lane]; bv[lane + 32] = bst[lane + 32];
-    }
-    tc::tmem_st_wait();
-    __syncthreads();
-    // the staged rows and gates are consumed: prefetch the next chunk
-    if (c + 1 < nch) stage(c + 1);
-    // L2 norm factors: warp w reduces (row, q | k) pairs w, w+8, ... in a fixed
-    // order; rows past the end get factor 0
-    {
-      float ss[16];
-#pragma unroll
-      for (int it = 0; it < 16; ++it) {
-        const int k = warp + 8 * it, t = k >> 1, isk = k & 1;
-        const float* yr = yf + t * 256 + isk * D;
-        float a = 0.f;
-#pragma unroll
-        for (int m = 0; m < D / 32; ++m) {
-          const float y = yr[lane + 32 * m];
-          a = fmaf(y, y, a);
-        }
-        ss[it] = a;
-      }
-#pragma unroll
-      for (int it = 0; it < 16; ++it) ss[it] = warp_sum(ss[it]);
-      if (lane < 16) {
-        float a = ss[0];
-#pragma unroll
-        for (int it = 1; it < 16; ++it) a = lane == it ? ss[it] : a;
-        const int k = warp + 8 * lane, t = k >> 1, isk = k & 1;
-        (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
-      }
-    }
-    __syncthreads();
-    // operands: [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T diag(dec) (row =
-    // k channel); each thread loads all of its inputs before it stores
-    {
-      float4 ya[8], yb[8];
-      float fv[8];
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int i = tid + kPfThreads * it, r = i >> 4, c8 = i & 15;
-        const int t = r & (C - 1);
-        const bool isq = r >= C;
-        fv[it] = isq ? rq[t] : rk[t];
-        const float4* src = reinterpret_cast<const float4*>(yf + t * 256 + (isq ? 0 : D) + 8 * c8);
-        ya[it] = src[0];
-        yb[it] = src[1];
-      }
-      float kt[4][8];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int i = tid + kPfThreads * it, k = i & 127, j8 = i >> 7;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = 8 * j8 + u;
-          kt[it][u] = (yf[j * 256 + D + k] * rk[j]) * dec[j];
+          for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + tid] = yv[u];
         }
       }
+      // v channel `row` for rows [32 half, +32) -> tensor memory (lane = channel)
+      {
+        const int tb = 32 * half;
+        float xr[35], vr[32];
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int i = tid + kPfThreads * it, r = i >> 4, c8 = i & 15;
-        const float f = fv[it];
-        const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
-                            yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
-        const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
-        store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
-      }
+        for (int u = 0; u < 35; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int i = tid + kPfThreads * it, k = i & 127, j8 = i >> 7;
-        const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
-        store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
+        for (int i = 0; i < 32; ++i) {
+          float z = wv.x * xr[i];
+          z = fmaf(wv.y, xr[i + 1], z);
+          z = fmaf(wv.z, xr[i + 2], z);
+          z = fmaf(wv.w, xr[i + 3], z);
+          vr[i] = silu_fast(z);
+        }
+        tc::tmem_st32(tbase + tlane + kColV + 32 * half, vr);
       }
+      // cumulative log decay, decay factors and b (rows past the end have g = b = 0)
+      if (warp == 0) {
+        float g0 = gst[lane], g1 = gst[lane + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+          const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+          if (lane >= o) { g0 += a0; g1 += a1; }
+        }
+        g1 += __shfl_sync(0xffffffffu, g0, 31);
+        const float gC = __shfl_sync(0xffffffffu, g1, 31);
+        Gs[lane] = g0; Gs[lane + 32] = g1;
+        gam[lane] = expf(g0); gam[lane + 32] = expf(g1);
+        dec[lane] = expf(gC - g0); dec[lane + 32] = expf(gC - g1);
+        bv[lane] = bst[lane]; bv[lane + 32] = bst[lane + 32];
+      }
+      tc::tmem_st_wait();
+      workers_sync();
+      // the staged rows and gates are consumed: prefetch the next chunk
+      if (c + 1 < nch) {
+        stage(c + 1);
+        x_issued = c + 1;
+      }
+      // L2 norm factors: warp w reduces (row, q | k) pairs w, w+8, ... in a
+      // fixed order; rows past the end get factor 0
+      {
+        float ss[16];
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int k = warp + 8 * it, t = k >> 1, isk = k & 1;
+          const float* yr = yf + t * 256 + isk * D;
+          float a = 0.f;
+#pragma unroll
+          for (int m = 0; m < D / 32; ++m) {
+            const float y = yr[lane + 32 * m];
+            a = fmaf(y, y, a);
+          }
+          ss[it] = a;
+        }
+#pragma unroll
+        for (int it = 0; it < 16; ++it) ss[it] = warp_sum(ss[it]);
+        if (lane < 16) {
+          float a = ss[0];
+#pragma unroll
+          for (int it = 1; it < 16; ++it) a = lane == it ? ss[it] : a;
+          const int k = warp + 8 * lane, t = k >> 1, isk = k & 1;
+          (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
+        }
+      }
+      workers_sync();
+      // operands: [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T diag(dec) (row =
+      // k channel); each thread loads all of its inputs before it stores
+      {
+        float4 ya[8], yb[8];
+        float fv[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
+          const int t = r & (C - 1);
+          const bool isq = r >= C;
+          fv[it] = isq ? rq[t] : rk[t];
+          const float4* src = reinterpret_cast<const float4*>(yf + t * 256 + (isq ? 0 : D) + 8 * c8);
+          ya[it] = src[0];
+          yb[it] = src[1];
+        }
+        float kt[4][8];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int i = tid + kPfWorkers * it, k = i & 127, j8 = i >> 7;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = 8 * j8 + u;
+            kt[it][u] = (yf[j * 256 + D + k] * rk[j]) * dec[j];
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
+          const float f = fv[it];
+          const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
+                              yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
+          const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
+          store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int i = tid + kPfWorkers * it, k = i & 127, j8 = i >> 7;
+          const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
+          store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
+        }
+      }
+      tc::fence_async_smem();
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();   // y is consumed before S0 overwrites it
-    tc::fence_after_sync();
+    ok = cta_sync_ok(ok);   // y is consumed; [K^; Q^] and K^T diag(dec) are in place
+    if (!ok) break;
     // [K^ K^T; Q^ K^T] (M 128, N 64, K 128) needs no state: it runs during the split
-    if (tid == 0) {
+    if (tid == kMmaTid) {
       mma3(tbase + kColKK, sbase + PfSmem::KQ, sbase + PfSmem::KQ_LO, 16384, sbase + PfSmem::KQ,
            sbase + PfSmem::KQ_LO, 16384, D / 16, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 0);
@@ -477,7 +526,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
     issued |= 1u;
 
     // ---- (B) S0 -> bf16 operand; checkpoint due at this boundary; gam_C S0 back
-    {
+    if (worker) {
       const float gC = gam[C - 1];
       float v0[32], v1[32];
       tc::tmem_ld32x2(tS, tS + 32, v0, v1);
@@ -503,12 +552,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
       tc::tmem_st32(tS + 32, v1);
       tc::tmem_st_wait();
       pend = -1;
+      tc::fence_async_smem();
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (tid == 0) {
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == kMmaTid) {
       // S0 [K^; Q^]^T (M 128, N 128, K 128)
       mma3(tbase + kColSK, sbase + PfSmem::S0, sbase + PfSmem::S0_LO, 16384, sbase + PfSmem::KQ,
            sbase + PfSmem::KQ_LO, 16384, D / 16, tc::idesc_bf16_f32(128, 128), false);
@@ -518,85 +566,84 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
 
     // ---- (C) A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j) for
     // columns j in [32 half, +32), computed while S0 [K^; Q^]^T runs
-    ok = mma_wait(mbar + 0, par);
-    if (!ok) break;
-    const int q4 = warp & 3;
-    const int ir = (q4 & 1) * 32 + lane;   // chunk row i of this thread's lane
-    float ap[32];
-    {
-      tc::tmem_ld32(tbase + tlane + kColKK + 32 * half, ap);
-      const float Gi = Gs[ir];
-      const float bi = q4 < 2 ? bv[ir] : 1.0f;
-      const int lim = q4 < 2 ? ir : ir + 1;        // A: j < i; P: j <= i
-      // exp(G_i - G_j) <= 1 where it is kept; the clamp keeps the masked
-      // entries finite, the 0/1 mask avoids a branch around the exponential
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = 32 * half + e;
-        const float m = j < lim ? bi : 0.f;
-        ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
-      }
-    }
-    ok = mma_wait(mbar + 1, par);
-    if (!ok) break;
-    if (q4 < 2) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) at[(32 * half + e) * C + ir] = ap[e];
-    } else {
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const uint32_t off = tc::sw128_offset(ir, 32 * half + 8 * c8, 64);
-        store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
-      }
-    }
-    __syncthreads();
-    if (half == 1) {
-      // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
-      tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 128);
-      for (int e = tid - 128; e < 512; e += 128) {
-        const int i = e >> 3, c8 = e & 7;
-        const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
-        const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
-        float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (8 * c8 + u > i) v8[u] = 0.f;
-        const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
-        store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
-      }
-    } else {
-      // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` -> the A operand of U^T = R T^T
-      float a[32], b[32];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        tc::tmem_ld32x2(tbase + tlane + kColSK + 32 * q, tbase + tlane + kColV + 32 * q, a, b);
+    if (worker) {
+      mma_wait(mbar + 0, par, ok);
+      const int q4 = warp & 3;
+      const int ir = (q4 & 1) * 32 + lane;   // chunk row i of this thread's lane
+      float ap[32];
+      {
+        tc::tmem_ld32(tbase + tlane + kColKK + 32 * half, ap);
+        const float Gi = Gs[ir];
+        const float bi = q4 < 2 ? bv[ir] : 1.0f;
+        const int lim = q4 < 2 ? ir : ir + 1;        // A: j < i; P: j <= i
+        // exp(G_i - G_j) <= 1 where it is kept; the clamp keeps the masked
+        // entries finite, the 0/1 mask avoids a branch around the exponential
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int i = 32 * q + e;
-          a[e] = bv[i] * fmaf(-gam[i], a[e], b[e]);
-        }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const uint32_t off = tc::sw128_offset(row, 32 * q + 8 * c8, 128);
-          store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
+          const int j = 32 * half + e;
+          const float m = j < lim ? bi : 0.f;
+          ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
         }
       }
+      mma_wait(mbar + 1, par, ok);
+      workers_sync();   // every worker is past the S0 [K^; Q^]^T wait: [K^; Q^] is free
+      if (q4 < 2) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) at[(32 * half + e) * C + ir] = ap[e];
+      } else {
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint32_t off = tc::sw128_offset(ir, 32 * half + 8 * c8, 64);
+          store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
+        }
+      }
+      workers_sync();
+      if (half == 1) {
+        // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
+        tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 128);
+        for (int e = tid - 128; e < 512; e += 128) {
+          const int i = e >> 3, c8 = e & 7;
+          const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
+          const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
+          float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (8 * c8 + u > i) v8[u] = 0.f;
+          const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
+          store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
+        }
+      } else {
+        // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` -> the A operand of U^T = R T^T
+        float a[32], b[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          tc::tmem_ld32x2(tbase + tlane + kColSK + 32 * q, tbase + tlane + kColV + 32 * q, a, b);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = 32 * q + e;
+            a[e] = bv[i] * fmaf(-gam[i], a[e], b[e]);
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const uint32_t off = tc::sw128_offset(row, 32 * q + 8 * c8, 128);
+            store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
+          }
+        }
+      }
+      tc::fence_async_smem();
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (tid == 0) {
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == kMmaTid) {
       // U^T = R T^T (M 128, N 64, K 64)
       mma3(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::TB,
            sbase + PfSmem::TB_LO, 0, C / 16, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 2);
     }
     issued |= 4u;
-    ok = mma_wait(mbar + 2, par);
-    if (!ok) break;
     // U^T (rows r, K = i) as the A operand of the state update and the outputs
-    {
+    if (worker) {
+      mma_wait(mbar + 2, par, ok);
       float u[32];
       tc::tmem_ld32(tbase + tlane + kColU + 32 * half, u);
 #pragma unroll
@@ -604,14 +651,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
         const uint32_t off = tc::sw128_offset(row, 32 * half + 8 * c8, 128);
         store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, u + 8 * c8);
       }
+      tc::fence_async_smem();
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
 
     // ---- (D) S += U^T (K^T diag(dec))^T (onto gam_C S0); U^T P^T
-    if (tid == 0) {
+    if (tid == kMmaTid) {
       mma3(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::KT,
            sbase + PfSmem::KT_LO, 0, C / 16, tc::idesc_bf16_f32(128, 128), true);
       mma3(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::PB,
@@ -619,62 +665,80 @@ __global__ void __launch_bounds__(kPfThreads, 1) tc_prefill_kernel(const ScanPar
       tc::mma_commit(mbar + 3);
     }
     issued |= 8u;
-    ok = mma_wait(mbar + 3, par);
-    if (!ok) break;
-    // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [32 half, +32)
-    {
+    if (worker) {
+      mma_wait(mbar + 3, par, ok);
+      // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [32 half, +32):
+      // a full chunk goes out as one TMA tile through shared memory, a
+      // partial one (the sequence's last) by plain stores
       float sq[32], up[32];
       tc::tmem_ld32x2(tbase + tlane + kColSQ + 32 * half, tbase + tlane + kColU + 32 * half, sq, up);
-      TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((int64_t)(p.cu_seqlens[s] + t0) * p.Hv + h) * D + row;
-      const int64_t tstride = (int64_t)p.Hv * D;
+      if (tma_out && cnt == C) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int i = 32 * half + e;
-        if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
+        for (int e = 0; e < 32; ++e) ot[(32 * half + e) * D + row] = from_f32<TOUT>(fmaf(gam[32 * half + e], sq[e], up[e]));
+        tc::fence_async_smem();
+        workers_sync();
+        if (tid == 0) {
+          tc::tma_store_2d(&omap, h * D, (int)(row0 + t0), ot);
+          tc::bulk_commit();
+        }
+      } else {
+        TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
+        const int64_t tstride = (int64_t)p.Hv * D;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int i = 32 * half + e;
+          if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
+        }
+      }
+      // a block boundary at this chunk's end: the state is checkpointed when
+      // it is next read
+      const int64_t pos = start + t0 + cnt;
+      if (pos % p.block_size == 0) {
+        const int64_t jb = pos / p.block_size - 1;
+        int32_t page = -1;
+        if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
+        else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+        if (page >= 0) {
+          if (page_ok(p.pool, page)) pend = page;
+          else if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
+        }
       }
     }
-    // a block boundary at this chunk's end: the state is checkpointed when it
-    // is next read
-    const int64_t pos = start + t0 + cnt;
-    if (pos % p.block_size == 0) {
-      const int64_t jb = pos / p.block_size - 1;
-      int32_t page = -1;
-      if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
-      else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
-      if (page >= 0) {
-        if (page_ok(p.pool, page)) pend = page;
-        else if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
-      }
-    }
-    tc::fence_before_sync();
   }
 
+  ok = cta_sync_ok(ok);
   if (ok) {
-    // final state (and a checkpoint due at the last chunk's end)
-    float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 64 * half;
-    float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
-    float v0[32], v1[32];
-    tc::tmem_ld32x2(tS, tS + 32, v0, v1);
+    if (worker) {
+      // final state (and a checkpoint due at the last chunk's end)
+      float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 64 * half;
+      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
+      float v0[32], v1[32];
+      tc::tmem_ld32x2(tS, tS + 32, v0, v1);
 #pragma unroll
-    for (int c4 = 0; c4 < 8; ++c4) {
-      const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
-      const float4 f1 = make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
-      reinterpret_cast<float4*>(dst)[c4] = f0;
-      reinterpret_cast<float4*>(dst + 32)[c4] = f1;
-      if (ck) {
-        reinterpret_cast<float4*>(ck)[c4] = f0;
-        reinterpret_cast<float4*>(ck + 32)[c4] = f1;
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+        const float4 f1 = make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
+        reinterpret_cast<float4*>(dst)[c4] = f0;
+        reinterpret_cast<float4*>(dst + 32)[c4] = f1;
+        if (ck) {
+          reinterpret_cast<float4*>(ck)[c4] = f0;
+          reinterpret_cast<float4*>(ck + 32)[c4] = f1;
+        }
       }
     }
   } else {
-    // a wait ran out: report it, give the tensor core one more bounded wait
-    // for each product it may still hold, then release the tensor memory
+    // a wait ran out: report it, give the tensor core and the copy engine one
+    // more bounded wait for each piece of work they may still hold, then
+    // release the tensor memory
     if (tid == 0) set_error(p.err, GDN_ERR_TIMEOUT);
+    const uint32_t par = (uint32_t)(c & 1);
 #pragma unroll 1
     for (int b = 0; b < 4; ++b)
-      if (issued & (1u << b)) tc::mbar_wait_bounded(mbar + b, (uint32_t)(c & 1), kPfWait);
+      if (issued & (1u << b)) tc::mbar_wait_bounded(mbar + b, par, kPfWait);
+    if (worker && x_issued >= 0) tc::mbar_wait_bounded(mbar + 4, (uint32_t)(x_issued & 1), kPfWait);
     cp_async_wait<0>();
   }
+  if (tid == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, kPfCols);
@@ -686,10 +750,40 @@ bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block
 
 cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
+  CUtensorMap xmap, omap;
+  memset(&xmap, 0, sizeof(xmap));
+  memset(&omap, 0, sizeof(omap));
+  int tma_out = 0;
+  if (p.total_rows > 0) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    // x as [rows][conv_dim] bf16; a box is 128 channels x 67 rows
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)p.conv_dim, (cuuint64_t)p.total_rows};
+      const cuuint64_t strides[1] = {(cuuint64_t)p.conv_dim * 2};
+      const cuuint32_t box[2] = {(cuuint32_t)kPfD, (cuuint32_t)kPfXRows};
+      if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    // o as [rows][Hv * dv] bf16; a box is one head's 128 channels x 64 rows
+    // (used for full chunks when o is 16-byte aligned)
+    if ((reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
+      const cuuint64_t dims[2] = {(cuuint64_t)p.Hv * kPfD, (cuuint64_t)p.total_rows};
+      const cuuint64_t strides[1] = {(cuuint64_t)p.Hv * kPfD * 2};
+      const cuuint32_t box[2] = {(cuuint32_t)kPfD, (cuuint32_t)kPfC};
+      if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.o, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+        tma_out = 1;
+    }
+  }
   const size_t smem = PfSmem::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_prefill_kernel<<<dim3(p.Hv, p.num_seqs), kPfThreads, smem, st>>>(p);
+  tc_prefill_kernel<<<dim3(p.Hv, p.num_seqs), kPfThreads, smem, st>>>(p, xmap, omap, tma_out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // conv windows of every crossed boundary and of the final slot
