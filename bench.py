@@ -43,11 +43,19 @@ METRIC = "GDN prefill tokens/s/layer; decode & replay-flush µs/layer; % of TC/H
 PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
-# DRAM bytes (read + write) of one prefill scan launch, from an ncu capture of
-# the current scan kernel at 4 x 2,048 tokens (profiles/
-# scan_kernel_prefill_27b_4x2048.md: 342.0 + 109.5 MB), scaled by 4 to the
+# DRAM bytes (read + write) of one tensor-core prefill launch, from an ncu
+# capture of the current kernel at 4 x 2,048 tokens (profiles/
+# tc_prefill_kernel_27b_4x2048.md: 173.6 + 95.4 MB), scaled by 4 to the
 # 4 x 8,192 launch (the traffic is per token).  None once the kernel changes.
-SCAN_TRAFFIC_PER_LAUNCH = (342.006528e6 + 109.522176e6) * 4
+PREFILL_TRAFFIC_PER_LAUNCH = (173.583104e6 + 95.399680e6) * 4
+# Algorithmic flops of the chunk form per token and value head (chunk C = 64,
+# d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
+# three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
+# chunk (M = 128 throughout): [K^;Q^]K^T 128x64x128, S0[K^;Q^]^T 128x128x128,
+# R T^T 128x64x64, U^T (K^T dec)^T 128x128x64, U^T P^T 128x64x64.
+CHUNK_FLOPS_PER_TOKEN_HEAD = 2 * (64 * (3 * 128 + 2 * 128) + 3 * 128 * 128)
+EXECUTED_FLOPS_PER_TOKEN_HEAD = 3 * 2 * (128 * 64 * 128 + 128 * 128 * 128 + 128 * 64 * 64 + 128 * 128 * 64
+                                         + 128 * 64 * 64) / 64
 DEC_SEQS, DEC_LAYERS = 256, 24
 REP_REQS, REP_ROWS, REP_LAYERS = 16, 16, 24
 
@@ -195,10 +203,10 @@ class PrefillWork:
     def d2h_bytes(self):
         return self.o_host.numel() * self.o_host.element_size()
 
-    # roofline inputs for the scan kernel
+    # roofline inputs for the prefill kernel
     def algorithmic_flops(self):
-        sh = self.sh
-        return 6.0 * sh.head_dim_k * sh.head_dim_v * sh.num_v_heads * self.tokens
+        """The chunk form's flops for every token of every value head."""
+        return float(CHUNK_FLOPS_PER_TOKEN_HEAD) * self.sh.num_v_heads * self.tokens
 
     def algorithmic_bytes(self):
         sh = self.sh
@@ -510,8 +518,7 @@ def main():
 
     peaks, peak_kind = _peaks()
     clocks = clk.summary()
-    sm_max = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    alu_peak = 2.0 * 128 * 152 * sm_max * 1e6 / 1e12      # fp32 FMA TFLOP/s
+    tc_peak = peaks["bf16_tflops"]                          # dense bf16, measured (burst)
     achieved = pre.algorithmic_flops() / (pre_ms * 1e-3) / 1e12
     dec_gbs = dec.bytes_per_layer() / (dec_ms / DEC_LAYERS * 1e-3) / 1e9
     fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
@@ -531,17 +538,25 @@ def main():
         "flush_us_per_layer": 1000.0 * fl_ms / REP_LAYERS,
         "decode_hbm_gbs": dec_gbs, "flush_hbm_gbs": fl_gbs,
         "decode_hbm_frac": dec_gbs / peaks["hbm_gbs"], "flush_hbm_frac": fl_gbs / peaks["hbm_gbs"],
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": achieved / alu_peak,
-                     "traffic": SCAN_TRAFFIC_PER_LAUNCH if args.seq_len == SEQ_LEN else None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak,
+                     "traffic": PREFILL_TRAFFIC_PER_LAUNCH if args.seq_len == SEQ_LEN else None,
                      "traffic_note": "bytes per launch, scaled from a 4 x 2048 capture",
-                     "kernel": "scan_kernel<128,128,2,bf16,bf16,prefill>",
-                     "peak_kind": f"fp32 FMA 152 SMs x 128 lanes x 2 x {sm_max:.0f} MHz",
+                     "kernel": "tc_prefill_kernel",
+                     "work": "chunk-form flops (C 64) per token and v-head x tokens x heads; "
+                             "executed as 3 bf16 passes",
+                     "executed_tflops": achieved * EXECUTED_FLOPS_PER_TOKEN_HEAD / CHUNK_FLOPS_PER_TOKEN_HEAD,
+                     "peak_kind": f"dense bf16 {peak_kind} (burst)",
+                     "algorithmic_bytes_per_launch": pre.algorithmic_bytes(),
+                     "hbm_gbs_achieved": pre.algorithmic_bytes() / (pre_ms * 1e-3) / 1e9,
                      "hbm_peak_kind": peak_kind},
         "e2e": {"value": job_throughput(pre.tokens, world, e2e_ms), "unit": "tokens/s/layer",
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
                 "scope": "prefill part of the step"},
-        "gpu_launches": args.steps * (3 + DEC_LAYERS + 9 * REP_LAYERS),
+        # per step: prefill 2 (chunk kernel, windows); decode 1 per layer; replay
+        # per layer 5 (conv, scan, log append, log_len, rollback) + flush 3
+        # (tensor-core update, windows, log_len)
+        "gpu_launches": args.steps * (2 + DEC_LAYERS + 8 * REP_LAYERS),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -71,6 +71,10 @@ size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens) {
   (void)num_seqs;
   if (gdn_conv_dim(desc) <= 0 || total_tokens < 0) return 0;
+  // the tensor-core prefill computes the conv in the kernel: no scratch
+  if (tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                           desc->block_size))
+    return 0;
   return scan_workspace_bytes(total_tokens, (int)gdn_conv_dim(desc), desc->num_qk_heads,
                               desc->num_v_heads);
 }
@@ -108,8 +112,7 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
       if (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages) return GDN_ERR_PAGE_RANGE;
   if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
-  if (a->total_tokens > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
-    return GDN_ERR_WORKSPACE;
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
   p.num_seqs = a->num_seqs;
   p.conv_w = a->conv_w;
@@ -125,7 +128,7 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.g = a->g;
   p.beta = a->beta;
   p.total_rows = a->total_tokens;
-  bind_workspace(p, workspace, a->total_tokens);
+  if (need > 0) bind_workspace(p, workspace, a->total_tokens);
   const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
   return cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
                                     desc->out_dtype, static_cast<cudaStream_t>(stream)));

@@ -232,9 +232,12 @@ typedef struct gdn_prefill_args {
 } gdn_prefill_args;
 
 /* Device workspace bytes gdn_prefill_chunked needs for a call with
- * total_tokens tokens: the SiLU(conv) rows of every token in fp32 (computed
- * once and shared by every head that reads them), the q / k norm factors and
- * the gates.  The caller allocates it (256-byte aligned); its contents are
+ * total_tokens tokens.  Layers that take the tensor-core chunk kernel
+ * (dk = dv = 128, bf16 in and out, block_size a multiple of 64) compute the
+ * conv inside it and need none: 0, and the workspace argument may be NULL.
+ * Other layers run a conv pre-pass whose SiLU(conv) rows (fp32, computed once
+ * and shared by every head that reads them), q / k norm factors and gates
+ * live here.  The caller allocates it (256-byte aligned); its contents are
  * scratch, overwritten by every call, so calls that share a workspace must
  * not overlap on the GPU.  0 for a malformed desc. */
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
@@ -255,8 +258,10 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
  * scratch is a fixed array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) in this
  * library's device memory, held by every GPU that loads the library until the
  * process exits.  Calls whose gdn_prefill_workspace_size exceeds it return
- * GDN_ERR_WORKSPACE and launch nothing (at the 27B shape, about 1,600 tokens
- * per call; split longer prefills at block boundaries, gdn_chunk_end).
+ * GDN_ERR_WORKSPACE and launch nothing (layers on the conv pre-pass path:
+ * about 3,200 tokens per call at d = 64 with 16 / 48 heads; split longer
+ * prefills at block boundaries, gdn_chunk_end).  Layers on the tensor-core
+ * path need no scratch and have no limit.
  * The entry point calls no cudaMalloc, cudaFree or other allocating routine.
  * The first call on each device looks up the array's device address with
  * cudaGetSymbolAddress (that device current); make that first call before

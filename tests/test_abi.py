@@ -82,11 +82,16 @@ def test_pool_too_small_or_misaligned_is_rejected():
 
 
 def test_workspace_is_required_and_sized():
-    sh = inputs.QWEN27B
-    need = gdn.gdn_prefill_workspace_size(sh, 4, 4 * 8192)
-    # SiLU(conv) rows in fp32 plus norm factors and gates
-    assert need >= 4 * 8192 * (sh.conv_dim + 2 * sh.num_qk_heads + 2 * sh.num_v_heads) * 4
-    assert need % 256 == 0
+    # the tensor-core prefill (d 128, bf16, block a multiple of 64) needs none
+    assert gdn.gdn_prefill_workspace_size(inputs.QWEN27B, 4, 4 * 8192) == 0
+    assert gdn.gdn_prefill_workspace_size(inputs.QWEN4B, 4, 4 * 8192) == 0
+    # the conv pre-pass path: SiLU(conv) rows in fp32 plus norm factors and gates
+    for sh in (inputs.with_(inputs.QWEN27B, head_dim_k=64, head_dim_v=64),
+               inputs.with_(inputs.QWEN27B, block_size=784),
+               inputs.with_(inputs.QWEN27B, in_dtype=inputs.F32, out_dtype=inputs.F32)):
+        need = gdn.gdn_prefill_workspace_size(sh, 4, 4 * 8192)
+        assert need >= 4 * 8192 * (sh.conv_dim + 2 * sh.num_qk_heads + 2 * sh.num_v_heads) * 4
+        assert need % 256 == 0
     assert gdn.gdn_replay_workspace_size(inputs.QWEN4B, 16) >= 16 * 32 * inputs.QWEN4B.conv_dim * 4
     lib = gdn.load_library()
     desc = gdn.make_desc(inputs.TINY)
