@@ -46,8 +46,8 @@ cudaError_t launch_replay_rollback(int32_t* log_len, const int32_t* accepted, in
 cudaError_t launch_decode(const DecodeParams& p, int dk, int dv, int in_dtype, int out_dtype,
                           cudaStream_t st);
 cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
-// Tensor-core replay flush (dk = dv = 128): the state update only; the window
-// and log_len passes follow it.
+// Tensor-core replay flush (dk = dv = 128, bf16): the state update and the v
+// windows, then a per-request pass for the q / k windows and log_len.
 bool tc_flush_supported(int dk, int dv, int in_dtype);
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on libcuda); nullptr if the driver lacks it.

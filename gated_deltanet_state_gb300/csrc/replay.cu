@@ -53,18 +53,9 @@ cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dty
 cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtype, int out_dtype,
                                 cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
-  if (tc_flush_supported(dk, dv, in_dtype)) {
-    // tensor-core state update, then the window pass and the log reset
-    cudaError_t e = launch_tc_flush(p, in_dtype, st);
-    if (e != cudaSuccess) return e;
-    const dim3 wgrid((p.conv_dim + 255) / 256, p.num_seqs);
-    if (in_dtype == GDN_BF16) window_kernel<__nv_bfloat16, kFlush><<<wgrid, 256, 0, st>>>(p);
-    else window_kernel<float, kFlush><<<wgrid, 256, 0, st>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    log_len_kernel<kFlush><<<(p.num_seqs + 255) / 256, 256, 0, st>>>(p);
-    return cudaGetLastError();
-  }
+  // tensor-core state update and v windows, then the q / k windows and the
+  // log reset
+  if (tc_flush_supported(dk, dv, in_dtype)) return launch_tc_flush(p, in_dtype, st);
   const int64_t max_len = GDN_REPLAY_LOG_SLOTS;
   GDN_SCAN_DISPATCH(kFlush)
 }

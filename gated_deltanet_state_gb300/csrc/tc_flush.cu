@@ -25,7 +25,7 @@
 
 namespace gdn {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;   // two threads per state row (64 columns each)
 constexpr int kTcD = 128;             // dk = dv
 constexpr int kTcMaxRows = GDN_REPLAY_LOG_SLOTS;
 constexpr uint32_t kTcCols = 256;     // tensor-memory columns: D1 at 0 (32), D2 at 32 (128), V at 160 (32)
@@ -34,7 +34,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 
 // Shared-memory plan (byte offsets from a 1024-byte aligned base).
 struct TcSmem {
-  static constexpr uint32_t A1 = 0;                    // S0 hi | lo: 2 x [2 kb][128][64] bf16 (64 KB)
+  static constexpr uint32_t A1 = 0;                    // S0 fp32 (TMA) | S0 hi | lo: 2 x [2 kb][128][64] bf16 (64 KB)
   static constexpr uint32_t A1_LO = 32768;
   static constexpr uint32_t A2 = 0;                    // W hi | lo: 2 x [128][64] bf16 (reuses A1)
   static constexpr uint32_t A2_LO = 16384;
@@ -43,11 +43,11 @@ struct TcSmem {
   static constexpr uint32_t B1 = 65536;                // K^ hi | lo: 2 x [2 kb][32][64] bf16 (16 KB)
   static constexpr uint32_t B1_LO = 65536 + 8192;
   static constexpr uint32_t XLOG = B1;                 // staging: bf16 [32][k 128 | v 128] log rows
-  static constexpr uint32_t KF = 81920;                // K^ fp32 [32][128] (16 KB)
-  static constexpr uint32_t AM = KF + 16384;           // fp32 [32][32]: A (strictly lower)
+  static constexpr uint32_t KF = 81920;                // K^ fp32 [32][132] (rows padded: distinct banks)
+  static constexpr int KF_LD = 132;
+  static constexpr uint32_t AM = KF + 32 * KF_LD * 4;  // fp32 [32][32]: A (strictly lower)
   static constexpr uint32_t XWIN = AM;                 // staging: bf16 [3][256] window rows
-  static constexpr uint32_t PART = AM + 4096;          // fp32 [4][32]: partial squared norms
-  static constexpr uint32_t GATE = PART + 512;         // fp32 [5][32]: G, gam, b, fk, exp(G_n-1 - G)
+  static constexpr uint32_t GATE = AM + 4096;          // fp32 [5][32]: G, gam, b, fk, exp(G_n-1 - G)
   static constexpr uint32_t MBAR = GATE + 640;         // uint64 mbarrier: MMA completion
   static constexpr uint32_t MBAR_TMA = MBAR + 8;       // uint64 mbarrier: state tile arrival
   static constexpr uint32_t TSLOT = MBAR_TMA + 8;      // uint32 tensor-memory base
@@ -65,12 +65,32 @@ __device__ __forceinline__ uint32_t state_smem_offset(int row, int col) {
   return (uint32_t)((col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) + ((col & 3) << 2));
 }
 
+// Eight fp32 values as bf16 hi and lo parts (x ~= hi + lo), converted in
+// pairs, each part stored as one 16-byte vector.
+__device__ __forceinline__ void flush_split8(uint8_t* hi, uint8_t* lo, const float* e) {
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(e[2 * u] - hf.x, e[2 * u + 1] - hf.y);
+    hw[u] = *reinterpret_cast<const uint32_t*>(&hb);
+    lw[u] = *reinterpret_cast<const uint32_t*>(&lb);
+  }
+  *reinterpret_cast<uint4*>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
 template <int NMAX>
 __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtensorMap* tmap, int h, int r,
                                               int32_t page, int n) {
   using TIN = __nv_bfloat16;
   constexpr int D = kTcD;
+  constexpr int LD = TcSmem::KF_LD;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;                 // state row / channel of this thread
+  const int half = tid >> 7;                 // which 64 columns (and which conv channel) it takes
+  const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -88,29 +108,8 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
   TIN* xlog = reinterpret_cast<TIN*>(sm + TcSmem::XLOG);
   TIN* xwin = reinterpret_cast<TIN*>(sm + TcSmem::XWIN);
 
-  // (0) async copies of this CTA's pre-conv rows (k | v channels: the window's
-  // three rows and the n logged rows) and of the gates
-  const int G = p.Hv / p.Hqk, jq = h / G;
-  const int ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
-  {
-    const TIN* win = page_window<TIN>(p.pool, page);
-    const TIN* lx = reinterpret_cast<const TIN*>(p.log_x) + (int64_t)r * kTcMaxRows * p.conv_dim;
-    constexpr int RC = 2 * D / 8;                     // 16-byte chunks per staged row
-    for (int i = tid; i < (3 + n) * RC; i += kTcThreads) {
-      const int row = i / RC, col = (i - row * RC) * 8;
-      const int ch = col < D ? ck0 + col : cv0 + col - D;
-      const TIN* src = row < 3 ? win + (int64_t)row * p.conv_dim + ch : lx + (int64_t)(row - 3) * p.conv_dim + ch;
-      TIN* dst = row < 3 ? xwin + row * 2 * D + col : xlog + (row - 3) * 2 * D + col;
-      cp_async16(dst, src, 16);
-    }
-    for (int i = tid; i < 2 * n; i += kTcThreads) {
-      const int row = i >> 1;
-      const int64_t lrow = (int64_t)r * kTcMaxRows + row;
-      cp_async4((i & 1) ? bs + row : Gs + row, ((i & 1) ? p.log_beta : p.log_g) + lrow * p.Hv + h, 4);
-    }
-    cp_async_commit();
-  }
-
+  // (0) the state, 64 KB of fp32, starts arriving by four TMA tile loads into
+  // the A1 region; everything up to step (5) needs no state and overlaps it
   if (warp == 0) {
     tc::tmem_alloc(tslot, kTcCols);
     tc::tmem_relinquish();
@@ -119,18 +118,165 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
     tc::mbar_init(mbar, 1);
     tc::mbar_init(mbar_tma, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    // (1) the state, 64 KB of fp32, arrives by four TMA tile loads into the A1 region
     tc::mbar_expect_tx(mbar_tma, D * D * 4);
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb)
       tc::tma_load_3d(sm + TcSmem::A1 + cb * 16384, tmap, 32 * cb, h * D, page, mbar_tma);
   }
-
+  // (1) async copies of this CTA's pre-conv rows (k | v channels: the
+  // window's three rows and the log's NMAX rows, zeros past n) and of the
+  // gates (zeros past n)
+  const int G = p.Hv / p.Hqk, jq = h / G;
+  const int ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
+  TIN* win = page_window<TIN>(p.pool, page);
+  {
+    const TIN* lx = reinterpret_cast<const TIN*>(p.log_x) + (int64_t)r * kTcMaxRows * p.conv_dim;
+    constexpr int RC = 2 * D / 8;                     // 16-byte chunks per staged row
+    for (int i = tid; i < (3 + NMAX) * RC; i += kTcThreads) {
+      const int srow = i / RC, col = (i - srow * RC) * 8;
+      const int ch = col < D ? ck0 + col : cv0 + col - D;
+      const bool in = srow < 3 + n;
+      const TIN* src = srow < 3 ? win + (int64_t)srow * p.conv_dim + ch
+                                : lx + (int64_t)(in ? srow - 3 : 0) * p.conv_dim + ch;
+      TIN* dst = srow < 3 ? xwin + srow * 2 * D + col : xlog + (srow - 3) * 2 * D + col;
+      cp_async16(dst, src, in ? 16 : 0);
+    }
+    if (tid < 2 * NMAX) {
+      const int lr = tid >> 1;
+      const bool in = lr < n;
+      const int64_t lrow = (int64_t)r * kTcMaxRows + (in ? lr : 0);
+      cp_async4((tid & 1) ? bs + lr : Gs + lr, ((tid & 1) ? p.log_beta : p.log_g) + lrow * p.Hv + h, in ? 4 : 0);
+    }
+    cp_async_commit();
+  }
+  // conv taps: the first half of the CTA takes k channel `row`, the second v channel `row`
+  const float4 w = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)((half ? cv0 : ck0) + row) * kConvK);
+  cp_async_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
-  const uint32_t tlane = (uint32_t)(warp * 32) << 16;
+
+  // (2) conv + SiLU over all NMAX rows (zero inputs past n), masked to zero
+  // past n: k channel -> kf; v channel -> tensor memory (lane = state row),
+  // and its new conv window (the last three rows of window || log), written
+  // to the page here: this CTA alone reads this head's v channels
+  {
+    const TIN* xw = xwin + half * D + row;
+    const TIN* xl = xlog + half * D + row;
+    float x[NMAX + 3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) x[i] = to_f32(xw[i * 2 * D]);
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) x[i + 3] = to_f32(xl[i * 2 * D]);
+    float y[32];
+#pragma unroll
+    for (int i = 0; i < NMAX; ++i) {
+      float z = w.x * x[i];
+      z = fmaf(w.y, x[i + 1], z);
+      z = fmaf(w.z, x[i + 2], z);
+      z = fmaf(w.w, x[i + 3], z);
+      y[i] = (i < n ? 1.f : 0.f) * silu_fast(z);
+    }
+    if (half == 0) {
+#pragma unroll
+      for (int i = 0; i < NMAX; ++i) kf[i * LD + row] = y[i];
+#pragma unroll
+      for (int i = NMAX; i < kTcMaxRows; ++i) kf[i * LD + row] = 0.f;
+    } else {
+#pragma unroll
+      for (int i = NMAX; i < 32; ++i) y[i] = 0.f;
+      tc::tmem_st32(tbase + tlane + kColV, y);
+      TIN* wdst = win + cv0 + row;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int t = n + j;   // position in window || log
+        wdst[(int64_t)j * p.conv_dim] = t < 3 ? xw[t * 2 * D] : xl[(t - 3) * 2 * D];
+      }
+      tc::tmem_st_wait();
+    }
+  }
+  __syncthreads();
+  // (3) squared norms of the k rows: warp w reduces rows w, w+8, ...
+  // (interleaved, fixed order); cumulative log decay and the decay factors
+  // (gates are zero past n)
+  {
+    constexpr int RPW = NMAX / 8;
+    float ss[RPW];
+#pragma unroll
+    for (int it = 0; it < RPW; ++it) {
+      const int i = warp + 8 * it;
+      float a = 0.f;
+#pragma unroll
+      for (int m = 0; m < D / 32; ++m) {
+        const float y = kf[i * LD + lane + 32 * m];
+        a = fmaf(y, y, a);
+      }
+      ss[it] = a;
+    }
+#pragma unroll
+    for (int it = 0; it < RPW; ++it) ss[it] = warp_sum(ss[it]);
+    if (lane == 0) {
+#pragma unroll
+      for (int it = 0; it < RPW; ++it) fk[warp + 8 * it] = 1.0f / sqrtf(ss[it] + p.eps);
+    }
+  }
+  if (warp == 1) {
+    float g = lane < NMAX ? Gs[lane] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, g, o);
+      if (lane >= o) g += t;
+    }
+    const float gn = __shfl_sync(0xffffffffu, g, n - 1);
+    if (lane < NMAX) { Gs[lane] = g; gam[lane] = expf(g); dec[lane] = expf(gn - g); }
+  }
+  __syncthreads();
+
+  // (4) k^ = k / |k| (channel `row`, rows of this thread's half) and
+  // B1 = K^ hi / lo (rows i < NMAX)
+  const int NB1 = NMAX;
+  {
+    constexpr int HR = NMAX / 2;
+    float kv[HR];
+#pragma unroll
+    for (int u = 0; u < HR; ++u) kv[u] = kf[(half * HR + u) * LD + row] * fk[half * HR + u];
+#pragma unroll
+    for (int u = 0; u < HR; ++u) {
+      const int i = half * HR + u;
+      kf[i * LD + row] = kv[u];
+      __nv_bfloat16 hi, lo;
+      tc::split_bf16(kv[u], hi, lo);
+      const uint32_t off = tc::sw128_offset(i, row, NB1);
+      *reinterpret_cast<__nv_bfloat16*>(sm + TcSmem::B1 + off) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(sm + TcSmem::B1_LO + off) = lo;
+    }
+  }
+  __syncthreads();
+  // A_ij = b_i exp(G_i - G_j) k^_i.k^_j for j < i < NMAX (rows past n are
+  // zero), one pair per thread and round; padded rows put the two operand
+  // rows of a warp's lanes on distinct banks
+  for (int q = tid; q < NMAX * (NMAX - 1) / 2; q += kTcThreads) {
+    int i = (int)((1.0f + sqrtf(1.0f + 8.0f * (float)q)) * 0.5f);
+    if (i * (i - 1) / 2 > q) --i;
+    if ((i + 1) * i / 2 <= q) ++i;
+    const int j = q - i * (i - 1) / 2;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D; c += 8) {
+      const float4 x0 = *reinterpret_cast<const float4*>(kf + i * LD + c);
+      const float4 y0 = *reinterpret_cast<const float4*>(kf + j * LD + c);
+      const float4 x1 = *reinterpret_cast<const float4*>(kf + i * LD + c + 4);
+      const float4 y1 = *reinterpret_cast<const float4*>(kf + j * LD + c + 4);
+      a0 = fmaf(x0.x, y0.x, a0); a1 = fmaf(x0.y, y0.y, a1); a2 = fmaf(x0.z, y0.z, a2); a3 = fmaf(x0.w, y0.w, a3);
+      a0 = fmaf(x1.x, y1.x, a0); a1 = fmaf(x1.y, y1.y, a1); a2 = fmaf(x1.z, y1.z, a2); a3 = fmaf(x1.w, y1.w, a3);
+    }
+    am[i * 32 + j] = bs[i] * __expf(fminf(Gs[i] - Gs[j], 0.f)) * ((a0 + a1) + (a2 + a3));
+  }
+
+  // (5) the state: columns [64 half, +64) of row `row` into registers; once
+  // every thread holds its part the region takes the bf16 hi / lo operand
+  // A1, and gam_{n-1} S0 goes to the D2 columns
   bool ok = tc::mbar_wait_bounded(mbar_tma, 0, kWaitCycles);
   ok = __syncthreads_and(ok);
   if (!ok) {   // the state never arrived: report, give the copy one more bounded wait, leave
@@ -140,108 +286,26 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
     if (warp == 0) tc::tmem_dealloc(tbase, kTcCols);
     return;
   }
-  // state row `tid` (= tensor-memory lane tid) into registers; once every
-  // thread holds its row the region takes the bf16 hi / lo operand A1
-  float sv[D];
-#pragma unroll
-  for (int c = 0; c < D; c += 4) {
-    const float4 f = *reinterpret_cast<const float4*>(sm + TcSmem::A1 + state_smem_offset(tid, c));
-    sv[c] = f.x; sv[c + 1] = f.y; sv[c + 2] = f.z; sv[c + 3] = f.w;
-  }
-  __syncthreads();
-  // bf16 hi / lo into A1 (for D1 = S0 K^T); raw S0 into the D2 columns
-#pragma unroll
-  for (int c8 = 0; c8 < D / 8; ++c8) {
-    __nv_bfloat16 hi[8], lo[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) tc::split_bf16(sv[8 * c8 + e], hi[e], lo[e]);
-    const uint32_t off = tc::sw128_offset(tid, 8 * c8, D);
-    *reinterpret_cast<uint4*>(sm + TcSmem::A1 + off) = *reinterpret_cast<const uint4*>(hi);
-    *reinterpret_cast<uint4*>(sm + TcSmem::A1_LO + off) = *reinterpret_cast<const uint4*>(lo);
-  }
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float v[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = sv[32 * q + c];
-    tc::tmem_st32(tbase + tlane + 32 + 32 * q, v);
-  }
-  tc::tmem_st_wait();
-
-  // (2) conv + SiLU of k channel `tid` (qk head of h) and v channel `tid` (head h)
-  cp_async_wait<0>();
-  __syncthreads();
-  const float4 wk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(ck0 + tid) * kConvK);
-  const float4 wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + tid) * kConvK);
-  float k0 = to_f32(xwin[tid]), k1 = to_f32(xwin[2 * D + tid]), k2 = to_f32(xwin[4 * D + tid]);
-  float v0 = to_f32(xwin[D + tid]), v1 = to_f32(xwin[3 * D + tid]), v2 = to_f32(xwin[5 * D + tid]);
-  float vr[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) vr[i] = 0.f;
-#pragma unroll
-  for (int i = 0; i < NMAX; ++i) {
-    const float xk = i < n ? to_f32(xlog[i * 2 * D + tid]) : 0.f;
-    const float xv = i < n ? to_f32(xlog[i * 2 * D + D + tid]) : 0.f;
-    float zk = wk.x * k0;
-    zk = fmaf(wk.y, k1, zk);
-    zk = fmaf(wk.z, k2, zk);
-    zk = fmaf(wk.w, xk, zk);
-    float zv = wv.x * v0;
-    zv = fmaf(wv.y, v1, zv);
-    zv = fmaf(wv.z, v2, zv);
-    zv = fmaf(wv.w, xv, zv);
-    k0 = k1; k1 = k2; k2 = xk;
-    v0 = v1; v1 = v2; v2 = xv;
-    kf[i * D + tid] = i < n ? silu_fast(zk) : 0.f;
-    vr[i] = i < n ? silu_fast(zv) : 0.f;
-  }
-  for (int i = NMAX; i < kTcMaxRows; ++i) kf[i * D + tid] = 0.f;
-  tc::tmem_st32(tbase + tlane + kColV, vr);   // park v (lane = state row) until the epilogue
-  tc::tmem_st_wait();
-  __syncthreads();
-  // squared norms of the k rows: warp w reduces rows w, w+4, ... (fixed order)
-  for (int i = warp; i < n; i += kTcThreads / 32) {
-    float ss = 0.f;
-#pragma unroll
-    for (int m = 0; m < D / 32; ++m) {
-      const float y = kf[i * D + lane + 32 * m];
-      ss = fmaf(y, y, ss);
-    }
-    ss = warp_sum(ss);
-    if (lane == 0) fk[i] = 1.0f / sqrtf(ss + p.eps);
-  }
-  if (warp == 1) {   // cumulative log decay and the decay factors
-    float g = lane < n ? Gs[lane] : 0.f;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, g, o);
-      if (lane >= o) g += t;
-    }
-    const float gn = __shfl_sync(0xffffffffu, g, n - 1);
-    if (lane < n) { Gs[lane] = g; gam[lane] = expf(g); dec[lane] = expf(gn - g); }
-  }
-  __syncthreads();
-
-  // (3) k^ = k / |k| (this thread's column); B1 = K^ hi / lo (rows i < NB1);
-  // D2 <- gam_{n-1} * S0 in tensor memory
-  for (int i = 0; i < n; ++i) kf[i * D + tid] *= fk[i];
-  const int NB1 = n <= 16 ? 16 : 32;
-  for (int i = 0; i < NB1; ++i) {
-    __nv_bfloat16 hi, lo;
-    tc::split_bf16(i < n ? kf[i * D + tid] : 0.f, hi, lo);
-    const uint32_t off = tc::sw128_offset(i, tid, NB1);
-    *reinterpret_cast<__nv_bfloat16*>(sm + TcSmem::B1 + off) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(sm + TcSmem::B1_LO + off) = lo;
-  }
   {
-    const float gN = gam[n - 1];
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      float v[32];
-      tc::tmem_ld32(tbase + tlane + 32 + 32 * q, v);
+    float sv[64];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) v[c] *= gN;
-      tc::tmem_st32(tbase + tlane + 32 + 32 * q, v);
+    for (int c = 0; c < 64; c += 4) {
+      const float4 f = *reinterpret_cast<const float4*>(sm + TcSmem::A1 + state_smem_offset(row, 64 * half + c));
+      sv[c] = f.x; sv[c + 1] = f.y; sv[c + 2] = f.z; sv[c + 3] = f.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8) {
+      const uint32_t off = tc::sw128_offset(row, 64 * half + 8 * c8, D);
+      flush_split8(sm + TcSmem::A1 + off, sm + TcSmem::A1_LO + off, sv + 8 * c8);
+    }
+    const float gN = gam[n - 1];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float v[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[c] = gN * sv[32 * q + c];
+      tc::tmem_st32(tbase + tlane + 32 + 64 * half + 32 * q, v);
     }
     tc::tmem_st_wait();
   }
@@ -250,7 +314,7 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
   __syncthreads();
   tc::fence_after_sync();
 
-  // (4) D1 = S0 K^T on the tensor cores (three bf16 passes, K = 128)
+  // (6) D1 = S0 K^T on the tensor cores (three bf16 passes, K = 128)
   if (tid == 0) {
     const uint32_t idesc = tc::idesc_bf16_f32(D, NB1);
     for (int pass = 0; pass < 3; ++pass) {
@@ -265,61 +329,41 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
     tc::mma_commit(mbar);
   }
 
-  // (5) meanwhile: A_ij = b_i exp(G_i - G_j) k^_i.k^_j for j < i < n
-  for (int e = tid; e < n * n; e += kTcThreads) {
-    const int i = e / n, j = e % n;
-    if (j < i) {
-      float acc = 0.f;
-      for (int c = 0; c < D; c += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(kf + i * D + c);
-        const float4 b4 = *reinterpret_cast<const float4*>(kf + j * D + c);
-        acc = fmaf(a4.x, b4.x, acc);
-        acc = fmaf(a4.y, b4.y, acc);
-        acc = fmaf(a4.z, b4.z, acc);
-        acc = fmaf(a4.w, b4.w, acc);
-      }
-      am[i * 32 + j] = bs[i] * expf(Gs[i] - Gs[j]) * acc;
-    }
-  }
-  __syncthreads();
-
-  // (6) wait for D1; this thread's state row r: R_i = b_i (v_i[r] - gam_i D1[r][i]),
-  // (I + A) U = R by forward substitution, W_i = U_i exp(G_{n-1} - G_i)
+  // (7) wait for D1.  First half, state row `row`: R_i = b_i (v_i[r] - gam_i
+  // D1[r][i]), (I + A) U = R by forward substitution, W_i = U_i exp(G_{n-1} -
+  // G_i) -> A2 row `row`.  Second half: K^T (row = k channel) -> B2.  Both go
+  // to the A1 region, which D1's product no longer reads; the second product
+  // reads K = NMAX <= 32 columns of them.
   ok = tc::mbar_wait_bounded(mbar, 0, kWaitCycles);
   ok = __syncthreads_and(ok);
   tc::fence_after_sync();
   if (ok) {
-    float d1[32], vr[32];
-    tc::tmem_ld32(tbase + tlane, d1);
-    tc::tmem_ld32(tbase + tlane + kColV, vr);
-    float u[NMAX];
+    if (half == 0) {
+      float d1[32], vr[32];
+      tc::tmem_ld32x2(tbase + tlane, tbase + tlane + kColV, d1, vr);
+      float u[NMAX];
 #pragma unroll
-    for (int i = 0; i < NMAX; ++i) u[i] = i < n ? bs[i] * fmaf(-gam[i], d1[i], vr[i]) : 0.f;
+      for (int i = 0; i < NMAX; ++i) u[i] = bs[i] * fmaf(-gam[i], d1[i], vr[i]);
 #pragma unroll
-    for (int j = 0; j < NMAX; ++j)
+      for (int j = 0; j < NMAX; ++j)
 #pragma unroll
-      for (int i = j + 1; i < NMAX; ++i) u[i] = fmaf(-am[i * 32 + j], u[j], u[i]);
-    __nv_bfloat16 whi[64], wlo[64];
+        for (int i = j + 1; i < NMAX; ++i) u[i] = fmaf(-am[i * 32 + j], u[j], u[i]);
 #pragma unroll
-    for (int i = 0; i < NMAX; ++i) tc::split_bf16(i < n ? u[i] * dec[i] : 0.f, whi[i], wlo[i]);
+      for (int i = 0; i < NMAX; ++i) u[i] *= dec[i];
 #pragma unroll
-    for (int i = NMAX; i < 64; ++i) whi[i] = wlo[i] = __float2bfloat16_rn(0.f);
-    // A2 row `tid` = W (K = 64, zeros past n); B2 row `tid` = column tid of K^
-    // (both in the A1 region, which MMA1 no longer reads)
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      const uint32_t off = tc::sw128_offset(tid, 8 * c8, D);
-      *reinterpret_cast<uint4*>(sm + TcSmem::A2 + off) = *reinterpret_cast<const uint4*>(whi + 8 * c8);
-      *reinterpret_cast<uint4*>(sm + TcSmem::A2_LO + off) = *reinterpret_cast<const uint4*>(wlo + 8 * c8);
-      __nv_bfloat16 khi[8], klo[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = 8 * c8 + e;
-        if (i < NMAX) tc::split_bf16(i < n ? kf[i * D + tid] : 0.f, khi[e], klo[e]);
-        else khi[e] = klo[e] = __float2bfloat16_rn(0.f);
+      for (int c8 = 0; c8 < NMAX / 8; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
+        flush_split8(sm + TcSmem::A2 + off, sm + TcSmem::A2_LO + off, u + 8 * c8);
       }
-      *reinterpret_cast<uint4*>(sm + TcSmem::B2 + off) = *reinterpret_cast<const uint4*>(khi);
-      *reinterpret_cast<uint4*>(sm + TcSmem::B2_LO + off) = *reinterpret_cast<const uint4*>(klo);
+    } else {
+      float kt[NMAX];
+#pragma unroll
+      for (int i = 0; i < NMAX; ++i) kt[i] = kf[i * LD + row];
+#pragma unroll
+      for (int c8 = 0; c8 < NMAX / 8; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
+        flush_split8(sm + TcSmem::B2 + off, sm + TcSmem::B2_LO + off, kt + 8 * c8);
+      }
     }
   }
   tc::fence_async_smem();
@@ -327,10 +371,10 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
   __syncthreads();
   tc::fence_after_sync();
 
-  // (7) D2 += W K^ on the tensor cores (three bf16 passes, K = n rounded to 16)
+  // (8) D2 += W K^ on the tensor cores (three bf16 passes, K = NMAX)
   if (ok && tid == 0) {
     const uint32_t idesc = tc::idesc_bf16_f32(D, D);
-    const int nks = (n + 15) / 16;
+    constexpr int nks = NMAX / 16;
     for (int pass = 0; pass < 3; ++pass) {
       const uint32_t a = sbase + (pass == 2 ? TcSmem::A2_LO : TcSmem::A2);
       const uint32_t b = sbase + (pass == 1 ? TcSmem::B2_LO : TcSmem::B2);
@@ -345,18 +389,18 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
   }
   tc::fence_after_sync();
 
-  // (8) D2 = gam_{n-1} S0 + W K^ is the new state: each thread parks its row
-  // in the A1 region (free once the second product has completed) in the
-  // tensor map's swizzled layout, then four TMA tile stores write it back
+  // (9) D2 = gam_{n-1} S0 + W K^ is the new state: each thread parks its 64
+  // columns in the A1 region (free once the second product has completed) in
+  // the tensor map's swizzled layout, then four TMA tile stores write it back
   if (ok) {
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      float d2[32];
-      tc::tmem_ld32(tbase + tlane + 32 + 32 * q, d2);
+    float d2[32], d3[32];
+    tc::tmem_ld32x2(tbase + tlane + 32 + 64 * half, tbase + tlane + 64 + 64 * half, d2, d3);
 #pragma unroll
-      for (int c = 0; c < 32; c += 4)
-        *reinterpret_cast<float4*>(sm + TcSmem::A1 + state_smem_offset(tid, 32 * q + c)) =
-            make_float4(d2[c], d2[c + 1], d2[c + 2], d2[c + 3]);
+    for (int c = 0; c < 32; c += 4) {
+      *reinterpret_cast<float4*>(sm + TcSmem::A1 + state_smem_offset(row, 64 * half + c)) =
+          make_float4(d2[c], d2[c + 1], d2[c + 2], d2[c + 3]);
+      *reinterpret_cast<float4*>(sm + TcSmem::A1 + state_smem_offset(row, 64 * half + 32 + c)) =
+          make_float4(d3[c], d3[c + 1], d3[c + 2], d3[c + 3]);
     }
     tc::fence_async_smem();
     __syncthreads();
@@ -364,7 +408,7 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tc::tma_store_3d(tmap, 32 * cb, h * D, page, sm + TcSmem::A1 + cb * 16384);
       tc::bulk_commit();
-      tc::bulk_wait_all();
+      tc::bulk_wait_read();
     }
   } else {
     // a wait ran out: report it, give the tensor core one more bounded wait
@@ -375,6 +419,39 @@ __device__ __forceinline__ void tc_flush_body(const ScanParams& p, const CUtenso
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, kTcCols);
+}
+
+// After the tensor-core flush (which read the k windows and rewrote the v
+// windows): the q and k channels of every request's conv window (the last
+// three rows of window || log), then log_len = 0.  One CTA per request; a
+// thread moves 16-byte chunks (8 channels) and reads a chunk's three source
+// rows before it writes them; log_len is cleared once every thread of the
+// request has read it.
+constexpr int kQkWinThreads = 512;
+__global__ void __launch_bounds__(kQkWinThreads) flush_qk_window_kernel(const ScanParams p) {
+  using TIN = __nv_bfloat16;
+  const int r = blockIdx.x;
+  const int32_t page = p.ckpt_slot[r];
+  const int32_t n = p.log_len[r];
+  if (!page_ok(p.pool, page) || n < 0 || n > kTcMaxRows) return;   // reported by the flush kernel
+  if (n > 0) {
+    TIN* win = page_window<TIN>(p.pool, page);
+    const TIN* lx = reinterpret_cast<const TIN*>(p.log_x) + (int64_t)r * kTcMaxRows * p.conv_dim;
+    const int chunks = 2 * p.Hqk * kTcD / 8;
+    for (int c = threadIdx.x; c < chunks; c += kQkWinThreads) {
+      uint4 keep[kWinRows];
+#pragma unroll
+      for (int j = 0; j < kWinRows; ++j) {
+        const int t = n + j;   // position in window || log
+        const TIN* src = t < kWinRows ? win + (int64_t)t * p.conv_dim : lx + (int64_t)(t - kWinRows) * p.conv_dim;
+        keep[j] = *reinterpret_cast<const uint4*>(src + 8 * c);
+      }
+#pragma unroll
+      for (int j = 0; j < kWinRows; ++j) *reinterpret_cast<uint4*>(win + (int64_t)j * p.conv_dim + 8 * c) = keep[j];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) const_cast<int32_t*>(p.log_len)[r] = 0;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 2) tc_flush_kernel(const ScanParams p,
@@ -428,6 +505,9 @@ cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st) 
   cudaError_t e = cudaFuncSetAttribute(tc_flush_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   tc_flush_kernel<<<dim3(p.Hv, p.num_seqs), kTcThreads, smem, st>>>(p, tmap);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  flush_qk_window_kernel<<<p.num_seqs, kQkWinThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

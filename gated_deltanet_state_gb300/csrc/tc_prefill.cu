@@ -90,8 +90,8 @@ struct PfSmem {
   static constexpr uint32_t XTILE = 17408;            // tile stride (1024-aligned)
   static constexpr uint32_t GT = XS + 2 * XTILE + kPfXRows * kPfD * 2;
   // fp32 [64] each at GT: staged g, staged b, G, gam, dec = exp(G_C - G), b, q factor, k factor
-  static constexpr uint32_t MBAR = GT + 8 * 256;      // mbarriers: K^K^T, S0[K^;Q^]^T, U, S/O, staged rows
-  static constexpr uint32_t TSLOT = MBAR + 40;
+  static constexpr uint32_t MBAR = GT + 8 * 256;      // mbarriers: K^K^T, S0[K^;Q^]^T, U, U^T P^T, staged rows, state update
+  static constexpr uint32_t TSLOT = MBAR + 48;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;     // + alignment slack
 };
@@ -142,7 +142,7 @@ __device__ __forceinline__ void wg1_sync() { asm volatile("bar.sync 1, 128;\n" :
 // second warpgroup.  The 16 x 16 diagonal blocks D_b = (I + A_bb)^{-1} by
 // forward substitution (a column per thread), then the blocks below them in
 // order of distance from the diagonal: T_pq = -D_p X, X = sum_{k=q}^{p-1}
-// A_pk T_kq (four adjacent columns per thread).  tf[i * 64 + j] receives T on
+// A_pk T_kq (a 2 x 4 tile per thread).  tf[i * 64 + j] receives T on
 // and below the diagonal (the blocks above it are left unwritten).
 __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
   if (t < 64) {
@@ -168,54 +168,50 @@ __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
     for (int i = 0; i < 16; ++i) tf[(o + i) * 64 + o + l] = x[i];
   }
   wg1_sync();
+  // every block of a distance level in one round: 32 tiles of 2 rows x 4
+  // columns per 16 x 16 block, one tile per thread
 #pragma unroll
   for (int d = 1; d < 4; ++d) {
-    const int tasks = (4 - d) * 64;
+    const int tasks = (4 - d) * 32;
+    const int q = t >> 5, p = q + d, i2 = 2 * ((t >> 2) & 7), j4 = 4 * (t & 3);
+    if (t < tasks) {
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
 #pragma unroll
-    for (int e0 = 0; e0 < tasks; e0 += 128) {
-      const int e = e0 + t;
-      if (e < tasks) {
-        const int q = e >> 6, p = q + d, i = (e >> 2) & 15, j4 = 4 * (e & 3);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int kk = 0; kk < 16 * d; ++kk) {
-          const int k = 16 * q + kk;
-          const float a = at[k * 64 + 16 * p + i];
-          const float4 b = *reinterpret_cast<const float4*>(tf + k * 64 + 16 * q + j4);
-          acc.x = fmaf(a, b.x, acc.x);
-          acc.y = fmaf(a, b.y, acc.y);
-          acc.z = fmaf(a, b.z, acc.z);
-          acc.w = fmaf(a, b.w, acc.w);
-        }
-        *reinterpret_cast<float4*>(xscr + q * 256 + i * 16 + j4) = acc;
+      for (int kk = 0; kk < 16 * d; ++kk) {
+        const int k = 16 * q + kk;
+        const float2 a = *reinterpret_cast<const float2*>(at + k * 64 + 16 * p + i2);
+        const float4 b = *reinterpret_cast<const float4*>(tf + k * 64 + 16 * q + j4);
+        a0.x = fmaf(a.x, b.x, a0.x); a0.y = fmaf(a.x, b.y, a0.y);
+        a0.z = fmaf(a.x, b.z, a0.z); a0.w = fmaf(a.x, b.w, a0.w);
+        a1.x = fmaf(a.y, b.x, a1.x); a1.y = fmaf(a.y, b.y, a1.y);
+        a1.z = fmaf(a.y, b.z, a1.z); a1.w = fmaf(a.y, b.w, a1.w);
       }
+      *reinterpret_cast<float4*>(xscr + q * 256 + i2 * 16 + j4) = a0;
+      *reinterpret_cast<float4*>(xscr + q * 256 + (i2 + 1) * 16 + j4) = a1;
     }
     wg1_sync();
+    if (t < tasks) {
+      // rows i2, i2 + 1 of D_p, read once (zero above its diagonal, so all 16
+      // terms can be taken)
+      float d0[16], d1[16];
 #pragma unroll
-    for (int e0 = 0; e0 < tasks; e0 += 128) {
-      const int e = e0 + t;
-      if (e < tasks) {
-        const int q = e >> 6, p = q + d, i = (e >> 2) & 15, j4 = 4 * (e & 3);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        // row i of D_p, read once (zero above its diagonal, so all 16 terms
-        // can be taken)
-        float dr[16];
-#pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-          const float4 f = *reinterpret_cast<const float4*>(tf + (16 * p + i) * 64 + 16 * p + 4 * m4);
-          dr[4 * m4] = f.x; dr[4 * m4 + 1] = f.y; dr[4 * m4 + 2] = f.z; dr[4 * m4 + 3] = f.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float a = dr[m];
-          const float4 b = *reinterpret_cast<const float4*>(xscr + q * 256 + m * 16 + j4);
-          acc.x = fmaf(-a, b.x, acc.x);
-          acc.y = fmaf(-a, b.y, acc.y);
-          acc.z = fmaf(-a, b.z, acc.z);
-          acc.w = fmaf(-a, b.w, acc.w);
-        }
-        *reinterpret_cast<float4*>(tf + (16 * p + i) * 64 + 16 * q + j4) = acc;
+      for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 f0 = *reinterpret_cast<const float4*>(tf + (16 * p + i2) * 64 + 16 * p + 4 * m4);
+        const float4 f1 = *reinterpret_cast<const float4*>(tf + (16 * p + i2 + 1) * 64 + 16 * p + 4 * m4);
+        d0[4 * m4] = f0.x; d0[4 * m4 + 1] = f0.y; d0[4 * m4 + 2] = f0.z; d0[4 * m4 + 3] = f0.w;
+        d1[4 * m4] = f1.x; d1[4 * m4 + 1] = f1.y; d1[4 * m4 + 2] = f1.z; d1[4 * m4 + 3] = f1.w;
       }
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float4 b = *reinterpret_cast<const float4*>(xscr + q * 256 + m * 16 + j4);
+        a0.x = fmaf(-d0[m], b.x, a0.x); a0.y = fmaf(-d0[m], b.y, a0.y);
+        a0.z = fmaf(-d0[m], b.z, a0.z); a0.w = fmaf(-d0[m], b.w, a0.w);
+        a1.x = fmaf(-d1[m], b.x, a1.x); a1.y = fmaf(-d1[m], b.y, a1.y);
+        a1.z = fmaf(-d1[m], b.z, a1.z); a1.w = fmaf(-d1[m], b.w, a1.w);
+      }
+      *reinterpret_cast<float4*>(tf + (16 * p + i2) * 64 + 16 * q + j4) = a0;
+      *reinterpret_cast<float4*>(tf + (16 * p + i2 + 1) * 64 + 16 * q + j4) = a1;
     }
     wg1_sync();
   }
@@ -280,7 +276,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   float* at = reinterpret_cast<float*>(sm + PfSmem::AT);
   float* tf = reinterpret_cast<float*>(sm + PfSmem::TF);
   TOUT* ot = reinterpret_cast<TOUT*>(sm + PfSmem::OT);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + PfSmem::MBAR);   // [0] K^K^T [1] S0 [K^;Q^]^T [2] U [3] S/O [4] rows
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + PfSmem::MBAR);   // [0] K^K^T [1] S0 [K^;Q^]^T [2] U [3] U^T P^T [4] rows [5] S update
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PfSmem::TSLOT);
 
   if (warp == 0) {
@@ -289,7 +285,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   if (tid == 0) {
 #pragma unroll
-    for (int b = 0; b < 5; ++b) tc::mbar_init(mbar + b, 1);
+    for (int b = 0; b < 6; ++b) tc::mbar_init(mbar + b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   tc::fence_before_sync();
@@ -351,12 +347,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   int32_t pend = -1;    // checkpoint page due at the next read of S
   bool ok = true;
   uint32_t issued = 0;  // tensor-core products committed in the current chunk (bit b: mbar[b])
+  bool s_pending = false;   // the previous chunk's state update may still be running
+  int64_t ci = 0;           // the chunk `issued` refers to
   int64_t c = 0;
   for (; c < nch; ++c) {
     const uint32_t par = (uint32_t)(c & 1);   // each mbarrier completes once per chunk
     const int64_t t0 = c * C;
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
     issued = 0;
+    ci = c;
 
     if (worker) {
       // ---- the chunk's rows and gates have landed; the previous output tile
@@ -473,7 +472,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       workers_sync();
       // operands: [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T diag(dec) (row =
-      // k channel); each thread loads all of its inputs before it stores
+      // k channel); each thread loads all of its inputs before it stores.
+      // The previous chunk's state update reads U^T and K^T diag(dec): it
+      // has finished first.
+      if (s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok);
       {
         float4 ya[8], yb[8];
         float fv[8];
@@ -517,6 +519,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     ok = cta_sync_ok(ok);   // y is consumed; [K^; Q^] and K^T diag(dec) are in place
     if (!ok) break;
+    s_pending = false;
     // [K^ K^T; Q^ K^T] (M 128, N 64, K 128) needs no state: it runs during the split
     if (tid == kMmaTid) {
       mma3(tbase + kColKK, sbase + PfSmem::KQ, sbase + PfSmem::KQ_LO, 16384, sbase + PfSmem::KQ,
@@ -656,15 +659,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ok = cta_sync_ok(ok);
     if (!ok) break;
 
-    // ---- (D) S += U^T (K^T diag(dec))^T (onto gam_C S0); U^T P^T
+    // ---- (D) U^T P^T first (the outputs wait for it), then S += U^T
+    // (K^T diag(dec))^T onto gam_C S0, which finishes while the next chunk's
+    // conv and norms run
     if (tid == kMmaTid) {
-      mma3(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::KT,
-           sbase + PfSmem::KT_LO, 0, C / 16, tc::idesc_bf16_f32(128, 128), true);
       mma3(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::PB,
            sbase + PfSmem::PB_LO, 0, C / 16, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 3);
+      mma3(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, 0, sbase + PfSmem::KT,
+           sbase + PfSmem::KT_LO, 0, C / 16, tc::idesc_bf16_f32(128, 128), true);
+      tc::mma_commit(mbar + 5);
     }
-    issued |= 8u;
+    issued |= 8u | 32u;
+    s_pending = true;
     if (worker) {
       mma_wait(mbar + 3, par, ok);
       // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [32 half, +32):
@@ -706,6 +713,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 
+  if (ok && worker && s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok);
   ok = cta_sync_ok(ok);
   if (ok) {
     if (worker) {
@@ -731,10 +739,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // more bounded wait for each piece of work they may still hold, then
     // release the tensor memory
     if (tid == 0) set_error(p.err, GDN_ERR_TIMEOUT);
-    const uint32_t par = (uint32_t)(c & 1);
+    const uint32_t par = (uint32_t)(ci & 1);
 #pragma unroll 1
     for (int b = 0; b < 4; ++b)
       if (issued & (1u << b)) tc::mbar_wait_bounded(mbar + b, par, kPfWait);
+    // the last state update issued: chunk ci's, or else the one before it
+    if (issued & 32u) tc::mbar_wait_bounded(mbar + 5, par, kPfWait);
+    else if (s_pending && ci > 0) tc::mbar_wait_bounded(mbar + 5, (uint32_t)((ci - 1) & 1), kPfWait);
     if (worker && x_issued >= 0) tc::mbar_wait_bounded(mbar + 4, (uint32_t)(x_issued & 1), kPfWait);
     cp_async_wait<0>();
   }
