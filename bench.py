@@ -308,6 +308,81 @@ class ReplayWork:
         return REP_REQS * (2 * sh.payload_bytes) + self.kept_rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4)
 
 
+class FlushSweep:
+    """The flush alone at R kept rows for each of N requests (the log holds
+    exactly R rows), over a few layers whose pools together exceed L2; one
+    CUDA graph flushes every layer, log_len is restored before each replay
+    outside the timed events."""
+
+    def __init__(self, seed: int, n_req: int, rows: int, layers: int):
+        sh = SMALL
+        self.sh, self.n, self.rows, self.nlayers = sh, n_req, rows, layers
+        L = gdn.REPLAY_LOG_SLOTS
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        self.lens = torch.full((layers, n_req), rows, dtype=torch.int32, device="cuda")
+        self.w = inputs.conv_weights(sh, seed).cuda()
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.layers = []
+        for layer in range(layers):
+            pool = gdn.StatePool(sh, n_req, fill=0)
+            st = pool.buf.view(n_req, sh.page)[:, :sh.state_bytes].view(torch.float32)
+            st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
+            self.layers.append(dict(
+                pool=pool, ckpt=inputs.permutation(n_req, seed + layer).cuda(),
+                log_x=torch.randn(n_req, L, sh.conv_dim, generator=gen, device="cuda").to(torch.bfloat16),
+                log_g=-0.1 * torch.nn.functional.softplus(torch.randn(n_req, L, sh.num_v_heads, generator=gen,
+                                                                      device="cuda")),
+                log_b=torch.sigmoid(torch.randn(n_req, L, sh.num_v_heads, generator=gen, device="cuda")),
+                log_len=self.lens[layer]))
+
+    def flush(self):
+        for l in self.layers:
+            gdn.gdn_replay_flush(self.sh, l["pool"], ckpt_slot=l["ckpt"], log_x=l["log_x"], log_g=l["log_g"],
+                                 log_beta=l["log_b"], log_len=l["log_len"], conv_w=self.w, dev_error=self.err)
+
+    def bytes_per_layer(self):
+        sh = self.sh
+        return self.n * (2 * sh.payload_bytes + self.rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4))
+
+    def time_us_per_layer(self, reps: int = 5) -> float:
+        self.flush()
+        self.lens.fill_(self.rows)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.flush()
+        total = 0.0
+        for _ in range(reps + 1):
+            self.lens.fill_(self.rows)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1) if _ else 0.0
+        if int(self.err.item()):
+            raise RuntimeError("device error word set in the flush sweep")
+        return 1000.0 * total / reps / self.nlayers
+
+
+def flush_sweep(seed: int, hbm_gbs: float):
+    """Flush time per layer: R = 1..17 kept rows at N = 16 requests, and
+    R = 16 at N = 64 and 256 (4B-shaped layer)."""
+    out = []
+    cases = [(16, r) for r in range(1, 18)] + [(64, 16), (256, 16)]
+    for n_req, rows in cases:
+        layers = max(2, 128 // n_req)          # 2.5 MiB pages: >= 320 MB of pools per replay
+        fs = FlushSweep(seed + 31 * rows + n_req, n_req, rows, layers)
+        us = fs.time_us_per_layer()
+        gbs = fs.bytes_per_layer() / (us * 1e-6) / 1e9
+        out.append({"N": n_req, "R": rows, "us_per_layer": round(us, 2), "hbm_gbs": round(gbs, 1),
+                    "hbm_frac": round(gbs / hbm_gbs, 3)})
+        del fs
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- cpu baseline
 
 def _oracle_setup(seed: int):
@@ -415,6 +490,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush-sweep", action="store_true",
+                    help="skip the flush sweep over kept rows and requests")
     ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "replay"],
                     help="time one part only (profiling); the default times the whole step")
     ap.add_argument("--seq-len", type=int, default=SEQ_LEN,
@@ -554,11 +631,13 @@ def main():
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
                 "scope": "prefill part of the step"},
         # per step: prefill 2 (chunk kernel, windows); decode 1 per layer; replay
-        # per layer 5 (conv, scan, log append, log_len, rollback) + flush 3
-        # (tensor-core update, windows, log_len)
-        "gpu_launches": args.steps * (2 + DEC_LAYERS + 8 * REP_LAYERS),
+        # per layer 5 (conv, scan, log append, log_len, rollback) + flush 2
+        # (tensor-core update with v windows; q / k windows and log_len)
+        "gpu_launches": args.steps * (2 + DEC_LAYERS + 7 * REP_LAYERS),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
+    if not args.no_flush_sweep:
+        line["flush_sweep"] = flush_sweep(args.seed + 40 + rank, peaks["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
