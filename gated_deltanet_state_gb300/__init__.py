@@ -29,6 +29,7 @@ __all__ = [
     "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_spec_copy_bytes",
     "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
     "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "workspace_for", "NOALLOC_SCRATCH_BYTES",
+    "gdn_mixed_workspace_size", "gdn_mixed_step",
     "gdn_decode_step", "gdn_checkpoint_resume", "gdn_checkpoint_save", "gdn_replay_append",
     "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "STATUS",
 ]
@@ -90,6 +91,15 @@ class _DecodeArgs(ctypes.Structure):
                 ("dev_error", _P)]
 
 
+class _MixedArgs(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("total_tokens", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
+                ("cu_seqlens", _P), ("cu_seqlens_host", _P), ("is_decode", _P), ("is_decode_host", _P),
+                ("start_pos", _P), ("start_pos_host", _P), ("init_page", _P), ("init_page_host", _P),
+                ("block_table", _P), ("slot", _P), ("x", _P), ("g", _P), ("beta", _P), ("conv_w", _P),
+                ("o", _P), ("dev_error", _P)]
+
+
 class _ReplayArgs(ctypes.Structure):
     _fields_ = [("num_reqs", ctypes.c_int32), ("num_new", ctypes.c_int32), ("ckpt_slot", _P),
                 ("log_x", _P), ("log_g", _P), ("log_beta", _P), ("log_len", _P), ("x_new", _P),
@@ -135,6 +145,8 @@ def load_library(build_if_missing: bool = True):
         "gdn_prefill_chunked": ([D, PL, ctypes.POINTER(_PrefillArgs), _P, sz, _P], i32),
         "gdn_prefill_chunked_noalloc": ([D, PL, ctypes.POINTER(_PrefillArgs), _P], i32),
         "gdn_decode_step": ([D, PL, ctypes.POINTER(_DecodeArgs), _P], i32),
+        "gdn_mixed_workspace_size": ([D, i32, i64], sz),
+        "gdn_mixed_step": ([D, PL, ctypes.POINTER(_MixedArgs), _P, sz, _P], i32),
         "gdn_checkpoint_resume": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
         "gdn_checkpoint_save": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
         "gdn_replay_append": ([D, PL, ctypes.POINTER(_ReplayArgs), _P], i32),
@@ -350,6 +362,41 @@ def gdn_prefill_chunked_noalloc(shape: LayerShape, pool: StatePool, *, cu_seqlen
     st = lib.gdn_prefill_chunked_noalloc(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
                                          ctypes.byref(a), _stream(stream))
     return _check(st, "gdn_prefill_chunked_noalloc") if raise_on_error else st
+
+
+def gdn_mixed_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: int) -> int:
+    return int(load_library().gdn_mixed_workspace_size(ctypes.byref(make_desc(shape)), num_seqs, total_tokens))
+
+
+def gdn_mixed_step(shape: LayerShape, pool: StatePool, *, cu_seqlens, is_decode, start_pos, init_page,
+                   block_table, slot, x, g, beta, conv_w, o, dev_error, start_pos_host=None,
+                   init_page_host=None, workspace=None, max_seq_len: int = 0, stream=None,
+                   raise_on_error: bool = True) -> int:
+    """A packed batch of prefill sequences and single decode tokens (gdn.h:
+    gdn_mixed_step).  The host copies of cu_seqlens and is_decode are taken
+    from the device tensors."""
+    lib = load_library()
+    n = int(cu_seqlens.numel()) - 1
+    T = int(x.shape[0])
+    if workspace is None:
+        workspace = workspace_for(gdn_mixed_workspace_size(shape, n, T), x.device)
+    cuh, k1 = _host(cu_seqlens, torch.int32, "cu_seqlens_host")
+    dh, k2 = _host(is_decode, torch.int8, "is_decode_host")
+    sph, k3 = _host(start_pos_host, torch.int64, "start_pos_host")
+    iph, k4 = _host(init_page_host, torch.int32, "init_page_host")
+    bt = block_table
+    a = _MixedArgs(n, int(bt.shape[1]) if bt is not None and bt.dim() == 2 else 0, T, int(max_seq_len),
+                   _dev(cu_seqlens, torch.int32, "cu_seqlens"), cuh, _dev(is_decode, torch.int8, "is_decode"), dh,
+                   _dev(start_pos, torch.int64, "start_pos"), sph, _dev(init_page, torch.int32, "init_page"), iph,
+                   _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
+                   _dev(slot, torch.int32, "slot"), _dev(x, shape.torch_in(), "x"), _dev(g, torch.float32, "g"),
+                   _dev(beta, torch.float32, "beta"), _dev(conv_w, torch.float32, "conv_w"),
+                   _dev(o, shape.torch_out(), "o"), _dev(dev_error, torch.int32, "dev_error"))
+    ws = _dev(workspace, None, "workspace")
+    wsb = workspace.numel() * workspace.element_size()
+    st = lib.gdn_mixed_step(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a), ws, wsb,
+                            _stream(stream))
+    return _check(st, "gdn_mixed_step") if raise_on_error else st
 
 
 def gdn_decode_step(shape: LayerShape, pool: StatePool, *, x, g, beta, conv_w, slot, o, dev_error,

@@ -158,8 +158,99 @@ gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.slot = a->slot;
   p.o = a->o;
   p.err = a->dev_error;
+  p.row = nullptr;
+  p.decode = nullptr;
   return cuda_status(launch_decode(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
                                    desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+size_t gdn_mixed_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens) {
+  return gdn_prefill_workspace_size(desc, num_seqs, total_tokens);
+}
+
+gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_mixed_args* a,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (!a || a->num_seqs < 0 || a->num_seqs > kMaxGrid || a->total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (a->num_seqs == 0) return GDN_OK;
+  if (!a->cu_seqlens || !a->cu_seqlens_host || !a->is_decode || !a->is_decode_host || !a->start_pos ||
+      !a->init_page || !a->slot || !a->conv_w || !a->dev_error || a->max_blocks < 0 ||
+      (a->max_blocks > 0 && !a->block_table))
+    return GDN_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 && (!a->x || !a->g || !a->beta || !a->o)) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(a->x) || !aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
+  if (a->cu_seqlens_host[0] != 0 || a->cu_seqlens_host[a->num_seqs] != a->total_tokens)
+    return GDN_ERR_INVALID_ARG;
+  int32_t n_dec = 0;
+  for (int32_t s = 0; s < a->num_seqs; ++s) {
+    const int64_t len = (int64_t)a->cu_seqlens_host[s + 1] - a->cu_seqlens_host[s];
+    if (len < 0) return GDN_ERR_INVALID_ARG;
+    if (a->is_decode_host[s]) {
+      if (len != 1) return GDN_ERR_INVALID_ARG;
+      ++n_dec;
+      continue;
+    }
+    if (a->start_pos_host) {
+      const int64_t sp = a->start_pos_host[s];
+      if (sp < 0) return GDN_ERR_INVALID_ARG;
+      const bool cold = a->init_page_host ? a->init_page_host[s] == -1 : sp == 0;
+      if (cold ? sp != 0 : (sp <= 0 || sp % desc->block_size != 0)) return GDN_ERR_NOT_BLOCK_ALIGNED;
+    }
+    if (a->init_page_host && (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages))
+      return GDN_ERR_PAGE_RANGE;
+  }
+  if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_mixed_workspace_size(desc, a->num_seqs, a->total_tokens);
+  if (n_dec < a->num_seqs && need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return GDN_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // the prefill sequences (the decode ones are skipped by every prefill kernel)
+  if (n_dec < a->num_seqs) {
+    ScanParams p = base_scan(desc, pool);
+    p.num_seqs = a->num_seqs;
+    p.conv_w = a->conv_w;
+    p.o = a->o;
+    p.err = a->dev_error;
+    p.cu_seqlens = a->cu_seqlens;
+    p.start_pos = a->start_pos;
+    p.init_page = a->init_page;
+    p.block_table = a->block_table;
+    p.max_blocks = a->max_blocks;
+    p.out_slot = a->slot;
+    p.x = a->x;
+    p.g = a->g;
+    p.beta = a->beta;
+    p.total_rows = a->total_tokens;
+    p.skip = a->is_decode;
+    if (need > 0) bind_workspace(p, workspace, a->total_tokens);
+    const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
+    st = cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                    desc->out_dtype, cs));
+    if (st != GDN_OK) return st;
+  }
+  // the decode tokens (gdn_decode_mixed): row cu_seqlens[s] of the packed tensors
+  if (n_dec > 0) {
+    DecodeParams p;
+    p.pool = make_pool(desc, pool);
+    p.Hqk = desc->num_qk_heads;
+    p.Hv = desc->num_v_heads;
+    p.conv_dim = (int32_t)gdn_conv_dim(desc);
+    p.num_seqs = a->num_seqs;
+    p.q_scale = desc->q_scale;
+    p.eps = desc->norm_eps;
+    p.x = a->x;
+    p.g = a->g;
+    p.beta = a->beta;
+    p.conv_w = a->conv_w;
+    p.slot = a->slot;
+    p.o = a->o;
+    p.err = a->dev_error;
+    p.row = a->cu_seqlens;
+    p.decode = a->is_decode;
+    st = cuda_status(launch_decode(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype, cs));
+  }
+  return st;
 }
 
 static gdn_status checkpoint_copy(const gdn_layer_desc* desc, const gdn_pool* pool,

@@ -8,6 +8,11 @@
 // slices.  Owning all readers of those window channels lets the CTA shift the
 // window in place after it has read it, with no cross-CTA ordering.
 //
+// In a mixed batch (prefill sequences and single decode tokens packed in one
+// varlen batch: the pages' gdn_decode_mixed, same section) the kernel reads
+// each decode sequence's token row through `row` and leaves the prefill
+// sequences, marked in `decode`, to the prefill kernels.
+//
 // 256 threads stream the group's rows in passes of 64 rows (4 lanes per row,
 // 128-bit loads); the next pass's rows are loaded while the current pass is
 // computed, so every thread keeps two 512-byte row slices in flight.
@@ -28,6 +33,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
   const int rows = G * DV;
   const int passes = (rows + kDecPassRows - 1) / kDecPassRows;
 
+  if (p.decode && !p.decode[s]) return;   // a prefill sequence of a mixed batch
+  const int64_t trow = p.row ? (int64_t)p.row[s] : (int64_t)s;   // token row in x, g, beta, o
   const int32_t slot = p.slot[s];
   if (!page_ok(p.pool, slot)) {
     if (jq == 0 && tid == 0) set_error(p.err, GDN_ERR_PAGE_RANGE);
@@ -55,7 +62,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
 
   // ---- conv + SiLU of this group's channels, and the shifted window
   const int NC = 2 * DK + G * DV;
-  const TIN* xs = reinterpret_cast<const TIN*>(p.x) + (int64_t)s * p.conv_dim;
+  const TIN* xs = reinterpret_cast<const TIN*>(p.x) + trow * p.conv_dim;
   for (int idx = tid; idx < NC; idx += kDecThreads) {
     const int c = idx < DK ? jq * DK + idx
                            : (idx < 2 * DK ? p.Hqk * DK + jq * DK + idx - DK
@@ -72,8 +79,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
     nw_s[2 * NC + idx] = xv;
   }
   if (tid < G) {
-    a_s[tid] = expf(p.g[(int64_t)s * p.Hv + jq * G + tid]);
-    b_s[tid] = p.beta[(int64_t)s * p.Hv + jq * G + tid];
+    a_s[tid] = expf(p.g[trow * p.Hv + jq * G + tid]);
+    b_s[tid] = p.beta[trow * p.Hv + jq * G + tid];
   }
   __syncthreads();
   if (warp < 2) {  // warp 0 normalises q, warp 1 normalises k
@@ -135,7 +142,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
     o = quad_sum(o);
     if (valid && cq == 0) {
       const int h = jq * G + hh, r = row - hh * DV;
-      out[((int64_t)s * p.Hv + h) * DV + r] = from_f32<TOUT>(o);
+      out[(trow * p.Hv + h) * DV + r] = from_f32<TOUT>(o);
     }
 #pragma unroll
     for (int m = 0; m < NCH; ++m) cur[m] = nxt[m];

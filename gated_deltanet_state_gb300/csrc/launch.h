@@ -19,6 +19,11 @@ struct DecodeParams {
   const int32_t* slot;
   void* o;
   int32_t* err;
+  // mixed batches: the token row of sequence s in x, g, beta and o (nullptr:
+  // row s), and the regime of each sequence (nullptr: every sequence
+  // decodes; 0 = a prefill sequence, skipped here)
+  const int32_t* row;
+  const int8_t* decode;
 };
 
 struct CopyParams {

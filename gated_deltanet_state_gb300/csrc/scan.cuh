@@ -61,6 +61,7 @@ struct ScanParams {
   const float* g;
   const float* beta;
   int64_t total_rows;   // rows of x, g, beta and o (all sequences)
+  const int8_t* skip;   // mixed batches: nonzero = a decode sequence, not prefilled here
   // replay
   const int32_t* ckpt_slot;
   const void* log_x;
@@ -133,6 +134,7 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
   v.conv_dim = p.conv_dim;
   v.Hv = p.Hv;
   if (MODE == kPrefill) {
+    if (p.skip && p.skip[s]) return false;   // decoded by the mixed step's decode kernel
     const int64_t t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
     start = p.start_pos[s];
     init = p.init_page[s];

@@ -291,6 +291,50 @@ typedef struct gdn_decode_args {
 gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
                            const gdn_decode_args* args, void* stream);
 
+/* Mixed batch: prefill sequences and single decode tokens packed in one
+ * varlen batch, in one call ("Hybrid linear attention (gated DeltaNet)", "The
+ * part that is easy to get wrong": in the mixed regime the prefill kernels
+ * run on the prefill sequences and gdn_decode_mixed on the decode tokens).
+ * Sequence s owns rows [cu_seqlens[s], cu_seqlens[s+1]) of x, g, beta and o.
+ * is_decode[s] = 1: exactly one row; the state and window in page slot[s]
+ * advance by that token in place (gdn_decode_step's step; start_pos,
+ * init_page and its block_table row are ignored).  is_decode[s] = 0: the
+ * sequence is prefilled as by gdn_prefill_chunked, with slot[s] as out_slot.
+ * Both parts run on `stream`, the prefill kernels first; every sequence gets
+ * exactly the bits of the corresponding separate call.
+ *
+ * Host checks (GDN_ERR_INVALID_ARG unless noted, nothing launched): the host
+ * copies of cu_seqlens and is_decode are required; a decode entry must have
+ * exactly one row; prefill entries are checked as in gdn_prefill_chunked
+ * (GDN_ERR_NOT_BLOCK_ALIGNED, GDN_ERR_PAGE_RANGE), and the workspace is
+ * gdn_mixed_workspace_size bytes (0 on the tensor-core path). */
+typedef struct gdn_mixed_args {
+  int32_t num_seqs;              /* N >= 0                                    */
+  int32_t max_blocks;            /* columns of block_table                    */
+  int64_t total_tokens;          /* rows of x, g, beta, o                     */
+  int64_t max_seq_len;           /* longest sequence, or 0 (= total_tokens)   */
+  const int32_t* cu_seqlens;     /* [N+1] device                              */
+  const int32_t* cu_seqlens_host;/* [N+1] host                                */
+  const int8_t* is_decode;       /* [N] device: 1 decode token, 0 prefill     */
+  const int8_t* is_decode_host;  /* [N] host copy                             */
+  const int64_t* start_pos;      /* [N] device (prefill entries)              */
+  const int64_t* start_pos_host; /* [N] host copy or NULL                     */
+  const int32_t* init_page;      /* [N] device (prefill entries), -1 = cold   */
+  const int32_t* init_page_host; /* [N] host copy or NULL                     */
+  const int32_t* block_table;    /* [N][max_blocks] (prefill entries)         */
+  const int32_t* slot;           /* [N] prefill: out_slot; decode: its page   */
+  const void* x;                 /* [T][conv_dim] in_dtype                    */
+  const float* g;                /* [T][Hv]                                   */
+  const float* beta;             /* [T][Hv]                                   */
+  const float* conv_w;           /* [conv_dim][4]                             */
+  void* o;                       /* [T][Hv][dv] out_dtype                     */
+  int32_t* dev_error;
+} gdn_mixed_args;
+
+size_t gdn_mixed_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens);
+gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_mixed_args* args,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bit-exact copies of whole state payloads (S and conv window, NaN encodings
  * included) between pages: dst_page[i] <- src_page[i] for i < n.  A page may
  * only be copied at a block boundary: num_computed_host[i] (tokens the state

@@ -134,3 +134,35 @@ def test_empty_batches_are_no_ops():
     r = gdn._ReplayArgs(0, 0, *([None] * 11), None, 0)
     assert lib.gdn_replay_flush(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(r), None) == 0
     assert lib.gdn_replay_rollback(None, None, 4, 0, None, None) == 0
+
+
+def test_mixed_step_host_checks():
+    """gdn_mixed_step validates its host arrays before launching anything
+    (device pointers here are fake and never dereferenced)."""
+    lib = gdn.load_library()
+    sh = inputs.TINY
+    desc = gdn.make_desc(sh)
+    pool = gdn._Pool(0x100000, sh.page, 8, 0)
+    F = 0x10000
+
+    # every case below fails a host check, so nothing is launched on the fake pointers
+    def call(cu, dec, sp=None, ip=None, drop_dec_host=False, total=None):
+        cu_h = (ctypes.c_int32 * len(cu))(*cu)
+        dec_h = (ctypes.c_int8 * len(dec))(*dec)
+        sp_h = (ctypes.c_int64 * len(sp))(*sp) if sp is not None else None
+        ip_h = (ctypes.c_int32 * len(ip))(*ip) if ip is not None else None
+        n = len(dec)
+        a = gdn._MixedArgs(n, 2, cu[-1] if total is None else total, 0, F, ctypes.addressof(cu_h), F,
+                           None if drop_dec_host else ctypes.addressof(dec_h), F,
+                           ctypes.addressof(sp_h) if sp_h is not None else None, F,
+                           ctypes.addressof(ip_h) if ip_h is not None else None, F, F, F, F, F, F, F, F)
+        return lib.gdn_mixed_step(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), F, 1 << 40, None)
+
+    code = gdn.STATUS_CODE
+    assert call([0, 2, 3], [1, 0]) == code["GDN_ERR_INVALID_ARG"]          # a decode entry of two rows
+    assert call([0, 1, 3], [1, 0], drop_dec_host=True) == code["GDN_ERR_INVALID_ARG"]
+    assert call([0, 1, 3], [1, 0], sp=[0, 10], ip=[-1, 2]) == code["GDN_ERR_NOT_BLOCK_ALIGNED"]
+    assert call([0, 1, 3], [1, 0], sp=[0, 64], ip=[-1, 9]) == code["GDN_ERR_PAGE_RANGE"]
+    assert call([0, 1, 4], [1, 0], total=5) == code["GDN_ERR_INVALID_ARG"]  # cu_seqlens end != total
+    a = gdn._MixedArgs(0, 0, 0, 0, *([None] * 16))
+    assert lib.gdn_mixed_step(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None, 0, None) == 0
