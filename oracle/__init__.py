@@ -19,6 +19,9 @@ recurrence:
   plus a log of inputs since it; outputs come from the two, rollback drops
   log rows, the flush rewrites the checkpoint ("Caching less to serve more
   requests", "What we changed").
+* ``core_prefill`` / ``core_decode`` — the packed core: gates from the b | a
+  rows, the same recurrence, gated RMS norm of the outputs ("Hybrid linear
+  attention (gated DeltaNet)", "Packed-core traces").
 
 Every function is pinned in ``tests/test_oracle_pins.py`` against brute force,
 closed forms, identities and the pages' worked values.
@@ -225,3 +228,61 @@ def replay_flush(d: Dims, conv_w, S_ckpt, win_ckpt, log_x, log_g, log_b, log_len
     bs = np.concatenate([log_b[r, :lens[r]] for r in range(N)]) if cu[-1] else np.zeros((0, d.Hv))
     res = prefill(d, cu, np.zeros(N, np.int64), 1 << 62, xs, gs, bs, conv_w, S_ckpt, win_ckpt, nthreads)
     return res["S"], res["win"]
+
+
+# --------------------------------------------------------------------------- packed core
+# "Hybrid linear attention (gated DeltaNet)", "Packed-core traces": the core
+# takes packed qkvz plus ba per token and returns gated-normalised value rows;
+# it owns the conv weights, dt_bias, a float32 A_log and the norm scale.  The
+# pages name the weights only; the gates and the norm are read as
+#   g    = -exp(A_log) * softplus(a + dt_bias)      (so a_t = exp(g))
+#   beta = sigmoid(b)
+#   y    = o / sqrt(mean_dv(o^2) + eps) * norm_w * silu(z)   per token and v head.
+
+
+def softplus(x) -> np.ndarray:
+    """log(1 + e^x), evaluated as max(x, 0) + log1p(e^-|x|)."""
+    x = _f64(x)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def core_gates(ba, A_log, dt_bias, Hv: int):
+    """Gates from the packed b | a rows [T][2 Hv]: (g, beta), each [T][Hv]."""
+    ba = _f64(ba).reshape(-1, 2 * Hv)
+    b, a = ba[:, :Hv], ba[:, Hv:]
+    g = -np.exp(_f64(A_log))[None, :] * softplus(a + _f64(dt_bias)[None, :])
+    beta = 1.0 / (1.0 + np.exp(-b))
+    return g, beta
+
+
+def gated_rmsnorm(o, z, norm_w, eps: float):
+    """RMS-normalise o [..., dv] over dv, scale by norm_w [dv], gate by silu(z)."""
+    o, z, w = _f64(o), _f64(z), _f64(norm_w)
+    rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return o / rms * w * (z / (1.0 + np.exp(-z)))
+
+
+def _split_qkvz(d: Dims, qkvz):
+    qkvz = _f64(qkvz)
+    return qkvz[:, :d.conv_dim], qkvz[:, d.conv_dim:].reshape(-1, d.Hv, d.dv)
+
+
+def core_prefill(d: Dims, cu_seqlens, start_pos, block_size: int, qkvz, ba, conv_w, A_log, dt_bias,
+                 norm_w, norm_eps: float, S0=None, win0=None, nthreads: int = 0):
+    """The prefill from packed inputs: gates from ba, the recurrence on the
+    q | k | v part, the gated norm on its outputs (returned as "y"; the rest
+    as ``prefill`` returns it)."""
+    x, z = _split_qkvz(d, qkvz)
+    g, beta = core_gates(ba, A_log, dt_bias, d.Hv)
+    r = prefill(d, cu_seqlens, start_pos, block_size, x, g, beta, conv_w, S0, win0, nthreads)
+    r["y"] = gated_rmsnorm(r["o"], z, norm_w, norm_eps)
+    return r
+
+
+def core_decode(d: Dims, qkvz, ba, conv_w, A_log, dt_bias, norm_w, norm_eps: float, S0, win0,
+                nthreads: int = 0):
+    """One packed token per sequence: returns (y [N][Hv][dv], S, win)."""
+    x, z = _split_qkvz(d, qkvz)
+    g, beta = core_gates(ba, A_log, dt_bias, d.Hv)
+    o, S, win = decode(d, x, g, beta, conv_w, S0, win0, nthreads)
+    return gated_rmsnorm(o, z, norm_w, norm_eps), S, win

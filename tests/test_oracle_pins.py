@@ -338,3 +338,71 @@ def test_replay_flush_of_empty_log_is_identity():
     z = np.zeros((2, 32, d.conv_dim)); zg = np.zeros((2, 32, d.Hv))
     S1, win1 = oracle.replay_flush(d, inputs.conv_weights(sh, 0), S0, win0, z, zg, zg, [0, 0])
     assert np.array_equal(S1, S0) and np.array_equal(win1, win0)
+
+
+# ---------------------------------------------------------------- packed core
+# "Hybrid linear attention (gated DeltaNet)", "Packed-core traces": gates from
+# the packed b | a rows with dt_bias and A_log, gated RMS norm of the outputs.
+
+def test_core_gates_closed_forms():
+    import math
+    Hv = 2
+    # b | a order: b = ln 3 gives beta = 3/4; a = 0, dt_bias = 0, A_log = 0 gives g = -ln 2
+    g, beta = oracle.core_gates([[math.log(3.0), 0.0, 0.0, 0.0]], [0.0, 0.0], [0.0, 0.0], Hv)
+    assert beta[0, 0] == pytest.approx(0.75, abs=1e-15) and beta[0, 1] == pytest.approx(0.5, abs=1e-15)
+    assert g[0, 0] == pytest.approx(-math.log(2.0), abs=1e-15)
+    # A_log = ln 3 scales the decay by 3; dt_bias shifts a
+    g, _ = oracle.core_gates([[0.0, 0.0, 1.0, -1.0]], [math.log(3.0), 0.0], [0.0, 1.0], Hv)
+    assert g[0, 0] == pytest.approx(-3.0 * math.log1p(math.e), rel=1e-14)
+    assert g[0, 1] == pytest.approx(-math.log(2.0), rel=1e-14)
+    # tails: softplus(40) = 40 + log1p(e^-40); softplus(-40) = log1p(e^-40)
+    g, _ = oracle.core_gates([[0.0, 0.0, 40.0, -40.0]], [0.0, 0.0], [0.0, 0.0], Hv)
+    assert g[0, 0] == pytest.approx(-(40.0 + math.log1p(math.exp(-40.0))), rel=1e-15)
+    assert g[0, 1] == pytest.approx(-math.log1p(math.exp(-40.0)), rel=1e-12)
+
+
+def test_gated_rmsnorm_closed_forms():
+    import math
+    silu2 = 2.0 / (1.0 + math.exp(-2.0))
+    # o = (3, 4), eps = 0: rms = sqrt(12.5)
+    y = oracle.gated_rmsnorm([3.0, 4.0], [2.0, 2.0], [1.0, 0.5], 0.0)
+    r = math.sqrt(12.5)
+    assert y[0] == pytest.approx(3.0 / r * silu2, rel=1e-15)
+    assert y[1] == pytest.approx(4.0 / r * 0.5 * silu2, rel=1e-15)
+    # a constant vector normalises to its sign (eps = 0), with eps: 1 / sqrt(1 + eps / c^2)
+    y = oracle.gated_rmsnorm(np.full(8, -0.25), np.full(8, 2.0), np.ones(8), 0.0)
+    assert np.allclose(y, -silu2, rtol=1e-15, atol=0)
+    y = oracle.gated_rmsnorm(np.full(8, 0.5), np.full(8, 2.0), np.ones(8), 0.25)
+    assert np.allclose(y, silu2 / math.sqrt(2.0), rtol=1e-15, atol=0)
+    # scale and sign invariance (eps = 0); a zero gate zeroes the row
+    rng = np.random.default_rng(3)
+    o, z, w = rng.normal(size=16), rng.normal(size=16), rng.normal(size=16)
+    assert np.allclose(oracle.gated_rmsnorm(7.5 * o, z, w, 0.0), oracle.gated_rmsnorm(o, z, w, 0.0), rtol=1e-13)
+    assert np.allclose(oracle.gated_rmsnorm(-o, z, w, 0.0), -oracle.gated_rmsnorm(o, z, w, 0.0), rtol=1e-13)
+    assert np.all(oracle.gated_rmsnorm(o, np.zeros(16), w, 1e-6) == 0.0)
+
+
+def test_core_prefill_is_the_recurrence_on_the_qkv_part():
+    """The packed core splits each row into x = q | k | v and z and takes its
+    gates from b | a: the states equal the plain prefill's on (x, g, beta),
+    and y is the gated norm of its outputs."""
+    d = oracle.Dims(1, 2, 4, 4)
+    T = 9
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(T, d.conv_dim))
+    z = rng.normal(size=(T, d.Hv * d.dv))
+    ba = rng.normal(size=(T, 2 * d.Hv))
+    A_log, dt_bias, nw = rng.normal(size=d.Hv) * 0.3, rng.normal(size=d.Hv) * 0.3, rng.normal(size=d.dv)
+    w = rng.normal(size=(d.conv_dim, 4)) * 0.5
+    r = oracle.core_prefill(d, [0, T], [0], 4, np.concatenate([x, z], 1), ba, w, A_log, dt_bias, nw, 1e-6)
+    # gates written out by hand for token 3, head 1
+    b, a = ba[3, 1], ba[3, d.Hv + 1]
+    g31 = -np.exp(A_log[1]) * np.log1p(np.exp(a + dt_bias[1]))
+    beta31 = 1.0 / (1.0 + np.exp(-b))
+    g, beta = oracle.core_gates(ba, A_log, dt_bias, d.Hv)
+    assert g[3, 1] == pytest.approx(g31, rel=1e-13) and beta[3, 1] == pytest.approx(beta31, rel=1e-14)
+    ref = oracle.prefill(d, [0, T], [0], 4, x, g, beta, w)
+    assert np.array_equal(r["S"], ref["S"]) and np.array_equal(r["o"], ref["o"])
+    o = ref["o"][5, 0]
+    y = o / np.sqrt(np.mean(o * o) + 1e-6) * nw * (z[5, :d.dv] / (1.0 + np.exp(-z[5, :d.dv])))
+    assert np.allclose(r["y"][5, 0], y, rtol=1e-13, atol=1e-15)
