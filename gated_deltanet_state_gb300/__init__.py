@@ -30,6 +30,7 @@ __all__ = [
     "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
     "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "workspace_for", "NOALLOC_SCRATCH_BYTES",
     "gdn_mixed_workspace_size", "gdn_mixed_step",
+    "gdn_core_prefill_workspace_size", "gdn_core_prefill", "gdn_core_decode",
     "gdn_decode_step", "gdn_checkpoint_resume", "gdn_checkpoint_save", "gdn_replay_append",
     "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "STATUS",
 ]
@@ -91,6 +92,11 @@ class _DecodeArgs(ctypes.Structure):
                 ("dev_error", _P)]
 
 
+class _CoreArgs(ctypes.Structure):
+    _fields_ = [("ba", _P), ("A_log", _P), ("dt_bias", _P), ("norm_w", _P), ("norm_eps", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
+
+
 class _MixedArgs(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("total_tokens", ctypes.c_int64), ("max_seq_len", ctypes.c_int64),
@@ -146,6 +152,9 @@ def load_library(build_if_missing: bool = True):
         "gdn_prefill_chunked_noalloc": ([D, PL, ctypes.POINTER(_PrefillArgs), _P], i32),
         "gdn_decode_step": ([D, PL, ctypes.POINTER(_DecodeArgs), _P], i32),
         "gdn_mixed_workspace_size": ([D, i32, i64], sz),
+        "gdn_core_prefill_workspace_size": ([D, i32, i64], sz),
+        "gdn_core_prefill": ([D, PL, ctypes.POINTER(_PrefillArgs), ctypes.POINTER(_CoreArgs), _P, sz, _P], i32),
+        "gdn_core_decode": ([D, PL, ctypes.POINTER(_DecodeArgs), ctypes.POINTER(_CoreArgs), _P], i32),
         "gdn_mixed_step": ([D, PL, ctypes.POINTER(_MixedArgs), _P, sz, _P], i32),
         "gdn_checkpoint_resume": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
         "gdn_checkpoint_save": ([D, PL, _P, _P, _P, i32, _P, _P], i32),
@@ -362,6 +371,59 @@ def gdn_prefill_chunked_noalloc(shape: LayerShape, pool: StatePool, *, cu_seqlen
     st = lib.gdn_prefill_chunked_noalloc(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
                                          ctypes.byref(a), _stream(stream))
     return _check(st, "gdn_prefill_chunked_noalloc") if raise_on_error else st
+
+
+def _core_args(shape, ba, A_log, dt_bias, norm_w, norm_eps):
+    return _CoreArgs(_dev(ba, shape.torch_in(), "ba"), _dev(A_log, torch.float32, "A_log"),
+                     _dev(dt_bias, torch.float32, "dt_bias"), _dev(norm_w, torch.float32, "norm_w"),
+                     float(norm_eps), 0)
+
+
+def gdn_core_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: int) -> int:
+    return int(load_library().gdn_core_prefill_workspace_size(ctypes.byref(make_desc(shape)), num_seqs,
+                                                              total_tokens))
+
+
+def gdn_core_prefill(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page, block_table,
+                     out_slot, qkvz, ba, conv_w, A_log, dt_bias, norm_w, norm_eps: float, o, dev_error,
+                     start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
+                     stream=None, raise_on_error: bool = True) -> int:
+    """The prefill on packed q | k | v | z and b | a rows, gated-normalised
+    outputs (gdn.h: gdn_core_prefill)."""
+    lib = load_library()
+    n = int(cu_seqlens.numel()) - 1
+    T = int(qkvz.shape[0])
+    if workspace is None:
+        workspace = workspace_for(gdn_core_prefill_workspace_size(shape, n, T), qkvz.device)
+    sph, keep1 = _host(start_pos_host, torch.int64, "start_pos_host")
+    iph, keep2 = _host(init_page_host, torch.int32, "init_page_host")
+    bt = block_table
+    a = _PrefillArgs(n, int(bt.shape[1]) if bt is not None and bt.dim() == 2 else 0, T, int(max_seq_len),
+                     _dev(cu_seqlens, torch.int32, "cu_seqlens"), _dev(start_pos, torch.int64, "start_pos"),
+                     sph, iph, _dev(qkvz, shape.torch_in(), "qkvz"), None, None,
+                     _dev(conv_w, torch.float32, "conv_w"), _dev(init_page, torch.int32, "init_page"),
+                     _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
+                     _dev(out_slot, torch.int32, "out_slot"), _dev(o, shape.torch_out(), "o"),
+                     _dev(dev_error, torch.int32, "dev_error"))
+    c = _core_args(shape, ba, A_log, dt_bias, norm_w, norm_eps)
+    st = lib.gdn_core_prefill(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
+                              ctypes.byref(c), _dev(workspace, None, "workspace"),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "gdn_core_prefill") if raise_on_error else st
+
+
+def gdn_core_decode(shape: LayerShape, pool: StatePool, *, qkvz, ba, conv_w, A_log, dt_bias, norm_w,
+                    norm_eps: float, slot, o, dev_error, stream=None, raise_on_error: bool = True) -> int:
+    """One packed token per sequence; gated-normalised outputs (gdn.h:
+    gdn_core_decode)."""
+    lib = load_library()
+    a = _DecodeArgs(int(qkvz.shape[0]), 0, _dev(qkvz, shape.torch_in(), "qkvz"), None, None,
+                    _dev(conv_w, torch.float32, "conv_w"), _dev(slot, torch.int32, "slot"),
+                    _dev(o, shape.torch_out(), "o"), _dev(dev_error, torch.int32, "dev_error"))
+    c = _core_args(shape, ba, A_log, dt_bias, norm_w, norm_eps)
+    st = lib.gdn_core_decode(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
+                             ctypes.byref(c), _stream(stream))
+    return _check(st, "gdn_core_decode") if raise_on_error else st
 
 
 def gdn_mixed_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: int) -> int:

@@ -52,6 +52,7 @@ ScanParams base_scan(const gdn_layer_desc* d, const gdn_pool* pool) {
   p.Hqk = d->num_qk_heads;
   p.Hv = d->num_v_heads;
   p.conv_dim = (int32_t)gdn_conv_dim(d);
+  p.x_ld = p.conv_dim;
   p.block_size = d->block_size;
   p.q_scale = d->q_scale;
   p.eps = d->norm_eps;
@@ -85,9 +86,13 @@ size_t gdn_replay_workspace_size(const gdn_layer_desc* desc, int32_t num_reqs) {
                               desc->num_qk_heads, desc->num_v_heads);
 }
 
-gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
-                               const gdn_prefill_args* a, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The prefill, plain or on packed rows (core != nullptr).
+gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* a,
+                        const gdn_core_args* core, void* workspace, size_t workspace_bytes, void* stream) {
   gdn_status st = check_desc_pool(desc, pool);
   if (st != GDN_OK) return st;
   if (!a || a->num_seqs < 0 || a->num_seqs > kMaxGrid || a->total_tokens < 0) return GDN_ERR_INVALID_ARG;
@@ -95,7 +100,14 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   if (!a->cu_seqlens || !a->start_pos || !a->conv_w || !a->init_page || !a->out_slot ||
       !a->dev_error || a->max_blocks < 0 || (a->max_blocks > 0 && !a->block_table))
     return GDN_ERR_INVALID_ARG;
-  if (a->total_tokens > 0 && (!a->x || !a->g || !a->beta || !a->o)) return GDN_ERR_INVALID_ARG;
+  if (a->total_tokens > 0 && (!a->x || (!core && (!a->g || !a->beta)) || !a->o)) return GDN_ERR_INVALID_ARG;
+  if (core) {
+    if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                              desc->block_size))
+      return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!core->A_log || !core->dt_bias || !core->norm_w || (a->total_tokens > 0 && !core->ba))
+      return GDN_ERR_INVALID_ARG;
+  }
   if (!aligned16(a->x) || !aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
   // Fail closed before launching anything when the host can see an
   // off-boundary resume or a cold start that does not begin at 0.
@@ -111,7 +123,8 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
     for (int32_t s = 0; s < a->num_seqs; ++s)
       if (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages) return GDN_ERR_PAGE_RANGE;
   if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
-  const size_t need = gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
+  const size_t need = core ? gdn_core_prefill_workspace_size(desc, a->num_seqs, a->total_tokens)
+                           : gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
   p.num_seqs = a->num_seqs;
@@ -128,10 +141,48 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.g = a->g;
   p.beta = a->beta;
   p.total_rows = a->total_tokens;
-  if (need > 0) bind_workspace(p, workspace, a->total_tokens);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (core) {
+    // packed rows q | k | v | z; the gates of every row into the workspace first
+    p.x_ld = p.conv_dim + desc->num_v_heads * desc->head_dim_v;
+    float* gw = static_cast<float*>(workspace);
+    float* bw = gw + (size_t)a->total_tokens * desc->num_v_heads;
+    p.g = gw;
+    p.beta = bw;
+    p.norm_w = core->norm_w;
+    p.norm_eps2 = core->norm_eps;
+    st = cuda_status(launch_core_gates(core->ba, desc->in_dtype, core->A_log, core->dt_bias, desc->num_v_heads,
+                                       a->total_tokens, gw, bw, cs));
+    if (st != GDN_OK) return st;
+  } else if (need > 0) {
+    bind_workspace(p, workspace, a->total_tokens);
+  }
   const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
   return cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
-                                    desc->out_dtype, static_cast<cudaStream_t>(stream)));
+                                    desc->out_dtype, cs));
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
+                               const gdn_prefill_args* a, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return prefill_call(desc, pool, a, nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t gdn_core_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens) {
+  (void)num_seqs;
+  if (gdn_conv_dim(desc) <= 0 || total_tokens < 0) return 0;
+  const size_t b = 2 * sizeof(float) * (size_t)total_tokens * desc->num_v_heads;
+  return (b + 255) / 256 * 256;
+}
+
+gdn_status gdn_core_prefill(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* a,
+                            const gdn_core_args* core, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!core) return GDN_ERR_INVALID_ARG;
+  return prefill_call(desc, pool, a, core, workspace, workspace_bytes, stream);
 }
 
 gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
@@ -143,11 +194,12 @@ gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
   if (!a->x || !a->g || !a->beta || !a->conv_w || !a->slot || !a->o || !a->dev_error)
     return GDN_ERR_INVALID_ARG;
   if (!aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
-  DecodeParams p;
+  DecodeParams p{};
   p.pool = make_pool(desc, pool);
   p.Hqk = desc->num_qk_heads;
   p.Hv = desc->num_v_heads;
   p.conv_dim = (int32_t)gdn_conv_dim(desc);
+  p.x_ld = p.conv_dim;
   p.num_seqs = a->num_seqs;
   p.q_scale = desc->q_scale;
   p.eps = desc->norm_eps;
@@ -160,6 +212,39 @@ gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
   p.err = a->dev_error;
   p.row = nullptr;
   p.decode = nullptr;
+  return cuda_status(launch_decode(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                   desc->out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_core_decode(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_decode_args* a,
+                           const gdn_core_args* core, void* stream) {
+  gdn_status st = check_desc_pool(desc, pool);
+  if (st != GDN_OK) return st;
+  if (!a || !core || a->num_seqs < 0 || a->num_seqs > kMaxGrid) return GDN_ERR_INVALID_ARG;
+  if (a->num_seqs == 0) return GDN_OK;
+  if (!a->x || !a->conv_w || !a->slot || !a->o || !a->dev_error || !core->ba || !core->A_log ||
+      !core->dt_bias || !core->norm_w)
+    return GDN_ERR_INVALID_ARG;
+  if (!aligned16(a->conv_w)) return GDN_ERR_INVALID_ARG;
+  DecodeParams p{};
+  p.pool = make_pool(desc, pool);
+  p.Hqk = desc->num_qk_heads;
+  p.Hv = desc->num_v_heads;
+  p.conv_dim = (int32_t)gdn_conv_dim(desc);
+  p.x_ld = p.conv_dim + desc->num_v_heads * desc->head_dim_v;
+  p.num_seqs = a->num_seqs;
+  p.q_scale = desc->q_scale;
+  p.eps = desc->norm_eps;
+  p.x = a->x;
+  p.conv_w = a->conv_w;
+  p.slot = a->slot;
+  p.o = a->o;
+  p.err = a->dev_error;
+  p.ba = core->ba;
+  p.A_log = core->A_log;
+  p.dt_bias = core->dt_bias;
+  p.norm_w = core->norm_w;
+  p.norm_eps2 = core->norm_eps;
   return cuda_status(launch_decode(p, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
                                    desc->out_dtype, static_cast<cudaStream_t>(stream)));
 }
@@ -231,11 +316,12 @@ gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, cons
   }
   // the decode tokens (gdn_decode_mixed): row cu_seqlens[s] of the packed tensors
   if (n_dec > 0) {
-    DecodeParams p;
+    DecodeParams p{};
     p.pool = make_pool(desc, pool);
     p.Hqk = desc->num_qk_heads;
     p.Hv = desc->num_v_heads;
     p.conv_dim = (int32_t)gdn_conv_dim(desc);
+    p.x_ld = p.conv_dim;
     p.num_seqs = a->num_seqs;
     p.q_scale = desc->q_scale;
     p.eps = desc->norm_eps;

@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
   float* a_s = y_s + 2 * DK + G * DV;              // [G]
   float* b_s = a_s + G;                            // [G]
   TIN* nw_s = reinterpret_cast<TIN*>(b_s + G);     // [3][2*DK + G*DV] shifted window
+  float* o_s = reinterpret_cast<float*>(nw_s + 3 * (2 * DK + G * DV));   // [G*DV] packed core: outputs
 
   // ---- start streaming the first pass
   float4 cur[NCH], nxt[NCH];
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
 
   // ---- conv + SiLU of this group's channels, and the shifted window
   const int NC = 2 * DK + G * DV;
-  const TIN* xs = reinterpret_cast<const TIN*>(p.x) + trow * p.conv_dim;
+  const TIN* xs = reinterpret_cast<const TIN*>(p.x) + trow * p.x_ld;
   for (int idx = tid; idx < NC; idx += kDecThreads) {
     const int c = idx < DK ? jq * DK + idx
                            : (idx < 2 * DK ? p.Hqk * DK + jq * DK + idx - DK
@@ -79,8 +80,17 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
     nw_s[2 * NC + idx] = xv;
   }
   if (tid < G) {
-    a_s[tid] = expf(p.g[trow * p.Hv + jq * G + tid]);
-    b_s[tid] = p.beta[trow * p.Hv + jq * G + tid];
+    const int h = jq * G + tid;
+    if (p.ba) {   // packed core: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)
+      const TIN* ba = reinterpret_cast<const TIN*>(p.ba) + trow * 2 * p.Hv;
+      const float b = to_f32(ba[h]), x = to_f32(ba[p.Hv + h]) + p.dt_bias[h];
+      const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+      a_s[tid] = expf(-expf(p.A_log[h]) * sp);
+      b_s[tid] = 1.0f / (1.0f + expf(-b));
+    } else {
+      a_s[tid] = expf(p.g[trow * p.Hv + h]);
+      b_s[tid] = p.beta[trow * p.Hv + h];
+    }
   }
   __syncthreads();
   if (warp < 2) {  // warp 0 normalises q, warp 1 normalises k
@@ -142,10 +152,39 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(const DecodePara
     o = quad_sum(o);
     if (valid && cq == 0) {
       const int h = jq * G + hh, r = row - hh * DV;
-      out[(trow * p.Hv + h) * DV + r] = from_f32<TOUT>(o);
+      if (p.norm_w) o_s[row] = o;   // normalised per head below
+      else out[(trow * p.Hv + h) * DV + r] = from_f32<TOUT>(o);
     }
 #pragma unroll
     for (int m = 0; m < NCH; ++m) cur[m] = nxt[m];
+  }
+
+  // ---- packed core: gated RMS norm of each head's outputs (a warp per head),
+  // gated by silu(z) from the packed row
+  if (p.norm_w) {
+    __syncthreads();
+    constexpr int PER = DV / 32 > 0 ? DV / 32 : 1;
+    for (int hh = warp; hh < G; hh += kDecThreads / 32) {
+      float v[PER];
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < PER; ++m) {
+        const int r = lane + 32 * m;
+        v[m] = r < DV ? o_s[hh * DV + r] : 0.f;
+        ss = fmaf(v[m], v[m], ss);
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.0f / sqrtf(ss / (float)DV + p.norm_eps2);
+      const int h = jq * G + hh;
+#pragma unroll
+      for (int m = 0; m < PER; ++m) {
+        const int r = lane + 32 * m;
+        if (r < DV) {
+          const float z = to_f32(xs[p.conv_dim + h * DV + r]);
+          out[(trow * p.Hv + h) * DV + r] = from_f32<TOUT>(v[m] * inv * p.norm_w[r] * silu(z));
+        }
+      }
+    }
   }
 
   // ---- shift the window of this group's channels (all reads happened above)
@@ -163,7 +202,7 @@ template <int DK, int DV, typename TIN, typename TOUT>
 static cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
   const int G = p.Hv / p.Hqk;
   const int NC = 2 * DK + G * DV;
-  const size_t smem = sizeof(float) * (NC + 2 * G) + sizeof(TIN) * 3 * NC + 16;
+  const size_t smem = sizeof(float) * (NC + 2 * G) + sizeof(TIN) * 3 * NC + sizeof(float) * G * DV + 16;
   auto kern = decode_kernel<DK, DV, TIN, TOUT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

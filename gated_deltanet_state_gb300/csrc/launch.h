@@ -24,6 +24,14 @@ struct DecodeParams {
   // decodes; 0 = a prefill sequence, skipped here)
   const int32_t* row;
   const int8_t* decode;
+  // packed core: x rows are q | k | v | z, x_ld elements apart; the gates come
+  // from the b | a rows with A_log and dt_bias; the outputs are gated-normalised
+  int32_t x_ld;
+  const void* ba;        // nullptr: plain rows (g, beta given, outputs as they are)
+  const float* A_log;
+  const float* dt_bias;
+  const float* norm_w;
+  float norm_eps2;
 };
 
 struct CopyParams {
@@ -48,6 +56,9 @@ cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtyp
                                 int out_dtype, cudaStream_t st);
 cudaError_t launch_replay_rollback(int32_t* log_len, const int32_t* accepted, int32_t num_appended,
                                    int32_t n, int32_t* err, cudaStream_t st);
+// Packed core: g and beta of `rows` rows from the b | a rows.
+cudaError_t launch_core_gates(const void* ba, int in_dtype, const float* A_log, const float* dt_bias, int Hv,
+                              int64_t rows, float* g, float* beta, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, int dk, int dv, int in_dtype, int out_dtype,
                           cudaStream_t st);
 cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);

@@ -62,6 +62,9 @@ struct ScanParams {
   const float* beta;
   int64_t total_rows;   // rows of x, g, beta and o (all sequences)
   const int8_t* skip;   // mixed batches: nonzero = a decode sequence, not prefilled here
+  int32_t x_ld;         // elements from one x row to the next (conv_dim; packed q|k|v|z rows: more)
+  const float* norm_w;  // packed core: gated-norm scale [dv] (nullptr: plain outputs)
+  float norm_eps2;      // packed core: gated-norm epsilon
   // replay
   const int32_t* ckpt_slot;
   const void* log_x;
@@ -90,24 +93,25 @@ struct TokenView {
   int64_t n0, n;
   int64_t wrow0;         // workspace row of token 0
   int32_t conv_dim, Hv;
+  int32_t ld;            // elements from one token row to the next (the window's rows: conv_dim)
 
   __device__ __forceinline__ float x(int64_t t, int c) const {
     if (t < 0) return win ? to_f32(win[(kWinRows + t) * conv_dim + c]) : 0.0f;
-    if (t < n0) return to_f32(seg0[t * conv_dim + c]);
-    return to_f32(seg1[(t - n0) * conv_dim + c]);
+    if (t < n0) return to_f32(seg0[t * ld + c]);
+    return to_f32(seg1[(t - n0) * ld + c]);
   }
   // Raw element (bit-exact copies of window rows).
   __device__ __forceinline__ TIN raw(int64_t t, int c) const {
     if (t < 0) return win ? win[(kWinRows + t) * conv_dim + c] : from_f32<TIN>(0.0f);
-    if (t < n0) return seg0[t * conv_dim + c];
-    return seg1[(t - n0) * conv_dim + c];
+    if (t < n0) return seg0[t * ld + c];
+    return seg1[(t - n0) * ld + c];
   }
   // Pointer to pre-conv row t, or nullptr where the row is zero (a cold
   // start's history, or past the end).
   __device__ __forceinline__ const TIN* row(int64_t t) const {
     if (t < 0) return win ? win + (kWinRows + t) * conv_dim : nullptr;
     if (t >= n) return nullptr;
-    return t < n0 ? seg0 + t * conv_dim : seg1 + (t - n0) * conv_dim;
+    return t < n0 ? seg0 + t * ld : seg1 + (t - n0) * ld;
   }
   __device__ __forceinline__ const float* gptr(int64_t t, int h) const {
     return t < n0 ? g0 + t * Hv + h : g1 + (t - n0) * Hv + h;
@@ -132,6 +136,7 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
                                           int64_t& start, int32_t& init, int32_t& final_page,
                                           int64_t& n_log, bool report) {
   v.conv_dim = p.conv_dim;
+  v.ld = p.conv_dim;
   v.Hv = p.Hv;
   if (MODE == kPrefill) {
     if (p.skip && p.skip[s]) return false;   // decoded by the mixed step's decode kernel
@@ -148,7 +153,8 @@ __device__ __forceinline__ bool make_view(const ScanParams& p, int s, TokenView<
       code = GDN_ERR_PAGE_RANGE;
     if (code) { if (report) set_error(p.err, code); return false; }
     v.win = init >= 0 ? page_window<TIN>(p.pool, init) : nullptr;
-    v.seg0 = reinterpret_cast<const TIN*>(p.x) + t0 * p.conv_dim;
+    v.ld = p.x_ld;
+    v.seg0 = reinterpret_cast<const TIN*>(p.x) + t0 * p.x_ld;
     v.seg1 = v.seg0;
     v.g0 = v.g1 = p.g + t0 * p.Hv;
     v.b0 = v.b1 = p.beta + t0 * p.Hv;

@@ -85,6 +85,7 @@ struct PfSmem {
   static constexpr uint32_t KT = 131072;              // K^T diag(dec) hi [128][64], lo at +16 KB
   static constexpr uint32_t KT_LO = KT + 16384;
   static constexpr uint32_t OT = R1;                  // (D) outputs bf16 [64 rows][128 dv]
+  static constexpr uint32_t OF = R1 + 16384;          // (D) packed core: outputs fp32 [64][128]
   // pre-conv rows t0-3 .. t0+63 of the chunk, bf16 [67][128] per tile: q, k, v
   static constexpr uint32_t XS = 163840;
   static constexpr uint32_t XTILE = 17408;            // tile stride (1024-aligned)
@@ -323,8 +324,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     x_issued = 0;
   }
 
-  // conv taps of this thread's q | k channel (tid) and v channel (row)
+  // conv taps of this thread's q | k channel (tid) and v channel (row); the
+  // packed core's norm scale at the channels this lane normalises
   float4 wqk = make_float4(0.f, 0.f, 0.f, 0.f), wv = wqk;
+  float nwr[4] = {0.f, 0.f, 0.f, 0.f};
+  if (worker && p.norm_w) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) nwr[m] = p.norm_w[lane + 32 * m];
+  }
   if (worker) {
     const int qkch = tid < D ? cq0 + tid : ck0 + tid - D;
     wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
@@ -679,7 +686,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // partial one (the sequence's last) by plain stores
       float sq[32], up[32];
       tc::tmem_ld32x2(tbase + tlane + kColSQ + 32 * half, tbase + tlane + kColU + 32 * half, sq, up);
-      if (tma_out && cnt == C) {
+      if (p.norm_w) {
+        // packed core: a token's 128 outputs are normalised together, so they
+        // meet in shared memory; warp w then takes tokens w, w+8, ...: RMS
+        // over dv, the norm scale, the silu(z) gate from the packed row
+        float* of = reinterpret_cast<float*>(sm + PfSmem::OF);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) of[(32 * half + e) * D + row] = fmaf(gam[32 * half + e], sq[e], up[e]);
+        workers_sync();
+        const TIN* zrow = reinterpret_cast<const TIN*>(p.x) + (row0 + t0) * p.x_ld + p.conv_dim + h * D;
+        TOUT* orow = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D;
+        for (int i = warp; i < cnt; i += kPfWorkers / 32) {
+          float v[4];
+          float ss = 0.f;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            v[m] = of[i * D + lane + 32 * m];
+            ss = fmaf(v[m], v[m], ss);
+          }
+          ss = warp_sum(ss);
+          const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float z = to_f32(zrow[(int64_t)i * p.x_ld + lane + 32 * m]);
+            orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nwr[m] * silu(z));
+          }
+        }
+      } else if (tma_out && cnt == C) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) ot[(32 * half + e) * D + row] = from_f32<TOUT>(fmaf(gam[32 * half + e], sq[e], up[e]));
         tc::fence_async_smem();
@@ -769,10 +802,11 @@ cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const cuuint32_t estr[2] = {1, 1};
-    // x as [rows][conv_dim] bf16; a box is 128 channels x 67 rows
+    // x as [rows][x_ld] bf16 (x_ld = conv_dim, or the packed q | k | v | z
+    // row); a box is 128 channels x 67 rows
     {
-      const cuuint64_t dims[2] = {(cuuint64_t)p.conv_dim, (cuuint64_t)p.total_rows};
-      const cuuint64_t strides[1] = {(cuuint64_t)p.conv_dim * 2};
+      const cuuint64_t dims[2] = {(cuuint64_t)p.x_ld, (cuuint64_t)p.total_rows};
+      const cuuint64_t strides[1] = {(cuuint64_t)p.x_ld * 2};
       const cuuint32_t box[2] = {(cuuint32_t)kPfD, (cuuint32_t)kPfXRows};
       if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -291,6 +291,42 @@ typedef struct gdn_decode_args {
 gdn_status gdn_decode_step(const gdn_layer_desc* desc, const gdn_pool* pool,
                            const gdn_decode_args* args, void* stream);
 
+/* Packed core ("Hybrid linear attention (gated DeltaNet)", "Packed-core
+ * traces"): the input rows are packed q | k | v | z and b | a, the output
+ * rows are gated-normalised values; the core owns the conv taps, dt_bias,
+ * A_log (float32) and the norm scale.  The pages name the weights only; the
+ * library reads them as
+ *   g    = -exp(A_log[h]) * softplus(a[h] + dt_bias[h])    (the decay is exp(g))
+ *   beta = sigmoid(b[h])
+ *   y    = o / sqrt(mean_dv(o^2) + norm_eps) * norm_w * silu(z)   per token and v head,
+ * with o the output of the plain step. */
+typedef struct gdn_core_args {
+  const void* ba;                /* [rows][2*Hv] in_dtype: b | a per v head   */
+  const float* A_log;            /* [Hv]                                      */
+  const float* dt_bias;          /* [Hv]                                      */
+  const float* norm_w;           /* [dv], shared by the heads                 */
+  float norm_eps;
+  int32_t reserved;
+} gdn_core_args;
+
+/* Device workspace of gdn_core_prefill: the gates of every row (fp32). */
+size_t gdn_core_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens);
+
+/* gdn_prefill_chunked on packed rows: args->x is [T][conv_dim + Hv*dv]
+ * in_dtype (q | k | v | z; the conv and the windows use the first conv_dim
+ * channels), args->g and args->beta are ignored (may be NULL), args->o
+ * receives y.  States, checkpoints and windows are those of the plain
+ * prefill on the same q | k | v rows and gates.  Layers on the tensor-core
+ * path only (dk = dv = 128, bf16, block a multiple of 64), else
+ * GDN_ERR_UNSUPPORTED_SHAPE. */
+gdn_status gdn_core_prefill(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* args,
+                            const gdn_core_args* core, void* workspace, size_t workspace_bytes, void* stream);
+
+/* gdn_decode_step on packed rows: args->x is [N][conv_dim + Hv*dv]
+ * (q | k | v | z), args->g / args->beta are ignored, args->o receives y. */
+gdn_status gdn_core_decode(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_decode_args* args,
+                           const gdn_core_args* core, void* stream);
+
 /* Mixed batch: prefill sequences and single decode tokens packed in one
  * varlen batch, in one call ("Hybrid linear attention (gated DeltaNet)", "The
  * part that is easy to get wrong": in the mixed regime the prefill kernels

@@ -166,3 +166,18 @@ def test_mixed_step_host_checks():
     assert call([0, 1, 4], [1, 0], total=5) == code["GDN_ERR_INVALID_ARG"]  # cu_seqlens end != total
     a = gdn._MixedArgs(0, 0, 0, 0, *([None] * 16))
     assert lib.gdn_mixed_step(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), None, 0, None) == 0
+
+
+def test_core_prefill_needs_the_tensor_core_path():
+    """The packed prefill's gated norm lives in the tensor-core kernel's
+    epilogue: other shapes are refused before anything launches."""
+    lib = gdn.load_library()
+    sh = inputs.LayerShape(2, 4, 64, 64, 64, 16)
+    desc = gdn.make_desc(sh)
+    pool = gdn._Pool(0x100000, sh.page, 8, 0)
+    F = 0x10000
+    a = gdn._PrefillArgs(1, 1, 64, 0, F, F, None, None, F, None, None, F, F, F, F, F, F)
+    c = gdn._CoreArgs(F, F, F, F, 1e-6, 0)
+    st = lib.gdn_core_prefill(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(a), ctypes.byref(c), F,
+                              1 << 40, None)
+    assert st == gdn.STATUS_CODE["GDN_ERR_UNSUPPORTED_SHAPE"]
