@@ -303,6 +303,13 @@ class ReplayWork:
         for l in self.layers:
             gdn.gdn_replay_flush(self.sh, l["pool"], **self._kw(l))
 
+    def verify_bytes_per_layer(self):
+        """Append: the checkpoint state read once per request and head, the
+        new rows read and copied into the log, the outputs written."""
+        sh = self.sh
+        row = sh.conv_dim * 2 + 2 * sh.num_v_heads * 4
+        return REP_REQS * (sh.payload_bytes + REP_ROWS * (2 * row + sh.num_v_heads * sh.head_dim_v * 2))
+
     def flush_bytes_per_layer(self):
         sh = self.sh
         return REP_REQS * (2 * sh.payload_bytes) + self.kept_rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4)
@@ -367,10 +374,10 @@ class FlushSweep:
 
 
 def flush_sweep(seed: int, hbm_gbs: float):
-    """Flush time per layer: R = 1..17 kept rows at N = 16 requests, and
-    R = 16 at N = 64 and 256 (4B-shaped layer)."""
+    """Flush time per layer: every log length R = 1..32 at N = 16 requests,
+    and R = 16 at N = 64 and 256 (4B-shaped layer)."""
     out = []
-    cases = [(16, r) for r in range(1, 18)] + [(64, 16), (256, 16)]
+    cases = [(16, r) for r in range(1, 33)] + [(64, 16), (256, 16)]
     for n_req, rows in cases:
         layers = max(2, 128 // n_req)          # 2.5 MiB pages: >= 320 MB of pools per replay
         fs = FlushSweep(seed + 31 * rows + n_req, n_req, rows, layers)
@@ -599,6 +606,7 @@ def main():
     achieved = pre.algorithmic_flops() / (pre_ms * 1e-3) / 1e12
     dec_gbs = dec.bytes_per_layer() / (dec_ms / DEC_LAYERS * 1e-3) / 1e9
     fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
+    ver_gbs = rep.verify_bytes_per_layer() / (ver_ms / REP_LAYERS * 1e-3) / 1e9
     value = job_throughput(pre.tokens, world, pre_ms)
 
     line = {
@@ -613,8 +621,9 @@ def main():
         "prefill_ms": pre_ms, "decode_us_per_layer": 1000.0 * dec_ms / DEC_LAYERS,
         "replay_verify_us_per_layer": 1000.0 * ver_ms / REP_LAYERS,
         "flush_us_per_layer": 1000.0 * fl_ms / REP_LAYERS,
-        "decode_hbm_gbs": dec_gbs, "flush_hbm_gbs": fl_gbs,
+        "decode_hbm_gbs": dec_gbs, "flush_hbm_gbs": fl_gbs, "verify_hbm_gbs": ver_gbs,
         "decode_hbm_frac": dec_gbs / peaks["hbm_gbs"], "flush_hbm_frac": fl_gbs / peaks["hbm_gbs"],
+        "verify_hbm_frac": ver_gbs / peaks["hbm_gbs"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak,
                      "traffic": PREFILL_TRAFFIC_PER_LAUNCH if args.seq_len == SEQ_LEN else None,
@@ -633,7 +642,7 @@ def main():
         # per step: prefill 2 (chunk kernel, windows); decode 1 per layer; replay
         # per layer 5 (conv, scan, log append, log_len, rollback) + flush 2
         # (tensor-core update with v windows; q / k windows and log_len)
-        "gpu_launches": args.steps * (2 + DEC_LAYERS + 7 * REP_LAYERS),
+        "gpu_launches": args.steps * (2 + DEC_LAYERS + 5 * REP_LAYERS),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if not args.no_flush_sweep:

@@ -62,13 +62,15 @@ cudaError_t launch_core_gates(const void* ba, int in_dtype, const float* A_log, 
 cudaError_t launch_decode(const DecodeParams& p, int dk, int dv, int in_dtype, int out_dtype,
                           cudaStream_t st);
 cudaError_t launch_copy(const CopyParams& p, cudaStream_t st);
-// Tensor-core replay flush (dk = dv = 128, bf16): the state update and the v
-// windows, then a per-request pass for the q / k windows and log_len.
-bool tc_flush_supported(int dk, int dv, int in_dtype);
+// Tensor-core replay (dk = dv = 128, bf16 inputs).  Flush: the state update
+// and the v windows, then a per-request pass for the q / k windows and
+// log_len.  Append: outputs of the new rows and the log rows, then log_len.
+bool tc_replay_supported(int dk, int dv, int in_dtype);
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (no link-time dependency on libcuda); nullptr if the driver lacks it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
-cudaError_t launch_tc_flush(const ScanParams& p, int in_dtype, cudaStream_t st);
+cudaError_t launch_tc_flush(const ScanParams& p, cudaStream_t st);
+cudaError_t launch_tc_append(const ScanParams& p, cudaStream_t st);
 // Tensor-core chunked prefill (dk = dv = 128, bf16 in and out, block size a
 // multiple of 64), followed by the window pass; needs no workspace.
 bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size);

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(256) log_append_kernel(const ScanParams p) {
 cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
                                  int out_dtype, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
+  // tensor-core outputs and log rows, then log_len
+  if (tc_replay_supported(dk, dv, in_dtype)) return launch_tc_append(p, st);
   const int64_t max_len = GDN_REPLAY_LOG_SLOTS;
   cudaError_t e = [&]() -> cudaError_t { GDN_SCAN_DISPATCH(kAppend) }();
   if (e != cudaSuccess) return e;
@@ -55,7 +57,7 @@ cudaError_t launch_replay_flush(const ScanParams& p, int dk, int dv, int in_dtyp
   if (p.num_seqs == 0) return cudaSuccess;
   // tensor-core state update and v windows, then the q / k windows and the
   // log reset
-  if (tc_flush_supported(dk, dv, in_dtype)) return launch_tc_flush(p, in_dtype, st);
+  if (tc_replay_supported(dk, dv, in_dtype)) return launch_tc_flush(p, st);
   const int64_t max_len = GDN_REPLAY_LOG_SLOTS;
   GDN_SCAN_DISPATCH(kFlush)
 }
