@@ -321,9 +321,12 @@ class FlushSweep:
     CUDA graph flushes every layer, log_len is restored before each replay
     outside the timed events."""
 
-    def __init__(self, seed: int, n_req: int, rows: int, layers: int):
+    def __init__(self, seed: int, n_req: int, rows: int, layers: int, boundary: int = 0):
         sh = SMALL
         self.sh, self.n, self.rows, self.nlayers = sh, n_req, rows, layers
+        # boundary > 0: every request's kept rows cross a block boundary after
+        # that many rows (the state there also goes to a boundary page)
+        self.boundary = boundary
         L = gdn.REPLAY_LOG_SLOTS
         gen = torch.Generator(device="cuda")
         gen.manual_seed(seed)
@@ -332,11 +335,13 @@ class FlushSweep:
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.layers = []
         for layer in range(layers):
-            pool = gdn.StatePool(sh, n_req, fill=0)
+            pool = gdn.StatePool(sh, 2 * n_req if boundary else n_req, fill=0)
             st = pool.buf.view(n_req, sh.page)[:, :sh.state_bytes].view(torch.float32)
             st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
             self.layers.append(dict(
                 pool=pool, ckpt=inputs.permutation(n_req, seed + layer).cuda(),
+                bpage=torch.arange(n_req, 2 * n_req, dtype=torch.int32, device="cuda") if boundary else None,
+                brows=torch.full((n_req,), boundary, dtype=torch.int32, device="cuda") if boundary else None,
                 log_x=torch.randn(n_req, L, sh.conv_dim, generator=gen, device="cuda").to(torch.bfloat16),
                 log_g=-0.1 * torch.nn.functional.softplus(torch.randn(n_req, L, sh.num_v_heads, generator=gen,
                                                                       device="cuda")),
@@ -346,11 +351,13 @@ class FlushSweep:
     def flush(self):
         for l in self.layers:
             gdn.gdn_replay_flush(self.sh, l["pool"], ckpt_slot=l["ckpt"], log_x=l["log_x"], log_g=l["log_g"],
-                                 log_beta=l["log_b"], log_len=l["log_len"], conv_w=self.w, dev_error=self.err)
+                                 log_beta=l["log_b"], log_len=l["log_len"], conv_w=self.w, dev_error=self.err,
+                                 boundary_rows=l["brows"], boundary_page=l["bpage"])
 
     def bytes_per_layer(self):
         sh = self.sh
-        return self.n * (2 * sh.payload_bytes + self.rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4))
+        pages = 3 if self.boundary else 2          # + the boundary checkpoint written
+        return self.n * (pages * sh.payload_bytes + self.rows * (sh.conv_dim * 2 + 2 * sh.num_v_heads * 4))
 
     def time_us_per_layer(self, reps: int = 5) -> float:
         self.flush()
@@ -375,16 +382,20 @@ class FlushSweep:
 
 def flush_sweep(seed: int, hbm_gbs: float):
     """Flush time per layer: every log length R = 1..32 at N = 16 requests,
-    and R = 16 at N = 64 and 256 (4B-shaped layer)."""
+    R = 16 at N = 64 and 256, and R = 16 at N = 16 with every request's kept
+    rows crossing a block boundary after 8 rows (4B-shaped layer)."""
     out = []
-    cases = [(16, r) for r in range(1, 33)] + [(64, 16), (256, 16)]
-    for n_req, rows in cases:
+    cases = [(16, r, 0) for r in range(1, 33)] + [(64, 16, 0), (256, 16, 0), (16, 16, 8)]
+    for n_req, rows, bnd in cases:
         layers = max(2, 128 // n_req)          # 2.5 MiB pages: >= 320 MB of pools per replay
-        fs = FlushSweep(seed + 31 * rows + n_req, n_req, rows, layers)
+        fs = FlushSweep(seed + 31 * rows + n_req, n_req, rows, layers, boundary=bnd)
         us = fs.time_us_per_layer()
         gbs = fs.bytes_per_layer() / (us * 1e-6) / 1e9
-        out.append({"N": n_req, "R": rows, "us_per_layer": round(us, 2), "hbm_gbs": round(gbs, 1),
-                    "hbm_frac": round(gbs / hbm_gbs, 3)})
+        case = {"N": n_req, "R": rows, "us_per_layer": round(us, 2), "hbm_gbs": round(gbs, 1),
+                "hbm_frac": round(gbs / hbm_gbs, 3)}
+        if bnd:
+            case["boundary_after"] = bnd
+        out.append(case)
         del fs
     torch.cuda.empty_cache()
     return out

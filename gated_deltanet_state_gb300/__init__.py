@@ -26,7 +26,7 @@ __all__ = [
     "GdnError", "LayerShape", "StatePool", "load_library", "library_path", "make_desc",
     "gdn_status_string", "gdn_version", "gdn_conv_dim", "gdn_mamba_page_bytes",
     "gdn_block_size_for", "gdn_mamba_pages_per_request", "gdn_pool_blocks_for_pages",
-    "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_spec_copy_bytes",
+    "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_replay_boundary_rows", "gdn_spec_copy_bytes",
     "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
     "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "workspace_for", "NOALLOC_SCRATCH_BYTES",
     "gdn_mixed_workspace_size", "gdn_mixed_step",
@@ -110,7 +110,8 @@ class _ReplayArgs(ctypes.Structure):
     _fields_ = [("num_reqs", ctypes.c_int32), ("num_new", ctypes.c_int32), ("ckpt_slot", _P),
                 ("log_x", _P), ("log_g", _P), ("log_beta", _P), ("log_len", _P), ("x_new", _P),
                 ("g_new", _P), ("beta_new", _P), ("conv_w", _P), ("o", _P), ("dev_error", _P),
-                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", _P), ("workspace_bytes", ctypes.c_size_t), ("boundary_rows", _P),
+                ("boundary_page", _P)]
 
 
 # --------------------------------------------------------------------------- loading
@@ -144,6 +145,7 @@ def load_library(build_if_missing: bool = True):
         "gdn_chunk_end": ([i64, i64, i64, i32], i64),
         "gdn_cached_tokens": ([i64, i32], i64),
         "gdn_resume_block": ([i64, i32, ctypes.POINTER(i32)], i32),
+        "gdn_replay_boundary_rows": ([i64, i32, i32], i32),
         "gdn_spec_copy_bytes": ([i32, i32, i64], i64),
         "gdn_replay_bytes_per_request": ([i32, i64, i32, i64], i64),
         "gdn_prefill_workspace_size": ([D, i32, i64], sz),
@@ -292,6 +294,10 @@ def gdn_resume_block(hit_tokens: int, block_size: int) -> int:
     out = ctypes.c_int32(0)
     _check(load_library().gdn_resume_block(hit_tokens, block_size, ctypes.byref(out)), "gdn_resume_block")
     return int(out.value)
+
+
+def gdn_replay_boundary_rows(absorbed: int, kept: int, block_size: int) -> int:
+    return int(load_library().gdn_replay_boundary_rows(absorbed, kept, block_size))
 
 
 def gdn_spec_copy_bytes(draft_tokens: int, num_gdn_layers: int, page_bytes: int) -> int:
@@ -499,7 +505,8 @@ def gdn_checkpoint_save(shape: LayerShape, pool: StatePool, src_page, dst_page, 
 
 
 def _replay_args(shape, *, ckpt_slot, log_x, log_g, log_beta, log_len, conv_w, dev_error,
-                 x_new=None, g_new=None, beta_new=None, o=None, num_new=0, workspace=None):
+                 x_new=None, g_new=None, beta_new=None, o=None, num_new=0, workspace=None,
+                 boundary_rows=None, boundary_page=None):
     if workspace is None:
         workspace = workspace_for(gdn_replay_workspace_size(shape, int(ckpt_slot.numel())), log_x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -509,7 +516,9 @@ def _replay_args(shape, *, ckpt_slot, log_x, log_g, log_beta, log_len, conv_w, d
                        _dev(x_new, shape.torch_in(), "x_new"), _dev(g_new, torch.float32, "g_new"),
                        _dev(beta_new, torch.float32, "beta_new"), _dev(conv_w, torch.float32, "conv_w"),
                        _dev(o, shape.torch_out(), "o"), _dev(dev_error, torch.int32, "dev_error"),
-                       _dev(workspace, None, "workspace"), ws_bytes)
+                       _dev(workspace, None, "workspace"), ws_bytes,
+                       _dev(boundary_rows, torch.int32, "boundary_rows"),
+                       _dev(boundary_page, torch.int32, "boundary_page"))
 
 
 def gdn_replay_append(shape: LayerShape, pool: StatePool, *, ckpt_slot, log_x, log_g, log_beta, log_len,
@@ -536,11 +545,15 @@ def gdn_replay_rollback(log_len, accepted, num_appended: int, dev_error, stream=
 
 
 def gdn_replay_flush(shape: LayerShape, pool: StatePool, *, ckpt_slot, log_x, log_g, log_beta, log_len,
-                     conv_w, dev_error, workspace=None, stream=None, raise_on_error: bool = True) -> int:
-    """Apply the logged rows to the checkpoint page in place; empties the log."""
+                     conv_w, dev_error, workspace=None, boundary_rows=None, boundary_page=None, stream=None,
+                     raise_on_error: bool = True) -> int:
+    """Apply the logged rows to the checkpoint page in place; empties the log.
+    With boundary_rows / boundary_page, the state after the first j kept rows
+    is also written to a block-boundary page."""
     lib = load_library()
     keep, a = _replay_args(shape, ckpt_slot=ckpt_slot, log_x=log_x, log_g=log_g, log_beta=log_beta,
-                           log_len=log_len, conv_w=conv_w, dev_error=dev_error, workspace=workspace)
+                           log_len=log_len, conv_w=conv_w, dev_error=dev_error, workspace=workspace,
+                           boundary_rows=boundary_rows, boundary_page=boundary_page)
     st = lib.gdn_replay_flush(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
                               _stream(stream))
     return _check(st, "gdn_replay_flush") if raise_on_error else st

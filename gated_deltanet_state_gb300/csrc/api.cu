@@ -391,6 +391,11 @@ static gdn_status replay_common(const gdn_layer_desc* desc, const gdn_pool* pool
     if (a->num_new > GDN_REPLAY_LOG_SLOTS) return GDN_ERR_LOG_OVERFLOW;
     if (a->num_new > 0 && (!a->x_new || !a->g_new || !a->beta_new || !a->o)) return GDN_ERR_INVALID_ARG;
   }
+  if (!append && a->boundary_rows) {
+    // boundary checkpoints are written by the tensor-core flush only
+    if (!a->boundary_page) return GDN_ERR_INVALID_ARG;
+    if (!tc_replay_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype)) return GDN_ERR_UNSUPPORTED_SHAPE;
+  }
   const size_t need = gdn_replay_workspace_size(desc, a->num_reqs);
   if (!a->workspace || a->workspace_bytes < need || !aligned16(a->workspace)) return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
@@ -408,6 +413,8 @@ static gdn_status replay_common(const gdn_layer_desc* desc, const gdn_pool* pool
   p.x_new = a->x_new;
   p.g_new = a->g_new;
   p.beta_new = a->beta_new;
+  p.boundary_rows = append ? nullptr : a->boundary_rows;
+  p.boundary_page = append ? nullptr : a->boundary_page;
   *out = p;
   return GDN_OK;
 }

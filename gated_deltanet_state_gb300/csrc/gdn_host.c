@@ -85,6 +85,15 @@ int64_t gdn_cached_tokens(int64_t shared_tokens, int32_t block_size) {
   return full >= 2 ? (full - 1) * block_size : 0;
 }
 
+int32_t gdn_replay_boundary_rows(int64_t absorbed, int32_t kept, int32_t block_size) {
+  if (absorbed < 0 || kept < 0 || block_size <= 0) return -1;
+  /* first multiple of block_size above absorbed */
+  const int64_t first = (absorbed / block_size + 1) * block_size;
+  if (first > absorbed + kept) return 0;
+  if (first + block_size <= absorbed + kept) return -1;   /* a second boundary */
+  return (int32_t)(first - absorbed);
+}
+
 gdn_status gdn_resume_block(int64_t hit_tokens, int32_t block_size, int32_t* out_block) {
   if (!out_block || hit_tokens < 0 || block_size <= 0) return GDN_ERR_INVALID_ARG;
   if (hit_tokens % block_size != 0) return GDN_ERR_NOT_BLOCK_ALIGNED;

@@ -75,6 +75,8 @@ struct ScanParams {
   const void* x_new;
   const float* g_new;
   const float* beta_new;
+  const int32_t* boundary_rows;   // flush: kept rows up to a block boundary ([N], optional)
+  const int32_t* boundary_page;   // flush: the boundary checkpoint's page ([N])
   // workspace written by the conv pre-pass, read by the scan
   float* ws_y;     // [rows][conv_dim]   SiLU(conv) of every channel
   float* ws_nrm;   // [rows][2*Hqk]      q (times q_scale) and k norm factors

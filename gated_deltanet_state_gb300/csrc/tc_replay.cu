@@ -134,9 +134,13 @@ __device__ __forceinline__ void rp_back_solve(float (&x)[NMAX], const float* am)
   }
 }
 
-template <int NMAX, bool APPEND>
+// BND: a flush that also writes a block-boundary checkpoint after its first
+// bj kept rows (a separate instantiation: the common path compiles as if the
+// boundary code did not exist).
+template <int NMAX, bool APPEND, bool BND = false>
 __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorMap* tmap, int h, int r,
-                                            int32_t page, int n, int L) {
+                                            int32_t page, int n, int L, int bj_arg = 0, int32_t bpage = -1) {
+  const int bj = BND ? bj_arg : 0;
   using TIN = __nv_bfloat16;
   using S = RpSmem<NMAX, APPEND>;
   using C = RpCols<APPEND>;
@@ -238,7 +242,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
   //   -> tensor memory, and its new conv window (the last three rows of
   //   window || log) to the page (this CTA alone reads this head's v channels).
   float y[32];
-  TIN wv3[3];
+  TIN wv3[3], wb3[3];
   {
     auto conv_col = [&](int sc, const float4& cw) {
       float x[NMAX + 3];
@@ -267,8 +271,9 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
       tc::tmem_st32(tbase + tlane + C::V, y);
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
-        const int t = n + j;   // position in window || log
+        const int t = n + j, tb = bj + j;   // positions in window || log
         wv3[j] = t < 3 ? xwin[t * S::CH + D + row] : xlog[(t - 3) * S::CH + D + row];
+        if (BND) wb3[j] = tb < 3 ? xwin[tb * S::CH + D + row] : xlog[(tb - 3) * S::CH + D + row];
       }
       tc::tmem_st_wait();
     }
@@ -290,6 +295,11 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
     TIN* wdst = win + cv0 + row;
 #pragma unroll
     for (int j = 0; j < 3; ++j) wdst[(int64_t)j * p.conv_dim] = wv3[j];
+    if (BND) {
+      TIN* bdst = page_window<TIN>(p.pool, bpage) + cv0 + row;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) bdst[(int64_t)j * p.conv_dim] = wb3[j];
+    }
   }
   if (APPEND && half == 1) {
     // the m new rows join the log after the n logged ones: this head's v
@@ -382,7 +392,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
       rp_split8(sm + S::A1 + off, sm + S::A1_LO + off, sv + 8 * c8);
     }
     if (!APPEND) {
-      const float gN = gam[L - 1];
+      const float gN = gam[(BND ? bj : L) - 1];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         float v[32];
@@ -538,10 +548,16 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
   // B2.  Second half (D1 done): R^T -> A2 for state row `row`.  Both go to
   // A1, which D1's product has finished reading once its barrier fires.
   bool ok1;
+  float kt[NMAX];
   if (ok && half == 0) {
-    float kt[NMAX];
+    if (BND) {
+      const float Gb = Gs[bj - 1];
 #pragma unroll
-    for (int l = 0; l < NMAX; ++l) kt[l] = dec[l] * fk[l] * kf[l * S::KF_LD + row];
+      for (int l = 0; l < NMAX; ++l) kt[l] = l < bj ? __expf(Gb - Gs[l]) * fk[l] * kf[l * S::KF_LD + row] : 0.f;
+    } else {
+#pragma unroll
+      for (int l = 0; l < NMAX; ++l) kt[l] = dec[l] * fk[l] * kf[l * S::KF_LD + row];
+    }
     rp_back_solve<NMAX, S::AM_LD>(kt, am);
     ok1 = tc::mbar_wait_bounded(mbar_1, 0, kRpWait);
     if (ok1) {
@@ -592,8 +608,63 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
     }
     tc::mma_commit(mbar_2);
   }
+  if (BND) {
+    // a block boundary after the first bj rows: D2 now holds that state.
+    // The first half solves for the remaining rows meanwhile; every thread
+    // writes its 64 columns of the boundary state to the boundary page,
+    // scales them to the end of the log, and the second product adds the
+    // rows from bj on: S = exp(G_{L-1} - G_{bj-1}) S_bj + R^T Kt_b.
+    if (ok && half == 0) {
+#pragma unroll
+      for (int l = 0; l < NMAX; ++l) kt[l] = l >= bj ? dec[l] * fk[l] * kf[l * S::KF_LD + row] : 0.f;
+      rp_back_solve<NMAX, S::AM_LD>(kt, am);
+    }
+    if (ok) {
+      const bool okb = tc::mbar_wait_bounded(mbar_2, 0, kRpWait);
+      ok = __syncthreads_and(okb);
+    }
+    tc::fence_after_sync();
+    if (ok) {
+      if (half == 0) {   // the first product has read B2: the remaining rows' Kt^T replace it
+#pragma unroll
+        for (int c8 = 0; c8 < NMAX / 8; ++c8) {
+          const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
+          rp_split8(sm + S::B2 + off, sm + S::B2_LO + off, kt + 8 * c8);
+        }
+      }
+      const float scale = __expf(Gs[L - 1] - Gs[bj - 1]);
+      float* bst = page_state(p.pool, bpage) + ((int64_t)h * D + row) * D + 64 * half;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float v[32];
+        tc::tmem_ld32(tbase + tlane + C::D2 + 64 * half + 32 * q, v);
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(bst + 32 * q + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] *= scale;
+        tc::tmem_st32(tbase + tlane + C::D2 + 64 * half + 32 * q, v);
+      }
+      tc::tmem_st_wait();
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    ok = __syncthreads_and(ok);
+    tc::fence_after_sync();
+    if (ok && tid == kIssue) {
+      const uint32_t idesc = tc::idesc_bf16_f32(D, D);
+      constexpr int nks = NMAX / 16;
+      for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t a = sbase + (pass == 2 ? S::A2_LO : S::A2);
+        const uint32_t b = sbase + (pass == 1 ? S::B2_LO : S::B2);
+        for (int ks = 0; ks < nks; ++ks)
+          tc::mma_bf16(tbase + C::D2, tc::desc_sw128(a + ks * 32), tc::desc_sw128(b + ks * 32), idesc, 1u);
+      }
+      tc::mma_commit(mbar_2);
+    }
+  }
   if (ok) {
-    const bool ok2 = tc::mbar_wait_bounded(mbar_2, 0, kRpWait);
+    const bool ok2 = tc::mbar_wait_bounded(mbar_2, BND ? 1 : 0, kRpWait);
     ok = __syncthreads_and(ok2);
   }
   tc::fence_after_sync();
@@ -624,7 +695,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
     // for the work it may still hold, then release the tensor memory
     if (tid == 0) set_error(p.err, GDN_ERR_TIMEOUT);
     tc::mbar_wait_bounded(mbar_1, 0, kRpWait);
-    tc::mbar_wait_bounded(mbar_2, 0, kRpWait);
+    tc::mbar_wait_bounded(mbar_2, BND ? 1 : 0, kRpWait);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -643,21 +714,31 @@ __global__ void __launch_bounds__(kQkWinThreads) flush_qk_window_kernel(const Sc
   const int r = blockIdx.x;
   const int32_t page = p.ckpt_slot[r];
   const int32_t n = p.log_len[r];
-  if (!page_ok(p.pool, page) || n < 0 || n > kRpMaxRows) return;   // reported by the flush kernel
+  // the flush kernel's validation (it reports the errors)
+  if (!page_ok(p.pool, page) || n < 0 || n > kRpMaxRows) return;
+  const int bj = (p.boundary_rows && n > 0) ? p.boundary_rows[r] : 0;
+  const int32_t bpage = bj > 0 ? p.boundary_page[r] : -1;
+  if (bj > 0 && (bj > n || bpage == page || !page_ok(p.pool, bpage))) return;
   if (n > 0) {
     TIN* win = page_window<TIN>(p.pool, page);
+    TIN* bwin = bj > 0 ? page_window<TIN>(p.pool, bpage) : nullptr;
     const TIN* lx = reinterpret_cast<const TIN*>(p.log_x) + (int64_t)r * kRpMaxRows * p.conv_dim;
     const int chunks = 2 * p.Hqk * kRpD / 8;
+    auto src = [&](int t) {   // row t of window || log
+      return t < kWinRows ? win + (int64_t)t * p.conv_dim : lx + (int64_t)(t - kWinRows) * p.conv_dim;
+    };
     for (int c = threadIdx.x; c < chunks; c += kQkWinThreads) {
-      uint4 keep[kWinRows];
+      uint4 keep[kWinRows], kb[kWinRows];
 #pragma unroll
       for (int j = 0; j < kWinRows; ++j) {
-        const int t = n + j;   // position in window || log
-        const TIN* src = t < kWinRows ? win + (int64_t)t * p.conv_dim : lx + (int64_t)(t - kWinRows) * p.conv_dim;
-        keep[j] = *reinterpret_cast<const uint4*>(src + 8 * c);
+        keep[j] = *reinterpret_cast<const uint4*>(src(n + j) + 8 * c);
+        if (bwin) kb[j] = *reinterpret_cast<const uint4*>(src(bj + j) + 8 * c);
       }
 #pragma unroll
-      for (int j = 0; j < kWinRows; ++j) *reinterpret_cast<uint4*>(win + (int64_t)j * p.conv_dim + 8 * c) = keep[j];
+      for (int j = 0; j < kWinRows; ++j) {
+        *reinterpret_cast<uint4*>(win + (int64_t)j * p.conv_dim + 8 * c) = keep[j];
+        if (bwin) *reinterpret_cast<uint4*>(bwin + (int64_t)j * p.conv_dim + 8 * c) = kb[j];
+      }
     }
   }
   __syncthreads();
@@ -686,8 +767,31 @@ __global__ void __launch_bounds__(kRpThreads, 2) tc_flush_kernel(const ScanParam
     return;
   }
   if (n == 0) return;   // nothing logged: the state stays as it is
+  if (p.boundary_rows && p.boundary_rows[r] > 0) return;   // tc_flush_boundary_kernel's request
   if (n <= 16) replay_body<16, false>(p, &tmap, h, r, page, n, n);
   else replay_body<32, false>(p, &tmap, h, r, page, n, n);
+}
+
+// The requests of a flush whose kept rows cross a block boundary (prefix
+// caching): also the state and conv window after the first bj rows, to the
+// boundary page.  A kernel of its own, launched only when the call passes
+// boundary rows, so that the common flush compiles without this path.
+__global__ void __launch_bounds__(kRpThreads, 2) tc_flush_boundary_kernel(const ScanParams p,
+                                                                          const __grid_constant__ CUtensorMap tmap) {
+  const int h = blockIdx.x, r = blockIdx.y;
+  const int bj = p.boundary_rows[r];
+  if (bj <= 0) return;
+  const int32_t page = p.ckpt_slot[r];
+  const int32_t n = p.log_len[r];
+  if (!page_ok(p.pool, page) || n < 0 || n > kRpMaxRows) return;   // reported by tc_flush_kernel
+  const int32_t bpage = p.boundary_page[r];
+  if (bj > n || bpage == page || !page_ok(p.pool, bpage)) {
+    if (h == 0 && threadIdx.x == 0)
+      set_error(p.err, page_ok(p.pool, bpage) ? GDN_ERR_INVALID_ARG : GDN_ERR_PAGE_RANGE);
+    return;
+  }
+  if (n <= 16) replay_body<16, false, true>(p, &tmap, h, r, page, n, n, bj, bpage);
+  else replay_body<32, false, true>(p, &tmap, h, r, page, n, n, bj, bpage);
 }
 
 __global__ void __launch_bounds__(kRpThreads, 2) tc_append_kernel(const ScanParams p,
@@ -752,6 +856,13 @@ cudaError_t launch_tc_flush(const ScanParams& p, cudaStream_t st) {
   tc_flush_kernel<<<dim3(p.Hv, p.num_seqs), kRpThreads, smem, st>>>(p, tmap);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.boundary_rows) {
+    e = cudaFuncSetAttribute(tc_flush_boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tc_flush_boundary_kernel<<<dim3(p.Hv, p.num_seqs), kRpThreads, smem, st>>>(p, tmap);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   flush_qk_window_kernel<<<p.num_seqs, kQkWinThreads, 0, st>>>(p);
   return cudaGetLastError();
 }

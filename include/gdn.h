@@ -175,6 +175,18 @@ int64_t gdn_cached_tokens(int64_t shared_tokens, int32_t block_size);
  * "The in-page layout": fail closed on a resume off a block boundary). */
 gdn_status gdn_resume_block(int64_t hit_tokens, int32_t block_size, int32_t* out_block);
 
+/* Kept rows after which a replay flush crosses a block boundary: a request
+ * whose checkpoint has absorbed `absorbed` tokens flushes `kept` logged rows,
+ * and the state after the first j of them lies on a block boundary when
+ * absorbed + j is a positive multiple of block_size.  Returns that j in
+ * [1, kept], or 0 when no boundary is crossed; -1 for bad arguments or when
+ * the rows cross more than one boundary (the flush writes one boundary
+ * checkpoint; flush earlier).  ("Prefix caching on Gated DeltaNet hybrids",
+ * "The in-page layout": a block's checkpoint is the state at its boundary;
+ * "Caching less to serve more requests", "Other models": serving the replay
+ * scheme with prefix caching.) */
+int32_t gdn_replay_boundary_rows(int64_t absorbed, int32_t kept, int32_t block_size);
+
 /* Bytes that per-position speculative state copies take for one request:
  * (draft_tokens + 1) * num_gdn_layers * page_bytes ("Caching less to serve
  * more requests", "Where the memory goes": (15+1) x 24 x 2.5 MiB = 960 MiB). */
@@ -401,7 +413,15 @@ gdn_status gdn_checkpoint_save(const gdn_layer_desc* desc, const gdn_pool* pool,
  *   [0, num_appended] or beyond the log sets GDN_ERR_ROLLBACK_RANGE and leaves
  *   log_len[r] unchanged.
  * flush: applies the log_len[r] logged rows to the checkpoint page (state and
- *   conv window, in place) as one block and sets log_len[r] = 0. */
+ *   conv window, in place) as one block and sets log_len[r] = 0.  With
+ *   boundary_rows given (prefix caching), a request with j = boundary_rows[r]
+ *   in [1, log_len[r]] also gets the state and conv window after its first j
+ *   kept rows written to page boundary_page[r] (a block-boundary checkpoint,
+ *   see gdn_replay_boundary_rows); j <= 0 writes none.  j > log_len[r] or a
+ *   boundary page equal to the checkpoint page sets GDN_ERR_INVALID_ARG, a
+ *   boundary page outside the pool GDN_ERR_PAGE_RANGE; such a request is left
+ *   unchanged.  Boundary checkpoints need the tensor-core path (dk = dv = 128,
+ *   bf16): other shapes return GDN_ERR_UNSUPPORTED_SHAPE before any launch. */
 typedef struct gdn_replay_args {
   int32_t num_reqs;              /* N >= 0; ckpt slots must be distinct       */
   int32_t num_new;               /* m, append only: 0 <= m <= 32              */
@@ -418,6 +438,8 @@ typedef struct gdn_replay_args {
   int32_t* dev_error;
   void* workspace;               /* device scratch, >= gdn_replay_workspace_size */
   size_t workspace_bytes;
+  const int32_t* boundary_rows;  /* [N] flush only, optional (NULL: none)     */
+  const int32_t* boundary_page;  /* [N] page ids, required with boundary_rows */
 } gdn_replay_args;
 
 /* Device workspace bytes of gdn_replay_append / gdn_replay_flush for

@@ -124,6 +124,20 @@ def test_replay_rejects_oversized_append_and_bad_rollback_args():
     assert lib.gdn_replay_rollback(0x10000, 0x10000, 40, 2, 0x10000, None) == gdn.STATUS_CODE["GDN_ERR_INVALID_ARG"]
 
 
+def test_flush_boundary_checkpoint_host_checks():
+    """Boundary checkpoints need both arrays and the tensor-core shape; the
+    checks run before any launch (the device pointers are fake)."""
+    lib = gdn.load_library()
+    F = 0x10000
+    for sh, bpage, want in ((inputs.QWEN4B, None, "GDN_ERR_INVALID_ARG"),
+                            (inputs.TINY, F, "GDN_ERR_UNSUPPORTED_SHAPE")):
+        desc = gdn.make_desc(sh)
+        pool = gdn._Pool(0x100000, sh.page, 8, 0)
+        r = gdn._ReplayArgs(2, 0, *([F] * 11), F, 1 << 40, F, bpage)
+        assert lib.gdn_replay_flush(ctypes.byref(desc), ctypes.byref(pool), ctypes.byref(r), None) == \
+            gdn.STATUS_CODE[want], sh
+
+
 def test_empty_batches_are_no_ops():
     lib = gdn.load_library()
     sh = inputs.TINY

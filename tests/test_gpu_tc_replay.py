@@ -19,10 +19,11 @@ SH = inputs.LayerShape(2, 4, 128, 128, 64, 16)          # d 128, bf16 in / out: 
 
 
 class Log:
-    def __init__(self, sh, N, seed):
+    def __init__(self, sh, N, seed, extra_pages=3):
         self.sh, self.N = sh, N
-        self.pool = gdn.StatePool(sh, N + 3, fill=0xFF)
-        self.slots = inputs.permutation(N + 3, seed).tolist()[:N]
+        self.pool = gdn.StatePool(sh, N + extra_pages, fill=0xFF)
+        self.perm = inputs.permutation(N + extra_pages, seed).tolist()
+        self.slots = self.perm[:N]
         self.st = inputs.random_state(sh, N, seed)
         for i, p in enumerate(self.slots):
             self.pool.state(p).copy_(self.st["S"][i].cuda())
@@ -134,3 +135,55 @@ def test_append_overflow_and_bad_page_are_reported():
     assert R.err.item() == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
     assert R.log_len.cpu().tolist() == [4, 0]
     assert torch.isnan(o[1].float()).all()
+
+
+@pytest.mark.parametrize("lens,bjs", [([5, 16, 17, 32], [2, 16, 3, 31]), ([20, 9, 32, 1], [17, 0, 32, 1]),
+                                      ([12, 30], [0, 29])])
+def test_flush_writes_the_block_boundary_checkpoint(lens, bjs):
+    """Replay with prefix caching: the state and conv window after the first
+    j kept rows go to the boundary page, the checkpoint absorbs all rows."""
+    N = len(lens)
+    R = Log(SH, N, seed=sum(lens) + 3, extra_pages=N + 1)
+    bpages = R.perm[N:2 * N]
+    R.log_len.copy_(torch.tensor(lens, dtype=torch.int32))
+    lx, lg, lb = R.host_log()
+    before = {p: R.pool.payload(p).cpu().clone() for p in bpages}
+    gdn.gdn_replay_flush(SH, R.pool, boundary_rows=dev(bjs, torch.int32), boundary_page=dev(bpages, torch.int32),
+                         **R.kw())
+    torch.cuda.synchronize()
+    assert R.err.item() == 0 and R.log_len.cpu().tolist() == [0] * N
+    d, S0, w0 = dims(SH), R.st["S"].double().numpy(), R.st["win"].float().numpy()
+    S_ref, win_ref = oracle.replay_flush(d, R.w, S0, w0, lx, lg, lb, lens)
+    assert_state_close(torch.stack([R.pool.state(p) for p in R.slots]).cpu(), S_ref)
+    Sb_ref, winb_ref = oracle.replay_flush(d, R.w, S0, w0, lx, lg, lb, [max(b, 0) for b in bjs])
+    for r, (p, bp, bj) in enumerate(zip(R.slots, bpages, bjs)):
+        assert torch.equal(R.pool.window(p).cpu().float(), torch.as_tensor(win_ref[r], dtype=torch.float32))
+        if bj > 0:
+            assert_state_close(R.pool.state(bp).cpu()[None], Sb_ref[r:r + 1])
+            assert torch.equal(R.pool.window(bp).cpu().float(), torch.as_tensor(winb_ref[r], dtype=torch.float32))
+        else:
+            assert torch.equal(R.pool.payload(bp).cpu(), before[bp])
+
+
+def test_flush_boundary_errors_leave_the_request_unchanged():
+    N = 3
+    R = Log(SH, N, seed=41, extra_pages=N + 1)
+    free = R.perm[N]
+    R.log_len.copy_(torch.tensor([8, 8, 8], dtype=torch.int32))
+    before = torch.stack([R.pool.payload(p) for p in R.slots]).cpu()
+    # request 0: j beyond the log; 1: boundary page = its checkpoint; 2: page outside the pool
+    bjs = dev([9, 4, 4], torch.int32)
+    for bp, code in (([free, R.slots[1], free], "GDN_ERR_INVALID_ARG"),):
+        gdn.gdn_replay_flush(SH, R.pool, boundary_rows=bjs, boundary_page=dev(bp, torch.int32), **R.kw())
+        torch.cuda.synchronize()
+        assert R.err.item() == gdn.STATUS_CODE[code]
+    after = torch.stack([R.pool.payload(p) for p in R.slots]).cpu()
+    assert torch.equal(after[:2], before[:2]) and R.log_len.cpu().tolist()[:2] == [8, 8]
+    assert R.log_len.cpu().tolist()[2] == 0      # request 2 had a valid boundary
+    R.err.zero_()
+    R.log_len.copy_(torch.tensor([8, 8, 8], dtype=torch.int32))
+    gdn.gdn_replay_flush(SH, R.pool, boundary_rows=dev([0, 0, 4], torch.int32),
+                         boundary_page=dev([free, free, 1000], torch.int32), **R.kw())
+    torch.cuda.synchronize()
+    assert R.err.item() == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
+    assert R.log_len.cpu().tolist() == [0, 0, 8]

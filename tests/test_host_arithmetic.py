@@ -103,3 +103,25 @@ def test_27b_config_block_geometry():
     # (state after 199,808 tokens); the cached-token rule stops one block earlier
     assert gdn.gdn_resume_block(200_000 // 896 * 896, 896) == 222
     assert gdn.gdn_cached_tokens(200_000, 896) == 198_912
+
+
+def _boundary_rows_brute(absorbed, kept, block):
+    # the states after 1..kept more rows sit at absorbed + j; block boundaries are positive multiples
+    hits = [j for j in range(1, kept + 1) if (absorbed + j) % block == 0]
+    return 0 if not hits else (hits[0] if len(hits) == 1 else -1)
+
+
+def test_replay_boundary_rows():
+    # a flush of kept rows crosses at most one boundary for blocks above 32 rows
+    cases = [(0, 16, 64, 0), (60, 16, 64, 4), (64, 16, 64, 0), (48, 16, 64, 16), (63, 1, 64, 1),
+             (10, 200, 64, -1), (199808 - 5, 16, 896, 5), (199808, 32, 896, 0), (0, 0, 64, 0)]
+    for absorbed, kept, block, want in cases:
+        assert gdn.gdn_replay_boundary_rows(absorbed, kept, block) == want, (absorbed, kept, block)
+    for block in (16, 64, 784, 896):
+        for absorbed in list(range(0, 3 * block, 7)) + [5 * block - 1, 5 * block]:
+            for kept in (0, 1, 15, 16, 17, 31, 32):
+                assert gdn.gdn_replay_boundary_rows(absorbed, kept, block) == \
+                    _boundary_rows_brute(absorbed, kept, block), (absorbed, kept, block)
+    assert gdn.gdn_replay_boundary_rows(-1, 4, 64) == -1
+    assert gdn.gdn_replay_boundary_rows(0, -1, 64) == -1
+    assert gdn.gdn_replay_boundary_rows(0, 4, 0) == -1
