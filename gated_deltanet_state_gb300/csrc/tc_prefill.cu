@@ -27,8 +27,8 @@
 //   (B) S0 from tensor memory into a bf16 operand (and gam_C S0 back);
 //       tensor cores: [K^K^T; Q^K^T] and S0 [K^; Q^]^T.
 //   (C) A and P = exp(G_i - G_j) q^_i.k^_j (j <= i) (computed while the
-//       tensor core forms S0 [K^; Q^]^T); T = (I + A)^{-1} by one warpgroup
-//       (16 x 16 blocks) while the other forms R_i = b_i (v_i - gam_i S0 k^_i);
+//       tensor core forms S0 [K^; Q^]^T); T = (I + A)^{-1} by two warpgroups
+//       (16 x 16 blocks) while the others form R_i = b_i (v_i - gam_i S0 k^_i);
 //       tensor cores: U^T = R T^T.
 //   (D) tensor cores: S += U^T (K^T diag(exp(G_C - G)))^T in tensor memory and
 //       U^T P^T; outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i.
@@ -44,9 +44,9 @@ namespace gdn {
 
 namespace {
 
-constexpr int kPfWorkers = 256;         // eight warps of CUDA-core work
+constexpr int kPfWorkers = 512;         // sixteen warps of CUDA-core work
 constexpr int kPfThreads = kPfWorkers + 32;   // + one warp that issues the tensor-core products
-constexpr int kMmaTid = kPfWorkers;      // the issuing thread (lane 0 of the ninth warp)
+constexpr int kMmaTid = kPfWorkers;      // the issuing thread (lane 0 of the seventeenth warp)
 constexpr int kPfC = 64;                 // chunk rows
 constexpr int kPfD = 128;                // dk = dv
 constexpr int kPfXRows = kPfC + kWinRows;
@@ -132,19 +132,19 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a, uint32_t a_lo, uint
   }
 }
 
-// Barrier of the eight worker warps alone (threads 0..255).
-__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
+// Barrier of the sixteen worker warps alone (threads 0..511).
+__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 512;\n" ::: "memory"); }
 
-// Barrier of the second warpgroup alone (threads 128..255).
-__device__ __forceinline__ void wg1_sync() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// Barrier of the threads that build T (256..511).
+__device__ __forceinline__ void tgrp_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
 // T = (I + A)^{-1} for the 64 x 64 strictly lower triangular A given as A^T
-// (at[j * 64 + i] = A_ij, zero for i <= j), by the 128 threads t of the
-// second warpgroup.  The 16 x 16 diagonal blocks D_b = (I + A_bb)^{-1} by
-// forward substitution (a column per thread), then the blocks below them in
-// order of distance from the diagonal: T_pq = -D_p X, X = sum_{k=q}^{p-1}
-// A_pk T_kq (a 2 x 4 tile per thread).  tf[i * 64 + j] receives T on
-// and below the diagonal (the blocks above it are left unwritten).
+// (at[j * 64 + i] = A_ij, zero for i <= j), by 256 threads t.  The 16 x 16
+// diagonal blocks D_b = (I + A_bb)^{-1} by forward substitution (a column per
+// thread), then the blocks below them in order of distance from the
+// diagonal: T_pq = -D_p X, X = sum_{k=q}^{p-1} A_pk T_kq (a 1 x 4 tile per
+// thread).  tf[i * 64 + j] receives T on and below the diagonal (the blocks
+// above it are left unwritten).
 __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
   if (t < 64) {
     // column sweep: once x_k is final, x_i -= A_ik x_k for every i > k (A^T
@@ -168,53 +168,45 @@ __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) tf[(o + i) * 64 + o + l] = x[i];
   }
-  wg1_sync();
-  // every block of a distance level in one round: 32 tiles of 2 rows x 4
+  tgrp_sync();
+  // every block of a distance level in one round: 64 tiles of 1 row x 4
   // columns per 16 x 16 block, one tile per thread
 #pragma unroll
   for (int d = 1; d < 4; ++d) {
-    const int tasks = (4 - d) * 32;
-    const int q = t >> 5, p = q + d, i2 = 2 * ((t >> 2) & 7), j4 = 4 * (t & 3);
+    const int tasks = (4 - d) * 64;
+    const int q = t >> 6, p = q + d, i = (t >> 2) & 15, j4 = 4 * (t & 3);
     if (t < tasks) {
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int kk = 0; kk < 16 * d; ++kk) {
         const int k = 16 * q + kk;
-        const float2 a = *reinterpret_cast<const float2*>(at + k * 64 + 16 * p + i2);
+        const float a = at[k * 64 + 16 * p + i];
         const float4 b = *reinterpret_cast<const float4*>(tf + k * 64 + 16 * q + j4);
-        a0.x = fmaf(a.x, b.x, a0.x); a0.y = fmaf(a.x, b.y, a0.y);
-        a0.z = fmaf(a.x, b.z, a0.z); a0.w = fmaf(a.x, b.w, a0.w);
-        a1.x = fmaf(a.y, b.x, a1.x); a1.y = fmaf(a.y, b.y, a1.y);
-        a1.z = fmaf(a.y, b.z, a1.z); a1.w = fmaf(a.y, b.w, a1.w);
+        a0.x = fmaf(a, b.x, a0.x); a0.y = fmaf(a, b.y, a0.y);
+        a0.z = fmaf(a, b.z, a0.z); a0.w = fmaf(a, b.w, a0.w);
       }
-      *reinterpret_cast<float4*>(xscr + q * 256 + i2 * 16 + j4) = a0;
-      *reinterpret_cast<float4*>(xscr + q * 256 + (i2 + 1) * 16 + j4) = a1;
+      *reinterpret_cast<float4*>(xscr + q * 256 + i * 16 + j4) = a0;
     }
-    wg1_sync();
+    tgrp_sync();
     if (t < tasks) {
-      // rows i2, i2 + 1 of D_p, read once (zero above its diagonal, so all 16
-      // terms can be taken)
-      float d0[16], d1[16];
+      // row i of D_p, read once (zero above its diagonal, so all 16 terms
+      // can be taken)
+      float d0[16];
 #pragma unroll
       for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 f0 = *reinterpret_cast<const float4*>(tf + (16 * p + i2) * 64 + 16 * p + 4 * m4);
-        const float4 f1 = *reinterpret_cast<const float4*>(tf + (16 * p + i2 + 1) * 64 + 16 * p + 4 * m4);
+        const float4 f0 = *reinterpret_cast<const float4*>(tf + (16 * p + i) * 64 + 16 * p + 4 * m4);
         d0[4 * m4] = f0.x; d0[4 * m4 + 1] = f0.y; d0[4 * m4 + 2] = f0.z; d0[4 * m4 + 3] = f0.w;
-        d1[4 * m4] = f1.x; d1[4 * m4 + 1] = f1.y; d1[4 * m4 + 2] = f1.z; d1[4 * m4 + 3] = f1.w;
       }
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const float4 b = *reinterpret_cast<const float4*>(xscr + q * 256 + m * 16 + j4);
         a0.x = fmaf(-d0[m], b.x, a0.x); a0.y = fmaf(-d0[m], b.y, a0.y);
         a0.z = fmaf(-d0[m], b.z, a0.z); a0.w = fmaf(-d0[m], b.w, a0.w);
-        a1.x = fmaf(-d1[m], b.x, a1.x); a1.y = fmaf(-d1[m], b.y, a1.y);
-        a1.z = fmaf(-d1[m], b.z, a1.z); a1.w = fmaf(-d1[m], b.w, a1.w);
       }
-      *reinterpret_cast<float4*>(tf + (16 * p + i2) * 64 + 16 * q + j4) = a0;
-      *reinterpret_cast<float4*>(tf + (16 * p + i2 + 1) * 64 + 16 * q + j4) = a1;
+      *reinterpret_cast<float4*>(tf + (16 * p + i) * 64 + 16 * q + j4) = a0;
     }
-    wg1_sync();
+    tgrp_sync();
   }
 }
 
@@ -245,7 +237,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool worker = tid < kPfWorkers;
   const int row = tid & 127;                  // state row = tensor-memory lane of this thread
-  const int half = (tid >> 7) & 1;            // column half handled in tensor-memory phases
+  const int quarter = (tid >> 7) & 3;         // column quarter handled in tensor-memory phases
   const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
 
   TokenView<TIN> V;
@@ -293,7 +285,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase + tlane + kColS + 64 * half;   // this thread's 64 state columns
+  const uint32_t tS = tbase + tlane + kColS + 32 * quarter;   // this thread's 32 state columns
 
   // chunk c's pre-conv rows t0-3 .. t0+63 (three TMA tiles: q, k, v channels;
   // rows outside x read as zeros) and its gates (zeros past the end).  Run by
@@ -324,8 +316,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     x_issued = 0;
   }
 
-  // conv taps of this thread's q | k channel (tid) and v channel (row); the
-  // packed core's norm scale at the channels this lane normalises
+  // conv taps of this thread's q | k channel (tid mod 256) and v channel
+  // (row); the packed core's norm scale at the channels this lane normalises
+  const int qkc = tid & 255;
   float4 wqk = make_float4(0.f, 0.f, 0.f, 0.f), wv = wqk;
   float nwr[4] = {0.f, 0.f, 0.f, 0.f};
   if (worker && p.norm_w) {
@@ -333,21 +326,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int m = 0; m < 4; ++m) nwr[m] = p.norm_w[lane + 32 * m];
   }
   if (worker) {
-    const int qkch = tid < D ? cq0 + tid : ck0 + tid - D;
+    const int qkch = qkc < D ? cq0 + qkc : ck0 + qkc - D;
     wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
     wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + row) * kConvK);
     // initial state (zeros on a cold start: the pool is not read)
-    const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
+    const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+    float v[32];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float v[32];
-#pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 f = src ? reinterpret_cast<const float4*>(src + 32 * q)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
-      }
-      tc::tmem_st32(tS + 32 * q, v);
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 f = src ? reinterpret_cast<const float4*>(src)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
     }
+    tc::tmem_st32(tS, v);
     tc::tmem_st_wait();
   }
 
@@ -386,16 +376,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         workers_sync();
       }
 
-      // ---- (A) conv + SiLU.  q | k channel tid for all 64 rows -> y, in
-      // blocks of 16 rows whose loads all precede their stores.  Rows past
-      // the end are computed too and masked later: their norm factors and b
-      // are zero, so they contribute nothing (no data-dependent branch around
+      // ---- (A) conv + SiLU.  q | k channel tid mod 256 for rows [32 rh, +32)
+      // -> y, in blocks of 16 rows whose loads all precede their stores.  Rows
+      // past the end are computed too and masked later: their norm factors and
+      // b are zero, so they contribute nothing (no data-dependent branch around
       // the SiLU)
       {
-        const TIN* xc_ = tid < D ? xq + tid : xk + tid - D;
-        float xa = to_f32(xc_[0]), xb = to_f32(xc_[D]), xc = to_f32(xc_[2 * D]);
+        const int r0 = 32 * (tid >> 8);
+        const TIN* xc_ = qkc < D ? xq + qkc : xk + qkc - D;
+        float xa = to_f32(xc_[r0 * D]), xb = to_f32(xc_[(r0 + 1) * D]), xc = to_f32(xc_[(r0 + 2) * D]);
 #pragma unroll 1
-        for (int tb = 0; tb < C; tb += 16) {
+        for (int tb = r0; tb < r0 + 32; tb += 16) {
           float xr[16], yv[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) xr[u] = to_f32(xc_[(tb + u + 3) * D]);
@@ -409,24 +400,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             xa = xb; xb = xc; xc = xr[u];
           }
 #pragma unroll
-          for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + tid] = yv[u];
+          for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + qkc] = yv[u];
         }
       }
-      // v channel `row` for rows [32 half, +32) -> tensor memory (lane = channel)
+      // v channel `row` for rows [16 quarter, +16) -> tensor memory (lane = channel)
       {
-        const int tb = 32 * half;
-        float xr[35], vr[32];
+        const int tb = 16 * quarter;
+        float xr[19], vr[16];
 #pragma unroll
-        for (int u = 0; u < 35; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
+        for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           float z = wv.x * xr[i];
           z = fmaf(wv.y, xr[i + 1], z);
           z = fmaf(wv.z, xr[i + 2], z);
           z = fmaf(wv.w, xr[i + 3], z);
           vr[i] = silu_fast(z);
         }
-        tc::tmem_st32(tbase + tlane + kColV + 32 * half, vr);
+        tc::tmem_st16(tbase + tlane + kColV + 16 * quarter, vr);
       }
       // cumulative log decay, decay factors and b (rows past the end have g = b = 0)
       if (warp == 0) {
@@ -451,13 +442,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         stage(c + 1);
         x_issued = c + 1;
       }
-      // L2 norm factors: warp w reduces (row, q | k) pairs w, w+8, ... in a
+      // L2 norm factors: warp w reduces (row, q | k) pairs w, w+16, ... in a
       // fixed order; rows past the end get factor 0
       {
-        float ss[16];
+        constexpr int NP = 128 / (kPfWorkers / 32);
+        float ss[NP];
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const int k = warp + 8 * it, t = k >> 1, isk = k & 1;
+        for (int it = 0; it < NP; ++it) {
+          const int k = warp + (kPfWorkers / 32) * it, t = k >> 1, isk = k & 1;
           const float* yr = yf + t * 256 + isk * D;
           float a = 0.f;
 #pragma unroll
@@ -468,12 +460,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ss[it] = a;
         }
 #pragma unroll
-        for (int it = 0; it < 16; ++it) ss[it] = warp_sum(ss[it]);
-        if (lane < 16) {
+        for (int it = 0; it < NP; ++it) ss[it] = warp_sum(ss[it]);
+        if (lane < NP) {
           float a = ss[0];
 #pragma unroll
-          for (int it = 1; it < 16; ++it) a = lane == it ? ss[it] : a;
-          const int k = warp + 8 * lane, t = k >> 1, isk = k & 1;
+          for (int it = 1; it < NP; ++it) a = lane == it ? ss[it] : a;
+          const int k = warp + (kPfWorkers / 32) * lane, t = k >> 1, isk = k & 1;
           (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
         }
       }
@@ -484,10 +476,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // has finished first.
       if (s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok);
       {
-        float4 ya[8], yb[8];
-        float fv[8];
+        constexpr int NKQ = 2048 / kPfWorkers, NKT = 1024 / kPfWorkers;
+        float4 ya[NKQ], yb[NKQ];
+        float fv[NKQ];
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
+        for (int it = 0; it < NKQ; ++it) {
           const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
           const int t = r & (C - 1);
           const bool isq = r >= C;
@@ -496,9 +489,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ya[it] = src[0];
           yb[it] = src[1];
         }
-        float kt[4][8];
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < NKQ; ++it) {
+          const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
+          const float f = fv[it];
+          const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
+                              yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
+          const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
+          store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
+        }
+        float kt[NKT][8];
+#pragma unroll
+        for (int it = 0; it < NKT; ++it) {
           const int i = tid + kPfWorkers * it, k = i & 127, j8 = i >> 7;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -507,16 +509,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
-          const float f = fv[it];
-          const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
-                              yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
-          const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
-          store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
-        }
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < NKT; ++it) {
           const int i = tid + kPfWorkers * it, k = i & 127, j8 = i >> 7;
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
           store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
@@ -538,28 +531,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---- (B) S0 -> bf16 operand; checkpoint due at this boundary; gam_C S0 back
     if (worker) {
       const float gC = gam[C - 1];
-      float v0[32], v1[32];
-      tc::tmem_ld32x2(tS, tS + 32, v0, v1);
-      if (pend >= 0) {
-        float* ck = page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half;
+      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          reinterpret_cast<float4*>(ck)[c4] = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
-          reinterpret_cast<float4*>(ck + 32)[c4] =
-              make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float v0[16];
+        tc::tmem_ld16(tS + 16 * hh, v0);
+        if (ck) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            reinterpret_cast<float4*>(ck + 16 * hh)[c4] =
+                make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
         }
-      }
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint32_t off = tc::sw128_offset(row, 64 * half + 8 * c8, 128);
-        store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
-        off = tc::sw128_offset(row, 64 * half + 32 + 8 * c8, 128);
-        store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v1 + 8 * c8);
-      }
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const uint32_t off = tc::sw128_offset(row, 32 * quarter + 16 * hh + 8 * c8, 128);
+          store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
+        }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) { v0[e] *= gC; v1[e] *= gC; }
-      tc::tmem_st32(tS, v0);
-      tc::tmem_st32(tS + 32, v1);
+        for (int e = 0; e < 16; ++e) v0[e] *= gC;
+        tc::tmem_st16(tS + 16 * hh, v0);
+      }
       tc::tmem_st_wait();
       pend = -1;
       tc::fence_async_smem();
@@ -575,22 +566,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     issued |= 2u;
 
     // ---- (C) A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j) for
-    // columns j in [32 half, +32), computed while S0 [K^; Q^]^T runs
+    // columns j in [16 quarter, +16), computed while S0 [K^; Q^]^T runs
     if (worker) {
       mma_wait(mbar + 0, par, ok);
       const int q4 = warp & 3;
       const int ir = (q4 & 1) * 32 + lane;   // chunk row i of this thread's lane
-      float ap[32];
+      float ap[16];
       {
-        tc::tmem_ld32(tbase + tlane + kColKK + 32 * half, ap);
+        tc::tmem_ld16(tbase + tlane + kColKK + 16 * quarter, ap);
         const float Gi = Gs[ir];
         const float bi = q4 < 2 ? bv[ir] : 1.0f;
         const int lim = q4 < 2 ? ir : ir + 1;        // A: j < i; P: j <= i
         // exp(G_i - G_j) <= 1 where it is kept; the clamp keeps the masked
         // entries finite, the 0/1 mask avoids a branch around the exponential
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = 32 * half + e;
+        for (int e = 0; e < 16; ++e) {
+          const int j = 16 * quarter + e;
           const float m = j < lim ? bi : 0.f;
           ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
         }
@@ -599,19 +590,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       workers_sync();   // every worker is past the S0 [K^; Q^]^T wait: [K^; Q^] is free
       if (q4 < 2) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) at[(32 * half + e) * C + ir] = ap[e];
+        for (int e = 0; e < 16; ++e) at[(16 * quarter + e) * C + ir] = ap[e];
       } else {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const uint32_t off = tc::sw128_offset(ir, 32 * half + 8 * c8, 64);
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const uint32_t off = tc::sw128_offset(ir, 16 * quarter + 8 * c8, 64);
           store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
         }
       }
       workers_sync();
-      if (half == 1) {
+      if (tid >= 256) {
         // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
-        tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 128);
-        for (int e = tid - 128; e < 512; e += 128) {
+        tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 256);
+        for (int e = tid - 256; e < 512; e += 256) {
           const int i = e >> 3, c8 = e & 7;
           const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
           const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
@@ -623,19 +614,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
         }
       } else {
-        // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` -> the A operand of U^T = R T^T
-        float a[32], b[32];
+        // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` for rows i in
+        // [32 qh, +32) -> the A operand of U^T = R T^T
+        const int qh = tid >> 7;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          tc::tmem_ld32x2(tbase + tlane + kColSK + 32 * q, tbase + tlane + kColV + 32 * q, a, b);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i0 = 32 * qh + 16 * hh;
+          float a[16], b[16];
+          tc::tmem_ld16x2(tbase + tlane + kColSK + i0, tbase + tlane + kColV + i0, a, b);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = 32 * q + e;
-            a[e] = bv[i] * fmaf(-gam[i], a[e], b[e]);
-          }
+          for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], b[e]);
 #pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            const uint32_t off = tc::sw128_offset(row, 32 * q + 8 * c8, 128);
+          for (int c8 = 0; c8 < 2; ++c8) {
+            const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
             store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
           }
         }
@@ -654,11 +645,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // U^T (rows r, K = i) as the A operand of the state update and the outputs
     if (worker) {
       mma_wait(mbar + 2, par, ok);
-      float u[32];
-      tc::tmem_ld32(tbase + tlane + kColU + 32 * half, u);
+      float u[16];
+      tc::tmem_ld16(tbase + tlane + kColU + 16 * quarter, u);
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const uint32_t off = tc::sw128_offset(row, 32 * half + 8 * c8, 128);
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, 16 * quarter + 8 * c8, 128);
         store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, u + 8 * c8);
       }
       tc::fence_async_smem();
@@ -681,18 +672,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     s_pending = true;
     if (worker) {
       mma_wait(mbar + 3, par, ok);
-      // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [32 half, +32):
+      // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [16 quarter, +16):
       // a full chunk goes out as one TMA tile through shared memory, a
       // partial one (the sequence's last) by plain stores
-      float sq[32], up[32];
-      tc::tmem_ld32x2(tbase + tlane + kColSQ + 32 * half, tbase + tlane + kColU + 32 * half, sq, up);
+      float sq[16], up[16];
+      tc::tmem_ld16x2(tbase + tlane + kColSQ + 16 * quarter, tbase + tlane + kColU + 16 * quarter, sq, up);
       if (p.norm_w) {
         // packed core: a token's 128 outputs are normalised together, so they
-        // meet in shared memory; warp w then takes tokens w, w+8, ...: RMS
+        // meet in shared memory; warp w then takes tokens w, w+16, ...: RMS
         // over dv, the norm scale, the silu(z) gate from the packed row
         float* of = reinterpret_cast<float*>(sm + PfSmem::OF);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) of[(32 * half + e) * D + row] = fmaf(gam[32 * half + e], sq[e], up[e]);
+        for (int e = 0; e < 16; ++e) of[(16 * quarter + e) * D + row] = fmaf(gam[16 * quarter + e], sq[e], up[e]);
         workers_sync();
         const TIN* zrow = reinterpret_cast<const TIN*>(p.x) + (row0 + t0) * p.x_ld + p.conv_dim + h * D;
         TOUT* orow = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D;
@@ -714,7 +705,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       } else if (tma_out && cnt == C) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ot[(32 * half + e) * D + row] = from_f32<TOUT>(fmaf(gam[32 * half + e], sq[e], up[e]));
+        for (int e = 0; e < 16; ++e)
+          ot[(16 * quarter + e) * D + row] = from_f32<TOUT>(fmaf(gam[16 * quarter + e], sq[e], up[e]));
         tc::fence_async_smem();
         workers_sync();
         if (tid == 0) {
@@ -725,8 +717,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
         const int64_t tstride = (int64_t)p.Hv * D;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = 32 * half + e;
+        for (int e = 0; e < 16; ++e) {
+          const int i = 16 * quarter + e;
           if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
         }
       }
@@ -751,20 +743,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (ok) {
     if (worker) {
       // final state (and a checkpoint due at the last chunk's end)
-      float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 64 * half;
-      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 64 * half : nullptr;
-      float v0[32], v1[32];
-      tc::tmem_ld32x2(tS, tS + 32, v0, v1);
+      float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 32 * quarter;
+      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+      float v0[32];
+      tc::tmem_ld32(tS, v0);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
-        const float4 f1 = make_float4(v1[4 * c4], v1[4 * c4 + 1], v1[4 * c4 + 2], v1[4 * c4 + 3]);
         reinterpret_cast<float4*>(dst)[c4] = f0;
-        reinterpret_cast<float4*>(dst + 32)[c4] = f1;
-        if (ck) {
-          reinterpret_cast<float4*>(ck)[c4] = f0;
-          reinterpret_cast<float4*>(ck + 32)[c4] = f1;
-        }
+        if (ck) reinterpret_cast<float4*>(ck)[c4] = f0;
       }
     }
   } else {
