@@ -44,9 +44,9 @@ PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
 # DRAM bytes (read + write) of one tensor-core prefill launch, from an ncu
-# capture of the current kernel at 4 x 2,048 tokens (profiles/
-# tc_prefill_kernel_27b_4x2048.md: 173.2 + 94.7 MB), scaled by 4 to the
-# 4 x 8,192 launch (the traffic is per token).  None once the kernel changes.
+# capture of the current kernel at 4 x 2,048 tokens (173.2 MB read + 94.7 MB
+# written), scaled by 4 to the 4 x 8,192 launch (the traffic is per token).
+# None once the kernel changes.
 PREFILL_TRAFFIC_PER_LAUNCH = (173.188864e6 + 94.731776e6) * 4
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
