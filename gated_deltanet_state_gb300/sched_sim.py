@@ -15,7 +15,18 @@ every step, that a request's slot holds exactly the state of the tokens it
 has computed.  It drives the library's own cache arithmetic (``gdn_chunk_end``,
 ``gdn_resume_block``), so a wrong block boundary or resume rule shows up as a
 failed check.  ``Mutation`` switches off one mechanism at a time (saves,
-restores, slot hand-back, zeroing): each must make the checks fail.
+restores, slot hand-back, zeroing, boundary checkpoints of replay flushes):
+each must make the checks fail.
+
+Replay mode ("Caching less to serve more requests", "What we changed" and
+"Other models": speculative decoding on one checkpoint plus an input log,
+served with prefix caching): a decoding request keeps its checkpoint in the
+slot and the kept rows in a log of REPLAY_LOG_SLOTS; each cycle appends a
+draft, keeps an accepted prefix (at least the row the previous cycle's
+verification produced), and flushes when the log would overflow or its rows
+would cross a second block boundary.  A flush whose kept rows cross a block
+boundary writes that block's checkpoint (``gdn_replay_boundary_rows``), so a
+later prefix hit can resume inside the decoded tokens.
 """
 from __future__ import annotations
 
@@ -25,7 +36,7 @@ import hashlib
 import random
 from collections import OrderedDict
 
-from . import gdn_chunk_end, gdn_resume_block
+from . import REPLAY_LOG_SLOTS, gdn_chunk_end, gdn_replay_boundary_rows, gdn_resume_block
 
 ZERO = b"zero"                  # a zeroed block or a fresh slot
 POISON = b"stale-checkpoint"    # what a reused block holds if it is not zeroed
@@ -52,6 +63,7 @@ class Mutation(enum.Enum):
     NO_RESTORE = "no_restore"      # a hit or a resume keeps the slot's previous contents
     NO_HANDBACK = "no_handback"    # preemption keeps the slot
     NO_ZEROING = "no_zeroing"      # blocks are handed out with their old contents
+    NO_BOUNDARY = "no_boundary"    # replay flushes skip the block-boundary checkpoint
 
 
 class SimFailure(AssertionError):
@@ -67,6 +79,7 @@ class Request:
     slot: int | None = None
     blocks: list = dataclasses.field(default_factory=list)
     started: bool = False
+    log_len: int = 0               # replay mode: kept rows past the slot's checkpoint
 
 
 class Engine:
@@ -74,8 +87,12 @@ class Engine:
     compact state slots, a token budget per step."""
 
     def __init__(self, block: int, num_blocks: int, num_slots: int, budget: int,
-                 mutation: Mutation = Mutation.NONE):
+                 mutation: Mutation = Mutation.NONE, replay: bool = False, seed: int = 0):
         self.block, self.budget, self.mutation = block, budget, mutation
+        self.replay = replay
+        self.rng = random.Random(seed)
+        self.flushes = 0
+        self.boundary_saves = 0
         self.block_ckpt = [ZERO] * num_blocks        # checkpoint content of each block
         self.block_key = [None] * num_blocks         # prefix-cache key of a sealed block
         self.free_blocks = OrderedDict((b, None) for b in range(num_blocks))   # LRU of free blocks
@@ -135,15 +152,17 @@ class Engine:
         # the tokens it generated join the prompt it re-prefills on resume
         req.prompt_len = max(req.prompt_len, req.computed)
         req.computed = 0
+        req.log_len = 0
         req.started = False
         self.waiting.insert(0, req)
 
     # ---- state checks and copies
     def _check(self, req: Request):
         self.checks += 1
-        want = fingerprint(req.tokens[:req.computed])
+        absorbed = req.computed - req.log_len
+        want = fingerprint(req.tokens[:absorbed])
         if self.slot_state[req.slot] != want:
-            raise SimFailure(f"request {req.rid}: slot state is not the state after {req.computed} tokens")
+            raise SimFailure(f"request {req.rid}: slot state is not the state after {absorbed} tokens")
 
     def _save(self, req: Request, pos: int):
         """slot -> block at a boundary (every crossed one, in-kernel)."""
@@ -189,6 +208,40 @@ class Engine:
                 self.slot_state[req.slot] = ZERO   # a cold start never reads the pool
         req.started = True
 
+    # ---- replay (speculative) decoding
+    def _replay_flush(self, req: Request):
+        """Fold the kept rows into the slot; a block boundary inside them gets
+        its checkpoint (the state after the rows up to it)."""
+        absorbed = req.computed - req.log_len
+        j = gdn_replay_boundary_rows(absorbed, req.log_len, self.block)
+        if j < 0:
+            raise SimFailure("a flush crossing two block boundaries")
+        if j > 0:
+            pos = absorbed + j
+            blk = pos // self.block - 1
+            if self.mutation != Mutation.NO_BOUNDARY:
+                self.block_ckpt[req.blocks[blk]] = fingerprint(req.tokens[:pos])
+                self.boundary_saves += 1
+            key = self._key(req, blk)
+            if key not in self.cache:
+                self.cache[key] = req.blocks[blk]
+                self.block_key[req.blocks[blk]] = key
+        self.slot_state[req.slot] = _chain(self.slot_state[req.slot], req.tokens[absorbed:req.computed])
+        req.log_len = 0
+        self.flushes += 1
+
+    def _replay_cycle(self, req: Request) -> int:
+        """One draft / verify cycle; returns the rows it keeps."""
+        m = min(self.rng.randint(1, 8), len(req.tokens) - req.computed)
+        absorbed = req.computed - req.log_len
+        if req.log_len + m > REPLAY_LOG_SLOTS or gdn_replay_boundary_rows(absorbed, req.log_len + m,
+                                                                          self.block) < 0:
+            self._replay_flush(req)
+        keep = self.rng.randint(1, m)      # the first row is the previous verification's token
+        req.computed += keep
+        req.log_len += keep
+        return keep
+
     # ---- one scheduler step
     def step(self):
         budget = self.budget
@@ -210,6 +263,8 @@ class Engine:
                 end = gdn_chunk_end(req.computed, req.prompt_len, budget, self.block)
                 if end <= req.computed:
                     continue
+            elif self.replay:                                 # replay: a draft of up to 8 rows
+                end = min(req.computed + 8, len(req.tokens))
             else:                                             # decode: one token
                 end = req.computed + 1
             try:
@@ -230,11 +285,16 @@ class Engine:
                 raise SimFailure(f"request {req.rid}: reads a block that was handed out unzeroed")
             self._check(req)
             start = req.computed
-            self.slot_state[req.slot] = _chain(self.slot_state[req.slot], req.tokens[start:end])
-            req.computed = end
-            for pos in range((start // self.block + 1) * self.block, end + 1, self.block):
-                self._save(req, pos)
-            budget -= end - start
+            if self.replay and start >= req.prompt_len:
+                budget -= self._replay_cycle(req)
+            else:
+                if req.log_len:
+                    self._replay_flush(req)        # a prefill chunk continues from a folded log
+                self.slot_state[req.slot] = _chain(self.slot_state[req.slot], req.tokens[start:end])
+                req.computed = end
+                for pos in range((start // self.block + 1) * self.block, end + 1, self.block):
+                    self._save(req, pos)
+                budget -= end - start
             if req.computed >= total:
                 self.running.remove(req)
                 self._release(req)
@@ -271,11 +331,12 @@ def agent_workload(seed: int, sessions: int = 4, turns: int = 6, sys_len: int = 
 
 
 def simulate(seed: int, mutation: Mutation = Mutation.NONE, block: int = 8, num_blocks: int = 32,
-             num_slots: int = 3, budget: int = 32, max_steps: int = 100000) -> Engine:
+             num_slots: int = 3, budget: int = 32, max_steps: int = 100000, replay: bool = False,
+             gen_len: int = 6) -> Engine:
     """Run one seeded workload to completion; raises SimFailure on the first
     broken check.  Turns of a session arrive after the previous turn ends."""
-    eng = Engine(block, num_blocks, num_slots, budget, mutation)
-    reqs = agent_workload(seed)
+    eng = Engine(block, num_blocks, num_slots, budget, mutation, replay=replay, seed=seed + 7)
+    reqs = agent_workload(seed, gen_len=gen_len)
     rng = random.Random(seed + 1)
     pending = {}
     for s, r in reqs:

@@ -66,3 +66,37 @@ def test_save_off_a_block_boundary_fails_closed():
     eng._ensure_blocks(req, 12)
     with pytest.raises(ss.SimFailure, match="off a block boundary"):
         eng._save(req, 12)
+
+
+REPLAY = dict(replay=True, gen_len=40, num_blocks=48)
+
+
+def test_replay_mode_passes_every_check():
+    """Speculative decoding on checkpoint + log with prefix caching: flushes
+    write the block-boundary checkpoints that later hits resume from."""
+    checks = hits = flushes = saves = preemptions = 0
+    for seed in SEEDS:
+        eng = ss.simulate(seed, **REPLAY)
+        assert eng.idle()
+        assert sorted(eng.free_slots) == list(range(len(eng.slot_state)))
+        checks += eng.checks
+        hits += eng.hits
+        flushes += eng.flushes
+        saves += eng.boundary_saves
+        preemptions += eng.preemptions
+    assert checks > 2000 and hits > 300 and flushes > 200 and saves > 200 and preemptions > 50
+
+
+@pytest.mark.parametrize("mutation", [ss.Mutation.NO_BOUNDARY, ss.Mutation.NO_SAVE, ss.Mutation.NO_RESTORE,
+                                      ss.Mutation.NO_HANDBACK, ss.Mutation.NO_ZEROING])
+def test_replay_mutant_fails_on_every_seed(mutation):
+    for seed in SEEDS:
+        with pytest.raises(ss.SimFailure):
+            ss.simulate(seed, mutation, **REPLAY)
+
+
+def test_boundary_mutant_is_harmless_without_replay():
+    # plain decoding writes its checkpoints step by step; the replay-only
+    # mechanism switched off changes nothing there
+    for seed in range(4):
+        ss.simulate(seed, ss.Mutation.NO_BOUNDARY)
