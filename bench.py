@@ -375,7 +375,7 @@ class FlushSweep:
         self.layers = []
         for layer in range(layers):
             pool = gdn.StatePool(sh, 2 * n_req if boundary else n_req, fill=0)
-            st = pool.buf.view(n_req, sh.page)[:, :sh.state_bytes].view(torch.float32)
+            st = pool.buf.view(-1, sh.page)[:, :sh.state_bytes].view(torch.float32)
             st.copy_(0.3 * torch.randn(st.shape, generator=gen, device="cuda"))
             self.layers.append(dict(
                 pool=pool, ckpt=inputs.permutation(n_req, seed + layer).cuda(),
