@@ -28,7 +28,9 @@
 //       tensor cores: [K^K^T; Q^K^T] and S0 [K^; Q^]^T.
 //   (C) A and P = exp(G_i - G_j) q^_i.k^_j (j <= i) (computed while the
 //       tensor core forms S0 [K^; Q^]^T); T = (I + A)^{-1} by two warpgroups
-//       (16 x 16 blocks) while the others form R_i = b_i (v_i - gam_i S0 k^_i);
+//       (16 x 16 blocks: diagonal inverses, the blocks N = -D A below them,
+//       then one product per distance from the diagonal) while the others form
+//       R_i = b_i (v_i - gam_i S0 k^_i);
 //       tensor cores: U^T = R T^T.
 //   (D) tensor cores: S += U^T (K^T diag(exp(G_C - G)))^T in tensor memory and
 //       U^T P^T; outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i.
@@ -63,7 +65,7 @@ constexpr long long kPfWait = 4000000000LL;
 // Shared-memory plan (byte offsets from a 1024-byte aligned base).  The
 // 128-byte swizzled operands are K-major bf16 tiles (sw128_offset), hi part
 // then lo part.  Regions are reused phase by phase:
-//   R1: (A) y | (B) S0 operand | (C) T fp32, block scratch, T operand
+//   R1: (A) y | (B) S0 operand | (C) T fp32, its blocks, T operand, A row-major
 //   R2: (A-B) [K^; Q^] operand | (C-D) R^T then U^T operand, P operand, A^T fp32
 struct PfSmem {
   static constexpr uint32_t R1 = 0;
@@ -71,9 +73,11 @@ struct PfSmem {
   static constexpr uint32_t S0 = R1;                  // S0 hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t S0_LO = R1 + 32768;
   static constexpr uint32_t TF = R1;                  // T fp32 [64 i][64 j]
-  static constexpr uint32_t XSCR = R1 + 16384;        // fp32 [3][16][16] block products
+  static constexpr uint32_t DT = R1 + 16384;          // fp32 [4][16][20]: diagonal inverses, transposed
+  static constexpr uint32_t NT = R1 + 21504;          // fp32 [6][16][16]: N_pk^T
   static constexpr uint32_t TB = R1 + 32768;          // T hi [64][64], lo at +8 KB
   static constexpr uint32_t TB_LO = R1 + 40960;
+  static constexpr uint32_t AM = R1 + 49152;          // A fp32 [64][64] row-major, slots swizzled
   static constexpr uint32_t R2 = 65536;
   static constexpr uint32_t KQ = R2;                  // [K^; Q^] hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t KQ_LO = R2 + 32768;
@@ -138,18 +142,28 @@ __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 512;\
 // Barrier of the threads that build T (256..511).
 __device__ __forceinline__ void tgrp_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
-// T = (I + A)^{-1} for the 64 x 64 strictly lower triangular A given as A^T
-// (at[j * 64 + i] = A_ij, zero for i <= j), by 256 threads t.  The 16 x 16
-// diagonal blocks D_b = (I + A_bb)^{-1} by forward substitution (a column per
-// thread), then the blocks below them in order of distance from the
-// diagonal: T_pq = -D_p X, X = sum_{k=q}^{p-1} A_pk T_kq (a 1 x 4 tile per
-// thread).  tf[i * 64 + j] receives T on and below the diagonal (the blocks
-// above it are left unwritten).
-__device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
+// Row-major A with 16-byte slots XOR-swizzled by row (conflict-free stores
+// of a row per lane, loads of a row segment per warp).
+__device__ __forceinline__ int am_index(int i, int j) { return i * 64 + (j ^ ((i & 7) << 2)); }
+
+// Block pair (p, k), p > k, of the 4 x 4 grid of 16 x 16 blocks:
+// (1,0) (2,0) (2,1) (3,0) (3,1) (3,2) -> 0..5.
+__device__ __forceinline__ int pair_index(int p, int k) { return p * (p - 1) / 2 + k; }
+
+// T = (I + A)^{-1} for the 64 x 64 strictly lower triangular A (at: A^T,
+// at[j * 64 + i] = A_ij; am: A row-major, am_index), by 256 threads t, in
+// 16 x 16 blocks.  With D_b = (I + A_bb)^{-1} and N_pk = -D_p A_pk (p > k),
+// T_bb = D_b and T_pq = sum_{k=q}^{p-1} N_pk T_kq, so after the diagonal
+// blocks (forward substitution, a column per thread) and all six N blocks (one
+// phase), each distance from the diagonal takes one product.  Register tiles
+// keep the shared-memory loads at one 16-byte vector per four to eight FMAs.
+// tf[i * 64 + j] receives T on and below the diagonal (the blocks above it
+// are left unwritten); dt holds D_b^T ([4][16][20]), nt the N_pk^T ([6][16][16]).
+__device__ void tri_inverse64(const float* at, const float* am, float* tf, float* dt, float* nt, int t) {
   if (t < 64) {
     // column sweep: once x_k is final, x_i -= A_ik x_k for every i > k (A^T
     // row o+k holds A_{o+i, o+k} contiguously in i; zero for i <= k)
-    const int o = 16 * (t >> 4), l = t & 15;
+    const int b = t >> 4, o = 16 * b, l = t & 15;
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = i == l ? 1.f : 0.f;
@@ -167,47 +181,91 @@ __device__ void tri_inverse64(const float* at, float* tf, float* xscr, int t) {
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) tf[(o + i) * 64 + o + l] = x[i];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4)
+      *reinterpret_cast<float4*>(dt + (o + l) * 20 + 4 * i4) =
+          make_float4(x[4 * i4], x[4 * i4 + 1], x[4 * i4 + 2], x[4 * i4 + 3]);
   }
   tgrp_sync();
-  // every block of a distance level in one round: 64 tiles of 1 row x 4
-  // columns per 16 x 16 block, one tile per thread
+  // N_pk^T[j][i] = -sum_m A_{16p+m, 16k+j} D_p[i][m]: 6 pairs x 16 tiles of 4 j x 4 i
+  if (t < 96) {
+    const int pr = t >> 4, tile = t & 15;
+    const int p = pr == 0 ? 1 : pr < 3 ? 2 : 3;
+    const int k = pr - pair_index(p, 0);
+    const int j0 = 4 * (tile >> 2), i0 = 4 * (tile & 3);
+    float acc[4][4];
 #pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int tasks = (4 - d) * 64;
-    const int q = t >> 6, p = q + d, i = (t >> 2) & 15, j4 = 4 * (t & 3);
-    if (t < tasks) {
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int kk = 0; kk < 16 * d; ++kk) {
-        const int k = 16 * q + kk;
-        const float a = at[k * 64 + 16 * p + i];
-        const float4 b = *reinterpret_cast<const float4*>(tf + k * 64 + 16 * q + j4);
-        a0.x = fmaf(a, b.x, a0.x); a0.y = fmaf(a, b.y, a0.y);
-        a0.z = fmaf(a, b.z, a0.z); a0.w = fmaf(a, b.w, a0.w);
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float4 a4 = *reinterpret_cast<const float4*>(am + am_index(16 * p + m, 16 * k + j0));
+      const float4 d4 = *reinterpret_cast<const float4*>(dt + (16 * p + m) * 20 + i0);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        acc[r][0] = fmaf(a[r], d4.x, acc[r][0]); acc[r][1] = fmaf(a[r], d4.y, acc[r][1]);
+        acc[r][2] = fmaf(a[r], d4.z, acc[r][2]); acc[r][3] = fmaf(a[r], d4.w, acc[r][3]);
       }
-      *reinterpret_cast<float4*>(xscr + q * 256 + i * 16 + j4) = a0;
     }
-    tgrp_sync();
-    if (t < tasks) {
-      // row i of D_p, read once (zero above its diagonal, so all 16 terms
-      // can be taken)
-      float d0[16];
 #pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 f0 = *reinterpret_cast<const float4*>(tf + (16 * p + i) * 64 + 16 * p + 4 * m4);
-        d0[4 * m4] = f0.x; d0[4 * m4 + 1] = f0.y; d0[4 * m4 + 2] = f0.z; d0[4 * m4 + 3] = f0.w;
-      }
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 4; ++r)
+      *reinterpret_cast<float4*>(nt + (pr * 16 + j0 + r) * 16 + i0) =
+          make_float4(-acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+  }
+  tgrp_sync();
+  // distances 1 and 2: blocks (p, q = p - d) in tiles of 2 rows x 4 columns
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float4 b = *reinterpret_cast<const float4*>(xscr + q * 256 + m * 16 + j4);
-        a0.x = fmaf(-d0[m], b.x, a0.x); a0.y = fmaf(-d0[m], b.y, a0.y);
-        a0.z = fmaf(-d0[m], b.z, a0.z); a0.w = fmaf(-d0[m], b.w, a0.w);
+  for (int d = 1; d < 3; ++d) {
+    if (t < (4 - d) * 32) {
+      const int q = t >> 5, p = q + d, tile = t & 31;
+      const int i0 = 2 * (tile >> 2), j0 = 4 * (tile & 3);
+      float acc[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < d; ++kk) {
+        const int k = q + kk;
+        const float* n = nt + pair_index(p, k) * 256;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 n2 = *reinterpret_cast<const float2*>(n + m * 16 + i0);
+          const float4 b4 = *reinterpret_cast<const float4*>(tf + (16 * k + m) * 64 + 16 * q + j0);
+          acc[0][0] = fmaf(n2.x, b4.x, acc[0][0]); acc[0][1] = fmaf(n2.x, b4.y, acc[0][1]);
+          acc[0][2] = fmaf(n2.x, b4.z, acc[0][2]); acc[0][3] = fmaf(n2.x, b4.w, acc[0][3]);
+          acc[1][0] = fmaf(n2.y, b4.x, acc[1][0]); acc[1][1] = fmaf(n2.y, b4.y, acc[1][1]);
+          acc[1][2] = fmaf(n2.y, b4.z, acc[1][2]); acc[1][3] = fmaf(n2.y, b4.w, acc[1][3]);
+        }
       }
-      *reinterpret_cast<float4*>(tf + (16 * p + i) * 64 + 16 * q + j4) = a0;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        *reinterpret_cast<float4*>(tf + (16 * p + i0 + r) * 64 + 16 * q + j0) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
     }
     tgrp_sync();
   }
+  // distance 3: block (3, 0) in tiles of 2 x 2 (64 threads)
+  if (t < 64) {
+    const int i0 = 2 * (t >> 3), j0 = 2 * (t & 7);
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const float* n = nt + pair_index(3, k) * 256;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float2 n2 = *reinterpret_cast<const float2*>(n + m * 16 + i0);
+        const float2 b2 = *reinterpret_cast<const float2*>(tf + (16 * k + m) * 64 + j0);
+        s0.x = fmaf(n2.x, b2.x, s0.x); s0.y = fmaf(n2.x, b2.y, s0.y);
+        s1.x = fmaf(n2.y, b2.x, s1.x); s1.y = fmaf(n2.y, b2.y, s1.y);
+      }
+    }
+    *reinterpret_cast<float2*>(tf + (48 + i0) * 64 + j0) = s0;
+    *reinterpret_cast<float2*>(tf + (48 + i0 + 1) * 64 + j0) = s1;
+  }
+  tgrp_sync();
 }
 
 // A worker's bounded wait for a tensor-core product; a wait that runs out
@@ -589,8 +647,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mma_wait(mbar + 1, par, ok);
       workers_sync();   // every worker is past the S0 [K^; Q^]^T wait: [K^; Q^] is free
       if (q4 < 2) {
+        float* am = reinterpret_cast<float*>(sm + PfSmem::AM);
 #pragma unroll
         for (int e = 0; e < 16; ++e) at[(16 * quarter + e) * C + ir] = ap[e];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<float4*>(am + am_index(ir, 16 * quarter + 4 * c4)) =
+              make_float4(ap[4 * c4], ap[4 * c4 + 1], ap[4 * c4 + 2], ap[4 * c4 + 3]);
       } else {
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
@@ -601,7 +664,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       workers_sync();
       if (tid >= 256) {
         // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
-        tri_inverse64(at, tf, reinterpret_cast<float*>(sm + PfSmem::XSCR), tid - 256);
+        tri_inverse64(at, reinterpret_cast<const float*>(sm + PfSmem::AM), tf, reinterpret_cast<float*>(sm + PfSmem::DT),
+                      reinterpret_cast<float*>(sm + PfSmem::NT), tid - 256);
         for (int e = tid - 256; e < 512; e += 256) {
           const int i = e >> 3, c8 = e & 7;
           const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
