@@ -169,6 +169,30 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// Three-pass product D (+)= A B^T (hi*hi + hi*lo + lo*hi) over KSTEPS
+// K-steps of 16: A (M rows) and B (N rows) are K-major 128-byte swizzled bf16
+// tiles, hi and lo parts apart, whose 64-wide K-blocks lie AKB / BKB bytes
+// apart.  The four descriptors are built once; each K-step adds a compile-time
+// offset to the start-address field (shared-memory addresses stay below
+// 256 KB, so the field does not carry), which keeps the issuing thread to a
+// few instructions per product.
+template <int KSTEPS, uint32_t AKB, uint32_t BKB>
+__device__ __forceinline__ void mma3_sw128(uint32_t d, uint32_t a, uint32_t a_lo, uint32_t b, uint32_t b_lo,
+                                           uint32_t idesc, bool accumulate) {
+  const uint64_t dA[2] = {desc_sw128(a), desc_sw128(a_lo)};
+  const uint64_t dB[2] = {desc_sw128(b), desc_sw128(b_lo)};
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass) {
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      const uint64_t oA = ((uint32_t)(ks >> 2) * AKB + (uint32_t)(ks & 3) * 32u) >> 4;
+      const uint64_t oB = ((uint32_t)(ks >> 2) * BKB + (uint32_t)(ks & 3) * 32u) >> 4;
+      mma_bf16(d, dA[pass == 2 ? 1 : 0] + oA, dB[pass == 1 ? 1 : 0] + oB, idesc,
+               (accumulate || pass != 0 || ks != 0) ? 1u : 0u);
+    }
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn
 

@@ -119,29 +119,6 @@ __device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, const flo
   *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Three-pass product D (+)= A B^T over KSTEPS K-steps of 16: A (M = 128
-// rows) and B (N rows) are K-major 128-byte swizzled tiles whose 64-wide
-// K-blocks lie AKB / BKB bytes apart.  The four descriptors are built once and
-// every K-step adds a compile-time offset to the start-address field, so the
-// issuing thread spends a few instructions per product (it shares its
-// sub-partition's issue slots with four worker warps).
-template <int KSTEPS, uint32_t AKB, uint32_t BKB>
-__device__ __forceinline__ void mma3(uint32_t d, uint32_t a, uint32_t a_lo, uint32_t b, uint32_t b_lo,
-                                     uint32_t idesc, bool accumulate) {
-  const uint64_t dA[2] = {tc::desc_sw128(a), tc::desc_sw128(a_lo)};
-  const uint64_t dB[2] = {tc::desc_sw128(b), tc::desc_sw128(b_lo)};
-#pragma unroll
-  for (int pass = 0; pass < 3; ++pass) {
-#pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-      const uint64_t oA = ((uint32_t)(ks >> 2) * AKB + (uint32_t)(ks & 3) * 32u) >> 4;
-      const uint64_t oB = ((uint32_t)(ks >> 2) * BKB + (uint32_t)(ks & 3) * 32u) >> 4;
-      tc::mma_bf16(d, dA[pass == 2 ? 1 : 0] + oA, dB[pass == 1 ? 1 : 0] + oB, idesc,
-                   (accumulate || pass != 0 || ks != 0) ? 1u : 0u);
-    }
-  }
-}
-
 // Barrier of the sixteen worker warps alone (threads 0..511).
 __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 512;\n" ::: "memory"); }
 
@@ -586,7 +563,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     s_pending = false;
     // [K^ K^T; Q^ K^T] (M 128, N 64, K 128) needs no state: it runs during the split
     if (tid == kMmaTid) {
-      mma3<D / 16, 16384, 16384>(tbase + kColKK, sbase + PfSmem::KQ, sbase + PfSmem::KQ_LO, sbase + PfSmem::KQ,
+      tc::mma3_sw128<D / 16, 16384, 16384>(tbase + kColKK, sbase + PfSmem::KQ, sbase + PfSmem::KQ_LO, sbase + PfSmem::KQ,
            sbase + PfSmem::KQ_LO, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 0);
     }
@@ -623,7 +600,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (!ok) break;
     if (tid == kMmaTid) {
       // S0 [K^; Q^]^T (M 128, N 128, K 128)
-      mma3<D / 16, 16384, 16384>(tbase + kColSK, sbase + PfSmem::S0, sbase + PfSmem::S0_LO, sbase + PfSmem::KQ,
+      tc::mma3_sw128<D / 16, 16384, 16384>(tbase + kColSK, sbase + PfSmem::S0, sbase + PfSmem::S0_LO, sbase + PfSmem::KQ,
            sbase + PfSmem::KQ_LO, tc::idesc_bf16_f32(128, 128), false);
       tc::mma_commit(mbar + 1);
     }
@@ -707,7 +684,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (!ok) break;
     if (tid == kMmaTid) {
       // U^T = R T^T (M 128, N 64, K 64)
-      mma3<C / 16, 0, 0>(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::TB,
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::TB,
            sbase + PfSmem::TB_LO, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 2);
     }
@@ -731,10 +708,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // (K^T diag(dec))^T onto gam_C S0, which finishes while the next chunk's
     // conv and norms run
     if (tid == kMmaTid) {
-      mma3<C / 16, 0, 0>(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::PB,
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kColU, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::PB,
            sbase + PfSmem::PB_LO, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + 3);
-      mma3<C / 16, 0, 0>(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::KT,
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kColS, sbase + PfSmem::UT, sbase + PfSmem::UT_LO, sbase + PfSmem::KT,
            sbase + PfSmem::KT_LO, tc::idesc_bf16_f32(128, 128), true);
       tc::mma_commit(mbar + 5);
     }
