@@ -119,6 +119,17 @@ __device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, const flo
   *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Four floats through the read-only path by an asm load that the compiler
+// keeps where it stands (a loop-invariant plain load would be hoisted and
+// its registers held through the whole loop).
+__device__ __forceinline__ float4 ldg_f4_fresh(const float* src) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(src));
+  return v;
+}
+
 // Barrier of the sixteen worker warps alone (threads 0..511).
 __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 512;\n" ::: "memory"); }
 
@@ -358,18 +369,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 
   // conv taps of this thread's q | k channel (tid mod 256) and v channel
-  // (row); the packed core's norm scale at the channels this lane normalises
+  // (row), re-read from L1 / L2 at every chunk (an asm load the compiler does
+  // not hoist) rather than held in registers through the chunk's other phases
   const int qkc = tid & 255;
-  float4 wqk = make_float4(0.f, 0.f, 0.f, 0.f), wv = wqk;
-  float nwr[4] = {0.f, 0.f, 0.f, 0.f};
-  if (worker && p.norm_w) {
-#pragma unroll
-    for (int m = 0; m < 4; ++m) nwr[m] = p.norm_w[lane + 32 * m];
-  }
+  const float* wqk_src = p.conv_w + (int64_t)(qkc < D ? cq0 + qkc : ck0 + qkc - D) * kConvK;
+  const float* wv_src = p.conv_w + (int64_t)(cv0 + row) * kConvK;
   if (worker) {
-    const int qkch = qkc < D ? cq0 + qkc : ck0 + qkc - D;
-    wqk = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)qkch * kConvK);
-    wv = *reinterpret_cast<const float4*>(p.conv_w + (int64_t)(cv0 + row) * kConvK);
     // initial state (zeros on a cold start: the pool is not read)
     const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
     float v[32];
@@ -396,6 +401,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ci = c;
 
     if (worker) {
+      const float4 wqk = ldg_f4_fresh(wqk_src), wv = ldg_f4_fresh(wv_src);
       // ---- the chunk's rows and gates have landed; the previous output tile
       // has been read out
       if (tid == 0) tc::bulk_wait_read();
@@ -747,7 +753,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const float z = to_f32(zrow[(int64_t)i * p.x_ld + lane + 32 * m]);
-            orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nwr[m] * silu(z));
+            orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * p.norm_w[lane + 32 * m] * silu(z));
           }
         }
       } else if (tma_out && cnt == C) {
