@@ -440,6 +440,36 @@ def flush_sweep(seed: int, hbm_gbs: float):
     return out
 
 
+def checkpoint_copy(seed: int, hbm_gbs: float, n: int = 256, reps: int = 5):
+    """Checkpoint saves of the 27B-shaped layer (`gdn_checkpoint_save`): n
+    working slots copied to n block pages in a permuted order, state and conv
+    window as 16-byte words, each byte read and written once; the pool (2n
+    pages, 1.9 GB at n = 256) is larger than L2."""
+    sh = PREFILL
+    pool = gdn.StatePool(sh, 2 * n, fill=0)
+    src = torch.arange(n, dtype=torch.int32, device="cuda")
+    dst = (n + inputs.permutation(n, seed)).cuda()
+    nch = torch.full((n,), 4 * sh.block_size, dtype=torch.int64)     # at a block boundary
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        gdn.gdn_checkpoint_save(sh, pool, src, dst, nch, err)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gdn.gdn_checkpoint_save(sh, pool, src, dst, nch, err)
+    e1.record()
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError("device error word set in the checkpoint copies")
+    us = 1000.0 * e0.elapsed_time(e1) / reps
+    gbs = 2 * n * sh.payload_bytes / (us * 1e-6) / 1e9
+    del pool
+    torch.cuda.empty_cache()
+    return {"pages": n, "payload_bytes": sh.payload_bytes, "us": round(us, 1), "hbm_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_gbs, 3)}
+
+
 # ----------------------------------------------------------------------------- cpu baseline
 
 def _oracle_setup(seed: int):
@@ -690,6 +720,7 @@ def main():
     }
     if not args.no_flush_sweep:
         line["flush_sweep"] = flush_sweep(args.seed + 40 + rank, peaks["hbm_gbs"])
+    line["checkpoint_copy"] = checkpoint_copy(args.seed + 50 + rank, peaks["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
