@@ -470,6 +470,67 @@ def checkpoint_copy(seed: int, hbm_gbs: float, n: int = 256, reps: int = 5):
             "hbm_frac": round(gbs / hbm_gbs, 3)}
 
 
+def long_context(seed: int, reps: int = 3):
+    """The long-context prefix hit on one 27B-shaped layer: a cold prefill of
+    a 229,376-token request (256 blocks of 896, a checkpoint at every
+    boundary), then the same request resumed from block 222 (the state after
+    199,808 tokens, the last full block of a 200,000-token shared prefix) over
+    its 29,568-token suffix.  One sequence gives 48 (sequence, v head) chains,
+    so 48 of the SMs work.  Inputs are drawn on the device (timing only)."""
+    sh = PREFILL
+    T, B = 256 * sh.block_size, sh.block_size
+    hit = (200_000 // B) * B
+    resume_block = gdn.gdn_resume_block(hit, B)
+    start = (resume_block + 1) * B
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    x = torch.empty(T, sh.conv_dim, dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, T, 16384):
+        r1 = min(T, r0 + 16384)
+        x[r0:r1] = torch.randn(r1 - r0, sh.conv_dim, generator=gen, device="cuda").to(torch.bfloat16)
+    g = -0.1 * torch.nn.functional.softplus(torch.randn(T, sh.num_v_heads, generator=gen, device="cuda"))
+    beta = torch.sigmoid(torch.randn(T, sh.num_v_heads, generator=gen, device="cuda"))
+    w = inputs.conv_weights(sh, seed).cuda()
+    pool = gdn.StatePool(sh, 258, fill=0)
+    bt = inputs.permutation(258, seed)[:256].view(1, 256).cuda()
+    used = set(bt.flatten().tolist())
+    slot = torch.tensor([next(p for p in range(258) if p not in used)], dtype=torch.int32).cuda()
+    o = torch.empty(T, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = gdn.workspace_for(gdn.gdn_prefill_workspace_size(sh, 1, T))
+
+    def run(t0, init):
+        n = T - t0
+        gdn.gdn_prefill_chunked(sh, pool, cu_seqlens=torch.tensor([0, n], dtype=torch.int32, device="cuda"),
+                                start_pos=torch.tensor([t0], dtype=torch.int64, device="cuda"),
+                                init_page=torch.tensor([init], dtype=torch.int32, device="cuda"),
+                                block_table=bt, out_slot=slot, x=x[t0:], g=g[t0:], beta=beta[t0:], conv_w=w,
+                                o=o[t0:], dev_error=err, start_pos_host=[t0], init_page_host=[init],
+                                workspace=ws, max_seq_len=n)
+
+    def timed(t0, init):
+        run(t0, init)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            run(t0, init)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    cold_ms = timed(0, -1)
+    resume_ms = timed(start, int(bt[0, resume_block]))
+    if int(err.item()):
+        raise RuntimeError("device error word set in the long-context prefill")
+    del x, o, pool, ws
+    torch.cuda.empty_cache()
+    return {"tokens": T, "cold_ms": round(cold_ms, 2), "cold_tokens_per_s_per_layer": round(T / cold_ms * 1e3),
+            "resume_block": resume_block, "resume_from_tokens": start, "suffix_tokens": T - start,
+            "resume_ms": round(resume_ms, 2),
+            "resume_tokens_per_s_per_layer": round((T - start) / resume_ms * 1e3), "chains": sh.num_v_heads}
+
+
 # ----------------------------------------------------------------------------- cpu baseline
 
 def _oracle_setup(seed: int):
@@ -721,6 +782,8 @@ def main():
     if not args.no_flush_sweep:
         line["flush_sweep"] = flush_sweep(args.seed + 40 + rank, peaks["hbm_gbs"])
     line["checkpoint_copy"] = checkpoint_copy(args.seed + 50 + rank, peaks["hbm_gbs"])
+    if not args.no_flush_sweep:
+        line["long_context"] = long_context(args.seed + 60 + rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
