@@ -94,8 +94,10 @@ struct PfSmem {
   static constexpr uint32_t XS = 163840;
   static constexpr uint32_t XTILE = 17408;            // tile stride (1024-aligned)
   static constexpr uint32_t GT = XS + 2 * XTILE + kPfXRows * kPfD * 2;
-  // fp32 [64] each at GT: staged g, staged b, G, gam, dec = exp(G_C - G), b, q factor, k factor
-  static constexpr uint32_t MBAR = GT + 8 * 256;      // mbarriers: K^K^T, S0[K^;Q^]^T, U, U^T P^T, staged rows, state update
+  // fp32 [64] each at GT: G, gam, dec = exp(G_C - G), b of even chunks, the
+  // same of odd chunks (the issuing warp fills the next set while the workers
+  // still read the current one), q factor, k factor
+  static constexpr uint32_t MBAR = GT + 10 * 256;      // mbarriers: K^K^T, S0[K^;Q^]^T, U, U^T P^T, staged rows, state update
   static constexpr uint32_t TSLOT = MBAR + 48;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;     // + alignment slack
@@ -128,6 +130,15 @@ __device__ __forceinline__ float4 ldg_f4_fresh(const float* src) {
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(src));
   return v;
+}
+
+// Named barrier `id` over `count` threads: wait for the others, or only mark
+// this warp's arrival (a producer that does not wait for its consumers).
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
 // Barrier of the sixteen worker warps alone (threads 0..511).
@@ -310,14 +321,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   TIN* xq = reinterpret_cast<TIN*>(sm + PfSmem::XS);
   TIN* xk = reinterpret_cast<TIN*>(sm + PfSmem::XS + PfSmem::XTILE);
   TIN* xv = reinterpret_cast<TIN*>(sm + PfSmem::XS + 2 * PfSmem::XTILE);
-  float* gst = reinterpret_cast<float*>(sm + PfSmem::GT);
-  float* bst = gst + 64;
-  float* Gs = gst + 128;
-  float* gam = gst + 192;
-  float* dec = gst + 256;
-  float* bv = gst + 320;
-  float* rq = gst + 384;
-  float* rk = gst + 448;
+  float* gbuf = reinterpret_cast<float*>(sm + PfSmem::GT);   // two gate sets (by chunk parity)
+  float* rq = gbuf + 512;
+  float* rk = gbuf + 576;
   float* at = reinterpret_cast<float*>(sm + PfSmem::AT);
   float* tf = reinterpret_cast<float*>(sm + PfSmem::TF);
   TOUT* ot = reinterpret_cast<TOUT*>(sm + PfSmem::OT);
@@ -340,9 +346,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tS = tbase + tlane + kColS + 32 * quarter;   // this thread's 32 state columns
 
   // chunk c's pre-conv rows t0-3 .. t0+63 (three TMA tiles: q, k, v channels;
-  // rows outside x read as zeros) and its gates (zeros past the end).  Run by
-  // the workers; the rows before a sequence's first token are fixed up after
-  // they land (they belong to the previous sequence).
+  // rows outside x read as zeros).  The rows before a sequence's first token
+  // are fixed up after they land (they belong to the previous sequence).
   auto stage = [&](int64_t c) {
     const int64_t t0 = c * C;
     if (tid == 0) {
@@ -352,15 +357,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 4);
       tc::tma_load_2d(xv, &xmap, cv0, y, mbar + 4);
     }
-    if (tid < 2 * C) {
-      const int tt = tid & (C - 1);
-      const bool isb = tid >= C;
-      const int64_t t = t0 + tt;
-      const bool in = t < n;
-      const float* src = in ? (isb ? V.bptr(t, h) : V.gptr(t, h)) : p.g;
-      cp_async4((isb ? bst : gst) + tt, src, in ? 4 : 0);
-    }
-    cp_async_commit();
   };
   int64_t x_issued = -1;   // chunk whose rows are in flight (every worker tracks it)
   if (worker && nch > 0) {
@@ -399,6 +395,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
     issued = 0;
     ci = c;
+    // this chunk's gate set: G (running sum of the log decays), gam = exp(G),
+    // dec = exp(G_C - G), b; rows past the end have g = b = 0
+    float* const Gs = gbuf + 256 * (int)(c & 1);
+    float* const gam = Gs + 64;
+    float* const dec = Gs + 128;
+    float* const bv = Gs + 192;
+    if (!worker) {
+      // the issuing warp forms the gate set while the workers convolve (the
+      // set it overwrites was last read two chunks ago); the workers meet it
+      // at named barrier 3 before their first use
+      float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+      if (t0 + lane < n) { g0 = *V.gptr(t0 + lane, h); b0 = *V.bptr(t0 + lane, h); }
+      if (t0 + lane + 32 < n) { g1 = *V.gptr(t0 + lane + 32, h); b1 = *V.bptr(t0 + lane + 32, h); }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+        const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+        if (lane >= o) { g0 += a0; g1 += a1; }
+      }
+      g1 += __shfl_sync(0xffffffffu, g0, 31);
+      const float gC = __shfl_sync(0xffffffffu, g1, 31);
+      Gs[lane] = g0; Gs[lane + 32] = g1;
+      gam[lane] = expf(g0); gam[lane + 32] = expf(g1);
+      dec[lane] = expf(gC - g0); dec[lane + 32] = expf(gC - g1);
+      bv[lane] = b0; bv[lane + 32] = b1;
+      named_arrive(3, kPfThreads);
+    }
 
     if (worker) {
       const float4 wqk = ldg_f4_fresh(wqk_src), wv = ldg_f4_fresh(wv_src);
@@ -406,7 +429,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // has been read out
       if (tid == 0) tc::bulk_wait_read();
       ok = tc::mbar_wait_bounded(mbar + 4, par, kPfWait) && ok;
-      cp_async_wait<0>();
       workers_sync();
       if (ok) x_issued = -1;
       if (c == 0) {
@@ -466,25 +488,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         tc::tmem_st16(tbase + tlane + kColV + 16 * quarter, vr);
       }
-      // cumulative log decay, decay factors and b (rows past the end have g = b = 0)
-      if (warp == 0) {
-        float g0 = gst[lane], g1 = gst[lane + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
-          const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
-          if (lane >= o) { g0 += a0; g1 += a1; }
-        }
-        g1 += __shfl_sync(0xffffffffu, g0, 31);
-        const float gC = __shfl_sync(0xffffffffu, g1, 31);
-        Gs[lane] = g0; Gs[lane + 32] = g1;
-        gam[lane] = expf(g0); gam[lane + 32] = expf(g1);
-        dec[lane] = expf(gC - g0); dec[lane + 32] = expf(gC - g1);
-        bv[lane] = bst[lane]; bv[lane + 32] = bst[lane + 32];
-      }
       tc::tmem_st_wait();
       workers_sync();
-      // the staged rows and gates are consumed: prefetch the next chunk
+      // the staged rows are consumed: prefetch the next chunk
       if (c + 1 < nch) {
         stage(c + 1);
         x_issued = c + 1;
@@ -516,7 +522,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
         }
       }
-      workers_sync();
+      named_sync(3, kPfThreads);   // the norm factors, and the issuing warp's gate set
       // operands: [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T diag(dec) (row =
       // k channel); each thread loads all of its inputs before it stores.
       // The previous chunk's state update reads U^T and K^T diag(dec): it
@@ -820,7 +826,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (issued & 32u) tc::mbar_wait_bounded(mbar + 5, par, kPfWait);
     else if (s_pending && ci > 0) tc::mbar_wait_bounded(mbar + 5, (uint32_t)((ci - 1) & 1), kPfWait);
     if (worker && x_issued >= 0) tc::mbar_wait_bounded(mbar + 4, (uint32_t)(x_issued & 1), kPfWait);
-    cp_async_wait<0>();
   }
   if (tid == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
