@@ -69,6 +69,40 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
+def _smi_id(local: int) -> str:
+    """nvidia-smi's id of this process's device: its UUID (nvidia-smi numbers
+    the GPUs of the machine, not the ones this process sees)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+def _bind_near_gpu(local: int):
+    """Run this process on the CPUs next to its GPU (the sysfs local_cpulist
+    of the device), so that the pinned host buffers of the end-to-end
+    measurement are allocated in that node's memory.  Returns the CPU count,
+    or None where the list is not available (the affinity is then left as
+    it is)."""
+    try:
+        pr = torch.cuda.get_device_properties(local)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/local_cpulist" % (
+            pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        cpus = set()
+        with open(path) as f:
+            for part in f.read().strip().split(","):
+                a, _, b = part.partition("-")
+                cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if not cpus:
+            return None
+        os.sched_setaffinity(0, cpus)
+        return len(cpus)
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -77,14 +111,14 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
-        self.index = index
+        self.index = _smi_id(index)
         self.proc = None
         self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", self.index, f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -657,6 +691,8 @@ def main():
         return
     args.warmup = max(args.warmup, 3)
     torch.cuda.set_device(local)
+    all_cpus = os.sched_getaffinity(0)
+    near_cpus = _bind_near_gpu(local) if args.only == "all" else None
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -788,6 +824,9 @@ def main():
     line["checkpoint_copy"] = checkpoint_copy(args.seed + 50 + rank, peaks["hbm_gbs"])
     if not args.no_flush_sweep:
         line["long_context"] = long_context(args.seed + 60 + rank)
+    line["config"]["host_cpus"] = (f"{near_cpus} next to the GPU (end-to-end buffers)" if near_cpus
+                                   else "not bound")
+    os.sched_setaffinity(0, all_cpus)          # the oracle baseline uses every host core
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
