@@ -768,7 +768,9 @@ def main():
     # end to end through the same call with host buffers (prefill part):
     # every step copies its inputs in and its outputs out; the copies of
     # neighbouring steps overlap the prefill on their own streams
-    e2e_ms = pre.e2e_pipelined_ms(args.steps)
+    # (at least 16 steps: the timed region also fills and drains the pipeline once)
+    e2e_steps = max(args.steps, 16)
+    e2e_ms = pre.e2e_pipelined_ms(e2e_steps)
     (e2e_ms,) = max_over_ranks([e2e_ms], dist, "cuda")
 
     peaks, peak_kind = _peaks()
@@ -811,9 +813,12 @@ def main():
                      "hbm_gbs_achieved": pre.algorithmic_bytes() / (pre_ms * 1e-3) / 1e9,
                      "hbm_peak_kind": peak_kind},
         "e2e": {"value": job_throughput(pre.tokens, world, e2e_ms), "unit": "tokens/s/layer",
-                "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes,
+                "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes, "steps": e2e_steps,
                 "scope": "prefill part of the step; each step's input and output copies run on their own "
-                         "streams, overlapping the neighbouring steps' prefill (three device buffer sets)"},
+                         "streams, overlapping the neighbouring steps' prefill (three device buffer sets); "
+                         "timed from the first input copy to the last output copy of `steps` steps",
+                "link_note": "the host link of these boxes moves ~210 GB/s in and ~193 GB/s out (~295 GB/s "
+                             "both ways, the same for SM-driven copies), so ~3.9 ms of a step is copies"},
         # per step: prefill 2 (chunk kernel, windows); decode 1 per layer; replay
         # per layer: append 2 (tensor-core append, log_len), rollback 1, flush 2
         "gpu_launches": args.steps * (2 + DEC_LAYERS + 5 * REP_LAYERS),
