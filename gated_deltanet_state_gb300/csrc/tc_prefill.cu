@@ -364,11 +364,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     x_issued = 0;
   }
 
-  // conv taps of this thread's q | k channel (tid mod 256) and v channel
-  // (row), re-read from L1 / L2 at every chunk (an asm load the compiler does
-  // not hoist) rather than held in registers through the chunk's other phases
-  const int qkc = tid & 255;
-  const float* wqk_src = p.conv_w + (int64_t)(qkc < D ? cq0 + qkc : ck0 + qkc - D) * kConvK;
+  // conv taps of this thread's q | k channel pair and v channel (row),
+  // re-read from L1 / L2 at every chunk (an asm load the compiler does not
+  // hoist) rather than held in registers through the chunk's other phases
+  const int qkp = 2 * (tid & 127);   // this thread's q | k channel pair in the conv
+  const float* wqk_src = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;   // two tap sets
   const float* wv_src = p.conv_w + (int64_t)(cv0 + row) * kConvK;
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
 
     if (worker) {
-      const float4 wqk = ldg_f4_fresh(wqk_src), wv = ldg_f4_fresh(wv_src);
+      const float4 wqa = ldg_f4_fresh(wqk_src), wqb = ldg_f4_fresh(wqk_src + kConvK), wv = ldg_f4_fresh(wv_src);
       // ---- the chunk's rows and gates have landed; the previous output tile
       // has been read out
       if (tid == 0) tc::bulk_wait_read();
@@ -445,31 +445,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         workers_sync();
       }
 
-      // ---- (A) conv + SiLU.  q | k channel tid mod 256 for rows [32 rh, +32)
-      // -> y, in blocks of 16 rows whose loads all precede their stores.  Rows
-      // past the end are computed too and masked later: their norm factors and
-      // b are zero, so they contribute nothing (no data-dependent branch around
-      // the SiLU)
+      // ---- (A) conv + SiLU.  q | k channels qkp, qkp + 1 for rows [16 rh, +16)
+      // -> y, the two channels as packed fp32 pairs (one 32-bit load of the two
+      // bf16 inputs, one f32x2 instruction per tap, one 8-byte store; each
+      // element's arithmetic as in a scalar evaluation).  Rows past the end are
+      // computed too and masked later: their norm factors and b are zero, so
+      // they contribute nothing (no data-dependent branch around the SiLU)
       {
-        const int r0 = 32 * (tid >> 8);
-        const TIN* xc_ = qkc < D ? xq + qkc : xk + qkc - D;
-        float xa = to_f32(xc_[r0 * D]), xb = to_f32(xc_[(r0 + 1) * D]), xc = to_f32(xc_[(r0 + 2) * D]);
-#pragma unroll 1
-        for (int tb = r0; tb < r0 + 32; tb += 16) {
-          float xr[16], yv[16];
+        const int tb = 16 * (tid >> 7);
+        const TIN* xp = (qkp < D ? xq + qkp : xk + qkp - D) + tb * D;
+        const f32x2 w0 = pack2(wqa.x, wqb.x), w1 = pack2(wqa.y, wqb.y), w2 = pack2(wqa.z, wqb.z),
+                    w3 = pack2(wqa.w, wqb.w);
+        f32x2 x[19];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) xr[u] = to_f32(xc_[(tb + u + 3) * D]);
+        for (int u = 0; u < 19; ++u) {
+          // a bf16 is the upper half of its fp32: shift the first channel up, mask the second
+          const uint32_t v = *reinterpret_cast<const uint32_t*>(xp + u * D);
+          x[u] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+        }
+        float* yrow = yf + tb * 256 + qkp;
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float z = wqk.x * xa;
-            z = fmaf(wqk.y, xb, z);
-            z = fmaf(wqk.z, xc, z);
-            z = fmaf(wqk.w, xr[u], z);
-            yv[u] = silu_fast(z);
-            xa = xb; xb = xc; xc = xr[u];
-          }
-#pragma unroll
-          for (int u = 0; u < 16; ++u) yf[(tb + u) * 256 + qkc] = yv[u];
+        for (int i = 0; i < 16; ++i) {
+          f32x2 z = mul2(w0, x[i]);
+          z = fma2(w1, x[i + 1], z);
+          z = fma2(w2, x[i + 2], z);
+          z = fma2(w3, x[i + 3], z);
+          const float2 zz = unpack2(z);
+          *reinterpret_cast<float2*>(yrow + i * 256) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
         }
       }
       // v channel `row` for rows [16 quarter, +16) -> tensor memory (lane = channel)
