@@ -163,6 +163,26 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)
   }
 }
 
+// Eight fp32 values as bf16 hi and lo parts (x ~= hi + lo), converted in
+// pairs, each part stored as one 16-byte vector.  The rounded pair comes back
+// to fp32 by shifting and masking its halves (a bf16 is the upper half of its
+// fp32), and both remainders take one packed subtraction.
+__device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, const float* e) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
+    const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hb);
+    const float2 r = unpack2(sub2(pack2(e[2 * u], e[2 * u + 1]),
+                                  pack2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xFFFF0000u))));
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
+    h[u] = hw;
+    l[u] = *reinterpret_cast<const uint32_t*>(&lb);
+  }
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // bf16 hi / lo split: x ~= hi + lo with |x - hi - lo| <= 2^-16 |x| (about).
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);

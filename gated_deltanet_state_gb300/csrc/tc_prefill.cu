@@ -105,26 +105,6 @@ struct PfSmem {
 static_assert(PfSmem::GT % 16 == 0, "gate staging must be 16-byte aligned");
 static_assert(PfSmem::ALLOC <= 232448, "shared memory plan exceeds the per-CTA limit");
 
-// Eight fp32 values as bf16 hi and lo parts (x ~= hi + lo), converted in
-// pairs, each part stored as one 16-byte vector.  The rounded pair comes back
-// to fp32 by shifting and masking its halves (a bf16 is the upper half of its
-// fp32), and both remainders take one packed subtraction.
-__device__ __forceinline__ void store_split8(uint8_t* hi, uint8_t* lo, const float* e) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const __nv_bfloat162 hb = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
-    const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hb);
-    const float2 r = unpack2(sub2(pack2(e[2 * u], e[2 * u + 1]),
-                                  pack2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xFFFF0000u))));
-    const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
-    h[u] = hw;
-    l[u] = *reinterpret_cast<const uint32_t*>(&lb);
-  }
-  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 // Four floats through the read-only path by an asm load that the compiler
 // keeps where it stands (a loop-invariant plain load would be hoisted and
 // its registers held through the whole loop).
@@ -555,7 +535,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
                               yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
           const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
-          store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
+          tc::store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
         }
         float kt[NKT][8];
 #pragma unroll
@@ -571,7 +551,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int it = 0; it < NKT; ++it) {
           const int i = tid + kPfWorkers * it, k = i & 127, j8 = i >> 7;
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
-          store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
+          tc::store_split8(sm + PfSmem::KT + off, sm + PfSmem::KT_LO + off, kt[it]);
         }
       }
       tc::fence_async_smem();
@@ -604,7 +584,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
           const uint32_t off = tc::sw128_offset(row, 32 * quarter + 16 * hh + 8 * c8, 128);
-          store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
+          tc::store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) v0[e] *= gC;
@@ -659,7 +639,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
           const uint32_t off = tc::sw128_offset(ir, 16 * quarter + 8 * c8, 64);
-          store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
+          tc::store_split8(sm + PfSmem::PB + off, sm + PfSmem::PB_LO + off, ap + 8 * c8);
         }
       }
       workers_sync();
@@ -676,7 +656,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int u = 0; u < 8; ++u)
             if (8 * c8 + u > i) v8[u] = 0.f;
           const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
-          store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
+          tc::store_split8(sm + PfSmem::TB + off, sm + PfSmem::TB_LO + off, v8);
         }
       } else {
         // R_i = b_i (v_i - gam_i (S0 k^_i)) of state row `row` for rows i in
@@ -692,7 +672,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int c8 = 0; c8 < 2; ++c8) {
             const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
-            store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
+            tc::store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, a + 8 * c8);
           }
         }
       }
@@ -715,7 +695,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int c8 = 0; c8 < 2; ++c8) {
         const uint32_t off = tc::sw128_offset(row, 16 * quarter + 8 * c8, 128);
-        store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, u + 8 * c8);
+        tc::store_split8(sm + PfSmem::UT + off, sm + PfSmem::UT_LO + off, u + 8 * c8);
       }
       tc::fence_async_smem();
     }

@@ -89,22 +89,6 @@ __device__ __forceinline__ uint32_t rp_state_offset(int row, int col) {
   return (uint32_t)((col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) + ((col & 3) << 2));
 }
 
-// Eight fp32 values as bf16 hi and lo parts (x ~= hi + lo), each part stored
-// as one 16-byte vector.
-__device__ __forceinline__ void rp_split8(uint8_t* hi, uint8_t* lo, const float* e) {
-  uint32_t hw[4], lw[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const __nv_bfloat162 hb = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
-    const float2 hf = __bfloat1622float2(hb);
-    const __nv_bfloat162 lb = __floats2bfloat162_rn(e[2 * u] - hf.x, e[2 * u + 1] - hf.y);
-    hw[u] = *reinterpret_cast<const uint32_t*>(&hb);
-    lw[u] = *reinterpret_cast<const uint32_t*>(&lb);
-  }
-  *reinterpret_cast<uint4*>(hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  *reinterpret_cast<uint4*>(lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-}
-
 // Diagonal entry `lane` of a register row (a select chain: no local memory).
 template <int N>
 __device__ __forceinline__ float rp_pick(const float (&v)[N], int idx) {
@@ -389,7 +373,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
 #pragma unroll
     for (int c8 = 0; c8 < 8; ++c8) {
       const uint32_t off = tc::sw128_offset(row, 64 * half + 8 * c8, D);
-      rp_split8(sm + S::A1 + off, sm + S::A1_LO + off, sv + 8 * c8);
+      tc::store_split8(sm + S::A1 + off, sm + S::A1_LO + off, sv + 8 * c8);
     }
     if (!APPEND) {
       const float gN = gam[(BND ? bj : L) - 1];
@@ -564,7 +548,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
 #pragma unroll
       for (int c8 = 0; c8 < NMAX / 8; ++c8) {
         const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
-        rp_split8(sm + S::B2 + off, sm + S::B2_LO + off, kt + 8 * c8);
+        tc::store_split8(sm + S::B2 + off, sm + S::B2_LO + off, kt + 8 * c8);
       }
     }
   } else if (ok && half == 1) {
@@ -585,7 +569,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
 #pragma unroll
       for (int c8 = 0; c8 < NMAX / 8; ++c8) {
         const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
-        rp_split8(sm + S::A2 + off, sm + S::A2_LO + off, rr + 8 * c8);
+        tc::store_split8(sm + S::A2 + off, sm + S::A2_LO + off, rr + 8 * c8);
       }
     }
   } else {
@@ -629,7 +613,7 @@ __device__ __forceinline__ void replay_body(const ScanParams& p, const CUtensorM
 #pragma unroll
         for (int c8 = 0; c8 < NMAX / 8; ++c8) {
           const uint32_t off = tc::sw128_offset(row, 8 * c8, D);
-          rp_split8(sm + S::B2 + off, sm + S::B2_LO + off, kt + 8 * c8);
+          tc::store_split8(sm + S::B2 + off, sm + S::B2_LO + off, kt + 8 * c8);
         }
       }
       const float scale = __expf(Gs[L - 1] - Gs[bj - 1]);
