@@ -460,17 +460,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // v channel `row` for rows [16 quarter, +16) -> tensor memory (lane = channel)
       {
+        // rows i and i + 8 as one packed pair (their windows do not overlap)
         const int tb = 16 * quarter;
         float xr[19], vr[16];
 #pragma unroll
         for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
+        const f32x2 w0 = pack2(wv.x, wv.x), w1 = pack2(wv.y, wv.y), w2 = pack2(wv.z, wv.z), w3 = pack2(wv.w, wv.w);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float z = wv.x * xr[i];
-          z = fmaf(wv.y, xr[i + 1], z);
-          z = fmaf(wv.z, xr[i + 2], z);
-          z = fmaf(wv.w, xr[i + 3], z);
-          vr[i] = silu_fast(z);
+        for (int i = 0; i < 8; ++i) {
+          f32x2 z = mul2(w0, pack2(xr[i], xr[i + 8]));
+          z = fma2(w1, pack2(xr[i + 1], xr[i + 9]), z);
+          z = fma2(w2, pack2(xr[i + 2], xr[i + 10]), z);
+          z = fma2(w3, pack2(xr[i + 3], xr[i + 11]), z);
+          const float2 zz = unpack2(z);
+          vr[i] = silu_fast(zz.x);
+          vr[i + 8] = silu_fast(zz.y);
         }
         tc::tmem_st16(tbase + tlane + kColV + 16 * quarter, vr);
       }
@@ -532,8 +536,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int it = 0; it < NKQ; ++it) {
           const int i = tid + kPfWorkers * it, r = i >> 4, c8 = i & 15;
           const float f = fv[it];
-          const float e[8] = {ya[it].x * f, ya[it].y * f, ya[it].z * f, ya[it].w * f,
-                              yb[it].x * f, yb[it].y * f, yb[it].z * f, yb[it].w * f};
+          const f32x2 f2 = pack2(f, f);
+          const float2 e01 = unpack2(mul2(pack2(ya[it].x, ya[it].y), f2));
+          const float2 e23 = unpack2(mul2(pack2(ya[it].z, ya[it].w), f2));
+          const float2 e45 = unpack2(mul2(pack2(yb[it].x, yb[it].y), f2));
+          const float2 e67 = unpack2(mul2(pack2(yb[it].z, yb[it].w), f2));
+          const float e[8] = {e01.x, e01.y, e23.x, e23.y, e45.x, e45.y, e67.x, e67.y};
           const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
           tc::store_split8(sm + PfSmem::KQ + off, sm + PfSmem::KQ_LO + off, e);
         }
@@ -587,7 +595,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc::store_split8(sm + PfSmem::S0 + off, sm + PfSmem::S0_LO + off, v0 + 8 * c8);
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v0[e] *= gC;
+        for (int e = 0; e < 16; e += 2) {
+          const float2 g = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+          v0[e] = g.x;
+          v0[e + 1] = g.y;
+        }
         tc::tmem_st16(tS + 16 * hh, v0);
       }
       tc::tmem_st_wait();
