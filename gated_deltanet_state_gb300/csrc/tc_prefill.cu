@@ -502,13 +502,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           ss[it] = a;
         }
+        // the eight sums over the warp at once: lanes 16 apart swap half of
+        // their partial sums and add (four sums left per lane), then lanes 8
+        // apart (two), 4 apart (one), and two more levels finish it; lane l
+        // ends with the total of pair (l >> 2) (9 shuffles instead of 40)
+        static_assert(NP == 8, "the halving reduction is written for eight sums");
+        float h4[4], h2[2];
 #pragma unroll
-        for (int it = 0; it < NP; ++it) ss[it] = warp_sum(ss[it]);
-        if (lane < NP) {
-          float a = ss[0];
+        for (int j = 0; j < 4; ++j) {
+          const bool up = lane & 16;
+          const float send = up ? ss[j] : ss[j + 4];
+          h4[j] = (up ? ss[j + 4] : ss[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
 #pragma unroll
-          for (int it = 1; it < NP; ++it) a = lane == it ? ss[it] : a;
-          const int k = warp + (kPfWorkers / 32) * lane, t = k >> 1, isk = k & 1;
+        for (int j = 0; j < 2; ++j) {
+          const bool up = lane & 8;
+          const float send = up ? h4[j] : h4[j + 2];
+          h2[j] = (up ? h4[j + 2] : h4[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        float a;
+        {
+          const bool up = lane & 4;
+          a = (up ? h2[1] : h2[0]) + __shfl_xor_sync(0xffffffffu, up ? h2[0] : h2[1], 4);
+        }
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        if ((lane & 3) == 0) {
+          const int k = warp + (kPfWorkers / 32) * (lane >> 2), t = k >> 1, isk = k & 1;
           (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
         }
       }
