@@ -45,10 +45,10 @@ PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
 # DRAM bytes (read + write) of one tensor-core prefill launch, from an ncu
-# capture of the current kernel at 4 x 2,048 tokens (173.1 MB read + 94.9 MB
+# capture of the current kernel at 4 x 2,048 tokens (173.0 MB read + 93.4 MB
 # written), scaled by 4 to the 4 x 8,192 launch (the traffic is per token).
 # None once the kernel changes.
-PREFILL_TRAFFIC_PER_LAUNCH = (173.051648e6 + 94.948096e6) * 4
+PREFILL_TRAFFIC_PER_LAUNCH = (172.977152e6 + 93.397248e6) * 4
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
