@@ -22,8 +22,9 @@
 // bit for bit.  The fp32 state lives in tensor memory from the first chunk to
 // the last.  Per chunk:
 //   (A) conv + SiLU of the chunk's q, k, v channels from pre-conv rows staged
-//       in shared memory (prefetched during the previous chunk), L2 norms,
-//       cumulative gates; operands [K^; Q^] and K^T diag(exp(G_C - G)).
+//       in shared memory (prefetched during the previous chunk; packed fp32
+//       pairs), L2 norms; meanwhile the issuing warp forms the cumulative
+//       gates; operands [K^; Q^] and K^T diag(exp(G_C - G)).
 //   (B) S0 from tensor memory into a bf16 operand (and gam_C S0 back);
 //       tensor cores: [K^K^T; Q^K^T] and S0 [K^; Q^]^T.
 //   (C) A and P = exp(G_i - G_j) q^_i.k^_j (j <= i) (computed while the
