@@ -88,8 +88,11 @@ def test_decode_bad_slot_sets_error_and_skips():
     assert torch.equal(pool.payload(0).cpu(), before[:sh.payload_bytes])
 
 
-def test_checkpoint_copy_is_bit_exact_with_nan_payloads():
-    sh = inputs.TINY
+@pytest.mark.parametrize("sh", [inputs.TINY, inputs.QWEN27B], ids=["tiny", "27b"])
+def test_checkpoint_copy_is_bit_exact_with_nan_payloads(sh):
+    # the tiny payload (656 words) is copied one word per thread; the 27B-shaped
+    # one (200,448 words) mostly four words per thread, then the remainder
+    B = sh.block_size
     pool = gdn.StatePool(sh, 6, fill=0)
     g = torch.Generator().manual_seed(3)
     raw = torch.randint(0, 256, (sh.payload_bytes,), dtype=torch.uint8, generator=g)
@@ -98,16 +101,16 @@ def test_checkpoint_copy_is_bit_exact_with_nan_payloads():
     pool.payload(1).copy_(raw.cuda())
     pool.payload(2).copy_(raw.flip(0).cuda())
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    gdn.gdn_checkpoint_resume(sh, pool, dev([1, 2], torch.int32), dev([4, 5], torch.int32), [64, 128], err)
+    gdn.gdn_checkpoint_resume(sh, pool, dev([1, 2], torch.int32), dev([4, 5], torch.int32), [B, 2 * B], err)
     torch.cuda.synchronize()
     assert err.item() == 0
     assert torch.equal(pool.payload(4).cpu(), raw)
     assert torch.equal(pool.payload(5).cpu(), raw.flip(0))
     with pytest.raises(gdn.GdnError) as ei:
-        gdn.gdn_checkpoint_save(sh, pool, dev([4], torch.int32), dev([3], torch.int32), [65], err)
+        gdn.gdn_checkpoint_save(sh, pool, dev([4], torch.int32), dev([3], torch.int32), [B + 1], err)
     assert ei.value.status == gdn.STATUS_CODE["GDN_ERR_NOT_BLOCK_ALIGNED"]
     assert (pool.payload(3).cpu() == 0).all()
-    gdn.gdn_checkpoint_save(sh, pool, dev([4], torch.int32), dev([9], torch.int32), [64], err)
+    gdn.gdn_checkpoint_save(sh, pool, dev([4], torch.int32), dev([9], torch.int32), [B], err)
     torch.cuda.synchronize()
     assert err.item() == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
 
