@@ -781,6 +781,7 @@ def main():
     fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
     ver_gbs = rep.verify_bytes_per_layer() / (ver_ms / REP_LAYERS * 1e-3) / 1e9
     value = job_throughput(pre.tokens, world, pre_ms)
+    pre_launches = gdn.gdn_prefill_plan_for(PREFILL, N_SEQ, args.seq_len)["launches"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
@@ -819,9 +820,11 @@ def main():
                          "timed from the first input copy to the last output copy of `steps` steps",
                 "link_note": "the host link of these boxes moves ~210 GB/s in and ~193 GB/s out (~295 GB/s "
                              "both ways, the same for SM-driven copies), so ~3.9 ms of a step is copies"},
-        # per step: prefill 2 (chunk kernel, windows); decode 1 per layer; replay
-        # per layer: append 2 (tensor-core append, log_len), rollback 1, flush 2
-        "gpu_launches": args.steps * (2 + DEC_LAYERS + 5 * REP_LAYERS),
+        # per step: prefill (the chunk kernel's launches, as the library plans
+        # them on this GPU, + the window pass); decode 1 per layer; replay per
+        # layer: append 2 (tensor-core append, log_len), rollback 1, flush 2
+        "gpu_launches": args.steps * (pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
+        "prefill_chunk_launches": pre_launches,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if not args.no_flush_sweep:

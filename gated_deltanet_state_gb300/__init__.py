@@ -27,7 +27,8 @@ __all__ = [
     "gdn_status_string", "gdn_version", "gdn_conv_dim", "gdn_mamba_page_bytes",
     "gdn_block_size_for", "gdn_mamba_pages_per_request", "gdn_pool_blocks_for_pages",
     "gdn_chunk_end", "gdn_cached_tokens", "gdn_resume_block", "gdn_replay_boundary_rows", "gdn_spec_copy_bytes",
-    "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_replay_workspace_size",
+    "gdn_replay_bytes_per_request", "gdn_prefill_workspace_size", "gdn_prefill_plan_for",
+    "gdn_replay_workspace_size",
     "gdn_prefill_chunked", "gdn_prefill_chunked_noalloc", "workspace_for", "NOALLOC_SCRATCH_BYTES",
     "gdn_mixed_workspace_size", "gdn_mixed_step",
     "gdn_core_prefill_workspace_size", "gdn_core_prefill", "gdn_core_decode",
@@ -114,6 +115,11 @@ class _ReplayArgs(ctypes.Structure):
                 ("boundary_page", _P)]
 
 
+class _PrefillPlan(ctypes.Structure):
+    _fields_ = [("chains", ctypes.c_int64), ("piece_chunks", ctypes.c_int64), ("levels", ctypes.c_int64),
+                ("ctas_per_launch", ctypes.c_int64), ("launches", ctypes.c_int64)]
+
+
 # --------------------------------------------------------------------------- loading
 
 def library_path() -> str:
@@ -149,6 +155,7 @@ def load_library(build_if_missing: bool = True):
         "gdn_spec_copy_bytes": ([i32, i32, i64], i64),
         "gdn_replay_bytes_per_request": ([i32, i64, i32, i64], i64),
         "gdn_prefill_workspace_size": ([D, i32, i64], sz),
+        "gdn_prefill_plan_for": ([D, i32, i64, i32, ctypes.POINTER(_PrefillPlan)], i32),
         "gdn_replay_workspace_size": ([D, i32], sz),
         "gdn_prefill_chunked": ([D, PL, ctypes.POINTER(_PrefillArgs), _P, sz, _P], i32),
         "gdn_prefill_chunked_noalloc": ([D, PL, ctypes.POINTER(_PrefillArgs), _P], i32),
@@ -310,6 +317,15 @@ def gdn_replay_bytes_per_request(num_gdn_layers: int, page_bytes: int, log_slots
 
 def gdn_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: int) -> int:
     return int(load_library().gdn_prefill_workspace_size(ctypes.byref(make_desc(shape)), num_seqs, total_tokens))
+
+
+def gdn_prefill_plan_for(shape: LayerShape, num_seqs: int, max_seq_len: int, num_sms: int = 0) -> dict:
+    """The chunk-kernel plan of one prefill call (num_sms <= 0: the current
+    device's SM count)."""
+    out = _PrefillPlan()
+    _check(load_library().gdn_prefill_plan_for(ctypes.byref(make_desc(shape)), num_seqs, max_seq_len, num_sms,
+                                               ctypes.byref(out)), "gdn_prefill_plan_for")
+    return {f: int(getattr(out, f)) for f, _ in _PrefillPlan._fields_}
 
 
 def gdn_replay_workspace_size(shape: LayerShape, num_reqs: int) -> int:

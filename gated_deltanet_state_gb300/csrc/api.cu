@@ -80,6 +80,23 @@ size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                               desc->num_v_heads);
 }
 
+gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
+                                int32_t num_sms, gdn_prefill_plan* out) {
+  if (!desc || !out || gdn_conv_dim(desc) <= 0 || num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                            desc->block_size))
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  const PrefillSchedule sc = tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len,
+                                                 num_sms > 0 ? num_sms : tc_prefill_sm_count());
+  out->chains = sc.nchains;
+  out->piece_chunks = sc.piece;
+  out->levels = sc.levels;
+  out->ctas_per_launch = sc.width;
+  out->launches = sc.launches;
+  return GDN_OK;
+}
+
 size_t gdn_replay_workspace_size(const gdn_layer_desc* desc, int32_t num_reqs) {
   if (gdn_conv_dim(desc) <= 0 || num_reqs < 0) return 0;
   return scan_workspace_bytes((int64_t)num_reqs * GDN_REPLAY_LOG_SLOTS, (int)gdn_conv_dim(desc),

@@ -72,8 +72,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t launch_tc_flush(const ScanParams& p, cudaStream_t st);
 cudaError_t launch_tc_append(const ScanParams& p, cudaStream_t st);
 // Tensor-core chunked prefill (dk = dv = 128, bf16 in and out, block size a
-// multiple of 64), followed by the window pass; needs no workspace.
+// multiple of 64), followed by the window pass; needs no workspace.  The
+// (sequence, value head) chains run whole in one launch, or cut into pieces
+// of `piece` chunks over several launches (tc_prefill_schedule).
+struct PrefillSchedule {
+  int64_t nchains;    // value heads x sequences
+  int64_t piece;      // chunks per piece (the last level runs to the end)
+  int64_t levels;     // pieces per chain of max_len tokens
+  int64_t width;      // CTAs per launch
+  int64_t launches;   // chunk-kernel launches
+};
+PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
+int tc_prefill_sm_count();   // SMs of the current device (0 if unknown: one launch)
 bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size);
-cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st);
+cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t st);
 
 }  // namespace gdn

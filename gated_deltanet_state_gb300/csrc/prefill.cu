@@ -12,7 +12,7 @@ void bind_workspace(ScanParams& p, void* ws, int64_t rows) { ws_bind(p, ws, rows
 
 cudaError_t launch_prefill(const ScanParams& p, int64_t max_len, int dk, int dv, int in_dtype,
                            int out_dtype, cudaStream_t st) {
-  if (tc_prefill_supported(dk, dv, in_dtype, out_dtype, p.block_size)) return launch_tc_prefill(p, st);
+  if (tc_prefill_supported(dk, dv, in_dtype, out_dtype, p.block_size)) return launch_tc_prefill(p, max_len, st);
   GDN_SCAN_DISPATCH(kPrefill)
 }
 

@@ -106,6 +106,16 @@ struct PfSmem {
 static_assert(PfSmem::GT % 16 == 0, "gate staging must be 16-byte aligned");
 static_assert(PfSmem::ALLOC <= 232448, "shared memory plan exceeds the per-CTA limit");
 
+// Which piece of which chain a CTA runs.  A launch takes consecutive
+// (level, sequence) pairs of the level-major order, at most nseqs of them,
+// each with all value heads: CTA (h, b) runs head h of sequence s0 + b at
+// level0, or past the last sequence, of sequence s0 + b - nseqs at level0 + 1;
+// its chunks are [level * piece, +piece) of the chain (the last level: to the
+// sequence's end).
+struct PieceMap {
+  int32_t s0, level0, nseqs, piece, last_level;
+};
+
 // Four floats through the read-only path by an asm load that the compiler
 // keeps where it stands (a loop-invariant plain load would be hoisted and
 // its registers held through the whole loop).
@@ -277,11 +287,17 @@ __device__ __forceinline__ bool cta_sync_ok(bool ok) {
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     tc_prefill_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap,
-                      const __grid_constant__ CUtensorMap omap, int tma_out) {
+                      const __grid_constant__ CUtensorMap omap, int tma_out, const PieceMap pm) {
   using TIN = __nv_bfloat16;
   using TOUT = __nv_bfloat16;
   constexpr int D = kPfD, C = kPfC;
-  const int h = blockIdx.x, s = blockIdx.y;
+  // this CTA's piece: chain (sequence s, value head h), chunks [cb, ce)
+  const int h = blockIdx.x;
+  int s = pm.s0 + (int)blockIdx.y, level = pm.level0;
+  if (s >= pm.nseqs) {
+    s -= pm.nseqs;
+    ++level;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool worker = tid < kPfWorkers;
   const int row = tid & 127;                  // state row = tensor-memory lane of this thread
@@ -291,10 +307,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   TokenView<TIN> V;
   int64_t start, n_log;
   int32_t init, final_page;
-  const bool report = (h == 0 && tid == 0);
+  const bool report = (h == 0 && level == 0 && tid == 0);
   if (!make_view<TIN, kPrefill>(p, s, V, start, init, final_page, n_log, report)) return;
   const int64_t n = V.n;
   const int64_t nch = (n + C - 1) / C;
+  // the first piece of a chain starts from the resumed page (or zeros) and
+  // always runs (it also writes the state of an empty sequence); a later one
+  // starts from the state the previous piece left in the final slot, and the
+  // last level runs to the sequence's end
+  const int64_t cb = (int64_t)level * pm.piece;   // even: a piece is a power of two >= 4 chunks
+  if (level > 0 && cb >= nch) return;
+  const int64_t ce = level == pm.last_level || cb + pm.piece > nch ? nch : cb + pm.piece;
+  const int32_t from = level > 0 ? final_page : init;
   const int grp = p.Hv / p.Hqk, jq = h / grp;
   const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
   const int64_t row0 = p.cu_seqlens[s];      // first row of this sequence in x, g, beta, o
@@ -344,9 +368,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   };
   int64_t x_issued = -1;   // chunk whose rows are in flight (every worker tracks it)
-  if (worker && nch > 0) {
-    stage(0);
-    x_issued = 0;
+  if (worker && cb < ce) {
+    stage(cb);
+    x_issued = cb;
   }
 
   // conv taps of this thread's q | k channel pair and v channel (row),
@@ -357,7 +381,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const float* wv_src = p.conv_w + (int64_t)(cv0 + row) * kConvK;
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
-    const float* src = init >= 0 ? page_state(p.pool, init) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+    const float* src = from >= 0 ? page_state(p.pool, from) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
     float v[32];
 #pragma unroll
     for (int c4 = 0; c4 < 8; ++c4) {
@@ -372,10 +396,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   bool ok = true;
   uint32_t issued = 0;  // tensor-core products committed in the current chunk (bit b: mbar[b])
   bool s_pending = false;   // the previous chunk's state update may still be running
-  int64_t ci = 0;           // the chunk `issued` refers to
-  int64_t c = 0;
-  for (; c < nch; ++c) {
-    const uint32_t par = (uint32_t)(c & 1);   // each mbarrier completes once per chunk
+  int64_t ci = cb;          // the chunk `issued` refers to
+  int64_t c = cb;
+  for (; c < ce; ++c) {
+    // each mbarrier completes once per chunk; a piece starts at an even chunk,
+    // so the parity of its first wait is 0
+    const uint32_t par = (uint32_t)(c & 1);
     const int64_t t0 = c * C;
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
     issued = 0;
@@ -482,7 +508,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc::tmem_st_wait();
       workers_sync();
       // the staged rows are consumed: prefetch the next chunk
-      if (c + 1 < nch) {
+      if (c + 1 < ce) {
         stage(c + 1);
         x_issued = c + 1;
       }
@@ -852,12 +878,65 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tbase, kPfCols);
 }
 
+int tc_prefill_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// One CTA holds an SM for a whole chain, so the Hv x N chains of maxc chunks
+// take ceil(Hv N / sms) rounds of maxc chunk times in one launch: 192 chains
+// on 152 SMs take two, the second with 40 SMs busy.  A chain's chunks must
+// run in order, but its state can move between launches exactly (fp32
+// through the final slot's page), so the chains are cut into pieces of P
+// chunks and run level by level: (level, sequence) pairs in level-major order
+// (every sequence's first pieces, then every second piece, ...), floor(sms /
+// Hv) pairs of Hv CTAs a launch.  With N >= that many pairs, consecutive
+// pieces of a chain are N pairs apart, so each lands in a later launch than
+// the one before it, and no launch holds two pieces of one chain.  Each
+// chunk's arithmetic is the same as in one launch, so the results are
+// bitwise the same.  A piece costs about one chunk time more (state in and
+// out, the first rows' load, the launch gap); P is the power of two >= 4 with
+// the least estimated time, kept only when it saves 5 % over one launch and
+// needs at most 64 launches.  A piece starts at an even chunk, which keeps
+// the kernel's mbarrier parities (chunk & 1) valid.
+PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int sms) {
+  constexpr int64_t kPieceCost = 1, kMinPiece = 4, kMaxLaunches = 64;
+  PrefillSchedule sc;
+  sc.nchains = (int64_t)Hv * num_seqs;
+  const int64_t maxc = max_len > 0 ? (max_len + kPfC - 1) / kPfC : 0;
+  sc.piece = maxc > 0 ? (maxc < (1 << 30) ? maxc : (1 << 30)) : 1;
+  sc.levels = 1;
+  sc.width = sc.nchains;
+  sc.launches = sc.nchains > 0 ? 1 : 0;
+  const int64_t per = Hv > 0 && sms > 0 ? sms / Hv : 0;   // pairs a launch
+  if (per < 1 || num_seqs < per || sc.nchains < sms || maxc < 2 * kMinPiece) return sc;
+  const double single = (double)((sc.nchains + sms - 1) / sms) * (double)(maxc + kPieceCost);
+  double best = 0.95 * single;
+  for (int64_t P = kMinPiece; P < maxc; P *= 2) {
+    const int64_t levels = (maxc + P - 1) / P;
+    const int64_t launches = (levels * num_seqs + per - 1) / per;
+    if (launches > kMaxLaunches) continue;
+    const double cost = (double)launches * (double)(P + kPieceCost);
+    if (cost < best) {
+      best = cost;
+      sc.piece = P;
+      sc.levels = levels;
+      sc.width = per * Hv;
+      sc.launches = launches;
+    }
+  }
+  return sc;
+}
+
 bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size) {
   return dk == kPfD && dv == kPfD && in_dtype == GDN_BF16 && out_dtype == GDN_BF16 && block_size % kPfC == 0;
 }
 
-cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st) {
+cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
+  if ((int64_t)p.Hv * p.num_seqs > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
   CUtensorMap xmap, omap;
   memset(&xmap, 0, sizeof(xmap));
   memset(&omap, 0, sizeof(omap));
@@ -892,9 +971,21 @@ cudaError_t launch_tc_prefill(const ScanParams& p, cudaStream_t st) {
   const size_t smem = PfSmem::ALLOC;
   cudaError_t e = cudaFuncSetAttribute(tc_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_prefill_kernel<<<dim3(p.Hv, p.num_seqs), kPfThreads, smem, st>>>(p, xmap, omap, tma_out);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  const PrefillSchedule sc = tc_prefill_schedule(p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
+  PieceMap pm;
+  pm.nseqs = p.num_seqs;
+  pm.piece = (int32_t)sc.piece;
+  pm.last_level = (int32_t)(sc.levels - 1);
+  const int64_t pairs = sc.levels * p.num_seqs, per = sc.width / p.Hv;   // (level, sequence) pairs
+  for (int64_t t = 0; t < sc.launches; ++t) {
+    const int64_t base = t * per;
+    pm.s0 = (int32_t)(base % p.num_seqs);
+    pm.level0 = (int32_t)(base / p.num_seqs);
+    const int64_t cnt = pairs - base < per ? pairs - base : per;
+    tc_prefill_kernel<<<dim3(p.Hv, (unsigned)cnt), kPfThreads, smem, st>>>(p, xmap, omap, tma_out, pm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // conv windows of every crossed boundary and of the final slot
   window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
   return cudaGetLastError();

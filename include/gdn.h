@@ -216,7 +216,10 @@ int64_t gdn_replay_bytes_per_request(int32_t num_gdn_layers, int64_t page_bytes,
  * (skipped when that entry is -1): every crossed boundary is checkpointed,
  * also inside one call ("The prefix cache changed the answer", section "The
  * fix: one line").  The state after the last token goes to page out_slot[s],
- * which may equal init_page[s].  o receives S_t q_t for every token.
+ * which may equal init_page[s]; during the call the page may also hold the
+ * state between launches (gdn_prefill_plan_for), so, as for any page
+ * the call writes, no other sequence of the call may read or write it.  o
+ * receives S_t q_t for every token.
  *
  * Determinism: results depend only on a sequence's own inputs, never on the
  * batch, the call's length or where earlier calls split the sequence; a
@@ -254,6 +257,33 @@ typedef struct gdn_prefill_args {
  * not overlap on the GPU.  0 for a malformed desc. */
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens);
+
+/* How gdn_prefill_chunked runs the chunk kernel of a layer on the
+ * tensor-core path.  Each (sequence, value head) chain runs on one SM, its
+ * chunks in order.  With at least as many chains as SMs and long chains,
+ * whole chains would leave SMs idle in the last round, so the chains are cut
+ * into pieces of piece_chunks chunks and run as `launches` launches of up to
+ * ctas_per_launch CTAs: all chains' first pieces, then all second pieces, and
+ * so on, ctas_per_launch at a time (a piece starts from the state the piece
+ * before it left in page out_slot[s]; the last piece of a chain runs to its
+ * end).  Every chunk's arithmetic is unchanged, so the results are bitwise
+ * those of one launch.  One launch (levels = 1) is kept unless pieces save
+ * an estimated 5 %. */
+typedef struct gdn_prefill_plan {
+  int64_t chains;           /* num_v_heads x num_seqs                        */
+  int64_t piece_chunks;     /* chunks (64 tokens) per piece                  */
+  int64_t levels;           /* pieces per chain of max_seq_len tokens        */
+  int64_t ctas_per_launch;  /* CTAs of each launch (the last may have fewer) */
+  int64_t launches;         /* chunk-kernel launches (+1 window pass)        */
+} gdn_prefill_plan;
+
+/* The plan of one gdn_prefill_chunked call with num_seqs sequences and the
+ * call's max_seq_len (its total_tokens when max_seq_len is 0) on a GPU with
+ * num_sms SMs (<= 0: the current device's count, as the call reads it).
+ * Host-only; launches nothing.  GDN_ERR_UNSUPPORTED_SHAPE for a layer on the
+ * conv pre-pass path, GDN_ERR_INVALID_ARG for a malformed argument. */
+gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
+                                int32_t num_sms, gdn_prefill_plan* out);
 
 gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
                                const gdn_prefill_args* args, void* workspace,

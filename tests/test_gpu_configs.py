@@ -34,7 +34,9 @@ def test_prefill_27b_4x8192_bench_configuration_matches_oracle_on_sampled_heads(
     bt = [perm[s * nck:(s + 1) * nck] for s in range(N)]
     slots = perm[N * nck:]
     pool = gdn.StatePool(sh, N * (nck + 1), fill=0xFF)
-    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, [0] * N, [-1] * N, bt, slots)
+    # max_seq_len as the benchmark passes it: the same pieces and launches
+    o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, [0] * N, [-1] * N, bt, slots,
+                            max_seq_len=L)
     assert err == 0
     for h in (0, 29, 47):   # first, middle (qk head 9), last value head
         ref = oracle_head(sh, ti["x"], ti["g"], ti["beta"], w, h, cu, [0] * N, sh.block_size)

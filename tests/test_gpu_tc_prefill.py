@@ -10,7 +10,7 @@ import oracle
 import gated_deltanet_state_gb300 as gdn
 from gated_deltanet_state_gb300 import inputs
 
-from harness import assert_out_close, assert_state_close, dims, run_prefill
+from harness import assert_out_close, assert_state_close, dims, oracle_head, run_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -119,3 +119,50 @@ def test_cold_equals_resume_bitwise_at_64_multiple_blocks():
     assert torch.equal(pool.payload(4).cpu(), pool.payload(0).cpu())
     assert torch.equal(pool.payload(5).cpu(), pool.payload(2).cpu())
     assert torch.equal(pool.payload(6).cpu(), pool.payload(3).cpu())
+
+
+def test_pieces_over_several_launches_equal_one_launch_bitwise():
+    """Four sequences of the 27B-shaped layer are 192 (sequence, v head)
+    chains, more than the GPU has SMs, so the prefill cuts them into pieces run
+    over several launches (a piece starts from the state the one before it
+    left in the final slot).  One sequence alone is 48 chains, one launch.
+    Outputs, final states, checkpoints and windows must be the same bits, with
+    block boundaries at piece ends, a resumed sequence, a sequence that ends
+    inside its second piece and one shorter than a piece."""
+    sh = inputs.LayerShape(16, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
+    lens = [2048, 1800, 77, 1536]
+    start = [0, 0, 0, 1024]
+    init = [-1, -1, -1, 4]
+    bt = [[5, 6], [7, -1], [-1, -1], [-1, 8]]
+    N = len(lens)
+    plan = gdn.gdn_prefill_plan_for(sh, N, max(lens))
+    assert plan["levels"] == 2 and plan["launches"] > 1, plan
+    assert gdn.gdn_prefill_plan_for(sh, 1, max(lens))["launches"] == 1
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    ti = inputs.token_inputs(sh, int(cu[-1]), seed=61)
+    w = inputs.conv_weights(sh, 61)
+    st = inputs.random_state(sh, 1, seed=62)
+    pools = []
+    for _ in range(2):
+        pool = gdn.StatePool(sh, 9, fill=0)
+        pool.state(4).copy_(st["S"][0].cuda())
+        pool.window(4).copy_(st["win"][0].cuda())
+        pools.append(pool)
+    o_all, err, _ = run_prefill(sh, pools[0], ti["x"], ti["g"], ti["beta"], w, cu, start, init, bt,
+                                list(range(N)), max_seq_len=max(lens))
+    assert err == 0
+    for s in range(N):
+        a, b = int(cu[s]), int(cu[s + 1])
+        o_one, err, _ = run_prefill(sh, pools[1], ti["x"][a:b], ti["g"][a:b], ti["beta"][a:b], w, [0, b - a],
+                                    [start[s]], [init[s]], [bt[s]], [s], max_seq_len=b - a)
+        assert err == 0
+        assert torch.equal(o_all[a:b].view(torch.int16), o_one.view(torch.int16)), s
+    for page in [0, 1, 2, 3, 5, 6, 7, 8]:
+        assert torch.equal(pools[0].payload(page).cpu(), pools[1].payload(page).cpu()), page
+    # and against the oracle on two heads of the resumed sequence
+    a, b = int(cu[3]), int(cu[4])
+    for h in (0, 47):
+        ref = oracle_head(sh, ti["x"][a:b], ti["g"][a:b], ti["beta"][a:b], w, h, [0, b - a], [1024], 1024,
+                          st["S"].double().numpy(), st["win"].float().numpy())
+        assert_out_close(o_all[a:b, h:h + 1], ref["o"], [0, b - a])
+        assert_state_close(pools[0].state(3).cpu()[None, h:h + 1], ref["S"])

@@ -1,0 +1,93 @@
+"""The prefill's launch plan (host arithmetic, no GPU): when the (sequence,
+value head) chains outnumber the SMs, the chains are cut into pieces run level
+by level over several launches.  The CTA -> piece map of the kernel is played
+out here for many shapes and SM counts: every chain gets each of its pieces
+once, in launches that strictly increase with the piece, no launch holds two
+pieces of one chain or more CTAs than the GPU has SMs, and the pieces cover a
+chain's chunks exactly once for any length up to the bound (the last piece
+runs to the end, so even a longer sequence is covered)."""
+import itertools
+
+import pytest
+
+import gated_deltanet_state_gb300 as gdn
+from gated_deltanet_state_gb300 import inputs
+
+
+def _play(plan, N, Hv):
+    """chain -> [(launch, level)] as the kernel maps CTA (h, b) of launch t."""
+    per = plan["ctas_per_launch"] // Hv
+    pairs = plan["levels"] * N
+    runs = {}
+    for t in range(plan["launches"]):
+        base = t * per
+        s0, level0 = base % N, base // N
+        cnt = min(per, pairs - base)
+        assert cnt >= 1
+        seen = set()
+        for b in range(cnt):
+            s, level = s0 + b, level0
+            if s >= N:
+                s, level = s - N, level + 1
+            assert s not in seen, "two pieces of one chain in one launch"
+            seen.add(s)
+            for h in range(Hv):
+                runs.setdefault((s, h), []).append((t, level))
+        assert cnt * Hv <= max(plan["ctas_per_launch"], 1)
+    return runs
+
+
+def _chunks(plan, level, nch):
+    P = plan["piece_chunks"]
+    lo = level * P
+    hi = nch if level == plan["levels"] - 1 else min(nch, lo + P)
+    return range(lo, hi) if (lo < nch or level == 0) else range(0)
+
+
+SHAPES = [(48, 1), (48, 3), (48, 4), (48, 5), (48, 8), (48, 64), (32, 8), (32, 5), (6, 40), (64, 3), (2, 200)]
+LENS = [0, 64, 500, 1024, 2048, 8192, 229376]
+SMS = [152, 148, 132, 16]
+
+
+@pytest.mark.parametrize("Hv,N", SHAPES)
+def test_plan_runs_every_piece_once_in_order(Hv, N):
+    sh = inputs.LayerShape(max(1, Hv // 3) if Hv % 3 == 0 else Hv, Hv, 128, 128, block_size=896, chunk_size=64)
+    for max_len, sms in itertools.product(LENS, SMS):
+        plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms)
+        assert plan["chains"] == Hv * N
+        if plan["levels"] > 1:
+            P = plan["piece_chunks"]
+            assert P >= 4 and P & (P - 1) == 0, "pieces start at even chunks"
+            assert plan["ctas_per_launch"] <= sms and plan["ctas_per_launch"] % Hv == 0
+            assert plan["launches"] <= 64
+        else:
+            assert plan["launches"] == 1 and plan["ctas_per_launch"] == Hv * N
+        runs = _play(plan, N, Hv)
+        assert len(runs) == Hv * N
+        maxc = -(-max_len // 64)
+        for key, lst in runs.items():
+            assert [lv for _, lv in lst] == list(range(plan["levels"])), key
+            assert all(t0 < t1 for (t0, _), (t1, _) in zip(lst, lst[1:])), key
+        # coverage for lengths up to the bound, and past it
+        for nch in sorted({0, 1, maxc // 2, max(maxc - 1, 0), maxc, maxc + 3}):
+            covered = [c for lv in range(plan["levels"]) for c in _chunks(plan, lv, nch)]
+            assert covered == list(range(nch)), (max_len, sms, nch)
+
+
+def test_benchmark_shape_plan():
+    # 4 x 8,192 tokens of the 27B-shaped layer on 152 SMs: 16-chunk pieces,
+    # three (level, sequence) pairs of 48 CTAs a launch, 32 pairs in 11 launches
+    plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152)
+    assert plan == {"chains": 192, "piece_chunks": 16, "levels": 8, "ctas_per_launch": 144, "launches": 11}
+    # one long sequence (48 chains) and a large batch (3,072 chains) stay one launch
+    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152)["launches"] == 1
+    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152)["launches"] == 1
+
+
+def test_plan_rejects_the_scan_path_and_bad_arguments():
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.gdn_prefill_plan_for(inputs.TINY, 4, 1024, 152)
+    assert ei.value.status == gdn.STATUS_CODE["GDN_ERR_UNSUPPORTED_SHAPE"]
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_plan_for(inputs.QWEN27B, -1, 1024, 152)
+    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 0, 1024, 152)["launches"] == 0
