@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // always runs (it also writes the state of an empty sequence); a later one
   // starts from the state the previous piece left in the final slot, and the
   // last level runs to the sequence's end
-  const int64_t cb = (int64_t)level * pm.piece;   // even: a piece is a power of two >= 4 chunks
+  const int64_t cb = (int64_t)level * pm.piece;   // even: a piece is an even number of chunks
   if (level > 0 && cb >= nch) return;
   const int64_t ce = level == pm.last_level || cb + pm.piece > nch ? nch : cb + pm.piece;
   const int32_t from = level > 0 ? final_page : init;
@@ -896,13 +896,16 @@ int tc_prefill_sm_count() {
 // pieces of a chain are N pairs apart, so each lands in a later launch than
 // the one before it, and no launch holds two pieces of one chain.  Each
 // chunk's arithmetic is the same as in one launch, so the results are
-// bitwise the same.  A piece costs about one chunk time more (state in and
-// out, the first rows' load, the launch gap); P is the power of two >= 4 with
-// the least estimated time, kept only when it saves 5 % over one launch and
-// needs at most 64 launches.  A piece starts at an even chunk, which keeps
-// the kernel's mbarrier parities (chunk & 1) valid.
+// bitwise the same.  A launch costs about 1.5 chunk times more than its
+// pieces' chunks (state in and out, the first rows' load, the slowest CTA,
+// the launch gap: measured 21 us a launch against 13 us a chunk); P is the
+// even piece length >= 4 with the least estimated time, kept only when it
+// saves 5 % over one launch and needs at most 64 launches.  A piece starts at
+// an even chunk, which keeps the kernel's mbarrier parities (chunk & 1)
+// valid.
 PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int sms) {
-  constexpr int64_t kPieceCost = 1, kMinPiece = 4, kMaxLaunches = 64;
+  constexpr double kLaunchCost = 1.5;
+  constexpr int64_t kMinPiece = 4, kMaxLaunches = 64;
   PrefillSchedule sc;
   sc.nchains = (int64_t)Hv * num_seqs;
   const int64_t maxc = max_len > 0 ? (max_len + kPfC - 1) / kPfC : 0;
@@ -912,13 +915,13 @@ PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int s
   sc.launches = sc.nchains > 0 ? 1 : 0;
   const int64_t per = Hv > 0 && sms > 0 ? sms / Hv : 0;   // pairs a launch
   if (per < 1 || num_seqs < per || sc.nchains < sms || maxc < 2 * kMinPiece) return sc;
-  const double single = (double)((sc.nchains + sms - 1) / sms) * (double)(maxc + kPieceCost);
+  const double single = (double)((sc.nchains + sms - 1) / sms) * ((double)maxc + kLaunchCost);
   double best = 0.95 * single;
-  for (int64_t P = kMinPiece; P < maxc; P *= 2) {
+  for (int64_t P = kMinPiece; P < maxc; P += 2) {
     const int64_t levels = (maxc + P - 1) / P;
     const int64_t launches = (levels * num_seqs + per - 1) / per;
     if (launches > kMaxLaunches) continue;
-    const double cost = (double)launches * (double)(P + kPieceCost);
+    const double cost = (double)launches * ((double)P + kLaunchCost);
     if (cost < best) {
       best = cost;
       sc.piece = P;
