@@ -44,11 +44,11 @@ HBM_NOMINAL_GBS = 7900.0    # nominal HBM3e rate of the part (fractions use the 
 PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
-# DRAM bytes (read + write) of one tensor-core prefill launch, from an ncu
-# capture of the current kernel at 4 x 2,048 tokens (173.0 MB read + 93.4 MB
-# written), scaled by 4 to the 4 x 8,192 launch (the traffic is per token).
-# None once the kernel changes.
-PREFILL_TRAFFIC_PER_LAUNCH = (172.977152e6 + 93.397248e6) * 4
+# DRAM bytes (read + write) of the tensor-core prefill kernel in one 4 x 8,192
+# call (its four piece launches summed: 711.96 MB read + 363.66 MB written),
+# from an ncu capture of the current kernel on this workload.  None once the
+# kernel changes.
+PREFILL_TRAFFIC_PER_CALL = 711.96e6 + 363.66e6
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
@@ -803,8 +803,9 @@ def main():
         "decode_hbm_frac_nominal": dec_gbs / HBM_NOMINAL_GBS, "flush_hbm_frac_nominal": fl_gbs / HBM_NOMINAL_GBS,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak,
-                     "traffic": PREFILL_TRAFFIC_PER_LAUNCH if args.seq_len == SEQ_LEN else None,
-                     "traffic_note": "bytes per launch, scaled from a 4 x 2048 capture",
+                     "traffic": PREFILL_TRAFFIC_PER_CALL if args.seq_len == SEQ_LEN else None,
+                     "traffic_note": "DRAM bytes per prefill call (the kernel's piece launches summed; "
+                                     "achieved is the call's work over its time), ncu capture of this workload",
                      "kernel": "tc_prefill_kernel",
                      "work": "chunk-form flops (C 64) per token and v-head x tokens x heads; "
                              "executed as 3 bf16 passes",
