@@ -811,7 +811,7 @@ def main():
                              "executed as 3 bf16 passes",
                      "executed_tflops": achieved * EXECUTED_FLOPS_PER_TOKEN_HEAD / CHUNK_FLOPS_PER_TOKEN_HEAD,
                      "peak_kind": f"dense bf16 {peak_kind} (burst)",
-                     "algorithmic_bytes_per_launch": pre.algorithmic_bytes(),
+                     "algorithmic_bytes_per_call": pre.algorithmic_bytes(),
                      "hbm_gbs_achieved": pre.algorithmic_bytes() / (pre_ms * 1e-3) / 1e9,
                      "hbm_peak_kind": peak_kind},
         "e2e": {"value": job_throughput(pre.tokens, world, e2e_ms), "unit": "tokens/s/layer",
