@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   TokenView<TIN> V;
   int64_t start, n_log;
   int32_t init, final_page;
-  const bool report = (h == 0 && level == 0 && tid == 0);
+  // errors are recorded first-wins, so every piece of head 0 may report
+  const bool report = (h == 0 && tid == 0);
   if (!make_view<TIN, kPrefill>(p, s, V, start, init, final_page, n_log, report)) return;
   const int64_t n = V.n;
   const int64_t nch = (n + C - 1) / C;

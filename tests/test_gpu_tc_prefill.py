@@ -159,6 +159,15 @@ def test_pieces_over_several_launches_equal_one_launch_bitwise():
         assert torch.equal(o_all[a:b].view(torch.int16), o_one.view(torch.int16)), s
     for page in [0, 1, 2, 3, 5, 6, 7, 8]:
         assert torch.equal(pools[0].payload(page).cpu(), pools[1].payload(page).cpu()), page
+    # a bad page for a boundary inside a later piece (sequence 0's block 1,
+    # reached in its second piece) is reported like one in the first
+    bad = [list(r) for r in bt]
+    bad[0][1] = 99
+    pool = gdn.StatePool(sh, 9, fill=0)
+    pool.state(4).copy_(st["S"][0].cuda())
+    _, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, start, init, bad, list(range(N)),
+                            max_seq_len=max(lens))
+    assert err == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
     # and against the oracle on two heads of the resumed sequence
     a, b = int(cu[3]), int(cu[4])
     for h in (0, 47):
