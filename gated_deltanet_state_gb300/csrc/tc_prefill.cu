@@ -19,8 +19,11 @@
 // start at absolute multiples of 64, so a block boundary (a multiple of the
 // block size, itself a multiple of 64) is always a chunk end: a checkpoint is
 // the state between two chunks and a resume replays the cold run's arithmetic
-// bit for bit.  The fp32 state lives in tensor memory from the first chunk to
-// the last.  Per chunk:
+// bit for bit.  The fp32 state lives in tensor memory from the CTA's first
+// chunk to its last.  When the chains outnumber the SMs, a CTA walks one
+// piece of its chain (an even number of chunks) and the next piece runs in a
+// later launch from the state this one leaves in the final slot's page
+// (tc_prefill_schedule).  Per chunk:
 //   (A) conv + SiLU of the chunk's q, k, v channels from pre-conv rows staged
 //       in shared memory (prefetched during the previous chunk; packed fp32
 //       pairs), L2 norms; meanwhile the issuing warp forms the cumulative
