@@ -363,7 +363,10 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
                         stream=None, raise_on_error: bool = True) -> int:
     """Chunked prefill with block checkpoints (see gdn.h for the contract).
     Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
-    taken from PyTorch's allocator for the call."""
+    taken from PyTorch's allocator for the call.  `max_seq_len` (the longest
+    sequence; 0: the call's total tokens) sizes the launch plan
+    (gdn_prefill_plan_for): a batch of several sequences runs best with the
+    exact value."""
     lib = load_library()
     n = int(cu_seqlens.numel()) - 1
     if workspace is None:
