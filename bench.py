@@ -786,11 +786,14 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16x3", "data": "synthetic",
         "config": {"workload": "prefill 27B-shaped GDN layer (16 qk / 48 v heads, d 128), 4 x 8192 tokens, "
                                "block 896, checkpoints every block; + decode 4B-shaped 256 seqs x 24 layers; "
                                "+ replay 16 req x 16 rows x 24 layers",
-                   "io_dtype": "bf16 x/o, fp32 state", "parallelism": f"replicas x{world}",
+                   "io_dtype": "bf16 x/o, fp32 state",
+                   "arithmetic": "tensor-core products as three bf16 passes (hi*hi + hi*lo + lo*hi of fp32 "
+                                 "operands split into bf16 hi + lo) with fp32 accumulation; the rest fp32",
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (no flush)"},
         "prefill_ms": pre_ms, "decode_us_per_layer": 1000.0 * dec_ms / DEC_LAYERS,
         "replay_verify_us_per_layer": 1000.0 * ver_ms / REP_LAYERS,
@@ -810,6 +813,10 @@ def main():
                      "work": "chunk-form flops (C 64) per token and v-head x tokens x heads; "
                              "executed as 3 bf16 passes",
                      "executed_tflops": achieved * EXECUTED_FLOPS_PER_TOKEN_HEAD / CHUNK_FLOPS_PER_TOKEN_HEAD,
+                     "executed_frac": achieved * EXECUTED_FLOPS_PER_TOKEN_HEAD / CHUNK_FLOPS_PER_TOKEN_HEAD / tc_peak,
+                     # the algorithmic fraction with the tensor pipe busy all the time: three passes per
+                     # product over M = 128 tiles execute this many times the algorithmic flops
+                     "pass_ceiling": CHUNK_FLOPS_PER_TOKEN_HEAD / EXECUTED_FLOPS_PER_TOKEN_HEAD,
                      "peak_kind": f"dense bf16 {peak_kind} (burst)",
                      "algorithmic_bytes_per_call": pre.algorithmic_bytes(),
                      "hbm_gbs_achieved": pre.algorithmic_bytes() / (pre_ms * 1e-3) / 1e9,
@@ -838,6 +845,19 @@ def main():
     os.sched_setaffinity(0, all_cpus)          # the oracle baseline uses every host core
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    # last key: a compact summary, so that the end of the line (what a log's
+    # tail keeps of a long line) carries every headline figure
+    line["summary"] = {
+        "prefill_ms": round(pre_ms, 4), "prefill_tokens_per_s_layer": round(value),
+        "prefill_tc_frac": round(achieved / tc_peak, 4),
+        "decode_us_per_layer": round(1000.0 * dec_ms / DEC_LAYERS, 2), "decode_hbm_frac": round(dec_gbs / peaks["hbm_gbs"], 3),
+        "verify_us_per_layer": round(1000.0 * ver_ms / REP_LAYERS, 2), "verify_hbm_frac": round(ver_gbs / peaks["hbm_gbs"], 3),
+        "flush_us_per_layer": round(1000.0 * fl_ms / REP_LAYERS, 2), "flush_hbm_frac": round(fl_gbs / peaks["hbm_gbs"], 3),
+        "e2e_tokens_per_s_layer": round(line["e2e"]["value"]),
+    }
+    lc = line.get("long_context")
+    if isinstance(lc, dict):
+        line["summary"]["long_context"] = {k: lc[k] for k in lc if k.endswith("_ms")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:

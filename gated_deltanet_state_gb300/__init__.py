@@ -84,7 +84,7 @@ class _PrefillArgs(ctypes.Structure):
                 ("cu_seqlens", _P), ("start_pos", _P),
                 ("start_pos_host", _P), ("init_page_host", _P), ("x", _P), ("g", _P),
                 ("beta", _P), ("conv_w", _P), ("init_page", _P), ("block_table", _P),
-                ("out_slot", _P), ("o", _P), ("dev_error", _P)]
+                ("out_slot", _P), ("o", _P), ("dev_error", _P), ("wait_cycles", ctypes.c_int64)]
 
 
 class _DecodeArgs(ctypes.Structure):
@@ -340,7 +340,7 @@ def workspace_for(nbytes: int, device="cuda") -> torch.Tensor:
 # --------------------------------------------------------------------------- device entry points
 
 def _prefill_args(shape, *, cu_seqlens, start_pos, init_page, block_table, out_slot, x, g, beta, conv_w,
-                  o, dev_error, start_pos_host, init_page_host, max_seq_len):
+                  o, dev_error, start_pos_host, init_page_host, max_seq_len, wait_cycles=0):
     n = int(cu_seqlens.numel()) - 1
     sph, keep1 = _host(start_pos_host, torch.int64, "start_pos_host")
     iph, keep2 = _host(init_page_host, torch.int32, "init_page_host")
@@ -353,20 +353,20 @@ def _prefill_args(shape, *, cu_seqlens, start_pos, init_page, block_table, out_s
                      _dev(init_page, torch.int32, "init_page"),
                      _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
                      _dev(out_slot, torch.int32, "out_slot"), _dev(o, shape.torch_out(), "o"),
-                     _dev(dev_error, torch.int32, "dev_error"))
+                     _dev(dev_error, torch.int32, "dev_error"), int(wait_cycles))
     return a, (keep1, keep2)
 
 
 def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
                         block_table, out_slot, x, g, beta, conv_w, o, dev_error,
                         start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
-                        stream=None, raise_on_error: bool = True) -> int:
+                        wait_cycles: int = 0, stream=None, raise_on_error: bool = True) -> int:
     """Chunked prefill with block checkpoints (see gdn.h for the contract).
     Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
     taken from PyTorch's allocator for the call.  `max_seq_len` (the longest
     sequence; 0: the call's total tokens) sizes the launch plan
     (gdn_prefill_plan_for): a batch of several sequences runs best with the
-    exact value."""
+    exact value.  `wait_cycles` bounds the device-side waits (gdn.h)."""
     lib = load_library()
     n = int(cu_seqlens.numel()) - 1
     if workspace is None:
@@ -374,7 +374,7 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
     a, keep = _prefill_args(shape, cu_seqlens=cu_seqlens, start_pos=start_pos, init_page=init_page,
                             block_table=block_table, out_slot=out_slot, x=x, g=g, beta=beta, conv_w=conv_w,
                             o=o, dev_error=dev_error, start_pos_host=start_pos_host,
-                            init_page_host=init_page_host, max_seq_len=max_seq_len)
+                            init_page_host=init_page_host, max_seq_len=max_seq_len, wait_cycles=wait_cycles)
     ws = _dev(workspace, None, "workspace")
     wsb = workspace.numel() * workspace.element_size()
     st = lib.gdn_prefill_chunked(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),

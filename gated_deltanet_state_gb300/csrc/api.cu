@@ -158,6 +158,7 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
   p.g = a->g;
   p.beta = a->beta;
   p.total_rows = a->total_tokens;
+  p.wait_cycles = a->wait_cycles;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (core) {
     // packed rows q | k | v | z; the gates of every row into the workspace first

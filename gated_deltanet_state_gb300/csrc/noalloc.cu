@@ -12,8 +12,9 @@
 // GDN_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds it until
 // the process exits.  Host code may not use the array's name as a device
 // address (on the host it names a host-side stand-in), so the first call on
-// each device looks the device address up with cudaGetSymbolAddress while that
-// device is current, and later calls reuse it.
+// each device that needs the scratch looks the device address up with
+// cudaGetSymbolAddress while that device is current, and later calls reuse
+// it; calls whose layer needs no scratch skip the array and the look-up.
 #include <mutex>
 
 #include "launch.h"
@@ -47,10 +48,12 @@ gdn_status scratch_address(void** out) {
 extern "C" gdn_status gdn_prefill_chunked_noalloc(const gdn_layer_desc* desc, const gdn_pool* pool,
                                                   const gdn_prefill_args* args, void* stream) {
   if (!desc || !args) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_prefill_workspace_size(desc, args->num_seqs, args->total_tokens);
+  // a layer that needs no scratch never touches the array (no set-up either)
+  if (need == 0) return gdn_prefill_chunked(desc, pool, args, nullptr, 0, stream);
   // Every workspace element the kernels read is written earlier in the same
   // call, so the scratch needs no clearing between calls.
-  if (gdn_prefill_workspace_size(desc, args->num_seqs, args->total_tokens) > GDN_NOALLOC_SCRATCH_BYTES)
-    return GDN_ERR_WORKSPACE;
+  if (need > GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
   void* scratch = nullptr;
   const gdn_status st = scratch_address(&scratch);
   if (st != GDN_OK) return st;

@@ -65,6 +65,8 @@ struct ScanParams {
   int32_t x_ld;         // elements from one x row to the next (conv_dim; packed q|k|v|z rows: more)
   const float* norm_w;  // packed core: gated-norm scale [dv] (nullptr: plain outputs)
   float norm_eps2;      // packed core: gated-norm epsilon
+  long long wait_cycles;   // bound of a tensor-core kernel's waits in SM clocks (0: the default;
+                           // < 0: every wait reports a timeout at once)
   // replay
   const int32_t* ckpt_slot;
   const void* log_x;
@@ -582,6 +584,8 @@ __global__ void __launch_bounds__(256) window_kernel(const ScanParams p) {
   int64_t start, n_log;
   int32_t init, final_page;
   if (!make_view<TIN, MODE>(p, s, V, start, init, final_page, n_log, false)) return;
+  // a prefill whose device wait ran out wrote no states: no windows either
+  if (MODE == kPrefill && *reinterpret_cast<volatile const int32_t*>(p.err) == GDN_ERR_TIMEOUT) return;
   const int64_t n = V.n;
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < p.conv_dim; c += gridDim.x * blockDim.x) {
     if (MODE == kPrefill) {

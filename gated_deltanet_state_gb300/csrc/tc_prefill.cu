@@ -41,8 +41,10 @@
 // Every product reads bf16 operands split into hi + lo parts and runs three
 // passes (hi*hi + hi*lo + lo*hi) into fp32 accumulators: each operand keeps
 // ~16 significant bits, so the chunk stays within ~1e-5 of an fp32 evaluation.
-// Every mbarrier wait is bounded; a wait that runs out sets GDN_ERR_TIMEOUT,
-// lets the tensor core drain (bounded again) and releases tensor memory.
+// Every mbarrier wait is bounded; a wait that runs out sets GDN_ERR_TIMEOUT
+// (over any earlier code), lets the tensor core and the copy engine drain
+// (bounded again, by the default limit) and releases tensor memory; later
+// pieces of the call and the window pass then write nothing.
 #include "launch.h"
 #include "tc.cuh"
 
@@ -141,6 +143,18 @@ __device__ __forceinline__ void named_arrive(int id, int count) {
 
 // Barrier of the sixteen worker warps alone (threads 0..511).
 __device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 2, 512;\n" ::: "memory"); }
+
+// The same barrier, returning whether `v` holds on every worker.
+__device__ __forceinline__ bool workers_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, 512, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 // Barrier of the threads that build T (256..511).
 __device__ __forceinline__ void tgrp_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
@@ -271,10 +285,17 @@ __device__ void tri_inverse64(const float* at, const float* am, float* tf, float
   tgrp_sync();
 }
 
+// A bounded wait of the chunk loop: at most `lim` SM clocks, or (lim < 0)
+// none at all, reporting a timeout at once (how the run-out path is tested).
+// The drain after a run-out always takes the default bound.
+__device__ __forceinline__ bool work_wait(uint64_t* m, uint32_t parity, long long lim) {
+  return lim >= 0 && tc::mbar_wait_bounded(m, parity, lim);
+}
+
 // A worker's bounded wait for a tensor-core product; a wait that runs out
 // clears `ok`, which the next whole-CTA barrier turns into a common exit.
-__device__ __forceinline__ void mma_wait(uint64_t* m, uint32_t parity, bool& ok) {
-  ok = tc::mbar_wait_bounded(m, parity, kPfWait) && ok;
+__device__ __forceinline__ void mma_wait(uint64_t* m, uint32_t parity, bool& ok, long long lim) {
+  ok = work_wait(m, parity, lim) && ok;
   tc::fence_after_sync();
 }
 
@@ -323,6 +344,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (level > 0 && cb >= nch) return;
   const int64_t ce = level == pm.last_level || cb + pm.piece > nch ? nch : cb + pm.piece;
   const int32_t from = level > 0 ? final_page : init;
+  // a later piece continues from the state the chain's previous piece left in
+  // the final slot; if a wait of an earlier launch of this call ran out, that
+  // state may be stale, so no later piece runs (the error word says so)
+  if (level > 0 &&
+      __syncthreads_or(tid == 0 && *reinterpret_cast<volatile const int32_t*>(p.err) == GDN_ERR_TIMEOUT))
+    return;
+  const long long wlim = p.wait_cycles > 0 ? p.wait_cycles : p.wait_cycles < 0 ? -1 : kPfWait;
   const int grp = p.Hv / p.Hqk, jq = h / grp;
   const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D, cv0 = 2 * p.Hqk * D + h * D;
   const int64_t row0 = p.cu_seqlens[s];      // first row of this sequence in x, g, beta, o
@@ -443,8 +471,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // ---- the chunk's rows and gates have landed; the previous output tile
       // has been read out
       if (tid == 0) tc::bulk_wait_read();
-      ok = tc::mbar_wait_bounded(mbar + 4, par, kPfWait) && ok;
-      workers_sync();
+      // the workers agree on the outcome: rows still landing are never
+      // staged over (a run-out skips the next chunk's rows and leaves at the
+      // next whole-CTA barrier)
+      ok = workers_sync_and(work_wait(mbar + 4, par, wlim) && ok);
       if (ok) x_issued = -1;
       if (c == 0) {
         // history rows of the first chunk: the resumed window, or zeros
@@ -512,7 +542,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc::tmem_st_wait();
       workers_sync();
       // the staged rows are consumed: prefetch the next chunk
-      if (c + 1 < ce) {
+      if (ok && c + 1 < ce) {
         stage(c + 1);
         x_issued = c + 1;
       }
@@ -568,7 +598,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // k channel); each thread loads all of its inputs before it stores.
       // The previous chunk's state update reads U^T and K^T diag(dec): it
       // has finished first.
-      if (s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok);
+      if (s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok, wlim);
       {
         constexpr int NKQ = 2048 / kPfWorkers, NKT = 1024 / kPfWorkers;
         float4 ya[NKQ], yb[NKQ];
@@ -670,7 +700,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---- (C) A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j) for
     // columns j in [16 quarter, +16), computed while S0 [K^; Q^]^T runs
     if (worker) {
-      mma_wait(mbar + 0, par, ok);
+      mma_wait(mbar + 0, par, ok, wlim);
       const int q4 = warp & 3;
       const int ir = (q4 & 1) * 32 + lane;   // chunk row i of this thread's lane
       float ap[16];
@@ -688,7 +718,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
         }
       }
-      mma_wait(mbar + 1, par, ok);
+      mma_wait(mbar + 1, par, ok, wlim);
       workers_sync();   // every worker is past the S0 [K^; Q^]^T wait: [K^; Q^] is free
       if (q4 < 2) {
         float* am = reinterpret_cast<float*>(sm + PfSmem::AM);
@@ -752,7 +782,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     issued |= 4u;
     // U^T (rows r, K = i) as the A operand of the state update and the outputs
     if (worker) {
-      mma_wait(mbar + 2, par, ok);
+      mma_wait(mbar + 2, par, ok, wlim);
       float u[16];
       tc::tmem_ld16(tbase + tlane + kColU + 16 * quarter, u);
 #pragma unroll
@@ -779,7 +809,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     issued |= 8u | 32u;
     s_pending = true;
     if (worker) {
-      mma_wait(mbar + 3, par, ok);
+      mma_wait(mbar + 3, par, ok, wlim);
       // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in [16 quarter, +16):
       // a full chunk goes out as one TMA tile through shared memory, a
       // partial one (the sequence's last) by plain stores
@@ -846,7 +876,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 
-  if (ok && worker && s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok);
+  if (ok && worker && s_pending) mma_wait(mbar + 5, (uint32_t)((c - 1) & 1), ok, wlim);
   ok = cta_sync_ok(ok);
   if (ok) {
     if (worker) {
@@ -866,7 +896,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // a wait ran out: report it, give the tensor core and the copy engine one
     // more bounded wait for each piece of work they may still hold, then
     // release the tensor memory
-    if (tid == 0) set_error(p.err, GDN_ERR_TIMEOUT);
+    if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);   // overrides an earlier code
     const uint32_t par = (uint32_t)(ci & 1);
 #pragma unroll 1
     for (int b = 0; b < 4; ++b)

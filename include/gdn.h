@@ -43,8 +43,12 @@
  * -------------------------------
  * The caller owns every buffer (pool, inputs, outputs, metadata, error word)
  * and every stream.  The library allocates no device or host memory and keeps
- * no global state; all entry points are asynchronous and stream-ordered, and
- * may be called from several host threads on different streams.
+ * no global state, with one exception: gdn_prefill_chunked_noalloc's scratch,
+ * a fixed device array of GDN_NOALLOC_SCRATCH_BYTES in the library's own
+ * image (and the device addresses of it the library caches), held by every
+ * GPU that loads the library.  All entry points are asynchronous and
+ * stream-ordered, and may be called from several host threads on different
+ * streams.
  * Host-detectable errors (bad shapes, null pointers, an off-boundary resume
  * visible in a host-side array) are returned before anything is launched.
  * Errors that only the device can see (a page id outside the pool, a log
@@ -244,6 +248,14 @@ typedef struct gdn_prefill_args {
   const int32_t* out_slot;       /* [N] page receiving the final state        */
   void* o;                       /* [T][Hv][dv] out_dtype                     */
   int32_t* dev_error;            /* one int32, set to a gdn_status on a fault */
+  int64_t wait_cycles;           /* bound of each device-side wait of the
+                                    tensor-core prefill in SM clocks; 0: the
+                                    default (~2 s).  A wait that runs out sets
+                                    GDN_ERR_TIMEOUT (over any earlier code);
+                                    the call then writes no further states,
+                                    checkpoints or windows.  < 0 makes every
+                                    such wait report a timeout at once (a test
+                                    of that path: nothing is written)         */
 } gdn_prefill_args;
 
 /* Device workspace bytes gdn_prefill_chunked needs for a call with
@@ -305,9 +317,11 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
  * prefills at block boundaries, gdn_chunk_end).  Layers on the tensor-core
  * path need no scratch and have no limit.
  * The entry point calls no cudaMalloc, cudaFree or other allocating routine.
- * The first call on each device looks up the array's device address with
- * cudaGetSymbolAddress (that device current); make that first call before
- * any stream capture.  Every call shares the one array and it keeps the last
+ * A call whose layer needs no scratch (gdn_prefill_workspace_size 0) goes
+ * straight to gdn_prefill_chunked and never touches the array.  The first
+ * call on a device that does need it looks up the array's device address
+ * with cudaGetSymbolAddress (that device current); make that first call
+ * before any stream capture.  Every call shares the one array and it keeps the last
  * call's contents (the kernels write every element they read, so nothing is
  * cleared): calls that overlap on the GPU, on any streams, race. */
 #define GDN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

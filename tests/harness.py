@@ -2,22 +2,27 @@
 the oracle on the same inputs, compare with the stated tolerances.
 
 Tolerances against the fp64 oracle:
-  * outputs: relative Frobenius error <= 2e-3 over each sequence's whole
-    output tensor [tokens, heads, dv].  Outputs are stored in the output dtype;
-    bf16 rounding alone costs ~1.7e-3 relative (rms), so a norm over a single
-    64-element row would fail even for an exact engine.  In addition the
-    error beyond the output format must stay <= 1e-3: per element, the part
-    of |o - oracle| that exceeds one unit in the last place of the output
-    dtype at the oracle's value (an engine value within an ulp of the oracle
-    is a correct rounding of a value within rounding distance of it), as a
-    relative Frobenius norm.  This bounds the kernel's own error apart from
-    the format, also for outputs of a few hundred elements, where a single
-    correctly rounded neighbour would otherwise weigh ~1e-3.
+  * outputs: relative Frobenius error <= 2e-3 per (sequence, value head),
+    over that head's [tokens, dv] block, wherever the block holds at least
+    1,024 elements.  A shorter block (a one-token decode: 128 elements) is
+    too small for the bound: bf16 rounding alone costs ~1.7e-3 relative (rms)
+    with a spread that grows as the block shrinks, so there the norm runs over
+    the sequence's whole [tokens, heads, dv] output instead.  In addition the
+    error beyond the output format must stay <= 1e-3 over the same blocks: per
+    element, the part of |o - oracle| that exceeds half a unit in the last
+    place of the output dtype at the oracle's value (a correctly rounded
+    fp64 value is within half an ulp of it, so only the kernel's own error
+    shows), as a relative Frobenius norm.
   * states: relative Frobenius error <= 1e-4 per (sequence, value head) over
     the dv x dk matrix (fp32 storage, no format loss).
   * conv windows, page indexing and checkpoint placement: exact.
+
+Every check records its worst value; the session prints the worst margin of
+each test at its end (tests/conftest.py).
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -29,6 +34,15 @@ from gated_deltanet_state_gb300 import inputs
 OUT_TOL = 2e-3
 OUT_FORMAT_TOL = 1e-3
 STATE_TOL = 1e-4
+HEAD_BLOCK_MIN = 1024     # elements of a (sequence, head) block checked on its own
+
+# (test id, quantity, worst value, tolerance) of every check in this process
+MARGINS: list[tuple[str, str, float, float]] = []
+
+
+def _record(kind: str, worst: float, tol: float) -> None:
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append((test, kind, float(worst), float(tol)))
 
 
 def dims(shape) -> oracle.Dims:
@@ -58,28 +72,43 @@ def ulp_of(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return np.where(a > 0, np.exp2(e - mant), 0.0)
 
 
-def out_errors(o_gpu, o_ref, cu):
-    """Worst per-sequence (plain, format-aware) relative Frobenius errors of
-    outputs laid out [T, ...] with sequences delimited by cu."""
+def out_errors(o_gpu, o_ref, cu, head_block_min=HEAD_BLOCK_MIN):
+    """Worst (plain, format-aware) relative Frobenius errors of outputs laid
+    out [rows, ..., heads, dv], sequences delimited along the rows by cu.
+
+    A sequence's outputs are compared head by head when a head's block
+    ([rows, ..., dv] of that head) holds at least `head_block_min` elements,
+    else as one block over all its heads."""
     dt = o_gpu.dtype if hasattr(o_gpu, "dtype") and isinstance(o_gpu.dtype, torch.dtype) else torch.float32
     o = o_gpu.double().cpu().numpy() if hasattr(o_gpu, "cpu") else np.asarray(o_gpu, np.float64)
-    o_ref = np.asarray(o_ref, np.float64)
-    beyond = np.maximum(np.abs(o - o_ref) - ulp_of(o_ref, dt), 0.0)
+    o_ref = np.asarray(o_ref, np.float64).reshape(o.shape)
+    beyond = np.maximum(np.abs(o - o_ref) - 0.5 * ulp_of(o_ref, dt), 0.0)
+    H, D = o.shape[-2], o.shape[-1]
     plain = fmt = 0.0
     for s in range(len(cu) - 1):
         a, b = int(cu[s]), int(cu[s + 1])
         if b == a:
             continue
-        den = max(np.linalg.norm(o_ref[a:b]), 1e-30)
-        plain = max(plain, float(np.linalg.norm(o[a:b] - o_ref[a:b]) / den))
-        fmt = max(fmt, float(np.linalg.norm(beyond[a:b]) / den))
+        ref = o_ref[a:b].reshape(-1, H, D)
+        diff = (o[a:b] - o_ref[a:b]).reshape(-1, H, D)
+        bey = beyond[a:b].reshape(-1, H, D)
+        if ref.shape[0] * D >= head_block_min:
+            den = np.maximum(np.sqrt((ref ** 2).sum(axis=(0, 2))), 1e-30)
+            plain = max(plain, float(np.max(np.sqrt((diff ** 2).sum(axis=(0, 2))) / den)))
+            fmt = max(fmt, float(np.max(np.sqrt((bey ** 2).sum(axis=(0, 2))) / den)))
+        else:
+            den = max(float(np.linalg.norm(ref)), 1e-30)
+            plain = max(plain, float(np.linalg.norm(diff)) / den)
+            fmt = max(fmt, float(np.linalg.norm(bey)) / den)
     return plain, fmt
 
 
 def assert_out_close(o_gpu, o_ref, cu, tol=OUT_TOL, fmt_tol=OUT_FORMAT_TOL):
     plain, fmt = out_errors(o_gpu, o_ref, cu)
+    _record("out", plain, tol)
+    _record("out_beyond_half_ulp", fmt, fmt_tol)
     assert plain <= tol, f"output rel. Frobenius error {plain:.3e} > {tol:.1e}"
-    assert fmt <= fmt_tol, f"output error beyond the output format {fmt:.3e} > {fmt_tol:.1e}"
+    assert fmt <= fmt_tol, f"output error beyond half an ulp of the output format {fmt:.3e} > {fmt_tol:.1e}"
     return plain
 
 
@@ -88,6 +117,7 @@ def assert_state_close(S_gpu, S_ref, tol=STATE_TOL):
     S_gpu = S_gpu.float().cpu().numpy() if hasattr(S_gpu, "cpu") else S_gpu
     e = rel_fro(S_gpu, S_ref, axis=(-2, -1))
     worst = float(np.max(e)) if e.size else 0.0
+    _record("state", worst, tol)
     assert worst <= tol, f"state rel. Frobenius error {worst:.3e} > {tol:.1e}"
     return worst
 

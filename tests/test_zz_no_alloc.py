@@ -16,7 +16,7 @@ import torch
 import gated_deltanet_state_gb300 as gdn
 from gated_deltanet_state_gb300 import inputs
 
-from harness import assert_out_close, assert_state_close, dev
+from harness import dev
 
 pytestmark = pytest.mark.gpu
 
@@ -53,13 +53,12 @@ def _run(fn, shape, lens, seed, **extra):
 @pytest.mark.parametrize("shape", [SHAPE, SHAPE_SCAN], ids=["tensor_core_path", "pre_pass_path"])
 def test_noalloc_prefill_matches_the_workspace_prefill_on_two_calls_in_a_row(shape):
     assert gdn.gdn_prefill_workspace_size(shape, len(LENS), sum(LENS)) <= gdn.NOALLOC_SCRATCH_BYTES
-    cu = np.concatenate([[0], np.cumsum(LENS)])
     for seed in (41, 42):   # the second call reuses the scratch the first one left
         o_ref, s_ref = _run(gdn.gdn_prefill_chunked, shape, LENS, seed)
         o_na, s_na = _run(gdn.gdn_prefill_chunked_noalloc, shape, LENS, seed)
-        assert_out_close(o_na, o_ref.double().numpy(), cu)
-        used = [0, 1] + [p for p in range(2, s_ref.shape[0]) if s_ref[p].abs().sum() > 0]
-        assert_state_close(s_na[used], s_ref[used].double().numpy())
+        # the same kernels on the same inputs: the same bits
+        assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(s_na.view(torch.int32), s_ref.view(torch.int32))
 
 
 def test_noalloc_prefill_has_no_limit_on_the_tensor_core_path():
