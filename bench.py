@@ -828,10 +828,11 @@ def main():
                          "timed from the first input copy to the last output copy of `steps` steps",
                 "link_note": "the host link of these boxes moves ~210 GB/s in and ~193 GB/s out (~295 GB/s "
                              "both ways, the same for SM-driven copies), so ~3.9 ms of a step is copies"},
-        # per step: prefill (the chunk kernel's launches, as the library plans
-        # them on this GPU, + the window pass); decode 1 per layer; replay per
-        # layer: append 2 (tensor-core append, log_len), rollback 1, flush 2
-        "gpu_launches": args.steps * (pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
+        # per step: prefill (the chunk kernel, the chain kernel's launches as
+        # the library plans them on this GPU, the window pass); decode 1 per
+        # layer; replay per layer: append 2 (tensor-core append, log_len),
+        # rollback 1, flush 2
+        "gpu_launches": args.steps * (1 + pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
         "prefill_chunk_launches": pre_launches,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }

@@ -155,7 +155,7 @@ def load_library(build_if_missing: bool = True):
         "gdn_spec_copy_bytes": ([i32, i32, i64], i64),
         "gdn_replay_bytes_per_request": ([i32, i64, i32, i64], i64),
         "gdn_prefill_workspace_size": ([D, i32, i64], sz),
-        "gdn_prefill_plan_for": ([D, i32, i64, i32, ctypes.POINTER(_PrefillPlan)], i32),
+        "gdn_prefill_plan_for": ([D, i32, i64, i32, i32, ctypes.POINTER(_PrefillPlan)], i32),
         "gdn_replay_workspace_size": ([D, i32], sz),
         "gdn_prefill_chunked": ([D, PL, ctypes.POINTER(_PrefillArgs), _P, sz, _P], i32),
         "gdn_prefill_chunked_noalloc": ([D, PL, ctypes.POINTER(_PrefillArgs), _P], i32),
@@ -319,12 +319,13 @@ def gdn_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: i
     return int(load_library().gdn_prefill_workspace_size(ctypes.byref(make_desc(shape)), num_seqs, total_tokens))
 
 
-def gdn_prefill_plan_for(shape: LayerShape, num_seqs: int, max_seq_len: int, num_sms: int = 0) -> dict:
-    """The chunk-kernel plan of one prefill call (num_sms <= 0: the current
-    device's SM count)."""
+def gdn_prefill_plan_for(shape: LayerShape, num_seqs: int, max_seq_len: int, num_sms: int = 0,
+                         fused: bool = False) -> dict:
+    """The chain plan of one prefill call (num_sms <= 0: the current device's
+    SM count; fused: the fused kernel of a call without a workspace)."""
     out = _PrefillPlan()
     _check(load_library().gdn_prefill_plan_for(ctypes.byref(make_desc(shape)), num_seqs, max_seq_len, num_sms,
-                                               ctypes.byref(out)), "gdn_prefill_plan_for")
+                                               int(bool(fused)), ctypes.byref(out)), "gdn_prefill_plan_for")
     return {f: int(getattr(out, f)) for f, _ in _PrefillPlan._fields_}
 
 
@@ -363,8 +364,9 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
                         wait_cycles: int = 0, stream=None, raise_on_error: bool = True) -> int:
     """Chunked prefill with block checkpoints (see gdn.h for the contract).
     Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
-    taken from PyTorch's allocator for the call.  `max_seq_len` (the longest
-    sequence; 0: the call's total tokens) sizes the launch plan
+    taken from PyTorch's allocator for the call; `workspace=False` passes none
+    (a tensor-core layer then takes the fused kernel).  `max_seq_len` (the
+    longest sequence; 0: the call's total tokens) sizes the launch plan
     (gdn_prefill_plan_for): a batch of several sequences runs best with the
     exact value.  `wait_cycles` bounds the device-side waits (gdn.h)."""
     lib = load_library()
@@ -375,8 +377,11 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
                             block_table=block_table, out_slot=out_slot, x=x, g=g, beta=beta, conv_w=conv_w,
                             o=o, dev_error=dev_error, start_pos_host=start_pos_host,
                             init_page_host=init_page_host, max_seq_len=max_seq_len, wait_cycles=wait_cycles)
-    ws = _dev(workspace, None, "workspace")
-    wsb = workspace.numel() * workspace.element_size()
+    if workspace is False:
+        ws, wsb = None, 0
+    else:
+        ws = _dev(workspace, None, "workspace")
+        wsb = workspace.numel() * workspace.element_size()
     st = lib.gdn_prefill_chunked(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()),
                                  ctypes.byref(a), ws, wsb, _stream(stream))
     return _check(st, "gdn_prefill_chunked") if raise_on_error else st

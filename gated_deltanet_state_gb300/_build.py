@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libgdn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]
-CU_SOURCES = ["api.cu", "prefill.cu", "replay.cu", "decode.cu", "checkpoint.cu", "noalloc.cu", "tc_replay.cu", "tc_prefill.cu"]
+CU_SOURCES = ["api.cu", "prefill.cu", "replay.cu", "decode.cu", "checkpoint.cu", "noalloc.cu", "tc_replay.cu", "tc_prefill.cu", "tc_chain.cu"]
 C_SOURCES = ["gdn_host.c"]
 
 

@@ -70,25 +70,27 @@ extern "C" {
 
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens) {
-  (void)num_seqs;
   if (gdn_conv_dim(desc) <= 0 || total_tokens < 0) return 0;
-  // the tensor-core prefill computes the conv in the kernel: no scratch
+  // the tensor-core shapes: the chunk kernel's operand images for the chain
+  // kernel (without a workspace they take the fused kernel, which needs none)
   if (tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                            desc->block_size))
-    return 0;
+    return tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, num_seqs < 0 ? 0 : num_seqs,
+                                    total_tokens);
   return scan_workspace_bytes(total_tokens, (int)gdn_conv_dim(desc), desc->num_qk_heads,
                               desc->num_v_heads);
 }
 
 gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
-                                int32_t num_sms, gdn_prefill_plan* out) {
+                                int32_t num_sms, int32_t fused, gdn_prefill_plan* out) {
   if (!desc || !out || gdn_conv_dim(desc) <= 0 || num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0)
     return GDN_ERR_INVALID_ARG;
   if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                             desc->block_size))
     return GDN_ERR_UNSUPPORTED_SHAPE;
-  const PrefillSchedule sc = tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len,
-                                                 num_sms > 0 ? num_sms : tc_prefill_sm_count());
+  const int sms = num_sms > 0 ? num_sms : tc_prefill_sm_count();
+  const PrefillSchedule sc = fused ? tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms)
+                                   : tc_chain_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms);
   out->chains = sc.nchains;
   out->piece_chunks = sc.piece;
   out->levels = sc.levels;
@@ -142,7 +144,13 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
   if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
   const size_t need = core ? gdn_core_prefill_workspace_size(desc, a->num_seqs, a->total_tokens)
                            : gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return GDN_ERR_WORKSPACE;
+  const bool tc = tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                                       desc->block_size);
+  // a tensor-core layer without a workspace takes the fused kernel
+  const bool two_kernels = tc && !core && !(workspace == nullptr && workspace_bytes == 0);
+  if (need > 0 && (tc && !core ? two_kernels : true) &&
+      (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
   p.num_seqs = a->num_seqs;
   p.conv_w = a->conv_w;
@@ -172,12 +180,12 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
     st = cuda_status(launch_core_gates(core->ba, desc->in_dtype, core->A_log, core->dt_bias, desc->num_v_heads,
                                        a->total_tokens, gw, bw, cs));
     if (st != GDN_OK) return st;
-  } else if (need > 0) {
+  } else if (need > 0 && !tc) {
     bind_workspace(p, workspace, a->total_tokens);
   }
   const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
-  return cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
-                                    desc->out_dtype, cs));
+  return cuda_status(launch_prefill(p, two_kernels ? workspace : nullptr, max_len, desc->head_dim_k,
+                                    desc->head_dim_v, desc->in_dtype, desc->out_dtype, cs));
 }
 
 }  // namespace
@@ -305,7 +313,12 @@ gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, cons
   }
   if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_mixed_workspace_size(desc, a->num_seqs, a->total_tokens);
-  if (n_dec < a->num_seqs && need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+  const bool tc = tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                                       desc->block_size);
+  // as gdn_prefill_chunked: a tensor-core layer without a workspace takes the fused kernel
+  const bool two_kernels = tc && !(workspace == nullptr && workspace_bytes == 0);
+  if (n_dec < a->num_seqs && need > 0 && (!tc || two_kernels) &&
+      (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   // the prefill sequences (the decode ones are skipped by every prefill kernel)
@@ -326,10 +339,10 @@ gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, cons
     p.beta = a->beta;
     p.total_rows = a->total_tokens;
     p.skip = a->is_decode;
-    if (need > 0) bind_workspace(p, workspace, a->total_tokens);
+    if (need > 0 && !tc) bind_workspace(p, workspace, a->total_tokens);
     const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
-    st = cuda_status(launch_prefill(p, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
-                                    desc->out_dtype, cs));
+    st = cuda_status(launch_prefill(p, two_kernels ? workspace : nullptr, max_len, desc->head_dim_k,
+                                    desc->head_dim_v, desc->in_dtype, desc->out_dtype, cs));
     if (st != GDN_OK) return st;
   }
   // the decode tokens (gdn_decode_mixed): row cu_seqlens[s] of the packed tensors

@@ -48,7 +48,9 @@ size_t scan_workspace_bytes(int64_t rows, int conv_dim, int Hqk, int Hv);
 // p.ws_* must be bound (bind_workspace) before the launchers run.
 void bind_workspace(ScanParams& p, void* ws, int64_t rows);
 
-cudaError_t launch_prefill(const ScanParams& p, int64_t max_len, int dk, int dv, int in_dtype,
+// workspace: the tensor-core shapes take the two-kernel prefill when it is
+// given (nullptr: the fused kernel); the scan path reads p.ws_* (bound).
+cudaError_t launch_prefill(const ScanParams& p, void* workspace, int64_t max_len, int dk, int dv, int in_dtype,
                            int out_dtype, cudaStream_t st);
 cudaError_t launch_replay_append(const ScanParams& p, int dk, int dv, int in_dtype,
                                  int out_dtype, cudaStream_t st);
@@ -83,8 +85,17 @@ struct PrefillSchedule {
   int64_t launches;   // chunk-kernel launches
 };
 PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
+// The same plan with a launch's fixed cost given in chunk times.
+PrefillSchedule tc_prefill_schedule_cost(int Hv, int num_seqs, int64_t max_len, int sms, double launch_cost);
 int tc_prefill_sm_count();   // SMs of the current device (0 if unknown: one launch)
 bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size);
 cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t st);
+// The same prefill as two kernels (tc_chain.cu): the state-independent chunk
+// kernel over every chunk of the call, writing operand images to the
+// workspace, then the chain kernel (in pieces, as tc_chain_schedule plans),
+// then the window pass.  The workspace holds tc_chain_workspace_bytes.
+size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens);
+PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
+cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st);
 
 }  // namespace gdn

@@ -48,8 +48,12 @@ gdn_status scratch_address(void** out) {
 extern "C" gdn_status gdn_prefill_chunked_noalloc(const gdn_layer_desc* desc, const gdn_pool* pool,
                                                   const gdn_prefill_args* args, void* stream) {
   if (!desc || !args) return GDN_ERR_INVALID_ARG;
+  // a tensor-core layer takes the fused kernel, which needs no scratch: it
+  // never touches the array (no set-up either)
+  if (gdn::tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                                desc->block_size))
+    return gdn_prefill_chunked(desc, pool, args, nullptr, 0, stream);
   const size_t need = gdn_prefill_workspace_size(desc, args->num_seqs, args->total_tokens);
-  // a layer that needs no scratch never touches the array (no set-up either)
   if (need == 0) return gdn_prefill_chunked(desc, pool, args, nullptr, 0, stream);
   // Every workspace element the kernels read is written earlier in the same
   // call, so the scratch needs no clearing between calls.

@@ -1,5 +1,6 @@
-// prefill.cu — launcher of the prefill: the tensor-core chunk kernel where the
-// shape allows it, else the scan; then the window pass.
+// prefill.cu — launcher of the prefill: on the tensor cores where the shape
+// allows it (the chunk + chain kernels with a workspace, the fused kernel
+// without), else the scan; then the window pass.
 #include "scan_launch.cuh"
 
 namespace gdn {
@@ -10,9 +11,10 @@ size_t scan_workspace_bytes(int64_t rows, int conv_dim, int Hqk, int Hv) {
 
 void bind_workspace(ScanParams& p, void* ws, int64_t rows) { ws_bind(p, ws, rows); }
 
-cudaError_t launch_prefill(const ScanParams& p, int64_t max_len, int dk, int dv, int in_dtype,
+cudaError_t launch_prefill(const ScanParams& p, void* workspace, int64_t max_len, int dk, int dv, int in_dtype,
                            int out_dtype, cudaStream_t st) {
-  if (tc_prefill_supported(dk, dv, in_dtype, out_dtype, p.block_size)) return launch_tc_prefill(p, max_len, st);
+  if (tc_prefill_supported(dk, dv, in_dtype, out_dtype, p.block_size))
+    return workspace ? launch_tc_prefill2(p, workspace, max_len, st) : launch_tc_prefill(p, max_len, st);
   GDN_SCAN_DISPATCH(kPrefill)
 }
 

@@ -345,3 +345,79 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 }  // namespace tc
 }  // namespace gdn
+
+namespace gdn {
+namespace tc {
+// ---- MMA with the A operand in tensor memory ----------------------------------
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulate.  A is M = 128
+// lanes (one row each) by K = 16 elements: eight 32-bit columns, each holding
+// two bf16 (the lower K index in the low half).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Three-pass product D (+)= A B^T with A = (a_hi + a_lo) in tensor memory
+// (KSTEPS x 8 columns each) and B = (b_hi + b_lo) K-major 128-byte swizzled
+// bf16 tiles in shared memory whose 64-wide K-blocks lie BKB bytes apart.
+template <int KSTEPS, uint32_t BKB>
+__device__ __forceinline__ void mma3_ts(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b, uint32_t b_lo,
+                                        uint32_t idesc, bool accumulate) {
+  const uint64_t dB[2] = {desc_sw128(b), desc_sw128(b_lo)};
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass) {
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      const uint64_t oB = ((uint32_t)(ks >> 2) * BKB + (uint32_t)(ks & 3) * 32u) >> 4;
+      mma_bf16_ts(d, (pass == 2 ? a_lo : a_hi) + 8u * (uint32_t)ks, dB[pass == 1 ? 1 : 0] + oB, idesc,
+                  (accumulate || pass != 0 || ks != 0) ? 1u : 0u);
+    }
+  }
+}
+
+// registers -> tensor memory, 8 columns of this thread's lane
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Two fp32 values as a packed pair of bf16 hi parts and a pair of bf16 lo
+// parts (x ~= hi + lo; the first value in the low halves).
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+  const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hb);
+  const float2 r = unpack2(sub2(pack2(a, b), pack2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xFFFF0000u))));
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
+  hi = hw;
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
+}
+
+// ---- untiled bulk copies (cp.async.bulk): 16-byte aligned addresses, sizes
+// a multiple of 16 ------------------------------------------------------------
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* m) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(m))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+}  // namespace tc
+}  // namespace gdn

@@ -1,0 +1,991 @@
+// tc_chain.cu — the chunked prefill as two kernels on the tensor cores
+// (dk = dv = 128, bf16 inputs and outputs, block size a multiple of 64).
+//
+// The chunk (UT) form of the gated delta rule ("Gated DeltaNet",
+// S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = S_t q_t) over a
+// chunk of C = 64 tokens, with k^, q^ the L2-normalised rows, G_i the running
+// sum of the log decays inside the chunk, gam_i = exp(G_i), dec_i =
+// exp(G_C - G_i), A_ij = b_i exp(G_i - G_j) k^_i.k^_j (j < i), T = (I + A)^{-1}
+// and S0 the state entering the chunk, regrouped so that everything that does
+// not depend on S0 is computed apart:
+//   W   = -T diag(b gam) K^        U' = T diag(b) V        (C x dk, C x dv)
+//   P_ij = exp(G_i - G_j) q^_i.k^_j   (j <= i)
+//   U   = U' + W S0^T                                          (C x dv)
+//   O   = diag(gam) Q^ S0^T + P U
+//   S_C = gam_C S0 + U^T diag(dec) K^
+// (U holds the chunk's rank-one updates u_i; the triangular system collects
+// the (I - b k k^T) factors of the tokens before each one.)
+//
+// tc_chunk_kernel: one CTA per (sequence, chunk, qk head).  The conv + SiLU of
+//   the chunk's q and k channels, their norms and the Gram products
+//   [K^ K^T; Q^ K^T] run once for the qk head's group of value heads; per
+//   value head of the group the gates, A, P and T, the v conv, and on the
+//   tensor cores U'^T = (V^T diag(b)) T^T and W = [-T diag(b gam); 0] K^.  It
+//   writes, per chunk slot of the workspace, ready-to-load operand images:
+//   W and P (bf16 hi / lo, 128-byte swizzled), U'^T (fp32) and gam, dec per
+//   value head; Q^ and K^T (bf16 hi / lo) per qk head.  No chunk waits for
+//   another, so the whole call's chunks fill every SM.
+// tc_chain_kernel: one CTA per (sequence, value head) chain (or a piece of
+//   it, as the fused kernel's schedule cuts them).  The fp32 state stays in
+//   tensor memory; per chunk it splits S0 into bf16 hi / lo parts held in
+//   tensor memory as the A operand, adds S0 W^T onto U'^T and forms S0 Q^T
+//   (tensor cores), splits U into tensor memory, and forms S += U^T diag(dec)
+//   K^ and U^T P^T (tensor cores), then the outputs.  Operand images of the
+//   next chunk load by bulk copies into the second of two buffers meanwhile.
+// Chunks start at absolute multiples of 64, so a block boundary is a chunk end
+// and a checkpoint is the tensor-memory state between two chunks: a resume
+// replays the cold run's arithmetic bit for bit.  Every product runs three
+// bf16 passes (hi*hi + hi*lo + lo*hi) with fp32 accumulation.  Every mbarrier
+// wait is bounded as in the fused kernel (gdn_prefill_args.wait_cycles).
+#include "launch.h"
+#include "tc.cuh"
+#include "tc_chunk.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kD = 128, kC = 64;
+constexpr int kWorkers = 512;                 // sixteen worker warps
+constexpr int kThreads = kWorkers + 32;       // + the issuing warp
+constexpr int kMma = kWorkers;                // the issuing thread
+constexpr int kXRows = kC + kWinRows;
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitDefault = 4000000000LL;
+
+// ---- workspace: per chunk slot, operand images ready for the chain ---------
+constexpr uint32_t kImgW = 32768;    // W hi | lo: 64 rows (i) x 128 k (c), two 64-wide k-blocks each
+constexpr uint32_t kImgQ = 32768;    // Q^ hi | lo: same shape
+constexpr uint32_t kImgP = 16384;    // P hi | lo: 64 rows (i) x 64 k (j)
+constexpr uint32_t kImgK = 32768;    // K^T hi | lo: 128 rows (c) x 64 k (j)
+constexpr uint32_t kImgU = 32768;    // U'^T fp32 [128 r][64 i]
+constexpr uint32_t kImgG = 512;      // gam[64], dec[64] fp32
+
+struct ChunkWs {
+  uint8_t* w;      // [slots][Hv] kImgW
+  uint8_t* pm;     // [slots][Hv] kImgP
+  float* u;        // [slots][Hv] kImgU
+  float* g;        // [slots][Hv] kImgG
+  uint8_t* q;      // [slots][Hqk] kImgQ
+  uint8_t* k;      // [slots][Hqk] kImgK
+  int64_t slots;
+};
+
+// A sequence's chunk c lives in slot floor(cu[s] / 64) + s + c: chunks of
+// consecutive sequences never share a slot, and the slots of a call number
+// at most floor(T / 64) + N + 1.
+__device__ __forceinline__ int64_t chunk_slot(const ScanParams& p, int s, int64_t c) {
+  return (int64_t)p.cu_seqlens[s] / kC + s + c;
+}
+
+// ---- shared memory of the chunk kernel (offsets from a 1024-aligned base) ----
+struct CkSmem {
+  static constexpr uint32_t R1 = 0;                  // (A) y fp32 [64][256] (q | k)
+  static constexpr uint32_t YF = R1;
+  static constexpr uint32_t AT = R1;                 // (B) A^T fp32 [64 j][64 i]
+  static constexpr uint32_t AM = R1 + 16384;         //     A fp32 row-major, slots swizzled
+  static constexpr uint32_t TF = R1 + 32768;         //     T fp32 [64][64]
+  static constexpr uint32_t DT = R1 + 49152;         //     diagonal inverses [4][16][20]
+  static constexpr uint32_t NT = R1 + 54272;         //     N blocks [6][16][16]
+  static constexpr uint32_t R2 = 65536;              // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
+  static constexpr uint32_t KQ = R2;
+  static constexpr uint32_t KQ_LO = R2 + 32768;
+  static constexpr uint32_t TP = R2;                 // (B) [-T diag(b gam); 0] hi [128][64], lo at +16 KB
+  static constexpr uint32_t TP_LO = R2 + 16384;
+  static constexpr uint32_t WB = R2;                 //     W hi [2 kb][64][64], lo at +16 KB (after the product)
+  static constexpr uint32_t VB = R2 + 32768;         //     V^T diag(b) hi [128][64], lo at +16 KB
+  static constexpr uint32_t VB_LO = R2 + 49152;
+  static constexpr uint32_t KT = 131072;             // K^T hi [128][64], lo at +16 KB (kept)
+  static constexpr uint32_t KT_LO = KT + 16384;
+  static constexpr uint32_t XQ = 163840;             // (A) pre-conv rows t0-3 .. t0+63, bf16 [67][128]
+  static constexpr uint32_t XK = XQ + 17408;
+  static constexpr uint32_t TB = XQ;                 // (B) T hi [64][64], lo at +8 KB
+  static constexpr uint32_t TB_LO = XQ + 8192;
+  static constexpr uint32_t PB = XQ + 16384;         //     P hi [64][64], lo at +8 KB
+  static constexpr uint32_t PB_LO = XQ + 24576;
+  static constexpr uint32_t XV = XK + 17408;         // v rows of the current value head
+  static constexpr uint32_t GT = XV + 17408;         // gate sets [2][4][64] fp32 (G, gam, dec, b), then rq, rk
+  static constexpr uint32_t MBAR = GT + 2048 + 512;  // [0] Gram [1] U' [2] W [3] q/k rows [4] v rows
+  static constexpr uint32_t TSLOT = MBAR + 40;
+  static constexpr uint32_t BYTES = TSLOT + 8;
+  static constexpr uint32_t ALLOC = BYTES + 1024;
+};
+static_assert(CkSmem::PB_LO + 8192 <= CkSmem::XV, "T and P images overlap the v rows");
+static_assert(CkSmem::ALLOC <= 232448, "chunk kernel shared memory exceeds the per-CTA limit");
+
+// tensor-memory columns of the chunk kernel
+constexpr uint32_t kCkGram = 0;     // [K^ K^T; Q^ K^T]: lanes 0-63 k^_i.k^_j, 64-127 q^_i.k^_j
+constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = row
+constexpr uint32_t kCkU = 128;      // U'^T, lane = channel r, column = row i
+constexpr uint32_t kCkW = 256;      // W, lanes 0-63 = row i, 128 columns c
+
+// ---- shared memory of the chain kernel: two buffers of one chunk's images --
+struct ChSmem {
+  static constexpr uint32_t W = 0;                   // W hi [2][64][64], lo at +16 KB
+  static constexpr uint32_t Q = 32768;               // Q^ hi | lo
+  static constexpr uint32_t P = 65536;               // P hi | lo
+  static constexpr uint32_t K = 81920;               // K^T hi | lo, turned into (K^T diag(dec)) in place
+  static constexpr uint32_t BUF = 114688;            // bytes of one buffer (1024-aligned)
+  static constexpr uint32_t G = 2 * BUF;             // gam | dec of each buffer [2][128] fp32
+  static constexpr uint32_t MBAR = G + 2 * kImgG;    // [0,1] images of buffer 0 / 1, [2] U, [3] SQ, [4] S, [5] UP
+  static constexpr uint32_t TSLOT = MBAR + 48;
+  static constexpr uint32_t BYTES = TSLOT + 8;
+  static constexpr uint32_t ALLOC = BYTES + 1024;
+};
+static_assert(ChSmem::ALLOC <= 232448, "chain kernel shared memory exceeds the per-CTA limit");
+
+// tensor-memory columns of the chain kernel (lane = state row r)
+constexpr uint32_t kChS = 0;        // S fp32 [128][128]
+constexpr uint32_t kChS0H = 128;    // S0 hi, bf16 pairs [128][64]
+constexpr uint32_t kChS0L = 192;    // S0 lo
+constexpr uint32_t kChU = 256;      // U'^T + S0 W^T fp32 [128][64]
+constexpr uint32_t kChSQ = 320;     // S0 Q^T fp32
+constexpr uint32_t kChUP = 384;     // U^T P^T fp32
+constexpr uint32_t kChUH = 448;     // U^T hi, bf16 pairs [128][32]
+constexpr uint32_t kChUL = 480;     // U^T lo
+
+__device__ __forceinline__ bool work_wait(uint64_t* m, uint32_t parity, long long lim) {
+  return lim >= 0 && tc::mbar_wait_bounded(m, parity, lim);
+}
+__device__ __forceinline__ void mma_wait(uint64_t* m, uint32_t parity, bool& ok, long long lim) {
+  ok = work_wait(m, parity, lim) && ok;
+  tc::fence_after_sync();
+}
+__device__ __forceinline__ bool cta_sync_ok(bool ok) {
+  tc::fence_before_sync();
+  ok = __syncthreads_and(ok);
+  tc::fence_after_sync();
+  return ok;
+}
+__device__ __forceinline__ long long wait_limit(const ScanParams& p) {
+  return p.wait_cycles > 0 ? p.wait_cycles : p.wait_cycles < 0 ? -1 : kWaitDefault;
+}
+
+// The issuing warp's gate set of value head h for the chunk's rows [t0, t0 +
+// 64): G (running sum of g), gam = exp(G), dec = exp(G_C - G), b; rows past
+// the end have g = b = 0.
+__device__ __forceinline__ void chunk_gates(const TokenView<__nv_bfloat16>& V, int64_t t0, int64_t n, int h,
+                                            int lane, float* Gs) {
+  float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+  if (t0 + lane < n) { g0 = *V.gptr(t0 + lane, h); b0 = *V.bptr(t0 + lane, h); }
+  if (t0 + lane + 32 < n) { g1 = *V.gptr(t0 + lane + 32, h); b1 = *V.bptr(t0 + lane + 32, h); }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float a0 = __shfl_up_sync(0xffffffffu, g0, o);
+    const float a1 = __shfl_up_sync(0xffffffffu, g1, o);
+    if (lane >= o) { g0 += a0; g1 += a1; }
+  }
+  g1 += __shfl_sync(0xffffffffu, g0, 31);
+  const float gC = __shfl_sync(0xffffffffu, g1, 31);
+  Gs[lane] = g0; Gs[lane + 32] = g1;
+  Gs[64 + lane] = expf(g0); Gs[96 + lane] = expf(g1);
+  Gs[128 + lane] = expf(gC - g0); Gs[160 + lane] = expf(gC - g1);
+  Gs[192 + lane] = b0; Gs[224 + lane] = b1;
+}
+
+}  // namespace
+
+// ============================================================================
+// Chunk kernel: grid (Hqk, max chunks, N), one CTA per (qk head, chunk, sequence)
+// ============================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_chunk_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap, const ChunkWs ws) {
+  using TIN = __nv_bfloat16;
+  constexpr int D = kD, C = kC;
+  const int jq = blockIdx.x;
+  const int64_t c = blockIdx.y;
+  const int s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool worker = tid < kWorkers;
+  const int row = tid & 127;
+  const int quarter = (tid >> 7) & 3;
+  const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
+
+  TokenView<TIN> V;
+  int64_t start, n_log;
+  int32_t init, final_page;
+  if (!make_view<TIN, kPrefill>(p, s, V, start, init, final_page, n_log, false)) return;
+  const int64_t n = V.n;
+  if (c * C >= n) return;
+  const int64_t t0 = c * C;
+  const int G = p.Hv / p.Hqk;
+  const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D;
+  const int64_t row0 = p.cu_seqlens[s];
+  const int64_t slot = chunk_slot(p, s, c);
+  const long long wlim = wait_limit(p);
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  float* yf = reinterpret_cast<float*>(sm + CkSmem::YF);
+  TIN* xq = reinterpret_cast<TIN*>(sm + CkSmem::XQ);
+  TIN* xk = reinterpret_cast<TIN*>(sm + CkSmem::XK);
+  TIN* xv = reinterpret_cast<TIN*>(sm + CkSmem::XV);
+  float* gbuf = reinterpret_cast<float*>(sm + CkSmem::GT);
+  float* rq = gbuf + 512;
+  float* rk = gbuf + 576;
+  float* at = reinterpret_cast<float*>(sm + CkSmem::AT);
+  float* tf = reinterpret_cast<float*>(sm + CkSmem::TF);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + CkSmem::MBAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CkSmem::TSLOT);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int b = 0; b < 5; ++b) tc::mbar_init(mbar + b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+
+  const int y = (int)(row0 + t0 - kWinRows);
+  auto stage_v = [&](int g) {
+    tc::mbar_expect_tx(mbar + 4, kXRows * D * 2);
+    tc::tma_load_2d(xv, &xmap, 2 * p.Hqk * D + (jq * G + g) * D, y, mbar + 4);
+  };
+  // track of the copies and products in flight (for the drain after a run-out)
+  bool qk_pending = false, gram_pending = false, prod_pending = false;
+  int v_pending = -1;   // value head whose rows are in flight
+  if (tid == 0) {
+    tc::mbar_expect_tx(mbar + 3, 2 * kXRows * D * 2);
+    tc::tma_load_2d(xq, &xmap, cq0, y, mbar + 3);
+    tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 3);
+    stage_v(0);
+  }
+  qk_pending = true;
+  v_pending = 0;
+
+  // history rows of a sequence's first chunk: the resumed window, or zeros
+  auto fix_history = [&](TIN* dst, int ch0) {
+    for (int e = tid; e < kWinRows * (D / 2); e += kWorkers) {
+      const int r = e / (D / 2), c2 = e % (D / 2);
+      uint32_t v = 0;
+      if (V.win) v = *reinterpret_cast<const uint32_t*>(V.win + (int64_t)r * p.conv_dim + ch0 + 2 * c2);
+      *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
+    }
+  };
+  // v conv of value head h: channel `row`, rows [16 quarter, +16) -> tensor memory
+  auto v_conv = [&](int h) {
+    const float4 wv = ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK);
+    const int tb = 16 * quarter;
+    float xr[19], vr[16];
+#pragma unroll
+    for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
+    const f32x2 w0 = pack2(wv.x, wv.x), w1 = pack2(wv.y, wv.y), w2 = pack2(wv.z, wv.z), w3 = pack2(wv.w, wv.w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f32x2 z = mul2(w0, pack2(xr[i], xr[i + 8]));
+      z = fma2(w1, pack2(xr[i + 1], xr[i + 9]), z);
+      z = fma2(w2, pack2(xr[i + 2], xr[i + 10]), z);
+      z = fma2(w3, pack2(xr[i + 3], xr[i + 11]), z);
+      const float2 zz = unpack2(z);
+      vr[i] = silu_fast(zz.x);
+      vr[i + 8] = silu_fast(zz.y);
+    }
+    tc::tmem_st16(tbase + tlane + kCkV + 16 * quarter, vr);
+    tc::tmem_st_wait();
+  };
+
+  bool ok = true;
+  // ---------------------------------------------------------------- (A) q / k
+  if (worker) {
+    ok = workers_sync_and(work_wait(mbar + 3, 0, wlim) && work_wait(mbar + 4, 0, wlim));
+    if (ok) { qk_pending = false; v_pending = -1; }
+    if (c == 0) {
+      fix_history(xq, cq0);
+      fix_history(xk, ck0);
+      fix_history(xv, 2 * p.Hqk * D + jq * G * D);
+      workers_sync();
+    }
+    // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16) -> y
+    {
+      const int qkp = 2 * (tid & 127);
+      const float* wsrc = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;
+      const float4 wqa = ldg_f4_fresh(wsrc), wqb = ldg_f4_fresh(wsrc + kConvK);
+      const int tb = 16 * (tid >> 7);
+      const TIN* xp = (qkp < D ? xq + qkp : xk + qkp - D) + tb * D;
+      const f32x2 w0 = pack2(wqa.x, wqb.x), w1 = pack2(wqa.y, wqb.y), w2 = pack2(wqa.z, wqb.z),
+                  w3 = pack2(wqa.w, wqb.w);
+      f32x2 x[19];
+#pragma unroll
+      for (int u = 0; u < 19; ++u) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(xp + u * D);
+        x[u] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+      }
+      float* yrow = yf + tb * 256 + qkp;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        f32x2 z = mul2(w0, x[i]);
+        z = fma2(w1, x[i + 1], z);
+        z = fma2(w2, x[i + 2], z);
+        z = fma2(w3, x[i + 3], z);
+        const float2 zz = unpack2(z);
+        *reinterpret_cast<float2*>(yrow + i * 256) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
+      }
+    }
+    v_conv(jq * G);
+    workers_sync();
+    // the first head's v rows are consumed: the next head's rows
+    if (tid == 0 && ok && G > 1) stage_v(1);
+    if (ok && G > 1) v_pending = 1;
+    // L2 norm factors (rows past the end: 0)
+    {
+      const int cnt = (int)(n - t0 < C ? n - t0 : C);
+      constexpr int NP = 128 / (kWorkers / 32);
+      float ss[NP];
+#pragma unroll
+      for (int it = 0; it < NP; ++it) {
+        const int k = warp + (kWorkers / 32) * it, t = k >> 1, isk = k & 1;
+        const float* yr = yf + t * 256 + isk * D;
+        float a = 0.f;
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) {
+          const float yv = yr[lane + 32 * m];
+          a = fmaf(yv, yv, a);
+        }
+        ss[it] = a;
+      }
+      float h4[4], h2[2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool up = lane & 16;
+        const float send = up ? ss[j] : ss[j + 4];
+        h4[j] = (up ? ss[j + 4] : ss[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const bool up = lane & 8;
+        const float send = up ? h4[j] : h4[j + 2];
+        h2[j] = (up ? h4[j + 2] : h4[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+      float a;
+      {
+        const bool up = lane & 4;
+        a = (up ? h2[1] : h2[0]) + __shfl_xor_sync(0xffffffffu, up ? h2[0] : h2[1], 4);
+      }
+      a += __shfl_xor_sync(0xffffffffu, a, 2);
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      if ((lane & 3) == 0) {
+        const int k = warp + (kWorkers / 32) * (lane >> 2), t = k >> 1, isk = k & 1;
+        (isk ? rk : rq)[t] = t < cnt ? (isk ? 1.0f : p.q_scale) / sqrtf(a + p.eps) : 0.f;
+      }
+    }
+    workers_sync();
+    // operands [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T (row = k channel)
+    {
+      constexpr int NKQ = 2048 / kWorkers, NKT = 1024 / kWorkers;
+#pragma unroll
+      for (int it = 0; it < NKQ; ++it) {
+        const int i = tid + kWorkers * it, r = i >> 4, c8 = i & 15;
+        const int t = r & (C - 1);
+        const bool isq = r >= C;
+        const float f = isq ? rq[t] : rk[t];
+        const float4* src = reinterpret_cast<const float4*>(yf + t * 256 + (isq ? 0 : D) + 8 * c8);
+        const float4 ya = src[0], yb = src[1];
+        const f32x2 f2 = pack2(f, f);
+        const float2 e01 = unpack2(mul2(pack2(ya.x, ya.y), f2));
+        const float2 e23 = unpack2(mul2(pack2(ya.z, ya.w), f2));
+        const float2 e45 = unpack2(mul2(pack2(yb.x, yb.y), f2));
+        const float2 e67 = unpack2(mul2(pack2(yb.z, yb.w), f2));
+        const float e[8] = {e01.x, e01.y, e23.x, e23.y, e45.x, e45.y, e67.x, e67.y};
+        const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
+        tc::store_split8(sm + CkSmem::KQ + off, sm + CkSmem::KQ_LO + off, e);
+      }
+#pragma unroll
+      for (int it = 0; it < NKT; ++it) {
+        const int i = tid + kWorkers * it, k = i & 127, j8 = i >> 7;
+        float kt[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = 8 * j8 + u;
+          kt[u] = yf[j * 256 + D + k] * rk[j];
+        }
+        const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
+        tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
+      }
+    }
+    tc::fence_async_smem();
+  }
+  ok = cta_sync_ok(ok);
+  if (ok && tid == kMma) {
+    // [K^ K^T; Q^ K^T] (M 128, N 64, K 128)
+    tc::mma3_sw128<D / 16, 16384, 16384>(tbase + kCkGram, sbase + CkSmem::KQ, sbase + CkSmem::KQ_LO,
+                                         sbase + CkSmem::KQ, sbase + CkSmem::KQ_LO, tc::idesc_bf16_f32(128, 64),
+                                         false);
+    tc::mma_commit(mbar + 0);
+    // the qk head's images for the chain: Q^ (rows 64-127 of [K^; Q^]) and K^T
+    uint8_t* qdst = ws.q + (slot * p.Hqk + jq) * (int64_t)kImgQ;
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb)
+        tc::bulk_store(qdst + part * 16384 + kb * 8192, sm + CkSmem::KQ + part * 32768 + kb * 16384 + 8192, 8192);
+    tc::bulk_store(ws.k + (slot * p.Hqk + jq) * (int64_t)kImgK, sm + CkSmem::KT, kImgK);
+    tc::bulk_commit();
+  }
+  if (ok) gram_pending = true;
+
+  // ---------------------------------------------------------- (B) value heads
+  int g = 0;
+  for (; ok && g < G; ++g) {
+    const int h = jq * G + g;
+    float* const Gs = gbuf + 256 * (g & 1);
+    const float* gam = Gs + 64;
+    const float* bv = Gs + 192;
+    if (!worker) {
+      // this head's gates; the set it overwrites went out with the head before last
+      if (tid == kMma) tc::bulk_wait_read();
+      __syncwarp();
+      chunk_gates(V, t0, n, h, lane, Gs);
+      named_arrive(3, kThreads);
+    } else {
+      if (g > 0) {
+        // v rows of this head (issued while the head before it was processed)
+        ok = workers_sync_and(work_wait(mbar + 4, (uint32_t)(g & 1), wlim) && ok);
+        if (ok) v_pending = -1;
+        if (c == 0) {
+          fix_history(xv, 2 * p.Hqk * D + h * D);
+          workers_sync();
+        }
+        v_conv(h);
+        workers_sync();
+        if (tid == 0 && ok && g + 1 < G) stage_v(g + 1);
+        if (ok && g + 1 < G) v_pending = g + 1;
+      }
+      named_sync(3, kThreads);   // the gates; the previous head's images have been read out
+      if (g == 0) {
+        mma_wait(mbar + 0, 0, ok, wlim);
+        if (ok) gram_pending = false;
+      }
+      // A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j), columns j in [16 quarter, +16)
+      {
+        const int q4 = warp & 3;
+        const int ir = (q4 & 1) * 32 + lane;
+        float ap[16];
+        tc::tmem_ld16(tbase + tlane + kCkGram + 16 * quarter, ap);
+        const float Gi = Gs[ir];
+        const float bi = q4 < 2 ? bv[ir] : 1.0f;
+        const int lim = q4 < 2 ? ir : ir + 1;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = 16 * quarter + e;
+          const float m = j < lim ? bi : 0.f;
+          ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
+        }
+        if (q4 < 2) {
+          float* am = reinterpret_cast<float*>(sm + CkSmem::AM);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) at[(16 * quarter + e) * C + ir] = ap[e];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<float4*>(am + am_index(ir, 16 * quarter + 4 * c4)) =
+                make_float4(ap[4 * c4], ap[4 * c4 + 1], ap[4 * c4 + 2], ap[4 * c4 + 3]);
+        } else {
+#pragma unroll
+          for (int c8 = 0; c8 < 2; ++c8) {
+            const uint32_t off = tc::sw128_offset(ir, 16 * quarter + 8 * c8, 64);
+            tc::store_split8(sm + CkSmem::PB + off, sm + CkSmem::PB_LO + off, ap + 8 * c8);
+          }
+        }
+      }
+      workers_sync();
+      if (tid >= 256) {
+        // T = (I + A)^{-1}; then T (rows i, K = j; zero above the diagonal) and
+        // [-T diag(b gam); 0] (128 rows) as operands
+        tri_inverse64(at, reinterpret_cast<const float*>(sm + CkSmem::AM), tf,
+                      reinterpret_cast<float*>(sm + CkSmem::DT), reinterpret_cast<float*>(sm + CkSmem::NT),
+                      tid - 256);
+        for (int e = tid - 256; e < 1024; e += 256) {
+          const int i = e >> 3, c8 = e & 7;
+          float v8[8], w8[8];
+          if (i < C) {
+            const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
+            const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
+            const float tv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = 8 * c8 + u;
+              v8[u] = j > i ? 0.f : tv[u];
+              w8[u] = -(v8[u] * (bv[j] * gam[j]));
+            }
+            const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
+            tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w8[u] = 0.f;
+          }
+          const uint32_t off = tc::sw128_offset(i, 8 * c8, 128);
+          tc::store_split8(sm + CkSmem::TP + off, sm + CkSmem::TP_LO + off, w8);
+        }
+      } else {
+        // V^T diag(b) of channel `row` for rows i in [32 qh, +32): the A operand of U'^T
+        const int qh = tid >> 7;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i0 = 32 * qh + 16 * hh;
+          float a[16];
+          tc::tmem_ld16(tbase + tlane + kCkV + i0, a);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a[e] *= bv[i0 + e];
+#pragma unroll
+          for (int c8 = 0; c8 < 2; ++c8) {
+            const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
+            tc::store_split8(sm + CkSmem::VB + off, sm + CkSmem::VB_LO + off, a + 8 * c8);
+          }
+        }
+      }
+      tc::fence_async_smem();
+    }
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == kMma) {
+      // U'^T = (V^T diag(b)) T^T (M 128, N 64, K 64); W = [-T diag(b gam); 0] K^ (M 128, N 128, K 64)
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kCkU, sbase + CkSmem::VB, sbase + CkSmem::VB_LO, sbase + CkSmem::TB,
+                                   sbase + CkSmem::TB_LO, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 1);
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kCkW, sbase + CkSmem::TP, sbase + CkSmem::TP_LO, sbase + CkSmem::KT,
+                                   sbase + CkSmem::KT_LO, tc::idesc_bf16_f32(128, 128), false);
+      tc::mma_commit(mbar + 2);
+    }
+    prod_pending = true;
+    if (worker) {
+      const uint32_t par = (uint32_t)(g & 1);
+      mma_wait(mbar + 1, par, ok, wlim);
+      // U'^T of channel `row`, rows [16 quarter, +16) -> the workspace (fp32 [r][i])
+      {
+        float u[16];
+        tc::tmem_ld16(tbase + tlane + kCkU + 16 * quarter, u);
+        float4* dst = reinterpret_cast<float4*>(ws.u + (slot * p.Hv + h) * (int64_t)(kImgU / 4) + row * 64 +
+                                                16 * quarter);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) dst[c4] = make_float4(u[4 * c4], u[4 * c4 + 1], u[4 * c4 + 2], u[4 * c4 + 3]);
+      }
+      mma_wait(mbar + 2, par, ok, wlim);
+      // W rows i (lanes 0-63) -> the W image (rows i, K = c), columns [32 (warp >> 2), +32)
+      if ((warp & 3) < 2) {
+        const int i = (warp & 3) * 32 + lane, c0 = 32 * (warp >> 2);
+        float wv[32];
+        tc::tmem_ld32(tbase + tlane + kCkW + c0, wv);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint32_t off = tc::sw128_offset(i, c0 + 8 * c8, 64);
+          tc::store_split8(sm + CkSmem::WB + off, sm + CkSmem::WB + 16384 + off, wv + 8 * c8);
+        }
+      }
+      tc::fence_async_smem();
+    }
+    ok = cta_sync_ok(ok);
+    if (ok) prod_pending = false;
+    if (!ok) break;
+    if (tid == kMma) {
+      const int64_t hv = slot * p.Hv + h;
+      tc::bulk_store(ws.w + hv * kImgW, sm + CkSmem::WB, kImgW);
+      tc::bulk_store(ws.pm + hv * kImgP, sm + CkSmem::PB, kImgP);
+      // gam | dec of the head for the chain (G and b are folded into W, U', P)
+      tc::bulk_store(ws.g + hv * (kImgG / 4), Gs + 64, 256);
+      tc::bulk_store(ws.g + hv * (kImgG / 4) + 64, Gs + 128, 256);
+      tc::bulk_commit();
+      // the next head rewrites the images these copies read
+      tc::bulk_wait_read();
+    }
+  }
+
+  if (!ok) {
+    // a wait ran out: report it, let the copies and products in flight finish
+    // (default bound), release the tensor memory
+    if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);
+    if (worker) {
+      if (qk_pending) tc::mbar_wait_bounded(mbar + 3, 0, kWaitDefault);
+      if (v_pending >= 0) tc::mbar_wait_bounded(mbar + 4, (uint32_t)(v_pending & 1), kWaitDefault);
+      if (gram_pending) tc::mbar_wait_bounded(mbar + 0, 0, kWaitDefault);
+      if (prod_pending) {
+        tc::mbar_wait_bounded(mbar + 1, (uint32_t)(g & 1), kWaitDefault);
+        tc::mbar_wait_bounded(mbar + 2, (uint32_t)(g & 1), kWaitDefault);
+      }
+    }
+  }
+  if (tid == kMma) tc::bulk_wait_all();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+}
+
+// ============================================================================
+// Chain kernel: grid (Hv, pieces), one CTA per (value head, (level, sequence))
+// ============================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_chain_kernel(const ScanParams p, const ChunkWs ws, const PieceMap pm, int64_t max_chunks) {
+  using TOUT = __nv_bfloat16;
+  constexpr int D = kD, C = kC;
+  const int h = blockIdx.x;
+  int s = pm.s0 + (int)blockIdx.y, level = pm.level0;
+  if (s >= pm.nseqs) {
+    s -= pm.nseqs;
+    ++level;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const bool worker = tid < kWorkers;
+  const int row = tid & 127;
+  const int quarter = (tid >> 7) & 3;
+  const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
+
+  TokenView<__nv_bfloat16> V;
+  int64_t start, n_log;
+  int32_t init, final_page;
+  const bool report = (h == 0 && tid == 0);
+  if (!make_view<__nv_bfloat16, kPrefill>(p, s, V, start, init, final_page, n_log, report)) return;
+  const int64_t n = V.n;
+  const int64_t nch = (n + C - 1) / C;
+  if (nch > max_chunks) {   // the call's max_seq_len was below this sequence's length
+    if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+    return;
+  }
+  const int64_t cb = (int64_t)level * pm.piece;
+  if (level > 0 && cb >= nch) return;
+  const int64_t ce = level == pm.last_level || cb + pm.piece > nch ? nch : cb + pm.piece;
+  const int32_t from = level > 0 ? final_page : init;
+  if (level > 0 &&
+      __syncthreads_or(tid == 0 && *reinterpret_cast<volatile const int32_t*>(p.err) == GDN_ERR_TIMEOUT))
+    return;
+  const long long wlim = wait_limit(p);
+  const int64_t row0 = p.cu_seqlens[s];
+
+  extern __shared__ uint8_t dyn_smem[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + ChSmem::MBAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + ChSmem::TSLOT);
+
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+#pragma unroll
+    for (int b = 0; b < 6; ++b) tc::mbar_init(mbar + b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase + tlane + kChS + 32 * quarter;
+
+  // chunk c's images into buffer c & 1 (issuing thread)
+  auto load_chunk = [&](int64_t c) {
+    const int b = (int)(c & 1);
+    const int64_t slot = chunk_slot(p, s, c);
+    const int64_t hv = slot * p.Hv + h;
+    const int64_t hq = slot * p.Hqk + h / (p.Hv / p.Hqk);
+    uint8_t* dst = sm + b * ChSmem::BUF;
+    uint64_t* m = mbar + b;
+    tc::mbar_expect_tx(m, kImgW + kImgQ + kImgP + kImgK + kImgG);
+    tc::bulk_load(dst + ChSmem::W, ws.w + hv * kImgW, kImgW, m);
+    tc::bulk_load(dst + ChSmem::Q, ws.q + hq * kImgQ, kImgQ, m);
+    tc::bulk_load(dst + ChSmem::P, ws.pm + hv * kImgP, kImgP, m);
+    tc::bulk_load(dst + ChSmem::K, ws.k + hq * kImgK, kImgK, m);
+    tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv * (kImgG / 4), kImgG, m);
+  };
+  // U'^T of chunk c, this thread's row and 16 columns, from the workspace
+  auto load_u = [&](int64_t c, float (&u)[16]) {
+    const float4* src = reinterpret_cast<const float4*>(
+        ws.u + (chunk_slot(p, s, c) * p.Hv + h) * (int64_t)(kImgU / 4) + row * 64 + 16 * quarter);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const float4 v = ldg_f4_fresh(reinterpret_cast<const float*>(src + c4));
+      u[4 * c4] = v.x; u[4 * c4 + 1] = v.y; u[4 * c4 + 2] = v.z; u[4 * c4 + 3] = v.w;
+    }
+  };
+
+  int64_t load_issued = -1;   // the last chunk whose images were requested
+  if (tid == kMma && cb < ce) load_chunk(cb);
+  if (cb < ce) load_issued = cb;
+  float un[16];
+  if (worker) {
+    // initial state (zeros on a cold start: the pool is not read)
+    const float* src = from >= 0 ? page_state(p.pool, from) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+    float v[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 f = src ? reinterpret_cast<const float4*>(src)[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
+    }
+    tc::tmem_st32(tS, v);
+    tc::tmem_st_wait();
+    if (cb < ce) load_u(cb, un);
+  }
+
+  int32_t pend = -1;        // checkpoint page due at the next read of S
+  bool ok = true;
+  uint32_t issued = 0;      // products committed in the current chunk (bit: mbar index)
+  bool s_pending = false;   // the previous chunk's state update may still run
+  int64_t c = cb;
+  for (; c < ce; ++c) {
+    const int b = (int)(c & 1);
+    const uint32_t par = (uint32_t)((c - cb) & 1);
+    const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
+    const int64_t t0 = c * C;
+    const int cnt = (int)(n - t0 < C ? n - t0 : C);
+    const float* gsm = reinterpret_cast<const float*>(sm + ChSmem::G + b * kImgG);   // gam[64], dec[64]
+    uint8_t* buf = sm + b * ChSmem::BUF;
+    issued = 0;
+    if (worker) {
+      // ---- S0: wait for the state update, checkpoint, split into tensor memory,
+      // gam_C S0 back; U'^T of this chunk into the U columns
+      if (s_pending) mma_wait(mbar + 4, par ^ 1u, ok, wlim);
+      ok = work_wait(mbar + b, bpar, wlim) && ok;   // this chunk's images (gam_C)
+      const float gC = gsm[C - 1];
+      float v0[32];
+      tc::tmem_ld32(tS, v0);
+      if (pend >= 0) {
+        float* ck = page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          reinterpret_cast<float4*>(ck)[c4] = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+      }
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) tc::split_pair(v0[2 * e], v0[2 * e + 1], hi[e], lo[e]);
+      tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
+      tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+        v0[e] = gg.x;
+        v0[e + 1] = gg.y;
+      }
+      tc::tmem_st32(tS, v0);
+      tc::tmem_st16(tbase + tlane + kChU + 16 * quarter, un);
+      tc::tmem_st_wait();
+      pend = -1;
+    }
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    s_pending = false;
+    if (tid == kMma) {
+      // the next chunk's images into the other buffer (its last reader, the
+      // chunk before this one, has finished)
+      if (c + 1 < ce) load_chunk(c + 1);
+      // this chunk's images, observed by the thread whose products read them
+      ok = work_wait(mbar + b, bpar, wlim) && ok;
+      // U += S0 W^T (M 128, N 64, K 128) onto U'^T; S0 Q^T (M 128, N 64, K 128)
+      tc::mma3_ts<D / 16, 8192>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + b * ChSmem::BUF + ChSmem::W,
+                                sbase + b * ChSmem::BUF + ChSmem::W + 16384, tc::idesc_bf16_f32(128, 64), true);
+      tc::mma_commit(mbar + 2);
+      tc::mma3_ts<D / 16, 8192>(tbase + kChSQ, tbase + kChS0H, tbase + kChS0L, sbase + b * ChSmem::BUF + ChSmem::Q,
+                                sbase + b * ChSmem::BUF + ChSmem::Q + 16384, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 3);
+    }
+    if (c + 1 < ce) load_issued = c + 1;
+    issued |= 4u | 8u;
+    if (worker) {
+      // K^T -> K^T diag(dec) in place: row `row` (k channel), rows i in [16 (tid >> 7), +16)
+      {
+        const int i0 = 16 * (tid >> 7);
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
+          uint8_t* ph = buf + ChSmem::K + off;
+          uint8_t* pl = buf + ChSmem::K + 16384 + off;
+          const uint4 vh = *reinterpret_cast<const uint4*>(ph);
+          const uint4 vl = *reinterpret_cast<const uint4*>(pl);
+          const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float a0 = __uint_as_float(wh[u] << 16) + __uint_as_float(wl[u] << 16);
+            const float a1 = __uint_as_float(wh[u] & 0xFFFF0000u) + __uint_as_float(wl[u] & 0xFFFF0000u);
+            e[2 * u] = a0 * gsm[64 + i0 + 8 * c8 + 2 * u];
+            e[2 * u + 1] = a1 * gsm[64 + i0 + 8 * c8 + 2 * u + 1];
+          }
+          tc::store_split8(ph, pl, e);
+        }
+        tc::fence_async_smem();
+      }
+      // ---- U: wait for U'^T + S0 W^T, split into tensor memory (the A operand
+      // of the state update and of U^T P^T)
+      mma_wait(mbar + 2, par, ok, wlim);
+      float u[16];
+      tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tc::split_pair(u[2 * e], u[2 * e + 1], hi[e], lo[e]);
+      tc::tmem_st8(tbase + tlane + kChUH + 8 * quarter, hi);
+      tc::tmem_st8(tbase + tlane + kChUL + 8 * quarter, lo);
+      tc::tmem_st_wait();
+    }
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == kMma) {
+      // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64) first: the next chunk waits for it;
+      // then U^T P^T (M 128, N 64, K 64)
+      tc::mma3_ts<C / 16, 0>(tbase + kChS, tbase + kChUH, tbase + kChUL, sbase + b * ChSmem::BUF + ChSmem::K,
+                             sbase + b * ChSmem::BUF + ChSmem::K + 16384, tc::idesc_bf16_f32(128, 128), true);
+      tc::mma_commit(mbar + 4);
+      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + b * ChSmem::BUF + ChSmem::P,
+                             sbase + b * ChSmem::BUF + ChSmem::P + 8192, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + 5);
+    }
+    issued |= 16u | 32u;
+    s_pending = true;
+    if (worker) {
+      // the next chunk's U'^T, while the products run
+      if (c + 1 < ce) load_u(c + 1, un);
+      mma_wait(mbar + 3, par, ok, wlim);
+      mma_wait(mbar + 5, par, ok, wlim);
+      // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i, rows i in [16 quarter, +16)
+      float sq[16], up[16];
+      tc::tmem_ld16x2(tbase + tlane + kChSQ + 16 * quarter, tbase + tlane + kChUP + 16 * quarter, sq, up);
+      TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
+      const int64_t tstride = (int64_t)p.Hv * D;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int i = 16 * quarter + e;
+        if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gsm[i], sq[e], up[e]));
+      }
+      // a block boundary at this chunk's end: checkpointed at the next read of S
+      const int64_t pos = start + t0 + cnt;
+      if (pos % p.block_size == 0) {
+        const int64_t jb = pos / p.block_size - 1;
+        int32_t page = -1;
+        if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
+        else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+        if (page >= 0) {
+          if (page_ok(p.pool, page)) pend = page;
+          else if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
+        }
+      }
+    }
+  }
+
+  const int64_t ci = c < ce ? c : ce - 1;   // the chunk `issued` refers to
+  if (ok && worker && s_pending) mma_wait(mbar + 4, (uint32_t)((ce - 1 - cb) & 1), ok, wlim);
+  ok = cta_sync_ok(ok);
+  if (ok) {
+    if (worker) {
+      // final state (and a checkpoint due at the last chunk's end)
+      float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 32 * quarter;
+      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+      float v0[32];
+      tc::tmem_ld32(tS, v0);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+        reinterpret_cast<float4*>(dst)[c4] = f0;
+        if (ck) reinterpret_cast<float4*>(ck)[c4] = f0;
+      }
+    }
+  } else if (cb < ce) {
+    // a wait ran out: report it, give every product and copy in flight one
+    // more wait with the default bound, release the tensor memory
+    if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);
+    if (worker) {
+      const uint32_t par = (uint32_t)((ci - cb) & 1);
+#pragma unroll 1
+      for (int k = 2; k < 6; ++k)
+        if (issued & (1u << k)) tc::mbar_wait_bounded(mbar + k, par, kWaitDefault);
+      if (!(issued & 16u) && s_pending && ci > cb) tc::mbar_wait_bounded(mbar + 4, par ^ 1u, kWaitDefault);
+      // image loads: the last one requested, and the one before it
+      for (int64_t lc = load_issued - 1; lc <= load_issued; ++lc)
+        if (lc >= cb) tc::mbar_wait_bounded(mbar + (lc & 1), (uint32_t)(((lc - cb) >> 1) & 1), kWaitDefault);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+}
+
+// ============================================================================
+// Host side
+// ============================================================================
+size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
+  const int64_t slots = total_tokens / kC + num_seqs + 1;
+  const int64_t per_v = (int64_t)kImgW + kImgP + kImgU + kImgG;
+  const int64_t per_q = (int64_t)kImgQ + kImgK;
+  return (size_t)(slots * (Hv * per_v + Hqk * per_q)) + 1024;
+}
+
+namespace {
+ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
+  ChunkWs w;
+  w.slots = total_tokens / kC + num_seqs + 1;
+  uint8_t* b = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 1023) & ~uintptr_t(1023));
+  auto take = [&](int64_t bytes) {
+    uint8_t* r = b;
+    b += bytes;
+    return r;
+  };
+  w.w = take(w.slots * Hv * (int64_t)kImgW);
+  w.pm = take(w.slots * Hv * (int64_t)kImgP);
+  w.u = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgU));
+  w.q = take(w.slots * Hqk * (int64_t)kImgQ);
+  w.k = take(w.slots * Hqk * (int64_t)kImgK);
+  w.g = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgG));
+  return w;
+}
+}  // namespace
+
+// The chain kernel's per-chunk work is small beside a launch's fixed costs
+// (state in and out, the first images' load, the slowest CTA, the gap between
+// launches), so the pieces are longer than the fused kernel's: a launch
+// counts as five chunk times.
+constexpr double kChainLaunchCost = 5.0;
+
+PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms) {
+  return tc_prefill_schedule_cost(Hv, num_seqs, max_len, sms, kChainLaunchCost);
+}
+
+cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  if ((int64_t)p.Hv * p.num_seqs > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+  const ChunkWs ws = bind_chunk_ws(workspace, p.Hqk, p.Hv, p.num_seqs, p.total_rows);
+  const int64_t maxc = max_len > 0 ? (max_len + kC - 1) / kC : 0;
+  if (maxc > 65535) return cudaErrorInvalidValue;
+  if (maxc > 0 && p.total_rows > 0) {
+    CUtensorMap xmap;
+    memset(&xmap, 0, sizeof(xmap));
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)p.x_ld, (cuuint64_t)p.total_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.x_ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kXRows};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    cudaError_t e =
+        cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CkSmem::ALLOC);
+    if (e != cudaSuccess) return e;
+    tc_chunk_kernel<<<dim3(p.Hqk, (unsigned)maxc, p.num_seqs), kThreads, CkSmem::ALLOC, st>>>(p, xmap, ws);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ChSmem::ALLOC);
+  if (e != cudaSuccess) return e;
+  const PrefillSchedule sc = tc_chain_schedule(p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
+  PieceMap pm;
+  pm.nseqs = p.num_seqs;
+  pm.piece = (int32_t)sc.piece;
+  pm.last_level = (int32_t)(sc.levels - 1);
+  const int64_t pairs = sc.levels * p.num_seqs, per = sc.width / p.Hv;
+  for (int64_t t = 0; t < sc.launches; ++t) {
+    const int64_t base = t * per;
+    pm.s0 = (int32_t)(base % p.num_seqs);
+    pm.level0 = (int32_t)(base / p.num_seqs);
+    const int64_t cnt = pairs - base < per ? pairs - base : per;
+    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, st>>>(p, ws, pm, maxc);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -233,7 +233,9 @@ typedef struct gdn_prefill_args {
   int32_t max_blocks;            /* row stride of block_table                 */
   int64_t total_tokens;          /* T = cu_seqlens[N]                         */
   int64_t max_seq_len;           /* host bound on any cu_seqlens[s+1] -
-                                    cu_seqlens[s] (0: T); sizes the grid      */
+                                    cu_seqlens[s] (0: T); sizes the grid.  A
+                                    longer sequence sets GDN_ERR_INVALID_ARG
+                                    on the two-kernel path                    */
   const int32_t* cu_seqlens;     /* [N+1], non-decreasing, cu_seqlens[0] = 0  */
   const int64_t* start_pos;      /* [N] absolute position of the first token  */
   const int64_t* start_pos_host; /* optional host copy of start_pos ([N]) for
@@ -258,21 +260,37 @@ typedef struct gdn_prefill_args {
                                     of that path: nothing is written)         */
 } gdn_prefill_args;
 
-/* Device workspace bytes gdn_prefill_chunked needs for a call with
- * total_tokens tokens.  Layers that take the tensor-core chunk kernel
- * (dk = dv = 128, bf16 in and out, block_size a multiple of 64) compute the
- * conv inside it and need none: 0, and the workspace argument may be NULL.
- * Other layers run a conv pre-pass whose SiLU(conv) rows (fp32, computed once
- * and shared by every head that reads them), q / k norm factors and gates
- * live here.  The caller allocates it (256-byte aligned); its contents are
- * scratch, overwritten by every call, so calls that share a workspace must
- * not overlap on the GPU.  0 for a malformed desc. */
+/* Device workspace bytes gdn_prefill_chunked needs for a call of num_seqs
+ * sequences with total_tokens tokens.
+ *
+ * Layers on the tensor cores (dk = dv = 128, bf16 in and out, block_size a
+ * multiple of 64) run the prefill as two kernels when given this workspace:
+ * a chunk kernel computes, for every 64-token chunk of the call at once,
+ * everything that does not depend on the state (conv, norms, the chunk's
+ * triangular solve and the products that fold it in) and leaves them here as
+ * ready operand images (about 80 KB per chunk and value head plus 64 KB per
+ * chunk and qk head); a chain kernel then carries each (sequence, value head)
+ * state through its chunks with a few tensor-core products per chunk.  Such
+ * a layer may instead pass NULL with workspace_bytes 0: it then takes one
+ * fused kernel that needs no scratch (slower on a long sequence, which it
+ * runs on as many SMs as the sequence has value heads).  The two paths agree
+ * with the same bounds but not bit for bit: a resume reproduces a cold run's
+ * bits when both take the same path, so serve a layer with one of them.
+ *
+ * Other layers run a conv pre-pass whose SiLU(conv) rows (fp32, computed
+ * once and shared by every head that reads them), q / k norm factors and
+ * gates live here; they need it.
+ *
+ * The caller allocates it (256-byte aligned); its contents are scratch,
+ * overwritten by every call, so calls that share a workspace must not
+ * overlap on the GPU.  0 for a malformed desc. */
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens);
 
-/* How gdn_prefill_chunked runs the chunk kernel of a layer on the
- * tensor-core path.  Each (sequence, value head) chain runs on one SM, its
- * chunks in order.  With at least as many chains as SMs and long chains,
+/* How gdn_prefill_chunked runs the chain of a layer on the tensor-core path
+ * (fused != 0: the fused kernel of a call without a workspace; else the
+ * chain kernel of the two-kernel path).  Each (sequence, value head) chain
+ * runs on one SM, its chunks in order.  With at least as many chains as SMs and long chains,
  * whole chains would leave SMs idle in the last round, so the chains are cut
  * into pieces of piece_chunks chunks and run as `launches` launches of up to
  * ctas_per_launch CTAs: all chains' first pieces, then all second pieces, and
@@ -286,7 +304,8 @@ typedef struct gdn_prefill_plan {
   int64_t piece_chunks;     /* chunks (64 tokens) per piece                  */
   int64_t levels;           /* pieces per chain of max_seq_len tokens        */
   int64_t ctas_per_launch;  /* CTAs of each launch (the last may have fewer) */
-  int64_t launches;         /* chunk-kernel launches (+1 window pass)        */
+  int64_t launches;         /* chain launches (+1 window pass; the two-kernel
+                               path also launches the chunk kernel once)    */
 } gdn_prefill_plan;
 
 /* The plan of one gdn_prefill_chunked call with num_seqs sequences and the
@@ -295,7 +314,7 @@ typedef struct gdn_prefill_plan {
  * Host-only; launches nothing.  GDN_ERR_UNSUPPORTED_SHAPE for a layer on the
  * conv pre-pass path, GDN_ERR_INVALID_ARG for a malformed argument. */
 gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
-                                int32_t num_sms, gdn_prefill_plan* out);
+                                int32_t num_sms, int32_t fused, gdn_prefill_plan* out);
 
 gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
                                const gdn_prefill_args* args, void* workspace,

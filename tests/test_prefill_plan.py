@@ -49,11 +49,12 @@ LENS = [0, 64, 500, 1024, 2048, 8192, 229376]
 SMS = [152, 148, 132, 16]
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "chain"])
 @pytest.mark.parametrize("Hv,N", SHAPES)
-def test_plan_runs_every_piece_once_in_order(Hv, N):
+def test_plan_runs_every_piece_once_in_order(Hv, N, fused):
     sh = inputs.LayerShape(max(1, Hv // 3) if Hv % 3 == 0 else Hv, Hv, 128, 128, block_size=896, chunk_size=64)
     for max_len, sms in itertools.product(LENS, SMS):
-        plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms)
+        plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms, fused)
         assert plan["chains"] == Hv * N
         if plan["levels"] > 1:
             P = plan["piece_chunks"]
@@ -78,11 +79,12 @@ def test_benchmark_shape_plan():
     # 4 x 8,192 tokens of the 27B-shaped layer on 152 SMs: 44-chunk pieces
     # (the last 40), three (level, sequence) pairs of 48 CTAs a launch, 12
     # pairs in 4 launches: ~4 x 44 chunk times against 2 x 128 in one launch
-    plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152)
-    assert plan == {"chains": 192, "piece_chunks": 44, "levels": 3, "ctas_per_launch": 144, "launches": 4}
-    # one long sequence (48 chains) and a large batch (3,072 chains) stay one launch
-    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152)["launches"] == 1
-    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152)["launches"] == 1
+    for fused in (True, False):
+        plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152, fused)
+        assert plan == {"chains": 192, "piece_chunks": 44, "levels": 3, "ctas_per_launch": 144, "launches": 4}
+        # one long sequence (48 chains) and a large batch (3,072 chains) stay one launch
+        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, fused)["launches"] == 1
+        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152, fused)["launches"] == 1
 
 
 def test_plan_rejects_the_scan_path_and_bad_arguments():

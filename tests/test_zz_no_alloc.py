@@ -4,10 +4,11 @@ The allocation-free prefill serves callers that cannot hand the library any
 device memory for scratch (a runtime whose free GPU memory is all reserved for
 its pools, or a C caller without an allocator).  It keeps its scratch in a
 fixed 64 MiB device array of the library instead.  Layers on the tensor-core
-path need no scratch at all; layers on the conv pre-pass path (here d = 64)
-use the array and are limited by it.  This file runs last so that a failure
-here leaves every other test already run; it also passes alone in a fresh
-process, because the first call does the per-device set-up.
+path take the fused kernel, which needs no scratch at all (the same kernel as
+gdn_prefill_chunked without a workspace); layers on the conv pre-pass path
+(here d = 64) use the array and are limited by it.  This file runs last so
+that a failure here leaves every other test already run; it also passes alone
+in a fresh process, because the first call does the per-device set-up.
 """
 import numpy as np
 import pytest
@@ -16,7 +17,7 @@ import torch
 import gated_deltanet_state_gb300 as gdn
 from gated_deltanet_state_gb300 import inputs
 
-from harness import dev
+from harness import assert_out_close, assert_state_close, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -52,9 +53,13 @@ def _run(fn, shape, lens, seed, **extra):
 
 @pytest.mark.parametrize("shape", [SHAPE, SHAPE_SCAN], ids=["tensor_core_path", "pre_pass_path"])
 def test_noalloc_prefill_matches_the_workspace_prefill_on_two_calls_in_a_row(shape):
-    assert gdn.gdn_prefill_workspace_size(shape, len(LENS), sum(LENS)) <= gdn.NOALLOC_SCRATCH_BYTES
+    tc = shape is SHAPE
+    assert tc or gdn.gdn_prefill_workspace_size(shape, len(LENS), sum(LENS)) <= gdn.NOALLOC_SCRATCH_BYTES
+    # the tensor-core layer's allocation-free call is the fused kernel, as is
+    # gdn_prefill_chunked without a workspace
+    extra = {"workspace": False} if tc else {}
     for seed in (41, 42):   # the second call reuses the scratch the first one left
-        o_ref, s_ref = _run(gdn.gdn_prefill_chunked, shape, LENS, seed)
+        o_ref, s_ref = _run(gdn.gdn_prefill_chunked, shape, LENS, seed, **extra)
         o_na, s_na = _run(gdn.gdn_prefill_chunked_noalloc, shape, LENS, seed)
         # the same kernels on the same inputs: the same bits
         assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16))
@@ -62,14 +67,21 @@ def test_noalloc_prefill_matches_the_workspace_prefill_on_two_calls_in_a_row(sha
 
 
 def test_noalloc_prefill_has_no_limit_on_the_tensor_core_path():
-    """8,192 tokens of the 27B-shaped layer: no scratch is needed, so the
-    allocation-free call runs whatever its length, with the same results."""
+    """8,192 tokens of the 27B-shaped layer: the fused kernel needs no scratch,
+    so the allocation-free call runs whatever its length (a workspace prefill
+    of this call would need more than the array holds): the bits of
+    gdn_prefill_chunked without a workspace, and the two-kernel path's
+    results within the parity bounds."""
     T = 8192
-    assert gdn.gdn_prefill_workspace_size(SHAPE, 1, T) == 0
-    o_ref, s_ref = _run(gdn.gdn_prefill_chunked, SHAPE, [T], 43)
+    assert gdn.gdn_prefill_workspace_size(SHAPE, 1, T) > gdn.NOALLOC_SCRATCH_BYTES
+    o_ref, s_ref = _run(gdn.gdn_prefill_chunked, SHAPE, [T], 43, workspace=False)
     o_na, s_na = _run(gdn.gdn_prefill_chunked_noalloc, SHAPE, [T], 43)
     assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16))
     assert torch.equal(s_na.view(torch.int32), s_ref.view(torch.int32))
+    o_2k, s_2k = _run(gdn.gdn_prefill_chunked, SHAPE, [T], 43)
+    assert_out_close(o_na, o_2k.double().numpy(), [0, T])
+    used = [0] + [p for p in range(2, s_2k.shape[0]) if s_2k[p].abs().sum() > 0]
+    assert_state_close(s_na[used], s_2k[used].double().numpy())
 
 
 def test_noalloc_prefill_rejects_calls_beyond_its_scratch():
