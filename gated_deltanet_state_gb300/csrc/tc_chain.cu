@@ -22,16 +22,16 @@
 //   value head of the group the gates, A, P and T, the v conv, and on the
 //   tensor cores U'^T = (V^T diag(b)) T^T and W = [-T diag(b gam); 0] K^.  It
 //   writes, per chunk slot of the workspace, ready-to-load operand images:
-//   W and P (bf16 hi / lo, 128-byte swizzled), U'^T (fp32) and gam, dec per
-//   value head; Q^ and K^T (bf16 hi / lo) per qk head.  No chunk waits for
-//   another, so the whole call's chunks fill every SM.
+//   W, P and K^T diag(dec) (bf16 hi / lo, 128-byte swizzled), U'^T (fp32)
+//   and gam, dec per value head; Q^ (bf16 hi / lo) per qk head.  No chunk
+//   waits for another, so the whole call's chunks fill every SM.
 // tc_chain_kernel: one CTA per (sequence, value head) chain (or a piece of
 //   it, as the fused kernel's schedule cuts them).  The fp32 state stays in
 //   tensor memory; per chunk it splits S0 into bf16 hi / lo parts held in
-//   tensor memory as the A operand, adds S0 W^T onto U'^T and forms S0 Q^T
-//   (tensor cores), splits U into tensor memory, and forms S += U^T diag(dec)
-//   K^ and U^T P^T (tensor cores), then the outputs.  Operand images of the
-//   next chunk load by bulk copies into the second of two buffers meanwhile.
+//   tensor memory as the A operand, adds S0 W^T onto U'^T (tensor cores),
+//   splits U into tensor memory, and forms S += U^T diag(dec) K^, S0 Q^T and
+//   U^T P^T (tensor cores), then the outputs.  The next chunk's operand
+//   images load by bulk copies meanwhile.
 // Chunks start at absolute multiples of 64, so a block boundary is a chunk end
 // and a checkpoint is the tensor-memory state between two chunks: a resume
 // replays the cold run's arithmetic bit for bit.  Every product runs three
@@ -57,7 +57,7 @@ constexpr long long kWaitDefault = 4000000000LL;
 constexpr uint32_t kImgW = 32768;    // W hi | lo: 64 rows (i) x 128 k (c), two 64-wide k-blocks each
 constexpr uint32_t kImgQ = 32768;    // Q^ hi | lo: same shape
 constexpr uint32_t kImgP = 16384;    // P hi | lo: 64 rows (i) x 64 k (j)
-constexpr uint32_t kImgK = 32768;    // K^T hi | lo: 128 rows (c) x 64 k (j)
+constexpr uint32_t kImgK = 32768;    // K^T diag(dec) hi | lo: 128 rows (c) x 64 k (j)
 constexpr uint32_t kImgU = 32768;    // U'^T fp32 [128 r][64 i]
 constexpr uint32_t kImgG = 512;      // gam[64], dec[64] fp32
 
@@ -67,7 +67,7 @@ struct ChunkWs {
   float* u;        // [slots][Hv] kImgU
   float* g;        // [slots][Hv] kImgG
   uint8_t* q;      // [slots][Hqk] kImgQ
-  uint8_t* k;      // [slots][Hqk] kImgK
+  uint8_t* k;      // [slots][Hv] kImgK
   int64_t slots;
 };
 
@@ -87,6 +87,8 @@ struct CkSmem {
   static constexpr uint32_t TF = R1 + 32768;         //     T fp32 [64][64]
   static constexpr uint32_t DT = R1 + 49152;         //     diagonal inverses [4][16][20]
   static constexpr uint32_t NT = R1 + 54272;         //     N blocks [6][16][16]
+  static constexpr uint32_t KD = R1;                 //     K^T diag(dec) hi [128][64], lo at +16 KB (after T)
+  static constexpr uint32_t KD_LO = R1 + 16384;
   static constexpr uint32_t R2 = 65536;              // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t KQ = R2;
   static constexpr uint32_t KQ_LO = R2 + 32768;
@@ -119,19 +121,27 @@ constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = 
 constexpr uint32_t kCkU = 128;      // U'^T, lane = channel r, column = row i
 constexpr uint32_t kCkW = 256;      // W, lanes 0-63 = row i, 128 columns c
 
-// ---- shared memory of the chain kernel: two buffers of one chunk's images --
+// ---- shared memory of the chain kernel: one chunk's images in flight while
+// the chunk before it reads its own (W, P, K~ in two buffers; Q^ and U'^T in
+// one, reloaded as soon as their reader is done) --------------------------------
 struct ChSmem {
-  static constexpr uint32_t W = 0;                   // W hi [2][64][64], lo at +16 KB
-  static constexpr uint32_t Q = 32768;               // Q^ hi | lo
-  static constexpr uint32_t P = 65536;               // P hi | lo
-  static constexpr uint32_t K = 81920;               // K^T hi | lo, turned into (K^T diag(dec)) in place
-  static constexpr uint32_t BUF = 114688;            // bytes of one buffer (1024-aligned)
-  static constexpr uint32_t G = 2 * BUF;             // gam | dec of each buffer [2][128] fp32
-  static constexpr uint32_t MBAR = G + 2 * kImgG;    // [0,1] images of buffer 0 / 1, [2] U, [3] SQ, [4] S, [5] UP
-  static constexpr uint32_t TSLOT = MBAR + 48;
+  static constexpr uint32_t W = 0;                   // W hi | lo [2 buffers], kImgW each
+  static constexpr uint32_t Q = 2 * kImgW;           // Q^ hi | lo
+  static constexpr uint32_t P = Q + kImgQ;           // P hi | lo [2]
+  static constexpr uint32_t K = P + 2 * kImgP;       // K^T diag(dec) hi | lo [2]
+  static constexpr uint32_t U = K + 2 * kImgK;       // U'^T fp32 [128][64]
+  static constexpr uint32_t G = U + kImgU;           // gam | dec [2]
+  static constexpr uint32_t MBAR = G + 2 * kImgG;
+  // mbarriers: W [2], Q, P | K~ | gates [2], U'^T, then the products
+  // S0 W^T, S0 Q^T, the state update, U^T P^T
+  static constexpr int kW = 0, kQ = 2, kPK = 3, kUl = 5, kU = 6, kSQ = 7, kS = 8, kUP = 9, kBars = 10;
+  static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]
+  static constexpr uint32_t TSLOT = ARMED + 8 * kBars;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
 };
+static_assert(ChSmem::W % 1024 == 0 && ChSmem::Q % 1024 == 0 && ChSmem::P % 1024 == 0 && ChSmem::K % 1024 == 0,
+              "operand images must be 1024-byte aligned");
 static_assert(ChSmem::ALLOC <= 232448, "chain kernel shared memory exceeds the per-CTA limit");
 
 // tensor-memory columns of the chain kernel (lane = state row r)
@@ -418,14 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          sbase + CkSmem::KQ, sbase + CkSmem::KQ_LO, tc::idesc_bf16_f32(128, 64),
                                          false);
     tc::mma_commit(mbar + 0);
-    // the qk head's images for the chain: Q^ (rows 64-127 of [K^; Q^]) and K^T
+    // the qk head's image for the chain: Q^ (rows 64-127 of [K^; Q^])
     uint8_t* qdst = ws.q + (slot * p.Hqk + jq) * (int64_t)kImgQ;
 #pragma unroll
     for (int part = 0; part < 2; ++part)
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
         tc::bulk_store(qdst + part * 16384 + kb * 8192, sm + CkSmem::KQ + part * 32768 + kb * 16384 + 8192, 8192);
-    tc::bulk_store(ws.k + (slot * p.Hqk + jq) * (int64_t)kImgK, sm + CkSmem::KT, kImgK);
     tc::bulk_commit();
   }
   if (ok) gram_pending = true;
@@ -554,6 +563,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     prod_pending = true;
     if (worker) {
+      // K^T diag(dec) for the chain's state update, into the T work area
+      // (free now): row `row` (k channel), rows i in [16 (tid >> 7), +16)
+      {
+        const float* dec = Gs + 128;
+        const int i0 = 16 * (tid >> 7);
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
+          const uint4 vh = *reinterpret_cast<const uint4*>(sm + CkSmem::KT + off);
+          const uint4 vl = *reinterpret_cast<const uint4*>(sm + CkSmem::KT_LO + off);
+          const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float a0 = __uint_as_float(wh[u] << 16) + __uint_as_float(wl[u] << 16);
+            const float a1 = __uint_as_float(wh[u] & 0xFFFF0000u) + __uint_as_float(wl[u] & 0xFFFF0000u);
+            e[2 * u] = a0 * dec[i0 + 8 * c8 + 2 * u];
+            e[2 * u + 1] = a1 * dec[i0 + 8 * c8 + 2 * u + 1];
+          }
+          tc::store_split8(sm + CkSmem::KD + off, sm + CkSmem::KD_LO + off, e);
+        }
+      }
       const uint32_t par = (uint32_t)(g & 1);
       mma_wait(mbar + 1, par, ok, wlim);
       // U'^T of channel `row`, rows [16 quarter, +16) -> the workspace (fp32 [r][i])
@@ -586,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t hv = slot * p.Hv + h;
       tc::bulk_store(ws.w + hv * kImgW, sm + CkSmem::WB, kImgW);
       tc::bulk_store(ws.pm + hv * kImgP, sm + CkSmem::PB, kImgP);
+      tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KD, kImgK);
       // gam | dec of the head for the chain (G and b are folded into W, U', P)
       tc::bulk_store(ws.g + hv * (kImgG / 4), Gs + 64, 256);
       tc::bulk_store(ws.g + hv * (kImgG / 4) + 64, Gs + 128, 256);
@@ -618,6 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 // Chain kernel: grid (Hv, pieces), one CTA per (value head, (level, sequence))
 // ============================================================================
+// Per chunk c the tensor pipe runs, in issue order, S0 W^T (onto U'^T), then
+// after the U split S += U^T K~ (the state update the next chunk waits for),
+// S0 Q^T and U^T P^T.  The workers split the next state while the last two
+// still run (they write the S0 operand only once S0 Q^T has read the old
+// one), and form chunk c's outputs while the next chunk's S0 W^T runs.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chain_kernel(const ScanParams p, const ChunkWs ws, const PieceMap pm, int64_t max_chunks) {
   using TOUT = __nv_bfloat16;
@@ -654,11 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   const long long wlim = wait_limit(p);
   const int64_t row0 = p.cu_seqlens[s];
+  const int hq = h / (p.Hv / p.Hqk);
 
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + ChSmem::MBAR);
+  int64_t* armed = reinterpret_cast<int64_t*>(sm + ChSmem::ARMED);   // last chunk each mbarrier was armed for
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + ChSmem::TSLOT);
 
   if (warp == 0) {
@@ -667,7 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
 #pragma unroll
-    for (int b = 0; b < 6; ++b) tc::mbar_init(mbar + b, 1);
+    for (int k = 0; k < ChSmem::kBars; ++k) {
+      tc::mbar_init(mbar + k, 1);
+      armed[k] = -1;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   tc::fence_before_sync();
@@ -676,36 +718,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
   const uint32_t tS = tbase + tlane + kChS + 32 * quarter;
 
-  // chunk c's images into buffer c & 1 (issuing thread)
-  auto load_chunk = [&](int64_t c) {
+  // the issuing thread's loads of chunk c's images (each arms its mbarrier)
+  auto hv_of = [&](int64_t c) { return chunk_slot(p, s, c) * p.Hv + h; };
+  auto load_w = [&](int64_t c) {
     const int b = (int)(c & 1);
-    const int64_t slot = chunk_slot(p, s, c);
-    const int64_t hv = slot * p.Hv + h;
-    const int64_t hq = slot * p.Hqk + h / (p.Hv / p.Hqk);
-    uint8_t* dst = sm + b * ChSmem::BUF;
-    uint64_t* m = mbar + b;
-    tc::mbar_expect_tx(m, kImgW + kImgQ + kImgP + kImgK + kImgG);
-    tc::bulk_load(dst + ChSmem::W, ws.w + hv * kImgW, kImgW, m);
-    tc::bulk_load(dst + ChSmem::Q, ws.q + hq * kImgQ, kImgQ, m);
-    tc::bulk_load(dst + ChSmem::P, ws.pm + hv * kImgP, kImgP, m);
-    tc::bulk_load(dst + ChSmem::K, ws.k + hq * kImgK, kImgK, m);
+    tc::mbar_expect_tx(mbar + ChSmem::kW + b, kImgW);
+    tc::bulk_load(sm + ChSmem::W + b * kImgW, ws.w + hv_of(c) * kImgW, kImgW, mbar + ChSmem::kW + b);
+    armed[ChSmem::kW + b] = c;
+  };
+  auto load_q = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kQ, kImgQ);
+    tc::bulk_load(sm + ChSmem::Q, ws.q + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgQ, kImgQ, mbar + ChSmem::kQ);
+    armed[ChSmem::kQ] = c;
+  };
+  auto load_pk = [&](int64_t c) {
+    const int b = (int)(c & 1);
+    const int64_t hv = hv_of(c);
+    uint64_t* m = mbar + ChSmem::kPK + b;
+    tc::mbar_expect_tx(m, kImgP + kImgK + kImgG);
+    tc::bulk_load(sm + ChSmem::P + b * kImgP, ws.pm + hv * kImgP, kImgP, m);
+    tc::bulk_load(sm + ChSmem::K + b * kImgK, ws.k + hv * kImgK, kImgK, m);
     tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv * (kImgG / 4), kImgG, m);
+    armed[ChSmem::kPK + b] = c;
   };
-  // U'^T of chunk c, this thread's row and 16 columns, from the workspace
-  auto load_u = [&](int64_t c, float (&u)[16]) {
-    const float4* src = reinterpret_cast<const float4*>(
-        ws.u + (chunk_slot(p, s, c) * p.Hv + h) * (int64_t)(kImgU / 4) + row * 64 + 16 * quarter);
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const float4 v = ldg_f4_fresh(reinterpret_cast<const float*>(src + c4));
-      u[4 * c4] = v.x; u[4 * c4 + 1] = v.y; u[4 * c4 + 2] = v.z; u[4 * c4 + 3] = v.w;
-    }
+  auto load_u = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kUl, kImgU);
+    tc::bulk_load(sm + ChSmem::U, ws.u + hv_of(c) * (kImgU / 4), kImgU, mbar + ChSmem::kUl);
+    armed[ChSmem::kUl] = c;
   };
+  // gam_C of chunk c (the decay of the whole chunk), read ahead by every worker
+  auto gam_c = [&](int64_t c) { return __ldg(ws.g + hv_of(c) * (kImgG / 4) + (C - 1)); };
 
-  int64_t load_issued = -1;   // the last chunk whose images were requested
-  if (tid == kMma && cb < ce) load_chunk(cb);
-  if (cb < ce) load_issued = cb;
-  float un[16];
+  if (tid == kMma && cb < ce) {
+    load_w(cb);
+    load_q(cb);
+    load_pk(cb);
+    load_u(cb);
+  }
+  float gC = 0.f;
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
     const float* src = from >= 0 ? page_state(p.pool, from) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
@@ -717,99 +767,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::tmem_st32(tS, v);
     tc::tmem_st_wait();
-    if (cb < ce) load_u(cb, un);
+    if (cb < ce) gC = gam_c(cb);
   }
 
-  int32_t pend = -1;        // checkpoint page due at the next read of S
+  // outputs of chunk c: o_i = gam_i (S0 q^_i) + (U^T P^T)_i, rows i in [16 quarter, +16)
+  auto outputs = [&](int64_t c, bool& okr) {
+    const uint32_t par = (uint32_t)((c - cb) & 1);
+    mma_wait(mbar + ChSmem::kSQ, par, okr, wlim);
+    mma_wait(mbar + ChSmem::kUP, par, okr, wlim);
+    const float* gam = reinterpret_cast<const float*>(sm + ChSmem::G + (int)(c & 1) * kImgG);
+    const int64_t t0 = c * C;
+    const int cnt = (int)(n - t0 < C ? n - t0 : C);
+    float sq[16], up[16];
+    tc::tmem_ld16x2(tbase + tlane + kChSQ + 16 * quarter, tbase + tlane + kChUP + 16 * quarter, sq, up);
+    TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
+    const int64_t tstride = (int64_t)p.Hv * D;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int i = 16 * quarter + e;
+      if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
+    }
+  };
+  // the checkpoint page of a block boundary at absolute position pos (-1: none)
+  auto boundary_page = [&](int64_t pos) {
+    int32_t page = -1;
+    if (pos % p.block_size == 0) {
+      const int64_t jb = pos / p.block_size - 1;
+      if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
+      else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+      if (page >= 0 && !page_ok(p.pool, page)) {
+        if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
+        page = -1;
+      }
+    }
+    return page;
+  };
+
   bool ok = true;
-  uint32_t issued = 0;      // products committed in the current chunk (bit: mbar index)
-  bool s_pending = false;   // the previous chunk's state update may still run
   int64_t c = cb;
   for (; c < ce; ++c) {
     const int b = (int)(c & 1);
     const uint32_t par = (uint32_t)((c - cb) & 1);
     const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
-    const int64_t t0 = c * C;
-    const int cnt = (int)(n - t0 < C ? n - t0 : C);
-    const float* gsm = reinterpret_cast<const float*>(sm + ChSmem::G + b * kImgG);   // gam[64], dec[64]
-    uint8_t* buf = sm + b * ChSmem::BUF;
-    issued = 0;
     if (worker) {
-      // ---- S0: wait for the state update, checkpoint, split into tensor memory,
-      // gam_C S0 back; U'^T of this chunk into the U columns
-      if (s_pending) mma_wait(mbar + 4, par ^ 1u, ok, wlim);
-      ok = work_wait(mbar + b, bpar, wlim) && ok;   // this chunk's images (gam_C)
-      const float gC = gsm[C - 1];
-      float v0[32];
-      tc::tmem_ld32(tS, v0);
-      if (pend >= 0) {
-        float* ck = page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter;
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          reinterpret_cast<float4*>(ck)[c4] = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
-      }
+      // ---- S0: the state after chunk c - 1 (its update done), checkpointed at
+      // a block boundary; gam_C S0 back into S; S0 split into tensor memory
+      // once S0 Q^T of chunk c - 1 has read the old split; U'^T of chunk c
+      if (c > cb) mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
+      const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
+      float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
       uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) tc::split_pair(v0[2 * e], v0[2 * e + 1], hi[e], lo[e]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float v0[16];
+        tc::tmem_ld16(tS + 16 * hh, v0);
+        if (ckp) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            reinterpret_cast<float4*>(ckp + 16 * hh)[c4] =
+                make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tc::split_pair(v0[2 * e], v0[2 * e + 1], hi[8 * hh + e], lo[8 * hh + e]);
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+          v0[e] = gg.x;
+          v0[e + 1] = gg.y;
+        }
+        tc::tmem_st16(tS + 16 * hh, v0);
+      }
+      if (c > cb) mma_wait(mbar + ChSmem::kSQ, par ^ 1u, ok, wlim);
       tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
       tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
+      ok = work_wait(mbar + ChSmem::kUl, par, wlim) && ok;
+      {
+        const float4* us = reinterpret_cast<const float4*>(sm + ChSmem::U) + (row * 64 + 16 * quarter) / 4;
+        float u[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
-        v0[e] = gg.x;
-        v0[e + 1] = gg.y;
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 f = us[c4];
+          u[4 * c4] = f.x; u[4 * c4 + 1] = f.y; u[4 * c4 + 2] = f.z; u[4 * c4 + 3] = f.w;
+        }
+        tc::tmem_st16(tbase + tlane + kChU + 16 * quarter, u);
       }
-      tc::tmem_st32(tS, v0);
-      tc::tmem_st16(tbase + tlane + kChU + 16 * quarter, un);
       tc::tmem_st_wait();
-      pend = -1;
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
-    s_pending = false;
     if (tid == kMma) {
-      // the next chunk's images into the other buffer (its last reader, the
-      // chunk before this one, has finished)
-      if (c + 1 < ce) load_chunk(c + 1);
-      // this chunk's images, observed by the thread whose products read them
-      ok = work_wait(mbar + b, bpar, wlim) && ok;
-      // U += S0 W^T (M 128, N 64, K 128) onto U'^T; S0 Q^T (M 128, N 64, K 128)
-      tc::mma3_ts<D / 16, 8192>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + b * ChSmem::BUF + ChSmem::W,
-                                sbase + b * ChSmem::BUF + ChSmem::W + 16384, tc::idesc_bf16_f32(128, 64), true);
-      tc::mma_commit(mbar + 2);
-      tc::mma3_ts<D / 16, 8192>(tbase + kChSQ, tbase + kChS0H, tbase + kChS0L, sbase + b * ChSmem::BUF + ChSmem::Q,
-                                sbase + b * ChSmem::BUF + ChSmem::Q + 16384, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + 3);
-    }
-    if (c + 1 < ce) load_issued = c + 1;
-    issued |= 4u | 8u;
-    if (worker) {
-      // K^T -> K^T diag(dec) in place: row `row` (k channel), rows i in [16 (tid >> 7), +16)
-      {
-        const int i0 = 16 * (tid >> 7);
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
-          uint8_t* ph = buf + ChSmem::K + off;
-          uint8_t* pl = buf + ChSmem::K + 16384 + off;
-          const uint4 vh = *reinterpret_cast<const uint4*>(ph);
-          const uint4 vl = *reinterpret_cast<const uint4*>(pl);
-          const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float a0 = __uint_as_float(wh[u] << 16) + __uint_as_float(wl[u] << 16);
-            const float a1 = __uint_as_float(wh[u] & 0xFFFF0000u) + __uint_as_float(wl[u] & 0xFFFF0000u);
-            e[2 * u] = a0 * gsm[64 + i0 + 8 * c8 + 2 * u];
-            e[2 * u + 1] = a1 * gsm[64 + i0 + 8 * c8 + 2 * u + 1];
-          }
-          tc::store_split8(ph, pl, e);
-        }
-        tc::fence_async_smem();
+      // U += S0 W^T (M 128, N 64, K 128) onto U'^T
+      ok = work_wait(mbar + ChSmem::kW + b, bpar, wlim) && ok;
+      tc::mma3_ts<D / 16, 8192>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::W + b * kImgW,
+                                sbase + ChSmem::W + b * kImgW + 16384, tc::idesc_bf16_f32(128, 64), true);
+      tc::mma_commit(mbar + ChSmem::kU);
+      armed[ChSmem::kU] = c;
+      // the next chunk's W (its buffer's last reader was chunk c - 1) and U'^T
+      // (this chunk's has gone into tensor memory)
+      if (c + 1 < ce) {
+        load_w(c + 1);
+        load_u(c + 1);
       }
-      // ---- U: wait for U'^T + S0 W^T, split into tensor memory (the A operand
-      // of the state update and of U^T P^T)
-      mma_wait(mbar + 2, par, ok, wlim);
+    }
+    if (worker) {
+      // ---- the previous chunk's outputs while S0 W^T runs, then U: split
+      // into tensor memory (the A operand of the state update and U^T P^T)
+      if (c > cb) outputs(c - 1, ok);
+      if (c + 1 < ce) gC = gam_c(c + 1);
+      mma_wait(mbar + ChSmem::kU, par, ok, wlim);
       float u[16];
       tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
       uint32_t hi[8], lo[8];
@@ -822,77 +887,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64) first: the next chunk waits for it;
-      // then U^T P^T (M 128, N 64, K 64)
-      tc::mma3_ts<C / 16, 0>(tbase + kChS, tbase + kChUH, tbase + kChUL, sbase + b * ChSmem::BUF + ChSmem::K,
-                             sbase + b * ChSmem::BUF + ChSmem::K + 16384, tc::idesc_bf16_f32(128, 128), true);
-      tc::mma_commit(mbar + 4);
-      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + b * ChSmem::BUF + ChSmem::P,
-                             sbase + b * ChSmem::BUF + ChSmem::P + 8192, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + 5);
-    }
-    issued |= 16u | 32u;
-    s_pending = true;
-    if (worker) {
-      // the next chunk's U'^T, while the products run
-      if (c + 1 < ce) load_u(c + 1, un);
-      mma_wait(mbar + 3, par, ok, wlim);
-      mma_wait(mbar + 5, par, ok, wlim);
-      // outputs o_i = gam_i (S0 q^_i) + (U^T P^T)_i, rows i in [16 quarter, +16)
-      float sq[16], up[16];
-      tc::tmem_ld16x2(tbase + tlane + kChSQ + 16 * quarter, tbase + tlane + kChUP + 16 * quarter, sq, up);
-      TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
-      const int64_t tstride = (int64_t)p.Hv * D;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int i = 16 * quarter + e;
-        if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gsm[i], sq[e], up[e]));
-      }
-      // a block boundary at this chunk's end: checkpointed at the next read of S
-      const int64_t pos = start + t0 + cnt;
-      if (pos % p.block_size == 0) {
-        const int64_t jb = pos / p.block_size - 1;
-        int32_t page = -1;
-        if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
-        else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
-        if (page >= 0) {
-          if (page_ok(p.pool, page)) pend = page;
-          else if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
-        }
+      // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64), S0 Q^T, U^T P^T (M 128, N 64)
+      ok = work_wait(mbar + ChSmem::kPK + b, bpar, wlim) && ok;
+      tc::mma3_ts<C / 16, 0>(tbase + kChS, tbase + kChUH, tbase + kChUL, sbase + ChSmem::K + b * kImgK,
+                             sbase + ChSmem::K + b * kImgK + 16384, tc::idesc_bf16_f32(128, 128), true);
+      tc::mma_commit(mbar + ChSmem::kS);
+      ok = work_wait(mbar + ChSmem::kQ, par, wlim) && ok;
+      tc::mma3_ts<D / 16, 8192>(tbase + kChSQ, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::Q,
+                                sbase + ChSmem::Q + 16384, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + ChSmem::kSQ);
+      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + ChSmem::P + b * kImgP,
+                             sbase + ChSmem::P + b * kImgP + 8192, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + ChSmem::kUP);
+      armed[ChSmem::kS] = armed[ChSmem::kSQ] = armed[ChSmem::kUP] = c;
+      if (c + 1 < ce) {
+        // the next chunk's P, K~ and gates (their buffer's last readers, chunk
+        // c - 1's products and outputs, have finished); its Q^ once S0 Q^T
+        // has read this chunk's
+        load_pk(c + 1);
+        if (work_wait(mbar + ChSmem::kSQ, par, wlim)) load_q(c + 1);
+        else ok = false;
       }
     }
   }
 
-  const int64_t ci = c < ce ? c : ce - 1;   // the chunk `issued` refers to
-  if (ok && worker && s_pending) mma_wait(mbar + 4, (uint32_t)((ce - 1 - cb) & 1), ok, wlim);
+  if (ok && c > cb) {
+    if (worker) {
+      outputs(c - 1, ok);
+      mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
+    }
+  }
   ok = cta_sync_ok(ok);
   if (ok) {
     if (worker) {
-      // final state (and a checkpoint due at the last chunk's end)
+      // final state (and the checkpoint of a boundary at the piece's end)
+      const int32_t ck = ce > cb ? boundary_page(start + (ce - 1) * C + (n - (ce - 1) * C < C ? n - (ce - 1) * C : C))
+                                 : -1;
       float* dst = page_state(p.pool, final_page) + ((int64_t)h * D + row) * D + 32 * quarter;
-      float* ck = pend >= 0 ? page_state(p.pool, pend) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
+      float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
       float v0[32];
       tc::tmem_ld32(tS, v0);
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 f0 = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
         reinterpret_cast<float4*>(dst)[c4] = f0;
-        if (ck) reinterpret_cast<float4*>(ck)[c4] = f0;
+        if (ckp) reinterpret_cast<float4*>(ckp)[c4] = f0;
       }
     }
-  } else if (cb < ce) {
-    // a wait ran out: report it, give every product and copy in flight one
-    // more wait with the default bound, release the tensor memory
+  } else {
+    // a wait ran out: report it, give every copy and product armed so far one
+    // more wait with the default bound (the last phase each mbarrier was armed
+    // for; none is armed past it), release the tensor memory
     if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);
     if (worker) {
-      const uint32_t par = (uint32_t)((ci - cb) & 1);
 #pragma unroll 1
-      for (int k = 2; k < 6; ++k)
-        if (issued & (1u << k)) tc::mbar_wait_bounded(mbar + k, par, kWaitDefault);
-      if (!(issued & 16u) && s_pending && ci > cb) tc::mbar_wait_bounded(mbar + 4, par ^ 1u, kWaitDefault);
-      // image loads: the last one requested, and the one before it
-      for (int64_t lc = load_issued - 1; lc <= load_issued; ++lc)
-        if (lc >= cb) tc::mbar_wait_bounded(mbar + (lc & 1), (uint32_t)(((lc - cb) >> 1) & 1), kWaitDefault);
+      for (int k = 0; k < ChSmem::kBars; ++k) {
+        const int64_t a = armed[k];
+        if (a < cb) continue;
+        const bool two = k == ChSmem::kW || k == ChSmem::kW + 1 || k == ChSmem::kPK || k == ChSmem::kPK + 1;
+        const uint32_t ph = (uint32_t)((two ? (a - cb) >> 1 : a - cb) & 1);
+        tc::mbar_wait_bounded(mbar + k, ph, kWaitDefault);
+      }
     }
   }
   tc::fence_before_sync();
@@ -905,8 +960,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
   const int64_t slots = total_tokens / kC + num_seqs + 1;
-  const int64_t per_v = (int64_t)kImgW + kImgP + kImgU + kImgG;
-  const int64_t per_q = (int64_t)kImgQ + kImgK;
+  const int64_t per_v = (int64_t)kImgW + kImgP + kImgU + kImgK + kImgG;
+  const int64_t per_q = (int64_t)kImgQ;
   return (size_t)(slots * (Hv * per_v + Hqk * per_q)) + 1024;
 }
 
@@ -924,7 +979,7 @@ ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total
   w.pm = take(w.slots * Hv * (int64_t)kImgP);
   w.u = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgU));
   w.q = take(w.slots * Hqk * (int64_t)kImgQ);
-  w.k = take(w.slots * Hqk * (int64_t)kImgK);
+  w.k = take(w.slots * Hv * (int64_t)kImgK);
   w.g = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgG));
   return w;
 }
