@@ -121,36 +121,38 @@ constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = 
 constexpr uint32_t kCkU = 128;      // U'^T, lane = channel r, column = row i
 constexpr uint32_t kCkW = 256;      // W, lanes 0-63 = row i, 128 columns c
 
-// ---- shared memory of the chain kernel: one chunk's images in flight while
-// the chunk before it reads its own (W, P, K~ in two buffers; Q^ and U'^T in
-// one, reloaded as soon as their reader is done) --------------------------------
+// ---- shared memory of the chain kernel ---------------------------------------
+// G1 = the B operand of S0 [W; Q^]^T (128 rows: W, then Q^; K = 128 in two
+// 64-wide blocks) in two buffers; G2 = the B operand of U^T [P; K~]^T (192
+// rows: P, then K^T diag(dec); K = 64) in one, reloaded once the state update
+// has read it; U'^T; the output tile; the gates of two chunks.
 struct ChSmem {
-  static constexpr uint32_t W = 0;                   // W hi | lo [2 buffers], kImgW each
-  static constexpr uint32_t Q = 2 * kImgW;           // Q^ hi | lo
-  static constexpr uint32_t P = Q + kImgQ;           // P hi | lo [2]
-  static constexpr uint32_t K = P + 2 * kImgP;       // K^T diag(dec) hi | lo [2]
-  static constexpr uint32_t U = K + 2 * kImgK;       // U'^T fp32 [128][64]
-  static constexpr uint32_t G = U + kImgU;           // gam | dec [2]
+  static constexpr uint32_t kG1 = 65536;             // bytes of one G1 buffer: hi 32 KB, lo 32 KB
+  static constexpr uint32_t kG2 = 49152;             // G2: hi 24 KB, lo 24 KB
+  static constexpr uint32_t G1 = 0;
+  static constexpr uint32_t G2 = 2 * kG1;
+  static constexpr uint32_t U = G2 + kG2;            // U'^T fp32 [128][64]
+  static constexpr uint32_t OT = U + kImgU;          // outputs bf16 [64 rows][128 dv]
+  static constexpr uint32_t G = OT + 16384;          // gam | dec [2]
   static constexpr uint32_t MBAR = G + 2 * kImgG;
-  // mbarriers: W [2], Q, P | K~ | gates [2], U'^T, then the products
-  // S0 W^T, S0 Q^T, the state update, U^T P^T
-  static constexpr int kW = 0, kQ = 2, kPK = 3, kUl = 5, kU = 6, kSQ = 7, kS = 8, kUP = 9, kBars = 10;
-  static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]
+  // mbarriers: G1 [2], U'^T, G2 + gates, then the products S0 [W; Q^]^T and U^T [P; K~]^T
+  static constexpr int kG1b = 0, kUl = 2, kPK = 3, kU = 4, kS = 5, kBars = 6;
+  static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]: last chunk each was armed for
   static constexpr uint32_t TSLOT = ARMED + 8 * kBars;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
 };
-static_assert(ChSmem::W % 1024 == 0 && ChSmem::Q % 1024 == 0 && ChSmem::P % 1024 == 0 && ChSmem::K % 1024 == 0,
-              "operand images must be 1024-byte aligned");
+static_assert(ChSmem::G2 % 1024 == 0 && ChSmem::U % 16 == 0 && ChSmem::OT % 1024 == 0, "operand alignment");
 static_assert(ChSmem::ALLOC <= 232448, "chain kernel shared memory exceeds the per-CTA limit");
 
-// tensor-memory columns of the chain kernel (lane = state row r)
-constexpr uint32_t kChS = 0;        // S fp32 [128][128]
-constexpr uint32_t kChS0H = 128;    // S0 hi, bf16 pairs [128][64]
-constexpr uint32_t kChS0L = 192;    // S0 lo
-constexpr uint32_t kChU = 256;      // U'^T + S0 W^T fp32 [128][64]
-constexpr uint32_t kChSQ = 320;     // S0 Q^T fp32
-constexpr uint32_t kChUP = 384;     // U^T P^T fp32
+// tensor-memory columns of the chain kernel (lane = state row r): the first
+// product writes [U | SQ], the second [UP | S], so each is one wide MMA
+constexpr uint32_t kChU = 0;        // U'^T + S0 W^T fp32 [128][64]
+constexpr uint32_t kChSQ = 64;      // S0 Q^T fp32
+constexpr uint32_t kChUP = 128;     // U^T P^T fp32
+constexpr uint32_t kChS = 192;      // S fp32 [128][128]
+constexpr uint32_t kChS0H = 320;    // S0 hi, bf16 pairs [128][64]
+constexpr uint32_t kChS0L = 384;    // S0 lo
 constexpr uint32_t kChUH = 448;     // U^T hi, bf16 pairs [128][32]
 constexpr uint32_t kChUL = 480;     // U^T lo
 
@@ -650,13 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 // Chain kernel: grid (Hv, pieces), one CTA per (value head, (level, sequence))
 // ============================================================================
-// Per chunk c the tensor pipe runs, in issue order, S0 W^T (onto U'^T), then
-// after the U split S += U^T K~ (the state update the next chunk waits for),
-// S0 Q^T and U^T P^T.  The workers split the next state while the last two
-// still run (they write the S0 operand only once S0 Q^T has read the old
-// one), and form chunk c's outputs while the next chunk's S0 W^T runs.
+// Per chunk c the tensor pipe runs two wide products: G1 = S0 [W; Q^]^T onto
+// [U'^T | 0] (M 128, N 128, K 128) and, after the U split, G2 = U^T [P; K~]^T
+// onto [0 | gam_C S0] (M 128, N 192, K 64), which yields U^T P^T and the next
+// state together.  Between them the workers split U and keep gam (S0 Q^T) of
+// the chunk in registers; the outputs gam (S0 Q^T) + U^T P^T go out through a
+// shared-memory tile once G2 is done, while the next state is split.
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_chain_kernel(const ScanParams p, const ChunkWs ws, const PieceMap pm, int64_t max_chunks) {
+    tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws,
+                    const PieceMap pm, int64_t max_chunks) {
   using TOUT = __nv_bfloat16;
   constexpr int D = kD, C = kC;
   const int h = blockIdx.x;
@@ -697,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + ChSmem::MBAR);
-  int64_t* armed = reinterpret_cast<int64_t*>(sm + ChSmem::ARMED);   // last chunk each mbarrier was armed for
+  int64_t* armed = reinterpret_cast<int64_t*>(sm + ChSmem::ARMED);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + ChSmem::TSLOT);
+  TOUT* ot = reinterpret_cast<TOUT*>(sm + ChSmem::OT);
 
   if (warp == 0) {
     tc::tmem_alloc(tslot, kTmemCols);
@@ -720,26 +725,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // the issuing thread's loads of chunk c's images (each arms its mbarrier)
   auto hv_of = [&](int64_t c) { return chunk_slot(p, s, c) * p.Hv + h; };
-  auto load_w = [&](int64_t c) {
+  auto load_g1 = [&](int64_t c) {
     const int b = (int)(c & 1);
-    tc::mbar_expect_tx(mbar + ChSmem::kW + b, kImgW);
-    tc::bulk_load(sm + ChSmem::W + b * kImgW, ws.w + hv_of(c) * kImgW, kImgW, mbar + ChSmem::kW + b);
-    armed[ChSmem::kW + b] = c;
+    uint64_t* m = mbar + ChSmem::kG1b + b;
+    uint8_t* dst = sm + ChSmem::G1 + b * ChSmem::kG1;
+    const uint8_t* w = ws.w + hv_of(c) * kImgW;
+    const uint8_t* q = ws.q + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgQ;
+    tc::mbar_expect_tx(m, kImgW + kImgQ);
+    // [W; Q^] as one 128-row operand: each 64-wide K-block holds W's 64 rows, then Q^'s
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        tc::bulk_load(dst + part * 32768 + kb * 16384, w + part * 16384 + kb * 8192, 8192, m);
+        tc::bulk_load(dst + part * 32768 + kb * 16384 + 8192, q + part * 16384 + kb * 8192, 8192, m);
+      }
+    armed[ChSmem::kG1b + b] = c;
   };
-  auto load_q = [&](int64_t c) {
-    tc::mbar_expect_tx(mbar + ChSmem::kQ, kImgQ);
-    tc::bulk_load(sm + ChSmem::Q, ws.q + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgQ, kImgQ, mbar + ChSmem::kQ);
-    armed[ChSmem::kQ] = c;
-  };
-  auto load_pk = [&](int64_t c) {
-    const int b = (int)(c & 1);
+  auto load_g2 = [&](int64_t c) {
     const int64_t hv = hv_of(c);
-    uint64_t* m = mbar + ChSmem::kPK + b;
+    uint64_t* m = mbar + ChSmem::kPK;
+    uint8_t* dst = sm + ChSmem::G2;
     tc::mbar_expect_tx(m, kImgP + kImgK + kImgG);
-    tc::bulk_load(sm + ChSmem::P + b * kImgP, ws.pm + hv * kImgP, kImgP, m);
-    tc::bulk_load(sm + ChSmem::K + b * kImgK, ws.k + hv * kImgK, kImgK, m);
-    tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv * (kImgG / 4), kImgG, m);
-    armed[ChSmem::kPK + b] = c;
+    // [P; K~] as one 192-row operand (K = 64): P's 64 rows, then K~'s 128
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      tc::bulk_load(dst + part * 24576, ws.pm + hv * kImgP + part * 8192, 8192, m);
+      tc::bulk_load(dst + part * 24576 + 8192, ws.k + hv * kImgK + part * 16384, 16384, m);
+    }
+    tc::bulk_load(sm + ChSmem::G + (int)(c & 1) * kImgG, ws.g + hv * (kImgG / 4), kImgG, m);
+    armed[ChSmem::kPK] = c;
   };
   auto load_u = [&](int64_t c) {
     tc::mbar_expect_tx(mbar + ChSmem::kUl, kImgU);
@@ -748,12 +763,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // gam_C of chunk c (the decay of the whole chunk), read ahead by every worker
   auto gam_c = [&](int64_t c) { return __ldg(ws.g + hv_of(c) * (kImgG / 4) + (C - 1)); };
+  // the checkpoint page of a block boundary at absolute position pos (-1: none)
+  auto boundary_page = [&](int64_t pos) {
+    int32_t page = -1;
+    if (pos % p.block_size == 0) {
+      const int64_t jb = pos / p.block_size - 1;
+      if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
+      else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
+      if (page >= 0 && !page_ok(p.pool, page)) {
+        if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
+        page = -1;
+      }
+    }
+    return page;
+  };
+  auto full_chunk = [&](int64_t c) { return n - c * C >= C; };
+  // outputs of chunk c from t = gam (S0 Q^T) and U^T P^T (rows i in [16 quarter, +16)):
+  // a full chunk into the tile (one TMA store), a partial one by plain stores
+  auto outputs = [&](int64_t c, const float (&t)[16]) {
+    float up[16];
+    tc::tmem_ld16(tbase + tlane + kChUP + 16 * quarter, up);
+    if (tma_out && full_chunk(c)) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ot[(16 * quarter + e) * D + row] = from_f32<TOUT>(t[e] + up[e]);
+    } else {
+      const int64_t t0 = c * C;
+      const int cnt = (int)(n - t0 < C ? n - t0 : C);
+      TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int i = 16 * quarter + e;
+        if (i < cnt) out[(int64_t)i * p.Hv * D] = from_f32<TOUT>(t[e] + up[e]);
+      }
+    }
+  };
 
   if (tid == kMma && cb < ce) {
-    load_w(cb);
-    load_q(cb);
-    load_pk(cb);
+    load_g1(cb);
     load_u(cb);
+    load_g2(cb);
   }
   float gC = 0.f;
   if (worker) {
@@ -770,50 +818,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (cb < ce) gC = gam_c(cb);
   }
 
-  // outputs of chunk c: o_i = gam_i (S0 q^_i) + (U^T P^T)_i, rows i in [16 quarter, +16)
-  auto outputs = [&](int64_t c, bool& okr) {
-    const uint32_t par = (uint32_t)((c - cb) & 1);
-    mma_wait(mbar + ChSmem::kSQ, par, okr, wlim);
-    mma_wait(mbar + ChSmem::kUP, par, okr, wlim);
-    const float* gam = reinterpret_cast<const float*>(sm + ChSmem::G + (int)(c & 1) * kImgG);
-    const int64_t t0 = c * C;
-    const int cnt = (int)(n - t0 < C ? n - t0 : C);
-    float sq[16], up[16];
-    tc::tmem_ld16x2(tbase + tlane + kChSQ + 16 * quarter, tbase + tlane + kChUP + 16 * quarter, sq, up);
-    TOUT* out = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D + row;
-    const int64_t tstride = (int64_t)p.Hv * D;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int i = 16 * quarter + e;
-      if (i < cnt) out[i * tstride] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
-    }
-  };
-  // the checkpoint page of a block boundary at absolute position pos (-1: none)
-  auto boundary_page = [&](int64_t pos) {
-    int32_t page = -1;
-    if (pos % p.block_size == 0) {
-      const int64_t jb = pos / p.block_size - 1;
-      if (jb < p.max_blocks) page = p.block_table[(int64_t)s * p.max_blocks + jb];
-      else if (report) set_error(p.err, GDN_ERR_INVALID_ARG);
-      if (page >= 0 && !page_ok(p.pool, page)) {
-        if (report) set_error(p.err, GDN_ERR_PAGE_RANGE);
-        page = -1;
-      }
-    }
-    return page;
-  };
-
+  float t[16];              // gam (S0 Q^T) of the chunk before, until its U^T P^T is done
   bool ok = true;
   int64_t c = cb;
   for (; c < ce; ++c) {
     const int b = (int)(c & 1);
     const uint32_t par = (uint32_t)((c - cb) & 1);
     const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
+    if (tid == kMma && c > cb) {
+      // this chunk's G2 and gates, once the previous state update has read G2
+      if (work_wait(mbar + ChSmem::kS, par ^ 1u, wlim)) load_g2(c);
+      else ok = false;
+    }
     if (worker) {
-      // ---- S0: the state after chunk c - 1 (its update done), checkpointed at
-      // a block boundary; gam_C S0 back into S; S0 split into tensor memory
-      // once S0 Q^T of chunk c - 1 has read the old split; U'^T of chunk c
-      if (c > cb) mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
+      // ---- the previous chunk's outputs (its G2 done: U^T P^T, and the state
+      // after it); S0 checkpointed at a block boundary, split into tensor
+      // memory, gam_C S0 back into S; [U'^T | 0] for G1; 0 where G2 accumulates U^T P^T
+      if (c > cb) {
+        mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
+        outputs(c - 1, t);
+      }
       const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
       float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
       uint32_t hi[16], lo[16];
@@ -837,9 +861,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_st16(tS + 16 * hh, v0);
       }
-      if (c > cb) mma_wait(mbar + ChSmem::kSQ, par ^ 1u, ok, wlim);
       tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
       tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
+      {
+        float z[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) z[e] = 0.f;
+        tc::tmem_st16(tbase + tlane + kChSQ + 16 * quarter, z);
+        tc::tmem_st16(tbase + tlane + kChUP + 16 * quarter, z);
+      }
       ok = work_wait(mbar + ChSmem::kUl, par, wlim) && ok;
       {
         const float4* us = reinterpret_cast<const float4*>(sm + ChSmem::U) + (row * 64 + 16 * quarter) / 4;
@@ -852,31 +882,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st16(tbase + tlane + kChU + 16 * quarter, u);
       }
       tc::tmem_st_wait();
+      tc::fence_async_smem();   // the output tile, before its TMA store
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // U += S0 W^T (M 128, N 64, K 128) onto U'^T
-      ok = work_wait(mbar + ChSmem::kW + b, bpar, wlim) && ok;
-      tc::mma3_ts<D / 16, 8192>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::W + b * kImgW,
-                                sbase + ChSmem::W + b * kImgW + 16384, tc::idesc_bf16_f32(128, 64), true);
+      // G1: [U | SQ] += S0 [W; Q^]^T (M 128, N 128, K 128)
+      ok = work_wait(mbar + ChSmem::kG1b + b, bpar, wlim) && ok;
+      tc::mma3_ts<D / 16, 16384>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::G1 + b * ChSmem::kG1,
+                                 sbase + ChSmem::G1 + b * ChSmem::kG1 + 32768, tc::idesc_bf16_f32(128, 128), true);
       tc::mma_commit(mbar + ChSmem::kU);
       armed[ChSmem::kU] = c;
-      // the next chunk's W (its buffer's last reader was chunk c - 1) and U'^T
-      // (this chunk's has gone into tensor memory)
+      // the previous chunk's output tile
+      if (c > cb && tma_out && full_chunk(c - 1)) {
+        tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
+        tc::bulk_commit();
+      }
+      // the next chunk's G1 (its buffer's last reader was chunk c - 1) and U'^T
       if (c + 1 < ce) {
-        load_w(c + 1);
+        load_g1(c + 1);
         load_u(c + 1);
       }
+      tc::bulk_wait_read();   // the tile is free again before the next chunk writes it
     }
     if (worker) {
-      // ---- the previous chunk's outputs while S0 W^T runs, then U: split
-      // into tensor memory (the A operand of the state update and U^T P^T)
-      if (c > cb) outputs(c - 1, ok);
+      // ---- U: the split into tensor memory (the A operand of G2); gam (S0 Q^T)
+      // of this chunk into registers
       if (c + 1 < ce) gC = gam_c(c + 1);
       mma_wait(mbar + ChSmem::kU, par, ok, wlim);
-      float u[16];
-      tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
+      ok = work_wait(mbar + ChSmem::kPK, par, wlim) && ok;   // this chunk's gates
+      float u[16], sq[16];
+      tc::tmem_ld16x2(tbase + tlane + kChU + 16 * quarter, tbase + tlane + kChSQ + 16 * quarter, u, sq);
+      const float* gam = reinterpret_cast<const float*>(sm + ChSmem::G + b * kImgG);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) t[e] = gam[16 * quarter + e] * sq[e];
       uint32_t hi[8], lo[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) tc::split_pair(u[2 * e], u[2 * e + 1], hi[e], lo[e]);
@@ -887,34 +926,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64), S0 Q^T, U^T P^T (M 128, N 64)
-      ok = work_wait(mbar + ChSmem::kPK + b, bpar, wlim) && ok;
-      tc::mma3_ts<C / 16, 0>(tbase + kChS, tbase + kChUH, tbase + kChUL, sbase + ChSmem::K + b * kImgK,
-                             sbase + ChSmem::K + b * kImgK + 16384, tc::idesc_bf16_f32(128, 128), true);
+      // G2: [UP | S] += U^T [P; K~]^T (M 128, N 192, K 64)
+      ok = work_wait(mbar + ChSmem::kPK, par, wlim) && ok;
+      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + ChSmem::G2,
+                             sbase + ChSmem::G2 + 24576, tc::idesc_bf16_f32(128, 192), true);
       tc::mma_commit(mbar + ChSmem::kS);
-      ok = work_wait(mbar + ChSmem::kQ, par, wlim) && ok;
-      tc::mma3_ts<D / 16, 8192>(tbase + kChSQ, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::Q,
-                                sbase + ChSmem::Q + 16384, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + ChSmem::kSQ);
-      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + ChSmem::P + b * kImgP,
-                             sbase + ChSmem::P + b * kImgP + 8192, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + ChSmem::kUP);
-      armed[ChSmem::kS] = armed[ChSmem::kSQ] = armed[ChSmem::kUP] = c;
-      if (c + 1 < ce) {
-        // the next chunk's P, K~ and gates (their buffer's last readers, chunk
-        // c - 1's products and outputs, have finished); its Q^ once S0 Q^T
-        // has read this chunk's
-        load_pk(c + 1);
-        if (work_wait(mbar + ChSmem::kSQ, par, wlim)) load_q(c + 1);
-        else ok = false;
-      }
+      armed[ChSmem::kS] = c;
     }
   }
 
-  if (ok && c > cb) {
-    if (worker) {
-      outputs(c - 1, ok);
+  // the last chunk's outputs (every thread takes these barriers: `ok` may
+  // differ between threads until a barrier agrees on it)
+  if (c > cb) {
+    if (ok && worker) {
       mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
+      outputs(c - 1, t);
+      tc::fence_async_smem();
+    }
+    ok = cta_sync_ok(ok);
+    if (ok && tid == kMma && tma_out && full_chunk(c - 1)) {
+      tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
+      tc::bulk_commit();
     }
   }
   ok = cta_sync_ok(ok);
@@ -944,12 +976,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < ChSmem::kBars; ++k) {
         const int64_t a = armed[k];
         if (a < cb) continue;
-        const bool two = k == ChSmem::kW || k == ChSmem::kW + 1 || k == ChSmem::kPK || k == ChSmem::kPK + 1;
+        const bool two = k == ChSmem::kG1b || k == ChSmem::kG1b + 1;
         const uint32_t ph = (uint32_t)((two ? (a - cb) >> 1 : a - cb) & 1);
         tc::mbar_wait_bounded(mbar + k, ph, kWaitDefault);
       }
     }
   }
+  if (tid == kMma) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
@@ -1021,6 +1054,23 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // o as [rows][Hv * dv] bf16; a box is one head's 128 channels x 64 rows
+  // (the chain's full chunks go out as one TMA store when o is 16-byte aligned)
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  int tma_out = 0;
+  if (p.total_rows > 0 && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)p.Hv * kD, (cuuint64_t)p.total_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.Hv * kD * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
+    if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.o, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      tma_out = 1;
+  }
   cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ChSmem::ALLOC);
   if (e != cudaSuccess) return e;
@@ -1035,7 +1085,7 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     pm.s0 = (int32_t)(base % p.num_seqs);
     pm.level0 = (int32_t)(base / p.num_seqs);
     const int64_t cnt = pairs - base < per ? pairs - base : per;
-    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, st>>>(p, ws, pm, maxc);
+    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, st>>>(p, omap, tma_out, ws, pm, maxc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
