@@ -1,42 +1,38 @@
-// tc_chain.cu — the chunked prefill as two kernels on the tensor cores
-// (dk = dv = 128, bf16 inputs and outputs, block size a multiple of 64).
+// tc_chain.cu — the chunked prefill as two kernels on the tensor cores (dk =
+// dv = 128, bf16 inputs and outputs, block size a multiple of 64), with the
+// same arithmetic as the fused kernel (tc_prefill.cu), bit for bit.
 //
 // The chunk (UT) form of the gated delta rule ("Gated DeltaNet",
 // S_t = a_t S_{t-1}(I - b_t k_t k_t^T) + b_t v_t k_t^T, o_t = S_t q_t) over a
 // chunk of C = 64 tokens, with k^, q^ the L2-normalised rows, G_i the running
 // sum of the log decays inside the chunk, gam_i = exp(G_i), dec_i =
-// exp(G_C - G_i), A_ij = b_i exp(G_i - G_j) k^_i.k^_j (j < i), T = (I + A)^{-1}
-// and S0 the state entering the chunk, regrouped so that everything that does
-// not depend on S0 is computed apart:
-//   W   = -T diag(b gam) K^        U' = T diag(b) V        (C x dk, C x dv)
-//   P_ij = exp(G_i - G_j) q^_i.k^_j   (j <= i)
-//   U   = U' + W S0^T                                          (C x dv)
-//   O   = diag(gam) Q^ S0^T + P U
-//   S_C = gam_C S0 + U^T diag(dec) K^
-// (U holds the chunk's rank-one updates u_i; the triangular system collects
-// the (I - b k k^T) factors of the tokens before each one.)
+// exp(G_C - G_i), S0 the state entering the chunk:
+//   A_ij = b_i exp(G_i - G_j) k^_i.k^_j (j < i),  T = (I + A)^{-1}
+//   P_ij = exp(G_i - G_j) q^_i.k^_j (j <= i)
+//   R_i  = b_i (v_i - gam_i S0 k^_i),  U = T R
+//   o_i  = gam_i S0 q^_i + (P U)_i,    S_C = gam_C S0 + U^T diag(dec) K^
+// Everything left of R depends only on the chunk's rows; the rest needs S0.
 //
 // tc_chunk_kernel: one CTA per (sequence, chunk, qk head).  The conv + SiLU of
-//   the chunk's q and k channels, their norms and the Gram products
-//   [K^ K^T; Q^ K^T] run once for the qk head's group of value heads; per
-//   value head of the group the gates, A, P and T, the v conv, and on the
-//   tensor cores U'^T = (V^T diag(b)) T^T and W = [-T diag(b gam); 0] K^.  It
-//   writes, per chunk slot of the workspace, ready-to-load operand images:
-//   W, P and K^T diag(dec) (bf16 hi / lo, 128-byte swizzled), U'^T (fp32)
-//   and gam, dec per value head; Q^ (bf16 hi / lo) per qk head.  No chunk
-//   waits for another, so the whole call's chunks fill every SM.
+//   the q and k channels, their norms, the operand [K^; Q^] and the Gram
+//   products [K^ K^T; Q^ K^T] run once for the qk head's group of value heads;
+//   then per value head the gates, A, P, T, the v conv and K^T diag(dec).  It
+//   leaves, per chunk slot of the workspace, the fused kernel's own operand
+//   images: [K^; Q^] per qk head; T, P and K^T diag(dec) (bf16 hi / lo,
+//   128-byte swizzled), v (fp32) and the gates per value head.  No chunk waits
+//   for another, so the whole call's chunks fill every SM.
 // tc_chain_kernel: one CTA per (sequence, value head) chain (or a piece of
-//   it, as the fused kernel's schedule cuts them).  The fp32 state stays in
-//   tensor memory; per chunk it splits S0 into bf16 hi / lo parts held in
-//   tensor memory as the A operand, adds S0 W^T onto U'^T (tensor cores),
-//   splits U into tensor memory, and forms S += U^T diag(dec) K^, S0 Q^T and
-//   U^T P^T (tensor cores), then the outputs.  The next chunk's operand
-//   images load by bulk copies meanwhile.
-// Chunks start at absolute multiples of 64, so a block boundary is a chunk end
-// and a checkpoint is the tensor-memory state between two chunks: a resume
-// replays the cold run's arithmetic bit for bit.  Every product runs three
-// bf16 passes (hi*hi + hi*lo + lo*hi) with fp32 accumulation.  Every mbarrier
-// wait is bounded as in the fused kernel (gdn_prefill_args.wait_cycles).
+//   one, as the fused kernel's schedule cuts them).  The fp32 state stays in
+//   tensor memory; per chunk, the fused kernel's state steps: S0 [K^; Q^]^T,
+//   R, U^T = R T^T, then S += U^T (K^T diag(dec))^T and U^T P^T, and the
+//   outputs.  The next chunk's images load by bulk copies as soon as their
+//   readers are done.
+// Every operand is split and every product issued exactly as in the fused
+// kernel (the same bf16 hi / lo parts, the same M x N x K shapes and passes in
+// the same order), so the two paths give the same bits and a call may take
+// either.  Chunks start at absolute multiples of 64, so a block boundary is a
+// chunk end and a checkpoint is the tensor-memory state between two chunks.
+// Every mbarrier wait is bounded (gdn_prefill_args.wait_cycles).
 #include "launch.h"
 #include "tc.cuh"
 #include "tc_chunk.cuh"
@@ -50,24 +46,23 @@ constexpr int kWorkers = 512;                 // sixteen worker warps
 constexpr int kThreads = kWorkers + 32;       // + the issuing warp
 constexpr int kMma = kWorkers;                // the issuing thread
 constexpr int kXRows = kC + kWinRows;
-constexpr uint32_t kTmemCols = 512;
 constexpr long long kWaitDefault = 4000000000LL;
 
-// ---- workspace: per chunk slot, operand images ready for the chain ---------
-constexpr uint32_t kImgW = 32768;    // W hi | lo: 64 rows (i) x 128 k (c), two 64-wide k-blocks each
-constexpr uint32_t kImgQ = 32768;    // Q^ hi | lo: same shape
+// ---- workspace: per chunk slot, the fused kernel's operand images ----------
+constexpr uint32_t kImgKQ = 65536;   // [K^; Q^] hi | lo: 128 rows x 128 k, two 64-wide k-blocks each (per qk head)
+constexpr uint32_t kImgT = 16384;    // T hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgP = 16384;    // P hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgK = 32768;    // K^T diag(dec) hi | lo: 128 rows (c) x 64 k (j)
-constexpr uint32_t kImgU = 32768;    // U'^T fp32 [128 r][64 i]
-constexpr uint32_t kImgG = 512;      // gam[64], dec[64] fp32
+constexpr uint32_t kImgV = 32768;    // v fp32 [128 channels][64 rows]
+constexpr uint32_t kImgG = 1024;     // G, gam, dec, b fp32 [4][64]
 
 struct ChunkWs {
-  uint8_t* w;      // [slots][Hv] kImgW
+  uint8_t* kq;     // [slots][Hqk] kImgKQ
+  uint8_t* t;      // [slots][Hv] kImgT
   uint8_t* pm;     // [slots][Hv] kImgP
-  float* u;        // [slots][Hv] kImgU
-  float* g;        // [slots][Hv] kImgG
-  uint8_t* q;      // [slots][Hqk] kImgQ
   uint8_t* k;      // [slots][Hv] kImgK
+  float* v;        // [slots][Hv] kImgV
+  float* g;        // [slots][Hv] kImgG
   int64_t slots;
 };
 
@@ -80,81 +75,71 @@ __device__ __forceinline__ int64_t chunk_slot(const ScanParams& p, int s, int64_
 
 // ---- shared memory of the chunk kernel (offsets from a 1024-aligned base) ----
 struct CkSmem {
-  static constexpr uint32_t R1 = 0;                  // (A) y fp32 [64][256] (q | k)
-  static constexpr uint32_t YF = R1;
-  static constexpr uint32_t AT = R1;                 // (B) A^T fp32 [64 j][64 i]
-  static constexpr uint32_t AM = R1 + 16384;         //     A fp32 row-major, slots swizzled
-  static constexpr uint32_t TF = R1 + 32768;         //     T fp32 [64][64]
-  static constexpr uint32_t DT = R1 + 49152;         //     diagonal inverses [4][16][20]
-  static constexpr uint32_t NT = R1 + 54272;         //     N blocks [6][16][16]
-  static constexpr uint32_t KD = R1;                 //     K^T diag(dec) hi [128][64], lo at +16 KB (after T)
-  static constexpr uint32_t KD_LO = R1 + 16384;
-  static constexpr uint32_t R2 = 65536;              // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
-  static constexpr uint32_t KQ = R2;
-  static constexpr uint32_t KQ_LO = R2 + 32768;
-  static constexpr uint32_t TP = R2;                 // (B) [-T diag(b gam); 0] hi [128][64], lo at +16 KB
-  static constexpr uint32_t TP_LO = R2 + 16384;
-  static constexpr uint32_t WB = R2;                 //     W hi [2 kb][64][64], lo at +16 KB (after the product)
-  static constexpr uint32_t VB = R2 + 32768;         //     V^T diag(b) hi [128][64], lo at +16 KB
-  static constexpr uint32_t VB_LO = R2 + 49152;
-  static constexpr uint32_t KT = 131072;             // K^T hi [128][64], lo at +16 KB (kept)
-  static constexpr uint32_t KT_LO = KT + 16384;
-  static constexpr uint32_t XQ = 163840;             // (A) pre-conv rows t0-3 .. t0+63, bf16 [67][128]
-  static constexpr uint32_t XK = XQ + 17408;
-  static constexpr uint32_t TB = XQ;                 // (B) T hi [64][64], lo at +8 KB
-  static constexpr uint32_t TB_LO = XQ + 8192;
-  static constexpr uint32_t PB = XQ + 16384;         //     P hi [64][64], lo at +8 KB
-  static constexpr uint32_t PB_LO = XQ + 24576;
-  static constexpr uint32_t XV = XK + 17408;         // v rows of the current value head
-  static constexpr uint32_t GT = XV + 17408;         // gate sets [2][4][64] fp32 (G, gam, dec, b), then rq, rk
-  static constexpr uint32_t MBAR = GT + 2048 + 512;  // [0] Gram [1] U' [2] W [3] q/k rows [4] v rows
-  static constexpr uint32_t TSLOT = MBAR + 40;
+  static constexpr uint32_t XQ = 0;                  // (A) pre-conv rows t0-3 .. t0+63, bf16 [67][128]
+  static constexpr uint32_t XK = 17408;
+  static constexpr uint32_t TB = 0;                  // (B) T hi [64][64], lo at +8 KB
+  static constexpr uint32_t TB_LO = 8192;
+  static constexpr uint32_t PB = 16384;              //     P hi [64][64], lo at +8 KB
+  static constexpr uint32_t PB_LO = 24576;
+  static constexpr uint32_t XV = 34816;              // v rows of the current value head
+  static constexpr uint32_t YQ = 53248;              // (A) SiLU(conv) of the q channels, fp32 [64][128]
+  static constexpr uint32_t KT = YQ;                 // (B) K^T diag(dec) hi [128][64], lo at +16 KB
+  static constexpr uint32_t KT_LO = YQ + 16384;
+  static constexpr uint32_t YK = 86016;              // SiLU(conv) of the k channels, fp32 [64][128] (kept)
+  static constexpr uint32_t KQ = 118784;             // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
+  static constexpr uint32_t KQ_LO = KQ + 32768;
+  static constexpr uint32_t AT = KQ;                 // (B) A^T fp32 [64 j][64 i]
+  static constexpr uint32_t AM = KQ + 16384;         //     A fp32 row-major, slots swizzled
+  static constexpr uint32_t TF = KQ + 32768;         //     T fp32 [64][64]
+  static constexpr uint32_t DT = KQ + 49152;         //     diagonal inverses [4][16][20]
+  static constexpr uint32_t NT = KQ + 54272;         //     N blocks [6][16][16]
+  static constexpr uint32_t GT = KQ + 65536;         // gate sets [2][4][64] fp32 (G, gam, dec, b), then rq, rk
+  static constexpr uint32_t MBAR = GT + 2048 + 512;  // [0] Gram [1] q / k rows [2] v rows
+  static constexpr uint32_t TSLOT = MBAR + 24;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
 };
-static_assert(CkSmem::PB_LO + 8192 <= CkSmem::XV, "T and P images overlap the v rows");
+static_assert(CkSmem::PB_LO + 8192 <= CkSmem::XV && CkSmem::XV + 17408 <= CkSmem::YQ, "chunk kernel regions overlap");
 static_assert(CkSmem::ALLOC <= 232448, "chunk kernel shared memory exceeds the per-CTA limit");
 
-// tensor-memory columns of the chunk kernel
+constexpr uint32_t kCkCols = 128;   // tensor memory of the chunk kernel
 constexpr uint32_t kCkGram = 0;     // [K^ K^T; Q^ K^T]: lanes 0-63 k^_i.k^_j, 64-127 q^_i.k^_j
 constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = row
-constexpr uint32_t kCkU = 128;      // U'^T, lane = channel r, column = row i
-constexpr uint32_t kCkW = 256;      // W, lanes 0-63 = row i, 128 columns c
 
-// ---- shared memory of the chain kernel ---------------------------------------
-// G1 = the B operand of S0 [W; Q^]^T (128 rows: W, then Q^; K = 128 in two
-// 64-wide blocks) in two buffers; G2 = the B operand of U^T [P; K~]^T (192
-// rows: P, then K^T diag(dec); K = 64) in one, reloaded once the state update
-// has read it; U'^T; the output tile; the gates of two chunks.
+// ---- shared memory of the chain kernel: one buffer per image, each reloaded
+// as soon as the product that reads it is done ----------------------------------
 struct ChSmem {
-  static constexpr uint32_t kG1 = 65536;             // bytes of one G1 buffer: hi 32 KB, lo 32 KB
-  static constexpr uint32_t kG2 = 49152;             // G2: hi 24 KB, lo 24 KB
-  static constexpr uint32_t G1 = 0;
-  static constexpr uint32_t G2 = 2 * kG1;
-  static constexpr uint32_t U = G2 + kG2;            // U'^T fp32 [128][64]
-  static constexpr uint32_t OT = U + kImgU;          // outputs bf16 [64 rows][128 dv]
-  static constexpr uint32_t G = OT + 16384;          // gam | dec [2]
+  static constexpr uint32_t KQ = 0;                  // [K^; Q^] hi | lo
+  static constexpr uint32_t KT = KQ + kImgKQ;        // K^T diag(dec) hi | lo
+  static constexpr uint32_t TB = KT + kImgK;         // T hi | lo
+  static constexpr uint32_t PB = TB + kImgT;         // P hi | lo
+  static constexpr uint32_t UT = PB + kImgP;         // R^T, then U^T: hi [128][64], lo at +16 KB
+  static constexpr uint32_t VS = UT + 32768;         // v of the next chunk, fp32 [128][64]
+  static constexpr uint32_t OT = VS + kImgV;         // outputs bf16 [64 rows][128 dv]
+  static constexpr uint32_t G = OT + 16384;          // gate sets [2][4][64]
   static constexpr uint32_t MBAR = G + 2 * kImgG;
-  // mbarriers: G1 [2], U'^T, G2 + gates, then the products S0 [W; Q^]^T and U^T [P; K~]^T
-  static constexpr int kG1b = 0, kUl = 2, kPK = 3, kU = 4, kS = 5, kBars = 6;
+  // mbarriers: the images [K^; Q^], K~ | P, T, v, the gates of two chunks;
+  // then the products S0 [K^; Q^]^T, R T^T, the state update, U^T P^T
+  static constexpr int kKQ = 0, kKP = 1, kTb = 2, kVb = 3, kGb = 4, kSK = 6, kU = 7, kS = 8, kUP = 9, kBars = 10;
   static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]: last chunk each was armed for
   static constexpr uint32_t TSLOT = ARMED + 8 * kBars;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
 };
-static_assert(ChSmem::G2 % 1024 == 0 && ChSmem::U % 16 == 0 && ChSmem::OT % 1024 == 0, "operand alignment");
+static_assert(ChSmem::KT % 1024 == 0 && ChSmem::TB % 1024 == 0 && ChSmem::PB % 1024 == 0 && ChSmem::UT % 1024 == 0 &&
+                  ChSmem::OT % 1024 == 0,
+              "operand images must be 1024-byte aligned");
 static_assert(ChSmem::ALLOC <= 232448, "chain kernel shared memory exceeds the per-CTA limit");
 
-// tensor-memory columns of the chain kernel (lane = state row r): the first
-// product writes [U | SQ], the second [UP | S], so each is one wide MMA
-constexpr uint32_t kChU = 0;        // U'^T + S0 W^T fp32 [128][64]
-constexpr uint32_t kChSQ = 64;      // S0 Q^T fp32
-constexpr uint32_t kChUP = 128;     // U^T P^T fp32
-constexpr uint32_t kChS = 192;      // S fp32 [128][128]
-constexpr uint32_t kChS0H = 320;    // S0 hi, bf16 pairs [128][64]
-constexpr uint32_t kChS0L = 384;    // S0 lo
-constexpr uint32_t kChUH = 448;     // U^T hi, bf16 pairs [128][32]
-constexpr uint32_t kChUL = 480;     // U^T lo
+// tensor-memory columns of the chain kernel (lane = state row r)
+constexpr uint32_t kChCols = 512;
+constexpr uint32_t kChS = 0;        // S fp32 [128][128]
+constexpr uint32_t kChSK = 128;     // S0 K^T fp32 [128][64] (then S0 Q^T: one product)
+constexpr uint32_t kChSQ = 192;     // S0 Q^T
+constexpr uint32_t kChU = 256;      // U^T = R T^T, then U^T P^T
+constexpr uint32_t kChV = 320;      // v, lane = channel, column = row
+constexpr uint32_t kChS0H = 384;    // S0 hi, bf16 pairs [128][64] (the A operand of S0 [K^; Q^]^T)
+constexpr uint32_t kChS0L = 448;    // S0 lo
 
 __device__ __forceinline__ bool work_wait(uint64_t* m, uint32_t parity, long long lim) {
   return lim >= 0 && tc::mbar_wait_bounded(m, parity, lim);
@@ -174,8 +159,8 @@ __device__ __forceinline__ long long wait_limit(const ScanParams& p) {
 }
 
 // The issuing warp's gate set of value head h for the chunk's rows [t0, t0 +
-// 64): G (running sum of g), gam = exp(G), dec = exp(G_C - G), b; rows past
-// the end have g = b = 0.
+// 64) (the fused kernel's expressions): G, gam = exp(G), dec = exp(G_C - G),
+// b; rows past the end have g = b = 0.
 __device__ __forceinline__ void chunk_gates(const TokenView<__nv_bfloat16>& V, int64_t t0, int64_t n, int h,
                                             int lane, float* Gs) {
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
@@ -220,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n = V.n;
   if (c * C >= n) return;
   const int64_t t0 = c * C;
+  const int cnt = (int)(n - t0 < C ? n - t0 : C);
   const int G = p.Hv / p.Hqk;
   const int cq0 = jq * D, ck0 = p.Hqk * D + jq * D;
   const int64_t row0 = p.cu_seqlens[s];
@@ -229,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t dyn_smem[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
-  float* yf = reinterpret_cast<float*>(sm + CkSmem::YF);
+  float* yq = reinterpret_cast<float*>(sm + CkSmem::YQ);
+  float* yk = reinterpret_cast<float*>(sm + CkSmem::YK);
   TIN* xq = reinterpret_cast<TIN*>(sm + CkSmem::XQ);
   TIN* xk = reinterpret_cast<TIN*>(sm + CkSmem::XK);
   TIN* xv = reinterpret_cast<TIN*>(sm + CkSmem::XV);
@@ -242,12 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CkSmem::TSLOT);
 
   if (warp == 0) {
-    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_alloc(tslot, kCkCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
 #pragma unroll
-    for (int b = 0; b < 5; ++b) tc::mbar_init(mbar + b, 1);
+    for (int b = 0; b < 3; ++b) tc::mbar_init(mbar + b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   tc::fence_before_sync();
@@ -257,20 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int y = (int)(row0 + t0 - kWinRows);
   auto stage_v = [&](int g) {
-    tc::mbar_expect_tx(mbar + 4, kXRows * D * 2);
-    tc::tma_load_2d(xv, &xmap, 2 * p.Hqk * D + (jq * G + g) * D, y, mbar + 4);
+    tc::mbar_expect_tx(mbar + 2, kXRows * D * 2);
+    tc::tma_load_2d(xv, &xmap, 2 * p.Hqk * D + (jq * G + g) * D, y, mbar + 2);
   };
-  // track of the copies and products in flight (for the drain after a run-out)
-  bool qk_pending = false, gram_pending = false, prod_pending = false;
-  int v_pending = -1;   // value head whose rows are in flight
+  // copies and products in flight, for the drain after a run-out
+  bool qk_pending = true, gram_pending = false;
+  int v_pending = 0;   // value head whose rows are in flight (-1: none)
   if (tid == 0) {
-    tc::mbar_expect_tx(mbar + 3, 2 * kXRows * D * 2);
-    tc::tma_load_2d(xq, &xmap, cq0, y, mbar + 3);
-    tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 3);
+    tc::mbar_expect_tx(mbar + 1, 2 * kXRows * D * 2);
+    tc::tma_load_2d(xq, &xmap, cq0, y, mbar + 1);
+    tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 1);
     stage_v(0);
   }
-  qk_pending = true;
-  v_pending = 0;
 
   // history rows of a sequence's first chunk: the resumed window, or zeros
   auto fix_history = [&](TIN* dst, int ch0) {
@@ -281,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
     }
   };
-  // v conv of value head h: channel `row`, rows [16 quarter, +16) -> tensor memory
+  // v conv of value head h: channel `row`, rows [16 quarter, +16) -> tensor
+  // memory (rows i and i + 8 as one packed pair)
   auto v_conv = [&](int h) {
     const float4 wv = ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK);
     const int tb = 16 * quarter;
@@ -306,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   // ---------------------------------------------------------------- (A) q / k
   if (worker) {
-    ok = workers_sync_and(work_wait(mbar + 3, 0, wlim) && work_wait(mbar + 4, 0, wlim));
+    ok = workers_sync_and(work_wait(mbar + 1, 0, wlim) && work_wait(mbar + 2, 0, wlim));
     if (ok) { qk_pending = false; v_pending = -1; }
     if (c == 0) {
       fix_history(xq, cq0);
@@ -314,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fix_history(xv, 2 * p.Hqk * D + jq * G * D);
       workers_sync();
     }
-    // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16) -> y
+    // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16)
     {
       const int qkp = 2 * (tid & 127);
       const float* wsrc = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;
@@ -329,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v = *reinterpret_cast<const uint32_t*>(xp + u * D);
         x[u] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
       }
-      float* yrow = yf + tb * 256 + qkp;
+      float* yrow = (qkp < D ? yq + qkp : yk + qkp - D) + tb * D;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         f32x2 z = mul2(w0, x[i]);
@@ -337,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         z = fma2(w2, x[i + 2], z);
         z = fma2(w3, x[i + 3], z);
         const float2 zz = unpack2(z);
-        *reinterpret_cast<float2*>(yrow + i * 256) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
+        *reinterpret_cast<float2*>(yrow + i * D) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
       }
     }
     v_conv(jq * G);
@@ -345,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first head's v rows are consumed: the next head's rows
     if (tid == 0 && ok && G > 1) stage_v(1);
     if (ok && G > 1) v_pending = 1;
-    // L2 norm factors (rows past the end: 0)
+    // L2 norm factors: warp w reduces (row, q | k) pairs w, w+16, ... in a
+    // fixed order (the fused kernel's); rows past the end get factor 0
     {
-      const int cnt = (int)(n - t0 < C ? n - t0 : C);
       constexpr int NP = 128 / (kWorkers / 32);
       float ss[NP];
 #pragma unroll
       for (int it = 0; it < NP; ++it) {
         const int k = warp + (kWorkers / 32) * it, t = k >> 1, isk = k & 1;
-        const float* yr = yf + t * 256 + isk * D;
+        const float* yr = (isk ? yk : yq) + t * D;
         float a = 0.f;
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) {
@@ -388,55 +374,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     workers_sync();
-    // operands [K^; Q^] (rows 0-63 k^, 64-127 q^) and K^T (row = k channel)
+    // the operand [K^; Q^] (rows 0-63 k^, 64-127 q^)
     {
-      constexpr int NKQ = 2048 / kWorkers, NKT = 1024 / kWorkers;
+      constexpr int NKQ = 2048 / kWorkers;
+      float4 ya[NKQ], yb[NKQ];
+      float fv[NKQ];
 #pragma unroll
       for (int it = 0; it < NKQ; ++it) {
         const int i = tid + kWorkers * it, r = i >> 4, c8 = i & 15;
         const int t = r & (C - 1);
         const bool isq = r >= C;
-        const float f = isq ? rq[t] : rk[t];
-        const float4* src = reinterpret_cast<const float4*>(yf + t * 256 + (isq ? 0 : D) + 8 * c8);
-        const float4 ya = src[0], yb = src[1];
+        fv[it] = isq ? rq[t] : rk[t];
+        const float4* src = reinterpret_cast<const float4*>((isq ? yq : yk) + t * D + 8 * c8);
+        ya[it] = src[0];
+        yb[it] = src[1];
+      }
+#pragma unroll
+      for (int it = 0; it < NKQ; ++it) {
+        const int i = tid + kWorkers * it, r = i >> 4, c8 = i & 15;
+        const float f = fv[it];
         const f32x2 f2 = pack2(f, f);
-        const float2 e01 = unpack2(mul2(pack2(ya.x, ya.y), f2));
-        const float2 e23 = unpack2(mul2(pack2(ya.z, ya.w), f2));
-        const float2 e45 = unpack2(mul2(pack2(yb.x, yb.y), f2));
-        const float2 e67 = unpack2(mul2(pack2(yb.z, yb.w), f2));
+        const float2 e01 = unpack2(mul2(pack2(ya[it].x, ya[it].y), f2));
+        const float2 e23 = unpack2(mul2(pack2(ya[it].z, ya[it].w), f2));
+        const float2 e45 = unpack2(mul2(pack2(yb[it].x, yb[it].y), f2));
+        const float2 e67 = unpack2(mul2(pack2(yb[it].z, yb[it].w), f2));
         const float e[8] = {e01.x, e01.y, e23.x, e23.y, e45.x, e45.y, e67.x, e67.y};
         const uint32_t off = tc::sw128_offset(r, 8 * c8, 128);
         tc::store_split8(sm + CkSmem::KQ + off, sm + CkSmem::KQ_LO + off, e);
-      }
-#pragma unroll
-      for (int it = 0; it < NKT; ++it) {
-        const int i = tid + kWorkers * it, k = i & 127, j8 = i >> 7;
-        float kt[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = 8 * j8 + u;
-          kt[u] = yf[j * 256 + D + k] * rk[j];
-        }
-        const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
-        tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
       }
     }
     tc::fence_async_smem();
   }
   ok = cta_sync_ok(ok);
   if (ok && tid == kMma) {
-    // [K^ K^T; Q^ K^T] (M 128, N 64, K 128)
+    // [K^ K^T; Q^ K^T] (M 128, N 64, K 128), and [K^; Q^] for the chain
     tc::mma3_sw128<D / 16, 16384, 16384>(tbase + kCkGram, sbase + CkSmem::KQ, sbase + CkSmem::KQ_LO,
                                          sbase + CkSmem::KQ, sbase + CkSmem::KQ_LO, tc::idesc_bf16_f32(128, 64),
                                          false);
     tc::mma_commit(mbar + 0);
-    // the qk head's image for the chain: Q^ (rows 64-127 of [K^; Q^])
-    uint8_t* qdst = ws.q + (slot * p.Hqk + jq) * (int64_t)kImgQ;
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-        tc::bulk_store(qdst + part * 16384 + kb * 8192, sm + CkSmem::KQ + part * 32768 + kb * 16384 + 8192, 8192);
+    tc::bulk_store(ws.kq + (slot * p.Hqk + jq) * (int64_t)kImgKQ, sm + CkSmem::KQ, kImgKQ);
     tc::bulk_commit();
   }
   if (ok) gram_pending = true;
@@ -446,10 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (; ok && g < G; ++g) {
     const int h = jq * G + g;
     float* const Gs = gbuf + 256 * (g & 1);
-    const float* gam = Gs + 64;
+    const float* dec = Gs + 128;
     const float* bv = Gs + 192;
     if (!worker) {
-      // this head's gates; the set it overwrites went out with the head before last
+      // this head's gates; the set it overwrites, and [K^; Q^] (the region of
+      // A and T), have been read out by the bulk copies
       if (tid == kMma) tc::bulk_wait_read();
       __syncwarp();
       chunk_gates(V, t0, n, h, lane, Gs);
@@ -457,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       if (g > 0) {
         // v rows of this head (issued while the head before it was processed)
-        ok = workers_sync_and(work_wait(mbar + 4, (uint32_t)(g & 1), wlim) && ok);
+        ok = workers_sync_and(work_wait(mbar + 2, (uint32_t)(g & 1), wlim) && ok);
         if (ok) v_pending = -1;
         if (c == 0) {
           fix_history(xv, 2 * p.Hqk * D + h * D);
@@ -506,126 +483,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       workers_sync();
       if (tid >= 256) {
-        // T = (I + A)^{-1}; then T (rows i, K = j; zero above the diagonal) and
-        // [-T diag(b gam); 0] (128 rows) as operands
+        // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
         tri_inverse64(at, reinterpret_cast<const float*>(sm + CkSmem::AM), tf,
                       reinterpret_cast<float*>(sm + CkSmem::DT), reinterpret_cast<float*>(sm + CkSmem::NT),
                       tid - 256);
-        for (int e = tid - 256; e < 1024; e += 256) {
+        for (int e = tid - 256; e < 512; e += 256) {
           const int i = e >> 3, c8 = e & 7;
-          float v8[8], w8[8];
-          if (i < C) {
-            const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
-            const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
-            const float tv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
+          const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
+          float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j = 8 * c8 + u;
-              v8[u] = j > i ? 0.f : tv[u];
-              w8[u] = -(v8[u] * (bv[j] * gam[j]));
-            }
-            const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
-            tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
-          } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) w8[u] = 0.f;
-          }
-          const uint32_t off = tc::sw128_offset(i, 8 * c8, 128);
-          tc::store_split8(sm + CkSmem::TP + off, sm + CkSmem::TP_LO + off, w8);
+          for (int u = 0; u < 8; ++u)
+            if (8 * c8 + u > i) v8[u] = 0.f;
+          const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
+          tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
         }
       } else {
-        // V^T diag(b) of channel `row` for rows i in [32 qh, +32): the A operand of U'^T
-        const int qh = tid >> 7;
+        // K^T diag(dec) (row = k channel): the fused kernel's elements and
+        // expression, four of its eight-row groups per thread
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int i = tid + 256 * it, k = i & 127, j8 = i >> 7;
+          float kt[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = 8 * j8 + u;
+            kt[u] = (yk[j * D + k] * rk[j]) * dec[j];
+          }
+          const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
+          tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
+        }
+        // v of channel `row`, rows [32 (tid >> 7), +32) -> the workspace (fp32 [r][i])
+        float* dst = ws.v + (slot * p.Hv + h) * (int64_t)(kImgV / 4) + row * 64 + 32 * (tid >> 7);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int i0 = 32 * qh + 16 * hh;
-          float a[16];
-          tc::tmem_ld16(tbase + tlane + kCkV + i0, a);
+          float v[16];
+          tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) a[e] *= bv[i0 + e];
-#pragma unroll
-          for (int c8 = 0; c8 < 2; ++c8) {
-            const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
-            tc::store_split8(sm + CkSmem::VB + off, sm + CkSmem::VB_LO + off, a + 8 * c8);
-          }
+          for (int c4 = 0; c4 < 4; ++c4)
+            reinterpret_cast<float4*>(dst + 16 * hh)[c4] =
+                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
         }
       }
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
-    if (!ok) break;
-    if (tid == kMma) {
-      // U'^T = (V^T diag(b)) T^T (M 128, N 64, K 64); W = [-T diag(b gam); 0] K^ (M 128, N 128, K 64)
-      tc::mma3_sw128<C / 16, 0, 0>(tbase + kCkU, sbase + CkSmem::VB, sbase + CkSmem::VB_LO, sbase + CkSmem::TB,
-                                   sbase + CkSmem::TB_LO, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + 1);
-      tc::mma3_sw128<C / 16, 0, 0>(tbase + kCkW, sbase + CkSmem::TP, sbase + CkSmem::TP_LO, sbase + CkSmem::KT,
-                                   sbase + CkSmem::KT_LO, tc::idesc_bf16_f32(128, 128), false);
-      tc::mma_commit(mbar + 2);
-    }
-    prod_pending = true;
-    if (worker) {
-      // K^T diag(dec) for the chain's state update, into the T work area
-      // (free now): row `row` (k channel), rows i in [16 (tid >> 7), +16)
-      {
-        const float* dec = Gs + 128;
-        const int i0 = 16 * (tid >> 7);
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
-          const uint4 vh = *reinterpret_cast<const uint4*>(sm + CkSmem::KT + off);
-          const uint4 vl = *reinterpret_cast<const uint4*>(sm + CkSmem::KT_LO + off);
-          const uint32_t wh[4] = {vh.x, vh.y, vh.z, vh.w}, wl[4] = {vl.x, vl.y, vl.z, vl.w};
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float a0 = __uint_as_float(wh[u] << 16) + __uint_as_float(wl[u] << 16);
-            const float a1 = __uint_as_float(wh[u] & 0xFFFF0000u) + __uint_as_float(wl[u] & 0xFFFF0000u);
-            e[2 * u] = a0 * dec[i0 + 8 * c8 + 2 * u];
-            e[2 * u + 1] = a1 * dec[i0 + 8 * c8 + 2 * u + 1];
-          }
-          tc::store_split8(sm + CkSmem::KD + off, sm + CkSmem::KD_LO + off, e);
-        }
-      }
-      const uint32_t par = (uint32_t)(g & 1);
-      mma_wait(mbar + 1, par, ok, wlim);
-      // U'^T of channel `row`, rows [16 quarter, +16) -> the workspace (fp32 [r][i])
-      {
-        float u[16];
-        tc::tmem_ld16(tbase + tlane + kCkU + 16 * quarter, u);
-        float4* dst = reinterpret_cast<float4*>(ws.u + (slot * p.Hv + h) * (int64_t)(kImgU / 4) + row * 64 +
-                                                16 * quarter);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) dst[c4] = make_float4(u[4 * c4], u[4 * c4 + 1], u[4 * c4 + 2], u[4 * c4 + 3]);
-      }
-      mma_wait(mbar + 2, par, ok, wlim);
-      // W rows i (lanes 0-63) -> the W image (rows i, K = c), columns [32 (warp >> 2), +32)
-      if ((warp & 3) < 2) {
-        const int i = (warp & 3) * 32 + lane, c0 = 32 * (warp >> 2);
-        float wv[32];
-        tc::tmem_ld32(tbase + tlane + kCkW + c0, wv);
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const uint32_t off = tc::sw128_offset(i, c0 + 8 * c8, 64);
-          tc::store_split8(sm + CkSmem::WB + off, sm + CkSmem::WB + 16384 + off, wv + 8 * c8);
-        }
-      }
-      tc::fence_async_smem();
-    }
-    ok = cta_sync_ok(ok);
-    if (ok) prod_pending = false;
     if (!ok) break;
     if (tid == kMma) {
       const int64_t hv = slot * p.Hv + h;
-      tc::bulk_store(ws.w + hv * kImgW, sm + CkSmem::WB, kImgW);
+      tc::bulk_store(ws.t + hv * kImgT, sm + CkSmem::TB, kImgT);
       tc::bulk_store(ws.pm + hv * kImgP, sm + CkSmem::PB, kImgP);
-      tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KD, kImgK);
-      // gam | dec of the head for the chain (G and b are folded into W, U', P)
-      tc::bulk_store(ws.g + hv * (kImgG / 4), Gs + 64, 256);
-      tc::bulk_store(ws.g + hv * (kImgG / 4) + 64, Gs + 128, 256);
+      tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
+      tc::bulk_store(ws.g + hv * (kImgG / 4), Gs, kImgG);
       tc::bulk_commit();
-      // the next head rewrites the images these copies read
-      tc::bulk_wait_read();
     }
   }
 
@@ -634,30 +544,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (default bound), release the tensor memory
     if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);
     if (worker) {
-      if (qk_pending) tc::mbar_wait_bounded(mbar + 3, 0, kWaitDefault);
-      if (v_pending >= 0) tc::mbar_wait_bounded(mbar + 4, (uint32_t)(v_pending & 1), kWaitDefault);
+      if (qk_pending) tc::mbar_wait_bounded(mbar + 1, 0, kWaitDefault);
+      if (v_pending >= 0) tc::mbar_wait_bounded(mbar + 2, (uint32_t)(v_pending & 1), kWaitDefault);
       if (gram_pending) tc::mbar_wait_bounded(mbar + 0, 0, kWaitDefault);
-      if (prod_pending) {
-        tc::mbar_wait_bounded(mbar + 1, (uint32_t)(g & 1), kWaitDefault);
-        tc::mbar_wait_bounded(mbar + 2, (uint32_t)(g & 1), kWaitDefault);
-      }
     }
   }
   if (tid == kMma) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tbase, kCkCols);
 }
 
 // ============================================================================
 // Chain kernel: grid (Hv, pieces), one CTA per (value head, (level, sequence))
 // ============================================================================
-// Per chunk c the tensor pipe runs two wide products: G1 = S0 [W; Q^]^T onto
-// [U'^T | 0] (M 128, N 128, K 128) and, after the U split, G2 = U^T [P; K~]^T
-// onto [0 | gam_C S0] (M 128, N 192, K 64), which yields U^T P^T and the next
-// state together.  Between them the workers split U and keep gam (S0 Q^T) of
-// the chunk in registers; the outputs gam (S0 Q^T) + U^T P^T go out through a
-// shared-memory tile once G2 is done, while the next state is split.
+// Per chunk c: (1) the state after chunk c - 1 (checkpointed at a block
+// boundary) split into tensor memory as the A operand, gam_C S0 back, v of
+// chunk c into tensor memory; then S0 [K^; Q^]^T.  (2) The outputs of chunk
+// c - 1; R into the U^T operand; then U^T = R T^T.  (3) U into the operand;
+// then the state update S += U^T (K^T diag(dec))^T and U^T P^T.  Every image
+// of chunk c + 1 is requested as soon as the product reading chunk c's is done.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws,
                     const PieceMap pm, int64_t max_chunks) {
@@ -706,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   TOUT* ot = reinterpret_cast<TOUT*>(sm + ChSmem::OT);
 
   if (warp == 0) {
-    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_alloc(tslot, kChCols);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -725,44 +631,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // the issuing thread's loads of chunk c's images (each arms its mbarrier)
   auto hv_of = [&](int64_t c) { return chunk_slot(p, s, c) * p.Hv + h; };
-  auto load_g1 = [&](int64_t c) {
-    const int b = (int)(c & 1);
-    uint64_t* m = mbar + ChSmem::kG1b + b;
-    uint8_t* dst = sm + ChSmem::G1 + b * ChSmem::kG1;
-    const uint8_t* w = ws.w + hv_of(c) * kImgW;
-    const uint8_t* q = ws.q + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgQ;
-    tc::mbar_expect_tx(m, kImgW + kImgQ);
-    // [W; Q^] as one 128-row operand: each 64-wide K-block holds W's 64 rows, then Q^'s
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        tc::bulk_load(dst + part * 32768 + kb * 16384, w + part * 16384 + kb * 8192, 8192, m);
-        tc::bulk_load(dst + part * 32768 + kb * 16384 + 8192, q + part * 16384 + kb * 8192, 8192, m);
-      }
-    armed[ChSmem::kG1b + b] = c;
+  auto load_kq = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kKQ, kImgKQ);
+    const uint8_t* src = ws.kq + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgKQ;
+    tc::bulk_load(sm + ChSmem::KQ, src, 32768, mbar + ChSmem::kKQ);
+    tc::bulk_load(sm + ChSmem::KQ + 32768, src + 32768, 32768, mbar + ChSmem::kKQ);
+    armed[ChSmem::kKQ] = c;
   };
-  auto load_g2 = [&](int64_t c) {
+  auto load_kp = [&](int64_t c) {
     const int64_t hv = hv_of(c);
-    uint64_t* m = mbar + ChSmem::kPK;
-    uint8_t* dst = sm + ChSmem::G2;
-    tc::mbar_expect_tx(m, kImgP + kImgK + kImgG);
-    // [P; K~] as one 192-row operand (K = 64): P's 64 rows, then K~'s 128
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      tc::bulk_load(dst + part * 24576, ws.pm + hv * kImgP + part * 8192, 8192, m);
-      tc::bulk_load(dst + part * 24576 + 8192, ws.k + hv * kImgK + part * 16384, 16384, m);
-    }
-    tc::bulk_load(sm + ChSmem::G + (int)(c & 1) * kImgG, ws.g + hv * (kImgG / 4), kImgG, m);
-    armed[ChSmem::kPK] = c;
+    tc::mbar_expect_tx(mbar + ChSmem::kKP, kImgK + kImgP);
+    tc::bulk_load(sm + ChSmem::KT, ws.k + hv * kImgK, kImgK, mbar + ChSmem::kKP);
+    tc::bulk_load(sm + ChSmem::PB, ws.pm + hv * kImgP, kImgP, mbar + ChSmem::kKP);
+    armed[ChSmem::kKP] = c;
   };
-  auto load_u = [&](int64_t c) {
-    tc::mbar_expect_tx(mbar + ChSmem::kUl, kImgU);
-    tc::bulk_load(sm + ChSmem::U, ws.u + hv_of(c) * (kImgU / 4), kImgU, mbar + ChSmem::kUl);
-    armed[ChSmem::kUl] = c;
+  auto load_t = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kTb, kImgT);
+    tc::bulk_load(sm + ChSmem::TB, ws.t + hv_of(c) * kImgT, kImgT, mbar + ChSmem::kTb);
+    armed[ChSmem::kTb] = c;
   };
-  // gam_C of chunk c (the decay of the whole chunk), read ahead by every worker
-  auto gam_c = [&](int64_t c) { return __ldg(ws.g + hv_of(c) * (kImgG / 4) + (C - 1)); };
+  auto load_v = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kVb, kImgV);
+    tc::bulk_load(sm + ChSmem::VS, ws.v + hv_of(c) * (kImgV / 4), kImgV, mbar + ChSmem::kVb);
+    armed[ChSmem::kVb] = c;
+  };
+  auto load_g = [&](int64_t c) {
+    const int b = (int)(c & 1);
+    tc::mbar_expect_tx(mbar + ChSmem::kGb + b, kImgG);
+    tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv_of(c) * (kImgG / 4), kImgG, mbar + ChSmem::kGb + b);
+    armed[ChSmem::kGb + b] = c;
+  };
+  auto gates_of = [&](int64_t c) { return reinterpret_cast<const float*>(sm + ChSmem::G + (int)(c & 1) * kImgG); };
   // the checkpoint page of a block boundary at absolute position pos (-1: none)
   auto boundary_page = [&](int64_t pos) {
     int32_t page = -1;
@@ -778,14 +677,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     return page;
   };
   auto full_chunk = [&](int64_t c) { return n - c * C >= C; };
-  // outputs of chunk c from t = gam (S0 Q^T) and U^T P^T (rows i in [16 quarter, +16)):
-  // a full chunk into the tile (one TMA store), a partial one by plain stores
-  auto outputs = [&](int64_t c, const float (&t)[16]) {
+  // outputs of chunk c: o_i = gam_i (S0 q^_i) + (U^T P^T)_i for rows i in
+  // [16 quarter, +16), from S0 Q^T kept in registers and U^T P^T in tensor
+  // memory; a full chunk into the tile (one TMA store), a partial one by plain stores
+  auto outputs = [&](int64_t c, const float (&sq)[16]) {
+    const float* gam = gates_of(c) + 64;
     float up[16];
-    tc::tmem_ld16(tbase + tlane + kChUP + 16 * quarter, up);
+    tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, up);
     if (tma_out && full_chunk(c)) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) ot[(16 * quarter + e) * D + row] = from_f32<TOUT>(t[e] + up[e]);
+      for (int e = 0; e < 16; ++e)
+        ot[(16 * quarter + e) * D + row] = from_f32<TOUT>(fmaf(gam[16 * quarter + e], sq[e], up[e]));
     } else {
       const int64_t t0 = c * C;
       const int cnt = (int)(n - t0 < C ? n - t0 : C);
@@ -793,17 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int i = 16 * quarter + e;
-        if (i < cnt) out[(int64_t)i * p.Hv * D] = from_f32<TOUT>(t[e] + up[e]);
+        if (i < cnt) out[(int64_t)i * p.Hv * D] = from_f32<TOUT>(fmaf(gam[i], sq[e], up[e]));
       }
     }
   };
 
   if (tid == kMma && cb < ce) {
-    load_g1(cb);
-    load_u(cb);
-    load_g2(cb);
+    load_kq(cb);
+    load_v(cb);
+    load_g(cb);
+    load_t(cb);
+    load_kp(cb);
   }
-  float gC = 0.f;
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
     const float* src = from >= 0 ? page_state(p.pool, from) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
@@ -815,29 +718,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::tmem_st32(tS, v);
     tc::tmem_st_wait();
-    if (cb < ce) gC = gam_c(cb);
   }
 
-  float t[16];              // gam (S0 Q^T) of the chunk before, until its U^T P^T is done
+  float sq[16];             // S0 Q^T of the chunk before, until its outputs
   bool ok = true;
   int64_t c = cb;
   for (; c < ce; ++c) {
     const int b = (int)(c & 1);
     const uint32_t par = (uint32_t)((c - cb) & 1);
-    const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
-    if (tid == kMma && c > cb) {
-      // this chunk's G2 and gates, once the previous state update has read G2
-      if (work_wait(mbar + ChSmem::kS, par ^ 1u, wlim)) load_g2(c);
-      else ok = false;
-    }
+    const uint32_t gpar = (uint32_t)(((c - cb) >> 1) & 1);
     if (worker) {
-      // ---- the previous chunk's outputs (its G2 done: U^T P^T, and the state
-      // after it); S0 checkpointed at a block boundary, split into tensor
-      // memory, gam_C S0 back into S; [U'^T | 0] for G1; 0 where G2 accumulates U^T P^T
-      if (c > cb) {
-        mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
-        outputs(c - 1, t);
-      }
+      // ---- (1) the state after chunk c - 1: checkpoint, split into tensor
+      // memory, gam_C S0 back; v of this chunk into tensor memory
+      if (c > cb) mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
+      ok = work_wait(mbar + ChSmem::kGb + b, gpar, wlim) && ok;
+      const float gC = gates_of(c)[64 + C - 1];
       const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
       float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
       uint32_t hi[16], lo[16];
@@ -863,75 +758,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
       tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
+      ok = work_wait(mbar + ChSmem::kVb, par, wlim) && ok;
       {
-        float z[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) z[e] = 0.f;
-        tc::tmem_st16(tbase + tlane + kChSQ + 16 * quarter, z);
-        tc::tmem_st16(tbase + tlane + kChUP + 16 * quarter, z);
-      }
-      ok = work_wait(mbar + ChSmem::kUl, par, wlim) && ok;
-      {
-        const float4* us = reinterpret_cast<const float4*>(sm + ChSmem::U) + (row * 64 + 16 * quarter) / 4;
-        float u[16];
+        const float4* vs = reinterpret_cast<const float4*>(sm + ChSmem::VS) + (row * 64 + 16 * quarter) / 4;
+        float v[16];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          const float4 f = us[c4];
-          u[4 * c4] = f.x; u[4 * c4 + 1] = f.y; u[4 * c4 + 2] = f.z; u[4 * c4 + 3] = f.w;
+          const float4 f = vs[c4];
+          v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
         }
-        tc::tmem_st16(tbase + tlane + kChU + 16 * quarter, u);
+        tc::tmem_st16(tbase + tlane + kChV + 16 * quarter, v);
       }
       tc::tmem_st_wait();
-      tc::fence_async_smem();   // the output tile, before its TMA store
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // G1: [U | SQ] += S0 [W; Q^]^T (M 128, N 128, K 128)
-      ok = work_wait(mbar + ChSmem::kG1b + b, bpar, wlim) && ok;
-      tc::mma3_ts<D / 16, 16384>(tbase + kChU, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::G1 + b * ChSmem::kG1,
-                                 sbase + ChSmem::G1 + b * ChSmem::kG1 + 32768, tc::idesc_bf16_f32(128, 128), true);
-      tc::mma_commit(mbar + ChSmem::kU);
-      armed[ChSmem::kU] = c;
-      // the previous chunk's output tile
+      // S0 [K^; Q^]^T (M 128, N 128, K 128) -> [S0 K^T | S0 Q^T]
+      ok = work_wait(mbar + ChSmem::kKQ, par, wlim) && ok;
+      tc::mma3_ts<D / 16, 16384>(tbase + kChSK, tbase + kChS0H, tbase + kChS0L, sbase + ChSmem::KQ,
+                                 sbase + ChSmem::KQ + 32768, tc::idesc_bf16_f32(128, 128), false);
+      tc::mma_commit(mbar + ChSmem::kSK);
+      armed[ChSmem::kSK] = c;
+      // v of the next chunk (this one's is in tensor memory)
+      if (c + 1 < ce) load_v(c + 1);
+    }
+    if (worker) {
+      // ---- (2) the previous chunk's outputs (its U^T P^T is done), then R_i =
+      // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16)
+      if (c > cb) {
+        mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
+        outputs(c - 1, sq);
+        tc::fence_async_smem();
+      }
+      mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
+      const float* gs = gates_of(c);
+      const float* gam = gs + 64;
+      const float* bv = gs + 192;
+      const int i0 = 16 * quarter;
+      float a[16], v[16];
+      tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChV + i0, a, v);
+      tc::tmem_ld16(tbase + tlane + kChSQ + i0, sq);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], v[e]);
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
+        tc::store_split8(sm + ChSmem::UT + off, sm + ChSmem::UT + 16384 + off, a + 8 * c8);
+      }
+      tc::fence_async_smem();
+    }
+    ok = cta_sync_ok(ok);
+    if (!ok) break;
+    if (tid == kMma) {
+      // the previous chunk's output tile; [K^; Q^] of the next chunk (S0 [K^; Q^]^T is done)
       if (c > cb && tma_out && full_chunk(c - 1)) {
         tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
         tc::bulk_commit();
       }
-      // the next chunk's G1 (its buffer's last reader was chunk c - 1) and U'^T
-      if (c + 1 < ce) {
-        load_g1(c + 1);
-        load_u(c + 1);
-      }
-      tc::bulk_wait_read();   // the tile is free again before the next chunk writes it
+      if (c + 1 < ce) load_kq(c + 1);
+      // U^T = R T^T (M 128, N 64, K 64)
+      ok = work_wait(mbar + ChSmem::kTb, par, wlim) && ok;
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChU, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::TB,
+                                   sbase + ChSmem::TB + 8192, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + ChSmem::kU);
+      armed[ChSmem::kU] = c;
+      // the next chunk's gates: their buffer's last reader, the outputs of chunk c - 1, is done
+      if (c + 1 < ce) load_g(c + 1);
+      tc::bulk_wait_read();   // the tile, before the next chunk's outputs
     }
     if (worker) {
-      // ---- U: the split into tensor memory (the A operand of G2); gam (S0 Q^T)
-      // of this chunk into registers
-      if (c + 1 < ce) gC = gam_c(c + 1);
+      // ---- (3) U (rows r, K = i) as the operand of the state update and U^T P^T
       mma_wait(mbar + ChSmem::kU, par, ok, wlim);
-      ok = work_wait(mbar + ChSmem::kPK, par, wlim) && ok;   // this chunk's gates
-      float u[16], sq[16];
-      tc::tmem_ld16x2(tbase + tlane + kChU + 16 * quarter, tbase + tlane + kChSQ + 16 * quarter, u, sq);
-      const float* gam = reinterpret_cast<const float*>(sm + ChSmem::G + b * kImgG);
+      float u[16];
+      tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) t[e] = gam[16 * quarter + e] * sq[e];
-      uint32_t hi[8], lo[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) tc::split_pair(u[2 * e], u[2 * e + 1], hi[e], lo[e]);
-      tc::tmem_st8(tbase + tlane + kChUH + 8 * quarter, hi);
-      tc::tmem_st8(tbase + tlane + kChUL + 8 * quarter, lo);
-      tc::tmem_st_wait();
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const uint32_t off = tc::sw128_offset(row, 16 * quarter + 8 * c8, 128);
+        tc::store_split8(sm + ChSmem::UT + off, sm + ChSmem::UT + 16384 + off, u + 8 * c8);
+      }
+      tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // G2: [UP | S] += U^T [P; K~]^T (M 128, N 192, K 64)
-      ok = work_wait(mbar + ChSmem::kPK, par, wlim) && ok;
-      tc::mma3_ts<C / 16, 0>(tbase + kChUP, tbase + kChUH, tbase + kChUL, sbase + ChSmem::G2,
-                             sbase + ChSmem::G2 + 24576, tc::idesc_bf16_f32(128, 192), true);
+      // T of the next chunk (R T^T is done)
+      if (c + 1 < ce) load_t(c + 1);
+      // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64) first, then U^T P^T (M 128, N 64, K 64)
+      ok = work_wait(mbar + ChSmem::kKP, par, wlim) && ok;
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChS, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::KT,
+                                   sbase + ChSmem::KT + 16384, tc::idesc_bf16_f32(128, 128), true);
       tc::mma_commit(mbar + ChSmem::kS);
-      armed[ChSmem::kS] = c;
+      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChU, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::PB,
+                                   sbase + ChSmem::PB + 8192, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + ChSmem::kUP);
+      armed[ChSmem::kS] = armed[ChSmem::kUP] = c;
+      // K~ and P of the next chunk once both products have read this chunk's
+      if (c + 1 < ce) {
+        if (work_wait(mbar + ChSmem::kUP, par, wlim)) load_kp(c + 1);
+        else ok = false;
+      }
     }
   }
 
@@ -940,7 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (c > cb) {
     if (ok && worker) {
       mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
-      outputs(c - 1, t);
+      mma_wait(mbar + ChSmem::kUP, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
+      outputs(c - 1, sq);
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
@@ -976,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < ChSmem::kBars; ++k) {
         const int64_t a = armed[k];
         if (a < cb) continue;
-        const bool two = k == ChSmem::kG1b || k == ChSmem::kG1b + 1;
+        const bool two = k == ChSmem::kGb || k == ChSmem::kGb + 1;
         const uint32_t ph = (uint32_t)((two ? (a - cb) >> 1 : a - cb) & 1);
         tc::mbar_wait_bounded(mbar + k, ph, kWaitDefault);
       }
@@ -985,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == kMma) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tbase, kTmemCols);
+  if (warp == 0) tc::tmem_dealloc(tbase, kChCols);
 }
 
 // ============================================================================
@@ -993,8 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
   const int64_t slots = total_tokens / kC + num_seqs + 1;
-  const int64_t per_v = (int64_t)kImgW + kImgP + kImgU + kImgK + kImgG;
-  const int64_t per_q = (int64_t)kImgQ;
+  const int64_t per_v = (int64_t)kImgT + kImgP + kImgK + kImgV + kImgG;
+  const int64_t per_q = (int64_t)kImgKQ;
   return (size_t)(slots * (Hv * per_v + Hqk * per_q)) + 1024;
 }
 
@@ -1008,11 +935,11 @@ ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total
     b += bytes;
     return r;
   };
-  w.w = take(w.slots * Hv * (int64_t)kImgW);
+  w.kq = take(w.slots * Hqk * (int64_t)kImgKQ);
+  w.t = take(w.slots * Hv * (int64_t)kImgT);
   w.pm = take(w.slots * Hv * (int64_t)kImgP);
-  w.u = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgU));
-  w.q = take(w.slots * Hqk * (int64_t)kImgQ);
   w.k = take(w.slots * Hv * (int64_t)kImgK);
+  w.v = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgV));
   w.g = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgG));
   return w;
 }
@@ -1034,11 +961,11 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   const ChunkWs ws = bind_chunk_ws(workspace, p.Hqk, p.Hv, p.num_seqs, p.total_rows);
   const int64_t maxc = max_len > 0 ? (max_len + kC - 1) / kC : 0;
   if (maxc > 65535) return cudaErrorInvalidValue;
+  auto encode = tensor_map_encoder();
+  if (p.total_rows > 0 && !encode) return cudaErrorNotSupported;
   if (maxc > 0 && p.total_rows > 0) {
     CUtensorMap xmap;
     memset(&xmap, 0, sizeof(xmap));
-    auto encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.x_ld, (cuuint64_t)p.total_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.x_ld * 2};
@@ -1060,8 +987,6 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   memset(&omap, 0, sizeof(omap));
   int tma_out = 0;
   if (p.total_rows > 0 && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
-    auto encode = tensor_map_encoder();
-    if (!encode) return cudaErrorNotSupported;
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.Hv * kD, (cuuint64_t)p.total_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.Hv * kD * 2};

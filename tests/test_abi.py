@@ -83,10 +83,10 @@ def test_pool_too_small_or_misaligned_is_rejected():
 
 def test_workspace_is_required_and_sized():
     # the tensor-core prefill (d 128, bf16, block a multiple of 64): the chunk
-    # kernel's images for floor(T / 64) + N + 1 chunk slots, per slot W, P,
-    # U'^T, K^T diag(dec) and gam | dec of every value head and Q^ of every qk head
+    # kernel's images for floor(T / 64) + N + 1 chunk slots, per slot T, P,
+    # K^T diag(dec), v and the gates of every value head and [K^; Q^] of every qk head
     for sh in (inputs.QWEN27B, inputs.QWEN4B):
-        per_slot = sh.num_v_heads * (32768 + 16384 + 32768 + 32768 + 512) + sh.num_qk_heads * 32768
+        per_slot = sh.num_v_heads * (16384 + 16384 + 32768 + 32768 + 1024) + sh.num_qk_heads * 65536
         for N, T in ((4, 4 * 8192), (1, 229376), (3, 1000), (1, 0)):
             assert gdn.gdn_prefill_workspace_size(sh, N, T) == (T // 64 + N + 1) * per_slot + 1024
     # the conv pre-pass path: SiLU(conv) rows in fp32 plus norm factors and gates

@@ -175,3 +175,49 @@ def test_pieces_over_several_launches_equal_one_launch_bitwise():
                           st["S"].double().numpy(), st["win"].float().numpy())
         assert_out_close(o_all[a:b, h:h + 1], ref["o"], [0, b - a])
         assert_state_close(pools[0].state(3).cpu()[None, h:h + 1], ref["S"])
+
+
+def _both_paths(sh, lens, start, init, bt, seed, npages, fill_state=None, max_seq_len=0):
+    """The same call through the fused kernel (no workspace) and the chunk +
+    chain kernels (with one): outputs, pool pages and error words."""
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    ti = inputs.token_inputs(sh, int(cu[-1]), seed=seed)
+    w = inputs.conv_weights(sh, seed)
+    res = []
+    for ws in (False, None):
+        pool = gdn.StatePool(sh, npages, fill=0x3C)
+        if fill_state is not None:
+            page, st = fill_state
+            pool.state(page).copy_(st["S"][0].cuda())
+            pool.window(page).copy_(st["win"][0].cuda())
+        o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, start, init, bt,
+                                list(range(len(lens))), max_seq_len=max_seq_len, workspace=ws)
+        assert err == 0
+        res.append((o, pool.buf.cpu()))
+    return res
+
+
+@pytest.mark.parametrize("case", ["edges_gqa3", "resumed_27b", "pieces_27b"])
+def test_two_kernel_path_gives_the_fused_kernels_bits(case):
+    """The chunk + chain kernels split and multiply every operand as the fused
+    kernel does, so a call gives the same bits on either path: a prefix hit
+    reproduces a cold run's bits whichever path each call takes."""
+    if case == "edges_gqa3":
+        sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+        lens = [1, 63, 64, 65, 127, 128, 129, 300, 700]
+        bt, npages = _tables(lens, 128, len(lens))
+        res = _both_paths(sh, lens, [0] * len(lens), [-1] * len(lens), bt, 81, npages)
+    elif case == "resumed_27b":
+        sh = inputs.with_(inputs.QWEN27B, block_size=256)
+        st = inputs.random_state(sh, 1, seed=83)
+        res = _both_paths(sh, [700, 300], [512, 0], [5, -1], [[-1, -1, 6, 7], [8, -1, -1, -1]], 82, 9,
+                          fill_state=(5, st))
+    else:
+        sh = inputs.LayerShape(16, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
+        lens = [2048, 1800, 77, 1536]
+        assert gdn.gdn_prefill_plan_for(sh, len(lens), max(lens))["levels"] == 2
+        res = _both_paths(sh, lens, [0] * 4, [-1] * 4, [[5, 6], [7, -1], [-1, -1], [8, -1]], 84, 9,
+                          max_seq_len=max(lens))
+    (o_f, pool_f), (o_2, pool_2) = res
+    assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
+    assert torch.equal(pool_f, pool_2)
