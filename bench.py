@@ -781,7 +781,10 @@ def main():
     fl_gbs = rep.flush_bytes_per_layer() / (fl_ms / REP_LAYERS * 1e-3) / 1e9
     ver_gbs = rep.verify_bytes_per_layer() / (ver_ms / REP_LAYERS * 1e-3) / 1e9
     value = job_throughput(pre.tokens, world, pre_ms)
-    pre_launches = gdn.gdn_prefill_plan_for(PREFILL, N_SEQ, args.seq_len)["launches"]
+    pre_plan = gdn.gdn_prefill_plan_for(PREFILL, N_SEQ, args.seq_len)
+    # the call's own path (both give the same bits): its chain launches, the
+    # chunk kernel when it takes the two-kernel path, the window pass
+    pre_launches = pre_plan["launches"] + pre_plan["two_kernels"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
@@ -828,11 +831,11 @@ def main():
                          "timed from the first input copy to the last output copy of `steps` steps",
                 "link_note": "the host link of these boxes moves ~210 GB/s in and ~193 GB/s out (~295 GB/s "
                              "both ways, the same for SM-driven copies), so ~3.9 ms of a step is copies"},
-        # per step: prefill (the chunk kernel, the chain kernel's launches as
-        # the library plans them on this GPU, the window pass); decode 1 per
-        # layer; replay per layer: append 2 (tensor-core append, log_len),
-        # rollback 1, flush 2
-        "gpu_launches": args.steps * (1 + pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
+        # per step: prefill (the launches of the path the library takes on
+        # this GPU, + the window pass); decode 1 per layer; replay per layer:
+        # append 2 (tensor-core append, log_len), rollback 1, flush 2
+        "gpu_launches": args.steps * (pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
+        "prefill_path": "chunk + chain kernels" if pre_plan["two_kernels"] else "fused kernel",
         "prefill_chunk_launches": pre_launches,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }

@@ -33,10 +33,11 @@ __all__ = [
     "gdn_mixed_workspace_size", "gdn_mixed_step",
     "gdn_core_prefill_workspace_size", "gdn_core_prefill", "gdn_core_decode",
     "gdn_decode_step", "gdn_checkpoint_resume", "gdn_checkpoint_save", "gdn_replay_append",
-    "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "STATUS",
+    "gdn_replay_rollback", "gdn_replay_flush", "REPLAY_LOG_SLOTS", "PREFILL_AUTO", "PREFILL_FUSED", "PREFILL_TWO_KERNELS", "STATUS",
 ]
 
 REPLAY_LOG_SLOTS = 32
+PREFILL_AUTO, PREFILL_FUSED, PREFILL_TWO_KERNELS = 0, 1, 2   # gdn_prefill_args.path
 NOALLOC_SCRATCH_BYTES = 64 << 20   # GDN_NOALLOC_SCRATCH_BYTES
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED_SHAPE",
@@ -84,7 +85,8 @@ class _PrefillArgs(ctypes.Structure):
                 ("cu_seqlens", _P), ("start_pos", _P),
                 ("start_pos_host", _P), ("init_page_host", _P), ("x", _P), ("g", _P),
                 ("beta", _P), ("conv_w", _P), ("init_page", _P), ("block_table", _P),
-                ("out_slot", _P), ("o", _P), ("dev_error", _P), ("wait_cycles", ctypes.c_int64)]
+                ("out_slot", _P), ("o", _P), ("dev_error", _P), ("wait_cycles", ctypes.c_int64),
+                ("path", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class _DecodeArgs(ctypes.Structure):
@@ -117,7 +119,7 @@ class _ReplayArgs(ctypes.Structure):
 
 class _PrefillPlan(ctypes.Structure):
     _fields_ = [("chains", ctypes.c_int64), ("piece_chunks", ctypes.c_int64), ("levels", ctypes.c_int64),
-                ("ctas_per_launch", ctypes.c_int64), ("launches", ctypes.c_int64)]
+                ("ctas_per_launch", ctypes.c_int64), ("launches", ctypes.c_int64), ("two_kernels", ctypes.c_int64)]
 
 
 # --------------------------------------------------------------------------- loading
@@ -320,12 +322,13 @@ def gdn_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_tokens: i
 
 
 def gdn_prefill_plan_for(shape: LayerShape, num_seqs: int, max_seq_len: int, num_sms: int = 0,
-                         fused: bool = False) -> dict:
-    """The chain plan of one prefill call (num_sms <= 0: the current device's
-    SM count; fused: the fused kernel of a call without a workspace)."""
+                         path: int = 0) -> dict:
+    """The path and chain plan of one prefill call (num_sms <= 0: the current
+    device's SM count; path: PREFILL_AUTO as a call with a workspace resolves
+    it, or one of the two paths)."""
     out = _PrefillPlan()
     _check(load_library().gdn_prefill_plan_for(ctypes.byref(make_desc(shape)), num_seqs, max_seq_len, num_sms,
-                                               int(bool(fused)), ctypes.byref(out)), "gdn_prefill_plan_for")
+                                               int(path), ctypes.byref(out)), "gdn_prefill_plan_for")
     return {f: int(getattr(out, f)) for f, _ in _PrefillPlan._fields_}
 
 
@@ -341,7 +344,7 @@ def workspace_for(nbytes: int, device="cuda") -> torch.Tensor:
 # --------------------------------------------------------------------------- device entry points
 
 def _prefill_args(shape, *, cu_seqlens, start_pos, init_page, block_table, out_slot, x, g, beta, conv_w,
-                  o, dev_error, start_pos_host, init_page_host, max_seq_len, wait_cycles=0):
+                  o, dev_error, start_pos_host, init_page_host, max_seq_len, wait_cycles=0, path=0):
     n = int(cu_seqlens.numel()) - 1
     sph, keep1 = _host(start_pos_host, torch.int64, "start_pos_host")
     iph, keep2 = _host(init_page_host, torch.int32, "init_page_host")
@@ -354,21 +357,22 @@ def _prefill_args(shape, *, cu_seqlens, start_pos, init_page, block_table, out_s
                      _dev(init_page, torch.int32, "init_page"),
                      _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
                      _dev(out_slot, torch.int32, "out_slot"), _dev(o, shape.torch_out(), "o"),
-                     _dev(dev_error, torch.int32, "dev_error"), int(wait_cycles))
+                     _dev(dev_error, torch.int32, "dev_error"), int(wait_cycles), int(path), 0)
     return a, (keep1, keep2)
 
 
 def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page,
                         block_table, out_slot, x, g, beta, conv_w, o, dev_error,
                         start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
-                        wait_cycles: int = 0, stream=None, raise_on_error: bool = True) -> int:
+                        wait_cycles: int = 0, path: int = 0, stream=None, raise_on_error: bool = True) -> int:
     """Chunked prefill with block checkpoints (see gdn.h for the contract).
     Without `workspace` a scratch tensor of gdn_prefill_workspace_size bytes is
     taken from PyTorch's allocator for the call; `workspace=False` passes none
     (a tensor-core layer then takes the fused kernel).  `max_seq_len` (the
     longest sequence; 0: the call's total tokens) sizes the launch plan
     (gdn_prefill_plan_for): a batch of several sequences runs best with the
-    exact value.  `wait_cycles` bounds the device-side waits (gdn.h)."""
+    exact value.  `wait_cycles` bounds the device-side waits; `path` picks the
+    tensor-core path (PREFILL_AUTO, PREFILL_FUSED, PREFILL_TWO_KERNELS; gdn.h)."""
     lib = load_library()
     n = int(cu_seqlens.numel()) - 1
     if workspace is None:
@@ -376,7 +380,8 @@ def gdn_prefill_chunked(shape: LayerShape, pool: StatePool, *, cu_seqlens, start
     a, keep = _prefill_args(shape, cu_seqlens=cu_seqlens, start_pos=start_pos, init_page=init_page,
                             block_table=block_table, out_slot=out_slot, x=x, g=g, beta=beta, conv_w=conv_w,
                             o=o, dev_error=dev_error, start_pos_host=start_pos_host,
-                            init_page_host=init_page_host, max_seq_len=max_seq_len, wait_cycles=wait_cycles)
+                            init_page_host=init_page_host, max_seq_len=max_seq_len, wait_cycles=wait_cycles,
+                            path=path)
     if workspace is False:
         ws, wsb = None, 0
     else:

@@ -82,15 +82,20 @@ size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
 }
 
 gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
-                                int32_t num_sms, int32_t fused, gdn_prefill_plan* out) {
+                                int32_t num_sms, int32_t path, gdn_prefill_plan* out) {
   if (!desc || !out || gdn_conv_dim(desc) <= 0 || num_seqs < 0 || num_seqs > kMaxGrid || max_seq_len < 0)
     return GDN_ERR_INVALID_ARG;
   if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                             desc->block_size))
     return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (path < GDN_PREFILL_AUTO || path > GDN_PREFILL_TWO_KERNELS) return GDN_ERR_INVALID_ARG;
   const int sms = num_sms > 0 ? num_sms : tc_prefill_sm_count();
-  const PrefillSchedule sc = fused ? tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms)
-                                   : tc_chain_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms);
+  const bool two = path == GDN_PREFILL_TWO_KERNELS ||
+                   (path == GDN_PREFILL_AUTO &&
+                    tc_prefill_two_kernels_faster(desc->num_qk_heads, desc->num_v_heads, num_seqs, max_seq_len, sms));
+  const PrefillSchedule sc = two ? tc_chain_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms)
+                                 : tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms);
+  out->two_kernels = two ? 1 : 0;
   out->chains = sc.nchains;
   out->piece_chunks = sc.piece;
   out->levels = sc.levels;
@@ -146,10 +151,20 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
                            : gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
   const bool tc = tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                                        desc->block_size);
-  // a tensor-core layer without a workspace takes the fused kernel
-  const bool two_kernels = tc && !core && !(workspace == nullptr && workspace_bytes == 0);
-  if (need > 0 && (tc && !core ? two_kernels : true) &&
-      (!workspace || workspace_bytes < need || !aligned16(workspace)))
+  if (a->path < GDN_PREFILL_AUTO || a->path > GDN_PREFILL_TWO_KERNELS || a->reserved != 0)
+    return GDN_ERR_INVALID_ARG;
+  const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
+  // a tensor-core layer: the two kernels when asked for, or (AUTO) when a
+  // workspace is given and they are expected to be faster; else the fused one
+  const bool has_ws = !(workspace == nullptr && workspace_bytes == 0);
+  const bool two_kernels =
+      tc && !core &&
+      (a->path == GDN_PREFILL_TWO_KERNELS ||
+       (a->path == GDN_PREFILL_AUTO && has_ws &&
+        tc_prefill_two_kernels_faster(desc->num_qk_heads, desc->num_v_heads, a->num_seqs, max_len,
+                                      tc_prefill_sm_count())));
+  const bool needs_ws = core || !tc || two_kernels || (a->path == GDN_PREFILL_AUTO && has_ws);
+  if (need > 0 && needs_ws && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
   ScanParams p = base_scan(desc, pool);
   p.num_seqs = a->num_seqs;
@@ -183,7 +198,6 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
   } else if (need > 0 && !tc) {
     bind_workspace(p, workspace, a->total_tokens);
   }
-  const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
   return cuda_status(launch_prefill(p, two_kernels ? workspace : nullptr, max_len, desc->head_dim_k,
                                     desc->head_dim_v, desc->in_dtype, desc->out_dtype, cs));
 }
@@ -315,9 +329,13 @@ gdn_status gdn_mixed_step(const gdn_layer_desc* desc, const gdn_pool* pool, cons
   const size_t need = gdn_mixed_workspace_size(desc, a->num_seqs, a->total_tokens);
   const bool tc = tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                                        desc->block_size);
-  // as gdn_prefill_chunked: a tensor-core layer without a workspace takes the fused kernel
-  const bool two_kernels = tc && !(workspace == nullptr && workspace_bytes == 0);
-  if (n_dec < a->num_seqs && need > 0 && (!tc || two_kernels) &&
+  // as gdn_prefill_chunked with GDN_PREFILL_AUTO
+  const bool has_ws = !(workspace == nullptr && workspace_bytes == 0);
+  const int64_t mixed_max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
+  const bool two_kernels = tc && has_ws &&
+                           tc_prefill_two_kernels_faster(desc->num_qk_heads, desc->num_v_heads, a->num_seqs,
+                                                         mixed_max_len, tc_prefill_sm_count());
+  if (n_dec < a->num_seqs && need > 0 && (!tc || has_ws) &&
       (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

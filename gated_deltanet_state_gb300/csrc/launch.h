@@ -97,5 +97,8 @@ cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t
 size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens);
 PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st);
+// Whether the two kernels beat the fused one for a call of num_seqs sequences
+// of at most max_len tokens on `sms` SMs (both give the same bits).
+bool tc_prefill_two_kernels_faster(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms);
 
 }  // namespace gdn

@@ -955,6 +955,26 @@ PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms
   return tc_prefill_schedule_cost(Hv, num_seqs, max_len, sms, kChainLaunchCost);
 }
 
+// A model of both paths in units of the fused kernel's chunk time (one chunk
+// of one chain, ~13.5 us on a GB300): the fused kernel runs its chains in
+// rounds of `sms`, a chunk at a time, plus ~1.5 for its launch; the two
+// kernels run every chunk of every qk head in parallel (a chunk CTA costs
+// ~0.55 + 0.55 G fused chunk times for G value heads a qk head: 29.5 us at
+// G = 3), then the chains at ~0.45 a chunk (6 us), plus ~3 for two launches.
+// Measured at 1-8 sequences of 8,192 and 1 of 65,536 and 229,376 tokens of
+// the 27B-shaped layer: the two kernels win at one or two sequences (0.68
+// and 0.89 of the fused time), lose from three on.
+bool tc_prefill_two_kernels_faster(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms) {
+  if (sms <= 0 || num_seqs <= 0 || max_len <= 0 || Hqk <= 0) return false;
+  const double maxc = (double)((max_len + kC - 1) / kC);
+  const double chains = (double)Hv * num_seqs;
+  const double rounds = chains > sms ? chains / sms : 1.0;
+  const double G = (double)Hv / Hqk;
+  const double fused = rounds * maxc + 1.5;
+  const double two = (double)num_seqs * maxc * Hqk / sms * (0.55 + 0.55 * G) + rounds * maxc * 0.45 + 3.0;
+  return two < 0.95 * fused;
+}
+
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   if ((int64_t)p.Hv * p.num_seqs > (int64_t)INT32_MAX) return cudaErrorInvalidValue;

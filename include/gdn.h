@@ -258,7 +258,14 @@ typedef struct gdn_prefill_args {
                                     checkpoints or windows.  < 0 makes every
                                     such wait report a timeout at once (a test
                                     of that path: nothing is written)         */
+  int32_t path;                  /* GDN_PREFILL_AUTO (0), _FUSED or
+                                    _TWO_KERNELS (tensor-core layers; see
+                                    gdn_prefill_workspace_size)               */
+  int32_t reserved;              /* 0                                         */
 } gdn_prefill_args;
+
+/* How a tensor-core layer's prefill runs (both give the same bits). */
+enum { GDN_PREFILL_AUTO = 0, GDN_PREFILL_FUSED = 1, GDN_PREFILL_TWO_KERNELS = 2 };
 
 /* Device workspace bytes gdn_prefill_chunked needs for a call of num_seqs
  * sequences with total_tokens tokens.
@@ -268,14 +275,18 @@ typedef struct gdn_prefill_args {
  * a chunk kernel computes, for every 64-token chunk of the call at once,
  * everything that does not depend on the state (conv, norms, the chunk's
  * triangular solve and the products that fold it in) and leaves them here as
- * ready operand images (about 80 KB per chunk and value head plus 64 KB per
- * chunk and qk head); a chain kernel then carries each (sequence, value head)
- * state through its chunks with a few tensor-core products per chunk.  Such
- * a layer may instead pass NULL with workspace_bytes 0: it then takes one
- * fused kernel that needs no scratch (slower on a long sequence, which it
- * runs on as many SMs as the sequence has value heads).  The two paths agree
- * with the same bounds but not bit for bit: a resume reproduces a cold run's
- * bits when both take the same path, so serve a layer with one of them.
+ * the fused kernel's own operand images (about 97 KB per chunk and value
+ * head plus 64 KB per chunk and qk head); a chain kernel then carries each
+ * (sequence, value head) state through its chunks with the fused kernel's
+ * state products.  The other path is one fused kernel that runs a chain's
+ * chunks one after another on one SM and needs no scratch.  Both split and
+ * multiply every operand alike and give the same bits, so the choice is
+ * speed only: the two kernels win when a call's chains leave SMs idle (a
+ * long prompt of one or two sequences), the fused kernel when they fill
+ * them.  With GDN_PREFILL_AUTO a call takes the two kernels when it has a
+ * workspace and a model of both paths' times (gdn_prefill_plan_for) favours
+ * them; a call without a workspace (NULL, workspace_bytes 0) takes the fused
+ * kernel.
  *
  * Other layers run a conv pre-pass whose SiLU(conv) rows (fp32, computed
  * once and shared by every head that reads them), q / k norm factors and
@@ -287,10 +298,10 @@ typedef struct gdn_prefill_args {
 size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
                                   int64_t total_tokens);
 
-/* How gdn_prefill_chunked runs the chain of a layer on the tensor-core path
- * (fused != 0: the fused kernel of a call without a workspace; else the
- * chain kernel of the two-kernel path).  Each (sequence, value head) chain
- * runs on one SM, its chunks in order.  With at least as many chains as SMs and long chains,
+/* How gdn_prefill_chunked runs a call of a layer on the tensor-core path:
+ * the path (two_kernels; `path` GDN_PREFILL_AUTO resolves it as a call with
+ * a workspace would) and the chain plan of that path.  Each (sequence, value
+ * head) chain runs on one SM, its chunks in order.  With at least as many chains as SMs and long chains,
  * whole chains would leave SMs idle in the last round, so the chains are cut
  * into pieces of piece_chunks chunks and run as `launches` launches of up to
  * ctas_per_launch CTAs: all chains' first pieces, then all second pieces, and
@@ -306,6 +317,7 @@ typedef struct gdn_prefill_plan {
   int64_t ctas_per_launch;  /* CTAs of each launch (the last may have fewer) */
   int64_t launches;         /* chain launches (+1 window pass; the two-kernel
                                path also launches the chunk kernel once)    */
+  int64_t two_kernels;      /* 1: the chunk + chain kernels, 0: the fused one */
 } gdn_prefill_plan;
 
 /* The plan of one gdn_prefill_chunked call with num_seqs sequences and the
@@ -314,7 +326,7 @@ typedef struct gdn_prefill_plan {
  * Host-only; launches nothing.  GDN_ERR_UNSUPPORTED_SHAPE for a layer on the
  * conv pre-pass path, GDN_ERR_INVALID_ARG for a malformed argument. */
 gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, int64_t max_seq_len,
-                                int32_t num_sms, int32_t fused, gdn_prefill_plan* out);
+                                int32_t num_sms, int32_t path, gdn_prefill_plan* out);
 
 gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
                                const gdn_prefill_args* args, void* workspace,

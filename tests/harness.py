@@ -130,7 +130,7 @@ def dev(t, dtype=None):
 
 
 def run_prefill(shape, pool, x, g, beta, conv_w, cu, start, init_page, block_table, out_slot,
-                raise_on_error=True, max_seq_len=0, workspace=None):
+                raise_on_error=True, max_seq_len=0, workspace=None, path=0):
     """One gdn_prefill_chunked call; returns (o on the host, device error code).
     workspace=False passes none (a tensor-core layer then takes the fused kernel)."""
     T = int(cu[-1])
@@ -144,7 +144,7 @@ def run_prefill(shape, pool, x, g, beta, conv_w, cu, start, init_page, block_tab
         init_page=dev(init_page, torch.int32), block_table=dev(bt), out_slot=dev(out_slot, torch.int32),
         x=dev(x), g=dev(g, torch.float32), beta=dev(beta, torch.float32), conv_w=dev(conv_w, torch.float32),
         o=o, dev_error=err, start_pos_host=list(start), init_page_host=list(init_page),
-        raise_on_error=raise_on_error, max_seq_len=max_seq_len, workspace=workspace)
+        raise_on_error=raise_on_error, max_seq_len=max_seq_len, workspace=workspace, path=path)
     torch.cuda.synchronize()
     return o.cpu(), int(err.item()), st
 

@@ -184,14 +184,14 @@ def _both_paths(sh, lens, start, init, bt, seed, npages, fill_state=None, max_se
     ti = inputs.token_inputs(sh, int(cu[-1]), seed=seed)
     w = inputs.conv_weights(sh, seed)
     res = []
-    for ws in (False, None):
+    for ws, path in ((False, gdn.PREFILL_FUSED), (None, gdn.PREFILL_TWO_KERNELS)):
         pool = gdn.StatePool(sh, npages, fill=0x3C)
         if fill_state is not None:
             page, st = fill_state
             pool.state(page).copy_(st["S"][0].cuda())
             pool.window(page).copy_(st["win"][0].cuda())
         o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, start, init, bt,
-                                list(range(len(lens))), max_seq_len=max_seq_len, workspace=ws)
+                                list(range(len(lens))), max_seq_len=max_seq_len, workspace=ws, path=path)
         assert err == 0
         res.append((o, pool.buf.cpu()))
     return res

@@ -49,12 +49,13 @@ LENS = [0, 64, 500, 1024, 2048, 8192, 229376]
 SMS = [152, 148, 132, 16]
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["fused", "chain"])
+@pytest.mark.parametrize("path", [gdn.PREFILL_FUSED, gdn.PREFILL_TWO_KERNELS], ids=["fused", "chain"])
 @pytest.mark.parametrize("Hv,N", SHAPES)
-def test_plan_runs_every_piece_once_in_order(Hv, N, fused):
+def test_plan_runs_every_piece_once_in_order(Hv, N, path):
     sh = inputs.LayerShape(max(1, Hv // 3) if Hv % 3 == 0 else Hv, Hv, 128, 128, block_size=896, chunk_size=64)
     for max_len, sms in itertools.product(LENS, SMS):
-        plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms, fused)
+        plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms, path)
+        assert plan.pop("two_kernels") == (path == gdn.PREFILL_TWO_KERNELS)
         assert plan["chains"] == Hv * N
         if plan["levels"] > 1:
             P = plan["piece_chunks"]
@@ -79,12 +80,24 @@ def test_benchmark_shape_plan():
     # 4 x 8,192 tokens of the 27B-shaped layer on 152 SMs: 44-chunk pieces
     # (the last 40), three (level, sequence) pairs of 48 CTAs a launch, 12
     # pairs in 4 launches: ~4 x 44 chunk times against 2 x 128 in one launch
-    for fused in (True, False):
-        plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152, fused)
-        assert plan == {"chains": 192, "piece_chunks": 44, "levels": 3, "ctas_per_launch": 144, "launches": 4}
+    for path in (gdn.PREFILL_FUSED, gdn.PREFILL_TWO_KERNELS):
+        plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152, path)
+        assert plan == {"chains": 192, "piece_chunks": 44, "levels": 3, "ctas_per_launch": 144, "launches": 4,
+                        "two_kernels": int(path == gdn.PREFILL_TWO_KERNELS)}
         # one long sequence (48 chains) and a large batch (3,072 chains) stay one launch
-        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, fused)["launches"] == 1
-        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152, fused)["launches"] == 1
+        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, path)["launches"] == 1
+        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152, path)["launches"] == 1
+
+
+def test_auto_path_takes_the_two_kernels_where_chains_leave_sms_idle():
+    """The model behind GDN_PREFILL_AUTO (both paths give the same bits): on
+    152 SMs the 27B-shaped layer's one or two long sequences (48 or 96 chains)
+    take the two kernels, three or more sequences the fused one."""
+    auto = lambda N, L: gdn.gdn_prefill_plan_for(inputs.QWEN27B, N, L, 152)["two_kernels"]
+    assert auto(1, 8192) == 1 and auto(2, 8192) == 1 and auto(1, 229376) == 1 and auto(1, 65536) == 1
+    assert auto(3, 8192) == 0 and auto(4, 8192) == 0 and auto(8, 8192) == 0 and auto(64, 8192) == 0
+    # a one-chunk call is no work for either: the fused kernel
+    assert auto(1, 64) == 0
 
 
 def test_plan_rejects_the_scan_path_and_bad_arguments():
