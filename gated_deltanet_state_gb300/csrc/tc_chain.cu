@@ -53,7 +53,7 @@ constexpr uint32_t kImgKQ = 65536;   // [K^; Q^] hi | lo: 128 rows x 128 k, two 
 constexpr uint32_t kImgT = 16384;    // T hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgP = 16384;    // P hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgK = 32768;    // K^T diag(dec) hi | lo: 128 rows (c) x 64 k (j)
-constexpr uint32_t kImgV = 32768;    // v fp32 [128 channels][64 rows]
+constexpr uint32_t kImgV = 32768;    // v fp32 [64 rows][128 channels]
 constexpr uint32_t kImgG = 1024;     // G, gam, dec, b fp32 [4][64]
 
 struct ChunkWs {
@@ -106,28 +106,27 @@ constexpr uint32_t kCkCols = 128;   // tensor memory of the chunk kernel
 constexpr uint32_t kCkGram = 0;     // [K^ K^T; Q^ K^T]: lanes 0-63 k^_i.k^_j, 64-127 q^_i.k^_j
 constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = row
 
-// ---- shared memory of the chain kernel: one buffer per image, each reloaded
-// as soon as the product that reads it is done ----------------------------------
+// ---- shared memory of the chain kernel: T and P (with the gates) in two
+// buffers, the others in one, each reloaded as soon as its reader is done -------
 struct ChSmem {
   static constexpr uint32_t KQ = 0;                  // [K^; Q^] hi | lo
   static constexpr uint32_t KT = KQ + kImgKQ;        // K^T diag(dec) hi | lo
-  static constexpr uint32_t TB = KT + kImgK;         // T hi | lo
-  static constexpr uint32_t PB = TB + kImgT;         // P hi | lo
-  static constexpr uint32_t UT = PB + kImgP;         // R^T, then U^T: hi [128][64], lo at +16 KB
-  static constexpr uint32_t VS = UT + 32768;         // v of the next chunk, fp32 [128][64]
+  static constexpr uint32_t TB = KT + kImgK;         // T hi | lo [2]
+  static constexpr uint32_t PB = TB + 2 * kImgT;     // P hi | lo [2]
+  static constexpr uint32_t VS = PB + 2 * kImgP;     // v fp32 [64 rows][128 channels]
   static constexpr uint32_t OT = VS + kImgV;         // outputs bf16 [64 rows][128 dv]
   static constexpr uint32_t G = OT + 16384;          // gate sets [2][4][64]
   static constexpr uint32_t MBAR = G + 2 * kImgG;
-  // mbarriers: the images [K^; Q^], K~ | P, T, v, the gates of two chunks;
-  // then the products S0 [K^; Q^]^T, R T^T, the state update, U^T P^T
-  static constexpr int kKQ = 0, kKP = 1, kTb = 2, kVb = 3, kGb = 4, kSK = 6, kU = 7, kS = 8, kUP = 9, kBars = 10;
+  // mbarriers: the images [K^; Q^], K~, T [2], P | gates [2], v; then the
+  // products S0 [K^; Q^]^T, R T^T, the state update, U^T P^T
+  static constexpr int kKQ = 0, kKT = 1, kTb = 2, kPG = 4, kVb = 6, kSK = 7, kU = 8, kS = 9, kUP = 10, kBars = 11;
   static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]: last chunk each was armed for
   static constexpr uint32_t TSLOT = ARMED + 8 * kBars;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
+  static constexpr bool two_buffers(int k) { return k == kTb || k == kTb + 1 || k == kPG || k == kPG + 1; }
 };
-static_assert(ChSmem::KT % 1024 == 0 && ChSmem::TB % 1024 == 0 && ChSmem::PB % 1024 == 0 && ChSmem::UT % 1024 == 0 &&
-                  ChSmem::OT % 1024 == 0,
+static_assert(ChSmem::KT % 1024 == 0 && ChSmem::TB % 1024 == 0 && ChSmem::PB % 1024 == 0 && ChSmem::OT % 1024 == 0,
               "operand images must be 1024-byte aligned");
 static_assert(ChSmem::ALLOC <= 232448, "chain kernel shared memory exceeds the per-CTA limit");
 
@@ -137,9 +136,10 @@ constexpr uint32_t kChS = 0;        // S fp32 [128][128]
 constexpr uint32_t kChSK = 128;     // S0 K^T fp32 [128][64] (then S0 Q^T: one product)
 constexpr uint32_t kChSQ = 192;     // S0 Q^T
 constexpr uint32_t kChU = 256;      // U^T = R T^T, then U^T P^T
-constexpr uint32_t kChV = 320;      // v, lane = channel, column = row
-constexpr uint32_t kChS0H = 384;    // S0 hi, bf16 pairs [128][64] (the A operand of S0 [K^; Q^]^T)
-constexpr uint32_t kChS0L = 448;    // S0 lo
+constexpr uint32_t kChS0H = 320;    // S0 hi, bf16 pairs [128][64] (the A operand of S0 [K^; Q^]^T)
+constexpr uint32_t kChS0L = 384;    // S0 lo
+constexpr uint32_t kChUH = 448;     // R^T, then U^T: hi, bf16 pairs [128][32] (the A operand of the rest)
+constexpr uint32_t kChUL = 480;     // lo
 
 __device__ __forceinline__ bool work_wait(uint64_t* m, uint32_t parity, long long lim) {
   return lim >= 0 && tc::mbar_wait_bounded(m, parity, lim);
@@ -513,16 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
           tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
         }
-        // v of channel `row`, rows [32 (tid >> 7), +32) -> the workspace (fp32 [r][i])
-        float* dst = ws.v + (slot * p.Hv + h) * (int64_t)(kImgV / 4) + row * 64 + 32 * (tid >> 7);
+        // v of channel `row`, rows [32 (tid >> 7), +32) -> the workspace (fp32
+        // [i][r]: a warp's stores of one row are 128 contiguous bytes)
+        float* dst = ws.v + (slot * p.Hv + h) * (int64_t)(kImgV / 4) + 32 * (tid >> 7) * D + row;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[16];
           tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            reinterpret_cast<float4*>(dst + 16 * hh)[c4] =
-                make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+          for (int e = 0; e < 16; ++e) dst[(16 * hh + e) * D] = v[e];
         }
       }
       tc::fence_async_smem();
@@ -559,11 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Chain kernel: grid (Hv, pieces), one CTA per (value head, (level, sequence))
 // ============================================================================
 // Per chunk c: (1) the state after chunk c - 1 (checkpointed at a block
-// boundary) split into tensor memory as the A operand, gam_C S0 back, v of
-// chunk c into tensor memory; then S0 [K^; Q^]^T.  (2) The outputs of chunk
-// c - 1; R into the U^T operand; then U^T = R T^T.  (3) U into the operand;
-// then the state update S += U^T (K^T diag(dec))^T and U^T P^T.  Every image
-// of chunk c + 1 is requested as soon as the product reading chunk c's is done.
+// boundary) split into tensor memory as the A operand, gam_C S0 back; then
+// S0 [K^; Q^]^T.  (2) The outputs of chunk c - 1; R into the tensor-memory
+// operand; then U^T = R T^T.  (3) U into that operand; then the state update
+// S += U^T (K^T diag(dec))^T and U^T P^T.  Every image of chunk c + 1 is
+// requested as soon as the reader of chunk c's (or c - 1's, for the two
+// buffers of T, P and the gates) is done.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws,
                     const PieceMap pm, int64_t max_chunks) {
@@ -638,28 +638,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::bulk_load(sm + ChSmem::KQ + 32768, src + 32768, 32768, mbar + ChSmem::kKQ);
     armed[ChSmem::kKQ] = c;
   };
-  auto load_kp = [&](int64_t c) {
-    const int64_t hv = hv_of(c);
-    tc::mbar_expect_tx(mbar + ChSmem::kKP, kImgK + kImgP);
-    tc::bulk_load(sm + ChSmem::KT, ws.k + hv * kImgK, kImgK, mbar + ChSmem::kKP);
-    tc::bulk_load(sm + ChSmem::PB, ws.pm + hv * kImgP, kImgP, mbar + ChSmem::kKP);
-    armed[ChSmem::kKP] = c;
+  auto load_kt = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kKT, kImgK);
+    tc::bulk_load(sm + ChSmem::KT, ws.k + hv_of(c) * kImgK, kImgK, mbar + ChSmem::kKT);
+    armed[ChSmem::kKT] = c;
   };
   auto load_t = [&](int64_t c) {
-    tc::mbar_expect_tx(mbar + ChSmem::kTb, kImgT);
-    tc::bulk_load(sm + ChSmem::TB, ws.t + hv_of(c) * kImgT, kImgT, mbar + ChSmem::kTb);
-    armed[ChSmem::kTb] = c;
+    const int b = (int)(c & 1);
+    tc::mbar_expect_tx(mbar + ChSmem::kTb + b, kImgT);
+    tc::bulk_load(sm + ChSmem::TB + b * kImgT, ws.t + hv_of(c) * kImgT, kImgT, mbar + ChSmem::kTb + b);
+    armed[ChSmem::kTb + b] = c;
+  };
+  auto load_pg = [&](int64_t c) {   // P and the gates
+    const int b = (int)(c & 1);
+    const int64_t hv = hv_of(c);
+    tc::mbar_expect_tx(mbar + ChSmem::kPG + b, kImgG + kImgP);
+    tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv * (kImgG / 4), kImgG, mbar + ChSmem::kPG + b);
+    tc::bulk_load(sm + ChSmem::PB + b * kImgP, ws.pm + hv * kImgP, kImgP, mbar + ChSmem::kPG + b);
+    armed[ChSmem::kPG + b] = c;
   };
   auto load_v = [&](int64_t c) {
     tc::mbar_expect_tx(mbar + ChSmem::kVb, kImgV);
     tc::bulk_load(sm + ChSmem::VS, ws.v + hv_of(c) * (kImgV / 4), kImgV, mbar + ChSmem::kVb);
     armed[ChSmem::kVb] = c;
-  };
-  auto load_g = [&](int64_t c) {
-    const int b = (int)(c & 1);
-    tc::mbar_expect_tx(mbar + ChSmem::kGb + b, kImgG);
-    tc::bulk_load(sm + ChSmem::G + b * kImgG, ws.g + hv_of(c) * (kImgG / 4), kImgG, mbar + ChSmem::kGb + b);
-    armed[ChSmem::kGb + b] = c;
   };
   auto gates_of = [&](int64_t c) { return reinterpret_cast<const float*>(sm + ChSmem::G + (int)(c & 1) * kImgG); };
   // the checkpoint page of a block boundary at absolute position pos (-1: none)
@@ -699,13 +700,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
+  // 16 fp32 values (rows [16 quarter, +16) of state row `row`) as bf16 hi / lo
+  // pairs into the tensor-memory A operand
+  auto split_to_tmem = [&](const float (&a)[16]) {
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tc::split_pair(a[2 * e], a[2 * e + 1], hi[e], lo[e]);
+    tc::tmem_st8(tbase + tlane + kChUH + 8 * quarter, hi);
+    tc::tmem_st8(tbase + tlane + kChUL + 8 * quarter, lo);
+    tc::tmem_st_wait();
+  };
 
   if (tid == kMma && cb < ce) {
+    load_pg(cb);
     load_kq(cb);
     load_v(cb);
-    load_g(cb);
     load_t(cb);
-    load_kp(cb);
+    load_kt(cb);
   }
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
@@ -726,12 +737,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (; c < ce; ++c) {
     const int b = (int)(c & 1);
     const uint32_t par = (uint32_t)((c - cb) & 1);
-    const uint32_t gpar = (uint32_t)(((c - cb) >> 1) & 1);
+    const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
     if (worker) {
       // ---- (1) the state after chunk c - 1: checkpoint, split into tensor
-      // memory, gam_C S0 back; v of this chunk into tensor memory
+      // memory, gam_C S0 back
       if (c > cb) mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
-      ok = work_wait(mbar + ChSmem::kGb + b, gpar, wlim) && ok;
+      ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
       const float gC = gates_of(c)[64 + C - 1];
       const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
       float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
@@ -758,17 +769,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
       tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
-      ok = work_wait(mbar + ChSmem::kVb, par, wlim) && ok;
-      {
-        const float4* vs = reinterpret_cast<const float4*>(sm + ChSmem::VS) + (row * 64 + 16 * quarter) / 4;
-        float v[16];
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const float4 f = vs[c4];
-          v[4 * c4] = f.x; v[4 * c4 + 1] = f.y; v[4 * c4 + 2] = f.z; v[4 * c4 + 3] = f.w;
-        }
-        tc::tmem_st16(tbase + tlane + kChV + 16 * quarter, v);
-      }
       tc::tmem_st_wait();
     }
     ok = cta_sync_ok(ok);
@@ -780,82 +780,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  sbase + ChSmem::KQ + 32768, tc::idesc_bf16_f32(128, 128), false);
       tc::mma_commit(mbar + ChSmem::kSK);
       armed[ChSmem::kSK] = c;
-      // v of the next chunk (this one's is in tensor memory)
-      if (c + 1 < ce) load_v(c + 1);
+      // T of the next chunk (its buffer's last reader, R T^T of chunk c - 1, is done)
+      if (c + 1 < ce) load_t(c + 1);
     }
     if (worker) {
       // ---- (2) the previous chunk's outputs (its U^T P^T is done), then R_i =
-      // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16)
+      // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16),
+      // into the tensor-memory operand
       if (c > cb) {
         mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
         outputs(c - 1, sq);
         tc::fence_async_smem();
       }
+      ok = work_wait(mbar + ChSmem::kVb, par, wlim) && ok;
       mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
       const float* gs = gates_of(c);
       const float* gam = gs + 64;
       const float* bv = gs + 192;
       const int i0 = 16 * quarter;
-      float a[16], v[16];
-      tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChV + i0, a, v);
+      const float* vs = reinterpret_cast<const float*>(sm + ChSmem::VS) + i0 * D + row;
+      float a[16];
+      tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
       tc::tmem_ld16(tbase + tlane + kChSQ + i0, sq);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], v[e]);
-#pragma unroll
-      for (int c8 = 0; c8 < 2; ++c8) {
-        const uint32_t off = tc::sw128_offset(row, i0 + 8 * c8, 128);
-        tc::store_split8(sm + ChSmem::UT + off, sm + ChSmem::UT + 16384 + off, a + 8 * c8);
-      }
-      tc::fence_async_smem();
+      for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vs[e * D]);
+      split_to_tmem(a);
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // the previous chunk's output tile; [K^; Q^] of the next chunk (S0 [K^; Q^]^T is done)
+      // U^T = R T^T (M 128, N 64, K 64)
+      ok = work_wait(mbar + ChSmem::kTb + b, bpar, wlim) && ok;
+      tc::mma3_ts<C / 16, 0>(tbase + kChU, tbase + kChUH, tbase + kChUL, sbase + ChSmem::TB + b * kImgT,
+                             sbase + ChSmem::TB + b * kImgT + 8192, tc::idesc_bf16_f32(128, 64), false);
+      tc::mma_commit(mbar + ChSmem::kU);
+      armed[ChSmem::kU] = c;
+      // the previous chunk's output tile; the next chunk's gates and P (their
+      // buffer's last readers, the outputs and U^T P^T of chunk c - 1, are
+      // done), [K^; Q^] (S0 [K^; Q^]^T is done) and v (R has read it)
       if (c > cb && tma_out && full_chunk(c - 1)) {
         tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
         tc::bulk_commit();
       }
-      if (c + 1 < ce) load_kq(c + 1);
-      // U^T = R T^T (M 128, N 64, K 64)
-      ok = work_wait(mbar + ChSmem::kTb, par, wlim) && ok;
-      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChU, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::TB,
-                                   sbase + ChSmem::TB + 8192, tc::idesc_bf16_f32(128, 64), false);
-      tc::mma_commit(mbar + ChSmem::kU);
-      armed[ChSmem::kU] = c;
-      // the next chunk's gates: their buffer's last reader, the outputs of chunk c - 1, is done
-      if (c + 1 < ce) load_g(c + 1);
+      if (c + 1 < ce) {
+        load_pg(c + 1);
+        load_kq(c + 1);
+        load_v(c + 1);
+      }
       tc::bulk_wait_read();   // the tile, before the next chunk's outputs
     }
     if (worker) {
-      // ---- (3) U (rows r, K = i) as the operand of the state update and U^T P^T
+      // ---- (3) U (rows r, K = i) into the operand of the state update and U^T P^T
       mma_wait(mbar + ChSmem::kU, par, ok, wlim);
       float u[16];
       tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
-#pragma unroll
-      for (int c8 = 0; c8 < 2; ++c8) {
-        const uint32_t off = tc::sw128_offset(row, 16 * quarter + 8 * c8, 128);
-        tc::store_split8(sm + ChSmem::UT + off, sm + ChSmem::UT + 16384 + off, u + 8 * c8);
-      }
-      tc::fence_async_smem();
+      split_to_tmem(u);
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      // T of the next chunk (R T^T is done)
-      if (c + 1 < ce) load_t(c + 1);
       // S += U^T (K^T diag(dec))^T (M 128, N 128, K 64) first, then U^T P^T (M 128, N 64, K 64)
-      ok = work_wait(mbar + ChSmem::kKP, par, wlim) && ok;
-      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChS, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::KT,
-                                   sbase + ChSmem::KT + 16384, tc::idesc_bf16_f32(128, 128), true);
+      ok = work_wait(mbar + ChSmem::kKT, par, wlim) && ok;
+      tc::mma3_ts<C / 16, 0>(tbase + kChS, tbase + kChUH, tbase + kChUL, sbase + ChSmem::KT,
+                             sbase + ChSmem::KT + 16384, tc::idesc_bf16_f32(128, 128), true);
       tc::mma_commit(mbar + ChSmem::kS);
-      tc::mma3_sw128<C / 16, 0, 0>(tbase + kChU, sbase + ChSmem::UT, sbase + ChSmem::UT + 16384, sbase + ChSmem::PB,
-                                   sbase + ChSmem::PB + 8192, tc::idesc_bf16_f32(128, 64), false);
+      ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
+      tc::mma3_ts<C / 16, 0>(tbase + kChU, tbase + kChUH, tbase + kChUL, sbase + ChSmem::PB + b * kImgP,
+                             sbase + ChSmem::PB + b * kImgP + 8192, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + ChSmem::kUP);
       armed[ChSmem::kS] = armed[ChSmem::kUP] = c;
-      // K~ and P of the next chunk once both products have read this chunk's
+      // K~ of the next chunk once the state update has read this chunk's
       if (c + 1 < ce) {
-        if (work_wait(mbar + ChSmem::kUP, par, wlim)) load_kp(c + 1);
+        if (work_wait(mbar + ChSmem::kS, par, wlim)) load_kt(c + 1);
         else ok = false;
       }
     }
@@ -903,8 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < ChSmem::kBars; ++k) {
         const int64_t a = armed[k];
         if (a < cb) continue;
-        const bool two = k == ChSmem::kGb || k == ChSmem::kGb + 1;
-        const uint32_t ph = (uint32_t)((two ? (a - cb) >> 1 : a - cb) & 1);
+        const uint32_t ph = (uint32_t)((ChSmem::two_buffers(k) ? (a - cb) >> 1 : a - cb) & 1);
         tc::mbar_wait_bounded(mbar + k, ph, kWaitDefault);
       }
     }
