@@ -782,9 +782,9 @@ def main():
     ver_gbs = rep.verify_bytes_per_layer() / (ver_ms / REP_LAYERS * 1e-3) / 1e9
     value = job_throughput(pre.tokens, world, pre_ms)
     pre_plan = gdn.gdn_prefill_plan_for(PREFILL, N_SEQ, args.seq_len)
-    # the call's own path (both give the same bits): its chain launches, the
-    # chunk kernel when it takes the two-kernel path, the window pass
-    pre_launches = pre_plan["launches"] + pre_plan["two_kernels"]
+    # the call's own path (both give the same bits): its chain (or fused)
+    # launches and, on the two-kernel path, the chunk kernel's launches
+    pre_launches = pre_plan["launches"] + pre_plan["chunk_launches"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
@@ -836,7 +836,7 @@ def main():
         # append 2 (tensor-core append, log_len), rollback 1, flush 2
         "gpu_launches": args.steps * (pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
         "prefill_path": "chunk + chain kernels" if pre_plan["two_kernels"] else "fused kernel",
-        "prefill_chunk_launches": pre_launches,
+        "prefill_launches": pre_launches,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }
     if not args.no_flush_sweep:

@@ -119,7 +119,8 @@ class _ReplayArgs(ctypes.Structure):
 
 class _PrefillPlan(ctypes.Structure):
     _fields_ = [("chains", ctypes.c_int64), ("piece_chunks", ctypes.c_int64), ("levels", ctypes.c_int64),
-                ("ctas_per_launch", ctypes.c_int64), ("launches", ctypes.c_int64), ("two_kernels", ctypes.c_int64)]
+                ("ctas_per_launch", ctypes.c_int64), ("launches", ctypes.c_int64), ("two_kernels", ctypes.c_int64),
+                ("chunk_launches", ctypes.c_int64)]
 
 
 # --------------------------------------------------------------------------- loading

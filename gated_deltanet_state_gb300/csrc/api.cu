@@ -93,7 +93,7 @@ gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, in
   const bool two = path == GDN_PREFILL_TWO_KERNELS ||
                    (path == GDN_PREFILL_AUTO &&
                     tc_prefill_two_kernels_faster(desc->num_qk_heads, desc->num_v_heads, num_seqs, max_seq_len, sms));
-  const PrefillSchedule sc = two ? tc_chain_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms)
+  const PrefillSchedule sc = two ? tc_chain_schedule(desc->num_qk_heads, desc->num_v_heads, num_seqs, max_seq_len, sms)
                                  : tc_prefill_schedule(desc->num_v_heads, num_seqs, max_seq_len, sms);
   out->two_kernels = two ? 1 : 0;
   out->chains = sc.nchains;
@@ -101,6 +101,7 @@ gdn_status gdn_prefill_plan_for(const gdn_layer_desc* desc, int32_t num_seqs, in
   out->levels = sc.levels;
   out->ctas_per_launch = sc.width;
   out->launches = sc.launches;
+  out->chunk_launches = two ? sc.chunk_launches : 0;
   return GDN_OK;
 }
 

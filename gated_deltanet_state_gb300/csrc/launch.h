@@ -82,7 +82,12 @@ struct PrefillSchedule {
   int64_t piece;      // chunks per piece (the last level runs to the end)
   int64_t levels;     // pieces per chain of max_len tokens
   int64_t width;      // CTAs per launch
-  int64_t launches;   // chunk-kernel launches
+  int64_t launches;   // chain (or fused-kernel) launches
+  // the two-kernel path: chunk-kernel launches.  Above 1, level l of every
+  // chain runs on a second stream as soon as the chunk kernel's launch l
+  // (that level's chunks) is done, while launch l + 1 takes the SMs the
+  // chains leave idle.
+  int64_t chunk_launches;
 };
 PrefillSchedule tc_prefill_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
 // The same plan with a launch's fixed cost given in chunk times.
@@ -95,7 +100,7 @@ cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t
 // workspace, then the chain kernel (in pieces, as tc_chain_schedule plans),
 // then the window pass.  The workspace holds tc_chain_workspace_bytes.
 size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens);
-PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms);
+PrefillSchedule tc_chain_schedule(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms);
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st);
 // Whether the two kernels beat the fused one for a call of num_seqs sequences
 // of at most max_len tokens on `sms` SMs (both give the same bits).

@@ -33,6 +33,9 @@
 // either.  Chunks start at absolute multiples of 64, so a block boundary is a
 // chunk end and a checkpoint is the tensor-memory state between two chunks.
 // Every mbarrier wait is bounded (gdn_prefill_args.wait_cycles).
+#include <cmath>
+#include <mutex>
+
 #include "launch.h"
 #include "tc.cuh"
 #include "tc_chunk.cuh"
@@ -183,14 +186,14 @@ __device__ __forceinline__ void chunk_gates(const TokenView<__nv_bfloat16>& V, i
 }  // namespace
 
 // ============================================================================
-// Chunk kernel: grid (Hqk, max chunks, N), one CTA per (qk head, chunk, sequence)
+// Chunk kernel: grid (Hqk, chunks, N), one CTA per (qk head, chunk c0 + y, sequence)
 // ============================================================================
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_chunk_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap, const ChunkWs ws) {
+    tc_chunk_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap, const ChunkWs ws, int64_t c0) {
   using TIN = __nv_bfloat16;
   constexpr int D = kD, C = kC;
   const int jq = blockIdx.x;
-  const int64_t c = blockIdx.y;
+  const int64_t c = c0 + blockIdx.y;
   const int s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool worker = tid < kWorkers;
@@ -596,8 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (level > 0 && cb >= nch) return;
   const int64_t ce = level == pm.last_level || cb + pm.piece > nch ? nch : cb + pm.piece;
   const int32_t from = level > 0 ? final_page : init;
-  if (level > 0 &&
-      __syncthreads_or(tid == 0 && *reinterpret_cast<volatile const int32_t*>(p.err) == GDN_ERR_TIMEOUT))
+  // a wait that ran out in an earlier launch of the call (the chunk kernel or
+  // an earlier piece) leaves images or a state that cannot be trusted
+  if (__syncthreads_or(tid == 0 && *reinterpret_cast<volatile const int32_t*>(p.err) == GDN_ERR_TIMEOUT))
     return;
   const long long wlim = wait_limit(p);
   const int64_t row0 = p.cu_seqlens[s];
@@ -746,29 +750,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gC = gates_of(c)[64 + C - 1];
       const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
       float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
-      uint32_t hi[16], lo[16];
+      float v0[32];
+      tc::tmem_ld32(tS, v0);
+      if (ckp) {
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          reinterpret_cast<float4*>(ckp)[c4] = make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
+      }
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float v0[16];
-        tc::tmem_ld16(tS + 16 * hh, v0);
-        if (ckp) {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            reinterpret_cast<float4*>(ckp + 16 * hh)[c4] =
-                make_float4(v0[4 * c4], v0[4 * c4 + 1], v0[4 * c4 + 2], v0[4 * c4 + 3]);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) tc::split_pair(v0[2 * e], v0[2 * e + 1], hi[8 * hh + e], lo[8 * hh + e]);
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
-          v0[e] = gg.x;
-          v0[e + 1] = gg.y;
-        }
-        tc::tmem_st16(tS + 16 * hh, v0);
+        for (int e = 0; e < 8; ++e) tc::split_pair(v0[16 * hh + 2 * e], v0[16 * hh + 2 * e + 1], hi[e], lo[e]);
+        tc::tmem_st8(tbase + tlane + kChS0H + 16 * quarter + 8 * hh, hi);
+        tc::tmem_st8(tbase + tlane + kChS0L + 16 * quarter + 8 * hh, lo);
       }
-      tc::tmem_st16u(tbase + tlane + kChS0H + 16 * quarter, hi);
-      tc::tmem_st16u(tbase + tlane + kChS0L + 16 * quarter, lo);
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+        v0[e] = gg.x;
+        v0[e + 1] = gg.y;
+      }
+      tc::tmem_st32(tS, v0);
       tc::tmem_st_wait();
     }
     ok = cta_sync_ok(ok);
@@ -800,8 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i0 = 16 * quarter;
       const float* vs = reinterpret_cast<const float*>(sm + ChSmem::VS) + i0 * D + row;
       float a[16];
-      tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
-      tc::tmem_ld16(tbase + tlane + kChSQ + i0, sq);
+      tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChSQ + i0, a, sq);
 #pragma unroll
       for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vs[e * D]);
       split_to_tmem(a);
@@ -827,7 +829,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_kq(c + 1);
         load_v(c + 1);
       }
-      tc::bulk_wait_read();   // the tile, before the next chunk's outputs
     }
     if (worker) {
       // ---- (3) U (rows r, K = i) into the operand of the state update and U^T P^T
@@ -854,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (work_wait(mbar + ChSmem::kS, par, wlim)) load_kt(c + 1);
         else ok = false;
       }
+      tc::bulk_wait_read();   // the output tile, before the next chunk's outputs rewrite it
     }
   }
 
@@ -945,30 +947,124 @@ ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total
 // launches), so the pieces are longer than the fused kernel's: a launch
 // counts as five chunk times.
 constexpr double kChainLaunchCost = 5.0;
+// Overlapped levels: an even number of chunks, at least 16, at most 64
+// levels a call.
+constexpr int64_t kSegMin = 16, kSegLevels = 64;
 
-PrefillSchedule tc_chain_schedule(int Hv, int num_seqs, int64_t max_len, int sms) {
-  return tc_prefill_schedule_cost(Hv, num_seqs, max_len, sms, kChainLaunchCost);
+// A model of the paths in units of the fused kernel's chunk time (one chunk
+// of one chain, ~13.5 us on a GB300), fitted to measured calls of the
+// 27B-shaped layer (1-8 sequences of 8,192 tokens, one of 65,536 and of
+// 229,376).  The fused kernel: each launch runs its chains a chunk at a time,
+// ~1.5 for a launch.  A chunk CTA costs ~0.55 + 0.55 G of one SM (G value heads
+// a qk head: 27 us at G = 3), in whole waves over the SMs; a chain chunk ~0.35
+// (4.6 us), a chain launch ~2 more (the state in and out, the first images).
+// Run one after the other, the two kernels take the chunk kernel's waves,
+// then the chain launches.  Overlapped (one round of chains), the first
+// level's chunk waves, then the longer of the chains' path and all the SM
+// time spread over every SM, plus the restart of each level.
+namespace {
+constexpr double kChainChunk = 0.35, kChainLaunch = 2.0, kFusedLaunch = 1.5;
+
+double chunk_cta_cost(int Hqk, int Hv) { return 0.55 + 0.55 * (double)Hv / Hqk; }
+
+double waves(double ctas, int sms) { return std::ceil(ctas / sms); }
+
+double chain_launches_cost(const PrefillSchedule& sc, int64_t maxc, int sms, double chunk, double launch) {
+  if (sc.levels <= 1) return waves((double)sc.nchains, sms) * (double)maxc * chunk + launch;
+  return (double)sc.launches * ((double)sc.piece * chunk + launch);
 }
 
-// A model of both paths in units of the fused kernel's chunk time (one chunk
-// of one chain, ~13.5 us on a GB300): the fused kernel runs its chains in
-// rounds of `sms`, a chunk at a time, plus ~1.5 for its launch; the two
-// kernels run every chunk of every qk head in parallel (a chunk CTA costs
-// ~0.55 + 0.55 G fused chunk times for G value heads a qk head: 29.5 us at
-// G = 3), then the chains at ~0.45 a chunk (6 us), plus ~3 for two launches.
-// Measured at 1-8 sequences of 8,192 and 1 of 65,536 and 229,376 tokens of
-// the 27B-shaped layer: the two kernels win at one or two sequences (0.68
-// and 0.89 of the fused time), lose from three on.
+double two_kernel_cost(int Hqk, int Hv, int num_seqs, int64_t maxc, int sms, const PrefillSchedule& sc) {
+  const double cta = chunk_cta_cost(Hqk, Hv);
+  const double ctas = (double)num_seqs * maxc * Hqk;
+  if (sc.chunk_launches <= 1)
+    return waves(ctas, sms) * cta + kFusedLaunch + chain_launches_cost(sc, maxc, sms, kChainChunk, kChainLaunch);
+  const double all_sm = (ctas * cta + (double)sc.nchains * maxc * kChainChunk) / sms;
+  const double path = (double)maxc * kChainChunk;
+  const double first = waves((double)num_seqs * sc.piece * Hqk, sms) * cta;
+  return first + (path > all_sm ? path : all_sm) + kChainLaunch * (double)sc.levels;
+}
+}  // namespace
+
+PrefillSchedule tc_chain_schedule(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms) {
+  PrefillSchedule sc = tc_prefill_schedule_cost(Hv, num_seqs, max_len, sms, kChainLaunchCost);
+  sc.chunk_launches = sc.nchains > 0 ? 1 : 0;
+  const int64_t maxc = max_len > 0 ? (max_len + kC - 1) / kC : 0;
+  if (sms <= 0 || Hqk <= 0 || sc.nchains <= 0 || sc.nchains > sms || maxc < 2 * kSegMin) return sc;
+  // every chain has an SM of its own: the chains leave sms - nchains SMs to
+  // the chunk kernel, which produces the next level's images meanwhile
+  PrefillSchedule best = sc;
+  double best_cost = two_kernel_cost(Hqk, Hv, num_seqs, maxc, sms, sc);
+  const int64_t at_least = (maxc + kSegLevels - 1) / kSegLevels;
+  for (int64_t P = at_least > kSegMin ? at_least + (at_least & 1) : kSegMin; 2 * P <= maxc; P += 2) {
+    PrefillSchedule ov;
+    ov.nchains = sc.nchains;
+    ov.piece = P;
+    ov.levels = (maxc + P - 1) / P;
+    ov.width = sc.nchains;
+    ov.launches = ov.levels;
+    ov.chunk_launches = ov.levels;
+    const double cost = two_kernel_cost(Hqk, Hv, num_seqs, maxc, sms, ov);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = ov;
+    }
+  }
+  return best;
+}
+
 bool tc_prefill_two_kernels_faster(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms) {
   if (sms <= 0 || num_seqs <= 0 || max_len <= 0 || Hqk <= 0) return false;
-  const double maxc = (double)((max_len + kC - 1) / kC);
-  const double chains = (double)Hv * num_seqs;
-  const double rounds = chains > sms ? chains / sms : 1.0;
-  const double G = (double)Hv / Hqk;
-  const double fused = rounds * maxc + 1.5;
-  const double two = (double)num_seqs * maxc * Hqk / sms * (0.55 + 0.55 * G) + rounds * maxc * 0.45 + 3.0;
-  return two < 0.95 * fused;
+  const int64_t maxc = (max_len + kC - 1) / kC;
+  const PrefillSchedule fs = tc_prefill_schedule(Hv, num_seqs, max_len, sms);
+  const double fused = chain_launches_cost(fs, maxc, sms, 1.0, kFusedLaunch);
+  const PrefillSchedule sc = tc_chain_schedule(Hqk, Hv, num_seqs, max_len, sms);
+  return two_kernel_cost(Hqk, Hv, num_seqs, maxc, sms, sc) < 0.95 * fused;
 }
+
+namespace {
+
+// The second stream of the overlapped levels (highest priority, so a level's
+// chain CTAs take SMs before the chunk kernel's next launch) and the events
+// of its fork and join, one set per device, made on first use.  The mutex
+// keeps one call's enqueue of the fork, the levels and the join together.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t ready = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+cudaError_t side_stream(SideStream*& out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& ss = g_side[dev];
+  if (!ss.stream) {
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e != cudaSuccess) return e;
+    cudaStream_t st = nullptr;
+    cudaEvent_t r = nullptr, j = nullptr;
+    e = cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      if (j) cudaEventDestroy(j);
+      if (r) cudaEventDestroy(r);
+      if (st) cudaStreamDestroy(st);
+      return e;
+    }
+    ss.stream = st;
+    ss.ready = r;
+    ss.join = j;
+  }
+  out = &ss;
+  return cudaSuccess;
+}
+
+}  // namespace
 
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
@@ -978,9 +1074,10 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   if (maxc > 65535) return cudaErrorInvalidValue;
   auto encode = tensor_map_encoder();
   if (p.total_rows > 0 && !encode) return cudaErrorNotSupported;
-  if (maxc > 0 && p.total_rows > 0) {
-    CUtensorMap xmap;
-    memset(&xmap, 0, sizeof(xmap));
+  CUtensorMap xmap;
+  memset(&xmap, 0, sizeof(xmap));
+  const bool chunks = maxc > 0 && p.total_rows > 0;
+  if (chunks) {
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.x_ld, (cuuint64_t)p.total_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.x_ld * 2};
@@ -992,10 +1089,13 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     cudaError_t e =
         cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CkSmem::ALLOC);
     if (e != cudaSuccess) return e;
-    tc_chunk_kernel<<<dim3(p.Hqk, (unsigned)maxc, p.num_seqs), kThreads, CkSmem::ALLOC, st>>>(p, xmap, ws);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
   }
+  // the chunk kernel over chunks [c0, c0 + cnt) of every sequence
+  auto chunk_launch = [&](int64_t c0, int64_t cnt, cudaStream_t s) {
+    if (!chunks || cnt <= 0) return cudaSuccess;
+    tc_chunk_kernel<<<dim3(p.Hqk, (unsigned)cnt, p.num_seqs), kThreads, CkSmem::ALLOC, s>>>(p, xmap, ws, c0);
+    return cudaGetLastError();
+  };
   // o as [rows][Hv * dv] bf16; a box is one head's 128 channels x 64 rows
   // (the chain's full chunks go out as one TMA store when o is 16-byte aligned)
   CUtensorMap omap;
@@ -1014,20 +1114,46 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ChSmem::ALLOC);
   if (e != cudaSuccess) return e;
-  const PrefillSchedule sc = tc_chain_schedule(p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
+  const PrefillSchedule sc = tc_chain_schedule(p.Hqk, p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
   PieceMap pm;
   pm.nseqs = p.num_seqs;
   pm.piece = (int32_t)sc.piece;
   pm.last_level = (int32_t)(sc.levels - 1);
-  const int64_t pairs = sc.levels * p.num_seqs, per = sc.width / p.Hv;
-  for (int64_t t = 0; t < sc.launches; ++t) {
-    const int64_t base = t * per;
-    pm.s0 = (int32_t)(base % p.num_seqs);
-    pm.level0 = (int32_t)(base / p.num_seqs);
-    const int64_t cnt = pairs - base < per ? pairs - base : per;
-    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, st>>>(p, omap, tma_out, ws, pm, maxc);
-    e = cudaGetLastError();
+  auto chain_launch = [&](int64_t level0, int32_t s0, int64_t cnt, cudaStream_t s) {
+    pm.s0 = s0;
+    pm.level0 = (int32_t)level0;
+    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, s>>>(p, omap, tma_out, ws, pm, maxc);
+    return cudaGetLastError();
+  };
+  if (sc.chunk_launches > 1) {
+    // level l of every chain on the second stream once the chunk kernel's
+    // launch l is done; its launch l + 1 meanwhile on the caller's stream
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream* ss = nullptr;
+    e = side_stream(ss);
     if (e != cudaSuccess) return e;
+    for (int64_t l = 0; l < sc.levels && e == cudaSuccess; ++l) {
+      const int64_t c0 = l * sc.piece;
+      e = chunk_launch(c0, maxc - c0 < sc.piece ? maxc - c0 : sc.piece, st);
+      if (e == cudaSuccess) e = cudaEventRecord(ss->ready, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->ready, 0);
+      if (e == cudaSuccess) e = chain_launch(l, 0, p.num_seqs, ss->stream);
+    }
+    // the join, also after a failed launch (a capture needs its fork joined)
+    const cudaError_t j = cudaEventRecord(ss->join, ss->stream);
+    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, ss->join, 0) : j;
+    if (e != cudaSuccess) return e;
+    if (w != cudaSuccess) return w;
+  } else {
+    e = chunk_launch(0, maxc, st);
+    if (e != cudaSuccess) return e;
+    const int64_t pairs = sc.levels * p.num_seqs, per = sc.width / p.Hv;
+    for (int64_t t = 0; t < sc.launches; ++t) {
+      const int64_t base = t * per;
+      const int64_t cnt = pairs - base < per ? pairs - base : per;
+      e = chain_launch(base / p.num_seqs, (int32_t)(base % p.num_seqs), cnt, st);
+      if (e != cudaSuccess) return e;
+    }
   }
   window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
   return cudaGetLastError();

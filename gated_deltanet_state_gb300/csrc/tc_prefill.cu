@@ -778,6 +778,7 @@ PrefillSchedule tc_prefill_schedule_cost(int Hv, int num_seqs, int64_t max_len, 
   sc.levels = 1;
   sc.width = sc.nchains;
   sc.launches = sc.nchains > 0 ? 1 : 0;
+  sc.chunk_launches = 0;
   const int64_t per = Hv > 0 && sms > 0 ? sms / Hv : 0;   // pairs a launch
   if (per < 1 || num_seqs < per || sc.nchains < sms || maxc < 2 * kMinPiece) return sc;
   const double single = (double)((sc.nchains + sms - 1) / sms) * ((double)maxc + kLaunchCost);

@@ -301,23 +301,35 @@ size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
 /* How gdn_prefill_chunked runs a call of a layer on the tensor-core path:
  * the path (two_kernels; `path` GDN_PREFILL_AUTO resolves it as a call with
  * a workspace would) and the chain plan of that path.  Each (sequence, value
- * head) chain runs on one SM, its chunks in order.  With at least as many chains as SMs and long chains,
- * whole chains would leave SMs idle in the last round, so the chains are cut
+ * head) chain runs on one SM, its chunks in order.  With at least as many
+ * chains as SMs and long chains, whole chains would leave SMs idle in the
+ * last round, so the chains are cut
  * into pieces of piece_chunks chunks and run as `launches` launches of up to
  * ctas_per_launch CTAs: all chains' first pieces, then all second pieces, and
  * so on, ctas_per_launch at a time (a piece starts from the state the piece
  * before it left in page out_slot[s]; the last piece of a chain runs to its
  * end).  Every chunk's arithmetic is unchanged, so the results are bitwise
  * those of one launch.  One launch (levels = 1) is kept unless pieces save
- * an estimated 5 %. */
+ * an estimated 5 %.  The two-kernel path with no more chains than SMs and
+ * chains of at least 32 chunks cuts every chain into levels of an even 16 to
+ * 64 chunks (about 32 levels, at most 64) and overlaps them with the chunk
+ * kernel (chunk_launches below).  The second stream and its two events are
+ * made once per device, on the first such call, and kept for the process. */
 typedef struct gdn_prefill_plan {
   int64_t chains;           /* num_v_heads x num_seqs                        */
   int64_t piece_chunks;     /* chunks (64 tokens) per piece                  */
   int64_t levels;           /* pieces per chain of max_seq_len tokens        */
   int64_t ctas_per_launch;  /* CTAs of each launch (the last may have fewer) */
-  int64_t launches;         /* chain launches (+1 window pass; the two-kernel
-                               path also launches the chunk kernel once)    */
+  int64_t launches;         /* chain launches (+1 window pass)              */
   int64_t two_kernels;      /* 1: the chunk + chain kernels, 0: the fused one */
+  int64_t chunk_launches;   /* two-kernel path: chunk-kernel launches, 0 on
+                               the fused path.  Above 1 the levels overlap:
+                               level l of every chain runs on a second,
+                               high-priority stream once the chunk kernel's
+                               launch l (chunks [l x piece_chunks, +piece_chunks)
+                               of every sequence) is done, while its launch
+                               l + 1 runs on the SMs the chains leave idle;
+                               the call's stream waits for the last level   */
 } gdn_prefill_plan;
 
 /* The plan of one gdn_prefill_chunked call with num_seqs sequences and the

@@ -128,7 +128,9 @@ def test_pieces_over_several_launches_equal_one_launch_bitwise():
     left in the final slot).  One sequence alone is 48 chains, one launch.
     Outputs, final states, checkpoints and windows must be the same bits, with
     block boundaries at piece ends, a resumed sequence, a sequence that ends
-    inside its second piece and one shorter than a piece."""
+    inside its second piece and one shorter than a piece.  (The single
+    sequences take the fused kernel: the two kernels would cut even one
+    sequence into overlapped levels.)"""
     sh = inputs.LayerShape(16, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
     lens = [2048, 1800, 77, 1536]
     start = [0, 0, 0, 1024]
@@ -137,7 +139,7 @@ def test_pieces_over_several_launches_equal_one_launch_bitwise():
     N = len(lens)
     plan = gdn.gdn_prefill_plan_for(sh, N, max(lens))
     assert plan["levels"] == 2 and plan["launches"] > 1, plan
-    assert gdn.gdn_prefill_plan_for(sh, 1, max(lens))["launches"] == 1
+    assert gdn.gdn_prefill_plan_for(sh, 1, max(lens), 0, gdn.PREFILL_FUSED)["launches"] == 1
     cu = np.concatenate([[0], np.cumsum(lens)])
     ti = inputs.token_inputs(sh, int(cu[-1]), seed=61)
     w = inputs.conv_weights(sh, 61)
@@ -154,7 +156,8 @@ def test_pieces_over_several_launches_equal_one_launch_bitwise():
     for s in range(N):
         a, b = int(cu[s]), int(cu[s + 1])
         o_one, err, _ = run_prefill(sh, pools[1], ti["x"][a:b], ti["g"][a:b], ti["beta"][a:b], w, [0, b - a],
-                                    [start[s]], [init[s]], [bt[s]], [s], max_seq_len=b - a)
+                                    [start[s]], [init[s]], [bt[s]], [s], max_seq_len=b - a, workspace=False,
+                                    path=gdn.PREFILL_FUSED)
         assert err == 0
         assert torch.equal(o_all[a:b].view(torch.int16), o_one.view(torch.int16)), s
     for page in [0, 1, 2, 3, 5, 6, 7, 8]:
@@ -197,11 +200,13 @@ def _both_paths(sh, lens, start, init, bt, seed, npages, fill_state=None, max_se
     return res
 
 
-@pytest.mark.parametrize("case", ["edges_gqa3", "resumed_27b", "pieces_27b"])
+@pytest.mark.parametrize("case", ["edges_gqa3", "resumed_27b", "pieces_27b", "overlap_27b"])
 def test_two_kernel_path_gives_the_fused_kernels_bits(case):
     """The chunk + chain kernels split and multiply every operand as the fused
     kernel does, so a call gives the same bits on either path: a prefix hit
-    reproduces a cold run's bits whichever path each call takes."""
+    reproduces a cold run's bits whichever path each call takes.  overlap_27b
+    runs the two kernels' overlapped levels (the chain on a second stream,
+    four checkpoints inside levels)."""
     if case == "edges_gqa3":
         sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
         lens = [1, 63, 64, 65, 127, 128, 129, 300, 700]
@@ -212,6 +217,13 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
         st = inputs.random_state(sh, 1, seed=83)
         res = _both_paths(sh, [700, 300], [512, 0], [5, -1], [[-1, -1, 6, 7], [8, -1, -1, -1]], 82, 9,
                           fill_state=(5, st))
+    elif case == "overlap_27b":
+        sh = inputs.QWEN27B
+        lens = [4133]
+        plan = gdn.gdn_prefill_plan_for(sh, 1, max(lens), 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+        res = _both_paths(sh, lens, [0], [-1], [[1, 2, 3, 4]], 85, 5, max_seq_len=max(lens))
     else:
         sh = inputs.LayerShape(16, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
         lens = [2048, 1800, 77, 1536]
@@ -221,3 +233,37 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
     (o_f, pool_f), (o_2, pool_2) = res
     assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
     assert torch.equal(pool_f, pool_2)
+
+
+def test_overlapped_levels_resume_bitwise():
+    """A long sequence on the two kernels' overlapped levels, then the same
+    sequence resumed from its second checkpoint (a shorter call, its own
+    levels): the resumed call reproduces the cold call's outputs and final
+    state bit for bit, and both match the oracle on two heads."""
+    sh = inputs.QWEN27B
+    T, B = 4133, sh.block_size
+    for L in (T, T - 2 * B):
+        plan = gdn.gdn_prefill_plan_for(sh, 1, L, 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+    ti = inputs.token_inputs(sh, T, seed=86)
+    w = inputs.conv_weights(sh, 86)
+    pool = gdn.StatePool(sh, 8, fill=0)
+    kw = dict(workspace=None, path=gdn.PREFILL_TWO_KERNELS)
+    o_cold, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [0], [-1], [[1, 2, 3, 4]],
+                                 [0], max_seq_len=T, **kw)
+    assert err == 0
+    P = 2 * B
+    o_res, err, _ = run_prefill(sh, pool, ti["x"][P:], ti["g"][P:], ti["beta"][P:], w, [0, T - P], [P], [2],
+                                [[-1, -1, 6, 7]], [5], max_seq_len=T - P, **kw)
+    assert err == 0
+    assert torch.equal(o_res.view(torch.int16), o_cold[P:].view(torch.int16))
+    assert torch.equal(pool.payload(5).cpu(), pool.payload(0).cpu())
+    assert torch.equal(pool.payload(6).cpu(), pool.payload(3).cpu())
+    assert torch.equal(pool.payload(7).cpu(), pool.payload(4).cpu())
+    for h in (0, 47):
+        ref = oracle_head(sh, ti["x"], ti["g"], ti["beta"], w, h, [0, T], [0], B)
+        assert_out_close(o_cold[:, h:h + 1], ref["o"], [0, T])
+        assert_state_close(pool.state(0).cpu()[None, h:h + 1], ref["S"])
+        for j, page in enumerate([1, 2, 3, 4]):
+            assert_state_close(pool.state(page).cpu()[None, h:h + 1], ref["ck_S"][j][None])

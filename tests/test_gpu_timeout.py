@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 TIMEOUT = gdn.STATUS_CODE["GDN_ERR_TIMEOUT"]
 
 
-def _call(sh, pool, ti, w, cu, bt, slots, err, wait_cycles, max_seq_len=0):
+def _call(sh, pool, ti, w, cu, bt, slots, err, wait_cycles, max_seq_len=0, path=gdn.PREFILL_AUTO):
     T = int(cu[-1])
     n = len(cu) - 1
     o = torch.full((T, sh.num_v_heads, sh.head_dim_v), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -32,7 +32,7 @@ def _call(sh, pool, ti, w, cu, bt, slots, err, wait_cycles, max_seq_len=0):
                             out_slot=dev(slots, torch.int32), x=dev(ti["x"]), g=dev(ti["g"]),
                             beta=dev(ti["beta"]), conv_w=dev(w), o=o, dev_error=err,
                             start_pos_host=[0] * n, init_page_host=[-1] * n, max_seq_len=max_seq_len,
-                            wait_cycles=wait_cycles)
+                            wait_cycles=wait_cycles, path=path)
     torch.cuda.synchronize()
     return o
 
@@ -59,6 +59,51 @@ def test_every_wait_running_out_writes_nothing_and_the_next_call_is_exact():
     assert_out_close(o2, ref["o"], cu)
     assert_state_close(torch.stack([pool.state(0), pool.state(1)]).cpu(), ref["S"])
     assert_state_close(torch.stack([pool.state(p) for p in (2, 3, 4)]).cpu(), ref["ck_S"])
+
+
+@pytest.mark.parametrize("case", ["levels", "one_level"])
+def test_the_chain_kernel_does_not_start_after_a_run_out(case):
+    """On the two-kernel path a chain launch that finds GDN_ERR_TIMEOUT in the
+    error word stands down: the word stands for a wait that ran out in an
+    earlier launch of the call (the chunk kernel, or the level before), whose
+    images or state cannot be trusted.  Nothing is written, neither by any
+    level (the overlapped levels of a 4,133-token sequence of the 27B-shaped
+    layer, or the single launch of two short ones) nor by the window pass; the
+    next call with a clear word is exact."""
+    if case == "levels":
+        sh, lens, heads = inputs.QWEN27B, [4133], (0, 47)
+        plan = gdn.gdn_prefill_plan_for(sh, 1, 4133, 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+    else:
+        sh, lens, heads = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64), [300, 200], None
+    N, B = len(lens), sh.block_size
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    ti = inputs.token_inputs(sh, int(cu[-1]), seed=74)
+    w = inputs.conv_weights(sh, 74)
+    nb = max(lens) // B
+    bt = [[N + s * nb + j if (j + 1) * B <= lens[s] else -1 for j in range(nb)] for s in range(N)]
+    pool = gdn.StatePool(sh, N + N * nb, fill=0x5A)
+    before = pool.buf.cpu().clone()
+    err = torch.full((1,), TIMEOUT, dtype=torch.int32, device="cuda")
+    o = _call(sh, pool, ti, w, cu, bt, list(range(N)), err, wait_cycles=0, max_seq_len=max(lens),
+              path=gdn.PREFILL_TWO_KERNELS)
+    assert err.item() == TIMEOUT
+    assert torch.equal(pool.buf.cpu(), before)
+    assert torch.isnan(o.float()).all()
+    err.zero_()
+    o = _call(sh, pool, ti, w, cu, bt, list(range(N)), err, wait_cycles=0, max_seq_len=max(lens),
+              path=gdn.PREFILL_TWO_KERNELS)
+    assert err.item() == 0
+    if heads is None:
+        ref = oracle.prefill(dims(sh), cu, [0] * N, B, ti["x"], ti["g"], ti["beta"], w)
+        assert_out_close(o, ref["o"], cu)
+        assert_state_close(torch.stack([pool.state(s) for s in range(N)]).cpu(), ref["S"])
+    else:
+        for h in heads:
+            ref = oracle_head(sh, ti["x"], ti["g"], ti["beta"], w, h, cu, [0] * N, B)
+            assert_out_close(o[:, h:h + 1], ref["o"], cu)
+            assert_state_close(pool.state(0).cpu()[None, h:h + 1], ref["S"])
 
 
 def _piece_case(seed):
@@ -99,7 +144,8 @@ def test_later_pieces_do_not_continue_after_a_run_out():
     pool = gdn.StatePool(sh, N + N * len(bt[0]), fill=0x5A)
     before = pool.buf.cpu().clone()
     err = torch.full((1,), TIMEOUT, dtype=torch.int32, device="cuda")
-    o = _call(sh, pool, ti, w, cu, bt, list(range(N)), err, wait_cycles=0, max_seq_len=L).cpu()
+    o = _call(sh, pool, ti, w, cu, bt, list(range(N)), err, wait_cycles=0, max_seq_len=L,
+              path=gdn.PREFILL_FUSED).cpu()
     assert err.item() == TIMEOUT
     B = sh.block_size
     for s in range(N):

@@ -57,6 +57,23 @@ def test_plan_runs_every_piece_once_in_order(Hv, N, path):
         plan = gdn.gdn_prefill_plan_for(sh, N, max_len, sms, path)
         assert plan.pop("two_kernels") == (path == gdn.PREFILL_TWO_KERNELS)
         assert plan["chains"] == Hv * N
+        maxc = -(-max_len // 64)
+        chunk_launches = plan.pop("chunk_launches")
+        if chunk_launches > 1:
+            # only the two kernels, with one round of chains of 32 chunks or more
+            assert path == gdn.PREFILL_TWO_KERNELS and 0 < Hv * N <= sms and maxc >= 32
+            # levels of every chain, each after the chunk launch of its chunks
+            assert chunk_launches == plan["levels"] == plan["launches"] > 1
+            assert plan["ctas_per_launch"] == Hv * N and 16 <= plan["piece_chunks"] <= maxc // 2
+            assert plan["levels"] <= 64
+            segs = [range(lv * plan["piece_chunks"], min(maxc, (lv + 1) * plan["piece_chunks"]))
+                    for lv in range(chunk_launches)]
+            assert [c for r in segs for c in r] == list(range(maxc))
+            for lv in range(plan["levels"]):
+                # level lv reads only chunks the launches up to lv produced
+                assert all(c < segs[lv].stop for c in _chunks(plan, lv, maxc))
+        else:
+            assert chunk_launches == (int(Hv * N > 0) if path == gdn.PREFILL_TWO_KERNELS else 0)
         if plan["levels"] > 1:
             P = plan["piece_chunks"]
             assert P >= 4 and P % 2 == 0, "pieces start at even chunks"
@@ -66,7 +83,6 @@ def test_plan_runs_every_piece_once_in_order(Hv, N, path):
             assert plan["launches"] == 1 and plan["ctas_per_launch"] == Hv * N
         runs = _play(plan, N, Hv)
         assert len(runs) == Hv * N
-        maxc = -(-max_len // 64)
         for key, lst in runs.items():
             assert [lv for _, lv in lst] == list(range(plan["levels"])), key
             assert all(t0 < t1 for (t0, _), (t1, _) in zip(lst, lst[1:])), key
@@ -81,12 +97,25 @@ def test_benchmark_shape_plan():
     # (the last 40), three (level, sequence) pairs of 48 CTAs a launch, 12
     # pairs in 4 launches: ~4 x 44 chunk times against 2 x 128 in one launch
     for path in (gdn.PREFILL_FUSED, gdn.PREFILL_TWO_KERNELS):
+        two = int(path == gdn.PREFILL_TWO_KERNELS)
         plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 4, 8192, 152, path)
         assert plan == {"chains": 192, "piece_chunks": 44, "levels": 3, "ctas_per_launch": 144, "launches": 4,
-                        "two_kernels": int(path == gdn.PREFILL_TWO_KERNELS)}
-        # one long sequence (48 chains) and a large batch (3,072 chains) stay one launch
-        assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, path)["launches"] == 1
+                        "two_kernels": two, "chunk_launches": two}
+        # a large batch (3,072 chains) stays one launch
         assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152, path)["launches"] == 1
+    # one long sequence (48 chains): one launch of the fused kernel; the two
+    # kernels overlap 20 levels of 180 chunks with the chunk kernel
+    assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, gdn.PREFILL_FUSED)["launches"] == 1
+    plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, gdn.PREFILL_TWO_KERNELS)
+    assert plan == {"chains": 48, "piece_chunks": 180, "levels": 20, "ctas_per_launch": 48, "launches": 20,
+                    "two_kernels": 1, "chunk_launches": 20}
+    # 1 x 8,192: five levels of 26 chunks; 2 x 8,192 (96 chains leave 56 SMs
+    # idle) runs the two kernels one after the other
+    plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 8192, 152, gdn.PREFILL_TWO_KERNELS)
+    assert (plan["piece_chunks"], plan["levels"], plan["chunk_launches"]) == (26, 5, 5)
+    for N in (2, 3):
+        plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, N, 8192, 152, gdn.PREFILL_TWO_KERNELS)
+        assert (plan["levels"], plan["launches"], plan["chunk_launches"]) == (1, 1, 1)
 
 
 def test_auto_path_takes_the_two_kernels_where_chains_leave_sms_idle():
