@@ -181,12 +181,15 @@ def job_throughput(units_per_rank: float, world: int, ms: float) -> float:
 # ----------------------------------------------------------------------------- workloads
 
 class PrefillWork:
-    """4 x 8192 tokens of the 27B-shaped layer, checkpoints every 896 tokens."""
+    """4 x 8192 tokens of the 27B-shaped layer, checkpoints every 896 tokens
+    (other batch shapes and a forced path for profiling)."""
 
-    def __init__(self, seed: int, seq_len: int = SEQ_LEN):
+    def __init__(self, seed: int, seq_len: int = SEQ_LEN, num_seqs: int = N_SEQ, path: int = gdn.PREFILL_AUTO):
         sh = PREFILL
         self.sh = sh
-        T = N_SEQ * seq_len
+        self.n = num_seqs
+        self.path = path
+        T = num_seqs * seq_len
         # a2: the scheduler's chunk for this call; the whole prompt fits the budget
         self.chunk_end = gdn.gdn_chunk_end(0, seq_len, seq_len, sh.block_size)
         assert self.chunk_end == seq_len
@@ -197,21 +200,21 @@ class PrefillWork:
         self.beta = ti["beta"].cuda()
         self.w = inputs.conv_weights(sh, seed).cuda()
         nck = max(1, seq_len // sh.block_size)    # 9 boundaries per sequence at 8192
-        self.num_pages = N_SEQ * (nck + 1)
+        self.num_pages = self.n * (nck + 1)
         perm = inputs.permutation(self.num_pages, seed).tolist()
-        self.block_table = torch.tensor([perm[s * nck:(s + 1) * nck] for s in range(N_SEQ)],
+        self.block_table = torch.tensor([perm[s * nck:(s + 1) * nck] for s in range(self.n)],
                                         dtype=torch.int32).cuda()
-        self.out_slot = torch.tensor(perm[N_SEQ * nck:], dtype=torch.int32).cuda()
+        self.out_slot = torch.tensor(perm[self.n * nck:], dtype=torch.int32).cuda()
         self.pool = gdn.StatePool(sh, self.num_pages, fill=0)
         self.cu = torch.arange(0, T + 1, seq_len, dtype=torch.int32).cuda()
         self.seq_len = seq_len
-        self.start = torch.zeros(N_SEQ, dtype=torch.int64).cuda()
-        self.init = torch.full((N_SEQ,), -1, dtype=torch.int32).cuda()
+        self.start = torch.zeros(self.n, dtype=torch.int64).cuda()
+        self.init = torch.full((self.n,), -1, dtype=torch.int32).cuda()
         self.o = torch.empty(T, sh.num_v_heads, sh.head_dim_v, dtype=torch.bfloat16, device="cuda")
         self.o_host = torch.empty_like(self.o, device="cpu").pin_memory()
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.tokens = T
-        self.ws = gdn.workspace_for(gdn.gdn_prefill_workspace_size(sh, N_SEQ, T))
+        self.ws = gdn.workspace_for(gdn.gdn_prefill_workspace_size(sh, self.n, T))
 
     def run(self, x=None, g=None, beta=None, o=None):
         gdn.gdn_prefill_chunked(self.sh, self.pool, cu_seqlens=self.cu, start_pos=self.start,
@@ -219,8 +222,8 @@ class PrefillWork:
                                 x=self.x if x is None else x, g=self.g if g is None else g,
                                 beta=self.beta if beta is None else beta, conv_w=self.w,
                                 o=self.o if o is None else o, dev_error=self.err,
-                                start_pos_host=[0] * N_SEQ, init_page_host=[-1] * N_SEQ,
-                                workspace=self.ws, max_seq_len=self.seq_len)
+                                start_pos_host=[0] * self.n, init_page_host=[-1] * self.n,
+                                workspace=self.ws, max_seq_len=self.seq_len, path=self.path)
 
     def e2e_pipelined_ms(self, steps: int, warmup: int = 3, nbuf: int = 3) -> float:
         """Streaming end to end: every step copies its inputs from pinned host
@@ -285,7 +288,7 @@ class PrefillWork:
     def algorithmic_bytes(self):
         sh = self.sh
         per_tok = sh.conv_dim * 2 + 2 * sh.num_v_heads * 4 + sh.num_v_heads * sh.head_dim_v * 2
-        ck = (self.seq_len // sh.block_size + 1) * N_SEQ * sh.payload_bytes
+        ck = (self.seq_len // sh.block_size + 1) * self.n * sh.payload_bytes
         return per_tok * self.tokens + ck
 
 
@@ -640,7 +643,8 @@ def run_part(args):
     """One part of the step alone (for profiling): W warm-up and K timed runs,
     one JSON line with the part's device time."""
     if args.only == "prefill":
-        w = PrefillWork(args.seed, args.seq_len)
+        path = {"auto": gdn.PREFILL_AUTO, "fused": gdn.PREFILL_FUSED, "two": gdn.PREFILL_TWO_KERNELS}[args.path]
+        w = PrefillWork(args.seed, args.seq_len, args.num_seqs, path)
         fn, unit_ms = w.run, None
     elif args.only == "decode":
         w = DecodeWork(args.seed, args.layers)
@@ -662,6 +666,8 @@ def run_part(args):
     if args.only == "prefill":
         line["tokens_per_s_per_layer"] = w.tokens / (ms * 1e-3)
         line["seq_len"] = args.seq_len
+        line["num_seqs"] = args.num_seqs
+        line["plan"] = gdn.gdn_prefill_plan_for(PREFILL, args.num_seqs, args.seq_len, 0, w.path)
     print(json.dumps(line), flush=True)
 
 
@@ -679,6 +685,10 @@ def main():
                     help="time one part only (profiling); the default times the whole step")
     ap.add_argument("--seq-len", type=int, default=SEQ_LEN,
                     help="prefill tokens per sequence (profiling of smaller cases)")
+    ap.add_argument("--num-seqs", type=int, default=N_SEQ,
+                    help="prefill sequences with --only prefill (profiling of other batch shapes)")
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "two"],
+                    help="tensor-core prefill path with --only prefill (both give the same bits)")
     ap.add_argument("--layers", type=int, default=DEC_LAYERS,
                     help="decode / replay layers with --only (profiling of smaller cases)")
     args = ap.parse_args()
