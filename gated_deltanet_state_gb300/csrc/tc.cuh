@@ -343,6 +343,11 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // The shared-memory sources of every committed bulk store have been read
 // (the region may be reused; the global writes may still be in flight).
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// The same for all but the N most recently committed groups.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_but() {
+  asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
 }  // namespace tc
 }  // namespace gdn
 

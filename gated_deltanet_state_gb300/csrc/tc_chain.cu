@@ -91,13 +91,13 @@ struct CkSmem {
   static constexpr uint32_t YK = 86016;              // SiLU(conv) of the k channels, fp32 [64][128] (kept)
   static constexpr uint32_t KQ = 118784;             // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t KQ_LO = KQ + 32768;
-  static constexpr uint32_t AT = KQ;                 // (B) A^T fp32 [64 j][64 i]
-  static constexpr uint32_t AM = KQ + 16384;         //     A fp32 row-major, slots swizzled
-  static constexpr uint32_t TF = KQ + 32768;         //     T fp32 [64][64]
+  static constexpr uint32_t TF = KQ + 32768;         // (B) T fp32 [64][64]
   static constexpr uint32_t DT = KQ + 49152;         //     diagonal inverses [4][16][20]
   static constexpr uint32_t NT = KQ + 54272;         //     N blocks [6][16][16]
-  static constexpr uint32_t GT = KQ + 65536;         // gate sets [2][4][64] fp32 (G, gam, dec, b), then rq, rk
-  static constexpr uint32_t MBAR = GT + 2048 + 512;  // [0] Gram [1] q / k rows [2] v rows
+  static constexpr uint32_t GT = KQ + 65536;         // gate sets [4][4][64] fp32 (G, gam, dec, b), then rq, rk
+  static constexpr uint32_t AT = GT + 4096 + 512;    // A^T fp32 [64 j][64 i]
+  static constexpr uint32_t AM = AT + 16384;         // A fp32 row-major, slots swizzled
+  static constexpr uint32_t MBAR = AM + 16384;       // [0] Gram [1] q / k rows [2] v rows
   static constexpr uint32_t TSLOT = MBAR + 24;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -105,6 +105,7 @@ struct CkSmem {
 static_assert(CkSmem::PB_LO + 8192 <= CkSmem::XV && CkSmem::XV + 17408 <= CkSmem::YQ, "chunk kernel regions overlap");
 static_assert(CkSmem::ALLOC <= 232448, "chunk kernel shared memory exceeds the per-CTA limit");
 
+constexpr int kGateSets = 4;        // gate sets of the chunk kernel (value heads formed ahead)
 constexpr uint32_t kCkCols = 128;   // tensor memory of the chunk kernel
 constexpr uint32_t kCkGram = 0;     // [K^ K^T; Q^ K^T]: lanes 0-63 k^_i.k^_j, 64-127 q^_i.k^_j
 constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = row
@@ -156,6 +157,19 @@ __device__ __forceinline__ bool cta_sync_ok(bool ok) {
   ok = __syncthreads_and(ok);
   tc::fence_after_sync();
   return ok;
+}
+// Barrier of the chunk kernel's K group (threads 0..255), and the same
+// barrier returning whether `v` holds on every one of them.
+__device__ __forceinline__ void kgrp_sync() { asm volatile("bar.sync 4, 256;\n" ::: "memory"); }
+__device__ __forceinline__ bool kgrp_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 4, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ long long wait_limit(const ScanParams& p) {
   return p.wait_cycles > 0 ? p.wait_cycles : p.wait_cycles < 0 ? -1 : kWaitDefault;
@@ -224,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   TIN* xk = reinterpret_cast<TIN*>(sm + CkSmem::XK);
   TIN* xv = reinterpret_cast<TIN*>(sm + CkSmem::XV);
   float* gbuf = reinterpret_cast<float*>(sm + CkSmem::GT);
-  float* rq = gbuf + 512;
-  float* rk = gbuf + 576;
+  float* rq = gbuf + 256 * kGateSets;
+  float* rk = rq + 64;
   float* at = reinterpret_cast<float*>(sm + CkSmem::AT);
   float* tf = reinterpret_cast<float*>(sm + CkSmem::TF);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + CkSmem::MBAR);
@@ -261,19 +275,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // history rows of a sequence's first chunk: the resumed window, or zeros
-  auto fix_history = [&](TIN* dst, int ch0) {
-    for (int e = tid; e < kWinRows * (D / 2); e += kWorkers) {
+  auto fix_history = [&](TIN* dst, int ch0, int t, int nthreads) {
+    for (int e = t; e < kWinRows * (D / 2); e += nthreads) {
       const int r = e / (D / 2), c2 = e % (D / 2);
       uint32_t v = 0;
       if (V.win) v = *reinterpret_cast<const uint32_t*>(V.win + (int64_t)r * p.conv_dim + ch0 + 2 * c2);
       *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
     }
   };
-  // v conv of value head h: channel `row`, rows [16 quarter, +16) -> tensor
+  // v conv of value head h: channel `row`, rows [16 qtr, +16) -> tensor
   // memory (rows i and i + 8 as one packed pair)
-  auto v_conv = [&](int h) {
+  auto v_conv = [&](int h, int qtr) {
     const float4 wv = ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK);
-    const int tb = 16 * quarter;
+    const int tb = 16 * qtr;
     float xr[19], vr[16];
 #pragma unroll
     for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[(tb + u) * D + row]);
@@ -288,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       vr[i] = silu_fast(zz.x);
       vr[i + 8] = silu_fast(zz.y);
     }
-    tc::tmem_st16(tbase + tlane + kCkV + 16 * quarter, vr);
+    tc::tmem_st16(tbase + tlane + kCkV + 16 * qtr, vr);
     tc::tmem_st_wait();
   };
 
@@ -298,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = workers_sync_and(work_wait(mbar + 1, 0, wlim) && work_wait(mbar + 2, 0, wlim));
     if (ok) { qk_pending = false; v_pending = -1; }
     if (c == 0) {
-      fix_history(xq, cq0);
-      fix_history(xk, ck0);
-      fix_history(xv, 2 * p.Hqk * D + jq * G * D);
+      fix_history(xq, cq0, tid, kWorkers);
+      fix_history(xk, ck0, tid, kWorkers);
+      fix_history(xv, 2 * p.Hqk * D + jq * G * D, tid, kWorkers);
       workers_sync();
     }
     // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16)
@@ -329,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(yrow + i * D) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
       }
     }
-    v_conv(jq * G);
+    v_conv(jq * G, quarter);
     workers_sync();
     // the first head's v rows are consumed: the next head's rows
     if (tid == 0 && ok && G > 1) stage_v(1);
@@ -408,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::fence_async_smem();
   }
+  if (!worker) {
+    // the value heads' gate sets (up to four) while the workers convolve
+    for (int g = 0; g < G && g < kGateSets; ++g) chunk_gates(V, t0, n, jq * G + g, lane, gbuf + 256 * g);
+    tc::fence_async_smem();
+  }
   ok = cta_sync_ok(ok);
   if (ok && tid == kMma) {
     // [K^ K^T; Q^ K^T] (M 128, N 64, K 128), and [K^; Q^] for the chain
@@ -421,34 +440,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ok) gram_pending = true;
 
   // ---------------------------------------------------------- (B) value heads
+  // After A and P, threads 0-255 (the K group) form K^T diag(dec) and v, then
+  // the next head's v conv; threads 256-511 (the T group) form T.  The issuing
+  // warp stores each image once it is complete: P after A and P, K~ when the K
+  // group is done, T and the gates at the head's end, and waits for a store
+  // to have left shared memory only before that region is written again.
+  const bool kgrp = tid < 256;
   int g = 0;
   for (; ok && g < G; ++g) {
     const int h = jq * G + g;
-    float* const Gs = gbuf + 256 * (g & 1);
+    float* const Gs = gbuf + 256 * (g % kGateSets);
     const float* dec = Gs + 128;
     const float* bv = Gs + 192;
+    const int64_t hv = slot * p.Hv + h;
     if (!worker) {
-      // this head's gates; the set it overwrites, and [K^; Q^] (the region of
-      // A and T), have been read out by the bulk copies
-      if (tid == kMma) tc::bulk_wait_read();
-      __syncwarp();
-      chunk_gates(V, t0, n, h, lane, Gs);
-      named_arrive(3, kThreads);
-    } else {
-      if (g > 0) {
-        // v rows of this head (issued while the head before it was processed)
-        ok = workers_sync_and(work_wait(mbar + 2, (uint32_t)(g & 1), wlim) && ok);
-        if (ok) v_pending = -1;
-        if (c == 0) {
-          fix_history(xv, 2 * p.Hqk * D + h * D);
-          workers_sync();
-        }
-        v_conv(h);
-        workers_sync();
-        if (tid == 0 && ok && g + 1 < G) stage_v(g + 1);
-        if (ok && g + 1 < G) v_pending = g + 1;
+      if (g >= kGateSets) {
+        // the set was last stored by head g - kGateSets
+        if (tid == kMma) tc::bulk_wait_read();
+        __syncwarp();
+        chunk_gates(V, t0, n, h, lane, Gs);
+        tc::fence_async_smem();
+      } else if (g > 0 && tid == kMma) {
+        tc::bulk_wait_read_but<2>();      // P of the head before
       }
-      named_sync(3, kThreads);   // the gates; the previous head's images have been read out
+      __syncwarp();
+      named_arrive(3, kThreads);          // the gates; the P region is free
+      // [K^; Q^] (T's work region) or the head before's K~ has been read out
+      if (tid == kMma) {
+        if (g == 0) tc::bulk_wait_read();
+        else tc::bulk_wait_read_but<1>();
+      }
+      __syncwarp();
+      named_sync(5, kThreads);            // A and P are formed
+      if (tid == kMma) {
+        tc::bulk_store(ws.pm + hv * kImgP, sm + CkSmem::PB, kImgP);
+        tc::bulk_commit();
+        if (g > 0) tc::bulk_wait_read_but<1>();   // T and the gates of the head before
+      }
+      __syncwarp();
+      named_arrive(6, 288);               // the T image region is free
+      named_sync(7, 288);                 // K~ is formed
+      if (tid == kMma) {
+        tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
+        tc::bulk_commit();
+      }
+    } else {
+      named_sync(3, kThreads);
       if (g == 0) {
         mma_wait(mbar + 0, 0, ok, wlim);
         if (ok) gram_pending = false;
@@ -484,12 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      workers_sync();
-      if (tid >= 256) {
+      tc::fence_async_smem();
+      named_sync(5, kThreads);
+      if (!kgrp) {
         // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
         tri_inverse64(at, reinterpret_cast<const float*>(sm + CkSmem::AM), tf,
                       reinterpret_cast<float*>(sm + CkSmem::DT), reinterpret_cast<float*>(sm + CkSmem::NT),
                       tid - 256);
+        named_sync(6, 288);
         for (int e = tid - 256; e < 512; e += 256) {
           const int i = e >> 3, c8 = e & 7;
           const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
@@ -516,9 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
           tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
         }
+        tc::fence_async_smem();
+        named_arrive(7, 288);
         // v of channel `row`, rows [32 (tid >> 7), +32) -> the workspace (fp32
         // [i][r]: a warp's stores of one row are 128 contiguous bytes)
-        float* dst = ws.v + (slot * p.Hv + h) * (int64_t)(kImgV / 4) + 32 * (tid >> 7) * D + row;
+        float* dst = ws.v + hv * (int64_t)(kImgV / 4) + 32 * (tid >> 7) * D + row;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[16];
@@ -526,16 +567,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) dst[(16 * hh + e) * D] = v[e];
         }
+        if (g + 1 < G) {
+          // the next head's v rows (requested after this head's v conv) -> its v conv
+          ok = kgrp_sync_and(work_wait(mbar + 2, (uint32_t)((g + 1) & 1), wlim) && ok);
+          if (ok) v_pending = -1;
+          if (c == 0) {
+            fix_history(xv, 2 * p.Hqk * D + (h + 1) * D, tid, 256);
+            kgrp_sync();
+          }
+          v_conv(h + 1, 2 * (tid >> 7));
+          v_conv(h + 1, 2 * (tid >> 7) + 1);
+          kgrp_sync();
+          if (tid == 0 && ok && g + 2 < G) stage_v(g + 2);
+          if (ok && g + 2 < G) v_pending = g + 2;
+        }
       }
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
     if (tid == kMma) {
-      const int64_t hv = slot * p.Hv + h;
       tc::bulk_store(ws.t + hv * kImgT, sm + CkSmem::TB, kImgT);
-      tc::bulk_store(ws.pm + hv * kImgP, sm + CkSmem::PB, kImgP);
-      tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
       tc::bulk_store(ws.g + hv * (kImgG / 4), Gs, kImgG);
       tc::bulk_commit();
     }
@@ -546,8 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (default bound), release the tensor memory
     if (tid == 0) atomicExch(p.err, GDN_ERR_TIMEOUT);
     if (worker) {
+      // (the K group alone tracks the v rows once the value heads start)
       if (qk_pending) tc::mbar_wait_bounded(mbar + 1, 0, kWaitDefault);
-      if (v_pending >= 0) tc::mbar_wait_bounded(mbar + 2, (uint32_t)(v_pending & 1), kWaitDefault);
+      if ((kgrp || g == 0) && v_pending >= 0) tc::mbar_wait_bounded(mbar + 2, (uint32_t)(v_pending & 1), kWaitDefault);
       if (gram_pending) tc::mbar_wait_bounded(mbar + 0, 0, kWaitDefault);
     }
   }
