@@ -44,11 +44,11 @@ HBM_NOMINAL_GBS = 7900.0    # nominal HBM3e rate of the part (fractions use the 
 PREFILL = inputs.QWEN27B
 SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
-# DRAM bytes (read + write) of the tensor-core prefill kernel in one 4 x 8,192
-# call (its four piece launches summed: 711.96 MB read + 363.66 MB written),
-# from an ncu capture of the current kernel on this workload.  None once the
-# kernel changes.
-PREFILL_TRAFFIC_PER_CALL = 711.96e6 + 363.66e6
+# DRAM bytes (read + write) of one 4 x 8,192 prefill call on each tensor-core
+# path (every launch of the call summed), from an ncu capture of the current
+# kernels on this workload; None until captured, and again once a kernel of
+# the path changes.
+PREFILL_TRAFFIC_PER_CALL = {"fused": None, "two_kernels": None}
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
@@ -290,6 +290,28 @@ class PrefillWork:
         per_tok = sh.conv_dim * 2 + 2 * sh.num_v_heads * 4 + sh.num_v_heads * sh.head_dim_v * 2
         ck = (self.seq_len // sh.block_size + 1) * self.n * sh.payload_bytes
         return per_tok * self.tokens + ck
+
+
+def prefill_paths_ms(pre, runs: int = 5) -> dict:
+    """The same prefill call forced onto each tensor-core path (both give the
+    same bits), outside the timed step: ms per call, CUDA events."""
+    out = {}
+    for name, path in (("fused", gdn.PREFILL_FUSED), ("two_kernels", gdn.PREFILL_TWO_KERNELS)):
+        keep = pre.path
+        pre.path = path
+        for _ in range(2):
+            pre.run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(runs):
+            pre.run()
+        e1.record()
+        torch.cuda.synchronize()
+        pre.path = keep
+        out[name + "_ms"] = round(e0.elapsed_time(e1) / runs, 4)
+    if int(pre.err.item()):
+        raise RuntimeError("device error word set while timing the prefill paths")
+    return out
 
 
 class DecodeWork:
@@ -795,6 +817,7 @@ def main():
     # the call's own path (both give the same bits): its chain (or fused)
     # launches and, on the two-kernel path, the chunk kernel's launches
     pre_launches = pre_plan["launches"] + pre_plan["chunk_launches"]
+    path_key = "two_kernels" if pre_plan["two_kernels"] else "fused"
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
@@ -819,10 +842,11 @@ def main():
         "decode_hbm_frac_nominal": dec_gbs / HBM_NOMINAL_GBS, "flush_hbm_frac_nominal": fl_gbs / HBM_NOMINAL_GBS,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak,
-                     "traffic": PREFILL_TRAFFIC_PER_CALL if args.seq_len == SEQ_LEN else None,
-                     "traffic_note": "DRAM bytes per prefill call (the kernel's piece launches summed; "
-                                     "achieved is the call's work over its time), ncu capture of this workload",
-                     "kernel": "tc_prefill_kernel",
+                     "traffic": PREFILL_TRAFFIC_PER_CALL[path_key] if args.seq_len == SEQ_LEN else None,
+                     "traffic_note": "DRAM bytes per prefill call (every launch of the call summed; achieved "
+                                     "is the call's work over its time), ncu capture of this workload",
+                     "kernel": ("tc_chunk_kernel + tc_chain_kernel (the call)" if pre_plan["two_kernels"]
+                                else "tc_prefill_kernel"),
                      "work": "chunk-form flops (C 64) per token and v-head x tokens x heads; "
                              "executed as 3 bf16 passes",
                      "executed_tflops": achieved * EXECUTED_FLOPS_PER_TOKEN_HEAD / CHUNK_FLOPS_PER_TOKEN_HEAD,
@@ -846,6 +870,7 @@ def main():
         # append 2 (tensor-core append, log_len), rollback 1, flush 2
         "gpu_launches": args.steps * (pre_launches + 1 + DEC_LAYERS + 5 * REP_LAYERS),
         "prefill_path": "chunk + chain kernels" if pre_plan["two_kernels"] else "fused kernel",
+        "prefill_paths": prefill_paths_ms(pre),
         "prefill_launches": pre_launches,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"]},
     }

@@ -91,7 +91,8 @@ struct CkSmem {
   static constexpr uint32_t YK = 86016;              // SiLU(conv) of the k channels, fp32 [64][128] (kept)
   static constexpr uint32_t KQ = 118784;             // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t KQ_LO = KQ + 32768;
-  static constexpr uint32_t TF = KQ + 32768;         // (B) T fp32 [64][64]
+  static constexpr uint32_t VS = KQ;                 // (B) v fp32 [64 rows][128 channels], stored with K~
+  static constexpr uint32_t TF = KQ + 32768;         //     T fp32 [64][64]
   static constexpr uint32_t DT = KQ + 49152;         //     diagonal inverses [4][16][20]
   static constexpr uint32_t NT = KQ + 54272;         //     N blocks [6][16][16]
   static constexpr uint32_t GT = KQ + 65536;         // gate sets [4][4][64] fp32 (G, gam, dec, b), then rq, rk
@@ -283,10 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
     }
   };
-  // v conv of value head h: channel `row`, rows [16 qtr, +16) -> tensor
-  // memory (rows i and i + 8 as one packed pair)
-  auto v_conv = [&](int h, int qtr) {
-    const float4 wv = ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK);
+  // v conv of a value head with taps wv (v_taps): channel `row`, rows
+  // [16 qtr, +16) -> tensor memory (rows i and i + 8 as one packed pair)
+  auto v_taps = [&](int h) { return ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK); };
+  auto v_conv = [&](const float4 wv, int qtr) {
     const int tb = 16 * qtr;
     float xr[19], vr[16];
 #pragma unroll
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(yrow + i * D) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
       }
     }
-    v_conv(jq * G, quarter);
+    v_conv(v_taps(jq * G), quarter);
     workers_sync();
     // the first head's v rows are consumed: the next head's rows
     if (tid == 0 && ok && G > 1) stage_v(1);
@@ -465,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(3, kThreads);          // the gates; the P region is free
-      // [K^; Q^] (T's work region) or the head before's K~ has been read out
+      // [K^; Q^] (T's work region and v's image) or the head before's K~ and v
+      // have been read out
       if (tid == kMma) {
         if (g == 0) tc::bulk_wait_read();
         else tc::bulk_wait_read_but<1>();
@@ -479,9 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(6, 288);               // the T image region is free
-      named_sync(7, 288);                 // K~ is formed
+      named_sync(7, 288);                 // K~ and v are formed
       if (tid == kMma) {
         tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
+        tc::bulk_store(ws.v + hv * (kImgV / 4), sm + CkSmem::VS, kImgV);
         tc::bulk_commit();
       }
     } else {
@@ -541,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
         }
       } else {
+        // the next head's conv taps (their load's latency hides behind K~ and v)
+        const float4 wv = g + 1 < G ? v_taps(h + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         // K^T diag(dec) (row = k channel): the fused kernel's elements and
         // expression, four of its eight-row groups per thread
 #pragma unroll
@@ -555,18 +560,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
           tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
         }
-        tc::fence_async_smem();
-        named_arrive(7, 288);
-        // v of channel `row`, rows [32 (tid >> 7), +32) -> the workspace (fp32
-        // [i][r]: a warp's stores of one row are 128 contiguous bytes)
-        float* dst = ws.v + hv * (int64_t)(kImgV / 4) + 32 * (tid >> 7) * D + row;
+        // v of channel `row`, rows [32 (tid >> 7), +32) -> its image ([i][r]:
+        // a warp's stores of one row are 128 contiguous bytes), which leaves
+        // by a bulk copy (per-thread global stores of every CTA at once would
+        // back up the load / store pipe that shared-memory loads also use)
+        float* vs = reinterpret_cast<float*>(sm + CkSmem::VS) + 32 * (tid >> 7) * D + row;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float v[16];
           tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dst[(16 * hh + e) * D] = v[e];
+          for (int e = 0; e < 16; ++e) vs[(16 * hh + e) * D] = v[e];
         }
+        tc::fence_async_smem();
+        named_arrive(7, 288);
         if (g + 1 < G) {
           // the next head's v rows (requested after this head's v conv) -> its v conv
           ok = kgrp_sync_and(work_wait(mbar + 2, (uint32_t)((g + 1) & 1), wlim) && ok);
@@ -575,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             fix_history(xv, 2 * p.Hqk * D + (h + 1) * D, tid, 256);
             kgrp_sync();
           }
-          v_conv(h + 1, 2 * (tid >> 7));
-          v_conv(h + 1, 2 * (tid >> 7) + 1);
+          v_conv(wv, 2 * (tid >> 7));
+          v_conv(wv, 2 * (tid >> 7) + 1);
           kgrp_sync();
           if (tid == 0 && ok && g + 2 < G) stage_v(g + 2);
           if (ok && g + 2 < G) v_pending = g + 2;
@@ -1007,18 +1014,19 @@ constexpr int64_t kSegMin = 16, kSegLevels = 64;
 // A model of the paths in units of the fused kernel's chunk time (one chunk
 // of one chain, ~13.5 us on a GB300), fitted to measured calls of the
 // 27B-shaped layer (1-8 sequences of 8,192 tokens, one of 65,536 and of
-// 229,376).  The fused kernel: each launch runs its chains a chunk at a time,
-// ~1.5 for a launch.  A chunk CTA costs ~0.55 + 0.55 G of one SM (G value heads
-// a qk head: 27 us at G = 3), in whole waves over the SMs; a chain chunk ~0.35
-// (4.6 us), a chain launch ~2 more (the state in and out, the first images).
+// 229,376; within 4 % of each).  The fused kernel: each launch runs its chains
+// a chunk at a time, ~1.5 for a launch.  A chunk CTA costs ~0.4 + 0.4 G of one
+// SM (G value heads a qk head: 21.6 us at G = 3), in whole waves over the SMs;
+// a chain chunk ~0.35 (4.7 us), a chain launch ~3.2 more (the state in and
+// out, the first images, the launch gap).
 // Run one after the other, the two kernels take the chunk kernel's waves,
 // then the chain launches.  Overlapped (one round of chains), the first
 // level's chunk waves, then the longer of the chains' path and all the SM
 // time spread over every SM, plus the restart of each level.
 namespace {
-constexpr double kChainChunk = 0.35, kChainLaunch = 2.0, kFusedLaunch = 1.5;
+constexpr double kChainChunk = 0.35, kChainLaunch = 3.2, kFusedLaunch = 1.5;
 
-double chunk_cta_cost(int Hqk, int Hv) { return 0.55 + 0.55 * (double)Hv / Hqk; }
+double chunk_cta_cost(int Hqk, int Hv) { return 0.4 + 0.4 * (double)Hv / Hqk; }
 
 double waves(double ctas, int sms) { return std::ceil(ctas / sms); }
 

@@ -111,7 +111,7 @@ def _piece_case(seed):
     than the SMs, so the call runs as pieces of 8 chunks over two levels."""
     sh = inputs.with_(inputs.QWEN27B, block_size=256)
     N, L = 4, 1024
-    plan = gdn.gdn_prefill_plan_for(sh, N, L)
+    plan = gdn.gdn_prefill_plan_for(sh, N, L, 0, gdn.PREFILL_FUSED)
     if plan["levels"] < 2:
         pytest.skip(f"this GPU runs the call in one level: {plan}")
     cu = np.arange(0, N * L + 1, L)
