@@ -46,9 +46,11 @@ SMALL = inputs.QWEN4B
 N_SEQ, SEQ_LEN = 4, 8192
 # DRAM bytes (read + write) of one 4 x 8,192 prefill call on each tensor-core
 # path (every launch of the call summed), from an ncu capture of the current
-# kernels on this workload; None until captured, and again once a kernel of
-# the path changes.
-PREFILL_TRAFFIC_PER_CALL = {"fused": None, "two_kernels": None}
+# kernels on this workload (profiles/prefill_traffic_27b_4x8192.md); None
+# once a kernel of the path changes.  fused: 4 tc_prefill_kernel launches +
+# the window pass; two kernels: 1 tc_chunk_kernel + 4 tc_chain_kernel
+# launches + the window pass.
+PREFILL_TRAFFIC_PER_CALL = {"fused": 713.26e6 + 366.86e6, "two_kernels": 3692.88e6 + 3372.39e6}
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
@@ -857,6 +859,13 @@ def main():
                      "peak_kind": f"dense bf16 {peak_kind} (burst)",
                      "algorithmic_bytes_per_call": pre.algorithmic_bytes(),
                      "hbm_gbs_achieved": pre.algorithmic_bytes() / (pre_ms * 1e-3) / 1e9,
+                     # the call's measured DRAM traffic over its time: how close the path runs to HBM
+                     "traffic_gbs": (PREFILL_TRAFFIC_PER_CALL[path_key] / (pre_ms * 1e-3) / 1e9
+                                     if args.seq_len == SEQ_LEN and PREFILL_TRAFFIC_PER_CALL[path_key] else None),
+                     "traffic_hbm_frac": (PREFILL_TRAFFIC_PER_CALL[path_key] / (pre_ms * 1e-3) / 1e9
+                                          / peaks["hbm_gbs"]
+                                          if args.seq_len == SEQ_LEN and PREFILL_TRAFFIC_PER_CALL[path_key]
+                                          else None),
                      "hbm_peak_kind": peak_kind},
         "e2e": {"value": job_throughput(pre.tokens, world, e2e_ms), "unit": "tokens/s/layer",
                 "h2d_bytes_per_step": pre.h2d_bytes, "d2h_bytes_per_step": pre.d2h_bytes, "steps": e2e_steps,

@@ -238,32 +238,36 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
 def test_overlapped_levels_resume_bitwise():
     """A long sequence on the two kernels' overlapped levels, then the same
     sequence resumed from its second checkpoint (a shorter call, its own
-    levels): the resumed call reproduces the cold call's outputs and final
-    state bit for bit, and both match the oracle on two heads."""
+    levels): the resumed call reproduces the cold call's outputs, later
+    checkpoints and final state bit for bit, and both match the oracle on
+    two heads."""
     sh = inputs.QWEN27B
-    T, B = 4133, sh.block_size
-    for L in (T, T - 2 * B):
+    T, B = 6000, sh.block_size
+    nb = T // B                                   # 6 checkpoints
+    P = 2 * B
+    for L in (T, T - P):
         plan = gdn.gdn_prefill_plan_for(sh, 1, L, 0, gdn.PREFILL_TWO_KERNELS)
         if plan["chunk_launches"] < 2:
             pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
     ti = inputs.token_inputs(sh, T, seed=86)
     w = inputs.conv_weights(sh, 86)
-    pool = gdn.StatePool(sh, 8, fill=0)
+    pool = gdn.StatePool(sh, 2 + 2 * nb, fill=0)
     kw = dict(workspace=None, path=gdn.PREFILL_TWO_KERNELS)
-    o_cold, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [0], [-1], [[1, 2, 3, 4]],
+    cold_pages = list(range(1, nb + 1))
+    o_cold, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, [0, T], [0], [-1], [cold_pages],
                                  [0], max_seq_len=T, **kw)
     assert err == 0
-    P = 2 * B
+    res_pages = [-1, -1] + list(range(nb + 2, 2 * nb))
     o_res, err, _ = run_prefill(sh, pool, ti["x"][P:], ti["g"][P:], ti["beta"][P:], w, [0, T - P], [P], [2],
-                                [[-1, -1, 6, 7]], [5], max_seq_len=T - P, **kw)
+                                [res_pages], [nb + 1], max_seq_len=T - P, **kw)
     assert err == 0
     assert torch.equal(o_res.view(torch.int16), o_cold[P:].view(torch.int16))
-    assert torch.equal(pool.payload(5).cpu(), pool.payload(0).cpu())
-    assert torch.equal(pool.payload(6).cpu(), pool.payload(3).cpu())
-    assert torch.equal(pool.payload(7).cpu(), pool.payload(4).cpu())
+    assert torch.equal(pool.payload(nb + 1).cpu(), pool.payload(0).cpu())
+    for j in range(2, nb):
+        assert torch.equal(pool.payload(res_pages[j]).cpu(), pool.payload(cold_pages[j]).cpu()), j
     for h in (0, 47):
         ref = oracle_head(sh, ti["x"], ti["g"], ti["beta"], w, h, [0, T], [0], B)
         assert_out_close(o_cold[:, h:h + 1], ref["o"], [0, T])
         assert_state_close(pool.state(0).cpu()[None, h:h + 1], ref["S"])
-        for j, page in enumerate([1, 2, 3, 4]):
+        for j, page in enumerate(cold_pages):
             assert_state_close(pool.state(page).cpu()[None, h:h + 1], ref["ck_S"][j][None])
