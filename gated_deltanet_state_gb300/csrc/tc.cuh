@@ -24,6 +24,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test for the completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete, for at most about
 // `max_cycles` SM clocks.  Returns false if the wait ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity, long long max_cycles) {
@@ -31,6 +42,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity, 
   while (!mbar_try_wait(m, parity))
     if (clock64() - t0 > max_cycles) return false;
   return true;
+}
+// The same, returning at once (without the clock read and the potentially
+// suspending try) when the phase has already completed.
+__device__ __forceinline__ bool mbar_wait_bounded_fast(uint64_t* m, uint32_t parity, long long max_cycles) {
+  return mbar_test_wait(m, parity) || mbar_wait_bounded(m, parity, max_cycles);
 }
 
 // ---- fences -------------------------------------------------------------------

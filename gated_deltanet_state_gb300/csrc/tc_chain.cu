@@ -147,7 +147,7 @@ constexpr uint32_t kChUH = 448;     // R^T, then U^T: hi, bf16 pairs [128][32] (
 constexpr uint32_t kChUL = 480;     // lo
 
 __device__ __forceinline__ bool work_wait(uint64_t* m, uint32_t parity, long long lim) {
-  return lim >= 0 && tc::mbar_wait_bounded(m, parity, lim);
+  return lim >= 0 && tc::mbar_wait_bounded_fast(m, parity, lim);
 }
 __device__ __forceinline__ void mma_wait(uint64_t* m, uint32_t parity, bool& ok, long long lim) {
   ok = work_wait(m, parity, lim) && ok;
@@ -694,10 +694,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tS = tbase + tlane + kChS + 32 * quarter;
 
   // the issuing thread's loads of chunk c's images (each arms its mbarrier)
-  auto hv_of = [&](int64_t c) { return chunk_slot(p, s, c) * p.Hv + h; };
+  // the chunk slots of this sequence start at slot0 (chunk_slot without the
+  // global load of cu_seqlens on the issuing thread's path)
+  const int64_t slot0 = row0 / kC + s;
+  auto hv_of = [&](int64_t c) { return (slot0 + c) * p.Hv + h; };
   auto load_kq = [&](int64_t c) {
     tc::mbar_expect_tx(mbar + ChSmem::kKQ, kImgKQ);
-    const uint8_t* src = ws.kq + (chunk_slot(p, s, c) * p.Hqk + hq) * kImgKQ;
+    const uint8_t* src = ws.kq + ((slot0 + c) * p.Hqk + hq) * kImgKQ;
     tc::bulk_load(sm + ChSmem::KQ, src, 32768, mbar + ChSmem::kKQ);
     tc::bulk_load(sm + ChSmem::KQ + 32768, src + 32768, 32768, mbar + ChSmem::kKQ);
     armed[ChSmem::kKQ] = c;
@@ -833,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tmem_st32(tS, v0);
       tc::tmem_st_wait();
+      if (tid == 0) tc::bulk_wait_read();   // the output tile, before this chunk's step 2 rewrites it
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
@@ -877,9 +881,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                              sbase + ChSmem::TB + b * kImgT + 8192, tc::idesc_bf16_f32(128, 64), false);
       tc::mma_commit(mbar + ChSmem::kU);
       armed[ChSmem::kU] = c;
-      // the previous chunk's output tile; the next chunk's gates and P (their
-      // buffer's last readers, the outputs and U^T P^T of chunk c - 1, are
-      // done), [K^; Q^] (S0 [K^; Q^]^T is done) and v (R has read it)
+    }
+    if (tid == 0) {
+      // (off the issuing thread's path, which goes on to R T^T) the previous
+      // chunk's output tile; the next chunk's gates and P (their buffer's last
+      // readers, the outputs and U^T P^T of chunk c - 1, are done), [K^; Q^]
+      // (S0 [K^; Q^]^T is done) and v (R has read it)
       if (c > cb && tma_out && full_chunk(c - 1)) {
         tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
         tc::bulk_commit();
@@ -915,7 +922,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (work_wait(mbar + ChSmem::kS, par, wlim)) load_kt(c + 1);
         else ok = false;
       }
-      tc::bulk_wait_read();   // the output tile, before the next chunk's outputs rewrite it
     }
   }
 
@@ -929,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
-    if (ok && tid == kMma && tma_out && full_chunk(c - 1)) {
+    if (ok && tid == 0 && tma_out && full_chunk(c - 1)) {
       tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
       tc::bulk_commit();
     }
@@ -966,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (tid == kMma) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, kChCols);
