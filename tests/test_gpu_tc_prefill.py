@@ -271,3 +271,69 @@ def test_overlapped_levels_resume_bitwise():
         assert_state_close(pool.state(0).cpu()[None, h:h + 1], ref["S"])
         for j, page in enumerate(cold_pages):
             assert_state_close(pool.state(page).cpu()[None, h:h + 1], ref["ck_S"][j][None])
+
+
+def _paths_with_error(sh, lens, bt, seed, npages, max_seq_len=0, two_max_seq_len=None):
+    """The same call on the fused kernel and on the two kernels, each into a
+    fresh pool: (outputs, pool bytes, error word) per path."""
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    ti = inputs.token_inputs(sh, int(cu[-1]), seed=seed)
+    w = inputs.conv_weights(sh, seed)
+    res = []
+    for ws, path, L in ((False, gdn.PREFILL_FUSED, max_seq_len),
+                        (None, gdn.PREFILL_TWO_KERNELS, max_seq_len if two_max_seq_len is None else two_max_seq_len)):
+        pool = gdn.StatePool(sh, npages, fill=0x3C)
+        o, err, _ = run_prefill(sh, pool, ti["x"], ti["g"], ti["beta"], w, cu, [0] * len(lens), [-1] * len(lens),
+                                bt, list(range(len(lens))), max_seq_len=L, workspace=ws, path=path)
+        res.append((o, pool.buf.cpu(), err))
+    return cu, res
+
+
+def test_two_kernel_path_empty_sequences():
+    """Empty sequences among others: both paths give the same bits (the empty
+    sequences' final slots included), and no error."""
+    sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+    lens = [0, 300, 0, 129, 64, 0]
+    bt, npages = _tables(lens, 128, len(lens))
+    cu, ((o_f, pool_f, e_f), (o_2, pool_2, e_2)) = _paths_with_error(sh, lens, bt, 87, npages)
+    assert e_f == 0 and e_2 == 0
+    assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
+    assert torch.equal(pool_f, pool_2)
+
+
+def test_two_kernel_path_refuses_a_sequence_past_max_seq_len():
+    """max_seq_len sizes the two kernels' grid: a longer sequence sets
+    GDN_ERR_INVALID_ARG and gets no outputs; the sequences within the bound
+    are unaffected (the fused kernel's bits)."""
+    sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+    lens = [300, 700]
+    bt, npages = _tables(lens, 128, len(lens))
+    cu, ((o_f, pool_f, e_f), (o_2, pool_2, e_2)) = _paths_with_error(sh, lens, bt, 88, npages, max_seq_len=700,
+                                                                      two_max_seq_len=300)
+    assert e_f == 0
+    assert e_2 == gdn.STATUS_CODE["GDN_ERR_INVALID_ARG"]
+    assert torch.equal(o_f[:300].view(torch.int16), o_2[:300].view(torch.int16))
+    assert torch.isnan(o_2[300:].float()).all()
+    page = sh.page
+    for p_ in [0] + [int(x) for x in bt[0] if x >= 0]:     # sequence 0's final slot and checkpoints
+        assert torch.equal(pool_f[p_ * page:p_ * page + sh.state_bytes], pool_2[p_ * page:p_ * page + sh.state_bytes])
+    for p_ in [1] + [int(x) for x in bt[1] if x >= 0]:     # sequence 1: no state written
+        assert (pool_2[p_ * page:p_ * page + sh.state_bytes] == 0x3C).all()
+
+
+def test_two_kernel_path_bad_page_in_a_later_level():
+    """A checkpoint page outside the pool, reached in the second of the
+    overlapped levels: GDN_ERR_PAGE_RANGE, as on the fused kernel, and the
+    same bits everywhere else."""
+    sh = inputs.QWEN27B
+    plan = gdn.gdn_prefill_plan_for(sh, 1, 4133, 0, gdn.PREFILL_TWO_KERNELS)
+    if plan["chunk_launches"] < 2:
+        pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+    level_tokens = plan["piece_chunks"] * 64
+    jb = next(j for j in range(4) if (j + 1) * sh.block_size > level_tokens)   # a boundary past level 0
+    bt = [[1, 2, 3, 4]]
+    bt[0][jb] = 99
+    cu, ((o_f, pool_f, e_f), (o_2, pool_2, e_2)) = _paths_with_error(sh, [4133], bt, 89, 5, max_seq_len=4133)
+    assert e_f == e_2 == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
+    assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
+    assert torch.equal(pool_f, pool_2)
