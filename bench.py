@@ -274,6 +274,39 @@ class PrefillWork:
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / steps
 
+    def link_gbs(self, reps: int = 3) -> dict:
+        """The host link on its own, with the same pinned buffers: GB/s of the
+        step's input copies alone, of its output copy alone, and of both at
+        once on two streams (the floor of the streamed step)."""
+        xd = torch.empty_like(self.host["x"], device="cuda")
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event(enable_timing=True)
+
+        def timed(streams):
+            torch.cuda.synchronize()
+            e0 = [ev() for _ in streams]
+            e1 = [ev() for _ in streams]
+            for i, st in enumerate(streams):
+                e0[i].record(st)
+            for _ in range(reps):
+                if s_in in streams:
+                    with torch.cuda.stream(s_in):
+                        xd.copy_(self.host["x"], non_blocking=True)
+                if s_out in streams:
+                    with torch.cuda.stream(s_out):
+                        self.o_host.copy_(self.o, non_blocking=True)
+            for i, st in enumerate(streams):
+                e1[i].record(st)
+            torch.cuda.synchronize()
+            return max(a.elapsed_time(b) for a, b in zip(e0, e1)) / reps
+
+        xb = self.host["x"].numel() * self.host["x"].element_size()
+        ob = self.o_host.numel() * self.o_host.element_size()
+        t_in, t_out, t_both = timed([s_in]), timed([s_out]), timed([s_in, s_out])
+        del xd
+        return {"h2d_gbs": round(xb / t_in / 1e6, 1), "d2h_gbs": round(ob / t_out / 1e6, 1),
+                "both_gbs": round((xb + ob) / t_both / 1e6, 1)}
+
     @property
     def h2d_bytes(self):
         return sum(v.numel() * v.element_size() for v in self.host.values())
@@ -805,6 +838,7 @@ def main():
     # (at least 16 steps: the timed region also fills and drains the pipeline once)
     e2e_steps = max(args.steps, 16)
     e2e_ms = pre.e2e_pipelined_ms(e2e_steps)
+    link = pre.link_gbs()
     (e2e_ms,) = max_over_ranks([e2e_ms], dist, "cuda")
 
     peaks, peak_kind = _peaks()
@@ -872,8 +906,11 @@ def main():
                 "scope": "prefill part of the step; each step's input and output copies run on their own "
                          "streams, overlapping the neighbouring steps' prefill (three device buffer sets); "
                          "timed from the first input copy to the last output copy of `steps` steps",
-                "link_note": "the host link of these boxes moves ~210 GB/s in and ~193 GB/s out (~295 GB/s "
-                             "both ways, the same for SM-driven copies), so ~3.9 ms of a step is copies"},
+                "link_measured": link,
+                "copies_floor_ms": (pre.h2d_bytes + pre.d2h_bytes) / link["both_gbs"] / 1e6,
+                "link_note": "the host link bounds the streamed step (copies_floor_ms: the step's bytes at the "
+                             "link's measured both-ways rate on this box); it has measured ~295 GB/s both ways on "
+                             "some boxes of the pool and well under 200 GB/s on others"},
         # per step: prefill (the launches of the path the library takes on
         # this GPU, + the window pass); decode 1 per layer; replay per layer:
         # append 2 (tensor-core append, log_len), rollback 1, flush 2
@@ -902,6 +939,8 @@ def main():
         "verify_us_per_layer": round(1000.0 * ver_ms / REP_LAYERS, 2), "verify_hbm_frac": round(ver_gbs / peaks["hbm_gbs"], 3),
         "flush_us_per_layer": round(1000.0 * fl_ms / REP_LAYERS, 2), "flush_hbm_frac": round(fl_gbs / peaks["hbm_gbs"], 3),
         "e2e_tokens_per_s_layer": round(line["e2e"]["value"]),
+        "e2e_ms_per_step": round(e2e_ms, 3), "e2e_copies_floor_ms": round(line["e2e"]["copies_floor_ms"], 3),
+        "prefill_path": line["prefill_path"],
     }
     lc = line.get("long_context")
     if isinstance(lc, dict):
