@@ -1108,13 +1108,22 @@ struct SideStream {
 std::mutex g_side_mu;
 SideStream g_side[64];
 
-cudaError_t side_stream(SideStream*& out) {
+// out = nullptr (and success) when the stream does not exist yet and the
+// caller's stream is capturing a graph: the call then runs its levels one
+// after the other on the caller's stream (the same bits), so that no stream
+// or event is created inside a capture.
+cudaError_t side_stream(cudaStream_t caller, SideStream*& out) {
+  out = nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   SideStream& ss = g_side[dev];
   if (!ss.stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(caller, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) return cudaSuccess;
     int least = 0, greatest = 0;
     e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
     if (e != cudaSuccess) return e;
@@ -1203,20 +1212,30 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     // launch l is done; its launch l + 1 meanwhile on the caller's stream
     std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream* ss = nullptr;
-    e = side_stream(ss);
+    e = side_stream(st, ss);
     if (e != cudaSuccess) return e;
-    for (int64_t l = 0; l < sc.levels && e == cudaSuccess; ++l) {
-      const int64_t c0 = l * sc.piece;
-      e = chunk_launch(c0, maxc - c0 < sc.piece ? maxc - c0 : sc.piece, st);
-      if (e == cudaSuccess) e = cudaEventRecord(ss->ready, st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->ready, 0);
-      if (e == cudaSuccess) e = chain_launch(l, 0, p.num_seqs, ss->stream);
+    if (!ss) {
+      // first use inside a graph capture: the levels one after the other
+      for (int64_t l = 0; l < sc.levels && e == cudaSuccess; ++l) {
+        const int64_t c0 = l * sc.piece;
+        e = chunk_launch(c0, maxc - c0 < sc.piece ? maxc - c0 : sc.piece, st);
+        if (e == cudaSuccess) e = chain_launch(l, 0, p.num_seqs, st);
+      }
+      if (e != cudaSuccess) return e;
+    } else {
+      for (int64_t l = 0; l < sc.levels && e == cudaSuccess; ++l) {
+        const int64_t c0 = l * sc.piece;
+        e = chunk_launch(c0, maxc - c0 < sc.piece ? maxc - c0 : sc.piece, st);
+        if (e == cudaSuccess) e = cudaEventRecord(ss->ready, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->ready, 0);
+        if (e == cudaSuccess) e = chain_launch(l, 0, p.num_seqs, ss->stream);
+      }
+      // the join, also after a failed launch (a capture needs its fork joined)
+      const cudaError_t j = cudaEventRecord(ss->join, ss->stream);
+      const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, ss->join, 0) : j;
+      if (e != cudaSuccess) return e;
+      if (w != cudaSuccess) return w;
     }
-    // the join, also after a failed launch (a capture needs its fork joined)
-    const cudaError_t j = cudaEventRecord(ss->join, ss->stream);
-    const cudaError_t w = j == cudaSuccess ? cudaStreamWaitEvent(st, ss->join, 0) : j;
-    if (e != cudaSuccess) return e;
-    if (w != cudaSuccess) return w;
   } else {
     e = chunk_launch(0, maxc, st);
     if (e != cudaSuccess) return e;

@@ -337,3 +337,44 @@ def test_two_kernel_path_bad_page_in_a_later_level():
     assert e_f == e_2 == gdn.STATUS_CODE["GDN_ERR_PAGE_RANGE"]
     assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
     assert torch.equal(pool_f, pool_2)
+
+
+def test_overlapped_levels_capture_into_a_cuda_graph():
+    """The two kernels' overlapped levels (a fork onto the second stream and a
+    join back per call) captured into a CUDA graph: a replay gives the eager
+    call's bits (outputs and pool)."""
+    sh = inputs.QWEN27B
+    T = 4133
+    plan = gdn.gdn_prefill_plan_for(sh, 1, T, 0, gdn.PREFILL_TWO_KERNELS)
+    if plan["chunk_launches"] < 2:
+        pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+    ti = inputs.token_inputs(sh, T, seed=90)
+    w = inputs.conv_weights(sh, 90).cuda()
+    x, g, beta = ti["x"].cuda(), ti["g"].cuda(), ti["beta"].cuda()
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    start = torch.zeros(1, dtype=torch.int64, device="cuda")
+    init = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    bt = torch.tensor([[1, 2, 3, 4]], dtype=torch.int32, device="cuda")
+    slot = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = gdn.workspace_for(gdn.gdn_prefill_workspace_size(sh, 1, T))
+    runs = []
+    for _ in range(2):
+        pool = gdn.StatePool(sh, 5, fill=0)
+        o = torch.full((T, sh.num_v_heads, sh.head_dim_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        runs.append((pool, o, err))
+    call = lambda pool, o, err: gdn.gdn_prefill_chunked(
+        sh, pool, cu_seqlens=cu, start_pos=start, init_page=init, block_table=bt, out_slot=slot, x=x, g=g,
+        beta=beta, conv_w=w, o=o, dev_error=err, start_pos_host=[0], init_page_host=[-1], workspace=ws,
+        max_seq_len=T, path=gdn.PREFILL_TWO_KERNELS)
+    call(*runs[0])                       # eager (also makes the second stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(*runs[1])
+    graph.replay()
+    torch.cuda.synchronize()
+    (p0, o0, e0), (p1, o1, e1) = runs
+    assert e0.item() == 0 and e1.item() == 0
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16))
+    assert torch.equal(p0.buf, p1.buf)
