@@ -1024,19 +1024,20 @@ constexpr double kChainLaunchCost = 5.0;
 constexpr int64_t kSegMin = 16, kSegLevels = 64;
 
 // A model of the paths in units of the fused kernel's chunk time (one chunk
-// of one chain, ~13.5 us on a GB300), fitted to measured calls of the
-// 27B-shaped layer (1-8 sequences of 8,192 tokens, one of 65,536 and of
-// 229,376; within 4 % of each).  The fused kernel: each launch runs its chains
-// a chunk at a time, ~1.5 for a launch.  A chunk CTA costs ~0.4 + 0.4 G of one
-// SM (G value heads a qk head: 21.6 us at G = 3), in whole waves over the SMs;
-// a chain chunk ~0.35 (4.7 us), a chain launch ~3.2 more (the state in and
-// out, the first images, the launch gap).
+// of one chain, ~13.7 us on a GB300), fitted to 17 measured calls of the
+// 27B-shaped layer (1 to 64 sequences of 512 to 8,192 tokens, one of 65,536
+// and of 229,376; within 6 % of each).  The fused kernel: each launch runs
+// its chains a chunk at a time, ~3 for a launch and the window pass.  A chunk
+// CTA costs ~0.4 + 0.4 G of one SM (G value heads a qk head: 21.9 us at
+// G = 3), in whole waves over the SMs; a chain chunk ~0.32 (4.4 us), a chain
+// launch ~1.6 more (the state in and out, the first images), and the call
+// ~3 (its first launch and the window pass).
 // Run one after the other, the two kernels take the chunk kernel's waves,
 // then the chain launches.  Overlapped (one round of chains), the first
 // level's chunk waves, then the longer of the chains' path and all the SM
 // time spread over every SM, plus the restart of each level.
 namespace {
-constexpr double kChainChunk = 0.35, kChainLaunch = 3.2, kFusedLaunch = 1.5;
+constexpr double kChainChunk = 0.32, kChainLaunch = 1.6, kTwoFixed = 3.0, kFusedFixed = 3.0;
 
 double chunk_cta_cost(int Hqk, int Hv) { return 0.4 + 0.4 * (double)Hv / Hqk; }
 
@@ -1051,11 +1052,11 @@ double two_kernel_cost(int Hqk, int Hv, int num_seqs, int64_t maxc, int sms, con
   const double cta = chunk_cta_cost(Hqk, Hv);
   const double ctas = (double)num_seqs * maxc * Hqk;
   if (sc.chunk_launches <= 1)
-    return waves(ctas, sms) * cta + kFusedLaunch + chain_launches_cost(sc, maxc, sms, kChainChunk, kChainLaunch);
+    return waves(ctas, sms) * cta + kTwoFixed + chain_launches_cost(sc, maxc, sms, kChainChunk, kChainLaunch);
   const double all_sm = (ctas * cta + (double)sc.nchains * maxc * kChainChunk) / sms;
   const double path = (double)maxc * kChainChunk;
   const double first = waves((double)num_seqs * sc.piece * Hqk, sms) * cta;
-  return first + (path > all_sm ? path : all_sm) + kChainLaunch * (double)sc.levels;
+  return first + (path > all_sm ? path : all_sm) + kChainLaunch * (double)sc.levels + kTwoFixed;
 }
 }  // namespace
 
@@ -1090,7 +1091,7 @@ bool tc_prefill_two_kernels_faster(int Hqk, int Hv, int num_seqs, int64_t max_le
   if (sms <= 0 || num_seqs <= 0 || max_len <= 0 || Hqk <= 0) return false;
   const int64_t maxc = (max_len + kC - 1) / kC;
   const PrefillSchedule fs = tc_prefill_schedule(Hv, num_seqs, max_len, sms);
-  const double fused = chain_launches_cost(fs, maxc, sms, 1.0, kFusedLaunch);
+  const double fused = chain_launches_cost(fs, maxc, sms, 1.0, kFusedFixed);
   const PrefillSchedule sc = tc_chain_schedule(Hqk, Hv, num_seqs, max_len, sms);
   return two_kernel_cost(Hqk, Hv, num_seqs, maxc, sms, sc) < 0.95 * fused;
 }

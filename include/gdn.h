@@ -281,12 +281,14 @@ enum { GDN_PREFILL_AUTO = 0, GDN_PREFILL_FUSED = 1, GDN_PREFILL_TWO_KERNELS = 2 
  * state products.  The other path is one fused kernel that runs a chain's
  * chunks one after another on one SM and needs no scratch.  Both split and
  * multiply every operand alike and give the same bits, so the choice is
- * speed only: the two kernels win when a call's chains leave SMs idle (a
- * long prompt of one or two sequences), the fused kernel when they fill
- * them.  With GDN_PREFILL_AUTO a call takes the two kernels when it has a
- * workspace and a model of both paths' times (gdn_prefill_plan_for) favours
- * them; a call without a workspace (NULL, workspace_bytes 0) takes the fused
- * kernel.
+ * speed only: on a GB300 the two kernels win for long prompts (most for
+ * one or two sequences, whose few chains leave SMs idle) and for batches of
+ * 8,192-token sequences, the fused kernel for short calls of a few
+ * sequences, where the second launch and the chunk kernel's fixed cost do
+ * not pay.  With GDN_PREFILL_AUTO a call takes
+ * the two kernels when it has a workspace and a model of both paths' times
+ * (gdn_prefill_plan_for) favours them; a call without a workspace (NULL,
+ * workspace_bytes 0) takes the fused kernel.
  *
  * Other layers run a conv pre-pass whose SiLU(conv) rows (fp32, computed
  * once and shared by every head that reads them), q / k norm factors and

@@ -104,32 +104,34 @@ def test_benchmark_shape_plan():
         # a large batch (3,072 chains) stays one launch
         assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 64, 8192, 152, path)["launches"] == 1
     # one long sequence (48 chains): one launch of the fused kernel; the two
-    # kernels overlap 14 levels of 256 chunks with the chunk kernel
+    # kernels overlap 20 levels of 180 chunks with the chunk kernel
     assert gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, gdn.PREFILL_FUSED)["launches"] == 1
     plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 229376, 152, gdn.PREFILL_TWO_KERNELS)
-    assert plan == {"chains": 48, "piece_chunks": 256, "levels": 14, "ctas_per_launch": 48, "launches": 14,
-                    "two_kernels": 1, "chunk_launches": 14}
-    # 1 x 8,192: three levels of 44 chunks; 2 x 8,192 (96 chains leave 56 SMs
+    assert plan == {"chains": 48, "piece_chunks": 180, "levels": 20, "ctas_per_launch": 48, "launches": 20,
+                    "two_kernels": 1, "chunk_launches": 20}
+    # 1 x 8,192: four levels of 32 chunks; 2 x 8,192 (96 chains leave 56 SMs
     # idle) runs the two kernels one after the other
     plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, 1, 8192, 152, gdn.PREFILL_TWO_KERNELS)
-    assert (plan["piece_chunks"], plan["levels"], plan["chunk_launches"]) == (44, 3, 3)
+    assert (plan["piece_chunks"], plan["levels"], plan["chunk_launches"]) == (32, 4, 4)
     for N in (2, 3):
         plan = gdn.gdn_prefill_plan_for(inputs.QWEN27B, N, 8192, 152, gdn.PREFILL_TWO_KERNELS)
         assert (plan["levels"], plan["launches"], plan["chunk_launches"]) == (1, 1, 1)
 
 
 def test_auto_path_follows_the_model():
-    """The model behind GDN_PREFILL_AUTO (both paths give the same bits): on
-    152 SMs every batch of 8,192-token sequences of the 27B-shaped layer and
-    every long sequence takes the two kernels (measured 0.86 / 1.27 / 1.58 /
-    2.12 / 4.25 ms for 1 / 2 / 3 / 4 / 8 sequences against the fused kernel's
-    1.81 / 1.80 / 1.81 / 2.45 / 4.84); short calls, whose chunk kernel and
-    second launch cost more than they save, take the fused kernel."""
+    """The model behind GDN_PREFILL_AUTO (both paths give the same bits),
+    fitted to 17 measured calls of the 27B-shaped layer on 152 SMs, in every
+    one of which the two kernels measured faster (e.g. 0.80 / 2.04 / 4.07 ms
+    for 1 / 4 / 8 sequences of 8,192 tokens against the fused kernel's 1.80 /
+    2.45 / 4.83; 0.129 against 0.161 ms for one of 512): those calls take the
+    two kernels; calls of a few chunks, whose chunk kernel and second launch
+    cost more than they save, take the fused kernel."""
     auto = lambda N, L: gdn.gdn_prefill_plan_for(inputs.QWEN27B, N, L, 152)["two_kernels"]
-    for N in (1, 2, 3, 4, 8, 64):
-        assert auto(N, 8192) == 1, N
-    assert auto(1, 229376) == 1 and auto(1, 65536) == 1
-    assert auto(1, 64) == 0 and auto(1, 512) == 0 and auto(2, 1024) == 0
+    for N, L in [(1, 512), (1, 768), (1, 1024), (2, 1024), (4, 1024), (4, 2048), (8, 2048), (16, 1024),
+                 (32, 2048), (64, 512), (1, 8192), (2, 8192), (3, 8192), (4, 8192), (8, 8192), (64, 8192),
+                 (1, 65536), (1, 229376)]:
+        assert auto(N, L) == 1, (N, L)
+    assert auto(1, 64) == 0 and auto(1, 256) == 0
 
 
 def test_plan_rejects_the_scan_path_and_bad_arguments():
