@@ -423,9 +423,10 @@ def gdn_core_prefill_workspace_size(shape: LayerShape, num_seqs: int, total_toke
 def gdn_core_prefill(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_pos, init_page, block_table,
                      out_slot, qkvz, ba, conv_w, A_log, dt_bias, norm_w, norm_eps: float, o, dev_error,
                      start_pos_host=None, init_page_host=None, workspace=None, max_seq_len: int = 0,
-                     stream=None, raise_on_error: bool = True) -> int:
+                     stream=None, raise_on_error: bool = True, path: int = PREFILL_AUTO) -> int:
     """The prefill on packed q | k | v | z and b | a rows, gated-normalised
-    outputs (gdn.h: gdn_core_prefill)."""
+    outputs (gdn.h: gdn_core_prefill).  Without `workspace` one of
+    gdn_core_prefill_workspace_size bytes is taken from PyTorch's allocator."""
     lib = load_library()
     n = int(cu_seqlens.numel()) - 1
     T = int(qkvz.shape[0])
@@ -441,6 +442,7 @@ def gdn_core_prefill(shape: LayerShape, pool: StatePool, *, cu_seqlens, start_po
                      _dev(bt, torch.int32, "block_table") if bt is not None and bt.numel() else None,
                      _dev(out_slot, torch.int32, "out_slot"), _dev(o, shape.torch_out(), "o"),
                      _dev(dev_error, torch.int32, "dev_error"))
+    a.path = int(path)
     c = _core_args(shape, ba, A_log, dt_bias, norm_w, norm_eps)
     st = lib.gdn_core_prefill(ctypes.byref(make_desc(shape)), ctypes.byref(pool.abi()), ctypes.byref(a),
                               ctypes.byref(c), _dev(workspace, None, "workspace"),

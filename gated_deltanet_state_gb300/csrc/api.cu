@@ -115,6 +115,13 @@ size_t gdn_replay_workspace_size(const gdn_layer_desc* desc, int32_t num_reqs) {
 
 namespace {
 
+// The packed core's gates g, b of every row and value head (fp32), 256-byte
+// rounded: the start of its workspace.
+size_t core_gates_bytes(const gdn_layer_desc* desc, int64_t total_tokens) {
+  const size_t b = 2 * sizeof(float) * (size_t)total_tokens * desc->num_v_heads;
+  return (b + 255) / 256 * 256;
+}
+
 // The prefill, plain or on packed rows (core != nullptr).
 gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* a,
                         const gdn_core_args* core, void* workspace, size_t workspace_bytes, void* stream) {
@@ -148,22 +155,30 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
     for (int32_t s = 0; s < a->num_seqs; ++s)
       if (a->init_page_host[s] < -1 || a->init_page_host[s] >= pool->num_pages) return GDN_ERR_PAGE_RANGE;
   if (a->max_seq_len < 0) return GDN_ERR_INVALID_ARG;
-  const size_t need = core ? gdn_core_prefill_workspace_size(desc, a->num_seqs, a->total_tokens)
-                           : gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
   const bool tc = tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                                        desc->block_size);
+  // the packed core: its rows' gates first in the workspace, then (two
+  // kernels) the operand images; a workspace of the gates alone keeps the
+  // fused kernel
+  const size_t core_gates = core ? core_gates_bytes(desc, a->total_tokens) : 0;
+  const size_t core_images =
+      core && tc ? tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, a->num_seqs, a->total_tokens)
+                 : 0;
   if (a->path < GDN_PREFILL_AUTO || a->path > GDN_PREFILL_TWO_KERNELS || a->reserved != 0)
     return GDN_ERR_INVALID_ARG;
   const int64_t max_len = a->max_seq_len > 0 ? a->max_seq_len : a->total_tokens;
   // a tensor-core layer: the two kernels when asked for, or (AUTO) when a
   // workspace is given and they are expected to be faster; else the fused one
   const bool has_ws = !(workspace == nullptr && workspace_bytes == 0);
+  const bool core_fits_two = !core || workspace_bytes >= core_gates + core_images;
   const bool two_kernels =
-      tc && !core &&
+      tc &&
       (a->path == GDN_PREFILL_TWO_KERNELS ||
-       (a->path == GDN_PREFILL_AUTO && has_ws &&
+       (a->path == GDN_PREFILL_AUTO && has_ws && core_fits_two &&
         tc_prefill_two_kernels_faster(desc->num_qk_heads, desc->num_v_heads, a->num_seqs, max_len,
                                       tc_prefill_sm_count())));
+  const size_t need = core ? core_gates + (two_kernels ? core_images : 0)
+                           : gdn_prefill_workspace_size(desc, a->num_seqs, a->total_tokens);
   const bool needs_ws = core || !tc || two_kernels || (a->path == GDN_PREFILL_AUTO && has_ws);
   if (need > 0 && needs_ws && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return GDN_ERR_WORKSPACE;
@@ -199,8 +214,9 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
   } else if (need > 0 && !tc) {
     bind_workspace(p, workspace, a->total_tokens);
   }
-  return cuda_status(launch_prefill(p, two_kernels ? workspace : nullptr, max_len, desc->head_dim_k,
-                                    desc->head_dim_v, desc->in_dtype, desc->out_dtype, cs));
+  void* images = two_kernels ? static_cast<uint8_t*>(workspace) + core_gates : nullptr;
+  return cuda_status(launch_prefill(p, images, max_len, desc->head_dim_k, desc->head_dim_v, desc->in_dtype,
+                                    desc->out_dtype, cs));
 }
 
 }  // namespace
@@ -214,10 +230,12 @@ gdn_status gdn_prefill_chunked(const gdn_layer_desc* desc, const gdn_pool* pool,
 }
 
 size_t gdn_core_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens) {
-  (void)num_seqs;
-  if (gdn_conv_dim(desc) <= 0 || total_tokens < 0) return 0;
-  const size_t b = 2 * sizeof(float) * (size_t)total_tokens * desc->num_v_heads;
-  return (b + 255) / 256 * 256;
+  if (gdn_conv_dim(desc) <= 0 || total_tokens < 0 || num_seqs < 0) return 0;
+  const size_t gates = core_gates_bytes(desc, total_tokens);
+  if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
+                            desc->block_size))
+    return gates;
+  return gates + tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, num_seqs, total_tokens);
 }
 
 gdn_status gdn_core_prefill(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* a,

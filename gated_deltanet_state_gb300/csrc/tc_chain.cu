@@ -773,6 +773,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
+  // packed core: the outputs of chunk c gated-normalised as the fused kernel
+  // does it (a token's 128 outputs meet in shared memory, the v image's
+  // region, free once R has read it; warp w then takes tokens w, w + 16, ...:
+  // RMS over dv, the norm scale, the silu(z) gate from the packed row).  Every
+  // worker calls it (two worker barriers).
+  const bool core = p.norm_w != nullptr;
+  auto outputs_core = [&](int64_t c, const float (&sq)[16]) {
+    const float* gam = gates_of(c) + 64;
+    float up[16];
+    tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, up);
+    float* of = reinterpret_cast<float*>(sm + ChSmem::VS);
+    workers_sync();   // every worker's R has read v
+#pragma unroll
+    for (int e = 0; e < 16; ++e) of[(16 * quarter + e) * D + row] = fmaf(gam[16 * quarter + e], sq[e], up[e]);
+    workers_sync();
+    const int64_t t0 = c * C;
+    const int cnt = (int)(n - t0 < C ? n - t0 : C);
+    const int lane = tid & 31;
+    const __nv_bfloat16* zrow =
+        reinterpret_cast<const __nv_bfloat16*>(p.x) + (row0 + t0) * p.x_ld + p.conv_dim + h * D;
+    TOUT* orow = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D;
+    for (int i = warp; i < cnt; i += kWorkers / 32) {
+      float v[4];
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        v[m] = of[i * D + lane + 32 * m];
+        ss = fmaf(v[m], v[m], ss);
+      }
+      ss = warp_sum(ss);
+      const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float z = to_f32(zrow[(int64_t)i * p.x_ld + lane + 32 * m]);
+        orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * p.norm_w[lane + 32 * m] * silu(z));
+      }
+    }
+  };
   // 16 fp32 values (rows [16 quarter, +16) of state row `row`) as bf16 hi / lo
   // pairs into the tensor-memory A operand
   auto split_to_tmem = [&](const float (&a)[16]) {
@@ -860,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- (2) the previous chunk's outputs (its U^T P^T is done), then R_i =
       // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16),
       // into the tensor-memory operand
-      if (c > cb) {
+      if (c > cb && !core) {
         mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
         outputs(c - 1, sq);
         tc::fence_async_smem();
@@ -873,10 +911,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i0 = 16 * quarter;
       const float* vs = reinterpret_cast<const float*>(sm + ChSmem::VS) + i0 * D + row;
       float a[16];
-      tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChSQ + i0, a, sq);
+      if (core) tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
+      else tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChSQ + i0, a, sq);
 #pragma unroll
       for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vs[e * D]);
       split_to_tmem(a);
+      if (core) {
+        // the previous chunk's outputs after R (they use v's region), with its
+        // S0 Q^T still in registers; then this chunk's
+        if (c > cb) {
+          mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
+          outputs_core(c - 1, sq);
+        }
+        tc::tmem_ld16(tbase + tlane + kChSQ + i0, sq);
+      }
     }
     ok = cta_sync_ok(ok);
     if (!ok) break;
@@ -937,7 +985,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && worker) {
       mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
       mma_wait(mbar + ChSmem::kUP, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
-      outputs(c - 1, sq);
+      if (core) outputs_core(c - 1, sq);
+      else outputs(c - 1, sq);
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
@@ -1184,7 +1233,7 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   CUtensorMap omap;
   memset(&omap, 0, sizeof(omap));
   int tma_out = 0;
-  if (p.total_rows > 0 && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
+  if (p.total_rows > 0 && !p.norm_w && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.Hv * kD, (cuuint64_t)p.total_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.Hv * kD * 2};

@@ -413,16 +413,23 @@ typedef struct gdn_core_args {
   int32_t reserved;
 } gdn_core_args;
 
-/* Device workspace of gdn_core_prefill: the gates of every row (fp32). */
+/* Device workspace of gdn_core_prefill: the gates of every row (fp32,
+ * 2 x 4 x T x Hv bytes rounded up to 256), then, on the tensor-core path,
+ * the two kernels' operand images (as gdn_prefill_workspace_size).  A
+ * workspace of the gates alone (at least that many bytes, less than this
+ * size) runs the fused kernel; with this size, GDN_PREFILL_AUTO chooses as
+ * gdn_prefill_chunked does.  Both paths give the same bits. */
 size_t gdn_core_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs, int64_t total_tokens);
 
 /* gdn_prefill_chunked on packed rows: args->x is [T][conv_dim + Hv*dv]
  * in_dtype (q | k | v | z; the conv and the windows use the first conv_dim
  * channels), args->g and args->beta are ignored (may be NULL), args->o
  * receives y.  States, checkpoints and windows are those of the plain
- * prefill on the same q | k | v rows and gates.  Layers on the tensor-core
- * path only (dk = dv = 128, bf16, block a multiple of 64), else
- * GDN_ERR_UNSUPPORTED_SHAPE. */
+ * prefill on the same q | k | v rows and gates.  args->path chooses between
+ * the fused kernel and the two kernels as for gdn_prefill_chunked
+ * (GDN_PREFILL_TWO_KERNELS needs the full gdn_core_prefill_workspace_size,
+ * else GDN_ERR_WORKSPACE).  Layers on the tensor-core path only (dk = dv =
+ * 128, bf16, block a multiple of 64), else GDN_ERR_UNSUPPORTED_SHAPE. */
 gdn_status gdn_core_prefill(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* args,
                             const gdn_core_args* core, void* workspace, size_t workspace_bytes, void* stream);
 

@@ -89,3 +89,75 @@ def test_core_decode_matches_oracle(shape):
     assert_state_close(torch.stack([pool.state(p) for p in range(N)]).cpu(), S_ref)
     for p in range(N):
         assert torch.equal(pool.window(p).cpu().float(), torch.as_tensor(win_ref[p], dtype=torch.float32))
+
+
+def _core_call(sh, pool, cu, start, init, bt, slots, qkvz, ba, w, A_log, dt_bias, norm_w, path, workspace=None):
+    T = int(cu[-1])
+    o = torch.full((T, sh.num_v_heads, sh.head_dim_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = gdn.gdn_core_prefill(sh, pool, cu_seqlens=dev(cu, torch.int32), start_pos=dev(start, torch.int64),
+                              init_page=dev(init, torch.int32), block_table=dev(bt, torch.int32),
+                              out_slot=dev(slots, torch.int32), qkvz=dev(qkvz), ba=dev(ba), conv_w=dev(w),
+                              A_log=dev(A_log), dt_bias=dev(dt_bias), norm_w=dev(norm_w), norm_eps=NORM_EPS, o=o,
+                              dev_error=err, start_pos_host=start, init_page_host=init, workspace=workspace,
+                              max_seq_len=int(np.max(np.diff(cu))), path=path, raise_on_error=False)
+    torch.cuda.synchronize()
+    return st, int(err.item()), o.cpu()
+
+
+@pytest.mark.parametrize("case", ["gqa3_resumed", "overlap_27b"])
+def test_core_prefill_two_kernels_give_the_fused_kernels_bits(case):
+    """The packed core on the chunk + chain kernels (the gated-norm epilogue
+    in the chain kernel) gives the fused kernel's bits: outputs, states,
+    checkpoints and windows; overlap_27b runs the overlapped levels."""
+    if case == "gqa3_resumed":
+        sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+        lens, start, init = [300, 65, 200], [0, 0, 256], [-1, -1, 9]
+        bt, slots, npages = [[3, 4, -1, -1], [-1] * 4, [-1, -1, 5, -1]], [0, 1, 2], 12
+    else:
+        sh = inputs.QWEN27B
+        lens, start, init = [4133], [0], [-1]
+        bt, slots, npages = [[1, 2, 3, 4]], [0], 5
+        plan = gdn.gdn_prefill_plan_for(sh, 1, 4133, 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    qkvz, ba, A_log, dt_bias, norm_w = _core_inputs(sh, int(cu[-1]), 94)
+    w = inputs.conv_weights(sh, 94)
+    st = inputs.random_state(sh, 1, seed=95)
+    res = []
+    for path in (gdn.PREFILL_FUSED, gdn.PREFILL_TWO_KERNELS):
+        pool = gdn.StatePool(sh, npages, fill=0x3C)
+        if 9 < npages:
+            pool.state(9).copy_(st["S"][0].cuda())
+            pool.window(9).copy_(st["win"][0].cuda())
+        status, err, o = _core_call(sh, pool, cu, start, init, bt, slots, qkvz, ba, w, A_log, dt_bias, norm_w, path)
+        assert status == 0 and err == 0
+        res.append((o, pool.buf.cpu()))
+    (o_f, p_f), (o_2, p_2) = res
+    assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
+    assert torch.equal(p_f, p_2)
+
+
+def test_core_prefill_workspace_of_the_gates_alone_keeps_the_fused_kernel():
+    """A workspace of the gates alone: AUTO runs the fused kernel (the same
+    bits as with the full workspace), the two kernels are refused."""
+    sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
+    lens = [700, 300]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    qkvz, ba, A_log, dt_bias, norm_w = _core_inputs(sh, T, 96)
+    w = inputs.conv_weights(sh, 96)
+    gates_only = gdn.workspace_for(-(-(2 * 4 * T * sh.num_v_heads) // 256) * 256)
+    args = (cu, [0, 0], [-1, -1], [[2, 3, 4, 5, 6], [7, 8, -1, -1, -1]], [0, 1], qkvz, ba, w, A_log, dt_bias, norm_w)
+    outs = []
+    for path, ws in ((gdn.PREFILL_AUTO, gates_only), (gdn.PREFILL_AUTO, None)):
+        pool = gdn.StatePool(sh, 9, fill=0)
+        status, err, o = _core_call(sh, pool, *args, path=path, workspace=ws)
+        assert status == 0 and err == 0
+        outs.append((o, pool.buf.cpu()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+    pool = gdn.StatePool(sh, 9, fill=0)
+    status, _, _ = _core_call(sh, pool, *args, path=gdn.PREFILL_TWO_KERNELS, workspace=gates_only)
+    assert status == gdn.STATUS_CODE["GDN_ERR_WORKSPACE"]
