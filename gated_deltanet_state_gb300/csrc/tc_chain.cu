@@ -130,9 +130,12 @@ struct ChSmem {
   static constexpr uint32_t MBAR = G + 2 * kImgG;
   // mbarriers: the images [K^; Q^], K~, T [2], P | gates [2], v; then the
   // products S0 [K^; Q^]^T, R T^T, the state update, U^T P^T
-  static constexpr int kKQ = 0, kKT = 1, kTb = 2, kPG = 4, kVb = 6, kSK = 7, kU = 8, kS = 9, kUP = 10, kBars = 11;
+  // (kZ: the packed core's z rows of a chunk, in the output tile's region)
+  static constexpr int kKQ = 0, kKT = 1, kTb = 2, kPG = 4, kVb = 6, kSK = 7, kU = 8, kS = 9, kUP = 10, kZ = 11,
+                       kBars = 12;
   static constexpr uint32_t ARMED = MBAR + 8 * kBars;    // int64 [kBars]: last chunk each was armed for
-  static constexpr uint32_t TSLOT = ARMED + 8 * kBars;
+  static constexpr uint32_t NW = ARMED + 8 * kBars;      // the packed core's norm scale fp32 [128]
+  static constexpr uint32_t TSLOT = NW + 512;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
   static constexpr bool two_buffers(int k) { return k == kTb || k == kTb + 1 || k == kPG || k == kPG + 1; }
@@ -636,6 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws,
                     const PieceMap pm, int64_t max_chunks) {
+  // omap: the outputs as [rows][Hv * dv] in 64-row tiles (tma_out), or for
+  // the packed core the z columns of the packed rows ([rows][x_ld], 128 x 64
+  // boxes), loaded a chunk ahead into the tile's shared memory
   using TOUT = __nv_bfloat16;
   constexpr int D = kD, C = kC;
   const int h = blockIdx.x;
@@ -693,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  if (p.norm_w && tid < D) reinterpret_cast<float*>(sm + ChSmem::NW)[tid] = p.norm_w[tid];
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -779,11 +786,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // RMS over dv, the norm scale, the silu(z) gate from the packed row).  Every
   // worker calls it (two worker barriers).
   const bool core = p.norm_w != nullptr;
-  auto outputs_core = [&](int64_t c, const float (&sq)[16]) {
+  auto load_z = [&](int64_t c) {
+    tc::mbar_expect_tx(mbar + ChSmem::kZ, 16384);
+    tc::tma_load_2d(ot, &omap, p.conv_dim + h * D, (int)(row0 + c * C), mbar + ChSmem::kZ);
+    armed[ChSmem::kZ] = c;
+  };
+  auto outputs_core = [&](int64_t c, const float (&sq)[16], bool& okc) {
     const float* gam = gates_of(c) + 64;
     float up[16];
     tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, up);
     float* of = reinterpret_cast<float*>(sm + ChSmem::VS);
+    okc = work_wait(mbar + ChSmem::kZ, (uint32_t)((c - cb) & 1), wlim) && okc;   // the z rows
     workers_sync();   // every worker's R has read v
 #pragma unroll
     for (int e = 0; e < 16; ++e) of[(16 * quarter + e) * D + row] = fmaf(gam[16 * quarter + e], sq[e], up[e]);
@@ -791,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t t0 = c * C;
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
     const int lane = tid & 31;
-    const __nv_bfloat16* zrow =
-        reinterpret_cast<const __nv_bfloat16*>(p.x) + (row0 + t0) * p.x_ld + p.conv_dim + h * D;
+    const __nv_bfloat16* zs = ot;
+    const float* nw = reinterpret_cast<const float*>(sm + ChSmem::NW);
     TOUT* orow = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D;
     for (int i = warp; i < cnt; i += kWorkers / 32) {
       float v[4];
@@ -806,8 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const float z = to_f32(zrow[(int64_t)i * p.x_ld + lane + 32 * m]);
-        orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * p.norm_w[lane + 32 * m] * silu(z));
+        const float z = to_f32(zs[i * D + lane + 32 * m]);
+        orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nw[lane + 32 * m] * silu_fast(z));
       }
     }
   };
@@ -921,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S0 Q^T still in registers; then this chunk's
         if (c > cb) {
           mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
-          outputs_core(c - 1, sq);
+          outputs_core(c - 1, sq, ok);
         }
         tc::tmem_ld16(tbase + tlane + kChSQ + i0, sq);
       }
@@ -945,6 +958,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
         tc::bulk_commit();
       }
+      // packed core: this chunk's z rows (the tile region is free: the
+      // previous chunk's outputs are done)
+      if (core) load_z(c);
       if (c + 1 < ce) {
         load_pg(c + 1);
         load_kq(c + 1);
@@ -985,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && worker) {
       mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
       mma_wait(mbar + ChSmem::kUP, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
-      if (core) outputs_core(c - 1, sq);
+      if (core) outputs_core(c - 1, sq, ok);
       else outputs(c - 1, sq);
       tc::fence_async_smem();
     }
@@ -1233,7 +1249,17 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   CUtensorMap omap;
   memset(&omap, 0, sizeof(omap));
   int tma_out = 0;
-  if (p.total_rows > 0 && !p.norm_w && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
+  if (p.total_rows > 0 && p.norm_w) {
+    // packed core: the z columns of the rows, 128 x 64 boxes
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[2] = {(cuuint64_t)p.x_ld, (cuuint64_t)p.total_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.x_ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
+    if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else if (p.total_rows > 0 && (reinterpret_cast<uintptr_t>(p.o) & 15) == 0) {
     const cuuint32_t estr[2] = {1, 1};
     const cuuint64_t dims[2] = {(cuuint64_t)p.Hv * kD, (cuuint64_t)p.total_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.Hv * kD * 2};

@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const float z = to_f32(zrow[(int64_t)i * p.x_ld + lane + 32 * m]);
-            orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * p.norm_w[lane + 32 * m] * silu(z));
+            orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * p.norm_w[lane + 32 * m] * silu_fast(z));
           }
         }
       } else if (tma_out && cnt == C) {
