@@ -27,7 +27,8 @@ def _core_inputs(sh, T, seed):
 NORM_EPS = 1e-6
 
 
-def test_core_prefill_matches_oracle_cold_and_resumed():
+@pytest.mark.parametrize("path", [gdn.PREFILL_FUSED, gdn.PREFILL_TWO_KERNELS], ids=["fused", "two_kernels"])
+def test_core_prefill_matches_oracle_cold_and_resumed(path):
     sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
     lens = [300, 65, 200]
     start = [0, 0, 256]
@@ -47,7 +48,7 @@ def test_core_prefill_matches_oracle_cold_and_resumed():
                          init_page=dev(init, torch.int32), block_table=dev(bt, torch.int32),
                          out_slot=dev([0, 1, 2], torch.int32), qkvz=dev(qkvz), ba=dev(ba), conv_w=dev(w),
                          A_log=dev(A_log), dt_bias=dev(dt_bias), norm_w=dev(norm_w), norm_eps=NORM_EPS, o=o,
-                         dev_error=err, start_pos_host=start, init_page_host=init)
+                         dev_error=err, start_pos_host=start, init_page_host=init, max_seq_len=max(lens), path=path)
     torch.cuda.synchronize()
     assert err.item() == 0
     S0 = np.zeros((3, sh.num_v_heads, sh.head_dim_v, sh.head_dim_k))
