@@ -1174,25 +1174,21 @@ struct SideStream {
 std::mutex g_side_mu;
 SideStream g_side[64];
 
-// out = nullptr (and success) when the stream does not exist yet and the
-// caller's stream is capturing a graph: the call then runs its levels one
-// after the other on the caller's stream (the same bits), so that no stream
-// or event is created inside a capture.
-cudaError_t side_stream(cudaStream_t caller, SideStream*& out) {
-  out = nullptr;
+// The stream of the current device, or nullptr when there is none to use:
+// it does not exist yet and the caller's stream is capturing a graph (so
+// that no stream or event is created inside a capture), the device index is
+// past the table, or making it failed.  The call then runs its levels one
+// after the other on the caller's stream (the same bits).
+SideStream* side_stream(cudaStream_t caller) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream& ss = g_side[dev];
   if (!ss.stream) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    e = cudaStreamIsCapturing(caller, &cap);
-    if (e != cudaSuccess) return e;
-    if (cap != cudaStreamCaptureStatusNone) return cudaSuccess;
+    if (cudaStreamIsCapturing(caller, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return nullptr;
     int least = 0, greatest = 0;
-    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e != cudaSuccess) return nullptr;
     cudaStream_t st = nullptr;
     cudaEvent_t r = nullptr, j = nullptr;
     e = cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest);
@@ -1202,14 +1198,13 @@ cudaError_t side_stream(cudaStream_t caller, SideStream*& out) {
       if (j) cudaEventDestroy(j);
       if (r) cudaEventDestroy(r);
       if (st) cudaStreamDestroy(st);
-      return e;
+      return nullptr;
     }
     ss.stream = st;
     ss.ready = r;
     ss.join = j;
   }
-  out = &ss;
-  return cudaSuccess;
+  return &ss;
 }
 
 }  // namespace
@@ -1287,11 +1282,9 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     // level l of every chain on the second stream once the chunk kernel's
     // launch l is done; its launch l + 1 meanwhile on the caller's stream
     std::lock_guard<std::mutex> lock(g_side_mu);
-    SideStream* ss = nullptr;
-    e = side_stream(st, ss);
-    if (e != cudaSuccess) return e;
+    SideStream* ss = side_stream(st);
     if (!ss) {
-      // first use inside a graph capture: the levels one after the other
+      // no second stream to use: the levels one after the other
       for (int64_t l = 0; l < sc.levels && e == cudaSuccess; ++l) {
         const int64_t c0 = l * sc.piece;
         e = chunk_launch(c0, maxc - c0 < sc.piece ? maxc - c0 : sc.piece, st);

@@ -317,9 +317,9 @@ size_t gdn_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_seqs,
  * 64 chunks (about 32 levels, at most 64) and overlaps them with the chunk
  * kernel (chunk_launches below).  The second stream and its two events are
  * made once per device, on the first such call, and kept for the process; a
- * first such call made while its stream captures a graph runs its levels on
- * that stream alone instead (the same bits), creating nothing during the
- * capture, and later captures record the fork and the join. */
+ * first such call made while its stream captures a graph, or one for which
+ * they cannot be made, runs its levels on its own stream alone instead (the
+ * same bits), and later captures record the fork and the join. */
 typedef struct gdn_prefill_plan {
   int64_t chains;           /* num_v_heads x num_seqs                        */
   int64_t piece_chunks;     /* chunks (64 tokens) per piece                  */
