@@ -864,10 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bpar = (uint32_t)(((c - cb) >> 1) & 1);
     if (worker) {
       // ---- (1) the state after chunk c - 1: checkpoint, split into tensor
-      // memory, gam_C S0 back
+      // memory (gam_C S0 goes back in step 2, while the first product runs)
       if (c > cb) mma_wait(mbar + ChSmem::kS, par ^ 1u, ok, wlim);
-      ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
-      const float gC = gates_of(c)[64 + C - 1];
       const int32_t ck = c > cb ? boundary_page(start + c * C) : -1;
       float* ckp = ck >= 0 ? page_state(p.pool, ck) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
       float v0[32];
@@ -885,13 +883,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_st8(tbase + tlane + kChS0H + 16 * quarter + 8 * hh, hi);
         tc::tmem_st8(tbase + tlane + kChS0L + 16 * quarter + 8 * hh, lo);
       }
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
-        v0[e] = gg.x;
-        v0[e + 1] = gg.y;
-      }
-      tc::tmem_st32(tS, v0);
       tc::tmem_st_wait();
       if (tid == 0) tc::bulk_wait_read();   // the output tile, before this chunk's step 2 rewrites it
     }
@@ -908,26 +899,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c + 1 < ce) load_t(c + 1);
     }
     if (worker) {
-      // ---- (2) the previous chunk's outputs (its U^T P^T is done), then R_i =
+      // ---- (2) gam_C S0 into the state's columns, which the state update
+      // accumulates onto (S0 [K^; Q^]^T reads only the hi / lo split); the
+      // previous chunk's outputs (its U^T P^T is done), then R_i =
       // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16),
       // into the tensor-memory operand
+      ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
+      {
+        const float gC = gates_of(c)[64 + C - 1];
+        float v0[32];
+        tc::tmem_ld32(tS, v0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+          v0[e] = gg.x;
+          v0[e + 1] = gg.y;
+        }
+        tc::tmem_st32(tS, v0);
+        tc::tmem_st_wait();
+      }
       if (c > cb && !core) {
         mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
         outputs(c - 1, sq);
         tc::fence_async_smem();
       }
       ok = work_wait(mbar + ChSmem::kVb, par, wlim) && ok;
-      mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
       const float* gs = gates_of(c);
       const float* gam = gs + 64;
       const float* bv = gs + 192;
       const int i0 = 16 * quarter;
       const float* vs = reinterpret_cast<const float*>(sm + ChSmem::VS) + i0 * D + row;
+      float vv[16];   // this row's v values, read before the product's wait
+#pragma unroll
+      for (int e = 0; e < 16; ++e) vv[e] = vs[e * D];
+      mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
       float a[16];
       if (core) tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
       else tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChSQ + i0, a, sq);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vs[e * D]);
+      for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vv[e]);
       split_to_tmem(a);
       if (core) {
         // the previous chunk's outputs after R (they use v's region), with its
