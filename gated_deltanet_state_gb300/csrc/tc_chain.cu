@@ -319,6 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   // ---------------------------------------------------------------- (A) q / k
   if (worker) {
+    // the conv taps of this thread's q | k channel pair and of its first
+    // head's v channel, requested before the rows' wait (their latency hides
+    // behind it)
+    const int qkp = 2 * (tid & 127);
+    const float* wsrc = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;
+    const float4 wqa = ldg_f4_fresh(wsrc), wqb = ldg_f4_fresh(wsrc + kConvK);
+    const float4 wv0 = v_taps(jq * G);
     ok = workers_sync_and(work_wait(mbar + 1, 0, wlim) && work_wait(mbar + 2, 0, wlim));
     if (ok) { qk_pending = false; v_pending = -1; }
     if (c == 0) {
@@ -329,9 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16)
     {
-      const int qkp = 2 * (tid & 127);
-      const float* wsrc = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;
-      const float4 wqa = ldg_f4_fresh(wsrc), wqb = ldg_f4_fresh(wsrc + kConvK);
       const int tb = 16 * (tid >> 7);
       const TIN* xp = (qkp < D ? xq + qkp : xk + qkp - D) + tb * D;
       const f32x2 w0 = pack2(wqa.x, wqb.x), w1 = pack2(wqa.y, wqb.y), w2 = pack2(wqa.z, wqb.z),
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(yrow + i * D) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
       }
     }
-    v_conv(v_taps(jq * G), quarter);
+    v_conv(wv0, quarter);
     workers_sync();
     // the first head's v rows are consumed: the next head's rows
     if (tid == 0 && ok && G > 1) stage_v(1);
