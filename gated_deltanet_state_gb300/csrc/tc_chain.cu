@@ -437,6 +437,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_async_smem();
   }
   if (!worker) {
+    // the q, k and first v rows of the CTA one round of SMs ahead (it starts
+    // about when this one ends) into L2, so that its first wait is short
+    if (tid == kMma) {
+      uint32_t nsm;
+      asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+      const int64_t gx = gridDim.x, gy = gridDim.y;
+      const int64_t nxt = (int64_t)blockIdx.x + gx * ((int64_t)blockIdx.y + gy * blockIdx.z) + nsm;
+      const int64_t s2 = nxt / (gx * gy);
+      if (s2 < p.num_seqs) {
+        const int j2 = (int)(nxt % gx);
+        const int64_t y2 = (int64_t)p.cu_seqlens[s2] + (c0 + (nxt / gx) % gy) * C - kWinRows;
+        if (y2 >= 0 && y2 + kXRows <= p.total_rows) {
+          tc::tma_prefetch_2d(&xmap, j2 * D, (int)y2);
+          tc::tma_prefetch_2d(&xmap, p.Hqk * D + j2 * D, (int)y2);
+          tc::tma_prefetch_2d(&xmap, 2 * p.Hqk * D + j2 * G * D, (int)y2);
+        }
+      }
+    }
     // the value heads' gate sets (up to four) while the workers convolve
     for (int g = 0; g < G && g < kGateSets; ++g) chunk_gates(V, t0, n, jq * G + g, lane, gbuf + 256 * g);
     tc::fence_async_smem();
@@ -624,7 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gram_pending) tc::mbar_wait_bounded(mbar + 0, 0, kWaitDefault);
     }
   }
-  if (tid == kMma) tc::bulk_wait_all();
+  // the images' shared memory has been read out (their global writes finish
+  // on their own; the chain kernel reads them only after this launch ends)
+  if (tid == kMma) tc::bulk_wait_read();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, kCkCols);
