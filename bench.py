@@ -710,6 +710,12 @@ def run_part(args):
     elif args.only == "decode":
         w = DecodeWork(args.seed, args.layers)
         fn = w.run
+    elif args.only == "flush":
+        w = FlushSweep(args.seed, args.requests, args.rows, args.layers, boundary=args.boundary)
+
+        def fn():
+            w.lens.fill_(w.rows)      # the flush clears log_len: every run flushes R rows
+            w.flush()
     else:
         w = ReplayWork(args.seed, args.layers)
         fn = lambda: (w.verify(), w.flush())
@@ -729,6 +735,9 @@ def run_part(args):
         line["seq_len"] = args.seq_len
         line["num_seqs"] = args.num_seqs
         line["plan"] = gdn.gdn_prefill_plan_for(PREFILL, args.num_seqs, args.seq_len, 0, w.path)
+    if args.only == "flush":
+        line.update(requests=args.requests, rows=args.rows, boundary_after=args.boundary,
+                    us_per_layer_incl_log_len_reset=1000.0 * ms / args.layers)
     print(json.dumps(line), flush=True)
 
 
@@ -742,8 +751,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-flush-sweep", action="store_true",
                     help="skip the flush sweep over kept rows and requests")
-    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "replay"],
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode", "replay", "flush"],
                     help="time one part only (profiling); the default times the whole step")
+    ap.add_argument("--requests", type=int, default=16, help="flush requests with --only flush")
+    ap.add_argument("--rows", type=int, default=16, help="kept rows per request with --only flush")
+    ap.add_argument("--boundary", type=int, default=0,
+                    help="with --only flush: every request's kept rows cross a block boundary after this many rows")
     ap.add_argument("--seq-len", type=int, default=SEQ_LEN,
                     help="prefill tokens per sequence (profiling of smaller cases)")
     ap.add_argument("--num-seqs", type=int, default=N_SEQ,
