@@ -62,7 +62,7 @@ constexpr uint32_t kImgKQ = 65536;   // [K^; Q^] hi | lo: 128 rows x 128 k, two 
 constexpr uint32_t kImgT = 16384;    // T hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgP = 16384;    // P hi | lo: 64 rows (i) x 64 k (j)
 constexpr uint32_t kImgK = 32768;    // K^T diag(dec) hi | lo: 128 rows (c) x 64 k (j)
-constexpr uint32_t kImgV = 32768;    // v fp32 [64 rows][128 channels]
+constexpr uint32_t kImgV = 32768;    // v fp32 [64 rows][128 channels] (image mode only)
 constexpr uint32_t kImgG = 1024;     // G, gam, dec, b fp32 [4][64]
 
 struct ChunkWs {
@@ -70,7 +70,7 @@ struct ChunkWs {
   uint8_t* t;      // [slots][Hv] kImgT
   uint8_t* pm;     // [slots][Hv] kImgP
   uint8_t* k;      // [slots][Hv] kImgK
-  float* v;        // [slots][Hv] kImgV
+  float* v;        // [slots][Hv] kImgV (image mode)
   float* g;        // [slots][Hv] kImgG
   int64_t slots;
 };
@@ -90,21 +90,21 @@ struct CkSmem {
   static constexpr uint32_t TB_LO = 8192;
   static constexpr uint32_t PB = 16384;              //     P hi [64][64], lo at +8 KB
   static constexpr uint32_t PB_LO = 24576;
-  static constexpr uint32_t XV = 34816;              // v rows of the current value head
+  static constexpr uint32_t XV = 34816;              // (image mode) v rows of the current value head
   static constexpr uint32_t YQ = 53248;              // (A) SiLU(conv) of the q channels, fp32 [64][128]
   static constexpr uint32_t KT = YQ;                 // (B) K^T diag(dec) hi [128][64], lo at +16 KB
   static constexpr uint32_t KT_LO = YQ + 16384;
   static constexpr uint32_t YK = 86016;              // SiLU(conv) of the k channels, fp32 [64][128] (kept)
   static constexpr uint32_t KQ = 118784;             // (A) [K^; Q^] hi [2 kb][128][64], lo at +32 KB
   static constexpr uint32_t KQ_LO = KQ + 32768;
-  static constexpr uint32_t VS = KQ;                 // (B) v fp32 [64 rows][128 channels], stored with K~
-  static constexpr uint32_t TF = KQ + 32768;         //     T fp32 [64][64]
+  static constexpr uint32_t VS = KQ;                 // (B, image mode) v fp32 [64 rows][128 channels], stored with K~
+  static constexpr uint32_t TF = KQ + 32768;         // (B) T fp32 [64][64]
   static constexpr uint32_t DT = KQ + 49152;         //     diagonal inverses [4][16][20]
   static constexpr uint32_t NT = KQ + 54272;         //     N blocks [6][16][16]
   static constexpr uint32_t GT = KQ + 65536;         // gate sets [4][4][64] fp32 (G, gam, dec, b), then rq, rk
   static constexpr uint32_t AT = GT + 4096 + 512;    // A^T fp32 [64 j][64 i]
   static constexpr uint32_t AM = AT + 16384;         // A fp32 row-major, slots swizzled
-  static constexpr uint32_t MBAR = AM + 16384;       // [0] Gram [1] q / k rows [2] v rows
+  static constexpr uint32_t MBAR = AM + 16384;       // [0] Gram [1] q / k rows [2] v rows (image mode)
   static constexpr uint32_t TSLOT = MBAR + 24;
   static constexpr uint32_t BYTES = TSLOT + 8;
   static constexpr uint32_t ALLOC = BYTES + 1024;
@@ -115,7 +115,7 @@ static_assert(CkSmem::ALLOC <= 232448, "chunk kernel shared memory exceeds the p
 constexpr int kGateSets = 4;        // gate sets of the chunk kernel (value heads formed ahead)
 constexpr uint32_t kCkCols = 128;   // tensor memory of the chunk kernel
 constexpr uint32_t kCkGram = 0;     // [K^ K^T; Q^ K^T]: lanes 0-63 k^_i.k^_j, 64-127 q^_i.k^_j
-constexpr uint32_t kCkV = 64;       // v of the chunk, lane = channel, column = row
+constexpr uint32_t kCkV = 64;       // (image mode) v of the chunk, lane = channel, column = row
 
 // ---- shared memory of the chain kernel: T and P (with the gates) in two
 // buffers, the others in one, each reloaded as soon as its reader is done -------
@@ -124,8 +124,9 @@ struct ChSmem {
   static constexpr uint32_t KT = KQ + kImgKQ;        // K^T diag(dec) hi | lo
   static constexpr uint32_t TB = KT + kImgK;         // T hi | lo [2]
   static constexpr uint32_t PB = TB + 2 * kImgT;     // P hi | lo [2]
-  static constexpr uint32_t VS = PB + 2 * kImgP;     // v fp32 [64 rows][128 channels]
-  static constexpr uint32_t OT = VS + kImgV;         // outputs bf16 [64 rows][128 dv]
+  static constexpr uint32_t XV = PB + 2 * kImgP;     // v: the image fp32 [64 rows][128 channels] (image mode), or
+                                                     // the pre-conv rows t0-3 .. t0+63 of the head, bf16 [67][128]
+  static constexpr uint32_t OT = XV + kImgV;         // outputs bf16 [64 rows][128 dv]
   static constexpr uint32_t G = OT + 16384;          // gate sets [2][4][64]
   static constexpr uint32_t MBAR = G + 2 * kImgG;
   // mbarriers: the images [K^; Q^], K~, T [2], P | gates [2], v; then the
@@ -212,6 +213,9 @@ __device__ __forceinline__ void chunk_gates(const TokenView<__nv_bfloat16>& V, i
 // ============================================================================
 // Chunk kernel: grid (Hqk, chunks, N), one CTA per (qk head, chunk c0 + y, sequence)
 // ============================================================================
+// VIMG (image mode): the chunk kernel also convolves v and writes it as an
+// image; otherwise the chain kernel convolves v from the rows itself.
+template <bool VIMG>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chunk_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap, const ChunkWs ws, int64_t c0) {
   using TIN = __nv_bfloat16;
@@ -276,12 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // copies and products in flight, for the drain after a run-out
   bool qk_pending = true, gram_pending = false;
-  int v_pending = 0;   // value head whose rows are in flight (-1: none)
+  int v_pending = VIMG ? 0 : -1;   // value head whose rows are in flight (-1: none)
   if (tid == 0) {
     tc::mbar_expect_tx(mbar + 1, 2 * kXRows * D * 2);
     tc::tma_load_2d(xq, &xmap, cq0, y, mbar + 1);
     tc::tma_load_2d(xk, &xmap, ck0, y, mbar + 1);
-    stage_v(0);
+    if (VIMG) stage_v(0);
   }
 
   // history rows of a sequence's first chunk: the resumed window, or zeros
@@ -293,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint32_t*>(dst + r * D + 2 * c2) = v;
     }
   };
-  // v conv of a value head with taps wv (v_taps): channel `row`, rows
-  // [16 qtr, +16) -> tensor memory (rows i and i + 8 as one packed pair)
+  // (image mode) v conv of a value head with taps wv (v_taps): channel `row`,
+  // rows [16 qtr, +16) -> tensor memory (rows i and i + 8 as one packed pair)
   auto v_taps = [&](int h) { return ldg_f4_fresh(p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK); };
   auto v_conv = [&](const float4 wv, int qtr) {
     const int tb = 16 * qtr;
@@ -315,23 +319,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_st16(tbase + tlane + kCkV + 16 * qtr, vr);
     tc::tmem_st_wait();
   };
-
   bool ok = true;
   // ---------------------------------------------------------------- (A) q / k
   if (worker) {
-    // the conv taps of this thread's q | k channel pair and of its first
-    // head's v channel, requested before the rows' wait (their latency hides
-    // behind it)
+    // the conv taps of this thread's q | k channel pair (and of its first
+    // head's v channel), requested before the rows' wait (their latency
+    // hides behind it)
     const int qkp = 2 * (tid & 127);
     const float* wsrc = p.conv_w + (int64_t)(qkp < D ? cq0 + qkp : ck0 + qkp - D) * kConvK;
     const float4 wqa = ldg_f4_fresh(wsrc), wqb = ldg_f4_fresh(wsrc + kConvK);
-    const float4 wv0 = v_taps(jq * G);
-    ok = workers_sync_and(work_wait(mbar + 1, 0, wlim) && work_wait(mbar + 2, 0, wlim));
+    const float4 wv0 = VIMG ? v_taps(jq * G) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ok = workers_sync_and(work_wait(mbar + 1, 0, wlim) && (!VIMG || work_wait(mbar + 2, 0, wlim)));
     if (ok) { qk_pending = false; v_pending = -1; }
     if (c == 0) {
       fix_history(xq, cq0, tid, kWorkers);
       fix_history(xk, ck0, tid, kWorkers);
-      fix_history(xv, 2 * p.Hqk * D + jq * G * D, tid, kWorkers);
+      if (VIMG) fix_history(xv, 2 * p.Hqk * D + jq * G * D, tid, kWorkers);
       workers_sync();
     }
     // conv + SiLU of the q | k channel pair qkp, qkp + 1, rows [16 rh, +16)
@@ -357,11 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(yrow + i * D) = make_float2(silu_fast(zz.x), silu_fast(zz.y));
       }
     }
-    v_conv(wv0, quarter);
+    if (VIMG) v_conv(wv0, quarter);
     workers_sync();
-    // the first head's v rows are consumed: the next head's rows
-    if (tid == 0 && ok && G > 1) stage_v(1);
-    if (ok && G > 1) v_pending = 1;
+    if (VIMG) {
+      // the first head's v rows are consumed: the next head's rows
+      if (tid == 0 && ok && G > 1) stage_v(1);
+      if (ok && G > 1) v_pending = 1;
+    }
     // L2 norm factors: warp w reduces (row, q | k) pairs w, w+16, ... in a
     // fixed order (the fused kernel's); rows past the end get factor 0
     {
@@ -497,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(3, kThreads);          // the gates; the P region is free
-      // [K^; Q^] (T's work region and v's image) or the head before's K~ and v
-      // have been read out
+      // [K^; Q^] (T's work region and v's image) or the head before's K~ (and
+      // v) have been read out
       if (tid == kMma) {
         if (g == 0) tc::bulk_wait_read();
         else tc::bulk_wait_read_but<1>();
@@ -512,10 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(6, 288);               // the T image region is free
-      named_sync(7, 288);                 // K~ and v are formed
+      named_sync(7, 288);                 // K~ (and v) are formed
       if (tid == kMma) {
         tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
-        tc::bulk_store(ws.v + hv * (kImgV / 4), sm + CkSmem::VS, kImgV);
+        if (VIMG) tc::bulk_store(ws.v + hv * (kImgV / 4), sm + CkSmem::VS, kImgV);
         tc::bulk_commit();
       }
     } else {
@@ -575,8 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
         }
       } else {
-        // the next head's conv taps (their load's latency hides behind K~ and v)
-        const float4 wv = g + 1 < G ? v_taps(h + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // (image mode) the next head's conv taps (their load's latency hides behind K~ and v)
+        const float4 wv = VIMG && g + 1 < G ? v_taps(h + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
         // K^T diag(dec) (row = k channel): the fused kernel's elements and
         // expression, four of its eight-row groups per thread
 #pragma unroll
@@ -591,21 +596,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
           tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
         }
-        // v of channel `row`, rows [32 (tid >> 7), +32) -> its image ([i][r]:
-        // a warp's stores of one row are 128 contiguous bytes), which leaves
-        // by a bulk copy (per-thread global stores of every CTA at once would
-        // back up the load / store pipe that shared-memory loads also use)
-        float* vs = reinterpret_cast<float*>(sm + CkSmem::VS) + 32 * (tid >> 7) * D + row;
+        if (VIMG) {
+          // v of channel `row`, rows [32 (tid >> 7), +32) -> its image ([i][r]:
+          // a warp's stores of one row are 128 contiguous bytes), which leaves
+          // by a bulk copy (per-thread global stores of every CTA at once would
+          // back up the load / store pipe that shared-memory loads also use)
+          float* vs = reinterpret_cast<float*>(sm + CkSmem::VS) + 32 * (tid >> 7) * D + row;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[16];
-          tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
+          for (int hh = 0; hh < 2; ++hh) {
+            float v[16];
+            tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) vs[(16 * hh + e) * D] = v[e];
+            for (int e = 0; e < 16; ++e) vs[(16 * hh + e) * D] = v[e];
+          }
         }
         tc::fence_async_smem();
         named_arrive(7, 288);
-        if (g + 1 < G) {
+        if (VIMG && g + 1 < G) {
           // the next head's v rows (requested after this head's v conv) -> its v conv
           ok = kgrp_sync_and(work_wait(mbar + 2, (uint32_t)((g + 1) & 1), wlim) && ok);
           if (ok) v_pending = -1;
@@ -660,12 +667,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S += U^T (K^T diag(dec))^T and U^T P^T.  Every image of chunk c + 1 is
 // requested as soon as the reader of chunk c's (or c - 1's, for the two
 // buffers of T, P and the gates) is done.
+template <bool VIMG>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws,
-                    const PieceMap pm, int64_t max_chunks) {
-  // omap: the outputs as [rows][Hv * dv] in 64-row tiles (tma_out), or for
-  // the packed core the z columns of the packed rows ([rows][x_ld], 128 x 64
-  // boxes), loaded a chunk ahead into the tile's shared memory
+    tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap,
+                    const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws, const PieceMap pm,
+                    int64_t max_chunks) {
+  // xmap: the pre-conv rows ([rows][x_ld], 128 x 67 boxes), of which the
+  // chain takes its head's v channels; omap: the outputs as [rows][Hv * dv]
+  // in 64-row tiles (tma_out), or for the packed core the z columns of the
+  // packed rows (128 x 64 boxes), loaded a chunk ahead into the tile's shared
+  // memory
   using TOUT = __nv_bfloat16;
   constexpr int D = kD, C = kC;
   const int h = blockIdx.x;
@@ -761,9 +772,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::bulk_load(sm + ChSmem::PB + b * kImgP, ws.pm + hv * kImgP, kImgP, mbar + ChSmem::kPG + b);
     armed[ChSmem::kPG + b] = c;
   };
+  // v of chunk c: its image (image mode), or the head's pre-conv v rows of
+  // chunk c and the three before it (for the first chunk of a sequence those
+  // three are another sequence's or out of range: the conv takes the carried
+  // window or zeros instead)
   auto load_v = [&](int64_t c) {
-    tc::mbar_expect_tx(mbar + ChSmem::kVb, kImgV);
-    tc::bulk_load(sm + ChSmem::VS, ws.v + hv_of(c) * (kImgV / 4), kImgV, mbar + ChSmem::kVb);
+    if (VIMG) {
+      tc::mbar_expect_tx(mbar + ChSmem::kVb, kImgV);
+      tc::bulk_load(sm + ChSmem::XV, ws.v + hv_of(c) * (kImgV / 4), kImgV, mbar + ChSmem::kVb);
+    } else {
+      tc::mbar_expect_tx(mbar + ChSmem::kVb, kXRows * D * 2);
+      tc::tma_load_2d(sm + ChSmem::XV, &xmap, 2 * p.Hqk * D + h * D, (int)(row0 + c * C - kWinRows),
+                      mbar + ChSmem::kVb);
+    }
     armed[ChSmem::kVb] = c;
   };
   auto gates_of = [&](int64_t c) { return reinterpret_cast<const float*>(sm + ChSmem::G + (int)(c & 1) * kImgG); };
@@ -805,10 +826,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // packed core: the outputs of chunk c gated-normalised as the fused kernel
-  // does it (a token's 128 outputs meet in shared memory, the v image's
-  // region, free once R has read it; warp w then takes tokens w, w + 16, ...:
+  // does it (a token's 128 outputs meet in shared memory, v's region, free
+  // once R or the conv has read it: all 64 tokens in the image mode, 32 at a
+  // time in the rows' smaller region; warp w then takes tokens w, w + 16, ...:
   // RMS over dv, the norm scale, the silu(z) gate from the packed row).  Every
-  // worker calls it (two worker barriers).
+  // worker calls it (two or four worker barriers).
   const bool core = p.norm_w != nullptr;
   auto load_z = [&](int64_t c) {
     tc::mbar_expect_tx(mbar + ChSmem::kZ, 16384);
@@ -819,32 +841,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* gam = gates_of(c) + 64;
     float up[16];
     tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, up);
-    float* of = reinterpret_cast<float*>(sm + ChSmem::VS);
+    // the tokens' outputs, all 64 at once (image mode: the 32 KB region) or
+    // 32 at a time (the rows' region)
+    constexpr int kTok = VIMG ? 64 : 32;
+    float* of = reinterpret_cast<float*>(sm + ChSmem::XV);
     okc = work_wait(mbar + ChSmem::kZ, (uint32_t)((c - cb) & 1), wlim) && okc;   // the z rows
-    workers_sync();   // every worker's R has read v
-#pragma unroll
-    for (int e = 0; e < 16; ++e) of[(16 * quarter + e) * D + row] = fmaf(gam[16 * quarter + e], sq[e], up[e]);
-    workers_sync();
     const int64_t t0 = c * C;
     const int cnt = (int)(n - t0 < C ? n - t0 : C);
     const int lane = tid & 31;
     const __nv_bfloat16* zs = ot;
     const float* nw = reinterpret_cast<const float*>(sm + ChSmem::NW);
     TOUT* orow = reinterpret_cast<TOUT*>(p.o) + ((row0 + t0) * p.Hv + h) * D;
-    for (int i = warp; i < cnt; i += kWorkers / 32) {
-      float v[4];
-      float ss = 0.f;
+#pragma unroll 1
+    for (int hf = 0; hf < 64 / kTok; ++hf) {
+      workers_sync();   // every worker has read v (R, the conv); the tokens before are done
+      if ((16 * quarter) / kTok == hf) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        v[m] = of[i * D + lane + 32 * m];
-        ss = fmaf(v[m], v[m], ss);
+        for (int e = 0; e < 16; ++e)
+          of[(16 * quarter - kTok * hf + e) * D + row] = fmaf(gam[16 * quarter + e], sq[e], up[e]);
       }
-      ss = warp_sum(ss);
-      const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
+      workers_sync();
+      const int iend = cnt < kTok * hf + kTok ? cnt : kTok * hf + kTok;
+      for (int i = kTok * hf + warp; i < iend; i += kWorkers / 32) {
+        const float* orw = of + (i - kTok * hf) * D;
+        float v[4];
+        float ss = 0.f;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float z = to_f32(zs[i * D + lane + 32 * m]);
-        orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nw[lane + 32 * m] * silu_fast(z));
+        for (int m = 0; m < 4; ++m) {
+          v[m] = orw[lane + 32 * m];
+          ss = fmaf(v[m], v[m], ss);
+        }
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float z = to_f32(zs[i * D + lane + 32 * m]);
+          orow[(int64_t)i * p.Hv * D + lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nw[lane + 32 * m] * silu_fast(z));
+        }
       }
     }
   };
@@ -866,6 +899,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_t(cb);
     load_kt(cb);
   }
+  // the conv taps of this worker's v channel (state row `row`)
+  const float* vtaps = p.conv_w + (int64_t)(2 * p.Hqk * D + h * D + row) * kConvK;
   if (worker) {
     // initial state (zeros on a cold start: the pool is not read)
     const float* src = from >= 0 ? page_state(p.pool, from) + ((int64_t)h * D + row) * D + 32 * quarter : nullptr;
@@ -923,25 +958,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (c + 1 < ce) load_t(c + 1);
     }
     if (worker) {
-      // ---- (2) gam_C S0 into the state's columns, which the state update
-      // accumulates onto (S0 [K^; Q^]^T reads only the hi / lo split); the
-      // previous chunk's outputs (its U^T P^T is done), then R_i =
-      // b_i (v_i - gam_i (S0 k^_i)) of state row `row`, rows [16 quarter, +16),
-      // into the tensor-memory operand
+      // ---- (2) the previous chunk's outputs (its U^T P^T is done); v by the
+      // conv, while S0 [K^; Q^]^T runs; then R_i = b_i (v_i - gam_i (S0 k^_i))
+      // of state row `row`, rows [16 quarter, +16), into the tensor-memory
+      // operand
+      const float4 wv = VIMG ? make_float4(0.f, 0.f, 0.f, 0.f) : ldg_f4_fresh(vtaps);
       ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
-      {
-        const float gC = gates_of(c)[64 + C - 1];
-        float v0[32];
-        tc::tmem_ld32(tS, v0);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
-          v0[e] = gg.x;
-          v0[e + 1] = gg.y;
-        }
-        tc::tmem_st32(tS, v0);
-        tc::tmem_st_wait();
-      }
       if (c > cb && !core) {
         mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
         outputs(c - 1, sq);
@@ -952,10 +974,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* gam = gs + 64;
       const float* bv = gs + 192;
       const int i0 = 16 * quarter;
-      const float* vs = reinterpret_cast<const float*>(sm + ChSmem::VS) + i0 * D + row;
-      float vv[16];   // this row's v values, read before the product's wait
+      // v of channel `row`, rows [16 quarter, +16): from its image, or the
+      // conv + SiLU of the pre-conv rows in the chunk kernel's expression
+      // (rows i and i + 8 as one packed pair), while S0 [K^; Q^]^T runs
+      float vv[16];
+      if (VIMG) {
+        const float* vs = reinterpret_cast<const float*>(sm + ChSmem::XV) + i0 * D + row;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) vv[e] = vs[e * D];
+        for (int e = 0; e < 16; ++e) vv[e] = vs[e * D];
+      } else {
+        const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(sm + ChSmem::XV) + i0 * D + row;
+        float xr[19];
+#pragma unroll
+        for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[u * D]);
+        if (c == 0 && quarter == 0) {
+          // rows before the sequence: the carried window, or zeros
+          const __nv_bfloat16* wr = V.win ? V.win + 2 * p.Hqk * D + h * D + row : nullptr;
+#pragma unroll
+          for (int u = 0; u < kWinRows; ++u) xr[u] = wr ? to_f32(wr[(int64_t)u * p.conv_dim]) : 0.f;
+        }
+        const f32x2 w0 = pack2(wv.x, wv.x), w1 = pack2(wv.y, wv.y), w2 = pack2(wv.z, wv.z), w3 = pack2(wv.w, wv.w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          f32x2 z = mul2(w0, pack2(xr[i], xr[i + 8]));
+          z = fma2(w1, pack2(xr[i + 1], xr[i + 9]), z);
+          z = fma2(w2, pack2(xr[i + 2], xr[i + 10]), z);
+          z = fma2(w3, pack2(xr[i + 3], xr[i + 11]), z);
+          const float2 zz = unpack2(z);
+          vv[i] = silu_fast(zz.x);
+          vv[i + 8] = silu_fast(zz.y);
+        }
+      }
       mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
       float a[16];
       if (core) tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
@@ -987,7 +1036,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (off the issuing thread's path, which goes on to R T^T) the previous
       // chunk's output tile; the next chunk's gates and P (their buffer's last
       // readers, the outputs and U^T P^T of chunk c - 1, are done), [K^; Q^]
-      // (S0 [K^; Q^]^T is done) and v (R has read it)
+      // (S0 [K^; Q^]^T is done) and the v rows (the conv has read them; the
+      // packed core's outputs have left their region)
       if (c > cb && tma_out && full_chunk(c - 1)) {
         tc::tma_store_2d(&omap, h * D, (int)(row0 + (c - 1) * C), ot);
         tc::bulk_commit();
@@ -1002,7 +1052,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (worker) {
-      // ---- (3) U (rows r, K = i) into the operand of the state update and U^T P^T
+      // ---- (3) gam_C S0 into the state's columns, which the state update
+      // accumulates onto (S0 [K^; Q^]^T read only the hi / lo split), while
+      // R T^T runs; then U (rows r, K = i) into the operand of the state
+      // update and U^T P^T
+      {
+        const float gC = gates_of(c)[64 + C - 1];
+        float v0[32];
+        tc::tmem_ld32(tS, v0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 gg = unpack2(mul2(pack2(v0[e], v0[e + 1]), pack2(gC, gC)));
+          v0[e] = gg.x;
+          v0[e + 1] = gg.y;
+        }
+        tc::tmem_st32(tS, v0);
+        tc::tmem_st_wait();
+      }
       mma_wait(mbar + ChSmem::kU, par, ok, wlim);
       float u[16];
       tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, u);
@@ -1088,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================================
 size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
   const int64_t slots = total_tokens / kC + num_seqs + 1;
-  const int64_t per_v = (int64_t)kImgT + kImgP + kImgK + kImgV + kImgG;
+  const int64_t per_v = (int64_t)kImgT + kImgP + kImgK + kImgG + kImgV;
   const int64_t per_q = (int64_t)kImgKQ;
   return (size_t)(slots * (Hv * per_v + Hqk * per_q)) + 1024;
 }
@@ -1251,6 +1317,15 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   if (maxc > 65535) return cudaErrorInvalidValue;
   auto encode = tensor_map_encoder();
   if (p.total_rows > 0 && !encode) return cudaErrorNotSupported;
+  const PrefillSchedule sc = tc_chain_schedule(p.Hqk, p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
+  // With overlapped levels the chain is the call's critical path: the chunk
+  // kernel convolves v and writes its image.  Otherwise the chain convolves v
+  // from the rows itself (same arithmetic, same bits), which takes the
+  // chunk kernel's largest task and 64 KB a chunk and head of image traffic
+  // off the call.
+  const bool vimg = sc.chunk_launches > 1;
+  auto chunk_k = vimg ? tc_chunk_kernel<true> : tc_chunk_kernel<false>;
+  auto chain_k = vimg ? tc_chain_kernel<true> : tc_chain_kernel<false>;
   CUtensorMap xmap;
   memset(&xmap, 0, sizeof(xmap));
   const bool chunks = maxc > 0 && p.total_rows > 0;
@@ -1263,14 +1338,13 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CkSmem::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(chunk_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CkSmem::ALLOC);
     if (e != cudaSuccess) return e;
   }
   // the chunk kernel over chunks [c0, c0 + cnt) of every sequence
   auto chunk_launch = [&](int64_t c0, int64_t cnt, cudaStream_t s) {
     if (!chunks || cnt <= 0) return cudaSuccess;
-    tc_chunk_kernel<<<dim3(p.Hqk, (unsigned)cnt, p.num_seqs), kThreads, CkSmem::ALLOC, s>>>(p, xmap, ws, c0);
+    chunk_k<<<dim3(p.Hqk, (unsigned)cnt, p.num_seqs), kThreads, CkSmem::ALLOC, s>>>(p, xmap, ws, c0);
     return cudaGetLastError();
   };
   // o as [rows][Hv * dv] bf16; a box is one head's 128 channels x 64 rows
@@ -1298,10 +1372,8 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       tma_out = 1;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)ChSmem::ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(chain_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChSmem::ALLOC);
   if (e != cudaSuccess) return e;
-  const PrefillSchedule sc = tc_chain_schedule(p.Hqk, p.Hv, p.num_seqs, max_len, tc_prefill_sm_count());
   PieceMap pm;
   pm.nseqs = p.num_seqs;
   pm.piece = (int32_t)sc.piece;
@@ -1309,7 +1381,7 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   auto chain_launch = [&](int64_t level0, int32_t s0, int64_t cnt, cudaStream_t s) {
     pm.s0 = s0;
     pm.level0 = (int32_t)level0;
-    tc_chain_kernel<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, s>>>(p, omap, tma_out, ws, pm, maxc);
+    chain_k<<<dim3(p.Hv, (unsigned)cnt), kThreads, ChSmem::ALLOC, s>>>(p, xmap, omap, tma_out, ws, pm, maxc);
     return cudaGetLastError();
   };
   if (sc.chunk_launches > 1) {

@@ -84,7 +84,9 @@ def test_pool_too_small_or_misaligned_is_rejected():
 def test_workspace_is_required_and_sized():
     # the tensor-core prefill (d 128, bf16, block a multiple of 64): the chunk
     # kernel's images for floor(T / 64) + N + 1 chunk slots, per slot T, P,
-    # K^T diag(dec), v and the gates of every value head and [K^; Q^] of every qk head
+    # K^T diag(dec), v and the gates of every value head and [K^; Q^] of every
+    # qk head (v's image is written only when the chain's levels overlap the
+    # chunk kernel; the workspace holds it for every call)
     for sh in (inputs.QWEN27B, inputs.QWEN4B):
         per_slot = sh.num_v_heads * (16384 + 16384 + 32768 + 32768 + 1024) + sh.num_qk_heads * 65536
         for N, T in ((4, 4 * 8192), (1, 229376), (3, 1000), (1, 0)):
