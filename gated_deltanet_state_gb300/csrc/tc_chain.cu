@@ -16,23 +16,26 @@
 // tc_chunk_kernel: one CTA per (sequence, chunk, qk head).  The conv + SiLU of
 //   the q and k channels, their norms, the operand [K^; Q^] and the Gram
 //   products [K^ K^T; Q^ K^T] run once for the qk head's group of value heads;
-//   then per value head the gates, A, P, T, the v conv and K^T diag(dec).  It
-//   leaves, per chunk slot of the workspace, the fused kernel's own operand
-//   images: [K^; Q^] per qk head; T, P and K^T diag(dec) (bf16 hi / lo,
-//   128-byte swizzled), v (fp32) and the gates per value head.  No chunk waits
-//   for another, so the whole call's chunks fill every SM.
+//   then per value head the gates, A, P, T and K^T diag(dec).  It leaves, per
+//   chunk slot of the workspace, the fused kernel's own operand images:
+//   [K^; Q^] per qk head; T, P and K^T diag(dec) (bf16 hi / lo, 128-byte
+//   swizzled) and the gates per value head.  No chunk waits for another, so
+//   the whole call's chunks fill every SM.
 // tc_chain_kernel: one CTA per (sequence, value head) chain, or a piece of
 //   one: a chain's chunks run in order, and a call cut into pieces passes the
 //   state between launches through the final page, exactly.  The fp32 state
 //   stays in tensor memory; per chunk, the fused kernel's state steps:
 //   S0 [K^; Q^]^T, R, U^T = R T^T, then S += U^T (K^T diag(dec))^T and U^T P^T,
-//   and the outputs.  The next chunk's images load by bulk copies as soon as
-//   their readers are done.
+//   and the outputs.  v comes from the conv + SiLU of the pre-conv rows, in
+//   the fused kernel's expression, while the first product runs.  The next
+//   chunk's images and rows load as soon as their readers are done.
 // With no more chains than SMs the two kernels overlap: the chains are cut
 // into levels, and level l of every chain runs on a second stream once the
 // chunk kernel's launch l has written that level's images, while launch
 // l + 1 takes the SMs the chains leave (tc_chain_schedule picks the level
-// length, or none, from a cost model of both paths).
+// length, or none, from a cost model of both paths).  The chain is then the
+// call's critical path, so in this mode (VIMG) the chunk kernel convolves v
+// and writes it as an fp32 image instead.
 // Every operand is split and every product issued exactly as in the fused
 // kernel (the same bf16 hi / lo parts, the same M x N x K shapes and passes in
 // the same order), so the two paths give the same bits and a call may take
