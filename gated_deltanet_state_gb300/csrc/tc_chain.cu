@@ -107,6 +107,13 @@ struct CkSmem {
   static constexpr uint32_t GT = KQ + 65536;         // gate sets [4][4][64] fp32 (G, gam, dec, b), then rq, rk
   static constexpr uint32_t AT = GT + 4096 + 512;    // A^T fp32 [64 j][64 i]
   static constexpr uint32_t AM = AT + 16384;         // A fp32 row-major, slots swizzled
+  // (B, conv mode) a second A^T / A / P set: the K group forms the next
+  // value head's while the T group inverts this one's (regions the image
+  // mode uses for v)
+  static constexpr uint32_t AT1 = KQ;
+  static constexpr uint32_t AM1 = KQ + 16384;
+  static constexpr uint32_t PB1 = XV;
+  static constexpr uint32_t PB1_LO = XV + 8192;
   static constexpr uint32_t MBAR = AM + 16384;       // [0] Gram [1] q / k rows [2] v rows (image mode)
   static constexpr uint32_t TSLOT = MBAR + 24;
   static constexpr uint32_t BYTES = TSLOT + 8;
@@ -480,18 +487,169 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (ok) gram_pending = true;
 
   // ---------------------------------------------------------- (B) value heads
+  const bool kgrp = tid < 256;
+  // A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j) of one value
+  // head, columns j in [16 cb, +16) of this warp's Gram lanes, into A^T / A /
+  // P set `set` (the second set: conv mode only)
+  auto form_ap = [&](int cb, const float* Gs, int set) {
+    float* atp = reinterpret_cast<float*>(sm + (set ? CkSmem::AT1 : CkSmem::AT));
+    float* amp = reinterpret_cast<float*>(sm + (set ? CkSmem::AM1 : CkSmem::AM));
+    const uint32_t pb = set ? CkSmem::PB1 : CkSmem::PB;
+    const float* bv = Gs + 192;
+    const int q4 = warp & 3;
+    const int ir = (q4 & 1) * 32 + lane;
+    float ap[16];
+    tc::tmem_ld16(tbase + tlane + kCkGram + 16 * cb, ap);
+    const float Gi = Gs[ir];
+    const float bi = q4 < 2 ? bv[ir] : 1.0f;
+    const int lim = q4 < 2 ? ir : ir + 1;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int j = 16 * cb + e;
+      const float m = j < lim ? bi : 0.f;
+      ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
+    }
+    if (q4 < 2) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) atp[(16 * cb + e) * C + ir] = ap[e];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        *reinterpret_cast<float4*>(amp + am_index(ir, 16 * cb + 4 * c4)) =
+            make_float4(ap[4 * c4], ap[4 * c4 + 1], ap[4 * c4 + 2], ap[4 * c4 + 3]);
+    } else {
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const uint32_t off = tc::sw128_offset(ir, 16 * cb + 8 * c8, 64);
+        tc::store_split8(sm + pb + off, sm + pb + 8192 + off, ap + 8 * c8);
+      }
+    }
+  };
+  // K^T diag(dec) (row = k channel) into the KT region: the fused kernel's
+  // elements and expression, four of its eight-row groups per K-group thread
+  auto form_kt = [&](const float* dec) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int i = tid + 256 * it, k = i & 127, j8 = i >> 7;
+      float kt[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = 8 * j8 + u;
+        kt[u] = (yk[j * D + k] * rk[j]) * dec[j];
+      }
+      const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
+      tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
+    }
+  };
+  // T = (I + A)^{-1} by the T group, then (its region free) T as the B
+  // operand (rows i, K = j; zero above the diagonal)
+  auto form_t = [&](int set) {
+    const float* atp = reinterpret_cast<const float*>(sm + (set ? CkSmem::AT1 : CkSmem::AT));
+    const float* amp = reinterpret_cast<const float*>(sm + (set ? CkSmem::AM1 : CkSmem::AM));
+    tri_inverse64(atp, amp, tf, reinterpret_cast<float*>(sm + CkSmem::DT), reinterpret_cast<float*>(sm + CkSmem::NT),
+                  tid - 256);
+    named_sync(6, 288);
+    for (int e = tid - 256; e < 512; e += 256) {
+      const int i = e >> 3, c8 = e & 7;
+      const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
+      const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
+      float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (8 * c8 + u > i) v8[u] = 0.f;
+      const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
+      tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
+    }
+  };
+  int g = 0;
+  if (!VIMG) {
+    // ------------------------------------------------------------ conv mode
+    // A and P of head 0 by every worker; then, head by head, the T group
+    // inverts head g's A while the K group forms head g's K~ and head g + 1's
+    // A and P (into the other A^T / A / P set).  The issuing warp stores P
+    // at the head's start, K~ when the K group has formed it, T and the gates
+    // at its end.
+    for (; ok && g < G; ++g) {
+      const int h = jq * G + g;
+      const int b = g & 1;
+      float* const Gs = gbuf + 256 * (g % kGateSets);
+      const int64_t hv = slot * p.Hv + h;
+      if (!worker) {
+        if (g == 0) {
+          __syncwarp();
+          named_arrive(3, kThreads);        // (the gates of the first heads were formed during the conv)
+          if (tid == kMma) tc::bulk_wait_read();   // [K^; Q^] (T's work region, the second A set) read out
+          __syncwarp();
+          named_sync(5, kThreads);          // head 0's A and P are formed
+        }
+        if (tid == kMma) {
+          tc::bulk_store(ws.pm + hv * kImgP, sm + (b ? CkSmem::PB1 : CkSmem::PB), kImgP);
+          tc::bulk_commit();
+          // all but this P: the head before's K~, T and gates, and the P before
+          if (g > 0) tc::bulk_wait_read_but<1>();
+        }
+        __syncwarp();
+        named_arrive(6, 288);               // the T image region is free
+        if (g > 0) named_arrive(9, 288);    // the K~ region is free
+        if (g + 1 < G) {
+          if (g + 1 >= kGateSets) {
+            // the set was last stored by head g + 1 - kGateSets
+            if (tid == kMma) tc::bulk_wait_read();
+            __syncwarp();
+            chunk_gates(V, t0, n, h + 1, lane, gbuf + 256 * ((g + 1) % kGateSets));
+            tc::fence_async_smem();
+          }
+          __syncwarp();
+          named_arrive(8, 288);             // the next head's gates; its P region is free
+        }
+        named_sync(7, 288);                 // K~ is formed
+        if (tid == kMma) {
+          tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
+          tc::bulk_commit();
+        }
+      } else {
+        if (g == 0) {
+          named_sync(3, kThreads);
+          mma_wait(mbar + 0, 0, ok, wlim);
+          if (ok) gram_pending = false;
+          form_ap(quarter, Gs, 0);
+          tc::fence_async_smem();
+          named_sync(5, kThreads);
+        }
+        if (!kgrp) {
+          form_t(b);
+        } else {
+          if (g > 0) named_sync(9, 288);
+          form_kt(Gs + 128);
+          tc::fence_async_smem();
+          named_arrive(7, 288);
+          if (g + 1 < G) {
+            named_sync(8, 288);
+            const float* Gn = gbuf + 256 * ((g + 1) % kGateSets);
+#pragma unroll 1
+            for (int cb = quarter; cb < 4; cb += 2) form_ap(cb, Gn, b ^ 1);
+          }
+        }
+        tc::fence_async_smem();
+      }
+      ok = cta_sync_ok(ok);
+      if (!ok) break;
+      if (tid == kMma) {
+        tc::bulk_store(ws.t + hv * kImgT, sm + CkSmem::TB, kImgT);
+        tc::bulk_store(ws.g + hv * (kImgG / 4), Gs, kImgG);
+        tc::bulk_commit();
+      }
+    }
+  }
+  // ----------------------------------------------------------- image mode
   // After A and P, threads 0-255 (the K group) form K^T diag(dec) and v, then
   // the next head's v conv; threads 256-511 (the T group) form T.  The issuing
-  // warp stores each image once it is complete: P after A and P, K~ when the K
-  // group is done, T and the gates at the head's end, and waits for a store
-  // to have left shared memory only before that region is written again.
-  const bool kgrp = tid < 256;
-  int g = 0;
-  for (; ok && g < G; ++g) {
+  // warp stores each image once it is complete: P after A and P, K~ and v
+  // when the K group is done, T and the gates at the head's end, and waits
+  // for a store to have left shared memory only before that region is
+  // written again.
+  for (; VIMG && ok && g < G; ++g) {
     const int h = jq * G + g;
     float* const Gs = gbuf + 256 * (g % kGateSets);
-    const float* dec = Gs + 128;
-    const float* bv = Gs + 192;
     const int64_t hv = slot * p.Hv + h;
     if (!worker) {
       if (g >= kGateSets) {
@@ -505,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(3, kThreads);          // the gates; the P region is free
-      // [K^; Q^] (T's work region and v's image) or the head before's K~ (and
-      // v) have been read out
+      // [K^; Q^] (T's work region and v's image) or the head before's K~ and
+      // v have been read out
       if (tid == kMma) {
         if (g == 0) tc::bulk_wait_read();
         else tc::bulk_wait_read_but<1>();
@@ -520,10 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       named_arrive(6, 288);               // the T image region is free
-      named_sync(7, 288);                 // K~ (and v) are formed
+      named_sync(7, 288);                 // K~ and v are formed
       if (tid == kMma) {
         tc::bulk_store(ws.k + hv * kImgK, sm + CkSmem::KT, kImgK);
-        if (VIMG) tc::bulk_store(ws.v + hv * (kImgV / 4), sm + CkSmem::VS, kImgV);
+        tc::bulk_store(ws.v + hv * (kImgV / 4), sm + CkSmem::VS, kImgV);
         tc::bulk_commit();
       }
     } else {
@@ -532,90 +690,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_wait(mbar + 0, 0, ok, wlim);
         if (ok) gram_pending = false;
       }
-      // A^T (lanes 0-63: k^_i.k^_j) and P (lanes 64-127: q^_i.k^_j), columns j in [16 quarter, +16)
-      {
-        const int q4 = warp & 3;
-        const int ir = (q4 & 1) * 32 + lane;
-        float ap[16];
-        tc::tmem_ld16(tbase + tlane + kCkGram + 16 * quarter, ap);
-        const float Gi = Gs[ir];
-        const float bi = q4 < 2 ? bv[ir] : 1.0f;
-        const int lim = q4 < 2 ? ir : ir + 1;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = 16 * quarter + e;
-          const float m = j < lim ? bi : 0.f;
-          ap[e] = m * __expf(fminf(Gi - Gs[j], 0.f)) * ap[e];
-        }
-        if (q4 < 2) {
-          float* am = reinterpret_cast<float*>(sm + CkSmem::AM);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) at[(16 * quarter + e) * C + ir] = ap[e];
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<float4*>(am + am_index(ir, 16 * quarter + 4 * c4)) =
-                make_float4(ap[4 * c4], ap[4 * c4 + 1], ap[4 * c4 + 2], ap[4 * c4 + 3]);
-        } else {
-#pragma unroll
-          for (int c8 = 0; c8 < 2; ++c8) {
-            const uint32_t off = tc::sw128_offset(ir, 16 * quarter + 8 * c8, 64);
-            tc::store_split8(sm + CkSmem::PB + off, sm + CkSmem::PB_LO + off, ap + 8 * c8);
-          }
-        }
-      }
+      form_ap(quarter, Gs, 0);
       tc::fence_async_smem();
       named_sync(5, kThreads);
       if (!kgrp) {
-        // T = (I + A)^{-1}, then T as the B operand (rows i, K = j; zero above the diagonal)
-        tri_inverse64(at, reinterpret_cast<const float*>(sm + CkSmem::AM), tf,
-                      reinterpret_cast<float*>(sm + CkSmem::DT), reinterpret_cast<float*>(sm + CkSmem::NT),
-                      tid - 256);
-        named_sync(6, 288);
-        for (int e = tid - 256; e < 512; e += 256) {
-          const int i = e >> 3, c8 = e & 7;
-          const float4 a = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8);
-          const float4 b = *reinterpret_cast<const float4*>(tf + i * C + 8 * c8 + 4);
-          float v8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (8 * c8 + u > i) v8[u] = 0.f;
-          const uint32_t off = tc::sw128_offset(i, 8 * c8, 64);
-          tc::store_split8(sm + CkSmem::TB + off, sm + CkSmem::TB_LO + off, v8);
-        }
+        form_t(0);
       } else {
-        // (image mode) the next head's conv taps (their load's latency hides behind K~ and v)
-        const float4 wv = VIMG && g + 1 < G ? v_taps(h + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-        // K^T diag(dec) (row = k channel): the fused kernel's elements and
-        // expression, four of its eight-row groups per thread
+        // the next head's conv taps (their load's latency hides behind K~ and v)
+        const float4 wv = g + 1 < G ? v_taps(h + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        form_kt(Gs + 128);
+        // v of channel `row`, rows [32 (tid >> 7), +32) -> its image ([i][r]:
+        // a warp's stores of one row are 128 contiguous bytes), which leaves
+        // by a bulk copy (per-thread global stores of every CTA at once would
+        // back up the load / store pipe that shared-memory loads also use)
+        float* vs = reinterpret_cast<float*>(sm + CkSmem::VS) + 32 * (tid >> 7) * D + row;
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int i = tid + 256 * it, k = i & 127, j8 = i >> 7;
-          float kt[8];
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[16];
+          tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = 8 * j8 + u;
-            kt[u] = (yk[j * D + k] * rk[j]) * dec[j];
-          }
-          const uint32_t off = tc::sw128_offset(k, 8 * j8, 128);
-          tc::store_split8(sm + CkSmem::KT + off, sm + CkSmem::KT_LO + off, kt);
-        }
-        if (VIMG) {
-          // v of channel `row`, rows [32 (tid >> 7), +32) -> its image ([i][r]:
-          // a warp's stores of one row are 128 contiguous bytes), which leaves
-          // by a bulk copy (per-thread global stores of every CTA at once would
-          // back up the load / store pipe that shared-memory loads also use)
-          float* vs = reinterpret_cast<float*>(sm + CkSmem::VS) + 32 * (tid >> 7) * D + row;
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float v[16];
-            tc::tmem_ld16(tbase + tlane + kCkV + 32 * (tid >> 7) + 16 * hh, v);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) vs[(16 * hh + e) * D] = v[e];
-          }
+          for (int e = 0; e < 16; ++e) vs[(16 * hh + e) * D] = v[e];
         }
         tc::fence_async_smem();
         named_arrive(7, 288);
-        if (VIMG && g + 1 < G) {
+        if (g + 1 < G) {
           // the next head's v rows (requested after this head's v conv) -> its v conv
           ok = kgrp_sync_and(work_wait(mbar + 2, (uint32_t)((g + 1) & 1), wlim) && ok);
           if (ok) v_pending = -1;
