@@ -1085,25 +1085,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) vv[e] = vs[e * D];
       } else {
         const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(sm + ChSmem::XV) + i0 * D + row;
-        float xr[19];
-#pragma unroll
-        for (int u = 0; u < 19; ++u) xr[u] = to_f32(xv[u * D]);
-        if (c == 0 && quarter == 0) {
-          // rows before the sequence: the carried window, or zeros
-          const __nv_bfloat16* wr = V.win ? V.win + 2 * p.Hqk * D + h * D + row : nullptr;
-#pragma unroll
-          for (int u = 0; u < kWinRows; ++u) xr[u] = wr ? to_f32(wr[(int64_t)u * p.conv_dim]) : 0.f;
-        }
+        // row u of the 19 this thread convolves (a sequence's first three:
+        // the carried window, or zeros); a sliding window of four rows for
+        // each of the pair's outputs keeps few registers live
+        const bool hist = c == 0 && quarter == 0;
+        const __nv_bfloat16* wr = hist && V.win ? V.win + 2 * p.Hqk * D + h * D + row : nullptr;
+        auto xrow = [&](int u) -> float {
+          if (u < kWinRows && hist) return wr ? to_f32(wr[(int64_t)u * p.conv_dim]) : 0.f;
+          return to_f32(xv[u * D]);
+        };
         const f32x2 w0 = pack2(wv.x, wv.x), w1 = pack2(wv.y, wv.y), w2 = pack2(wv.z, wv.z), w3 = pack2(wv.w, wv.w);
+        float a0 = xrow(0), a1 = xrow(1), a2 = xrow(2), b0 = xrow(8), b1 = xrow(9), b2 = xrow(10);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          f32x2 z = mul2(w0, pack2(xr[i], xr[i + 8]));
-          z = fma2(w1, pack2(xr[i + 1], xr[i + 9]), z);
-          z = fma2(w2, pack2(xr[i + 2], xr[i + 10]), z);
-          z = fma2(w3, pack2(xr[i + 3], xr[i + 11]), z);
+          const float a3 = xrow(i + 3), b3 = xrow(i + 11);
+          f32x2 z = mul2(w0, pack2(a0, b0));
+          z = fma2(w1, pack2(a1, b1), z);
+          z = fma2(w2, pack2(a2, b2), z);
+          z = fma2(w3, pack2(a3, b3), z);
           const float2 zz = unpack2(z);
           vv[i] = silu_fast(zz.x);
           vv[i + 8] = silu_fast(zz.y);
+          a0 = a1; a1 = a2; a2 = a3;
+          b0 = b1; b1 = b2; b2 = b3;
         }
       }
       mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
