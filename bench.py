@@ -852,11 +852,12 @@ def main():
     # end to end through the same call with host buffers (prefill part):
     # every step copies its inputs in and its outputs out; the copies of
     # neighbouring steps overlap the prefill on their own streams
-    # (at least 16 steps: the timed region also fills and drains the pipeline
-    # once).  Three trials, the median reported and every trial listed: now
-    # and then a whole trial runs far below the host link's rate while the
-    # link, measured alone in the same process, runs at its full rate.
-    e2e_steps = max(args.steps, 16)
+    # (at least 32 steps: the timed region also fills and drains the pipeline
+    # once, about one prefill and one output copy beyond the steps' copies).
+    # Three trials, the median reported and every trial listed: now and then
+    # a whole trial runs far below the host link's rate while the link,
+    # measured alone in the same process, runs at its full rate.
+    e2e_steps = max(args.steps, 32)
     e2e_trials = [pre.e2e_pipelined_ms(e2e_steps) for _ in range(3)]
     e2e_ms = statistics.median(e2e_trials)
     link = pre.link_gbs()
