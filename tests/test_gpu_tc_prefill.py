@@ -235,6 +235,37 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
     assert torch.equal(pool_f, pool_2)
 
 
+@pytest.mark.parametrize("case", ["serial", "overlap"])
+def test_six_value_heads_a_group_two_kernels(case):
+    """Six value heads to a qk head: the chunk kernel forms the gates of its
+    first four heads during the conv and the later ones inside the head loop
+    (both modes: v convolved in the chain, serial here; v's image, overlapped
+    levels).  The two kernels give the fused kernel's bits, and the serial
+    case matches the oracle."""
+    if case == "serial":
+        sh = inputs.LayerShape(1, 6, 128, 128, block_size=128, chunk_size=64)
+        lens = [700, 129, 1, 300]
+        plan = gdn.gdn_prefill_plan_for(sh, len(lens), max(lens), 0, gdn.PREFILL_TWO_KERNELS)
+        assert plan["chunk_launches"] == 1
+        bt, npages = _tables(lens, 128, len(lens))
+        res = _both_paths(sh, lens, [0] * len(lens), [-1] * len(lens), bt, 87, npages)
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        ti = inputs.token_inputs(sh, int(cu[-1]), seed=87)
+        ref = oracle.prefill(dims(sh), cu, [0] * len(lens), 128, ti["x"], ti["g"], ti["beta"],
+                             inputs.conv_weights(sh, 87))
+        assert_out_close(res[1][0], ref["o"], cu)
+    else:
+        sh = inputs.LayerShape(8, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
+        lens = [4133]
+        plan = gdn.gdn_prefill_plan_for(sh, 1, max(lens), 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+        res = _both_paths(sh, lens, [0], [-1], [[1, 2, 3, 4]], 88, 5, max_seq_len=max(lens))
+    (o_f, pool_f), (o_2, pool_2) = res
+    assert torch.equal(o_f.view(torch.int16), o_2.view(torch.int16))
+    assert torch.equal(pool_f, pool_2)
+
+
 def test_overlapped_levels_resume_bitwise():
     """A long sequence on the two kernels' overlapped levels, then the same
     sequence resumed from its second checkpoint (a shorter call, its own
