@@ -112,8 +112,7 @@ struct CkSmem {
   // mode uses for v)
   static constexpr uint32_t AT1 = KQ;
   static constexpr uint32_t AM1 = KQ + 16384;
-  static constexpr uint32_t PB1 = XV;
-  static constexpr uint32_t PB1_LO = XV + 8192;
+  static constexpr uint32_t PB1 = XV;               //     (P hi, lo at +8 KB)
   static constexpr uint32_t MBAR = AM + 16384;       // [0] Gram [1] q / k rows [2] v rows (image mode)
   static constexpr uint32_t TSLOT = MBAR + 24;
   static constexpr uint32_t BYTES = TSLOT + 8;
@@ -264,7 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* gbuf = reinterpret_cast<float*>(sm + CkSmem::GT);
   float* rq = gbuf + 256 * kGateSets;
   float* rk = rq + 64;
-  float* at = reinterpret_cast<float*>(sm + CkSmem::AT);
   float* tf = reinterpret_cast<float*>(sm + CkSmem::TF);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + CkSmem::MBAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CkSmem::TSLOT);
