@@ -276,7 +276,9 @@ enum { GDN_PREFILL_AUTO = 0, GDN_PREFILL_FUSED = 1, GDN_PREFILL_TWO_KERNELS = 2 
  * everything that does not depend on the state (conv, norms, the chunk's
  * triangular solve and the products that fold it in) and leaves them here as
  * the fused kernel's own operand images (about 97 KB per chunk and value
- * head plus 64 KB per chunk and qk head); a chain kernel then carries each
+ * head plus 64 KB per chunk and qk head; the 32 KB of v in that is written
+ * only when the chains' levels overlap the chunk kernel, otherwise the chain
+ * convolves v from the rows itself); a chain kernel then carries each
  * (sequence, value head) state through its chunks with the fused kernel's
  * state products.  The other path is one fused kernel that runs a chain's
  * chunks one after another on one SM and needs no scratch.  Both split and
