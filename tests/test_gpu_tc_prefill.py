@@ -235,15 +235,17 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
     assert torch.equal(pool_f, pool_2)
 
 
-@pytest.mark.parametrize("case", ["serial", "overlap"])
+@pytest.mark.parametrize("case", ["serial", "overlap", "one_per_group"])
 def test_six_value_heads_a_group_two_kernels(case):
     """Six value heads to a qk head: the chunk kernel forms the gates of its
     first four heads during the conv and the later ones inside the head loop
     (both modes: v convolved in the chain, serial here; v's image, overlapped
-    levels).  The two kernels give the fused kernel's bits, and the serial
-    case matches the oracle."""
-    if case == "serial":
-        sh = inputs.LayerShape(1, 6, 128, 128, block_size=128, chunk_size=64)
+    levels); and one value head to a qk head (no next head to prepare).  The
+    two kernels give the fused kernel's bits, and the serial cases match the
+    oracle."""
+    if case in ("serial", "one_per_group"):
+        sh = inputs.LayerShape(1, 6, 128, 128, block_size=128, chunk_size=64) if case == "serial" else \
+            inputs.LayerShape(2, 2, 128, 128, block_size=128, chunk_size=64)
         lens = [700, 129, 1, 300]
         plan = gdn.gdn_prefill_plan_for(sh, len(lens), max(lens), 0, gdn.PREFILL_TWO_KERNELS)
         assert plan["chunk_launches"] == 1
