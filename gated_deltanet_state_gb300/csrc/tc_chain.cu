@@ -1201,9 +1201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the last chunk's outputs (every thread takes these barriers: `ok` may
   // differ between threads until a barrier agrees on it)
   if (c > cb) {
-    if (ok && worker) {
+    if (ok && worker) {   // (every worker: `ok` agreed at the loop's last barrier)
       mma_wait(mbar + ChSmem::kS, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
       mma_wait(mbar + ChSmem::kUP, (uint32_t)((c - 1 - cb) & 1), ok, wlim);
+      if (!core) {
+        // the tile's previous store (issued in the last chunk's step 2) has
+        // been read out before the last outputs rewrite it
+        if (tid == 0) tc::bulk_wait_read();
+        workers_sync();
+      }
       if (core) outputs_core(c - 1, sq, ok);
       else outputs(c - 1, sq);
       tc::fence_async_smem();
