@@ -162,7 +162,8 @@ gdn_status prefill_call(const gdn_layer_desc* desc, const gdn_pool* pool, const 
   // fused kernel
   const size_t core_gates = core ? core_gates_bytes(desc, a->total_tokens) : 0;
   const size_t core_images =
-      core && tc ? tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, a->num_seqs, a->total_tokens)
+      core && tc ? tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, a->num_seqs, a->total_tokens,
+                                            true)
                  : 0;
   if (a->path < GDN_PREFILL_AUTO || a->path > GDN_PREFILL_TWO_KERNELS || a->reserved != 0)
     return GDN_ERR_INVALID_ARG;
@@ -235,7 +236,7 @@ size_t gdn_core_prefill_workspace_size(const gdn_layer_desc* desc, int32_t num_s
   if (!tc_prefill_supported(desc->head_dim_k, desc->head_dim_v, desc->in_dtype, desc->out_dtype,
                             desc->block_size))
     return gates;
-  return gates + tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, num_seqs, total_tokens);
+  return gates + tc_chain_workspace_bytes(desc->num_qk_heads, desc->num_v_heads, num_seqs, total_tokens, true);
 }
 
 gdn_status gdn_core_prefill(const gdn_layer_desc* desc, const gdn_pool* pool, const gdn_prefill_args* a,

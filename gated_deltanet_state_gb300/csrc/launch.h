@@ -98,8 +98,9 @@ cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t
 // The same prefill as two kernels (tc_chain.cu): the state-independent chunk
 // kernel over every chunk of the call, writing operand images to the
 // workspace, then the chain kernel (in pieces, as tc_chain_schedule plans),
-// then the window pass.  The workspace holds tc_chain_workspace_bytes.
-size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens);
+// then the window pass.  The workspace holds tc_chain_workspace_bytes (with
+// core: also the packed core's fp32 outputs before their gated norm).
+size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens, bool core = false);
 PrefillSchedule tc_chain_schedule(int Hqk, int Hv, int num_seqs, int64_t max_len, int sms);
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st);
 // Whether the two kernels beat the fused one for a call of num_seqs sequences

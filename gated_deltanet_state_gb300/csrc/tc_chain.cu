@@ -75,6 +75,7 @@ struct ChunkWs {
   uint8_t* k;      // [slots][Hv] kImgK
   float* v;        // [slots][Hv] kImgV (image mode)
   float* g;        // [slots][Hv] kImgG
+  float* core_o;   // packed core: fp32 outputs [rows][Hv][dv] before the gated norm (else null)
   int64_t slots;
 };
 
@@ -766,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S += U^T (K^T diag(dec))^T and U^T P^T.  Every image of chunk c + 1 is
 // requested as soon as the reader of chunk c's (or c - 1's, for the two
 // buffers of T, P and the gates) is done.
-template <bool VIMG>
+template <bool VIMG, bool POST>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_chain_kernel(const ScanParams p, const __grid_constant__ CUtensorMap xmap,
                     const __grid_constant__ CUtensorMap omap, int tma_out, const ChunkWs ws, const PieceMap pm,
@@ -936,6 +937,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_load_2d(ot, &omap, p.conv_dim + h * D, (int)(row0 + c * C), mbar + ChSmem::kZ);
     armed[ChSmem::kZ] = c;
   };
+  // (POST: the packed core's outputs leave fp32, into the workspace, for the
+  // gated-norm pass after the chains, core_gate_norm_kernel, which takes a
+  // token's 128 values together in the same expression)
+  auto outputs_f32 = [&](int64_t c, const float (&sq)[16]) {
+    const float* gam = gates_of(c) + 64;
+    float up[16];
+    tc::tmem_ld16(tbase + tlane + kChU + 16 * quarter, up);
+    const int64_t t0 = c * C;
+    const int cnt = (int)(n - t0 < C ? n - t0 : C);
+    float* out = ws.core_o + ((row0 + t0) * p.Hv + h) * D + row;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int i = 16 * quarter + e;
+      if (i < cnt) out[(int64_t)i * p.Hv * D] = fmaf(gam[i], sq[e], up[e]);
+    }
+  };
   auto outputs_core = [&](int64_t c, const float (&sq)[16], bool& okc) {
     const float* gam = gates_of(c) + 64;
     float up[16];
@@ -1063,10 +1080,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // operand
       const float4 wv = VIMG ? make_float4(0.f, 0.f, 0.f, 0.f) : ldg_f4_fresh(vtaps);
       ok = work_wait(mbar + ChSmem::kPG + b, bpar, wlim) && ok;
-      if (c > cb && !core) {
+      if (c > cb && (POST || !core)) {
         mma_wait(mbar + ChSmem::kUP, par ^ 1u, ok, wlim);
-        outputs(c - 1, sq);
-        tc::fence_async_smem();
+        if constexpr (POST) {
+          outputs_f32(c - 1, sq);
+        } else {
+          outputs(c - 1, sq);
+          tc::fence_async_smem();
+        }
       }
       ok = work_wait(mbar + ChSmem::kVb, par, wlim) && ok;
       const float* gs = gates_of(c);
@@ -1110,12 +1131,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_wait(mbar + ChSmem::kSK, par, ok, wlim);
       float a[16];
-      if (core) tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
+      if (core && !POST) tc::tmem_ld16(tbase + tlane + kChSK + i0, a);
       else tc::tmem_ld16x2(tbase + tlane + kChSK + i0, tbase + tlane + kChSQ + i0, a, sq);
 #pragma unroll
       for (int e = 0; e < 16; ++e) a[e] = bv[i0 + e] * fmaf(-gam[i0 + e], a[e], vv[e]);
       split_to_tmem(a);
-      if (core) {
+      if (core && !POST) {
         // the previous chunk's outputs after R (they use v's region), with its
         // S0 Q^T still in registers; then this chunk's
         if (c > cb) {
@@ -1147,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // packed core: this chunk's z rows (the tile region is free: the
       // previous chunk's outputs are done)
-      if (core) load_z(c);
+      if (core && !POST) load_z(c);
       if (c + 1 < ce) {
         load_pg(c + 1);
         load_kq(c + 1);
@@ -1210,8 +1231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) tc::bulk_wait_read();
         workers_sync();
       }
-      if (core) outputs_core(c - 1, sq, ok);
-      else outputs(c - 1, sq);
+      if (core) {
+        if constexpr (POST) outputs_f32(c - 1, sq);
+        else outputs_core(c - 1, sq, ok);
+      } else {
+        outputs(c - 1, sq);
+      }
       tc::fence_async_smem();
     }
     ok = cta_sync_ok(ok);
@@ -1259,17 +1284,58 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================================
+// Packed core, overlapped levels: the gated RMS norm of the chain's fp32
+// outputs.  One warp per (row, value head): lane l holds channels l, l + 32,
+// l + 64, l + 96; the fused kernel's expression in its order (the sum of
+// squares over the four, then the warp's butterfly; o * inv * w * silu(z)),
+// so the paths give the same bits.  Memory-bound: 512 B of outputs and 256 B
+// of z in, 256 B out.
+// ============================================================================
+__global__ void __launch_bounds__(256) core_gate_norm_kernel(const ScanParams p, const float* __restrict__ of) {
+  using TOUT = __nv_bfloat16;
+  constexpr int D = kD;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * 8;
+  const int64_t total = p.total_rows * p.Hv;
+  float nw[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) nw[m] = p.norm_w[lane + 32 * m];
+  for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < total; w += nwarps) {
+    const int64_t t = w / p.Hv;
+    const int h = (int)(w - t * p.Hv);
+    const float* orw = of + w * D;
+    float v[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      v[m] = orw[lane + 32 * m];
+      ss = fmaf(v[m], v[m], ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss * (1.0f / D) + p.norm_eps2);
+    const __nv_bfloat16* zrow = reinterpret_cast<const __nv_bfloat16*>(p.x) + t * p.x_ld + p.conv_dim + h * D;
+    TOUT* orow = reinterpret_cast<TOUT*>(p.o) + w * D;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float z = to_f32(zrow[lane + 32 * m]);
+      orow[lane + 32 * m] = from_f32<TOUT>(v[m] * inv * nw[m] * silu_fast(z));
+    }
+  }
+}
+
+// ============================================================================
 // Host side
 // ============================================================================
-size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
+size_t tc_chain_workspace_bytes(int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens, bool core) {
   const int64_t slots = total_tokens / kC + num_seqs + 1;
   const int64_t per_v = (int64_t)kImgT + kImgP + kImgK + kImgG + kImgV;
   const int64_t per_q = (int64_t)kImgKQ;
-  return (size_t)(slots * (Hv * per_v + Hqk * per_q)) + 1024;
+  const int64_t outs = core ? total_tokens * Hv * kD * (int64_t)sizeof(float) : 0;
+  return (size_t)(slots * (Hv * per_v + Hqk * per_q) + outs) + 1024;
 }
 
 namespace {
-ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens) {
+ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total_tokens, bool core) {
   ChunkWs w;
   w.slots = total_tokens / kC + num_seqs + 1;
   uint8_t* b = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ws) + 1023) & ~uintptr_t(1023));
@@ -1284,6 +1350,7 @@ ChunkWs bind_chunk_ws(void* ws, int Hqk, int Hv, int32_t num_seqs, int64_t total
   w.k = take(w.slots * Hv * (int64_t)kImgK);
   w.v = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgV));
   w.g = reinterpret_cast<float*>(take(w.slots * Hv * (int64_t)kImgG));
+  w.core_o = core ? reinterpret_cast<float*>(take(total_tokens * Hv * kD * (int64_t)sizeof(float))) : nullptr;
   return w;
 }
 }  // namespace
@@ -1421,7 +1488,7 @@ SideStream* side_stream(cudaStream_t caller) {
 cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max_len, cudaStream_t st) {
   if (p.num_seqs == 0) return cudaSuccess;
   if ((int64_t)p.Hv * p.num_seqs > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
-  const ChunkWs ws = bind_chunk_ws(workspace, p.Hqk, p.Hv, p.num_seqs, p.total_rows);
+  const ChunkWs ws = bind_chunk_ws(workspace, p.Hqk, p.Hv, p.num_seqs, p.total_rows, p.norm_w != nullptr);
   const int64_t maxc = max_len > 0 ? (max_len + kC - 1) / kC : 0;
   if (maxc > 65535) return cudaErrorInvalidValue;
   auto encode = tensor_map_encoder();
@@ -1434,7 +1501,12 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
   // off the call.
   const bool vimg = sc.chunk_launches > 1;
   auto chunk_k = vimg ? tc_chunk_kernel<true> : tc_chunk_kernel<false>;
-  auto chain_k = vimg ? tc_chain_kernel<true> : tc_chain_kernel<false>;
+  // the packed core with overlapped levels: the gated norm in a pass of its
+  // own after the chains, off the chain's critical path (the norm in the
+  // chain would cost a chunk ~2.8 us)
+  const bool post = vimg && p.norm_w != nullptr;
+  auto chain_k = vimg ? (post ? tc_chain_kernel<true, true> : tc_chain_kernel<true, false>)
+                      : tc_chain_kernel<false, false>;
   CUtensorMap xmap;
   memset(&xmap, 0, sizeof(xmap));
   const bool chunks = maxc > 0 && p.total_rows > 0;
@@ -1530,6 +1602,13 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
       e = chain_launch(base / p.num_seqs, (int32_t)(base % p.num_seqs), cnt, st);
       if (e != cudaSuccess) return e;
     }
+  }
+  if (post && p.total_rows > 0) {
+    const int64_t warps = p.total_rows * p.Hv;
+    const unsigned blocks = (unsigned)((warps + 7) / 8 < 65535 * 8 ? (warps + 7) / 8 : 65535 * 8);
+    core_gate_norm_kernel<<<blocks, 256, 0, st>>>(p, ws.core_o);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
   window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
   return cudaGetLastError();

@@ -417,7 +417,9 @@ typedef struct gdn_core_args {
 
 /* Device workspace of gdn_core_prefill: the gates of every row (fp32,
  * 2 x 4 x T x Hv bytes rounded up to 256), then, on the tensor-core path,
- * the two kernels' operand images (as gdn_prefill_workspace_size).  A
+ * the two kernels' operand images (as gdn_prefill_workspace_size) and a
+ * T x Hv x dv fp32 buffer where the chains leave the outputs before the
+ * gated norm when the chain levels overlap the chunk launches.  A
  * workspace of the gates alone (at least that many bytes, less than this
  * size) runs the fused kernel; with this size, GDN_PREFILL_AUTO chooses as
  * gdn_prefill_chunked does.  Both paths give the same bits. */

@@ -92,8 +92,10 @@ def test_workspace_is_required_and_sized():
         for N, T in ((4, 4 * 8192), (1, 229376), (3, 1000), (1, 0)):
             assert gdn.gdn_prefill_workspace_size(sh, N, T) == (T // 64 + N + 1) * per_slot + 1024
             # the packed core: its rows' gates (256-byte rounded) first, then the same images
+            # and its fp32 outputs before the gated norm
             gates = -(-(2 * 4 * T * sh.num_v_heads) // 256) * 256
-            assert gdn.gdn_core_prefill_workspace_size(sh, N, T) == gates + (T // 64 + N + 1) * per_slot + 1024
+            outs = T * sh.num_v_heads * 128 * 4
+            assert gdn.gdn_core_prefill_workspace_size(sh, N, T) == gates + (T // 64 + N + 1) * per_slot + outs + 1024
     # the conv pre-pass path: SiLU(conv) rows in fp32 plus norm factors and gates
     for sh in (inputs.with_(inputs.QWEN27B, head_dim_k=64, head_dim_v=64),
                inputs.with_(inputs.QWEN27B, block_size=784),
