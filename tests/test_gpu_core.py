@@ -106,19 +106,25 @@ def _core_call(sh, pool, cu, start, init, bt, slots, qkvz, ba, w, A_log, dt_bias
     return st, int(err.item()), o.cpu()
 
 
-@pytest.mark.parametrize("case", ["gqa3_resumed", "overlap_27b"])
+@pytest.mark.parametrize("case", ["gqa3_resumed", "overlap_27b", "overlap_27b_resumed"])
 def test_core_prefill_two_kernels_give_the_fused_kernels_bits(case):
-    """The packed core on the chunk + chain kernels (the gated-norm epilogue
-    in the chain kernel) gives the fused kernel's bits: outputs, states,
-    checkpoints and windows; overlap_27b runs the overlapped levels."""
+    """The packed core on the chunk + chain kernels gives the fused kernel's
+    bits: outputs, states, checkpoints and windows.  gqa3_resumed runs the
+    chain's gated-norm epilogue; the overlap cases run the overlapped levels,
+    whose chains leave fp32 outputs for the separate gated-norm pass (cold,
+    and resumed from a block boundary with a carried state and window)."""
     if case == "gqa3_resumed":
         sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
         lens, start, init = [300, 65, 200], [0, 0, 256], [-1, -1, 9]
         bt, slots, npages = [[3, 4, -1, -1], [-1] * 4, [-1, -1, 5, -1]], [0, 1, 2], 12
     else:
         sh = inputs.QWEN27B
-        lens, start, init = [4133], [0], [-1]
-        bt, slots, npages = [[1, 2, 3, 4]], [0], 5
+        if case == "overlap_27b":
+            lens, start, init = [4133], [0], [-1]
+            bt, slots, npages = [[1, 2, 3, 4]], [0], 5
+        else:   # tokens 1,792 .. 5,925: boundaries 2,688 .. 5,376 in blocks 2 .. 5
+            lens, start, init = [4133], [2 * 896], [9]
+            bt, slots, npages = [[-1, -1, 1, 2, 3, 4, -1]], [0], 10
         plan = gdn.gdn_prefill_plan_for(sh, 1, 4133, 0, gdn.PREFILL_TWO_KERNELS)
         if plan["chunk_launches"] < 2:
             pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")

@@ -200,13 +200,13 @@ def _both_paths(sh, lens, start, init, bt, seed, npages, fill_state=None, max_se
     return res
 
 
-@pytest.mark.parametrize("case", ["edges_gqa3", "resumed_27b", "pieces_27b", "overlap_27b"])
+@pytest.mark.parametrize("case", ["edges_gqa3", "resumed_27b", "pieces_27b", "overlap_27b", "overlap_27b_resumed"])
 def test_two_kernel_path_gives_the_fused_kernels_bits(case):
     """The chunk + chain kernels split and multiply every operand as the fused
     kernel does, so a call gives the same bits on either path: a prefix hit
-    reproduces a cold run's bits whichever path each call takes.  overlap_27b
-    runs the two kernels' overlapped levels (the chain on a second stream,
-    four checkpoints inside levels)."""
+    reproduces a cold run's bits whichever path each call takes.  The overlap
+    cases run the two kernels' overlapped levels (the chain on a second
+    stream, four checkpoints inside levels), cold and resumed."""
     if case == "edges_gqa3":
         sh = inputs.LayerShape(2, 6, 128, 128, block_size=128, chunk_size=64)
         lens = [1, 63, 64, 65, 127, 128, 129, 300, 700]
@@ -224,6 +224,16 @@ def test_two_kernel_path_gives_the_fused_kernels_bits(case):
         if plan["chunk_launches"] < 2:
             pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
         res = _both_paths(sh, lens, [0], [-1], [[1, 2, 3, 4]], 85, 5, max_seq_len=max(lens))
+    elif case == "overlap_27b_resumed":
+        # tokens 1,792 .. 5,925 from a carried state and window in page 9
+        sh = inputs.QWEN27B
+        lens = [4133]
+        plan = gdn.gdn_prefill_plan_for(sh, 1, max(lens), 0, gdn.PREFILL_TWO_KERNELS)
+        if plan["chunk_launches"] < 2:
+            pytest.skip(f"this GPU runs the two kernels one after the other: {plan}")
+        st = inputs.random_state(sh, 1, seed=86)
+        res = _both_paths(sh, lens, [2 * 896], [9], [[-1, -1, 1, 2, 3, 4, -1]], 86, 10, fill_state=(9, st),
+                          max_seq_len=max(lens))
     else:
         sh = inputs.LayerShape(16, 48, 128, 128, block_size=1024, chunk_size=64, page_bytes=inputs.QWEN27B.page)
         lens = [2048, 1800, 77, 1536]
