@@ -50,7 +50,7 @@ N_SEQ, SEQ_LEN = 4, 8192
 # once a kernel of the path changes.  fused: 4 tc_prefill_kernel launches +
 # the window pass; two kernels: 1 tc_chunk_kernel + 4 tc_chain_kernel
 # launches + the window pass.
-PREFILL_TRAFFIC_PER_CALL = {"fused": 713.26e6 + 366.86e6, "two_kernels": 3025.16e6 + 2547.96e6}
+PREFILL_TRAFFIC_PER_CALL = {"fused": 713.26e6 + 366.86e6, "two_kernels": 3025.60e6 + 2546.00e6}
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
@@ -900,7 +900,7 @@ def main():
         "decode_hbm_frac_nominal": dec_gbs / HBM_NOMINAL_GBS, "flush_hbm_frac_nominal": fl_gbs / HBM_NOMINAL_GBS,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak,
-                     "traffic": PREFILL_TRAFFIC_PER_CALL[path_key] if args.seq_len == SEQ_LEN else None,
+                     "traffic": PREFILL_TRAFFIC_PER_CALL[path_key] if (args.seq_len == SEQ_LEN and args.num_seqs == N_SEQ) else None,
                      "traffic_note": "DRAM bytes per prefill call (every launch of the call summed; achieved "
                                      "is the call's work over its time), ncu capture of this workload",
                      "kernel": ("tc_chunk_kernel + tc_chain_kernel (the call)" if pre_plan["two_kernels"]
