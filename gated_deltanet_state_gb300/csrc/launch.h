@@ -95,6 +95,13 @@ PrefillSchedule tc_prefill_schedule_cost(int Hv, int num_seqs, int64_t max_len, 
 int tc_prefill_sm_count();   // SMs of the current device (0 if unknown: one launch)
 bool tc_prefill_supported(int dk, int dv, int in_dtype, int out_dtype, int block_size);
 cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t st);
+// z CTAs of the prefill's window pass: one per block boundary a sequence of
+// up to max_len tokens can cross (at least 1, at most 1,024; any count covers
+// every boundary, the count sets how many are written at once)
+inline unsigned window_slices(const ScanParams& p, int64_t max_len) {
+  const int64_t b = p.block_size > 0 && max_len > 0 ? max_len / p.block_size + 1 : 1;
+  return (unsigned)(b < 1 ? 1 : b > 1024 ? 1024 : b);
+}
 // The same prefill as two kernels (tc_chain.cu): the state-independent chunk
 // kernel over every chunk of the call, writing operand images to the
 // workspace, then the chain kernel (in pieces, as tc_chain_schedule plans),

@@ -575,8 +575,12 @@ __global__ void __launch_bounds__(kScanThreads, 3) scan_kernel(const ScanParams 
 // Conv windows after the scan: every crossed boundary (prefill) and the final
 // window (prefill: out_slot, flush: the checkpoint page).  One thread owns one
 // channel of one sequence and reads all three rows before writing them, so an
-// in-place update (out_slot == init_page, or the flush) is safe.  log_len is
-// only read here; the flush clears it in log_len_kernel afterwards.
+// in-place update (out_slot == init_page, or the flush) is safe.  The grid's
+// z CTAs of a (channel block, sequence) share its boundaries (boundary b goes
+// to z = b mod gridDim.z; their rows lie a block or more after the call's
+// first token, so none of them reads the carried window) and z = 0 writes
+// the final window.  log_len is only read here; the flush clears it in
+// log_len_kernel afterwards.
 template <typename TIN, int MODE>
 __global__ void __launch_bounds__(256) window_kernel(const ScanParams p) {
   const int s = blockIdx.y;
@@ -589,7 +593,8 @@ __global__ void __launch_bounds__(256) window_kernel(const ScanParams p) {
   const int64_t n = V.n;
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < p.conv_dim; c += gridDim.x * blockDim.x) {
     if (MODE == kPrefill) {
-      for (int64_t P = (start / p.block_size + 1) * p.block_size; P <= start + n; P += p.block_size) {
+      const int64_t step = (int64_t)gridDim.z * p.block_size;
+      for (int64_t P = (start / p.block_size + 1 + blockIdx.z) * p.block_size; P <= start + n; P += step) {
         const int64_t jb = P / p.block_size - 1;
         if (jb >= p.max_blocks) break;
         const int32_t page = p.block_table[(int64_t)s * p.max_blocks + jb];
@@ -601,7 +606,7 @@ __global__ void __launch_bounds__(256) window_kernel(const ScanParams p) {
           w[(int64_t)r * p.conv_dim + c] = V.raw(rel - kWinRows + r, c);
       }
     }
-    if (final_page >= 0) {
+    if (final_page >= 0 && blockIdx.z == 0) {
       TIN keep[kWinRows];
 #pragma unroll
       for (int r = 0; r < kWinRows; ++r) keep[r] = V.raw(n - kWinRows + r, c);

@@ -1610,7 +1610,8 @@ cudaError_t launch_tc_prefill2(const ScanParams& p, void* workspace, int64_t max
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs, window_slices(p, max_len)), 256, 0,
+                                            st>>>(p);
   return cudaGetLastError();
 }
 

@@ -856,7 +856,8 @@ cudaError_t launch_tc_prefill(const ScanParams& p, int64_t max_len, cudaStream_t
     if (e != cudaSuccess) return e;
   }
   // conv windows of every crossed boundary and of the final slot
-  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+  window_kernel<__nv_bfloat16, kPrefill><<<dim3((p.conv_dim + 255) / 256, p.num_seqs, window_slices(p, max_len)), 256, 0,
+                                            st>>>(p);
   return cudaGetLastError();
 }
 
