@@ -50,7 +50,7 @@ N_SEQ, SEQ_LEN = 4, 8192
 # once a kernel of the path changes.  fused: 4 tc_prefill_kernel launches +
 # the window pass; two kernels: 1 tc_chunk_kernel + 4 tc_chain_kernel
 # launches + the window pass.
-PREFILL_TRAFFIC_PER_CALL = {"fused": 713.26e6 + 366.86e6, "two_kernels": 3025.60e6 + 2546.00e6}
+PREFILL_TRAFFIC_PER_CALL = {"fused": 713.26e6 + 366.86e6, "two_kernels": 3025.54e6 + 2545.82e6}
 # Algorithmic flops of the chunk form per token and value head (chunk C = 64,
 # d = 128): 2 [C (3 dk + 2 dv) + 3 dk dv]; the kernel runs every product as
 # three bf16 passes (hi*hi + hi*lo + lo*hi) over the shapes it issues per
