@@ -52,7 +52,8 @@ cudaError_t launch_scan_t(const ScanParams& p, int64_t max_len, cudaStream_t st)
   if (e != cudaSuccess) return e;
   // 3. windows: channel blocks x sequences (the append writes none)
   if (MODE != kAppend) {
-    window_kernel<TIN, MODE><<<dim3((p.conv_dim + 255) / 256, p.num_seqs), 256, 0, st>>>(p);
+    const unsigned zs = MODE == kPrefill ? window_slices(p, max_len) : 1u;
+    window_kernel<TIN, MODE><<<dim3((p.conv_dim + 255) / 256, p.num_seqs, zs), 256, 0, st>>>(p);
     e = cudaGetLastError();
   }
   if (MODE == kFlush && e == cudaSuccess) {
